@@ -1,0 +1,323 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the
+oracle itself (the pages' worked numbers and byte extremes, closed forms,
+library routines on special cases, brute force over raw codes, invariants).
+
+Each pin takes ``mutation`` so the same check runs against the clean oracle
+(all must pass) and against builds with one planted mistake (at least one
+must fail).  Raw codes are drawn here and packed by ``workloads.pack``; the
+expected values are computed from the raw codes with numpy, never from the
+packed bytes, so a decoding mistake in the oracle cannot cancel out.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+import workloads as wl
+from oracle import oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _raw(g, fmt, O, I):
+    lo, hi = wl.CODE_RANGE[fmt]
+    return g.integers(lo, hi + 1, (O, I))
+
+
+def _deq_from_raw(fmt, gs, codes, scales):
+    """Dequantized matrix from raw codes (numpy, f64)."""
+    v = codes.astype(np.float64) - wl.OFFSET[fmt]
+    O, I = codes.shape
+    if fmt == 4:
+        ng = wl.n_groups(I, gs)
+        s = np.asarray(scales, np.float64).reshape(O, ng)
+        return v * np.repeat(s, gs, axis=1)[:, :I]
+    return v * np.asarray(scales, np.float64)[:, None]
+
+
+def pin_golden_layout(mutation=0):
+    """tests/golden/nibble_layout.txt: byte extremes and documented element order."""
+    for line in open(os.path.join(GOLDEN, "nibble_layout.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        lhs, rhs = line.split("->")
+        fmt, hexb = lhs.split()
+        fmt = int(fmt)
+        want = [int(t) for t in rhs.split()]
+        data = np.frombuffer(bytes.fromhex(hexb), dtype=np.uint8).reshape(1, -1)
+        I = len(want)
+        gs = 2 if fmt == 4 else 0
+        sc = np.ones(wl.scale_count(fmt, 1, I, gs), np.float32)
+        got = orc.dequant(fmt, gs, 1, I, data, sc, mutation=mutation)[0]
+        if list(got) != [float(v) for v in want]:
+            return False
+    return True
+
+
+def pin_expert_bytes(mutation=0):
+    """Per-expert bytes times the load count round to the printed GB figures."""
+    for line in open(os.path.join(GOLDEN, "expert_bytes.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        fmt, gs, H, F, loads, gb = line.split()
+        fmt, gs, H, F, loads = int(fmt), int(gs), int(H), int(F), int(loads)
+        per = 0
+        for (O, I) in ((F, H), (F, H), (H, F)):
+            per += O * orc.row_bytes(fmt, I, mutation) + 4 * orc.scale_count(fmt, gs, O, I, mutation)
+        if f"{per * loads / 1e9:.3f}" != gb:
+            return False
+    return True
+
+
+def pin_all_bytes_brute(mutation=0):
+    """All 256 byte values, unit scale: fmt 2/4 and 3 against raw codes."""
+    b = np.arange(256, dtype=np.uint8).reshape(1, -1)
+    ok = True
+    for fmt in (2, 4):
+        raw = np.stack([b[0] & 0xF, b[0] >> 4], axis=1).reshape(1, -1).astype(np.int64)
+        gs = 512
+        got = orc.dequant(fmt, gs, 1, 512, b, np.ones(wl.scale_count(fmt, 1, 512, gs), np.float32),
+                          mutation=mutation)
+        ok &= np.array_equal(got, raw - 8)
+    raw3 = np.stack([(b[0] >> (2 * t)) & 3 for t in range(4)], axis=1).reshape(1, -1).astype(np.int64)
+    got3 = orc.dequant(3, 0, 1, 1024, b, np.ones(1, np.float32), mutation=mutation)
+    ok &= np.array_equal(got3, raw3 - 2)
+    return bool(ok)
+
+
+def pin_exact_integer_cases(mutation=0):
+    """Power-of-two scales and integer x: every product and partial sum is exact
+    in f32 and f64, so the oracle's f32 output must equal the integer result."""
+    g = wl.rng(11)
+    for fmt, gs, O, I in ((1, 0, 7, 33), (2, 0, 5, 31), (3, 0, 6, 45), (4, 16, 5, 70),
+                          (4, 64, 4, 200), (4, 6, 3, 29), (4, 128, 3, 77)):
+        codes = _raw(g, fmt, O, I)
+        sc = (2.0 ** g.integers(-3, 4, wl.scale_count(fmt, O, I, gs))).astype(np.float32)
+        x = g.integers(-8, 9, (3, I)).astype(np.float32)
+        want = x.astype(np.float64) @ _deq_from_raw(fmt, gs, codes, sc).T
+        got = orc.matmul(fmt, gs, O, I, wl.pack(fmt, codes), sc, x, mutation=mutation)
+        if not np.array_equal(got.astype(np.float64), want):
+            return False
+    return True
+
+
+def pin_random_vs_library(mutation=0):
+    """Random codes/scales/x: oracle vs numpy matmul of the matrix dequantized
+    from raw codes, within 1e-12 of the sum of |terms| ([T] tolerance form)."""
+    g = wl.rng(12)
+    for fmt, gs, O, I, S in ((1, 0, 9, 130, 2), (2, 0, 8, 129, 3), (3, 0, 7, 131, 2),
+                             (4, 32, 6, 300, 2), (4, 64, 5, 1000, 1), (4, 128, 4, 100, 2),
+                             (4, 16, 3, 47, 1)):
+        codes = _raw(g, fmt, O, I)
+        sc = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(fmt, O, I, gs))
+        x = g.standard_normal((S, I)).astype(np.float32)
+        deq = _deq_from_raw(fmt, gs, codes, sc)
+        want = x.astype(np.float64) @ deq.T
+        mag = np.abs(x.astype(np.float64)) @ np.abs(deq).T
+        y64, = orc.matmul(fmt, gs, O, I, wl.pack(fmt, codes), sc, x, mutation=mutation, want=("y64",))
+        if not np.all(np.abs(y64 - want) <= 1e-12 * mag + 1e-300):
+            return False
+    # fmt=0 is a plain f32 GEMV: numpy in f64
+    W = g.normal(0, 0.02, (11, 90)).astype(np.float32)
+    x = g.standard_normal((2, 90)).astype(np.float32)
+    y64, = orc.matmul(0, 0, 11, 90, W, None, x, mutation=mutation, want=("y64",))
+    want = x.astype(np.float64) @ W.astype(np.float64).T
+    return bool(np.allclose(y64, want, rtol=0, atol=1e-12))
+
+
+def pin_int8_unit_scale(mutation=0):
+    """fmt=1 with all scales 1 equals an integer matvec (numpy int64)."""
+    g = wl.rng(13)
+    codes = _raw(g, 1, 10, 64)
+    x = g.integers(-100, 101, (2, 64))
+    got = orc.matmul(1, 0, 10, 64, wl.pack(1, codes), np.ones(10, np.float32), x.astype(np.float32),
+                     mutation=mutation)
+    return bool(np.array_equal(got.astype(np.int64), x @ codes.T))
+
+
+def pin_fmt4_wide_group_is_fmt2(mutation=0):
+    """fmt=4 with gs >= I is fmt=2 with a per-row scale (same nibble layout)."""
+    g = wl.rng(14)
+    for I, gs in ((64, 64), (65, 66), (100, 128), (33, 34)):
+        codes = _raw(g, 2, 6, I)
+        sc = wl.log_uniform(g, 1e-3, 1e-2, 6)
+        x = g.standard_normal((2, I)).astype(np.float32)
+        a, = orc.matmul(2, 0, 6, I, wl.pack(2, codes), sc, x, mutation=mutation, want=("y64",))
+        b, = orc.matmul(4, gs, 6, I, wl.pack(4, codes), sc, x, mutation=mutation, want=("y64",))
+        if not np.array_equal(a, b):
+            return False
+    return True
+
+
+def pin_inline_order(mutation=0):
+    """Group scale folded in per group equals dequantize-then-multiply, within
+    1e-14 of the sum of |terms|."""
+    g = wl.rng(15)
+    for fmt, gs, O, I in ((4, 64, 6, 500), (4, 16, 4, 97), (2, 0, 5, 99), (1, 0, 5, 77), (3, 0, 4, 70)):
+        codes = _raw(g, fmt, O, I)
+        sc = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(fmt, O, I, gs))
+        x = g.standard_normal((2, I)).astype(np.float32)
+        y64, mag = orc.matmul(fmt, gs, O, I, wl.pack(fmt, codes), sc, x, mutation=mutation,
+                              want=("y64", "yabs"))
+        yi = orc.matmul_inline(fmt, gs, O, I, wl.pack(fmt, codes), sc, x, mutation=mutation)
+        if not np.all(np.abs(y64 - yi) <= 1e-14 * mag):
+            return False
+    return True
+
+
+def pin_scale_linearity(mutation=0):
+    """y(2s) = 2 y(s) exactly; y(s1+s2) = y(s1) + y(s2) for fmt=4 per group."""
+    g = wl.rng(16)
+    codes = _raw(g, 4, 5, 200)
+    s1 = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(4, 5, 200, 64))
+    s2 = wl.log_uniform(g, 1e-3, 1e-2, s1.size)
+    x = g.standard_normal((2, 200)).astype(np.float32)
+    q = wl.pack(4, codes)
+    a, = orc.matmul(4, 64, 5, 200, q, s1, x, mutation=mutation, want=("y64",))
+    b, = orc.matmul(4, 64, 5, 200, q, (2 * s1).astype(np.float32), x, mutation=mutation, want=("y64",))
+    if not np.array_equal(2 * a, b):
+        return False
+    # additivity with s1 + s2 exactly representable: use powers of two
+    p1 = (2.0 ** g.integers(-8, -4, s1.size)).astype(np.float32)
+    p2 = (2.0 ** g.integers(-8, -4, s1.size)).astype(np.float32)
+    c, = orc.matmul(4, 64, 5, 200, q, p1, x, mutation=mutation, want=("y64",))
+    d, m = orc.matmul(4, 64, 5, 200, q, p2, x, mutation=mutation, want=("y64", "yabs"))
+    e, = orc.matmul(4, 64, 5, 200, q, (p1 + p2).astype(np.float32), x, mutation=mutation, want=("y64",))
+    return bool(np.all(np.abs(c + d - e) <= 1e-13 * m * 4))
+
+
+def pin_partial_last_group(mutation=0):
+    """Glen clamp: with only the last (partial) group's scale non-zero, y is the
+    last group's code dot product times that scale."""
+    g = wl.rng(17)
+    for I, gs in ((100, 64), (70, 16), (129, 32), (10, 4)):
+        ng = wl.n_groups(I, gs)
+        codes = _raw(g, 4, 3, I)
+        sc = np.zeros((3, ng), np.float32)
+        sc[:, -1] = 0.5
+        x = g.integers(-8, 9, (2, I)).astype(np.float32)
+        i0 = (ng - 1) * gs
+        want = 0.5 * (x[:, i0:].astype(np.int64) @ (codes[:, i0:] - 8).T)
+        got = orc.matmul(4, gs, 3, I, wl.pack(4, codes), sc.reshape(-1), x, mutation=mutation)
+        if not np.array_equal(got.astype(np.float64), want.astype(np.float64)):
+            return False
+    return True
+
+
+def pin_silu_closed_form(mutation=0):
+    """silu(g) = g * sigmoid(g): closed-form values."""
+    cases = {0.0: 0.0, 1.0: 1.0 / (1.0 + math.exp(-1.0)), -1.0: -1.0 / (1.0 + math.e),
+             2.0: 2.0 / (1.0 + math.exp(-2.0))}
+    return all(abs(orc.silu(k, mutation) - v) <= 1e-15 for k, v in cases.items()) and \
+        abs(orc.silu(40.0, mutation) - 40.0) < 1e-12 and abs(orc.silu(-40.0, mutation)) < 1e-12
+
+
+def pin_route_vs_sorted(mutation=0):
+    """Counting sort equals Python's stable sorted() over (s, k) slots by id."""
+    g = wl.rng(18)
+    for S, K, E in ((1, 8, 256), (5, 8, 16), (17, 4, 3), (32, 8, 256)):
+        ids = g.integers(-1, E, (S, K)).astype(np.int32)
+        offsets, order = orc.route(ids, E, mutation=mutation)
+        flat = ids.reshape(-1)
+        want = sorted([t for t in range(S * K) if flat[t] >= 0], key=lambda t: flat[t])
+        counts = np.bincount(flat[flat >= 0], minlength=E)
+        if list(order) != want or not np.array_equal(np.diff(offsets), counts):
+            return False
+        if offsets[-1] != (flat >= 0).sum():
+            return False
+    try:
+        orc.route(np.array([[0, 3]], np.int32), 3, mutation=mutation)
+        return False
+    except ValueError:
+        return True
+
+
+def _moe_problem(g, H, F, E, fmt, gs):
+    raw = []
+    mats = []
+    for _ in range(E):
+        trip = []
+        rtrip = []
+        for (O, I) in ((F, H), (F, H), (H, F)):
+            c = _raw(g, fmt, O, I)
+            sc = wl.log_uniform(g, 1e-2, 5e-2, wl.scale_count(fmt, O, I, gs))
+            trip.append(orc.Mat(fmt, gs, O, I, wl.pack(fmt, c), sc))
+            rtrip.append(_deq_from_raw(fmt, gs, c, sc))
+        mats.append(tuple(trip))
+        raw.append(tuple(rtrip))
+    return mats, raw
+
+
+def pin_moe_composition(mutation=0):
+    """One expert, w=1, S=1: down(silu(gate x) * (up x)) composed with numpy
+    from matrices dequantized from raw codes."""
+    g = wl.rng(19)
+    H, F = 96, 40
+    mats, raw = _moe_problem(g, H, F, 1, 4, 16)
+    x = g.standard_normal((1, H)).astype(np.float32)
+    y64, = orc.moe_block(H, F, mats, x, np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32),
+                         mutation=mutation, want=("y64",))
+    G, U, D = raw[0]
+    gv = G @ x[0].astype(np.float64)
+    uv = U @ x[0].astype(np.float64)
+    h = gv / (1.0 + np.exp(-gv)) * uv
+    want = D @ h
+    mag = np.abs(D) @ np.abs(h)
+    return bool(np.all(np.abs(y64[0] - want) <= 1e-12 * mag))
+
+
+def pin_moe_invariants(mutation=0):
+    """Linearity in w, permutation of the expert table, empty slots, the shared
+    expert as one more weight-1 expert, duplicate ids counted twice."""
+    g = wl.rng(20)
+    H, F, E, S, K = 64, 24, 5, 4, 3
+    mats, raw = _moe_problem(g, H, F, E, 2, 0)
+    x = g.standard_normal((S, H)).astype(np.float32)
+    ids = g.integers(0, E, (S, K)).astype(np.int32)
+    ids[1, 2] = -1
+    ids[2, :] = -1
+    w = g.uniform(0.1, 1.0, (S, K)).astype(np.float32)
+    y, = orc.moe_block(H, F, mats, x, ids, w, mutation=mutation, want=("y64",))
+    y2, = orc.moe_block(H, F, mats, x, ids, (2 * w).astype(np.float32), mutation=mutation, want=("y64",))
+    if not np.array_equal(2 * y, y2) or np.any(y[2] != 0):
+        return False
+    perm = g.permutation(E)
+    inv = np.argsort(perm)
+    mats_p = [mats[perm[j]] for j in range(E)]
+    ids_p = np.where(ids >= 0, inv[np.maximum(ids, 0)], -1).astype(np.int32)
+    yp, = orc.moe_block(H, F, mats_p, x, ids_p, w, mutation=mutation, want=("y64",))
+    if not np.array_equal(y, yp):
+        return False
+    # single-slot results against numpy composition (w = 1): catches a dropped weight
+    ids1 = np.array([[3]], np.int32)
+    y1, = orc.moe_block(H, F, mats, x[:1], ids1, np.full((1, 1), 0.25, np.float32), mutation=mutation,
+                        want=("y64",))
+    G, U, D = raw[3]
+    gv, uv = G @ x[0].astype(np.float64), U @ x[0].astype(np.float64)
+    want = 0.25 * (D @ (gv / (1 + np.exp(-gv)) * uv))
+    if not np.allclose(y1[0], want, rtol=1e-12, atol=1e-12):
+        return False
+    # duplicate id counts twice
+    yd, = orc.moe_block(H, F, mats, x[:1], np.array([[3, 3]], np.int32),
+                        np.full((1, 2), 0.25, np.float32), mutation=mutation, want=("y64",))
+    return bool(np.allclose(yd[0], 2 * want, rtol=1e-12, atol=1e-12))
+
+
+PINS = [pin_golden_layout, pin_expert_bytes, pin_all_bytes_brute, pin_exact_integer_cases,
+        pin_random_vs_library, pin_int8_unit_scale, pin_fmt4_wide_group_is_fmt2, pin_inline_order,
+        pin_scale_linearity, pin_partial_last_group, pin_silu_closed_form, pin_route_vs_sorted,
+        pin_moe_composition, pin_moe_invariants]
+
+MUTATIONS = {
+    1: "int4 nibble order swapped",
+    2: "int4 read as two's complement",
+    3: "fmt=4 uses a per-row scale",
+    4: "fmt=4 group boundary shifted by one",
+    5: "last term of the dot product dropped",
+    6: "silu sign error",
+    7: "routing weight dropped",
+}
