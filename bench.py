@@ -1,0 +1,381 @@
+"""Benchmark of the quantized-weight matvec / routed-expert library on GB300.
+
+Default workload (one JSON line): the decode expert block at full size --
+hidden 6144, expert intermediate 2048, 256 resident experts (fmt=4 grouped
+int4, gs=64), top-8 softmax routing drawn afresh every step, S=1.  One step
+is one coli_moe_block call (routing, gate/up, silu*mul, down, weighted
+scatter-add: the whole hot path).  The metric is algorithmic HBM GB/s: the
+packed codes and scales of the 8 routed experts plus x and y, divided by the
+device time.  The 5.4 GB expert pool is far larger than L2 and every step
+routes to a fresh random set, so no step finds its weights in L2.
+
+Other workloads (--workload): gemv_single, gemv_sweep, moe_prefill,
+streaming.  --impl reference times the CPU oracle (the reference arm of this
+benchmark) on a bounded sample of the same workload.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, one rank per GPU, each running its own independent
+replica (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside and self.samples:
+            nearest = min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
+            inside = [nearest[1]]
+            note = "timed region shorter than the sampling interval: nearest sample"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def aggregate(value_units: float, seconds: float, world: int):
+    """Sum the units and take the max time over ranks (identity for one rank)."""
+    if world == 1:
+        return value_units, seconds
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([value_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(u.item()), float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- workloads
+class DecodeBlock:
+    """Decode expert block, S=1, 256 experts, top-8."""
+
+    name = "moe_decode_block"
+    metric_unit = "GB/s"
+
+    def __init__(self, coli, torch, seed_offset=0):
+        self.coli, self.torch = coli, torch
+        c = self.c = wl.MOE_DECODE
+        g = wl.rng(c["seed"] + seed_offset)
+        self.H, self.F, self.E, self.K = c["H"], c["F"], c["E"], c["K"]
+        self.host = []
+        dev = []
+        for _ in range(self.E):
+            trip = wl.expert(g, self.H, self.F, c["fmt"], c["gs"])
+            self.host.append(trip)
+            dev.append(tuple(coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in trip))
+        self.table = coli.ExpertTable(dev)
+        self.n_routes = 4096
+        ids, w = wl.routing_topk_softmax(g, self.n_routes, self.E, self.K)
+        self.ids_h, self.w_h = ids, w
+        self.ids = torch.from_numpy(ids).cuda()
+        self.w = torch.from_numpy(w).cuda()
+        self.xs_h = wl.activations(g, 64, self.H)
+        self.x = torch.from_numpy(self.xs_h).cuda()
+        self.y = torch.empty(1, self.H, device="cuda")
+        self.expert_bytes = wl.expert_bytes(self.H, self.F, c["fmt"], c["gs"])
+        self.bytes_per_step = self.K * self.expert_bytes + 2 * 4 * self.H + 8 * self.K
+        self.launches_per_step = 1
+
+    def step(self, i, stream=None):
+        r = i % self.n_routes
+        self.coli.moe_block(self.x[i % 64: i % 64 + 1], self.table, self.ids[r: r + 1], self.w[r: r + 1], self.y,
+                            stream=stream)
+
+    def e2e_setup(self):
+        t = self.torch
+        self.hx = t.from_numpy(self.xs_h[:1].copy()).pin_memory()
+        self.hids = t.from_numpy(self.ids_h[:64].copy()).pin_memory()
+        self.hw = t.from_numpy(self.w_h[:64].copy()).pin_memory()
+        self.hy = t.empty(1, self.H).pin_memory()
+        self.dx = t.empty(1, self.H, device="cuda")
+        self.dids = t.empty(1, self.K, dtype=t.int32, device="cuda")
+        self.dw = t.empty(1, self.K, device="cuda")
+        self.h2d = 4 * self.H + 8 * self.K
+        self.d2h = 4 * self.H
+
+    def e2e_step(self, i):
+        r = i % 64
+        self.dx.copy_(self.hx, non_blocking=True)
+        self.dids.copy_(self.hids[r: r + 1], non_blocking=True)
+        self.dw.copy_(self.hw[r: r + 1], non_blocking=True)
+        self.coli.moe_block(self.dx, self.table, self.dids, self.dw, self.y)
+        self.hy.copy_(self.y, non_blocking=True)
+
+    def oracle_sample(self, budget_s: float):
+        """The oracle on whole decode steps of this workload, as many as fit."""
+        from oracle import oracle as orc
+        mats_cache = {}
+        done, t0, nbytes = 0, time.time(), 0
+        while True:
+            r = done % self.n_routes
+            ids = self.ids_h[r: r + 1]
+            used = sorted(set(int(e) for e in ids[0]))
+            mats = []
+            remap = {}
+            for j, e in enumerate(used):
+                if e not in mats_cache:
+                    mats_cache[e] = tuple(orc.Mat(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in self.host[e])
+                mats.append(mats_cache[e])
+                remap[e] = j
+            ids_l = np.vectorize(remap.get)(ids).astype(np.int32)
+            orc.moe_block(self.H, self.F, mats, self.xs_h[done % 64: done % 64 + 1], ids_l, self.w_h[r: r + 1])
+            done += 1
+            nbytes += self.bytes_per_step
+            if time.time() - t0 > budget_s:
+                break
+        dt = time.time() - t0
+        return nbytes / dt / 1e9, done, dt
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle, timed as it stands, on a bounded
+    sample of the default workload: one routed (row, expert) slot per step."""
+    if rank != 0:
+        return 0
+    from oracle import oracle as orc
+    c = wl.MOE_DECODE
+    g = wl.rng(c["seed"])
+    H, F = c["H"], c["F"]
+    experts = [wl.expert(g, H, F, c["fmt"], c["gs"]) for _ in range(4)]
+    mats = [tuple(orc.Mat(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in e) for e in experts]
+    ids, w = wl.routing_topk_softmax(g, 64, 4, 1)
+    x = wl.activations(g, 64, H)
+    per_step = wl.expert_bytes(H, F, c["fmt"], c["gs"]) + 2 * 4 * H + 8
+    for i in range(args.warmup):
+        orc.moe_block(H, F, mats, x[i % 64: i % 64 + 1], ids[i % 64: i % 64 + 1], w[i % 64: i % 64 + 1])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        orc.moe_block(H, F, mats, x[i % 64: i % 64 + 1], ids[i % 64: i % 64 + 1], w[i % 64: i % 64 + 1])
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt / 1e9
+    cores = orc.threads()
+    line = {"impl": "reference", "metric": "decode MoE-block HBM GB/s (algorithmic bytes / time)", "value": value,
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / max(args.steps, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "moe_decode_block", "hidden": H, "intermediate": F, "experts": 256, "topk": 8,
+                       "fmt": 4, "gs": 64, "S": 1},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "one routed (row, expert) slot of the decode block per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_steps(torch, wk, steps, stream):
+    """Time exactly `steps` steps; per-launch durations from events between launches."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(steps):
+            wk.step(1_000_000 + i, stream=stream)
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    return evs[0].elapsed_time(evs[-1]) / 1e3, per
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--workload", default="moe_decode", choices=("moe_decode",))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    torch.cuda.set_device(local)
+    import bit_weight_gemv_fmt1_gb300 as coli
+    peaks = load_peaks()
+
+    wk = DecodeBlock(coli, torch, seed_offset=rank)
+    stream = torch.cuda.Stream()
+    coli.reset_stats()
+    for i in range(args.warmup):
+        wk.step(i, stream=stream)
+    torch.cuda.synchronize()
+    coli.sync_check(stream)
+    barrier(world)
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    s0 = coli.stats()
+    t_wall0 = time.time()
+    seconds, per_launch = time_steps(torch, wk, args.steps, stream)
+    t_wall1 = time.time()
+    s1 = coli.stats()
+    coli.sync_check(stream)
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    units, seconds_max = aggregate(wk.bytes_per_step * args.steps, seconds, world)
+    barrier(world)
+    value = units / seconds_max / 1e9
+    launches = int(s1["launches"] - s0["launches"])
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    wk.e2e_setup()
+    for i in range(args.warmup):
+        wk.e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_steps = args.steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(e2e_steps):
+        wk.e2e_step(i)
+    t1.record()
+    torch.cuda.synchronize()
+    e2e_s = t0.elapsed_time(t1) / 1e3
+    e2e_units, e2e_max = aggregate(wk.bytes_per_step * e2e_steps, e2e_s, world)
+    e2e_value = e2e_units / e2e_max / 1e9
+
+    # roofline of the dominant kernel (the single decode launch of each step)
+    avg_launch_s = statistics.mean(per_launch) / 1e3
+    achieved = wk.bytes_per_step / avg_launch_s / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        traffic = json.load(open(tr_path)).get("moe_decode_kernel")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, dt = wk.oracle_sample(args.cpu_budget)
+        from oracle import oracle as orc
+        cpu = {"value": v, "unit": "GB/s", "cores": orc.threads(), "kind": "oracle",
+               "sample": f"{n} whole decode steps (8 routed experts each) in {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "decode MoE-block HBM GB/s (algorithmic bytes / time)",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": seconds_max * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "moe_decode_block", "hidden": wk.H, "intermediate": wk.F, "experts": wk.E,
+                       "topk": wk.K, "fmt": 4, "gs": 64, "S": 1, "global_batch": world,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: 5.4 GB expert pool, fresh top-8 routing every step",
+                       "bytes_per_step": wk.bytes_per_step},
+            "hbm_frac_of_measured": value / peaks["hbm_gbs"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "peak_source": peaks["source"], "kernel": "moe_decode_kernel<4>",
+                         "avg_launch_us": avg_launch_s * 1e6},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": wk.h2d, "d2h_bytes_per_step": wk.d2h},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

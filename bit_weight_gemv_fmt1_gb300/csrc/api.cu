@@ -1,0 +1,623 @@
+// api.cu -- the C ABI declared in include/coli.h: argument checks, uploads,
+// per-device / per-stream scratch, dispatch to the kernels, error reporting.
+// Every entry point refuses what it cannot compute (with a code and a
+// message) before launching anything; there is no other implementation to
+// fall back to.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <unordered_map>
+#include <algorithm>
+#include <vector>
+
+#include "coli_internal.cuh"
+
+using namespace coli;
+
+namespace {
+
+// ------------------------------------------------------------------ errors
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    if (e == cudaErrorMemoryAllocation)
+        return fail(COLI_ENOMEM, "%s: %s", what, cudaGetErrorString(e));
+    return fail(COLI_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CU(call, what)                                   \
+    do {                                                 \
+        cudaError_t e_ = (call);                         \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+// ------------------------------------------------------------------ stats
+std::atomic<uint64_t> g_calls{0}, g_launches{0}, g_wbytes{0};
+std::atomic<uint64_t> g_uid{1};
+
+std::atomic<int64_t> &fail_after() {
+    static std::atomic<int64_t> v{[] {
+        const char *s = getenv("COLI_FAIL_AFTER");
+        return s && *s ? (int64_t)atoll(s) : (int64_t)-1;
+    }()};
+    return v;
+}
+
+// Host-side fault injection gate for compute calls.
+int injected() {
+    auto &f = fail_after();
+    int64_t cur = f.load();
+    while (cur > 0 && !f.compare_exchange_weak(cur, cur - 1)) {
+    }
+    if (cur == 0) return fail(COLI_EINJECTED, "failure injected (fail-after counter reached zero)");
+    return COLI_OK;
+}
+
+void count(int launches, uint64_t wbytes) {
+    g_calls++;
+    g_launches += launches;
+    g_wbytes += wbytes;
+}
+
+// ------------------------------------------------------------------ device state
+struct Workspace {
+    unsigned *bar = nullptr;      // grid barrier words [2]
+    void *buf = nullptr;          // scratch
+    size_t cap = 0;
+};
+
+struct CachedTable {
+    ExpertDesc *d = nullptr;
+    int n = 0;
+    uint64_t last_use = 0;
+};
+
+struct DeviceState {
+    std::mutex mu;
+    int *err = nullptr;           // device error word
+    int n_sm = 0;
+    size_t smem_optin = 0;
+    std::map<cudaStream_t, Workspace> ws;
+    std::unordered_map<uint64_t, CachedTable> tables;
+    uint64_t tick = 0;
+};
+
+std::mutex g_dev_mu;
+std::map<int, DeviceState *> g_dev;
+
+int device_state(DeviceState **out) {
+    int dev = 0;
+    CU(cudaGetDevice(&dev), "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    auto it = g_dev.find(dev);
+    if (it != g_dev.end()) {
+        *out = it->second;
+        return COLI_OK;
+    }
+    DeviceState *d = new DeviceState();
+    CU(cudaMalloc(&d->err, sizeof(int)), "cudaMalloc(error word)");
+    CU(cudaMemset(d->err, 0, sizeof(int)), "cudaMemset(error word)");
+    CU(cudaDeviceGetAttribute(&d->n_sm, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+    int optin = 0;
+    CU(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev), "cudaDeviceGetAttribute");
+    d->smem_optin = (size_t)optin;
+    g_dev[dev] = d;
+    *out = d;
+    return COLI_OK;
+}
+
+// Scratch of at least `bytes` for this stream (grown on demand; growing waits
+// for the device so that no queued kernel still uses the old buffer).
+int workspace(DeviceState *d, cudaStream_t st, size_t bytes, Workspace **out) {
+    std::lock_guard<std::mutex> lk(d->mu);
+    Workspace &w = d->ws[st];
+    if (!w.bar) {
+        CU(cudaMalloc(&w.bar, 2 * sizeof(unsigned)), "cudaMalloc(barrier)");
+        CU(cudaMemset(w.bar, 0, 2 * sizeof(unsigned)), "cudaMemset(barrier)");
+    }
+    if (w.cap < bytes) {
+        if (w.buf) {
+            CU(cudaDeviceSynchronize(), "cudaDeviceSynchronize(workspace growth)");
+            CU(cudaFree(w.buf), "cudaFree(workspace)");
+            w.buf = nullptr;
+            w.cap = 0;
+        }
+        const size_t want = bytes + bytes / 4;
+        CU(cudaMalloc(&w.buf, want), "cudaMalloc(workspace)");
+        w.cap = want;
+    }
+    *out = &w;
+    return COLI_OK;
+}
+
+int check_tensor(const coli_tensor *t, const char *name) {
+    if (!t) return fail(COLI_EINVAL, "%s is NULL", name);
+    int dev = 0;
+    CU(cudaGetDevice(&dev), "cudaGetDevice");
+    if (t->device != dev)
+        return fail(COLI_EDEVICE, "%s lives on device %d but device %d is current", name, t->device, dev);
+    return COLI_OK;
+}
+
+int64_t host_row_bytes(int fmt, int64_t I) {
+    switch (fmt) {
+    case 0: return 4 * I;
+    case 1: return I;
+    case 2: case 4: return (I + 1) / 2;
+    case 3: return (I + 3) / 4;
+    default: return -1;
+    }
+}
+
+MatDesc desc_of(const coli_tensor *t) {
+    MatDesc m;
+    m.q = t->q;
+    m.s = t->s;
+    m.rs = t->rs;
+    m.gs = t->fmt == 4 ? t->gs : 0;
+    m.ng = t->fmt == 4 ? t->ng : 1;
+    return m;
+}
+
+}  // namespace
+
+// =================================================================== ABI
+extern "C" {
+
+const char *coli_version(void) { return "coli-gb300 1.0 (sm_103a)"; }
+
+const char *coli_last_error(void) { return g_msg; }
+
+void coli_get_stats(coli_stats *out) {
+    if (!out) return;
+    out->calls = g_calls.load();
+    out->launches = g_launches.load();
+    out->weight_bytes = g_wbytes.load();
+}
+
+void coli_reset_stats(void) {
+    g_calls = 0;
+    g_launches = 0;
+    g_wbytes = 0;
+}
+
+void coli_set_fail_after(int64_t n) { fail_after().store(n < 0 ? -1 : n); }
+
+int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
+                       void *stream, coli_tensor **out) {
+    g_msg[0] = 0;
+    if (!out) return fail(COLI_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (fmt < 0 || fmt > 4) return fail(COLI_EFMT, "unknown weight format %d (supported: 0..4)", fmt);
+    if (fmt == 4 && (gs < 2 || (gs & 1)))
+        return fail(COLI_EFMT, "fmt=4 needs an even group size >= 2, got gs=%d", gs);
+    if (O < 1 || I < 1) return fail(COLI_EINVAL, "O and I must be >= 1 (got O=%lld I=%lld)", (long long)O, (long long)I);
+    if (O > (1LL << 31) - 1 || I > (1LL << 30))
+        return fail(COLI_EINVAL, "matrix too large (O=%lld I=%lld)", (long long)O, (long long)I);
+    if (!data) return fail(COLI_EINVAL, "data is NULL");
+    if (fmt != 0 && !scales) return fail(COLI_EINVAL, "fmt=%d needs scales", fmt);
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    coli_tensor *t = new coli_tensor();
+    CU(cudaGetDevice(&t->device), "cudaGetDevice");
+    t->fmt = fmt;
+    t->gs = fmt == 4 ? gs : 0;
+    t->O = O;
+    t->I = I;
+    t->ng = fmt == 4 ? (int)((I + gs - 1) / gs) : 1;
+    const int64_t hrb = host_row_bytes(fmt, I);
+    t->rs = (hrb + 15) / 16 * 16;
+    t->cpr = (int)((I + epc_of(fmt) - 1) / epc_of(fmt));
+    const int64_t n_scales = fmt == 0 ? 0 : (fmt == 4 ? O * t->ng : O);
+    t->alg_bytes = O * hrb + 4 * n_scales;
+    t->dev_bytes = O * t->rs + 4 * n_scales;
+    t->uid = g_uid++;
+    cudaError_t e = cudaMalloc(&t->q, (size_t)(O * t->rs));
+    if (e == cudaSuccess && n_scales) e = cudaMalloc(&t->s, (size_t)n_scales * 4);
+    if (e == cudaSuccess) e = cudaMemsetAsync(t->q, 0, (size_t)(O * t->rs), st);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(t->q, (size_t)t->rs, data, (size_t)hrb, (size_t)hrb, (size_t)O,
+                              cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && n_scales)
+        e = cudaMemcpyAsync(t->s, scales, (size_t)n_scales * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && fmt == 1) {
+        e = launch_fmt1_encode(t->q, O * t->rs, st);
+        g_launches++;
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        coli_tensor_free(t);
+        return cuda_fail(e, "coli_tensor_upload");
+    }
+    *out = t;
+    return COLI_OK;
+}
+
+void coli_tensor_free(coli_tensor *t) {
+    if (!t) return;
+    if (t->q) cudaFree(t->q);
+    if (t->s) cudaFree(t->s);
+    delete t;
+}
+
+int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_t *I, int64_t *device_bytes,
+                     int64_t *alg_bytes) {
+    if (!t) return fail(COLI_EINVAL, "tensor is NULL");
+    if (fmt) *fmt = t->fmt;
+    if (gs) *gs = t->gs;
+    if (O) *O = t->O;
+    if (I) *I = t->I;
+    if (device_bytes) *device_bytes = t->dev_bytes;
+    if (alg_bytes) *alg_bytes = t->alg_bytes;
+    return COLI_OK;
+}
+
+// ------------------------------------------------------------------ matmul
+static int run_matmul(int n, const coli_tensor *const *W, const float *x, float *const *y, int S,
+                      cudaStream_t st) {
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    const coli_tensor *W0 = W[0];
+    uint64_t wbytes = 0;
+    for (int m = 0; m < n; m++) wbytes += (uint64_t)W[m]->alg_bytes;
+    bool generic = false;
+    for (int m = 0; m < n; m++) generic |= (W0->fmt == 4 && (W[m]->gs % 32) != 0);
+    const size_t smem = gemv_smem_bytes(W0->fmt, W0->cpr, S, (int)W0->I, generic);
+    if (S <= 8 && smem <= ds->smem_optin) {
+        GemvJob job;
+        memset(&job, 0, sizeof job);
+        job.n = n;
+        job.fmt = W0->fmt;
+        job.I = (int)W0->I;
+        job.cpr = W0->cpr;
+        job.S = S;
+        job.x = x;
+        job.row_start[0] = 0;
+        for (int m = 0; m < n; m++) {
+            job.q[m] = W[m]->q;
+            job.s[m] = W[m]->s;
+            job.y[m] = y[m];
+            job.O[m] = (int)W[m]->O;
+            job.gs[m] = W[m]->fmt == 4 ? W[m]->gs : 32;
+            job.ng[m] = W[m]->ng;
+            job.rs[m] = W[m]->rs;
+            job.row_start[m + 1] = job.row_start[m] + job.O[m];
+        }
+        int nl = 0;
+        cudaError_t e = launch_gemv(job, st, &nl);
+        if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
+        count(nl, wbytes);
+        return COLI_OK;
+    }
+    // larger S (or activations too large to stage): tiled GEMM, one launch per matrix
+    for (int m = 0; m < n; m++) {
+        GemmArgs a;
+        memset(&a, 0, sizeof a);
+        a.single = desc_of(W[m]);
+        a.fmt = W[m]->fmt;
+        a.O = (int)W[m]->O;
+        a.I = (int)W[m]->I;
+        a.X = x;
+        a.ldx = W[m]->I;
+        a.kdiv = 1;
+        a.P = S;
+        a.out = y[m];
+        a.ldo = W[m]->O;
+        cudaError_t e = launch_gemm_cc(a, false, (S + kGemmBP - 1) / kGemmBP, st);
+        if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    }
+    count(n, wbytes);
+    return COLI_OK;
+}
+
+static int check_ptr(const void *p, const char *name) {
+    if (!p) return fail(COLI_EINVAL, "%s is NULL", name);
+    if ((uintptr_t)p & 3) return fail(COLI_EINVAL, "%s is not 4-byte aligned", name);
+    return COLI_OK;
+}
+
+int coli_matmul(const coli_tensor *W, const float *x, float *y, int S, void *stream) {
+    g_msg[0] = 0;
+    if (int rc = check_tensor(W, "W")) return rc;
+    if (int rc = check_ptr(x, "x")) return rc;
+    if (int rc = check_ptr(y, "y")) return rc;
+    if (S < 1) return fail(COLI_EINVAL, "S must be >= 1 (got %d)", S);
+    if (int rc = injected()) return rc;
+    return run_matmul(1, &W, x, &y, S, (cudaStream_t)stream);
+}
+
+int coli_matmul_multi(int n, const coli_tensor *const *W, const float *x, float *const *y, int S, void *stream) {
+    g_msg[0] = 0;
+    if (n < 1 || n > GemvJob::MAXM) return fail(COLI_EINVAL, "n must be in 1..%d (got %d)", GemvJob::MAXM, n);
+    if (!W || !y) return fail(COLI_EINVAL, "W or y array is NULL");
+    for (int m = 0; m < n; m++) {
+        if (int rc = check_tensor(W[m], "W[m]")) return rc;
+        if (int rc = check_ptr(y[m], "y[m]")) return rc;
+        if (W[m]->fmt != W[0]->fmt || W[m]->I != W[0]->I)
+            return fail(COLI_EINVAL, "matrix %d differs in format or I from matrix 0", m);
+    }
+    if (int rc = check_ptr(x, "x")) return rc;
+    if (S < 1) return fail(COLI_EINVAL, "S must be >= 1 (got %d)", S);
+    if (int rc = injected()) return rc;
+    return run_matmul(n, W, x, y, S, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ routing
+int coli_moe_route(const int32_t *ids, int S, int K, int n_experts, int32_t *offsets, int32_t *order,
+                   void *stream) {
+    g_msg[0] = 0;
+    if (int rc = check_ptr(ids, "ids")) return rc;
+    if (int rc = check_ptr(offsets, "offsets")) return rc;
+    if (int rc = check_ptr(order, "order")) return rc;
+    if (S < 1 || K < 1 || K > 64) return fail(COLI_EINVAL, "need S >= 1 and 1 <= K <= 64 (got S=%d K=%d)", S, K);
+    if (n_experts < 1 || n_experts > 8192)
+        return fail(COLI_EINVAL, "n_experts must be in 1..8192 (got %d)", n_experts);
+    if ((long long)S * K > (1LL << 30)) return fail(COLI_EINVAL, "S*K too large");
+    if (int rc = injected()) return rc;
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    RouteArgs a;
+    memset(&a, 0, sizeof a);
+    a.ids = ids;
+    a.S = S;
+    a.K = K;
+    a.E = n_experts;
+    a.offsets = offsets;
+    a.order = order;
+    a.err = ds->err;
+    a.tile_rows = kGemmBP;
+    cudaError_t e = launch_route(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
+    count(1, 0);
+    return COLI_OK;
+}
+
+// ------------------------------------------------------------------ expert block
+static int expert_table(DeviceState *ds, const coli_expert *ex, int n, cudaStream_t st, const ExpertDesc **out) {
+    uint64_t key = 1469598103934665603ULL ^ (uint64_t)n;
+    for (int e = 0; e < n; e++) {
+        const coli_tensor *m[3] = {ex[e].gate, ex[e].up, ex[e].down};
+        for (int k = 0; k < 3; k++) key = (key ^ m[k]->uid) * 1099511628211ULL;
+    }
+    std::lock_guard<std::mutex> lk(ds->mu);
+    auto it = ds->tables.find(key);
+    if (it != ds->tables.end() && it->second.n == n) {
+        it->second.last_use = ++ds->tick;
+        *out = it->second.d;
+        return COLI_OK;
+    }
+    if (ds->tables.size() >= 16) {   // evict the least recently used table
+        auto victim = ds->tables.begin();
+        for (auto i = ds->tables.begin(); i != ds->tables.end(); ++i)
+            if (i->second.last_use < victim->second.last_use) victim = i;
+        CU(cudaDeviceSynchronize(), "cudaDeviceSynchronize(table eviction)");
+        cudaFree(victim->second.d);
+        ds->tables.erase(victim);
+    }
+    std::vector<ExpertDesc> h((size_t)n);
+    for (int e = 0; e < n; e++) {
+        h[e].m[0] = desc_of(ex[e].gate);
+        h[e].m[1] = desc_of(ex[e].up);
+        h[e].m[2] = desc_of(ex[e].down);
+    }
+    CachedTable ct;
+    ct.n = n;
+    ct.last_use = ++ds->tick;
+    CU(cudaMalloc(&ct.d, sizeof(ExpertDesc) * (size_t)n), "cudaMalloc(expert table)");
+    cudaError_t e = cudaMemcpyAsync(ct.d, h.data(), sizeof(ExpertDesc) * (size_t)n, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        cudaFree(ct.d);
+        return cuda_fail(e, "expert table upload");
+    }
+    ds->tables[key] = ct;
+    *out = ct.d;
+    return COLI_OK;
+}
+
+int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_experts, const int32_t *ids,
+                   const float *w, int K, float *y, void *stream) {
+    g_msg[0] = 0;
+    if (int rc = check_ptr(x, "x")) return rc;
+    if (int rc = check_ptr(y, "y")) return rc;
+    if (int rc = check_ptr(ids, "ids")) return rc;
+    if (int rc = check_ptr(w, "w")) return rc;
+    if (!experts) return fail(COLI_EINVAL, "experts is NULL");
+    if (S < 1 || K < 1 || K > 64) return fail(COLI_EINVAL, "need S >= 1 and 1 <= K <= 64 (got S=%d K=%d)", S, K);
+    if (n_experts < 1 || n_experts > 8192)
+        return fail(COLI_EINVAL, "n_experts must be in 1..8192 (got %d)", n_experts);
+    const coli_tensor *g0 = experts[0].gate;
+    if (int rc = check_tensor(g0, "experts[0].gate")) return rc;
+    const int64_t F = g0->O, H = g0->I;
+    const int fmt = g0->fmt;
+    if (F > (1 << 30) || H > (1 << 30)) return fail(COLI_EINVAL, "expert dimensions too large");
+    for (int e = 0; e < n_experts; e++) {
+        const coli_tensor *m[3] = {experts[e].gate, experts[e].up, experts[e].down};
+        const char *nm[3] = {"gate", "up", "down"};
+        for (int k = 0; k < 3; k++) {
+            if (int rc = check_tensor(m[k], nm[k])) {
+                char why[256];
+                snprintf(why, sizeof why, "%s", g_msg);
+                return fail(rc, "expert %d %s: %s", e, nm[k], why);
+            }
+            if (m[k]->fmt != fmt)
+                return fail(COLI_EFMT, "expert %d %s has fmt=%d but expert 0 gate has fmt=%d; one format per "
+                                       "expert table is supported", e, nm[k], m[k]->fmt, fmt);
+        }
+        if (m[0]->O != F || m[0]->I != H || m[1]->O != F || m[1]->I != H || m[2]->O != H || m[2]->I != F)
+            return fail(COLI_EINVAL, "expert %d: gate/up must be [%lld][%lld] and down [%lld][%lld]", e,
+                        (long long)F, (long long)H, (long long)H, (long long)F);
+    }
+    if (int rc = injected()) return rc;
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    const ExpertDesc *table = nullptr;
+    if (int rc = expert_table(ds, experts, n_experts, st, &table)) return rc;
+
+    const int n_slots = S * K;
+    const int cpr_gu = g0->cpr, cpr_d = experts[0].down->cpr;
+    bool gs_ok = true;
+    if (fmt == 4)
+        for (int e = 0; e < n_experts && gs_ok; e++)
+            gs_ok = experts[e].gate->gs % 32 == 0 && experts[e].up->gs % 32 == 0 && experts[e].down->gs % 32 == 0;
+
+    // ---------------- decode: one cooperative launch
+    if (n_slots <= kMaxDecodeSlots && gs_ok) {
+        const int xlen_gu = staged_len(fmt, cpr_gu), xlen_d = staged_len(fmt, cpr_d);
+        const size_t budget = 110 * 1024 / 4;   // floats per CTA: two CTAs per SM
+        const int rpc_alloc = (int)((H + ds->n_sm - 1) / ds->n_sm);
+        const size_t fixed = (size_t)S * rpc_alloc;
+        int sb = 0;
+        if (budget > fixed + xlen_d + rpc_alloc)
+            sb = (int)std::min<size_t>((size_t)n_slots, (budget - fixed) / (size_t)(xlen_d + rpc_alloc));
+        const size_t stage = std::max((size_t)S * xlen_gu, (size_t)sb * xlen_d);
+        const size_t smem = (stage + (size_t)sb * rpc_alloc + fixed) * sizeof(float);
+        if (sb >= 1 && (size_t)S * xlen_gu <= budget && smem <= ds->smem_optin) {
+            int per_sm = 0;
+            cudaError_t e = moe_decode_occupancy(fmt, smem, &per_sm);
+            if (e != cudaSuccess) return cuda_fail(e, "decode occupancy");
+            if (per_sm >= 1) {
+                Workspace *ws = nullptr;
+                if (int rc = workspace(ds, st, (size_t)n_slots * F * sizeof(float), &ws)) return rc;
+                const int grid = per_sm * ds->n_sm;
+                MoeDecodeArgs a;
+                memset(&a, 0, sizeof a);
+                a.x = x;
+                a.ids = ids;
+                a.w = w;
+                a.y = y;
+                a.table = table;
+                a.n_experts = n_experts;
+                a.S = S;
+                a.K = K;
+                a.H = (int)H;
+                a.F = (int)F;
+                a.cpr_gu = cpr_gu;
+                a.cpr_d = cpr_d;
+                a.hbuf = (float *)ws->buf;
+                a.bar = ws->bar;
+                a.err = ds->err;
+                a.sb = sb;
+                a.rpc = (int)((H + grid - 1) / grid);
+                a.timeout_ns = 2000000000LL;
+                e = launch_moe_decode(a, fmt, grid, smem, st);
+                if (e != cudaSuccess) return cuda_fail(e, "decode expert-block launch");
+                count(1, 0);
+                return COLI_OK;
+            }
+        }
+    }
+
+    // ---------------- prefill pipeline
+    const int max_tiles = (n_slots + kGemmBP - 1) / kGemmBP + std::min(n_experts, n_slots);
+    auto al = [](size_t b) { return (b + 255) / 256 * 256; };
+    const size_t sz_off = al((size_t)(n_experts + 1) * 4), sz_ord = al((size_t)n_slots * 4);
+    const size_t sz_tile = al((size_t)max_tiles * 4), sz_h = al((size_t)n_slots * F * 4);
+    const size_t sz_out = al((size_t)n_slots * H * 4);
+    const size_t total = sz_off + 2 * sz_ord + 3 * sz_tile + 256 + sz_h + sz_out;
+    Workspace *ws = nullptr;
+    if (int rc = workspace(ds, st, total, &ws)) return rc;
+    char *p = (char *)ws->buf;
+    int32_t *offsets = (int32_t *)p; p += sz_off;
+    int32_t *order = (int32_t *)p; p += sz_ord;
+    int32_t *inv = (int32_t *)p; p += sz_ord;
+    int32_t *te = (int32_t *)p; p += sz_tile;
+    int32_t *tp0 = (int32_t *)p; p += sz_tile;
+    int32_t *tp1 = (int32_t *)p; p += sz_tile;
+    int32_t *ntiles = (int32_t *)p; p += 256;
+    float *hbuf = (float *)p; p += sz_h;
+    float *slot_out = (float *)p;
+
+    RouteArgs r;
+    memset(&r, 0, sizeof r);
+    r.ids = ids;
+    r.S = S;
+    r.K = K;
+    r.E = n_experts;
+    r.offsets = offsets;
+    r.order = order;
+    r.inv = inv;
+    r.tile_e = te;
+    r.tile_p0 = tp0;
+    r.tile_p1 = tp1;
+    r.n_tiles = ntiles;
+    r.tile_rows = kGemmBP;
+    r.err = ds->err;
+    cudaError_t e = launch_route(r, st);
+    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
+
+    GemmArgs gu;
+    memset(&gu, 0, sizeof gu);
+    gu.table = table;
+    gu.mi = 0;
+    gu.fmt = fmt;
+    gu.O = (int)F;
+    gu.I = (int)H;
+    gu.X = x;
+    gu.ldx = H;
+    gu.order = order;
+    gu.kdiv = K;
+    gu.tile_e = te;
+    gu.tile_p0 = tp0;
+    gu.tile_p1 = tp1;
+    gu.n_tiles = ntiles;
+    gu.out = hbuf;
+    gu.ldo = F;
+    e = launch_gemm_cc(gu, true, max_tiles, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
+
+    GemmArgs dn = gu;
+    dn.mi = 2;
+    dn.O = (int)H;
+    dn.I = (int)F;
+    dn.X = hbuf;
+    dn.ldx = F;
+    dn.order = nullptr;
+    dn.kdiv = 1;
+    dn.out = slot_out;
+    dn.ldo = H;
+    e = launch_gemm_cc(dn, false, max_tiles, st);
+    if (e != cudaSuccess) return cuda_fail(e, "down launch");
+
+    e = launch_combine(slot_out, inv, w, S, K, (int)H, y, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    count(4, 0);
+    return COLI_OK;
+}
+
+int coli_sync_check(void *stream) {
+    g_msg[0] = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    int word = 0;
+    CU(cudaMemcpy(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost), "reading the device error word");
+    if (word == DEV_ERR_NONE) return COLI_OK;
+    CU(cudaMemset(ds->err, 0, sizeof(int)), "clearing the device error word");
+    if (word == DEV_ERR_TIMEOUT) {
+        std::lock_guard<std::mutex> lk(ds->mu);
+        for (auto &kv : ds->ws)
+            if (kv.second.bar) cudaMemset(kv.second.bar, 0, 2 * sizeof(unsigned));
+        return fail(COLI_ETIMEOUT, "a grid-wide wait in the expert block ran out of time");
+    }
+    if (word == DEV_ERR_BAD_ID) return fail(COLI_EINVAL, "a routing id was outside [-1, n_experts)");
+    return fail(COLI_ECUDA, "device error word %d", word);
+}
+
+}  // extern "C"

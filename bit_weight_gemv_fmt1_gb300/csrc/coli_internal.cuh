@@ -1,0 +1,475 @@
+// coli_internal.cuh -- shared definitions of the CUDA library (not installed).
+//
+// Device layout of an uploaded matrix W [O][I]:
+//   q  : O rows of `rs` bytes, rs = row_bytes rounded up to 16; the padding is
+//        zero.  fmt=1 bytes are stored offset binary (b ^ 0x80) so that every
+//        integer format decodes as (unsigned code - offset).  fmt 2/3/4 keep
+//        the host nibble/crumb order; fmt=0 keeps the f32 values.
+//   s  : f32 scales exactly as on the host ([O] or [O][ng]); none for fmt=0.
+//
+// The bandwidth-bound kernels stream each row as 16-byte chunks, lane l of a
+// warp taking chunks l, l+32, l+64, ...  A chunk holds EPC elements (4, 16,
+// 32, 64, 32 for fmt 0..4).  The activations are staged in shared memory in an
+// order made for those chunks (see stage_vec): the four floats a lane needs
+// for one 32-bit word of codes are one 16-byte shared load, and the float4
+// units of a chunk are XOR-swizzled by the chunk index so that the 8 lanes of
+// a shared-memory phase hit 8 different bank groups.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coli.h"
+
+struct coli_tensor {
+    int fmt, gs, ng, device;
+    int64_t O, I;
+    int64_t rs;          // device row stride in bytes (multiple of 16)
+    int cpr;             // 16-byte chunks per row that hold data
+    uint8_t *q;          // device codes
+    float *s;            // device scales (NULL for fmt=0)
+    int64_t dev_bytes, alg_bytes;
+    uint64_t uid;        // unique per upload, never reused
+};
+
+namespace coli {
+
+// ------------------------------------------------------------------ errors
+// Device-side error codes recorded in the per-device error word.
+enum : int { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_ID = 2 };
+
+// ------------------------------------------------------------------ traits
+template <int FMT> struct Fmt;
+template <> struct Fmt<0> { static constexpr int EPC = 4; };
+template <> struct Fmt<1> { static constexpr int EPC = 16; };
+template <> struct Fmt<2> { static constexpr int EPC = 32; };
+template <> struct Fmt<3> { static constexpr int EPC = 64; };
+template <> struct Fmt<4> { static constexpr int EPC = 32; };
+
+__host__ __device__ inline int epc_of(int fmt) {
+    return fmt == 0 ? 4 : fmt == 1 ? 16 : fmt == 3 ? 64 : 32;
+}
+
+// Length (floats) of one staged activation vector for a row of `cpr` chunks:
+// a whole number of warp iterations, so every lane of the last iteration
+// reads zeros instead of running past the end.
+__host__ __device__ inline int staged_len(int fmt, int cpr) {
+    return ((cpr + 31) / 32) * 32 * epc_of(fmt);
+}
+
+// Position of element e of a staged vector.
+template <int FMT>
+__device__ __forceinline__ int stage_pos(int e) {
+    if constexpr (FMT == 0) {
+        return e;
+    } else if constexpr (FMT == 1) {
+        const int c = e >> 4, r = e & 15;
+        return c * 16 + (((r >> 2) ^ ((c >> 1) & 3)) << 2) + (r & 3);
+    } else if constexpr (FMT == 2 || FMT == 4) {
+        // per 8-element word: order x0 x1 x2 x5 | x3 x6 x4 x7 (pairs that
+        // match the packed f32x2 lanes of dot_word4)
+        const int c = e >> 5, r = e & 31;
+        const int k = r & 7;
+        const int pos = (0x75364210 >> (4 * k)) & 0xF;   // 0,1,2,4,6,3,5,7
+        const int within = (r & ~7) + pos;
+        return c * 32 + (((within >> 2) ^ (c & 7)) << 2) + (within & 3);
+    } else {
+        const int c = e >> 6, r = e & 63;
+        return c * 64 + (((r >> 2) ^ (c & 7)) << 2) + (r & 3);
+    }
+}
+
+// Stage one activation vector src[0..n) into dst[0..len) (zeros past n).
+template <int FMT>
+__device__ __forceinline__ void stage_vec(float *dst, const float *__restrict__ src, int n, int len,
+                                          int tid, int nthreads) {
+    for (int e = tid; e < len; e += nthreads)
+        dst[stage_pos<FMT>(e)] = e < n ? src[e] : 0.0f;
+}
+
+// ------------------------------------------------------------- primitives
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float lop_mag(uint32_t w, uint32_t mask, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(magic));   // (w & mask) | magic
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ float prmt_byte(uint32_t w, uint32_t magic, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(magic), "r"(sel));
+    return __uint_as_float(r);
+}
+
+union F2U {
+    float2 f;
+    unsigned long long u;
+};
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    F2U A{a}, B{b}, D;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(D.u) : "l"(A.u), "l"(B.u));
+    return D.f;
+}
+
+__device__ __forceinline__ void ffma2(float2 &acc, float2 a, float2 b) {
+    F2U A{a}, B{b}, C{acc};
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(C.u) : "l"(A.u), "l"(B.u));
+    acc = C.f;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ----------------------------------------------------- per-format decode
+// Each 32-bit word of codes is turned into f32 values with one lop3 / prmt
+// per element: the code is OR-ed into the mantissa of 1.0 (or 2^23 for int8),
+// which gives 1 + code * 2^(p-23) exactly, and one packed subtract removes the
+// offset exactly (both operands lie in [1,2)).  The result (code - offset) *
+// 2^(p-23) is multiplied into a per-bit-position ("class") accumulator; the
+// classes are re-scaled by 2^(23-p), a power of two, when they are combined.
+
+// int4, 8 elements: classes (p0|p4) (p8|p8) (p12|p12) (p16|p16)
+struct Acc4 { float2 a01, a25, a36, a47; };
+__device__ __forceinline__ void acc_zero(Acc4 &a) {
+    a.a01 = a.a25 = a.a36 = a.a47 = make_float2(0.f, 0.f);
+}
+__device__ __forceinline__ float acc_combine(const Acc4 &a) {
+    return a.a01.x * 8388608.0f + a.a01.y * 524288.0f + (a.a25.x + a.a25.y) * 32768.0f +
+           (a.a36.x + a.a36.y) * 2048.0f + (a.a47.x + a.a47.y) * 128.0f;
+}
+struct Dec4 { float2 v01, v25, v36, v47; };
+__device__ __forceinline__ Dec4 decode4(uint32_t w) {
+    const uint32_t M = 0x3F800000u;
+    const uint32_t b = w >> 12;
+    Dec4 d;
+    d.v01 = fadd2(make_float2(lop_mag(w, 0xFu, M), lop_mag(w, 0xF0u, M)),
+                  make_float2(-__uint_as_float(M | (8u << 0)), -__uint_as_float(M | (8u << 4))));
+    d.v25 = fadd2(make_float2(lop_mag(w, 0xF00u, M), lop_mag(b, 0xF00u, M)),
+                  make_float2(-__uint_as_float(M | (8u << 8)), -__uint_as_float(M | (8u << 8))));
+    d.v36 = fadd2(make_float2(lop_mag(w, 0xF000u, M), lop_mag(b, 0xF000u, M)),
+                  make_float2(-__uint_as_float(M | (8u << 12)), -__uint_as_float(M | (8u << 12))));
+    d.v47 = fadd2(make_float2(lop_mag(w, 0xF0000u, M), lop_mag(b, 0xF0000u, M)),
+                  make_float2(-__uint_as_float(M | (8u << 16)), -__uint_as_float(M | (8u << 16))));
+    return d;
+}
+__device__ __forceinline__ void fma4(Acc4 &a, const Dec4 &d, float4 x0, float4 x1) {
+    ffma2(a.a01, d.v01, make_float2(x0.x, x0.y));
+    ffma2(a.a25, d.v25, make_float2(x0.z, x0.w));
+    ffma2(a.a36, d.v36, make_float2(x1.x, x1.y));
+    ffma2(a.a47, d.v47, make_float2(x1.z, x1.w));
+}
+
+// int8 (stored offset binary), 4 elements, one class: 2^23 + u - (2^23 + 128)
+struct Acc1 { float2 a, b; };
+__device__ __forceinline__ void acc_zero(Acc1 &a) { a.a = a.b = make_float2(0.f, 0.f); }
+__device__ __forceinline__ float acc_combine(const Acc1 &a) { return (a.a.x + a.a.y) + (a.b.x + a.b.y); }
+struct Dec1 { float2 v01, v23; };
+__device__ __forceinline__ Dec1 decode1(uint32_t w) {
+    const uint32_t M = 0x4B000000u;
+    const float2 off = make_float2(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
+    Dec1 d;
+    d.v01 = fadd2(make_float2(prmt_byte(w, M, 0x7650u), prmt_byte(w, M, 0x7651u)), off);
+    d.v23 = fadd2(make_float2(prmt_byte(w, M, 0x7652u), prmt_byte(w, M, 0x7653u)), off);
+    return d;
+}
+__device__ __forceinline__ void fma1(Acc1 &a, const Dec1 &d, float4 x) {
+    ffma2(a.a, d.v01, make_float2(x.x, x.y));
+    ffma2(a.b, d.v23, make_float2(x.z, x.w));
+}
+
+// int2, 16 elements as 4 byte views (shift 0/8/16/24), classes (p0|p2) (p4|p6);
+// two copies of the accumulators (even / odd views) for instruction-level
+// parallelism.
+struct Acc3 { float2 a0, b0, a1, b1; };
+__device__ __forceinline__ void acc_zero(Acc3 &a) {
+    a.a0 = a.b0 = a.a1 = a.b1 = make_float2(0.f, 0.f);
+}
+__device__ __forceinline__ float acc_combine(const Acc3 &a) {
+    return (a.a0.x + a.a1.x) * 8388608.0f + (a.a0.y + a.a1.y) * 2097152.0f +
+           (a.b0.x + a.b1.x) * 524288.0f + (a.b0.y + a.b1.y) * 131072.0f;
+}
+__device__ __forceinline__ void view3(float2 &va, float2 &vb, uint32_t v) {
+    const uint32_t M = 0x3F800000u;
+    va = fadd2(make_float2(lop_mag(v, 0x3u, M), lop_mag(v, 0xCu, M)),
+               make_float2(-__uint_as_float(M | (2u << 0)), -__uint_as_float(M | (2u << 2))));
+    vb = fadd2(make_float2(lop_mag(v, 0x30u, M), lop_mag(v, 0xC0u, M)),
+               make_float2(-__uint_as_float(M | (2u << 4)), -__uint_as_float(M | (2u << 6))));
+}
+
+// f32 weights, 4 per chunk
+struct Acc0 { float2 a, b; };
+__device__ __forceinline__ void acc_zero(Acc0 &a) { a.a = a.b = make_float2(0.f, 0.f); }
+__device__ __forceinline__ float acc_combine(const Acc0 &a) { return (a.a.x + a.a.y) + (a.b.x + a.b.y); }
+
+template <int FMT> struct AccOf;
+template <> struct AccOf<0> { using T = Acc0; };
+template <> struct AccOf<1> { using T = Acc1; };
+template <> struct AccOf<2> { using T = Acc4; };
+template <> struct AccOf<3> { using T = Acc3; };
+template <> struct AccOf<4> { using T = Acc4; };
+
+// Multiply-accumulate one 16-byte chunk `q` of codes against the staged
+// activations of that chunk (xs4 points at the chunk's first float4 unit of
+// one activation vector; c7 = chunk index & 7 selects the swizzle).
+template <int FMT>
+__device__ __forceinline__ void chunk_fma(typename AccOf<FMT>::T &acc, uint4 q, const float4 *xs4, int c) {
+    if constexpr (FMT == 2 || FMT == 4) {
+        const int sw = c & 7;
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            const Dec4 d = decode4(wv[t]);
+            fma4(acc, d, xs4[(2 * t) ^ sw], xs4[(2 * t + 1) ^ sw]);
+        }
+    } else if constexpr (FMT == 1) {
+        const int sw = (c >> 1) & 3;
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; t++) fma1(acc, decode1(wv[t]), xs4[t ^ sw]);
+    } else if constexpr (FMT == 3) {
+        const int sw = c & 7;
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                const uint32_t v = m == 0 ? wv[t] : (wv[t] >> (8 * m));
+                float2 va, vb;
+                view3(va, vb, v);
+                const float4 x = xs4[(4 * t + m) ^ sw];
+                if (m & 1) {
+                    ffma2(acc.a1, va, make_float2(x.x, x.y));
+                    ffma2(acc.b1, vb, make_float2(x.z, x.w));
+                } else {
+                    ffma2(acc.a0, va, make_float2(x.x, x.y));
+                    ffma2(acc.b0, vb, make_float2(x.z, x.w));
+                }
+            }
+        }
+    } else {
+        const float4 x = xs4[0];
+        ffma2(acc.a, make_float2(__uint_as_float(q.x), __uint_as_float(q.y)), make_float2(x.x, x.y));
+        ffma2(acc.b, make_float2(__uint_as_float(q.z), __uint_as_float(q.w)), make_float2(x.z, x.w));
+    }
+}
+
+// Dot products of R matrix rows against NS staged activation vectors, by one
+// warp.  rows[r] = row base pointers (16-byte aligned), scl[r] = the row's
+// scales (per-row formats: one float; fmt=4: ng floats), gpc[r] = chunks per
+// group of row r for fmt=4 (gs / 32).  xsv[n] = staged vector n.  Results are the
+// warp-reduced sums, valid in every lane.
+template <int FMT, int R, int NS>
+__device__ __forceinline__ void dot_rows(const uint8_t *const (&rows)[R], const float *const (&scl)[R],
+                                         const int (&gpc)[R], const float *const (&xsv)[NS], int cpr,
+                                         int lane, float (&out)[R][NS]) {
+    using Acc = typename AccOf<FMT>::T;
+    constexpr int U = ((FMT == 3) ? 4 : 8) / R > 0 ? ((FMT == 3) ? 4 : 8) / R : 1;   // chunks per row loaded ahead
+    float y[R][NS];
+#pragma unroll
+    for (int r = 0; r < R; r++)
+#pragma unroll
+        for (int n = 0; n < NS; n++) y[r][n] = 0.f;
+    Acc acc[R][NS];
+    if constexpr (FMT != 4) {
+#pragma unroll
+        for (int r = 0; r < R; r++)
+#pragma unroll
+            for (int n = 0; n < NS; n++) acc_zero(acc[r][n]);
+    }
+    const int n_iter = (cpr + 31) >> 5;
+    for (int it0 = 0; it0 < n_iter; it0 += U) {
+        uint4 q[U][R];
+        float sc[U][R];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int c = (it0 + u) * 32 + lane;
+            const bool ok = (it0 + u < n_iter) && c < cpr;
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                q[u][r] = ok ? ld_stream(rows[r] + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
+                if constexpr (FMT == 4) sc[u][r] = ok ? __ldg(scl[r] + c / gpc[r]) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            if (it0 + u >= n_iter) break;
+            const int c = (it0 + u) * 32 + lane;
+            const int EPC = Fmt<FMT>::EPC;
+            if constexpr (FMT == 4) {
+#pragma unroll
+                for (int r = 0; r < R; r++)
+#pragma unroll
+                    for (int n = 0; n < NS; n++) acc_zero(acc[r][n]);
+            }
+#pragma unroll
+            for (int n = 0; n < NS; n++) {
+                const float4 *xs4 = reinterpret_cast<const float4 *>(xsv[n] + (size_t)c * EPC);
+#pragma unroll
+                for (int r = 0; r < R; r++) chunk_fma<FMT>(acc[r][n], q[u][r], xs4, c);
+            }
+            if constexpr (FMT == 4) {
+#pragma unroll
+                for (int r = 0; r < R; r++)
+#pragma unroll
+                    for (int n = 0; n < NS; n++) y[r][n] = fmaf(sc[u][r], acc_combine(acc[r][n]), y[r][n]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        float rs = 1.f;
+        if constexpr (FMT == 1 || FMT == 2 || FMT == 3) rs = __ldg(scl[r]);
+#pragma unroll
+        for (int n = 0; n < NS; n++) {
+            float v;
+            if constexpr (FMT == 4) v = y[r][n];
+            else if constexpr (FMT == 0) v = acc_combine(acc[r][n]);
+            else v = rs * acc_combine(acc[r][n]);
+            out[r][n] = warp_sum(v);
+        }
+    }
+}
+
+// Generic path for fmt=4 with a group size that is not a multiple of 32
+// (any even gs): one element at a time with its own group scale.
+__device__ __forceinline__ float dot_row_fmt4_generic(const uint8_t *row, const float *scl, int gs, int I,
+                                                      const float *x, int lane) {
+    float acc = 0.f;
+    for (int i = lane; i < I; i += 32) {
+        const uint8_t b = row[i >> 1];
+        const int code = (i & 1) ? (b >> 4) : (b & 0xF);
+        acc = fmaf((float)(code - 8) * __ldg(scl + i / gs), x[i], acc);
+    }
+    return warp_sum(acc);
+}
+
+// ------------------------------------------------------------- timing
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// ------------------------------------------------------------- host side
+
+// Launch helpers implemented in the .cu files.
+struct GemvJob {
+    static constexpr int MAXM = 16;
+    const uint8_t *q[MAXM];
+    const float *s[MAXM];
+    float *y[MAXM];
+    int O[MAXM];
+    int gs[MAXM];
+    int ng[MAXM];
+    long long rs[MAXM];
+    int row_start[MAXM + 1];   // prefix of O over matrices
+    int n, fmt, I, cpr, S;
+    const float *x;
+};
+
+cudaError_t launch_gemv(const GemvJob &job, cudaStream_t st, int *n_launch);
+
+}  // namespace coli
+
+namespace coli {
+
+// Device view of one uploaded matrix.
+struct MatDesc {
+    const uint8_t *q;
+    const float *s;
+    long long rs;
+    int gs, ng;
+};
+// gate, up, down of one routed expert.
+struct ExpertDesc {
+    MatDesc m[3];
+};
+
+// Decode one element (o fixed by `row`, input index i) of the device layout,
+// scale included.  Used by the tiled GEMM and the gather kernels.
+__device__ __forceinline__ float decode_elem(int fmt, const uint8_t *row, const float *rscale, int gs, int i) {
+    switch (fmt) {
+    case 0: return reinterpret_cast<const float *>(row)[i];
+    case 1: return (float)((int)row[i] - 128) * rscale[0];
+    case 2: { const uint8_t b = row[i >> 1]; return (float)(((i & 1) ? (b >> 4) : (b & 0xF)) - 8) * rscale[0]; }
+    case 3: { const uint8_t b = row[i >> 2]; return (float)(((b >> (2 * (i & 3))) & 3) - 2) * rscale[0]; }
+    default: { const uint8_t b = row[i >> 1]; return (float)(((i & 1) ? (b >> 4) : (b & 0xF)) - 8) * rscale[i / gs]; }
+    }
+}
+
+// Arguments of the single-launch decode expert block.
+struct MoeDecodeArgs {
+    const float *x;
+    const int32_t *ids;
+    const float *w;
+    float *y;
+    const ExpertDesc *table;
+    int n_experts, S, K, H, F;
+    int cpr_gu, cpr_d;       // 16-byte chunks per gate/up row (H inputs) and per down row (F inputs)
+    float *hbuf;             // [S*K][F] scratch
+    unsigned *bar;           // grid barrier words [2]
+    int *err;                // device error word
+    int sb;                  // slots per phase-B shared-memory batch
+    int rpc;                 // phase-B output rows per CTA
+    long long timeout_ns;    // bound of the grid-wide wait
+};
+
+// Arguments of the tiled CUDA-core GEMM (prefill / S > 8).
+struct GemmArgs {
+    const ExpertDesc *table;  // expert table (NULL: use `single`)
+    MatDesc single;
+    int mi;                   // matrix index in the expert (0 gate, 1 up, 2 down); DUAL uses mi and mi+1
+    int fmt, O, I;
+    const float *X;           // activations, rows of ldx floats
+    long long ldx;
+    const int32_t *order;     // p -> slot (s*K+k); source row = order[p] / kdiv.  NULL: source row = p
+    int kdiv;
+    const int32_t *tile_e, *tile_p0, *tile_p1, *n_tiles;   // NULL: tiles of BP rows over [0, P)
+    int P;
+    float *out;               // out[p][o], rows of ldo floats
+    long long ldo;
+};
+
+// Arguments of the routing inversion.
+struct RouteArgs {
+    const int32_t *ids;
+    int S, K, E;
+    int32_t *offsets;         // [E+1]
+    int32_t *order;           // [S*K]
+    int32_t *inv;             // [S*K] slot -> position or -1 (may be NULL)
+    int32_t *tile_e, *tile_p0, *tile_p1, *n_tiles;   // may be NULL
+    int tile_rows;
+    int *err;
+};
+
+cudaError_t launch_moe_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t smem, cudaStream_t st);
+cudaError_t moe_decode_occupancy(int fmt, size_t smem, int *per_sm);
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
+cudaError_t launch_gemm_cc(const GemmArgs &a, bool dual, int max_tiles, cudaStream_t st);
+cudaError_t launch_combine(const float *slot_out, const int32_t *inv, const float *w, int S, int K, int H,
+                           float *y, cudaStream_t st);
+cudaError_t launch_fmt1_encode(uint8_t *q, long long n, cudaStream_t st);
+size_t gemv_smem_bytes(int fmt, int cpr, int S, int I, bool generic);
+
+constexpr int kDecodeThreads = 256;
+constexpr int kMaxDecodeSlots = 64;
+constexpr int kGemmBP = 32;    // token rows per GEMM tile
+
+}  // namespace coli

@@ -1,0 +1,209 @@
+/*
+ * coli.h -- C ABI of the GB300 (sm_103a) quantized-weight matvec / routed-expert
+ * library.  Plain pointers and sizes only; no C++ or framework types.
+ *
+ * The operation (colibri project pages):
+ *   - y[s][o] = sum_i w[o][i] * x[s][i] over a quantized weight matrix W [O][I]
+ *     in one of five formats (PR #298 page, commit message "metal: grouped-int4
+ *     (fmt=4) GEMV support": mm_gemv handled "fmt 0-3", fmt=4 added with one f32
+ *     scale per gs inputs folded into the accumulation per group; commit message
+ *     "CUDA backend had no fmt=4 case": per-row scale for fmt 1/2/3, per-group
+ *     for fmt=4, O*ceil(I/gs) scales).
+ *   - the routed-expert block: per routed (row, expert) pair, gate/up matvecs,
+ *     silu(gate)*up, the down matvec, and a weighted scatter-add of the expert
+ *     outputs over ragged per-row routing (colibri-strix commit log, "metal:
+ *     batched moe_block": "gate/up/silu/down for a whole expert block",
+ *     "per-row ragged expert routing", "weighted scatter-add").
+ *
+ * Host byte layout accepted by coli_tensor_upload (rows contiguous, each row
+ * starting on a byte boundary):
+ *   fmt=0  f32 [O][I], no scales.
+ *   fmt=1  int8 two's complement [O][I]; scales f32 [O].
+ *   fmt=2  int4 offset binary, value = nibble - 8; rows of ceil(I/2) bytes;
+ *          element 2j is the LOW nibble of byte j; scales f32 [O].
+ *   fmt=3  int2 offset binary, value = crumb - 2; rows of ceil(I/4) bytes
+ *          (PR #298 page, qt_addrow commit message: stride (I+3)/4); element
+ *          4j+t is bits [2t, 2t+1] of byte j; scales f32 [O].
+ *   fmt=4  int4 as fmt=2; scales f32 [O][ceil(I/gs)], group g covering inputs
+ *          [g*gs, min((g+1)*gs, I)) (PR #298 page, test_i4_grouped commit: the
+ *          partial last group and gs > I).
+ * The int4 offset encoding and the extremes 0x00 -> -8, 0xFF -> +7 are printed
+ * on the PR #298 page (test_i4_grouped commit message); the element order in a
+ * byte, the int2 and int8 encodings are this library's documented readings.
+ *
+ * Conventions for every entry point:
+ *   - Return 0 (COLI_OK) or a negative COLI_E* code; coli_last_error() then
+ *     gives a message for the calling thread.  No entry point ever falls back
+ *     to another implementation or returns a partial result: an argument it
+ *     cannot handle is refused with an error, before anything is launched.
+ *   - "device" pointers are CUDA global-memory pointers on the current device;
+ *     "host" pointers are ordinary host memory.  The caller owns every pointer
+ *     it passes and the stream.  `stream` is a cudaStream_t (NULL = legacy
+ *     default stream).
+ *   - Compute calls are asynchronous on `stream`.  Their return code covers
+ *     argument checks and launch errors.  Errors found on the device (a bounded
+ *     wait that ran out) are reported by the next coli_sync_check(stream).
+ *   - Each device has its own library state; tensors live on the device that
+ *     was current at upload and must be used with that device current.
+ */
+#ifndef COLI_H
+#define COLI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    COLI_OK = 0,
+    COLI_EINVAL = -1,     /* bad size, pointer, stride or combination of arguments */
+    COLI_EFMT = -2,       /* unknown format or invalid group size */
+    COLI_ENOMEM = -3,     /* device allocation failed */
+    COLI_ECUDA = -4,      /* a CUDA runtime call failed (message names it) */
+    COLI_ETIMEOUT = -5,   /* a bounded device-side wait ran out (from coli_sync_check) */
+    COLI_EINJECTED = -6,  /* failure injected by coli_set_fail_after / COLI_FAIL_AFTER */
+    COLI_EDEVICE = -7     /* tensor used on a device other than the one it lives on */
+};
+
+/* Opaque uploaded weight matrix.  The library owns its device memory. */
+typedef struct coli_tensor coli_tensor;
+
+/* One routed expert: gate [F][H], up [F][H], down [H][F]. */
+typedef struct {
+    const coli_tensor *gate, *up, *down;
+} coli_expert;
+
+/* Library-wide counters (all threads, all devices). */
+typedef struct {
+    uint64_t calls;        /* compute entry points that launched work */
+    uint64_t launches;     /* CUDA kernels launched by this library */
+    uint64_t weight_bytes; /* algorithmic weight bytes (codes + scales) of launched work */
+} coli_stats;
+
+/*
+ * Upload one weight matrix W [O][I] (PR #298 page, "CUDA backend had no fmt=4
+ * case" commit message: coli_cuda_tensor_upload_grouped takes gs and stores
+ * O*ceil(I/gs) scales; this entry point is that upload for every format).
+ *   fmt     0..4 as in the layout above.
+ *   gs      fmt=4: group size, even and >= 2 (gs >= I means one group per row).
+ *           Other formats: ignored.
+ *   O, I    rows (outputs) and columns (inputs), each >= 1, I <= 2^30.
+ *   data    HOST pointer to the packed codes in the host layout above.
+ *   scales  HOST pointer to the f32 scales (NULL for fmt=0).
+ *   stream  stream for the copies; the call returns after they completed, so
+ *           data and scales may be freed or reused right away.
+ *   out     receives the new tensor; on error *out is set to NULL.
+ * The device copy is re-laid out for the kernels (rows padded to 16 bytes,
+ * int8 stored offset binary); the padding never contributes to a result.
+ * Errors: COLI_EFMT (fmt or gs), COLI_EINVAL (sizes, NULL data/scales/out),
+ * COLI_ENOMEM, COLI_ECUDA.
+ */
+int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data,
+                       const float *scales, void *stream, coli_tensor **out);
+
+/* Free a tensor (NULL is ignored).  The caller must make sure no queued work
+ * still reads it (synchronize the streams that used it first). */
+void coli_tensor_free(coli_tensor *t);
+
+/* Shape and storage of a tensor.  Any output pointer may be NULL.
+ * device_bytes = device memory held; alg_bytes = host-layout codes + scales. */
+int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_t *I,
+                     int64_t *device_bytes, int64_t *alg_bytes);
+
+/*
+ * y[S][O] = x[S][I] * W^T   (the quantized matvec for S = 1, the small-S
+ * matmul for S > 1; PR #298 page, "metal: grouped-int4 (fmt=4) GEMV support"
+ * commit message, Shader paragraph).
+ *   W       uploaded tensor.
+ *   x       device f32 [S][I], row-major, 16-byte aligned.
+ *   y       device f32 [S][O], row-major, overwritten; must not overlap x.
+ *   S       rows, >= 1.  S <= 16 runs the bandwidth-bound CUDA-core kernels;
+ *           larger S runs the tensor-core GEMM.
+ * Errors: COLI_EINVAL (NULL/misaligned pointer, S < 1), COLI_EDEVICE, COLI_ECUDA.
+ */
+int coli_matmul(const coli_tensor *W, const float *x, float *y, int S, void *stream);
+
+/*
+ * y_m = x * W_m^T for m < n, several matrices that share one input x (e.g. the
+ * attention projections that read the same activations, or a layer's set of
+ * expert matrices), as ONE launch.
+ *   n       1..16 matrices; all have the same fmt and I (O and gs may differ).
+ *   W       HOST array of n tensor pointers.
+ *   x       device f32 [S][I].
+ *   y       HOST array of n device pointers, y[m] is f32 [S][O_m], overwritten.
+ *   S       1..16.
+ * Errors as coli_matmul, plus COLI_EINVAL when formats or I differ.
+ */
+int coli_matmul_multi(int n, const coli_tensor *const *W, const float *x, float *const *y, int S,
+                      void *stream);
+
+/*
+ * Routing inversion: a stable counting sort of the slots (s, k), s < S, k < K,
+ * by expert id ids[s*K+k] (colibri-strix commit log, "metal: batched
+ * moe_block": per-row ragged routing; id -1 is an empty slot).
+ *   ids      device int32 [S][K], each in [-1, n_experts).
+ *   offsets  device int32 [n_experts+1]: expert e's slots are
+ *            order[offsets[e] .. offsets[e+1]); offsets[n_experts] = valid slots.
+ *   order    device int32 [S*K]: slot indices s*K+k, grouped by expert, each
+ *            group in ascending slot order (deterministic).
+ *   S >= 1, 1 <= K <= 64, 1 <= n_experts <= 65536.
+ * An id out of range makes the kernel record COLI_EINVAL for the next
+ * coli_sync_check(stream) and leaves offsets/order unspecified.
+ */
+int coli_moe_route(const int32_t *ids, int S, int K, int n_experts, int32_t *offsets, int32_t *order,
+                   void *stream);
+
+/*
+ * The routed-expert block (colibri-strix commit log, "metal: batched
+ * moe_block"; the shared expert is one more expert with weight 1 for every
+ * row, "fuse shared expert into GPU block"):
+ *   y[s][:] = sum over k with e = ids[s*K+k] >= 0 of
+ *             w[s*K+k] * down_e( silu(gate_e x[s]) * up_e x[s] )
+ *   x        device f32 [S][H].
+ *   experts  HOST array of n_experts descriptors; every gate/up is [F][H] and
+ *            every down is [H][F] with one F and H for the whole table; all
+ *            gates and ups share one format, all downs share one format; gs may
+ *            differ per matrix.  The table may be reused across calls; the
+ *            library caches its device copy keyed by the tensors it names.
+ *   ids      device int32 [S][K], each in [-1, n_experts).
+ *   w        device f32 [S][K] routing weights, used as given.
+ *   y        device f32 [S][H], overwritten; must not overlap x.
+ *   S >= 1, 1 <= K <= 64.
+ * S*K <= 64 runs the single-launch decode kernel (a cooperative grid with one
+ * bounded grid-wide wait between the gate/up and down phases).  Larger S*K
+ * runs the prefill pipeline (routing, gather, grouped gate/up, grouped down,
+ * combine).  An id out of range is recorded for coli_sync_check(stream) and y
+ * is then unspecified.
+ * Errors: COLI_EINVAL, COLI_EFMT, COLI_EDEVICE, COLI_ENOMEM, COLI_ECUDA.
+ */
+int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_experts,
+                   const int32_t *ids, const float *w, int K, float *y, void *stream);
+
+/* Synchronize `stream`, then report (and clear) any error the library's
+ * kernels recorded on this device: COLI_ETIMEOUT for a bounded wait that ran
+ * out, COLI_EINVAL for an out-of-range routing id, COLI_ECUDA for a CUDA
+ * error.  Returns COLI_OK otherwise. */
+int coli_sync_check(void *stream);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char *coli_last_error(void);
+
+/* Counters since load or the last reset. */
+void coli_get_stats(coli_stats *out);
+void coli_reset_stats(void);
+
+/* Host-side fault injection: after n more successful compute calls, every
+ * compute call returns COLI_EINJECTED without launching anything.  n < 0
+ * switches it off.  The environment variable COLI_FAIL_AFTER=n sets it at
+ * load time. */
+void coli_set_fail_after(int64_t n);
+
+/* Library version string. */
+const char *coli_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLI_H */

@@ -1,0 +1,153 @@
+"""coli_matmul / coli_matmul_multi on the GPU against the oracle.
+
+Tolerance: max|gpu - oracle| / max|oracle| <= 1e-5 per output tensor (f32
+accumulation on the GPU, f64 in the oracle).  Exact integer cases (power-of-
+two scales, small integer activations) must match bit for bit, which pins
+the group index, the nibble order and the scale placement independently of
+any tolerance.
+"""
+import numpy as np
+import pytest
+
+import workloads as wl
+from gpu_util import TOL, cuda_or_skip, norm_err, upload
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+FMT_CASES = [(0, 0), (1, 0), (2, 0), (3, 0), (4, 32), (4, 64), (4, 128)]
+
+
+def _run(coli, torch, m, x):
+    W = upload(coli, m)
+    xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    yd = torch.full((x.shape[0], m.O), float("nan"), device="cuda")
+    coli.matmul(W, xd, yd)
+    coli.sync_check()
+    return yd.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt,gs", FMT_CASES)
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 5, 8])
+def test_matvec_formats(fmt, gs, S):
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(100 + 10 * fmt + S)
+    m = wl.random_matrix(g, fmt, 333, 2500, gs)
+    x = wl.activations(g, S, 2500)
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(fmt, gs, 333, 2500, m.data, m.scales, x)
+    assert norm_err(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("fmt,gs", FMT_CASES + [(4, 2), (4, 6), (4, 16), (4, 48), (4, 4096)])
+@pytest.mark.parametrize("O,I", [(1, 1), (3, 7), (5, 31), (17, 33), (9, 65), (64, 1023), (7, 1025), (130, 4097)])
+def test_ragged_shapes(fmt, gs, O, I):
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(O * 131 + I + fmt)
+    m = wl.random_matrix(g, fmt, O, I, gs)
+    x = wl.activations(g, 2, I)
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(fmt, gs, O, I, m.data, m.scales, x)
+    assert norm_err(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("fmt,gs,O,I", [(1, 0, 70, 3000), (2, 0, 70, 3001), (3, 0, 65, 2999), (4, 64, 66, 3000),
+                                        (4, 128, 40, 700), (4, 16, 33, 500), (4, 6, 9, 100)])
+@pytest.mark.parametrize("S", [1, 4, 20])
+def test_exact_integer_cases(fmt, gs, O, I, S):
+    """Power-of-two scales and integer x in [-8, 8]: every product and partial
+    sum is exact in f32, so the GPU result must equal the oracle bit for bit."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(7 * O + I + S)
+    m = wl.random_matrix(g, fmt, O, I, gs)
+    m.scales = (2.0 ** g.integers(-2, 3, m.scales.size)).astype(np.float32)
+    x = g.integers(-8, 9, (S, I)).astype(np.float32)
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(fmt, gs, O, I, m.data, m.scales, x)
+    assert np.array_equal(got, ref)
+
+
+def test_fmt4_wide_group_equals_fmt2():
+    """fmt=4 with gs >= I and the same codes/scales gives fmt=2's result."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(77)
+    m2 = wl.random_matrix(g, 2, 200, 1000)
+    m4 = wl.Matrix(4, 1024, 200, 1000, m2.data, m2.scales)
+    x = wl.activations(g, 3, 1000)
+    a = _run(coli, torch, m2, x)
+    b = _run(coli, torch, m4, x)
+    assert norm_err(a, b) <= TOL
+
+
+@pytest.mark.parametrize("S", [9, 16, 33, 70])
+@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 10)])
+def test_large_s_gemm_path(fmt, gs, S):
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(500 + S + fmt)
+    m = wl.random_matrix(g, fmt, 150, 700, gs)
+    x = wl.activations(g, S, 700)
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(fmt, gs, 150, 700, m.data, m.scales, x)
+    assert norm_err(got, ref) <= TOL
+
+
+def test_matmul_multi_shared_input():
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(91)
+    mats = [wl.random_matrix(g, 4, O, 1536, gs) for O, gs in ((100, 64), (257, 128), (31, 32), (512, 64))]
+    x = wl.activations(g, 2, 1536)
+    Ws = [upload(coli, m) for m in mats]
+    xd = torch.from_numpy(x).cuda()
+    ys = [torch.empty(2, m.O, device="cuda") for m in mats]
+    coli.matmul_multi(Ws, xd, ys)
+    coli.sync_check()
+    for m, y in zip(mats, ys):
+        ref = orc.matmul(4, m.gs, m.O, 1536, m.data, m.scales, x)
+        assert norm_err(y.cpu().numpy(), ref) <= TOL
+
+
+def test_single_gemv_workload():
+    """The single grouped-int4 GEMV: S=1, I=2048, O=1536, gs=64."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    c = wl.GEMV_SINGLE
+    g = wl.rng(c["seed"])
+    m = wl.random_matrix(g, 4, c["O"], c["I"], c["gs"])
+    x = wl.activations(g, 1, c["I"])
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(4, c["gs"], c["O"], c["I"], m.data, m.scales, x)
+    assert norm_err(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 128)])
+@pytest.mark.parametrize("S", [1, 2, 4])
+def test_format_sweep_workload(fmt, gs, S):
+    """Format sweep at full size: I=6144, O=2048, N(0,0.02) weights quantised
+    by symmetric absmax, x ~ N(0,1)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    c = wl.GEMV_SWEEP
+    g = wl.rng(c["seed"] + 10 * fmt + gs)
+    Wf = g.normal(0.0, 0.02, (c["O"], c["I"])).astype(np.float32)
+    m = wl.quantize(fmt, Wf, gs)
+    x = wl.activations(g, S, c["I"])
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(fmt, gs, c["O"], c["I"], m.data, m.scales, x)
+    assert norm_err(got, ref) <= TOL
+
+
+def test_repeat_is_bitwise_stable():
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(5)
+    m = wl.random_matrix(g, 4, 777, 3000, 64)
+    x = wl.activations(g, 2, 3000)
+    a = _run(coli, torch, m, x)
+    b = _run(coli, torch, m, x)
+    assert np.array_equal(a, b)

@@ -1,0 +1,164 @@
+"""coli_moe_block and coli_moe_route on the GPU against the oracle.
+
+Routing indices are compared bit for bit with the oracle's counting sort;
+expert-block outputs with max|gpu - oracle| / max|oracle| <= 1e-5.
+"""
+import numpy as np
+import pytest
+
+import workloads as wl
+from gpu_util import TOL, cuda_or_skip, norm_err, upload
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def _experts(g, H, F, E, fmt, gs, distinct=None):
+    """E experts; with `distinct`, only that many are drawn and reused."""
+    n = E if distinct is None else distinct
+    host = [wl.expert(g, H, F, fmt, gs) for _ in range(n)]
+    return [host[e % n] for e in range(E)]
+
+
+def _device_table(coli, host):
+    cache = {}
+    dev = []
+    for trip in host:
+        key = id(trip)
+        if key not in cache:
+            cache[key] = tuple(upload(coli, m) for m in trip)
+        dev.append(cache[key])
+    return coli.ExpertTable(dev)
+
+
+def _oracle_mats(host):
+    return [tuple(orc.Mat(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in trip) for trip in host]
+
+
+def _run_block(coli, torch, table, x, ids, w, H):
+    y = torch.full((x.shape[0], H), float("nan"), device="cuda")
+    coli.moe_block(torch.from_numpy(x).cuda(), table, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), y)
+    coli.sync_check()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (2, 0), (1, 0), (3, 0), (0, 0), (4, 32)])
+@pytest.mark.parametrize("S,K", [(1, 8), (2, 4), (4, 8), (8, 8)])
+def test_decode_block(fmt, gs, S, K):
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E = 512, 256, 12
+    g = wl.rng(1000 + 7 * fmt + S + K + gs)
+    host = _experts(g, H, F, E, fmt, gs)
+    x = wl.activations(g, S, H)
+    ids, w = wl.routing_topk_softmax(g, S, E, K)
+    got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert norm_err(got, ref) <= TOL
+
+
+def test_decode_ragged_routing_and_empty_slots():
+    """Empty slots (-1), duplicate ids in a row, a row with no expert, the
+    shared expert as one more weight-1 expert on every row."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E = 384, 200, 7
+    g = wl.rng(2024)
+    host = _experts(g, H, F, E, 4, 64)
+    x = wl.activations(g, 4, H)
+    ids = np.array([[0, 3, -1, 6], [2, 2, 5, -1], [-1, -1, -1, -1], [6, 1, 0, 4]], np.int32)
+    w = g.uniform(0.05, 1.0, ids.shape).astype(np.float32)
+    ids[:, 3] = np.where(ids[:, 3] >= 0, ids[:, 3], -1)
+    ids_sh = np.concatenate([ids, np.full((4, 1), 6, np.int32)], axis=1)   # expert 6 as the shared expert
+    w_sh = np.concatenate([w, np.ones((4, 1), np.float32)], axis=1)
+    table = _device_table(coli, host)
+    mats = _oracle_mats(host)
+    for I_, W_ in ((ids, w), (ids_sh, w_sh)):
+        got = _run_block(coli, torch, table, x, I_, W_, H)
+        ref = orc.moe_block(H, F, mats, x, I_, W_)
+        assert norm_err(got, ref) <= TOL
+    got = _run_block(coli, torch, table, x, ids, w, H)
+    assert np.all(got[2] == 0.0)
+
+
+@pytest.mark.parametrize("fmt,gs", [(4, 128), (4, 64), (2, 0), (4, 16), (1, 0)])
+@pytest.mark.parametrize("S,K", [(9, 8), (40, 4), (100, 8)])
+def test_prefill_block(fmt, gs, S, K):
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E = 384, 160, 24
+    g = wl.rng(3000 + S + K + fmt + gs)
+    host = _experts(g, H, F, E, fmt, gs)
+    x = wl.activations(g, S, H, bf16_exact=True)
+    ids, w = wl.routing_zipf(g, S, E, K)
+    ids[3, 1] = -1
+    got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert norm_err(got, ref) <= TOL
+
+
+def test_decode_is_bitwise_deterministic():
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E = 1024, 512, 16
+    g = wl.rng(44)
+    host = _experts(g, H, F, E, 4, 64)
+    table = _device_table(coli, host)
+    x = wl.activations(g, 2, H)
+    ids, w = wl.routing_topk_softmax(g, 2, E, 8)
+    a = _run_block(coli, torch, table, x, ids, w, H)
+    b = _run_block(coli, torch, table, x, ids, w, H)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("S,K,E", [(1, 8, 256), (4, 8, 256), (544, 8, 256), (37, 3, 5), (1000, 6, 8192)])
+def test_route_bit_exact(S, K, E):
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(S + K + E)
+    ids = g.integers(-1, E, (S, K)).astype(np.int32)
+    off_ref, ord_ref = orc.route(ids, E)
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    order = torch.full((S * K,), -7, dtype=torch.int32, device="cuda")
+    coli.moe_route(torch.from_numpy(ids).cuda(), E, off, order)
+    coli.sync_check()
+    off = off.cpu().numpy()
+    assert np.array_equal(off, off_ref)
+    assert np.array_equal(order.cpu().numpy()[: len(ord_ref)], ord_ref)
+
+
+def test_decode_workload_full_size():
+    """Decode expert block at full size: H=6144, F=2048, 256 experts, top-8
+    softmax routing, fmt=4 gs=64, S=1 (32 distinct seeded experts, each
+    resident at 8 addresses)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    c = wl.MOE_DECODE
+    g = wl.rng(c["seed"])
+    host = _experts(g, c["H"], c["F"], c["E"], c["fmt"], c["gs"], distinct=32)
+    table = _device_table(coli, host)
+    mats = _oracle_mats(host)
+    for rep in range(2):
+        x = wl.activations(g, 1, c["H"])
+        ids, w = wl.routing_topk_softmax(g, 1, c["E"], c["K"])
+        got = _run_block(coli, torch, table, x, ids, w, c["H"])
+        ref = orc.moe_block(c["H"], c["F"], mats, x, ids, w)
+        assert norm_err(got, ref) <= TOL
+
+
+def test_prefill_workload_sampled_rows():
+    """Prefill expert block at full size (S=544, Zipf(1.1) routing over 256
+    experts, fmt=4 gs=128, bf16-representable x); 6 sampled rows checked
+    against the oracle (each row depends only on its own x and routing)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    c = wl.MOE_PREFILL
+    g = wl.rng(c["seed"])
+    host = _experts(g, c["H"], c["F"], c["E"], c["fmt"], c["gs"], distinct=32)
+    table = _device_table(coli, host)
+    x = wl.activations(g, c["S"], c["H"], bf16_exact=True)
+    ids, w = wl.routing_zipf(g, c["S"], c["E"], c["K"], c["zipf"])
+    got = _run_block(coli, torch, table, x, ids, w, c["H"])
+    rows = np.sort(g.choice(c["S"], 6, replace=False))
+    ref = orc.moe_block(c["H"], c["F"], _oracle_mats(host), x[rows], ids[rows], w[rows])
+    assert norm_err(got[rows], ref) <= TOL
