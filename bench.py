@@ -142,11 +142,11 @@ class DecodeBlock:
     name = "moe_decode_block"
     metric_unit = "GB/s"
 
-    def __init__(self, coli, torch, seed_offset=0):
+    def __init__(self, coli, torch, seed_offset=0, n_experts=None):
         self.coli, self.torch = coli, torch
         c = self.c = wl.MOE_DECODE
         g = wl.rng(c["seed"] + seed_offset)
-        self.H, self.F, self.E, self.K = c["H"], c["F"], c["E"], c["K"]
+        self.H, self.F, self.E, self.K = c["H"], c["F"], n_experts or c["E"], c["K"]
         self.host = []
         dev = []
         for _ in range(self.E):
@@ -217,6 +217,130 @@ class DecodeBlock:
         return nbytes / dt / 1e9, done, dt
 
 
+# ---------------------------------------------------------------- other workloads of the metric
+def _time_loop(torch, fn, n, warm=5):
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(n):
+        fn(i)
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / n
+
+
+def _time_graph(torch, fn, n, warm=3):
+    """Average device time of fn(0..n-1) replayed from one CUDA graph (no
+    Python launch overhead inside the timed region)."""
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for i in range(n):
+            fn(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / n
+
+
+def bench_gemv(coli, torch, peaks, l2_bytes):
+    """Single fmt=4 GEMV and the format sweep, each over enough distinct copies
+    of the matrix that the rotation exceeds 4x L2 (no call finds its weights in L2)."""
+    out = {}
+    cases = [("gemv_single_fmt4_g64", 4, 64, wl.GEMV_SINGLE["O"], wl.GEMV_SINGLE["I"], (1,), wl.GEMV_SINGLE["seed"])]
+    for fmt, gs in wl.GEMV_SWEEP["variants"]:
+        name = f"sweep_fmt{fmt}" + (f"_g{gs}" if fmt == 4 else "")
+        cases.append((name, fmt, gs, wl.GEMV_SWEEP["O"], wl.GEMV_SWEEP["I"], wl.GEMV_SWEEP["S"], wl.GEMV_SWEEP["seed"]))
+    for name, fmt, gs, O, I, Ss, seed in cases:
+        g = wl.rng(seed + fmt + gs)
+        if name.startswith("sweep"):
+            m = wl.quantize(fmt, g.normal(0, 0.02, (O, I)).astype(np.float32), gs)
+        else:
+            m = wl.random_matrix(g, fmt, O, I, gs)
+        ncopy = max(2, math.ceil(4 * l2_bytes / m.nbytes))
+        Ws = [coli.tensor_upload(m.fmt, m.gs, O, I, m.data, m.scales) for _ in range(ncopy)]
+        res = {}
+        for S in Ss:
+            x = torch.randn(S, I, device="cuda")
+            y = torch.empty(S, O, device="cuda")
+            t = _time_graph(torch, lambda i: coli.matmul(Ws[i % ncopy], x, y), max(200, 2 * ncopy))
+            nbytes = m.nbytes + 4 * S * (I + O)
+            res[f"S{S}"] = {"us": t * 1e6, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"]}
+        coli.sync_check()
+        out[name] = {"bytes": m.nbytes, "copies": ncopy, **res}
+        del Ws
+    return out
+
+
+def bench_prefill(coli, torch, peaks, steps=5):
+    """Prefill expert block: S=544, Zipf(1.1) top-8 over 256 experts, fmt=4
+    gs=128; tokens/s and the fraction of the per-expert roofline
+    sum_e max(bytes_e / HBM, flops_e / bf16 peak)."""
+    c = wl.MOE_PREFILL
+    g = wl.rng(c["seed"])
+    H, F, E, K, S = c["H"], c["F"], c["E"], c["K"], c["S"]
+    dev = []
+    for _ in range(E):
+        trip = wl.expert(g, H, F, c["fmt"], c["gs"])
+        dev.append(tuple(coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in trip))
+    table = coli.ExpertTable(dev)
+    x = torch.from_numpy(wl.activations(g, S, H, bf16_exact=True)).cuda()
+    ids_h, w_h = wl.routing_zipf(g, S, E, K, c["zipf"])
+    ids = torch.from_numpy(ids_h).cuda()
+    w = torch.from_numpy(w_h).cuda()
+    y = torch.empty(S, H, device="cuda")
+    t = _time_loop(torch, lambda i: coli.moe_block(x, table, ids, w, y), steps, warm=2)
+    coli.sync_check()
+    counts = np.bincount(ids_h.reshape(-1), minlength=E)
+    eb = wl.expert_bytes(H, F, c["fmt"], c["gs"])
+    flops_per_row = 2 * 3 * H * F
+    roof = sum(max(eb / (peaks["hbm_gbs"] * 1e9), n * flops_per_row / (peaks["bf16_tflops"] * 1e12))
+               for n in counts if n > 0)
+    touched = int((counts > 0).sum())
+    return {"tokens/s": S / t, "ms": t * 1e3, "experts_touched": touched, "max_rows_per_expert": int(counts.max()),
+            "GB/s": touched * eb / t / 1e9, "GFLOP": float(counts.sum() * flops_per_row / 1e9),
+            "roofline_ms": roof * 1e3, "frac_of_per_expert_roofline": roof / t}
+
+
+def bench_streaming(coli, torch, peaks, tokens=10):
+    """Weight streaming: S=1 GEMVs of 2048x6144 over a 40 GB resident pool,
+    8 random matrices per layer (one launch: shared input), 75 layers per token."""
+    c = wl.STREAMING
+    res = {}
+    for fmt, gs in c["variants"]:
+        g = wl.rng(c["seed"] + fmt)
+        per = wl.tensor_bytes(fmt, c["O"], c["I"], gs)
+        n_pool = int(c["pool_gb"] * 1e9 // per)
+        srcs = [wl.random_matrix(g, fmt, c["O"], c["I"], gs) for _ in range(16)]
+        pool = [coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in
+                (srcs[i % 16] for i in range(n_pool))]
+        sel = g.integers(0, n_pool, (c["layers"] * (tokens + 1), c["per_layer"]))
+        x = torch.randn(1, c["I"], device="cuda")
+        ys = [torch.empty(1, c["O"], device="cuda") for _ in range(c["per_layer"])]
+        n_layers = c["layers"] * tokens
+        t = _time_graph(torch, lambda i: coli.matmul_multi([pool[j] for j in sel[i]], x, ys), n_layers, warm=c["layers"])
+        coli.sync_check()
+        nbytes = c["per_layer"] * per
+        res[f"fmt{fmt}" + (f"_g{gs}" if fmt == 4 else "")] = {
+            "pool_matrices": n_pool, "pool_GB": n_pool * per / 1e9, "layer_us": t * 1e6,
+            "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+            "tokens/s": 1.0 / (c["layers"] * t)}
+        del pool
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle, timed as it stands, on a bounded
     sample of the default workload: one routed (row, expert) slot per step."""
@@ -275,6 +399,8 @@ def main():
     ap.add_argument("--workload", default="moe_decode", choices=("moe_decode",))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--experts", type=int, default=None, help="resident experts of the decode workload (default 256)")
+    ap.add_argument("--quick", action="store_true", help="headline workload only (no by_workload sweep)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()
@@ -290,7 +416,7 @@ def main():
     import bit_weight_gemv_fmt1_gb300 as coli
     peaks = load_peaks()
 
-    wk = DecodeBlock(coli, torch, seed_offset=rank)
+    wk = DecodeBlock(coli, torch, seed_offset=rank, n_experts=args.experts)
     stream = torch.cuda.Stream()
     coli.reset_stats()
     for i in range(args.warmup):
@@ -348,6 +474,12 @@ def main():
         cpu = {"value": v, "unit": "GB/s", "cores": orc.threads(), "kind": "oracle",
                "sample": f"{n} whole decode steps (8 routed experts each) in {dt:.1f} s"}
 
+    by_wl = None
+    if rank == 0 and not args.quick:
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+        by_wl = {"gemv": bench_gemv(coli, torch, peaks, l2), "moe_prefill": bench_prefill(coli, torch, peaks),
+                 "weight_streaming": bench_streaming(coli, torch, peaks)}
+
     if rank == 0:
         line = {
             "metric": "decode MoE-block HBM GB/s (algorithmic bytes / time)",
@@ -368,6 +500,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": wk.h2d, "d2h_bytes_per_step": wk.d2h},
             "gpu_launches": launches,
             "clocks": clocks,
+            "by_workload": by_wl,
         }
         print(json.dumps(line), flush=True)
     barrier(world)

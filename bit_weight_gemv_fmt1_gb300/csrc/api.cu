@@ -168,6 +168,7 @@ MatDesc desc_of(const coli_tensor *t) {
     m.rs = t->rs;
     m.gs = t->fmt == 4 ? t->gs : 0;
     m.ng = t->fmt == 4 ? t->ng : 1;
+    m.tmap = t->tmap;
     return m;
 }
 
@@ -238,6 +239,12 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
         e = launch_fmt1_encode(t->q, O * t->rs, st);
         g_launches++;
     }
+    if (e == cudaSuccess && (fmt == 2 || fmt == 4)) {
+        alignas(64) unsigned char map[128];
+        e = encode_codes_map(t->q, t->rs, O, map);
+        if (e == cudaSuccess) e = cudaMalloc(&t->tmap, 128);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(t->tmap, map, 128, cudaMemcpyHostToDevice, st);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         coli_tensor_free(t);
@@ -251,6 +258,7 @@ void coli_tensor_free(coli_tensor *t) {
     if (!t) return;
     if (t->q) cudaFree(t->q);
     if (t->s) cudaFree(t->s);
+    if (t->tmap) cudaFree(t->tmap);
     delete t;
 }
 
@@ -303,8 +311,45 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
         count(nl, wbytes);
         return COLI_OK;
     }
-    // larger S (or activations too large to stage): tiled GEMM, one launch per matrix
+    // larger S (or activations too large to stage): tensor-core GEMM for int4
+    // formats, tiled CUDA-core GEMM otherwise; one pass per matrix
     for (int m = 0; m < n; m++) {
+        if (tc_supported_fmt(W[m]->fmt, W[m]->gs) && W[m]->tmap) {
+            const int I = (int)W[m]->I, I_pad = (I + 63) / 64 * 64;
+            const int rows_alloc = std::max(S, 64);
+            Workspace *ws = nullptr;
+            const size_t planes = (size_t)3 * rows_alloc * I_pad * 2;
+            if (int rc = workspace(ds, st, planes + 256, &ws)) return rc;
+            int *flag = (int *)ws->buf;
+            void *pl = (char *)ws->buf + 256;
+            CU(cudaMemsetAsync(flag, 0, sizeof(int), st), "cudaMemsetAsync(flag)");
+            cudaError_t e = launch_gather_planes(x, I, nullptr, 1, nullptr, S, I, I_pad, pl, (long long)rows_alloc * I_pad,
+                                                 flag, st);
+            if (e != cudaSuccess) return cuda_fail(e, "activation planes launch");
+            alignas(64) unsigned char map[128];
+            e = encode_planes_map(pl, I_pad, 3LL * rows_alloc, map);
+            if (e != cudaSuccess) return cuda_fail(e, "activation tensor map");
+            TcArgs a;
+            memset(&a, 0, sizeof a);
+            a.single = desc_of(W[m]);
+            a.fmt = W[m]->fmt;
+            a.O = (int)W[m]->O;
+            a.I = I;
+            a.nkb = I_pad / 64;
+            a.gkb = W[m]->fmt == 4 ? W[m]->gs / 64 : a.nkb;
+            a.n_mblk = (a.O + 127) / 128;
+            a.P = S;
+            a.rows_alloc = rows_alloc;
+            a.nterm_flag = flag;
+            a.out = y[m];
+            a.ldo = W[m]->O;
+            a.err = ds->err;
+            a.timeout_ns = 2000000000LL;
+            e = launch_gemm_tc(a, map, (S + 63) / 64, ds->n_sm, st);
+            if (e != cudaSuccess) return cuda_fail(e, "tensor-core gemm launch");
+            count(2, (uint64_t)W[m]->alg_bytes);
+            continue;
+        }
         GemmArgs a;
         memset(&a, 0, sizeof a);
         a.single = desc_of(W[m]);
@@ -319,8 +364,8 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
         a.ldo = W[m]->O;
         cudaError_t e = launch_gemm_cc(a, false, (S + kGemmBP - 1) / kGemmBP, st);
         if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+        count(1, (uint64_t)W[m]->alg_bytes);
     }
-    count(n, wbytes);
     return COLI_OK;
 }
 
@@ -523,7 +568,103 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         }
     }
 
-    // ---------------- prefill pipeline
+    // ---------------- prefill on the tensor cores (int4 formats with one gs per role)
+    bool tc_ok = fmt == 2 || fmt == 4;
+    for (int e = 0; e < n_experts && tc_ok; e++) {
+        tc_ok = tc_supported_fmt(fmt, experts[e].gate->gs) && experts[e].gate->gs == g0->gs &&
+                experts[e].up->gs == g0->gs && experts[e].down->gs == experts[0].down->gs &&
+                tc_supported_fmt(fmt, experts[e].down->gs) && experts[e].gate->tmap && experts[e].up->tmap &&
+                experts[e].down->tmap;
+    }
+    if (tc_ok) {
+        const int TR = tc_block_rows();
+        const int max_tiles = (n_slots + TR - 1) / TR + std::min(n_experts, n_slots);
+        const int H_pad = (int)((H + 63) / 64 * 64), F_pad = (int)((F + 63) / 64 * 64);
+        const int rows_alloc = std::max(n_slots, 64);
+        auto al = [](size_t b) { return (b + 255) / 256 * 256; };
+        const size_t sz_off = al((size_t)(n_experts + 1) * 4), sz_ord = al((size_t)n_slots * 4);
+        const size_t sz_tile = al((size_t)max_tiles * 4);
+        const size_t sz_px = al((size_t)3 * rows_alloc * H_pad * 2), sz_gu = al((size_t)n_slots * 2 * F * 4);
+        const size_t sz_ph = al((size_t)3 * rows_alloc * F_pad * 2), sz_out = al((size_t)n_slots * H * 4);
+        const size_t total = sz_off + 2 * sz_ord + 3 * sz_tile + 256 + sz_px + sz_gu + sz_ph + sz_out;
+        Workspace *ws = nullptr;
+        if (int rc = workspace(ds, st, total, &ws)) return rc;
+        char *p = (char *)ws->buf;
+        int32_t *offsets = (int32_t *)p; p += sz_off;
+        int32_t *order = (int32_t *)p; p += sz_ord;
+        int32_t *inv = (int32_t *)p; p += sz_ord;
+        int32_t *te = (int32_t *)p; p += sz_tile;
+        int32_t *tp0 = (int32_t *)p; p += sz_tile;
+        int32_t *tp1 = (int32_t *)p; p += sz_tile;
+        int32_t *ntiles = (int32_t *)p;
+        int *flags = (int *)(p + 64);
+        p += 256;
+        void *px = p; p += sz_px;
+        float *gu = (float *)p; p += sz_gu;
+        void *ph = p; p += sz_ph;
+        float *slot_out = (float *)p;
+        CU(cudaMemsetAsync(flags, 0, 2 * sizeof(int), st), "cudaMemsetAsync(flags)");
+
+        RouteArgs r;
+        memset(&r, 0, sizeof r);
+        r.ids = ids; r.S = S; r.K = K; r.E = n_experts;
+        r.offsets = offsets; r.order = order; r.inv = inv;
+        r.tile_e = te; r.tile_p0 = tp0; r.tile_p1 = tp1; r.n_tiles = ntiles;
+        r.tile_rows = TR;
+        r.err = ds->err;
+        cudaError_t e = launch_route(r, st);
+        if (e != cudaSuccess) return cuda_fail(e, "routing launch");
+        e = launch_gather_planes(x, H, order, K, offsets + n_experts, n_slots, (int)H, H_pad, px,
+                                 (long long)rows_alloc * H_pad, &flags[0], st);
+        if (e != cudaSuccess) return cuda_fail(e, "activation planes launch");
+        alignas(64) unsigned char mapx[128], maph[128];
+        e = encode_planes_map(px, H_pad, 3LL * rows_alloc, mapx);
+        if (e != cudaSuccess) return cuda_fail(e, "activation tensor map");
+        TcArgs a;
+        memset(&a, 0, sizeof a);
+        a.table = table;
+        a.mi = 0;
+        a.dual_mb = (int)((F + 127) / 128);
+        a.fmt = fmt;
+        a.O = (int)F;
+        a.I = (int)H;
+        a.nkb = H_pad / 64;
+        a.gkb = fmt == 4 ? g0->gs / 64 : a.nkb;
+        a.n_mblk = 2 * a.dual_mb;
+        a.tile_e = te; a.tile_p0 = tp0; a.tile_p1 = tp1; a.n_tiles = ntiles;
+        a.rows_alloc = rows_alloc;
+        a.nterm_flag = &flags[0];
+        a.out = gu;
+        a.ldo = 2 * F;
+        a.err = ds->err;
+        a.timeout_ns = 2000000000LL;
+        e = launch_gemm_tc(a, mapx, max_tiles, ds->n_sm, st);
+        if (e != cudaSuccess) return cuda_fail(e, "gate/up tensor-core launch");
+        e = launch_silu_planes(gu, (int)F, offsets + n_experts, n_slots, F_pad, ph, (long long)rows_alloc * F_pad,
+                               &flags[1], st);
+        if (e != cudaSuccess) return cuda_fail(e, "silu planes launch");
+        e = encode_planes_map(ph, F_pad, 3LL * rows_alloc, maph);
+        if (e != cudaSuccess) return cuda_fail(e, "hidden tensor map");
+        TcArgs d = a;
+        d.mi = 2;
+        d.dual_mb = 0;
+        d.O = (int)H;
+        d.I = (int)F;
+        d.nkb = F_pad / 64;
+        d.gkb = fmt == 4 ? experts[0].down->gs / 64 : d.nkb;
+        d.n_mblk = (int)((H + 127) / 128);
+        d.nterm_flag = &flags[1];
+        d.out = slot_out;
+        d.ldo = H;
+        e = launch_gemm_tc(d, maph, max_tiles, ds->n_sm, st);
+        if (e != cudaSuccess) return cuda_fail(e, "down tensor-core launch");
+        e = launch_combine(slot_out, inv, w, S, K, (int)H, y, st);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+        count(6, 0);
+        return COLI_OK;
+    }
+
+    // ---------------- prefill pipeline on the CUDA cores (other formats / group sizes)
     const int max_tiles = (n_slots + kGemmBP - 1) / kGemmBP + std::min(n_experts, n_slots);
     auto al = [](size_t b) { return (b + 255) / 256 * 256; };
     const size_t sz_off = al((size_t)(n_experts + 1) * 4), sz_ord = al((size_t)n_slots * 4);

@@ -30,6 +30,7 @@ struct coli_tensor {
     float *s;            // device scales (NULL for fmt=0)
     int64_t dev_bytes, alg_bytes;
     uint64_t uid;        // unique per upload, never reused
+    void *tmap;          // device copy of the codes' TMA descriptor (int4 formats), else NULL
 };
 
 namespace coli {
@@ -396,6 +397,7 @@ struct MatDesc {
     const float *s;
     long long rs;
     int gs, ng;
+    const void *tmap;         // device copy of the codes' TMA descriptor (int4 formats), else NULL
 };
 // gate, up, down of one routed expert.
 struct ExpertDesc {
@@ -458,6 +460,36 @@ struct RouteArgs {
     int tile_rows;
     int *err;
 };
+
+// Arguments of the tensor-core grouped GEMM (gemm_tc.cu).
+struct TcArgs {
+    const ExpertDesc *table;  // expert table (NULL: use `single`)
+    MatDesc single;
+    int mi;                   // matrix index in the expert
+    int dual_mb;              // > 0: m-blocks >= dual_mb belong to matrix mi+1, written at column offset O
+    int fmt, O, I;
+    int nkb, gkb;             // K-blocks of 64 inputs; K-blocks per scale group
+    int n_mblk;               // m-blocks (of 128 rows) in the launch
+    const int32_t *tile_e, *tile_p0, *tile_p1, *n_tiles;   // NULL: tiles of 64 rows over [0, P)
+    int P;
+    int rows_alloc;           // rows per activation plane
+    const int *nterm_flag;    // device: non-zero when the mid/lo planes are needed
+    float *out;
+    long long ldo;
+    int *err;
+    long long timeout_ns;
+};
+
+bool tc_supported_fmt(int fmt, int gs);
+int tc_block_rows();
+cudaError_t encode_codes_map(const uint8_t *q, long long rs, long long O, void *out128);
+cudaError_t encode_planes_map(const void *planes, long long I_pad, long long total_rows, void *out128);
+cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *order, int kdiv, const int32_t *n_valid,
+                                 int n_rows, int I, int I_pad, void *planes, long long plane_elems, int *flag,
+                                 cudaStream_t st);
+cudaError_t launch_silu_planes(const float *gu, int F, const int32_t *n_valid, int n_rows, int F_pad, void *planes,
+                               long long plane_elems, int *flag, cudaStream_t st);
+cudaError_t launch_gemm_tc(const TcArgs &a, const void *planes_map128, int max_tiles, int n_sm, cudaStream_t st);
 
 cudaError_t launch_moe_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t smem, cudaStream_t st);
 cudaError_t moe_decode_occupancy(int fmt, size_t smem, int *per_sm);

@@ -1,0 +1,527 @@
+// gemm_tc.cu -- grouped dequantizing GEMM on the 5th-generation tensor cores
+// (tcgen05, TMEM accumulators, TMA), for int4 weights (fmt 2 and 4).
+//
+//   out[p][col0 + o] = sum_i W[o][i] * X[p][i]
+//
+// over tiles of (weight matrix, 128 weight rows, up to 64 activation rows).
+// The weights are the M=128 side of the MMA, the activation rows the N side
+// (most routed experts see only a handful of rows).  Codes are exact in bf16
+// (code - 8 in [-8, 7]); each K-group of the scale (gs inputs, fmt=4) is
+// accumulated into its own TMEM buffer and the f32 group scale is applied when
+// the epilogue drains that buffer, so the products and the per-group sums are
+// exact f32 tensor-core arithmetic.  Activations arrive as up to three bf16
+// planes hi/mid/lo with x = hi + mid + lo to f32 precision; when the gather
+// found every mid/lo zero (bf16-representable activations) only the first
+// plane is loaded and multiplied.
+//
+// Warp roles (320 threads, persistent over a static tile schedule):
+//   warps 0-3  dequant: codes (smem) -> bf16 A tile, SW128 K-major layout
+//   warps 4-7  epilogue: TMEM -> registers, group scale, final row scale, store
+//   warp  8    TMA producer: codes box [128 rows x 32 B] + activation planes
+//   warp  9    MMA issuer (one thread), tcgen05.mma kind::f16, M=128, N<=64
+// Every mbarrier wait is bounded in time; on expiry the kernel records
+// DEV_ERR_TIMEOUT, drains its own copies and MMAs (bounded) and frees TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "coli_internal.cuh"
+
+namespace coli {
+
+namespace {
+
+constexpr int BM = 128, BK = 64, BN = 64;
+constexpr int NL = 6;                               // load stages (codes + activation planes)
+constexpr int NA = 2;                               // dequantized A stages
+constexpr int NPL = 3;                              // activation planes
+constexpr int CODES_BYTES = BM * BK / 2;            // 4096
+constexpr int PLANE_BYTES = BN * BK * 2;            // 8192
+constexpr int A_BYTES = BM * BK * 2;                // 16384
+constexpr int OFF_B = 0;
+constexpr int OFF_A = OFF_B + NL * NPL * PLANE_BYTES;
+constexpr int OFF_CODES = OFF_A + NA * A_BYTES;
+constexpr int OFF_BAR = OFF_CODES + NL * CODES_BYTES;
+constexpr int N_BAR = 2 * NL + 2 * NA + 4 + 1;
+constexpr int SMEM_BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;   // + alignment slack
+constexpr int kTcThreads = 320;
+constexpr uint32_t TMEM_COLS = 128;                 // 2 accumulator buffers x 64 columns
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: false once `deadline` (globaltimer ns) has passed or the CTA aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, uint64_t deadline, volatile int *abort) {
+    while (!mbar_try(b, parity)) {
+        if (*abort) return false;
+        if (global_ns() > deadline) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_addr(dst)), "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (SBO), version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading byte offset (unused for K-major SW128)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+    d |= (uint64_t)1 << 46;                 // descriptor version
+    d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
+    return d;
+}
+// Instruction descriptor, kind::f16: D f32, A bf16, B bf16, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+    uint32_t v[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) r[i] = __uint_as_float(v[i]);
+}
+
+struct Tile {
+    int mi, mb, col0, p0, p1, e;
+};
+
+__device__ __forceinline__ Tile tile_of(const TcArgs &a, int L, int n_tiles) {
+    Tile t;
+    int mb = L / n_tiles;
+    const int ti = L - mb * n_tiles;
+    t.mi = a.mi;
+    t.col0 = 0;
+    if (a.dual_mb > 0 && mb >= a.dual_mb) {
+        mb -= a.dual_mb;
+        t.mi = a.mi + 1;
+        t.col0 = a.O;
+    }
+    t.mb = mb;
+    if (a.tile_e) {
+        t.e = a.tile_e[ti];
+        t.p0 = a.tile_p0[ti];
+        t.p1 = a.tile_p1[ti];
+    } else {
+        t.e = 0;
+        t.p0 = ti * BN;
+        t.p1 = min(a.P, t.p0 + BN);
+    }
+    return t;
+}
+
+__device__ __forceinline__ const MatDesc &mat_of(const TcArgs &a, const Tile &t) {
+    return a.table ? a.table[t.e].m[t.mi] : a.single;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
+    uint64_t *load_full = bars, *load_empty = bars + NL;
+    uint64_t *a_full = bars + 2 * NL, *a_empty = bars + 2 * NL + NA;
+    uint64_t *acc_full = bars + 2 * NL + 2 * NA, *acc_empty = acc_full + 2;
+    uint64_t *done = acc_full + 4;
+    uint32_t *tmem_slot = (uint32_t *)(bars + N_BAR);
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_tiles = a.tile_e ? *a.n_tiles : (a.P + BN - 1) / BN;
+    const int total = n_tiles * a.n_mblk;
+    const int nt = (*a.nterm_flag) ? NPL : 1;
+    const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < NL; i++) {
+            mbar_init(&load_full[i], 1);
+            mbar_init(&load_empty[i], 128 + 1);
+        }
+        for (int i = 0; i < NA; i++) {
+            mbar_init(&a_full[i], 128);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 128);
+        }
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 9) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        if (!abort_flag) {
+            abort_flag = 1;
+            atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+        }
+    };
+
+    if (warp == 8) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmx) : "memory");
+            int it = 0;
+            for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
+                const Tile t = tile_of(a, L, n_tiles);
+                const MatDesc &M = mat_of(a, t);
+                for (int kb = 0; kb < a.nkb; kb++, it++) {
+                    const int s = it % NL;
+                    if (it >= NL && !mbar_wait(&load_empty[s], ((it / NL) & 1) ^ 1, deadline, &abort_flag)) {
+                        fail();
+                        break;
+                    }
+                    mbar_expect_tx(&load_full[s], CODES_BYTES + nt * PLANE_BYTES);
+                    tma_load_2d(smem + OFF_CODES + s * CODES_BYTES, (const CUtensorMap *)M.tmap, kb * (BK / 2), t.mb * BM, &load_full[s]);
+                    for (int pl = 0; pl < nt; pl++)
+                        tma_load_2d(smem + OFF_B + (s * NPL + pl) * PLANE_BYTES, &tmx, kb * BK,
+                                    pl * a.rows_alloc + t.p0, &load_full[s]);
+                }
+            }
+            // every copy this thread issued has landed before the CTA may exit
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int k = max(0, it - NL); k < it; k++)
+                mbar_wait(&load_full[k % NL], (k / NL) & 1, dl2, &no_abort);
+        }
+    } else if (warp == 9) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            int it = 0, g = 0;
+            for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
+                const Tile t = tile_of(a, L, n_tiles);
+                const int N = ((t.p1 - t.p0) + 15) & ~15;
+                const uint32_t idesc = idesc_bf16(BM, N);
+                bool ok = true;
+                for (int kb = 0; kb < a.nkb && ok; kb++, it++) {
+                    const bool first = (kb % a.gkb) == 0;
+                    const bool last = ((kb % a.gkb) == a.gkb - 1) || kb == a.nkb - 1;
+                    const int b = g & 1;
+                    const int as = it % NA, s = it % NL;
+                    if (first && g >= 2 && !mbar_wait(&acc_empty[b], ((g >> 1) & 1) ^ 1, deadline, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&a_full[as], (it / NA) & 1, deadline, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_addr(smem + OFF_A + as * A_BYTES);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; j++) {
+                        for (int pl = 0; pl < nt; pl++) {
+                            const uint32_t b_base = smem_addr(smem + OFF_B + (s * NPL + pl) * PLANE_BYTES);
+                            mma_bf16(tmem + b * BN, sdesc_sw128(a_base + j * 32), sdesc_sw128(b_base + j * 32), idesc,
+                                     (first && j == 0 && pl == 0) ? 0u : 1u);
+                        }
+                    }
+                    mma_commit(&a_empty[as]);
+                    mma_commit(&load_empty[s]);
+                    if (last) {
+                        mma_commit(&acc_full[b]);
+                        g++;
+                    }
+                }
+                if (!ok) {
+                    fail();
+                    break;
+                }
+            }
+            mma_commit(done);
+            volatile int no_abort = 0;
+            mbar_wait(done, 0, global_ns() + 200000000ull, &no_abort);
+        }
+    } else if (warp < 4) {
+        // ---------------- dequant: thread r owns weight row r of the tile
+        const int r = tid;
+        int it = 0;
+        for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
+            bool ok = true;
+            for (int kb = 0; kb < a.nkb; kb++, it++) {
+                const int s = it % NL, as = it % NA;
+                if (!mbar_wait(&load_full[s], (it / NL) & 1, deadline, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint4 *crow = (const uint4 *)(smem + OFF_CODES + s * CODES_BYTES + r * 32);
+                const uint4 c0 = crow[0], c1 = crow[1];
+                mbar_arrive(&load_empty[s]);
+                if (it >= NA && !mbar_wait(&a_empty[as], ((it / NA) & 1) ^ 1, deadline, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                uint8_t *arow = smem + OFF_A + as * A_BYTES + r * 128;
+                const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    uint32_t q[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        uint32_t v = ((w[c] >> (4 * k)) & 0x000F000Fu) | 0x43004300u;
+                        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&v);
+                        h = __hsub2(h, off);
+                        q[k] = *reinterpret_cast<uint32_t *>(&h);
+                    }
+                    *reinterpret_cast<uint4 *>(arow + ((c ^ (r & 7)) << 4)) = make_uint4(q[0], q[1], q[2], q[3]);
+                }
+                fence_async_smem();
+                mbar_arrive(&a_full[as]);
+            }
+            if (!ok) {
+                fail();
+                break;
+            }
+        }
+    } else {
+        // ---------------- epilogue: warp 4+q reads TMEM lanes 32q..32q+31
+        const int q = warp - 4;
+        const int m = q * 32 + lane;
+        int g = 0;
+        for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
+            const Tile t = tile_of(a, L, n_tiles);
+            const MatDesc &M = mat_of(a, t);
+            const int n_tok = t.p1 - t.p0;
+            const int nch = (n_tok + 15) >> 4;
+            const int o = t.mb * BM + m;
+            const bool row_ok = o < a.O;
+            float acc[BN];
+#pragma unroll
+            for (int i = 0; i < BN; i++) acc[i] = 0.f;
+            const int ngrp = (a.nkb + a.gkb - 1) / a.gkb;
+            bool ok = true;
+            for (int grp = 0; grp < ngrp; grp++, g++) {
+                const int b = g & 1;
+                if (!mbar_wait(&acc_full[b], (g >> 1) & 1, deadline, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float sc = (a.fmt == 4 && row_ok) ? __ldg(M.s + (size_t)o * M.ng + grp) : 1.0f;
+#pragma unroll
+                for (int c = 0; c < BN / 16; c++) {
+                    if (c < nch) {
+                        float v[16];
+                        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + b * BN + c * 16, v);
+#pragma unroll
+                        for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(sc, v[i], acc[c * 16 + i]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[b]);
+            }
+            if (!ok) {
+                fail();
+                break;
+            }
+            if (row_ok) {
+                const float rs = (a.fmt == 4) ? 1.0f : __ldg(M.s + o);
+                float *dst = a.out + (size_t)t.p0 * a.ldo + t.col0 + o;
+#pragma unroll
+                for (int n = 0; n < BN; n++)
+                    if (n < n_tok) dst[(size_t)n * a.ldo] = acc[n] * rs;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    }
+}
+
+// bf16 planes of the activations: plane t of row p holds the t-th bf16 term
+// of X[src(p)], inputs permuted inside every group of 8 as 0,4,1,5,2,6,3,7 (the
+// order the dequant writes the codes in), zero past I.
+__global__ void gather_planes_kernel(const float *__restrict__ X, long long ldx, const int32_t *order, int kdiv,
+                                     const int32_t *n_valid, int n_rows, int I, int I_pad, __nv_bfloat16 *planes,
+                                     long long plane_elems, int *flag) {
+    const int p = blockIdx.x;
+    if (p >= n_rows) return;
+    const int nv = n_valid ? *n_valid : n_rows;
+    long long src = -1;
+    if (p < nv) src = order ? (long long)(order[p] / kdiv) : (long long)p;
+    bool nz = false;
+    for (int k8 = threadIdx.x; k8 < I_pad / 8; k8 += blockDim.x) {
+        __nv_bfloat16 hi[8], mid[8], lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int e = 8 * k8 + ((i & 1) ? 4 + (i >> 1) : (i >> 1));
+            const float v = (src >= 0 && e < I) ? X[src * ldx + e] : 0.f;
+            hi[i] = __float2bfloat16_rn(v);
+            const float r1 = v - __bfloat162float(hi[i]);
+            mid[i] = __float2bfloat16_rn(r1);
+            const float r2 = r1 - __bfloat162float(mid[i]);
+            lo[i] = __float2bfloat16_rn(r2);
+            nz |= (r1 != 0.f);
+        }
+        const size_t base = (size_t)p * I_pad + 8 * k8;
+        *reinterpret_cast<uint4 *>(planes + base) = *reinterpret_cast<uint4 *>(hi);
+        *reinterpret_cast<uint4 *>(planes + plane_elems + base) = *reinterpret_cast<uint4 *>(mid);
+        *reinterpret_cast<uint4 *>(planes + 2 * plane_elems + base) = *reinterpret_cast<uint4 *>(lo);
+    }
+    if (__syncthreads_or(nz) && threadIdx.x == 0) atomicOr(flag, 1);
+}
+
+// h = silu(g) * u from the fused gate|up output [rows][2F], written as bf16
+// planes for the down projection (same permutation as gather_planes_kernel).
+__global__ void silu_planes_kernel(const float *__restrict__ gu, int F, const int32_t *n_valid, int n_rows, int F_pad,
+                                   __nv_bfloat16 *planes, long long plane_elems, int *flag) {
+    const int p = blockIdx.x;
+    if (p >= n_rows) return;
+    const bool live = p < *n_valid;
+    bool nz = false;
+    for (int k8 = threadIdx.x; k8 < F_pad / 8; k8 += blockDim.x) {
+        __nv_bfloat16 hi[8], mid[8], lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int e = 8 * k8 + ((i & 1) ? 4 + (i >> 1) : (i >> 1));
+            float v = 0.f;
+            if (live && e < F) {
+                const float g = gu[(size_t)p * 2 * F + e], u = gu[(size_t)p * 2 * F + F + e];
+                v = g / (1.0f + expf(-g)) * u;
+            }
+            hi[i] = __float2bfloat16_rn(v);
+            const float r1 = v - __bfloat162float(hi[i]);
+            mid[i] = __float2bfloat16_rn(r1);
+            const float r2 = r1 - __bfloat162float(mid[i]);
+            lo[i] = __float2bfloat16_rn(r2);
+            nz |= (r1 != 0.f);
+        }
+        const size_t base = (size_t)p * F_pad + 8 * k8;
+        *reinterpret_cast<uint4 *>(planes + base) = *reinterpret_cast<uint4 *>(hi);
+        *reinterpret_cast<uint4 *>(planes + plane_elems + base) = *reinterpret_cast<uint4 *>(mid);
+        *reinterpret_cast<uint4 *>(planes + 2 * plane_elems + base) = *reinterpret_cast<uint4 *>(lo);
+    }
+    if (__syncthreads_or(nz) && threadIdx.x == 0) atomicOr(flag, 1);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+}  // namespace
+
+bool tc_supported_fmt(int fmt, int gs) { return fmt == 2 || (fmt == 4 && gs % BK == 0); }
+
+int tc_block_rows() { return BN; }
+
+cudaError_t encode_codes_map(const uint8_t *q, long long rs, long long O, void *out128) {
+    CUtensorMap *out = (CUtensorMap *)out128;
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)rs, (cuuint64_t)O};
+    cuuint64_t strides[1] = {(cuuint64_t)rs};
+    cuuint32_t box[2] = {BK / 2, BM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void *)q, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_planes_map(const void *planes, long long I_pad, long long total_rows, void *out128) {
+    CUtensorMap *out = (CUtensorMap *)out128;
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)I_pad, (cuuint64_t)total_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(I_pad * 2)};
+    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)planes, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *order, int kdiv, const int32_t *n_valid,
+                                 int n_rows, int I, int I_pad, void *planes, long long plane_elems, int *flag,
+                                 cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    gather_planes_kernel<<<n_rows, 128, 0, st>>>(X, ldx, order, kdiv, n_valid, n_rows, I, I_pad,
+                                                 (__nv_bfloat16 *)planes, plane_elems, flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_silu_planes(const float *gu, int F, const int32_t *n_valid, int n_rows, int F_pad, void *planes,
+                               long long plane_elems, int *flag, cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    silu_planes_kernel<<<n_rows, 128, 0, st>>>(gu, F, n_valid, n_rows, F_pad, (__nv_bfloat16 *)planes, plane_elems,
+                                               flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const TcArgs &a, const void *planes_map128, int max_tiles, int n_sm, cudaStream_t st) {
+    const CUtensorMap &tmx = *(const CUtensorMap *)planes_map128;
+    const long long total = (long long)max_tiles * a.n_mblk;
+    if (total <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)(total < n_sm ? total : n_sm);
+    gemm_tc_kernel<<<grid, kTcThreads, SMEM_BYTES, st>>>(tmx, a);
+    return cudaGetLastError();
+}
+
+}  // namespace coli

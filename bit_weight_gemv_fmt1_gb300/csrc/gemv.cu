@@ -11,6 +11,8 @@
 // loads) with U chunks per row in flight, decoding them in registers and
 // accumulating against the staged x; a warp-shuffle reduction finishes each
 // output.  Weights are read exactly once per call.
+#include <atomic>
+
 #include "coli_internal.cuh"
 
 namespace coli {
@@ -101,12 +103,23 @@ template <int FMT, int S, int R>
 cudaError_t launch_t(const GemvJob &job, cudaStream_t st, int n_sm) {
     const size_t smem = (size_t)S * staged_len(FMT, job.cpr) * sizeof(float);
     auto kern = gemv_kernel<FMT, S, R>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    // attribute and occupancy per (instantiation, device, shared-memory size), queried once
+    static std::atomic<long long> cache[16];   // zero = not queried yet (smem is never 0)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::atomic<long long> &cached = cache[dev & 15];
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const long long c = dev < 16 ? cached.load(std::memory_order_relaxed) : -1;
+    if (c >= 0 && (c >> 8) == (long long)smem) {
+        per_sm = (int)(c & 0xFF);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        cached.store(((long long)smem << 8) | (per_sm & 0xFF), std::memory_order_relaxed);
+    }
     int n_tasks = 0;
     for (int m = 0; m < job.n; m++) n_tasks += (job.O[m] + R - 1) / R;
     const int want = (n_tasks + kThreads / 32 - 1) / (kThreads / 32);

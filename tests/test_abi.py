@@ -18,8 +18,8 @@ def declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from bit_weight_gemv_fmt1_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._load_build_module().build()
     return ctypes.CDLL(path)
 
 
