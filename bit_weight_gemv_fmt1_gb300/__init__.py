@@ -50,6 +50,7 @@ _lib.coli_matmul.argtypes = [_vp, _vp, _vp, _int, _vp]
 _lib.coli_matmul_multi.argtypes = [_int, ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp), _int, _vp]
 _lib.coli_moe_route.argtypes = [_vp, _int, _int, _int, _vp, _vp, _vp]
 _lib.coli_moe_block.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp]
+_lib.coli_moe_block_noalloc.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp, _vp]
 _lib.coli_sync_check.argtypes = [_vp]
 _lib.coli_get_stats.argtypes = [ctypes.POINTER(_Stats)]
 _lib.coli_get_stats.restype = None
@@ -58,7 +59,7 @@ _lib.coli_set_fail_after.argtypes = [_i64]
 _lib.coli_set_fail_after.restype = None
 
 EXPORTS = ("coli_tensor_upload", "coli_tensor_free", "coli_tensor_info", "coli_matmul", "coli_matmul_multi",
-           "coli_moe_route", "coli_moe_block", "coli_sync_check", "coli_last_error", "coli_get_stats",
+           "coli_moe_route", "coli_moe_block", "coli_moe_block_noalloc", "coli_sync_check", "coli_last_error", "coli_get_stats",
            "coli_reset_stats", "coli_set_fail_after", "coli_version")
 
 
@@ -168,6 +169,16 @@ def moe_block(x, table: ExpertTable, ids, w, y, stream=None):
     S, K = ids.shape
     _check(_lib.coli_moe_block(_ptr(x), int(S), table.arr, len(table), _ptr(ids), _ptr(w), int(K), _ptr(y),
                                _stream(stream)))
+    return y
+
+
+def moe_block_noalloc(x, table: ExpertTable, ids, w, y, dev_error, stream=None):
+    """The decode expert block without any device allocation (see coli.h);
+    dev_error is a 1-element int32 CUDA tensor that receives the kernel's
+    error code (0 = none)."""
+    S, K = ids.shape
+    _check(_lib.coli_moe_block_noalloc(_ptr(x), int(S), table.arr, len(table), _ptr(ids), _ptr(w), int(K), _ptr(y),
+                                       _ptr(dev_error), _stream(stream)))
     return y
 
 

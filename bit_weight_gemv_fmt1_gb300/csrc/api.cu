@@ -174,6 +174,11 @@ MatDesc desc_of(const coli_tensor *t) {
 
 }  // namespace
 
+namespace coli {
+// Record `msg` as this thread's last error (for coli_last_error) and return code.
+int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+}  // namespace coli
+
 // =================================================================== ABI
 extern "C" {
 

@@ -500,6 +500,9 @@ cudaError_t launch_combine(const float *slot_out, const int32_t *inv, const floa
 cudaError_t launch_fmt1_encode(uint8_t *q, long long n, cudaStream_t st);
 size_t gemv_smem_bytes(int fmt, int cpr, int S, int I, bool generic);
 
+// Record `msg` as the calling thread's last error (coli_last_error) and return code.
+int set_last_error(int code, const char *msg);
+
 constexpr int kDecodeThreads = 256;
 constexpr int kMaxDecodeSlots = 64;
 constexpr int kGemmBP = 32;    // token rows per GEMM tile

@@ -181,6 +181,34 @@ int coli_moe_route(const int32_t *ids, int S, int K, int n_experts, int32_t *off
 int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_experts,
                    const int32_t *ids, const float *w, int K, float *y, void *stream);
 
+/*
+ * The decode expert block of coli_moe_block for callers that cannot allocate
+ * device memory.  The colibri pages have no counterpart of this entry point.
+ *
+ * Some callers must not call cudaMalloc/cudaFree: code that records CUDA
+ * graphs, latency-critical decode loops (allocation synchronises the device),
+ * processes whose GPU memory is owned by another allocator.  coli_moe_block
+ * allocates scratch and an expert-table copy on first use; this entry point
+ * allocates nothing.  Its scratch (expert descriptors, the h buffer, the grid
+ * barrier words) is one file-scope device array of about 2.2 MB that every GPU
+ * loading the library holds until the process exits.
+ *   Arguments as coli_moe_block, plus:
+ *   dev_error  device int32, an output: cleared by the call, then set by the
+ *              kernel to 1 if its bounded grid-wide wait ran out or 2 if a
+ *              routing id was outside [-1, n_experts) (y is then unspecified).
+ *   Limits (refused with COLI_EINVAL, nothing launched): S*K <= 64,
+ *   n_experts <= 1024, S*K*F <= 524288, and the activations must fit the
+ *   single-launch decode kernel's shared memory; fmt=4 needs gs % 32 == 0
+ *   (COLI_EFMT).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that call before any stream capture.  Every
+ * call shares the array: calls that may overlap on the GPU (unordered streams,
+ * several host threads) race and must be serialised by the caller.
+ */
+int coli_moe_block_noalloc(const float *x, int S, const coli_expert *experts, int n_experts,
+                           const int32_t *ids, const float *w, int K, float *y, int32_t *dev_error,
+                           void *stream);
+
 /* Synchronize `stream`, then report (and clear) any error the library's
  * kernels recorded on this device: COLI_ETIMEOUT for a bounded wait that ran
  * out, COLI_EINVAL for an out-of-range routing id, COLI_ECUDA for a CUDA
