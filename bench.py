@@ -285,13 +285,13 @@ def bench_gemv(coli, torch, peaks, l2_bytes):
     return out
 
 
-def bench_prefill(coli, torch, peaks, steps=5):
+def bench_prefill(coli, torch, peaks, steps=5, n_experts=None):
     """Prefill expert block: S=544, Zipf(1.1) top-8 over 256 experts, fmt=4
     gs=128; tokens/s and the fraction of the per-expert roofline
     sum_e max(bytes_e / HBM, flops_e / bf16 peak)."""
     c = wl.MOE_PREFILL
     g = wl.rng(c["seed"])
-    H, F, E, K, S = c["H"], c["F"], c["E"], c["K"], c["S"]
+    H, F, E, K, S = c["H"], c["F"], n_experts or c["E"], c["K"], c["S"]
     dev = []
     for _ in range(E):
         trip = wl.expert(g, H, F, c["fmt"], c["gs"])
@@ -414,7 +414,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--workload", default="moe_decode", choices=("moe_decode",))
+    ap.add_argument("--workload", default="moe_decode", choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming"),
+                    help="moe_decode is the headline line; the others print their own line (for profiling)")
+    ap.add_argument("--experts-prefill", type=int, default=None, help="resident experts of the prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--experts", type=int, default=None, help="resident experts of the decode workload (default 256)")
@@ -433,6 +435,17 @@ def main():
     torch.cuda.set_device(local)
     import bit_weight_gemv_fmt1_gb300 as coli
     peaks = load_peaks()
+    if args.workload != "moe_decode":
+        if rank == 0:
+            if args.workload == "moe_prefill":
+                res = bench_prefill(coli, torch, peaks, steps=max(1, args.steps), n_experts=args.experts_prefill)
+            elif args.workload == "gemv_sweep":
+                l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+                res = bench_gemv(coli, torch, peaks, l2)
+            else:
+                res = bench_streaming(coli, torch, peaks)
+            print(json.dumps({"workload": args.workload, "result": res}), flush=True)
+        return 0
 
     wk = DecodeBlock(coli, torch, seed_offset=rank, n_experts=args.experts)
     stream = torch.cuda.Stream()

@@ -290,6 +290,8 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
     bool generic = false;
     for (int m = 0; m < n; m++) generic |= (W0->fmt == 4 && (W[m]->gs % 32) != 0);
     const size_t smem = gemv_smem_bytes(W0->fmt, W0->cpr, S, (int)W0->I, generic);
+    bool slab = S == 1 && !generic;
+    for (int m = 0; m < n && slab; m++) slab = slab_supported(W[m]->fmt, W[m]->gs) && W[m]->gs == W0->gs;
     if (S <= 8 && smem <= ds->smem_optin) {
         GemvJob job;
         memset(&job, 0, sizeof job);
@@ -311,7 +313,13 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
             job.row_start[m + 1] = job.row_start[m] + job.O[m];
         }
         int nl = 0;
-        cudaError_t e = launch_gemv(job, st, &nl);
+        cudaError_t e;
+        if (slab && slab_gemv_smem(job, ds->n_sm) <= ds->smem_optin) {
+            e = launch_slab_gemv(job, ds->n_sm, st);
+            nl = 1;
+        } else {
+            e = launch_gemv(job, st, &nl);
+        }
         if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
         count(nl, wbytes);
         return COLI_OK;
@@ -525,6 +533,53 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
     if (fmt == 4)
         for (int e = 0; e < n_experts && gs_ok; e++)
             gs_ok = experts[e].gate->gs % 32 == 0 && experts[e].up->gs % 32 == 0 && experts[e].down->gs % 32 == 0;
+
+    // ---------------- decode, S = 1: activation slab in registers, one cooperative launch
+    bool slab_ok = S == 1 && n_slots <= kMaxDecodeSlots && fmt != 3 && F % 32 == 0;
+    for (int e = 0; e < n_experts && slab_ok; e++)
+        slab_ok = slab_supported(fmt, experts[e].gate->gs) && experts[e].gate->gs == g0->gs &&
+                  experts[e].up->gs == g0->gs && slab_supported(fmt, experts[e].down->gs) &&
+                  experts[e].down->gs == experts[0].down->gs;
+    if (slab_ok) {
+        const int grid_min = ds->n_sm;
+        int sb = std::min(n_slots, 8);
+        size_t smem = slab_decode_smem(fmt, cpr_gu, cpr_d, (int)F, n_slots, grid_min, (int)H, sb);
+        while (sb > 1 && smem > 110 * 1024) {
+            sb--;
+            smem = slab_decode_smem(fmt, cpr_gu, cpr_d, (int)F, n_slots, grid_min, (int)H, sb);
+        }
+        int per_sm = 0;
+        if (smem <= ds->smem_optin && slab_decode_occupancy(fmt, smem, &per_sm) == cudaSuccess && per_sm >= 1) {
+            Workspace *ws = nullptr;
+            if (int rc = workspace(ds, st, (size_t)n_slots * F * sizeof(float), &ws)) return rc;
+            const int grid = std::min(per_sm, 2) * ds->n_sm;
+            MoeDecodeArgs a;
+            memset(&a, 0, sizeof a);
+            a.x = x;
+            a.ids = ids;
+            a.w = w;
+            a.y = y;
+            a.table = table;
+            a.n_experts = n_experts;
+            a.S = 1;
+            a.K = K;
+            a.H = (int)H;
+            a.F = (int)F;
+            a.cpr_gu = cpr_gu;
+            a.cpr_d = cpr_d;
+            a.hbuf = (float *)ws->buf;
+            a.bar = ws->bar;
+            a.err = ds->err;
+            a.sb = sb;
+            a.rpc = (int)((H + grid - 1) / grid);
+            a.timeout_ns = 2000000000LL;
+            cudaError_t e = launch_slab_decode(a, fmt, grid, smem, fmt == 4 ? g0->gs : 32,
+                                               fmt == 4 ? experts[0].down->gs : 32, st);
+            if (e != cudaSuccess) return cuda_fail(e, "decode expert-block launch");
+            count(1, 0);
+            return COLI_OK;
+        }
+    }
 
     // ---------------- decode: one cooperative launch
     if (n_slots <= kMaxDecodeSlots && gs_ok) {

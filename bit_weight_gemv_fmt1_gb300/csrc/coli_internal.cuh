@@ -80,12 +80,42 @@ __device__ __forceinline__ int stage_pos(int e) {
     }
 }
 
-// Stage one activation vector src[0..n) into dst[0..len) (zeros past n).
+// Stage one activation vector src[0..n) into dst[0..len) (zeros past n);
+// len is a multiple of 8.  Each thread takes groups of 8 consecutive inputs
+// and issues the loads of UN groups (two 16-byte loads each when src is
+// 16-byte aligned) before any store, so a CTA pays about one memory round
+// trip per UN * nthreads * 8 inputs instead of one per nthreads inputs.
+// Loads go through L2 (.cg): src may have been written earlier in the same
+// kernel by other CTAs.
 template <int FMT>
-__device__ __forceinline__ void stage_vec(float *dst, const float *__restrict__ src, int n, int len,
-                                          int tid, int nthreads) {
-    for (int e = tid; e < len; e += nthreads)
-        dst[stage_pos<FMT>(e)] = e < n ? src[e] : 0.0f;
+__device__ __forceinline__ void stage_vec(float *dst, const float *src, int n, int len, int tid, int nthreads) {
+    constexpr int UN = 4;
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    const int ng = len >> 3;
+    for (int g0 = tid; g0 < ng; g0 += nthreads * UN) {
+        float v[UN][8];
+#pragma unroll
+        for (int u = 0; u < UN; u++) {
+            const int e0 = (g0 + u * nthreads) * 8;
+            if (g0 + u * nthreads < ng && vec && e0 + 8 <= n) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + e0));
+                const float4 b = __ldcg(reinterpret_cast<const float4 *>(src + e0 + 4));
+                v[u][0] = a.x; v[u][1] = a.y; v[u][2] = a.z; v[u][3] = a.w;
+                v[u][4] = b.x; v[u][5] = b.y; v[u][6] = b.z; v[u][7] = b.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i++) v[u][i] = (g0 + u * nthreads < ng && e0 + i < n) ? __ldcg(src + e0 + i) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UN; u++) {
+            const int g = g0 + u * nthreads;
+            if (g < ng) {
+#pragma unroll
+                for (int i = 0; i < 8; i++) dst[stage_pos<FMT>(g * 8 + i)] = v[u][i];
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------- primitives
@@ -499,6 +529,15 @@ cudaError_t launch_combine(const float *slot_out, const int32_t *inv, const floa
                            float *y, cudaStream_t st);
 cudaError_t launch_fmt1_encode(uint8_t *q, long long n, cudaStream_t st);
 size_t gemv_smem_bytes(int fmt, int cpr, int S, int I, bool generic);
+
+// S = 1 kernels with the activation slab in registers (slab.cu).
+bool slab_supported(int fmt, int gs);
+size_t slab_gemv_smem(const GemvJob &job, int n_sm);
+cudaError_t launch_slab_gemv(const GemvJob &job, int n_sm, cudaStream_t st);
+size_t slab_decode_smem(int fmt, int cpr_gu, int cpr_d, int F, int n_slots, int grid_min, int H, int sb);
+cudaError_t slab_decode_occupancy(int fmt, size_t smem, int *per_sm);
+cudaError_t launch_slab_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t smem, int gs_gu, int gs_d,
+                               cudaStream_t st);
 
 // Record `msg` as the calling thread's last error (coli_last_error) and return code.
 int set_last_error(int code, const char *msg);

@@ -14,11 +14,16 @@
 // found every mid/lo zero (bf16-representable activations) only the first
 // plane is loaded and multiplied.
 //
-// Warp roles (320 threads, persistent over a static tile schedule):
+// Warp roles (352 threads, persistent over a static tile schedule):
 //   warps 0-3  dequant: codes (smem) -> bf16 A tile, SW128 K-major layout
 //   warps 4-7  epilogue: TMEM -> registers, group scale, final row scale, store
-//   warp  8    TMA producer: codes box [128 rows x 32 B] + activation planes
+//   warp  8    TMA producer of the codes: box [128 rows x 32 B], 24 stages deep
 //   warp  9    MMA issuer (one thread), tcgen05.mma kind::f16, M=128, N<=64
+//   warp 10    TMA producer of the activation planes: 16-row boxes, only as
+//              many as the tile's rows need
+// The codes ring is released by the dequant warps as soon as they have read a
+// stage, so its depth alone sets the bytes in flight from HBM; the plane ring
+// (activations, mostly L2 hits) is released by the MMA commits.
 // Every mbarrier wait is bounded in time; on expiry the kernel records
 // DEV_ERR_TIMEOUT, drains its own copies and MMAs (bounded) and frees TMEM.
 #include <cuda.h>
@@ -32,20 +37,25 @@ namespace coli {
 namespace {
 
 constexpr int BM = 128, BK = 64, BN = 64;
-constexpr int NL = 6;                               // load stages (codes + activation planes)
+constexpr int NC = 24;                              // codes stages (4 KB each): the HBM stream
+constexpr int B_RING = 72 * 1024;                   // activation-plane ring: 9 stages of 1 plane, 3 of 3
+constexpr int NBMAX = 9;
 constexpr int NA = 2;                               // dequantized A stages
 constexpr int NPL = 3;                              // activation planes
 constexpr int CODES_BYTES = BM * BK / 2;            // 4096
-constexpr int PLANE_BYTES = BN * BK * 2;            // 8192
+constexpr int PLANE_BYTES = BN * BK * 2;            // 8192 (64 rows x 128 B)
+constexpr int BOX_ROWS = 16;                        // activation rows per TMA box
+constexpr int BOX_BYTES = BOX_ROWS * BK * 2;        // 2048
 constexpr int A_BYTES = BM * BK * 2;                // 16384
 constexpr int OFF_B = 0;
-constexpr int OFF_A = OFF_B + NL * NPL * PLANE_BYTES;
+constexpr int OFF_A = OFF_B + B_RING;
 constexpr int OFF_CODES = OFF_A + NA * A_BYTES;
-constexpr int OFF_BAR = OFF_CODES + NL * CODES_BYTES;
-constexpr int N_BAR = 2 * NL + 2 * NA + 4 + 1;
+constexpr int OFF_BAR = OFF_CODES + NC * CODES_BYTES;
+constexpr int NACC = 4;                             // TMEM accumulator buffers (64 columns each)
+constexpr int N_BAR = 2 * NC + 2 * NBMAX + 2 * NA + 2 * NACC + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;   // + alignment slack
-constexpr int kTcThreads = 320;
-constexpr uint32_t TMEM_COLS = 128;                 // 2 accumulator buffers x 64 columns
+constexpr int kTcThreads = 352;
+constexpr uint32_t TMEM_COLS = 256;                 // NACC accumulator buffers x 64 columns
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -112,17 +122,15 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
-    uint32_t v[16];
+// 16 consecutive TMEM columns of this thread's lane; complete after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; i++) r[i] = __uint_as_float(v[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 struct Tile {
     int mi, mb, col0, p0, p1, e;
@@ -160,10 +168,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
-    uint64_t *load_full = bars, *load_empty = bars + NL;
-    uint64_t *a_full = bars + 2 * NL, *a_empty = bars + 2 * NL + NA;
-    uint64_t *acc_full = bars + 2 * NL + 2 * NA, *acc_empty = acc_full + 2;
-    uint64_t *done = acc_full + 4;
+    uint64_t *c_full = bars, *c_empty = bars + NC;
+    uint64_t *b_full = bars + 2 * NC, *b_empty = b_full + NBMAX;
+    uint64_t *a_full = b_empty + NBMAX, *a_empty = a_full + NA;
+    uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + NACC;
+    uint64_t *done = acc_empty + NACC;
     uint32_t *tmem_slot = (uint32_t *)(bars + N_BAR);
     __shared__ volatile int abort_flag;
 
@@ -171,19 +180,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const int n_tiles = a.tile_e ? *a.n_tiles : (a.P + BN - 1) / BN;
     const int total = n_tiles * a.n_mblk;
     const int nt = (*a.nterm_flag) ? NPL : 1;
+    const int NB = B_RING / (nt * PLANE_BYTES);      // plane stages: 9 (one plane) or 3 (three)
+    const int b_stage = nt * PLANE_BYTES;
     const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
 
     if (tid == 0) {
         abort_flag = 0;
-        for (int i = 0; i < NL; i++) {
-            mbar_init(&load_full[i], 1);
-            mbar_init(&load_empty[i], 128 + 1);
+        for (int i = 0; i < NC; i++) {
+            mbar_init(&c_full[i], 1);
+            mbar_init(&c_empty[i], 128);
+        }
+        for (int i = 0; i < NBMAX; i++) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
         }
         for (int i = 0; i < NA; i++) {
             mbar_init(&a_full[i], 128);
             mbar_init(&a_empty[i], 1);
         }
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < NACC; i++) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 128);
         }
@@ -208,31 +223,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     };
 
     if (warp == 8) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer: codes
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmx) : "memory");
             int it = 0;
             for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
                 const Tile t = tile_of(a, L, n_tiles);
                 const MatDesc &M = mat_of(a, t);
                 for (int kb = 0; kb < a.nkb; kb++, it++) {
-                    const int s = it % NL;
-                    if (it >= NL && !mbar_wait(&load_empty[s], ((it / NL) & 1) ^ 1, deadline, &abort_flag)) {
+                    const int s = it % NC;
+                    if (it >= NC && !mbar_wait(&c_empty[s], ((it / NC) & 1) ^ 1, deadline, &abort_flag)) {
                         fail();
                         break;
                     }
-                    mbar_expect_tx(&load_full[s], CODES_BYTES + nt * PLANE_BYTES);
-                    tma_load_2d(smem + OFF_CODES + s * CODES_BYTES, (const CUtensorMap *)M.tmap, kb * (BK / 2), t.mb * BM, &load_full[s]);
-                    for (int pl = 0; pl < nt; pl++)
-                        tma_load_2d(smem + OFF_B + (s * NPL + pl) * PLANE_BYTES, &tmx, kb * BK,
-                                    pl * a.rows_alloc + t.p0, &load_full[s]);
+                    mbar_expect_tx(&c_full[s], CODES_BYTES);
+                    tma_load_2d(smem + OFF_CODES + s * CODES_BYTES, (const CUtensorMap *)M.tmap, kb * (BK / 2),
+                                t.mb * BM, &c_full[s]);
                 }
             }
             // every copy this thread issued has landed before the CTA may exit
             const uint64_t dl2 = global_ns() + 200000000ull;
             volatile int no_abort = 0;
-            for (int k = max(0, it - NL); k < it; k++)
-                mbar_wait(&load_full[k % NL], (k / NL) & 1, dl2, &no_abort);
+            for (int k = max(0, it - NC); k < it; k++) mbar_wait(&c_full[k % NC], (k / NC) & 1, dl2, &no_abort);
+        }
+    } else if (warp == 10) {
+        // ---------------- TMA producer: activation planes, 16-row boxes
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmx) : "memory");
+            int it = 0;
+            for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
+                const Tile t = tile_of(a, L, n_tiles);
+                const int nbox = (t.p1 - t.p0 + BOX_ROWS - 1) / BOX_ROWS;
+                for (int kb = 0; kb < a.nkb; kb++, it++) {
+                    const int s = it % NB;
+                    if (it >= NB && !mbar_wait(&b_empty[s], ((it / NB) & 1) ^ 1, deadline, &abort_flag)) {
+                        fail();
+                        break;
+                    }
+                    mbar_expect_tx(&b_full[s], nt * nbox * BOX_BYTES);
+                    for (int pl = 0; pl < nt; pl++)
+                        for (int bx = 0; bx < nbox; bx++)
+                            tma_load_2d(smem + OFF_B + s * b_stage + pl * PLANE_BYTES + bx * BOX_BYTES, &tmx,
+                                        kb * BK, pl * a.rows_alloc + t.p0 + bx * BOX_ROWS, &b_full[s]);
+                }
+            }
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int k = max(0, it - NB); k < it; k++) mbar_wait(&b_full[k % NB], (k / NB) & 1, dl2, &no_abort);
         }
     } else if (warp == 9) {
         // ---------------- MMA issuer
@@ -246,13 +282,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 for (int kb = 0; kb < a.nkb && ok; kb++, it++) {
                     const bool first = (kb % a.gkb) == 0;
                     const bool last = ((kb % a.gkb) == a.gkb - 1) || kb == a.nkb - 1;
-                    const int b = g & 1;
-                    const int as = it % NA, s = it % NL;
-                    if (first && g >= 2 && !mbar_wait(&acc_empty[b], ((g >> 1) & 1) ^ 1, deadline, &abort_flag)) {
+                    const int b = g % NACC;
+                    const int as = it % NA, bs = it % NB;
+                    if (first && g >= NACC &&
+                        !mbar_wait(&acc_empty[b], ((g / NACC) & 1) ^ 1, deadline, &abort_flag)) {
                         ok = false;
                         break;
                     }
-                    if (!mbar_wait(&a_full[as], (it / NA) & 1, deadline, &abort_flag)) {
+                    if (!mbar_wait(&a_full[as], (it / NA) & 1, deadline, &abort_flag) ||
+                        !mbar_wait(&b_full[bs], (it / NB) & 1, deadline, &abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -261,13 +299,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
                     for (int j = 0; j < BK / 16; j++) {
                         for (int pl = 0; pl < nt; pl++) {
-                            const uint32_t b_base = smem_addr(smem + OFF_B + (s * NPL + pl) * PLANE_BYTES);
+                            const uint32_t b_base = smem_addr(smem + OFF_B + bs * b_stage + pl * PLANE_BYTES);
                             mma_bf16(tmem + b * BN, sdesc_sw128(a_base + j * 32), sdesc_sw128(b_base + j * 32), idesc,
                                      (first && j == 0 && pl == 0) ? 0u : 1u);
                         }
                     }
                     mma_commit(&a_empty[as]);
-                    mma_commit(&load_empty[s]);
+                    mma_commit(&b_empty[bs]);
                     if (last) {
                         mma_commit(&acc_full[b]);
                         g++;
@@ -289,14 +327,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
             bool ok = true;
             for (int kb = 0; kb < a.nkb; kb++, it++) {
-                const int s = it % NL, as = it % NA;
-                if (!mbar_wait(&load_full[s], (it / NL) & 1, deadline, &abort_flag)) {
+                const int s = it % NC, as = it % NA;
+                if (!mbar_wait(&c_full[s], (it / NC) & 1, deadline, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 const uint4 *crow = (const uint4 *)(smem + OFF_CODES + s * CODES_BYTES + r * 32);
                 const uint4 c0 = crow[0], c1 = crow[1];
-                mbar_arrive(&load_empty[s]);
+                mbar_arrive(&c_empty[s]);
                 if (it >= NA && !mbar_wait(&a_empty[as], ((it / NA) & 1) ^ 1, deadline, &abort_flag)) {
                     ok = false;
                     break;
@@ -324,7 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 break;
             }
         }
-    } else {
+    } else if (warp < 8) {
         // ---------------- epilogue: warp 4+q reads TMEM lanes 32q..32q+31
         const int q = warp - 4;
         const int m = q * 32 + lane;
@@ -340,26 +378,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
             for (int i = 0; i < BN; i++) acc[i] = 0.f;
             const int ngrp = (a.nkb + a.gkb - 1) / a.gkb;
+            // group scales of this row, loaded SD groups ahead of their use
+            constexpr int SD = 4;
+            const bool grouped = a.fmt == 4 && row_ok;
+            const float *srow = grouped ? M.s + (size_t)o * M.ng : nullptr;
+            float scq[SD];
+#pragma unroll
+            for (int i = 0; i < SD; i++) scq[i] = (grouped && i < ngrp) ? __ldg(srow + i) : 1.0f;
             bool ok = true;
-            for (int grp = 0; grp < ngrp; grp++, g++) {
-                const int b = g & 1;
-                if (!mbar_wait(&acc_full[b], (g >> 1) & 1, deadline, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const float sc = (a.fmt == 4 && row_ok) ? __ldg(M.s + (size_t)o * M.ng + grp) : 1.0f;
+            for (int grp0 = 0; grp0 < ngrp && ok; grp0 += SD) {
 #pragma unroll
-                for (int c = 0; c < BN / 16; c++) {
-                    if (c < nch) {
-                        float v[16];
-                        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + b * BN + c * 16, v);
-#pragma unroll
-                        for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(sc, v[i], acc[c * 16 + i]);
+                for (int i = 0; i < SD; i++) {
+                    const int grp = grp0 + i;
+                    if (grp >= ngrp) break;
+                    const float sc = scq[i];
+                    scq[i] = (grouped && grp + SD < ngrp) ? __ldg(srow + grp + SD) : 1.0f;
+                    const int b = g % NACC;
+                    if (!mbar_wait(&acc_full[b], (g / NACC) & 1, deadline, &abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    uint32_t v[BN / 16][16];
+#pragma unroll
+                    for (int c = 0; c < BN / 16; c++)
+                        if (c < nch) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + b * BN + c * 16, v[c]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < BN / 16; c++) {
+                        if (c < nch) {
+#pragma unroll
+                            for (int k = 0; k < 16; k++)
+                                acc[c * 16 + k] = fmaf(sc, __uint_as_float(v[c][k]), acc[c * 16 + k]);
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&acc_empty[b]);
+                    g++;
                 }
-                tc_fence_before();
-                mbar_arrive(&acc_empty[b]);
             }
             if (!ok) {
                 fail();
@@ -488,7 +544,7 @@ cudaError_t encode_planes_map(const void *planes, long long I_pad, long long tot
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)I_pad, (cuuint64_t)total_rows};
     cuuint64_t strides[1] = {(cuuint64_t)(I_pad * 2)};
-    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t box[2] = {BK, BOX_ROWS};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)planes, dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

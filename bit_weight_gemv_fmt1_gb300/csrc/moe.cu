@@ -207,10 +207,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) moe_decode_kernel(const Moe
         for (int b0 = 0; b0 < nvalid; b0 += a.sb) {
             const int b1 = min(nvalid, b0 + a.sb);
             __syncthreads();
-            for (int p = b0; p < b1; p++) {
-                float *dst = stage + (size_t)(p - b0) * xlen_d;
-                const float *src = a.hbuf + (size_t)p * a.F;
-                for (int e = tid; e < xlen_d; e += blockDim.x) dst[stage_pos<FMT>(e)] = e < a.F ? __ldcg(src + e) : 0.f;
+            if (xlen_d == a.F) {   // contiguous unpadded rows: one staging pass for the batch
+                stage_vec<FMT>(stage, a.hbuf + (size_t)b0 * a.F, (b1 - b0) * a.F, (b1 - b0) * xlen_d, tid, blockDim.x);
+            } else {
+                for (int p = b0; p < b1; p++)
+                    stage_vec<FMT>(stage + (size_t)(p - b0) * xlen_d, a.hbuf + (size_t)p * a.F, a.F, xlen_d, tid,
+                                   blockDim.x);
             }
             __syncthreads();
             // experts intersecting [b0, b1)

@@ -1,0 +1,576 @@
+// slab.cu -- S = 1 matvec and S = 1 decode expert block, "activation slab in
+// registers" form.
+//
+// A row of W is cut into slabs of 32 chunks of 16 bytes (512 bytes: 1024 int4,
+// 512 int8 or 128 f32 inputs).  A warp owns one slab at a time: each lane keeps
+// the activations of its own 16-byte chunk in registers (read once from the
+// swizzled shared-memory copy) and the warp streams rows of that slab -- one
+// coalesced 512-byte load per row -- through a software prefetch ring of P
+// rows, so the loads of the next P rows are in flight while the current one is
+// decoded and multiplied.  Each row's slab partial is reduced across the warp
+// and stored per (slab, row) in shared memory; the CTA then adds the slabs of
+// a row in ascending order, so results do not depend on timing.
+//
+// Formats 0, 1, 2 and 4 (fmt=4 with gs = 32 * 2^k, one scale per chunk).
+//
+// The arithmetic per chunk is that of dot_rows: exact decode of each code into
+// the mantissa of 1.0 (or 2^23 for int8), exact offset removal, packed f32x2
+// FMA into bit-position classes that are rescaled by powers of two.
+#include "coli_internal.cuh"
+
+namespace coli {
+
+namespace {
+
+constexpr int kSlabThreads = 256;
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    F2U A{a}, B{b}, D;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(D.u) : "l"(A.u), "l"(B.u));
+    return D.f;
+}
+
+__host__ __device__ inline size_t staged_words(int fmt, int cpr) { return (size_t)staged_len(fmt, cpr); }
+
+// Activations of one lane's chunk, in registers, and the chunk dot product.
+template <int FMT> struct XReg;
+
+template <> struct XReg<4> {
+    float4 v[8];
+    __device__ __forceinline__ void load(const uint32_t *stage, int c) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(stage + (size_t)c * 32);
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[j] = s4[j ^ (c & 7)];
+    }
+    __device__ __forceinline__ float dot(uint4 q) const {
+        Acc4 a;
+        Dec4 d = decode4(q.x);
+        a.a01 = fmul2(d.v01, make_float2(v[0].x, v[0].y));
+        a.a25 = fmul2(d.v25, make_float2(v[0].z, v[0].w));
+        a.a36 = fmul2(d.v36, make_float2(v[1].x, v[1].y));
+        a.a47 = fmul2(d.v47, make_float2(v[1].z, v[1].w));
+        fma4(a, decode4(q.y), v[2], v[3]);
+        fma4(a, decode4(q.z), v[4], v[5]);
+        fma4(a, decode4(q.w), v[6], v[7]);
+        return acc_combine(a);
+    }
+};
+template <> struct XReg<2> : XReg<4> {};
+
+template <> struct XReg<1> {
+    float4 v[4];
+    __device__ __forceinline__ void load(const uint32_t *stage, int c) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(stage + (size_t)c * 16);
+#pragma unroll
+        for (int j = 0; j < 4; j++) v[j] = s4[j ^ ((c >> 1) & 3)];
+    }
+    __device__ __forceinline__ float dot(uint4 q) const {
+        Acc1 a;
+        Dec1 d = decode1(q.x);
+        a.a = fmul2(d.v01, make_float2(v[0].x, v[0].y));
+        a.b = fmul2(d.v23, make_float2(v[0].z, v[0].w));
+        fma1(a, decode1(q.y), v[1]);
+        fma1(a, decode1(q.z), v[2]);
+        fma1(a, decode1(q.w), v[3]);
+        return acc_combine(a);
+    }
+};
+
+template <> struct XReg<0> {
+    float4 v;
+    __device__ __forceinline__ void load(const uint32_t *stage, int c) {
+        v = reinterpret_cast<const float4 *>(stage)[c];
+    }
+    __device__ __forceinline__ float dot(uint4 q) const {
+        float2 a = fmul2(make_float2(__uint_as_float(q.x), __uint_as_float(q.y)), make_float2(v.x, v.y));
+        ffma2(a, make_float2(__uint_as_float(q.z), __uint_as_float(q.w)), make_float2(v.z, v.w));
+        return a.x + a.y;
+    }
+};
+
+// Unit walker: units u = w, w+NW, ... over a slab-major index space
+// u = s * n_rows + rr, kept incrementally (no division per unit).
+struct Walk {
+    int s, rr;
+    __device__ __forceinline__ void init(int u, int n_rows) {
+        s = u / n_rows;
+        rr = u - s * n_rows;
+    }
+    __device__ __forceinline__ void step(int nw, int n_rows) {
+        rr += nw;
+        while (rr >= n_rows) {
+            rr -= n_rows;
+            s++;
+        }
+    }
+};
+
+// Stage activations in the swizzled order XReg<FMT> reads.
+template <int FMT>
+__device__ __forceinline__ void stage_x(uint32_t *dst, const float *src, int n, int cpr) {
+    stage_vec<FMT>(reinterpret_cast<float *>(dst), src, n, staged_len(FMT, cpr), threadIdx.x, blockDim.x);
+}
+
+__device__ __forceinline__ uint4 ld_or_zero(const uint8_t *p, bool ok) {
+    return ok ? ld_stream(p) : make_uint4(0, 0, 0, 0);
+}
+
+// ------------------------------------------------------------------ matvec
+// Rows of all matrices of the job form one index space (row_start prefix);
+// CTA b owns rows [b*rpc, (b+1)*rpc).
+template <int FMT, int P>
+__global__ void __launch_bounds__(kSlabThreads, 2) slab_gemv_kernel(const GemvJob job, int rpc, int gshift) {
+    extern __shared__ float4 smem4[];
+    uint32_t *xs = reinterpret_cast<uint32_t *>(smem4);
+    const size_t xwords = staged_words(FMT, job.cpr);
+    float *red = reinterpret_cast<float *>(xs + xwords);   // [n_slab][rpc]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int n_slab = (job.cpr + 31) >> 5;
+    const int total_rows = job.row_start[job.n];
+    const int r0 = blockIdx.x * rpc;
+    const int n_rows = min(rpc, total_rows - r0);
+    if (n_rows <= 0) return;
+    stage_x<FMT>(xs, job.x, job.I, job.cpr);
+    __syncthreads();
+
+    const int n_units = n_slab * n_rows;
+    auto row_of = [&](int rr, int &m, int &o) {
+        const int r = r0 + rr;
+        m = 0;
+        while (r >= job.row_start[m + 1]) m++;
+        o = r - job.row_start[m];
+    };
+    uint4 qb[P];
+    float sb[P];
+    Walk wl, wc;
+    wl.init(warp < n_units ? warp : 0, n_rows);
+    wc = wl;
+#pragma unroll
+    for (int i = 0; i < P; i++) {
+        const int u = warp + i * nw;
+        const bool ok = u < n_units;
+        int m = 0, o = 0;
+        if (ok) row_of(wl.rr, m, o);
+        const int c = wl.s * 32 + lane;
+        const bool okc = ok && c < job.cpr;
+        qb[i] = ld_or_zero(job.q[m] + (size_t)o * job.rs[m] + (size_t)c * 16, okc);
+        if constexpr (FMT == 4) sb[i] = okc ? __ldg(job.s[m] + (size_t)o * job.ng[m] + (c >> gshift)) : 0.f;
+        else if constexpr (FMT != 0) sb[i] = ok ? __ldg(job.s[m] + o) : 0.f;
+        else sb[i] = 1.f;
+        if (ok) wl.step(nw, n_rows);
+    }
+    XReg<FMT> xr;
+    int cur_s = -1;
+    for (int k0 = 0; warp + k0 * nw < n_units; k0 += P) {
+#pragma unroll
+        for (int i = 0; i < P; i++) {
+            const int u = warp + (k0 + i) * nw;
+            if (u >= n_units) break;
+            if (wc.s != cur_s) {
+                cur_s = wc.s;
+                const int c = cur_s * 32 + lane;
+                xr.load(xs, c < n_slab * 32 ? c : 0);
+            }
+            float p = xr.dot(qb[i]) * sb[i];
+            // refill slot i with unit u + P*nw
+            const int un = u + P * nw;
+            const bool ok = un < n_units;
+            int m = 0, o = 0;
+            if (ok) row_of(wl.rr, m, o);
+            const int cn = wl.s * 32 + lane;
+            const bool okc = ok && cn < job.cpr;
+            qb[i] = ld_or_zero(job.q[m] + (size_t)o * job.rs[m] + (size_t)cn * 16, okc);
+            if constexpr (FMT == 4) sb[i] = okc ? __ldg(job.s[m] + (size_t)o * job.ng[m] + (cn >> gshift)) : 0.f;
+            else if constexpr (FMT != 0) sb[i] = ok ? __ldg(job.s[m] + o) : 0.f;
+            if (ok) wl.step(nw, n_rows);
+            p = warp_sum(p);
+            if (lane == 0) red[cur_s * rpc + wc.rr] = p;
+            wc.step(nw, n_rows);
+        }
+    }
+    __syncthreads();
+    for (int rr = threadIdx.x; rr < n_rows; rr += blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < n_slab; s++) acc += red[s * rpc + rr];
+        int m, o;
+        row_of(rr, m, o);
+        job.y[m][o] = acc;
+    }
+}
+
+// ------------------------------------------------------------------ decode block, S = 1
+__device__ bool slab_grid_barrier(unsigned *bar, int *err, long long timeout_ns) {
+    __shared__ int ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ok = 1;
+        const unsigned gen = ld_acquire(bar + 1);
+        __threadfence();
+        const unsigned prev = atomicAdd(bar, 1u);
+        if (prev == gridDim.x - 1) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            atomicAdd(bar + 1, 1u);
+        } else {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire(bar + 1) == gen) {
+                if ((long long)(global_ns() - t0) > timeout_ns) {
+                    atomicCAS(err, 0, DEV_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(100);
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return ok != 0;
+}
+
+__device__ __forceinline__ const float *srow(int fmt, const MatDesc &m, int row) {
+    return fmt == 4 ? m.s + (size_t)row * m.ng : m.s + row;
+}
+
+template <int FMT>
+__device__ __forceinline__ float unit_scale(const MatDesc &m, int row, int c, int gshift, bool ok) {
+    if constexpr (FMT == 4) return ok ? __ldg(m.s + (size_t)row * m.ng + (c >> gshift)) : 0.f;
+    else if constexpr (FMT == 0) return 1.f;
+    else return ok ? __ldg(m.s + row) : 0.f;
+}
+
+// Phase A unit = (slab s, pair index pr) -> expert a = pr / F, row j = pr % F,
+// two rows (gate j, up j) of expert a; all against the token's activations.
+// Phase B unit = (expert-in-batch a, slab s, row rr of the CTA's output rows).
+template <int FMT, int P>
+__global__ void __launch_bounds__(kSlabThreads, 2) moe_decode_slab_kernel(const MoeDecodeArgs a, int gshift_gu,
+                                                                           int gshift_d) {
+    extern __shared__ float4 smem4[];
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem4);
+    __shared__ int s_ids[kMaxDecodeSlots];
+    __shared__ float s_w[kMaxDecodeSlots];
+    __shared__ int s_exp[kMaxDecodeSlots];
+    __shared__ float s_ew[kMaxDecodeSlots];
+    __shared__ int s_nact, s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int n = a.K;   // S = 1
+
+    // ---- phase 0: distinct routed experts in ascending id order, weights summed
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    if (tid < n) {
+        const int e = a.ids[tid];
+        s_ids[tid] = e;
+        s_w[tid] = a.w[tid];
+        if (e < -1 || e >= a.n_experts) atomicOr(&s_bad, 1);
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (blockIdx.x == 0 && tid == 0) atomicCAS(a.err, 0, DEV_ERR_BAD_ID);
+        return;
+    }
+    if (tid == 0) {
+        int na = 0;
+        int last = -1;
+        for (;;) {   // next larger id
+            int best = 0x7fffffff;
+            for (int t = 0; t < n; t++)
+                if (s_ids[t] > last && s_ids[t] < best) best = s_ids[t];
+            if (best == 0x7fffffff) break;
+            float wsum = 0.f;
+            for (int t = 0; t < n; t++)
+                if (s_ids[t] == best) wsum += s_w[t];
+            s_exp[na] = best;
+            s_ew[na] = wsum;
+            na++;
+            last = best;
+        }
+        s_nact = na;
+    }
+    __syncthreads();
+    const int nact = s_nact;
+
+    // ---- phase A: h[a][j] = silu(G_a[j] x) * (U_a[j] x)
+    const size_t xw_gu = staged_words(FMT, a.cpr_gu);
+    const int n_slab_gu = (a.cpr_gu + 31) >> 5;
+    const long long pairs = (long long)nact * a.F;
+    const int ppc = (int)((pairs + gridDim.x - 1) / gridDim.x);       // pairs per CTA
+    const long long pr0 = (long long)blockIdx.x * ppc;
+    const int n_pr = (int)max(0LL, min((long long)ppc, pairs - pr0));
+    float *redA = reinterpret_cast<float *>(stage + xw_gu);           // [n_slab][ppc][2]
+    if (n_pr > 0) {
+        stage_x<FMT>(stage, a.x, a.H, a.cpr_gu);
+        __syncthreads();
+        const int n_units = n_slab_gu * n_pr;
+        uint4 qg[P], qu[P];
+        float sg[P], su[P];
+        Walk wl, wc;
+        wl.init(warp < n_units ? warp : 0, n_pr);
+        wc = wl;
+        // (expert index, row) of the prefetch walker, kept incrementally; the
+        // expert's gate/up descriptors are cached and reloaded on change
+        int lai, lj;
+        {
+            const long long pr = pr0 + wl.rr;
+            lai = (int)(pr / a.F);
+            lj = (int)(pr - (long long)lai * a.F);
+        }
+        int cur_ai = -1;
+        MatDesc Gd = {}, Ud = {};
+        auto load = [&](int i, bool ok) {
+            if (ok && lai != cur_ai) {
+                cur_ai = lai;
+                const ExpertDesc &E = a.table[s_exp[lai]];
+                Gd = E.m[0];
+                Ud = E.m[1];
+            }
+            const int j = lj;
+            const int c = wl.s * 32 + lane;
+            const bool okc = ok && c < a.cpr_gu;
+            qg[i] = ld_or_zero(Gd.q + (size_t)j * Gd.rs + (size_t)c * 16, okc);
+            qu[i] = ld_or_zero(Ud.q + (size_t)j * Ud.rs + (size_t)c * 16, okc);
+            sg[i] = unit_scale<FMT>(Gd, j, c, gshift_gu, okc);
+            su[i] = unit_scale<FMT>(Ud, j, c, gshift_gu, okc);
+            if (ok) {
+                const int rr_before = wl.rr;
+                wl.step(nw, n_pr);
+                // advance (lai, lj) by the same pair-index step (rr moved by nw, minus n_pr per slab wrap)
+                lj += wl.rr - rr_before;
+                while (lj >= a.F) { lj -= a.F; lai++; }
+                while (lj < 0) { lj += a.F; lai--; }
+            }
+        };
+#pragma unroll
+        for (int i = 0; i < P; i++) load(i, warp + i * nw < n_units);
+        XReg<FMT> xr;
+        int cur_s = -1;
+        for (int k0 = 0; warp + k0 * nw < n_units; k0 += P) {
+#pragma unroll
+            for (int i = 0; i < P; i++) {
+                const int u = warp + (k0 + i) * nw;
+                if (u >= n_units) break;
+                if (wc.s != cur_s) {
+                    cur_s = wc.s;
+                    const int c = cur_s * 32 + lane;
+                    xr.load(stage, c);
+                }
+                float pg = xr.dot(qg[i]) * sg[i];
+                float pu = xr.dot(qu[i]) * su[i];
+                load(i, u + P * nw < n_units);
+                pg = warp_sum(pg);
+                pu = warp_sum(pu);
+                if (lane == 0) {
+                    redA[(cur_s * ppc + wc.rr) * 2] = pg;
+                    redA[(cur_s * ppc + wc.rr) * 2 + 1] = pu;
+                }
+                wc.step(nw, n_pr);
+            }
+        }
+        __syncthreads();
+        for (int rr = tid; rr < n_pr; rr += blockDim.x) {
+            float g = 0.f, u = 0.f;
+            for (int s = 0; s < n_slab_gu; s++) {
+                g += redA[(s * ppc + rr) * 2];
+                u += redA[(s * ppc + rr) * 2 + 1];
+            }
+            a.hbuf[pr0 + rr] = g / (1.0f + expf(-g)) * u;   // hbuf[a][j] = hbuf[pr]
+        }
+    }
+
+    if (!slab_grid_barrier(a.bar, a.err, a.timeout_ns)) return;
+
+    // ---- phase B: y[o] = sum_a w_a * D_a[o] h_a over this CTA's rows
+    const size_t xw_d = staged_words(FMT, a.cpr_d);
+    const int n_slab_d = (a.cpr_d + 31) >> 5;
+    const int rpc = a.rpc;
+    const int oc0 = blockIdx.x * rpc;
+    const int n_o = min(rpc, a.H - oc0);
+    if (n_o <= 0) return;
+    float *redB = reinterpret_cast<float *>(stage + (size_t)a.sb * xw_d);   // [sb][n_slab][rpc]
+    float *yacc = redB + (size_t)a.sb * n_slab_d * rpc;
+    for (int t = tid; t < n_o; t += blockDim.x) yacc[t] = 0.f;
+    for (int b0 = 0; b0 < nact; b0 += a.sb) {
+        const int nb = min(a.sb, nact - b0);
+        __syncthreads();
+        if (xw_d == (size_t)a.F) {   // contiguous unpadded rows of h: one staging pass
+            stage_vec<FMT>(reinterpret_cast<float *>(stage), a.hbuf + (size_t)b0 * a.F, nb * a.F, nb * (int)xw_d, tid,
+                           blockDim.x);
+        } else {
+            for (int bi = 0; bi < nb; bi++)
+                stage_x<FMT>(stage + (size_t)bi * xw_d, a.hbuf + (size_t)(b0 + bi) * a.F, a.F, a.cpr_d);
+        }
+        __syncthreads();
+        const int per_e = n_slab_d * n_o;
+        const int n_units = nb * per_e;
+        uint4 qb[2 * P];
+        float sb[2 * P];
+        // unit u -> (bi, s, rr) with u = (bi * n_slab_d + s) * n_o + rr; walker over (bs, rr)
+        Walk wl, wc;
+        wl.init(warp < n_units ? warp : 0, n_o);
+        wc = wl;
+        int lbi = wl.s / n_slab_d, lsl = wl.s - lbi * n_slab_d;   // (expert in batch, slab) of the prefetch walker
+        int cur_bi = -1;
+        MatDesc Dd = {};
+        auto load = [&](int i, bool ok) {
+            if (ok && lbi != cur_bi) {
+                cur_bi = lbi;
+                Dd = a.table[s_exp[b0 + lbi]].m[2];
+            }
+            const int o = oc0 + wl.rr;
+            const int c = lsl * 32 + lane;
+            const bool okc = ok && c < a.cpr_d;
+            qb[i] = ld_or_zero(Dd.q + (size_t)o * Dd.rs + (size_t)c * 16, okc);
+            sb[i] = unit_scale<FMT>(Dd, o, c, gshift_d, okc);
+            if (ok) {
+                const int s_before = wl.s;
+                wl.step(nw, n_o);
+                for (int k = s_before; k < wl.s; k++)
+                    if (++lsl == n_slab_d) { lsl = 0; lbi++; }
+            }
+        };
+#pragma unroll
+        for (int i = 0; i < 2 * P; i++) load(i, warp + i * nw < n_units);
+        XReg<FMT> xr;
+        int cur = -1;
+        for (int k0 = 0; warp + k0 * nw < n_units; k0 += 2 * P) {
+#pragma unroll
+            for (int i = 0; i < 2 * P; i++) {
+                const int u = warp + (k0 + i) * nw;
+                if (u >= n_units) break;
+                if (wc.s != cur) {
+                    cur = wc.s;
+                    const int bi = cur / n_slab_d, s = cur - bi * n_slab_d;
+                    xr.load(stage + (size_t)bi * xw_d, s * 32 + lane);
+                }
+                float p = xr.dot(qb[i]) * sb[i];
+                load(i, u + 2 * P * nw < n_units);
+                p = warp_sum(p);
+                if (lane == 0) redB[(size_t)cur * rpc + wc.rr] = p;
+                wc.step(nw, n_o);
+            }
+        }
+        __syncthreads();
+        for (int rr = tid; rr < n_o; rr += blockDim.x) {
+            float acc = yacc[rr];
+            for (int bi = 0; bi < nb; bi++) {
+                float d = 0.f;
+                for (int s = 0; s < n_slab_d; s++) d += redB[(size_t)(bi * n_slab_d + s) * rpc + rr];
+                acc = fmaf(s_ew[b0 + bi], d, acc);
+            }
+            yacc[rr] = acc;
+        }
+    }
+    __syncthreads();
+    for (int rr = tid; rr < n_o; rr += blockDim.x) a.y[oc0 + rr] = yacc[rr];
+}
+
+template <int FMT>
+cudaError_t slab_gemv_t(const GemvJob &job, int n_sm, int gshift, cudaStream_t st) {
+    const int total = job.row_start[job.n];
+    const int n_slab = (job.cpr + 31) / 32;
+    // CTAs: two per SM, each owning a contiguous block of rows
+    int grid = 2 * n_sm;
+    int rpc = (total + grid - 1) / grid;
+    grid = (total + rpc - 1) / rpc;
+    const size_t smem = (staged_words(FMT, job.cpr) + (size_t)n_slab * rpc) * sizeof(float);
+    auto kern = slab_gemv_kernel<FMT, 4>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kSlabThreads, smem, st>>>(job, rpc, gshift);
+    return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t slab_decode_t(const MoeDecodeArgs &a, int grid, size_t smem, int gs_gu, int gs_d, cudaStream_t st) {
+    auto kern = moe_decode_slab_kernel<FMT, 4>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kSlabThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, gs_gu, gs_d);
+}
+
+template <int FMT>
+cudaError_t slab_decode_occ_t(size_t smem, int *per_sm) {
+    auto kern = moe_decode_slab_kernel<FMT, 4>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, kSlabThreads, smem);
+}
+
+int log2_exact(int v) {
+    int k = 0;
+    while ((1 << k) < v) k++;
+    return (1 << k) == v ? k : -1;
+}
+
+}  // namespace
+
+// gs (fmt=4) usable by the slab kernels: a power-of-two number of 32-input chunks.
+bool slab_supported(int fmt, int gs) {
+    if (fmt == 3) return false;
+    if (fmt == 4) return gs % 32 == 0 && log2_exact(gs / 32) >= 0;
+    return true;
+}
+
+size_t slab_gemv_smem(const GemvJob &job, int n_sm) {
+    const int total = job.row_start[job.n];
+    int grid = 2 * n_sm;
+    const int rpc = (total + grid - 1) / grid;
+    return (staged_words(job.fmt, job.cpr) + (size_t)((job.cpr + 31) / 32) * rpc) * sizeof(float);
+}
+
+cudaError_t launch_slab_gemv(const GemvJob &job, int n_sm, cudaStream_t st) {
+    const int gshift = job.fmt == 4 ? log2_exact(job.gs[0] / 32) : 0;
+    switch (job.fmt) {
+    case 0: return slab_gemv_t<0>(job, n_sm, gshift, st);
+    case 1: return slab_gemv_t<1>(job, n_sm, gshift, st);
+    case 2: return slab_gemv_t<2>(job, n_sm, gshift, st);
+    case 4: return slab_gemv_t<4>(job, n_sm, gshift, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// Shared memory of the slab decode kernel for `sb` experts per phase-B batch.
+size_t slab_decode_smem(int fmt, int cpr_gu, int cpr_d, int F, int n_slots, int grid_min, int H, int sb) {
+    const size_t xlen_gu = staged_words(fmt, cpr_gu), xlen_d = staged_words(fmt, cpr_d);
+    const int n_slab_gu = (cpr_gu + 31) / 32, n_slab_d = (cpr_d + 31) / 32;
+    const long long pairs_max = (long long)n_slots * F;
+    const size_t ppc = (size_t)((pairs_max + grid_min - 1) / grid_min);
+    const size_t rpc = (size_t)((H + grid_min - 1) / grid_min);
+    const size_t a_part = xlen_gu + (size_t)n_slab_gu * ppc * 2;
+    const size_t b_part = (size_t)sb * xlen_d + (size_t)sb * n_slab_d * rpc + rpc;
+    return (a_part > b_part ? a_part : b_part) * sizeof(float);
+}
+
+cudaError_t slab_decode_occupancy(int fmt, size_t smem, int *per_sm) {
+    switch (fmt) {
+    case 0: return slab_decode_occ_t<0>(smem, per_sm);
+    case 1: return slab_decode_occ_t<1>(smem, per_sm);
+    case 2: return slab_decode_occ_t<2>(smem, per_sm);
+    case 4: return slab_decode_occ_t<4>(smem, per_sm);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_slab_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t smem, int gs_gu, int gs_d,
+                               cudaStream_t st) {
+    const int sh_gu = fmt == 4 ? log2_exact(gs_gu / 32) : 0, sh_d = fmt == 4 ? log2_exact(gs_d / 32) : 0;
+    switch (fmt) {
+    case 0: return slab_decode_t<0>(a, grid, smem, sh_gu, sh_d, st);
+    case 1: return slab_decode_t<1>(a, grid, smem, sh_gu, sh_d, st);
+    case 2: return slab_decode_t<2>(a, grid, smem, sh_gu, sh_d, st);
+    case 4: return slab_decode_t<4>(a, grid, smem, sh_gu, sh_d, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace coli
