@@ -245,10 +245,12 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
         g_launches++;
     }
     if (e == cudaSuccess && (fmt == 2 || fmt == 4)) {
+        // without a map (a shape the TMA descriptor rejects) the tensor-core path is not used for this tensor
         alignas(64) unsigned char map[128];
-        e = encode_codes_map(t->q, t->rs, O, map);
-        if (e == cudaSuccess) e = cudaMalloc(&t->tmap, 128);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(t->tmap, map, 128, cudaMemcpyHostToDevice, st);
+        if (encode_codes_map(t->q, t->rs, O, map) == cudaSuccess) {
+            e = cudaMalloc(&t->tmap, 128);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(t->tmap, map, 128, cudaMemcpyHostToDevice, st);
+        }
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {

@@ -14,13 +14,20 @@
 // found every mid/lo zero (bf16-representable activations) only the first
 // plane is loaded and multiplied.
 //
-// Warp roles (352 threads, persistent over a static tile schedule):
-//   warps 0-3  dequant: codes (smem) -> bf16 A tile, SW128 K-major layout
-//   warps 4-7  epilogue: TMEM -> registers, group scale, final row scale, store
-//   warp  8    TMA producer of the codes: box [128 rows x 32 B], 24 stages deep
-//   warp  9    MMA issuer (one thread), tcgen05.mma kind::f16, M=128, N<=64
-//   warp 10    TMA producer of the activation planes: 16-row boxes, only as
-//              many as the tile's rows need
+// Warp roles (480 threads, persistent over a static tile schedule):
+//   warps 0-7   dequant: codes (smem) -> bf16 A tile, SW128 K-major layout;
+//               two threads per weight row, each half a K-block
+//   warps 8-11  epilogue: TMEM -> registers, group scale, row scale, store
+//   warp  12    TMA producer of the codes: box [128 rows x 128 B] = 4 K-blocks
+//   warp  13    MMA issuer (one thread), tcgen05.mma kind::f16, M=128
+//   warp  14    TMA producer of the activation planes: 16-row boxes, only as
+//               many as the tile's rows need; a plane stage holds 64 rows per
+//               plane, so a tile of <= 16 rows takes 4 K-blocks per stage
+// With three planes they are stacked along N (N = 3 x the tile's padded rows)
+// so a K-step is one MMA whatever the plane count; the epilogue adds the three
+// column blocks.  A tcgen05.mma with N <= 64 costs the same issue time as one
+// with N = 64, so the issuing thread's loop is kept to the MMAs, the waits and
+// the commits (descriptors advance by adding offsets, ring indices by wrap).
 // The codes ring is released by the dequant warps as soon as they have read a
 // stage, so its depth alone sets the bytes in flight from HBM; the plane ring
 // (activations, mostly L2 hits) is released by the MMA commits.
@@ -37,25 +44,32 @@ namespace coli {
 namespace {
 
 constexpr int BM = 128, BK = 64, BN = 64;
-constexpr int NC = 24;                              // codes stages (4 KB each): the HBM stream
-constexpr int B_RING = 72 * 1024;                   // activation-plane ring: 9 stages of 1 plane, 3 of 3
-constexpr int NBMAX = 9;
-constexpr int NA = 2;                               // dequantized A stages
-constexpr int NPL = 3;                              // activation planes
-constexpr int CODES_BYTES = BM * BK / 2;            // 4096
-constexpr int PLANE_BYTES = BN * BK * 2;            // 8192 (64 rows x 128 B)
-constexpr int BOX_ROWS = 16;                        // activation rows per TMA box
-constexpr int BOX_BYTES = BOX_ROWS * BK * 2;        // 2048
-constexpr int A_BYTES = BM * BK * 2;                // 16384
+constexpr int KB_PER_CS = 4;                          // K-blocks per codes stage: 128-byte row segments
+constexpr int NC = 4;                                 // codes stages (16 KB each): the HBM stream
+constexpr int NA = 3;                                 // dequantized A stages (16 KB each)
+constexpr int NPL = 3;                                // activation planes
+constexpr int CODES_BYTES = BM * BK / 2 * KB_PER_CS;  // 16384: 128 rows x 128 B, 128-byte swizzle
+constexpr int A_BYTES = BM * BK * 2;                  // 16384
+constexpr int BOX_ROWS = 16;                          // activation rows per TMA box
+constexpr int BOX_BYTES = BOX_ROWS * BK * 2;          // 2048
+constexpr int PLANE_BYTES = BN * BK * 2;              // 8192: 64 rows x 128 B
+constexpr int B_RING = 4 * NPL * PLANE_BYTES;         // 96 KB
+constexpr int NB1 = B_RING / PLANE_BYTES;             // plane stages with one plane: 12
+constexpr int NB3 = B_RING / (NPL * PLANE_BYTES);     // with three planes: 4
+constexpr int NBMAX = NB1;
+constexpr int NACCMAX = 8;
 constexpr int OFF_B = 0;
 constexpr int OFF_A = OFF_B + B_RING;
 constexpr int OFF_CODES = OFF_A + NA * A_BYTES;
 constexpr int OFF_BAR = OFF_CODES + NC * CODES_BYTES;
-constexpr int NACC = 4;                             // TMEM accumulator buffers (64 columns each)
-constexpr int N_BAR = 2 * NC + 2 * NBMAX + 2 * NA + 2 * NACC + 1;
+constexpr int N_BAR = 2 * NC + 2 * NBMAX + 2 * NA + 2 * NACCMAX + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;   // + alignment slack
-constexpr int kTcThreads = 352;
-constexpr uint32_t TMEM_COLS = 256;                 // NACC accumulator buffers x 64 columns
+constexpr int kDqWarps = 8;                           // dequant warps: two per weight row (half a K-block each)
+constexpr int kEpWarps = 4;                           // epilogue warps 8-11, one per TMEM lane quarter
+constexpr int kCodesWarp = 12, kMmaWarp = 13, kPlanesWarp = 14;
+constexpr int kTcThreads = 15 * 32;                   // <= 4 warps per SM sub-partition: 128 registers each
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -122,6 +136,12 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
 }
+// 8 consecutive TMEM columns of this thread's lane; complete after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+}
 // 16 consecutive TMEM columns of this thread's lane; complete after tmem_wait_ld().
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile(
@@ -164,56 +184,40 @@ __device__ __forceinline__ const MatDesc &mat_of(const TcArgs &a, const Tile &t)
     return a.table ? a.table[t.e].m[t.mi] : a.single;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
-    uint64_t *c_full = bars, *c_empty = bars + NC;
-    uint64_t *b_full = bars + 2 * NC, *b_empty = b_full + NBMAX;
-    uint64_t *a_full = b_empty + NBMAX, *a_empty = a_full + NA;
-    uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + NACC;
-    uint64_t *done = acc_empty + NACC;
-    uint32_t *tmem_slot = (uint32_t *)(bars + N_BAR);
-    __shared__ volatile int abort_flag;
+// Bounded wait taken by a whole warp: every lane polls, lane 0 decides on
+// expiry, so the warp leaves together either way.
+__device__ __forceinline__ bool warp_wait(uint64_t *b, uint32_t parity, uint64_t deadline, volatile int *abort,
+                                          int lane) {
+    while (true) {
+        const bool done = mbar_try(b, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        int stop = 0;
+        if (lane == 0) stop = (*abort != 0) || global_ns() > deadline;
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
 
+struct Bars {
+    uint64_t *c_full, *c_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty, *done;
+};
+
+// Token rows per tile rounded to the MMA's N granule, and how many K-blocks
+// of activations share one plane stage (a stage holds 64 rows per plane).
+__device__ __forceinline__ int npad_of(const Tile &t) { return ((t.p1 - t.p0) + 15) & ~15; }
+__device__ __forceinline__ int kps_of(int npad) { return npad <= 16 ? 4 : (npad <= 32 ? 2 : 1); }
+
+// The warp roles for NT activation planes.  With NT = 3 the planes are
+// stacked along N: one MMA of N = 3 * npad multiplies all three, and the
+// epilogue adds the three column blocks.
+template <int NT>
+__device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &a, uint8_t *smem, const Bars &B,
+                                          uint32_t tmem, volatile int &abort_flag, uint64_t deadline) {
+    constexpr int NB = NT == 1 ? NB1 : NB3;
+    constexpr int NACC = NT == 1 ? 8 : 2;             // TMEM accumulators of NT * 64 columns
+    constexpr int B_STAGE = NT * PLANE_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = a.tile_e ? *a.n_tiles : (a.P + BN - 1) / BN;
     const int total = n_tiles * a.n_mblk;
-    const int nt = (*a.nterm_flag) ? NPL : 1;
-    const int NB = B_RING / (nt * PLANE_BYTES);      // plane stages: 9 (one plane) or 3 (three)
-    const int b_stage = nt * PLANE_BYTES;
-    const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
-
-    if (tid == 0) {
-        abort_flag = 0;
-        for (int i = 0; i < NC; i++) {
-            mbar_init(&c_full[i], 1);
-            mbar_init(&c_empty[i], 128);
-        }
-        for (int i = 0; i < NBMAX; i++) {
-            mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1);
-        }
-        for (int i = 0; i < NA; i++) {
-            mbar_init(&a_full[i], 128);
-            mbar_init(&a_empty[i], 1);
-        }
-        for (int i = 0; i < NACC; i++) {
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 128);
-        }
-        mbar_init(done, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 9) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(TMEM_COLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     auto fail = [&]() {
         if (!abort_flag) {
@@ -222,156 +226,202 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         }
     };
 
-    if (warp == 8) {
-        // ---------------- TMA producer: codes
+    if (warp == kCodesWarp) {
+        // ---------------- TMA producer: codes, 4 K-blocks (128 B of each of 128 rows) per stage
         if (lane == 0) {
-            int it = 0;
-            for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
+            int it = 0, s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok && !abort_flag; L += gridDim.x) {
                 const Tile t = tile_of(a, L, n_tiles);
                 const MatDesc &M = mat_of(a, t);
-                for (int kb = 0; kb < a.nkb; kb++, it++) {
-                    const int s = it % NC;
-                    if (it >= NC && !mbar_wait(&c_empty[s], ((it / NC) & 1) ^ 1, deadline, &abort_flag)) {
-                        fail();
-                        break;
-                    }
-                    mbar_expect_tx(&c_full[s], CODES_BYTES);
-                    tma_load_2d(smem + OFF_CODES + s * CODES_BYTES, (const CUtensorMap *)M.tmap, kb * (BK / 2),
-                                t.mb * BM, &c_full[s]);
-                }
-            }
-            // every copy this thread issued has landed before the CTA may exit
-            const uint64_t dl2 = global_ns() + 200000000ull;
-            volatile int no_abort = 0;
-            for (int k = max(0, it - NC); k < it; k++) mbar_wait(&c_full[k % NC], (k / NC) & 1, dl2, &no_abort);
-        }
-    } else if (warp == 10) {
-        // ---------------- TMA producer: activation planes, 16-row boxes
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmx) : "memory");
-            int it = 0;
-            for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
-                const Tile t = tile_of(a, L, n_tiles);
-                const int nbox = (t.p1 - t.p0 + BOX_ROWS - 1) / BOX_ROWS;
-                for (int kb = 0; kb < a.nkb; kb++, it++) {
-                    const int s = it % NB;
-                    if (it >= NB && !mbar_wait(&b_empty[s], ((it / NB) & 1) ^ 1, deadline, &abort_flag)) {
-                        fail();
-                        break;
-                    }
-                    mbar_expect_tx(&b_full[s], nt * nbox * BOX_BYTES);
-                    for (int pl = 0; pl < nt; pl++)
-                        for (int bx = 0; bx < nbox; bx++)
-                            tma_load_2d(smem + OFF_B + s * b_stage + pl * PLANE_BYTES + bx * BOX_BYTES, &tmx,
-                                        kb * BK, pl * a.rows_alloc + t.p0 + bx * BOX_ROWS, &b_full[s]);
-                }
-            }
-            const uint64_t dl2 = global_ns() + 200000000ull;
-            volatile int no_abort = 0;
-            for (int k = max(0, it - NB); k < it; k++) mbar_wait(&b_full[k % NB], (k / NB) & 1, dl2, &no_abort);
-        }
-    } else if (warp == 9) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            int it = 0, g = 0;
-            for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
-                const Tile t = tile_of(a, L, n_tiles);
-                const int N = ((t.p1 - t.p0) + 15) & ~15;
-                const uint32_t idesc = idesc_bf16(BM, N);
-                bool ok = true;
-                for (int kb = 0; kb < a.nkb && ok; kb++, it++) {
-                    const bool first = (kb % a.gkb) == 0;
-                    const bool last = ((kb % a.gkb) == a.gkb - 1) || kb == a.nkb - 1;
-                    const int b = g % NACC;
-                    const int as = it % NA, bs = it % NB;
-                    if (first && g >= NACC &&
-                        !mbar_wait(&acc_empty[b], ((g / NACC) & 1) ^ 1, deadline, &abort_flag)) {
+                const int ncs = (a.nkb + KB_PER_CS - 1) / KB_PER_CS;
+                for (int kc = 0; kc < ncs; kc++) {
+                    if (it >= NC && !mbar_wait(&B.c_empty[s], ph ^ 1, deadline, &abort_flag)) {
                         ok = false;
                         break;
                     }
-                    if (!mbar_wait(&a_full[as], (it / NA) & 1, deadline, &abort_flag) ||
-                        !mbar_wait(&b_full[bs], (it / NB) & 1, deadline, &abort_flag)) {
+                    mbar_expect_tx(&B.c_full[s], CODES_BYTES);
+                    tma_load_2d(smem + OFF_CODES + s * CODES_BYTES, (const CUtensorMap *)M.tmap,
+                                kc * KB_PER_CS * (BK / 2), t.mb * BM, &B.c_full[s]);
+                    it++;
+                    if (++s == NC) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) fail();
+            // every copy this thread issued has landed before the CTA may exit
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int k = max(0, it - NC); k < it; k++) mbar_wait(&B.c_full[k % NC], (k / NC) & 1, dl2, &no_abort);
+        }
+    } else if (warp == kPlanesWarp) {
+        // ---------------- TMA producer: activation planes, 16-row boxes, kps K-blocks per stage
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmx) : "memory");
+            int it = 0, s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok && !abort_flag; L += gridDim.x) {
+                const Tile t = tile_of(a, L, n_tiles);
+                const int npad = npad_of(t), nbox = npad / BOX_ROWS, kps = kps_of(npad);
+                for (int kb0 = 0; kb0 < a.nkb; kb0 += kps) {
+                    const int nk = min(kps, a.nkb - kb0);
+                    if (it >= NB && !mbar_wait(&B.b_empty[s], ph ^ 1, deadline, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&B.b_full[s], nk * NT * nbox * BOX_BYTES);
+                    uint8_t *dst = smem + OFF_B + s * B_STAGE;
+                    for (int kk = 0; kk < nk; kk++)
+                        for (int pl = 0; pl < NT; pl++)
+                            for (int bx = 0; bx < nbox; bx++)
+                                tma_load_2d(dst + ((kk * NT + pl) * npad + bx * BOX_ROWS) * (BK * 2), &tmx,
+                                            (kb0 + kk) * BK, pl * a.rows_alloc + t.p0 + bx * BOX_ROWS, &B.b_full[s]);
+                    it++;
+                    if (++s == NB) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) fail();
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int k = max(0, it - NB); k < it; k++) mbar_wait(&B.b_full[k % NB], (k / NB) & 1, dl2, &no_abort);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issuer (one thread)
+        if (lane == 0) {
+            int ai = 0, as = 0, bs = 0, gb = 0, g = 0;
+            uint32_t aph = 0, bph = 0, gph = 0;
+            const uint64_t ad0 = sdesc_sw128(smem_addr(smem + OFF_A));
+            const uint64_t bd0 = sdesc_sw128(smem_addr(smem + OFF_B));
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok && !abort_flag; L += gridDim.x) {
+                const Tile t = tile_of(a, L, n_tiles);
+                const int npad = npad_of(t), kps = kps_of(npad);
+                const uint32_t idesc = idesc_bf16(BM, NT * npad);
+                const uint32_t kstep = (uint32_t)(NT * npad * BK * 2) >> 4;   // one K-block inside a plane stage
+                int kk = 0, kg = 0;
+                for (int kb = 0; kb < a.nkb; kb++) {
+                    const bool first = kg == 0;
+                    if (first && g >= NACC && !mbar_wait(&B.acc_empty[gb], gph ^ 1, deadline, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&B.a_full[as], aph, deadline, &abort_flag) ||
+                        (kk == 0 && !mbar_wait(&B.b_full[bs], bph, deadline, &abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_addr(smem + OFF_A + as * A_BYTES);
+                    const uint64_t ad = ad0 + (uint64_t)(as * (A_BYTES >> 4));
+                    const uint64_t bd = bd0 + (uint64_t)(bs * (B_STAGE >> 4) + kk * kstep);
+                    const uint32_t d = tmem + (uint32_t)(gb * NT * BN);
 #pragma unroll
-                    for (int j = 0; j < BK / 16; j++) {
-                        for (int pl = 0; pl < nt; pl++) {
-                            const uint32_t b_base = smem_addr(smem + OFF_B + bs * b_stage + pl * PLANE_BYTES);
-                            mma_bf16(tmem + b * BN, sdesc_sw128(a_base + j * 32), sdesc_sw128(b_base + j * 32), idesc,
-                                     (first && j == 0 && pl == 0) ? 0u : 1u);
+                    for (int j = 0; j < BK / 16; j++)
+                        mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
+                    mma_commit(&B.a_empty[as]);
+                    ai++;
+                    if (++as == NA) {
+                        as = 0;
+                        aph ^= 1;
+                    }
+                    if (++kk == kps || kb == a.nkb - 1) {
+                        mma_commit(&B.b_empty[bs]);
+                        kk = 0;
+                        if (++bs == NB) {
+                            bs = 0;
+                            bph ^= 1;
                         }
                     }
-                    mma_commit(&a_empty[as]);
-                    mma_commit(&b_empty[bs]);
-                    if (last) {
-                        mma_commit(&acc_full[b]);
+                    if (++kg == a.gkb || kb == a.nkb - 1) {
+                        mma_commit(&B.acc_full[gb]);
+                        kg = 0;
                         g++;
+                        if (++gb == NACC) {
+                            gb = 0;
+                            gph ^= 1;
+                        }
                     }
                 }
-                if (!ok) {
-                    fail();
-                    break;
-                }
             }
-            mma_commit(done);
+            if (!ok) fail();
+            mma_commit(B.done);
             volatile int no_abort = 0;
-            mbar_wait(done, 0, global_ns() + 200000000ull, &no_abort);
+            mbar_wait(B.done, 0, global_ns() + 200000000ull, &no_abort);
         }
-    } else if (warp < 4) {
-        // ---------------- dequant: thread r owns weight row r of the tile
-        const int r = tid;
-        int it = 0;
-        for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
-            bool ok = true;
-            for (int kb = 0; kb < a.nkb; kb++, it++) {
-                const int s = it % NC, as = it % NA;
-                if (!mbar_wait(&c_full[s], (it / NC) & 1, deadline, &abort_flag)) {
+    } else if (warp < kDqWarps) {
+        // ---------------- dequant: thread (h, r) writes half h of weight row r of each K-block
+        const int r = tid & (BM - 1), h = tid >> 7;
+        int cs = 0, as = 0, it = 0;
+        uint32_t cph = 0, aph = 0;
+        bool ok = true;
+        const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+        for (int L = blockIdx.x; L < total && ok && !__shfl_sync(0xffffffffu, (int)abort_flag, 0); L += gridDim.x) {
+            for (int kb = 0; kb < a.nkb; kb++) {
+                const int sub = kb & (KB_PER_CS - 1);
+                if (sub == 0 && !warp_wait(&B.c_full[cs], cph, deadline, &abort_flag, lane)) {
                     ok = false;
                     break;
                 }
-                const uint4 *crow = (const uint4 *)(smem + OFF_CODES + s * CODES_BYTES + r * 32);
-                const uint4 c0 = crow[0], c1 = crow[1];
-                mbar_arrive(&c_empty[s]);
-                if (it >= NA && !mbar_wait(&a_empty[as], ((it / NA) & 1) ^ 1, deadline, &abort_flag)) {
+                // row r of the stage is 128 B in 16-byte chunks swizzled by (r & 7)
+                const uint4 c = *reinterpret_cast<const uint4 *>(smem + OFF_CODES + cs * CODES_BYTES + r * 128 +
+                                                                 (((2 * sub + h) ^ (r & 7)) << 4));
+                if (sub == KB_PER_CS - 1 || kb == a.nkb - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&B.c_empty[cs]);
+                    if (++cs == NC) {
+                        cs = 0;
+                        cph ^= 1;
+                    }
+                }
+                if (it >= NA && !warp_wait(&B.a_empty[as], aph ^ 1, deadline, &abort_flag, lane)) {
                     ok = false;
                     break;
                 }
-                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const uint32_t w[4] = {c.x, c.y, c.z, c.w};
                 uint8_t *arow = smem + OFF_A + as * A_BYTES + r * 128;
-                const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
-                for (int c = 0; c < 8; c++) {
+                for (int cc = 0; cc < 4; cc++) {
                     uint32_t q[4];
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
-                        uint32_t v = ((w[c] >> (4 * k)) & 0x000F000Fu) | 0x43004300u;
-                        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&v);
-                        h = __hsub2(h, off);
-                        q[k] = *reinterpret_cast<uint32_t *>(&h);
+                        uint32_t v = ((w[cc] >> (4 * k)) & 0x000F000Fu) | 0x43004300u;
+                        __nv_bfloat162 hv = *reinterpret_cast<__nv_bfloat162 *>(&v);
+                        hv = __hsub2(hv, off);
+                        q[k] = *reinterpret_cast<uint32_t *>(&hv);
                     }
-                    *reinterpret_cast<uint4 *>(arow + ((c ^ (r & 7)) << 4)) = make_uint4(q[0], q[1], q[2], q[3]);
+                    *reinterpret_cast<uint4 *>(arow + (((4 * h + cc) ^ (r & 7)) << 4)) =
+                        make_uint4(q[0], q[1], q[2], q[3]);
                 }
                 fence_async_smem();
-                mbar_arrive(&a_full[as]);
-            }
-            if (!ok) {
-                fail();
-                break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.a_full[as]);
+                it++;
+                if (++as == NA) {
+                    as = 0;
+                    aph ^= 1;
+                }
             }
         }
-    } else if (warp < 8) {
-        // ---------------- epilogue: warp 4+q reads TMEM lanes 32q..32q+31
-        const int q = warp - 4;
+        if (!ok) fail();
+    } else if (warp < kDqWarps + kEpWarps) {
+        // ---------------- epilogue: warp 8+q reads TMEM lanes 32q..32q+31
+        const int q = warp & 3;
         const int m = q * 32 + lane;
-        int g = 0;
-        for (int L = blockIdx.x; L < total && !abort_flag; L += gridDim.x) {
+        int gb = 0;
+        uint32_t gph = 0;
+        bool ok = true;
+        for (int L = blockIdx.x; L < total && ok && !__shfl_sync(0xffffffffu, (int)abort_flag, 0); L += gridDim.x) {
             const Tile t = tile_of(a, L, n_tiles);
             const MatDesc &M = mat_of(a, t);
             const int n_tok = t.p1 - t.p0;
-            const int nch = (n_tok + 15) >> 4;
+            const int npad = npad_of(t);
+            const int nch = npad >> 4;
             const int o = t.mb * BM + m;
             const bool row_ok = o < a.O;
             float acc[BN];
@@ -385,7 +435,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             float scq[SD];
 #pragma unroll
             for (int i = 0; i < SD; i++) scq[i] = (grouped && i < ngrp) ? __ldg(srow + i) : 1.0f;
-            bool ok = true;
             for (int grp0 = 0; grp0 < ngrp && ok; grp0 += SD) {
 #pragma unroll
                 for (int i = 0; i < SD; i++) {
@@ -393,34 +442,59 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                     if (grp >= ngrp) break;
                     const float sc = scq[i];
                     scq[i] = (grouped && grp + SD < ngrp) ? __ldg(srow + grp + SD) : 1.0f;
-                    const int b = g % NACC;
-                    if (!mbar_wait(&acc_full[b], (g / NACC) & 1, deadline, &abort_flag)) {
+                    if (!warp_wait(&B.acc_full[gb], gph, deadline, &abort_flag, lane)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t v[BN / 16][16];
+                    const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(gb * NT * BN);
+                    if (NT == 1) {
+                        // two batches of 32 columns
 #pragma unroll
-                    for (int c = 0; c < BN / 16; c++)
-                        if (c < nch) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + b * BN + c * 16, v[c]);
-                    tmem_wait_ld();
+                        for (int hb = 0; hb < 2; hb++) {
+                            if (2 * hb >= nch) break;
+                            uint32_t v[2][16];
 #pragma unroll
-                    for (int c = 0; c < BN / 16; c++) {
-                        if (c < nch) {
+                            for (int c = 0; c < 2; c++)
+                                if (2 * hb + c < nch) tmem_ld16(base + (2 * hb + c) * 16, v[c]);
+                            tmem_wait_ld();
 #pragma unroll
-                            for (int k = 0; k < 16; k++)
-                                acc[c * 16 + k] = fmaf(sc, __uint_as_float(v[c][k]), acc[c * 16 + k]);
+                            for (int c = 0; c < 2; c++)
+                                if (2 * hb + c < nch) {
+#pragma unroll
+                                    for (int k = 0; k < 16; k++)
+                                        acc[(2 * hb + c) * 16 + k] =
+                                            fmaf(sc, __uint_as_float(v[c][k]), acc[(2 * hb + c) * 16 + k]);
+                                }
+                        }
+                    } else {
+                        // 8 columns of each plane at a time
+#pragma unroll
+                        for (int c8 = 0; c8 < BN / 8; c8++) {
+                            if (c8 >= 2 * nch) break;
+                            uint32_t v[NT][8];
+#pragma unroll
+                            for (int pl = 0; pl < NT; pl++) tmem_ld8(base + pl * npad + c8 * 8, v[pl]);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 8; k++) {
+                                float sum = __uint_as_float(v[NT - 1][k]);
+#pragma unroll
+                                for (int pl = NT - 2; pl >= 0; pl--) sum += __uint_as_float(v[pl][k]);
+                                acc[c8 * 8 + k] = fmaf(sc, sum, acc[c8 * 8 + k]);
+                            }
                         }
                     }
                     tc_fence_before();
-                    mbar_arrive(&acc_empty[b]);
-                    g++;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&B.acc_empty[gb]);
+                    if (++gb == NACC) {
+                        gb = 0;
+                        gph ^= 1;
+                    }
                 }
             }
-            if (!ok) {
-                fail();
-                break;
-            }
+            if (!ok) break;
             if (row_ok) {
                 const float rs = (a.fmt == 4) ? 1.0f : __ldg(M.s + o);
                 float *dst = a.out + (size_t)t.p0 * a.ldo + t.col0 + o;
@@ -429,11 +503,70 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                     if (n < n_tok) dst[(size_t)n * a.ldo] = acc[n] * rs;
             }
         }
+        if (!ok) fail();
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
+    Bars B;
+    B.c_full = bars;
+    B.c_empty = B.c_full + NC;
+    B.b_full = B.c_empty + NC;
+    B.b_empty = B.b_full + NBMAX;
+    B.a_full = B.b_empty + NBMAX;
+    B.a_empty = B.a_full + NA;
+    B.acc_full = B.a_empty + NA;
+    B.acc_empty = B.acc_full + NACCMAX;
+    B.done = B.acc_empty + NACCMAX;
+    uint32_t *tmem_slot = (uint32_t *)(bars + N_BAR);
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < NC; i++) {
+            mbar_init(&B.c_full[i], 1);
+            mbar_init(&B.c_empty[i], kDqWarps);
+        }
+        for (int i = 0; i < NBMAX; i++) {
+            mbar_init(&B.b_full[i], 1);
+            mbar_init(&B.b_empty[i], 1);
+        }
+        for (int i = 0; i < NA; i++) {
+            mbar_init(&B.a_full[i], kDqWarps);
+            mbar_init(&B.a_empty[i], 1);
+        }
+        for (int i = 0; i < NACCMAX; i++) {
+            mbar_init(&B.acc_full[i], 1);
+            mbar_init(&B.acc_empty[i], kEpWarps);
+        }
+        mbar_init(B.done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) {
+    const uint32_t tmem = *tmem_slot;
+
+    if (*a.nterm_flag)
+        run_roles<NPL>(tmx, a, smem, B, tmem, abort_flag, deadline);
+    else
+        run_roles<1>(tmx, a, smem, B, tmem, abort_flag, deadline);
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
     }
@@ -530,10 +663,10 @@ cudaError_t encode_codes_map(const uint8_t *q, long long rs, long long O, void *
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)rs, (cuuint64_t)O};
     cuuint64_t strides[1] = {(cuuint64_t)rs};
-    cuuint32_t box[2] = {BK / 2, BM};
+    cuuint32_t box[2] = {BK / 2 * KB_PER_CS, BM};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void *)q, dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
