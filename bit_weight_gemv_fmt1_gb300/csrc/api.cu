@@ -341,8 +341,8 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
             cudaError_t e = launch_gather_planes(x, I, nullptr, 1, nullptr, S, I, I_pad, pl, (long long)rows_alloc * I_pad,
                                                  flag, st);
             if (e != cudaSuccess) return cuda_fail(e, "activation planes launch");
-            alignas(64) unsigned char map[128];
-            e = encode_planes_map(pl, I_pad, 3LL * rows_alloc, map);
+            PlaneMapSet map;
+            e = encode_plane_maps(pl, I_pad, rows_alloc, &map);
             if (e != cudaSuccess) return cuda_fail(e, "activation tensor map");
             TcArgs a;
             memset(&a, 0, sizeof a);
@@ -536,6 +536,64 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         for (int e = 0; e < n_experts && gs_ok; e++)
             gs_ok = experts[e].gate->gs % 32 == 0 && experts[e].up->gs % 32 == 0 && experts[e].down->gs % 32 == 0;
 
+    // ---------------- decode, S = 1, int4 groups: weights streamed by bulk copies, one cooperative launch
+    if (S == 1 && fmt == 4 && n_slots <= kMaxDecodeSlots) {
+        const coli_tensor *d0 = experts[0].down;
+        const int gs_gu = g0->gs, gs_d = d0->gs;
+        bool ok = gs_gu % 32 == 0 && gs_d % 32 == 0 && slab_supported(4, gs_gu) && slab_supported(4, gs_d) &&
+                  g0->ng % 4 == 0 && d0->ng % 4 == 0;
+        for (int e = 0; e < n_experts && ok; e++)
+            ok = experts[e].gate->gs == gs_gu && experts[e].up->gs == gs_gu && experts[e].down->gs == gs_d;
+        const int nsA = (cpr_gu + 31) / 32, nsB = (cpr_d + 31) / 32;
+        ok = ok && kStreamConsumerWarps % nsA == 0 && kStreamConsumerWarps % nsB == 0;
+        const int rs_gu = (int)g0->rs, rs_d = (int)d0->rs;
+        // each consumer warp takes at most 2 pairs (phase A) or 4 rows (phase B) of a stage
+        const int RP = std::min(kStreamStageBytes / (2 * (rs_gu + 4 * g0->ng)), 2 * (kStreamConsumerWarps / nsA));
+        const int RB = std::min(kStreamStageBytes / (rs_d + 4 * d0->ng), 4 * (kStreamConsumerWarps / nsB));
+        const int grid = ds->n_sm;
+        const long long ppc = ((long long)K * F + grid - 1) / grid, rpc = (H + grid - 1) / grid;
+        ok = ok && RP >= 1 && RB >= 1 && (long long)staged_len(4, cpr_gu) * 4 <= kStreamXhBytes &&
+             (long long)K * staged_len(4, cpr_d) * 4 <= kStreamXhBytes &&
+             ppc * nsA * 2 * 4 <= kStreamRedBytes && (long long)K * rpc * nsB * 4 <= kStreamRedBytes &&
+             stream_decode_smem() <= (size_t)ds->smem_optin;
+        int per_sm = 0;
+        if (ok && stream_decode_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) {
+            Workspace *ws = nullptr;
+            if (int rc = workspace(ds, st, (size_t)n_slots * F * sizeof(float), &ws)) return rc;
+            StreamArgs a;
+            memset(&a, 0, sizeof a);
+            a.m.x = x;
+            a.m.ids = ids;
+            a.m.w = w;
+            a.m.y = y;
+            a.m.table = table;
+            a.m.n_experts = n_experts;
+            a.m.S = 1;
+            a.m.K = K;
+            a.m.H = (int)H;
+            a.m.F = (int)F;
+            a.m.cpr_gu = cpr_gu;
+            a.m.cpr_d = cpr_d;
+            a.m.hbuf = (float *)ws->buf;
+            a.m.bar = ws->bar;
+            a.m.err = ds->err;
+            a.m.timeout_ns = 2000000000LL;
+            a.rs_gu = rs_gu;
+            a.rs_d = rs_d;
+            a.ng_gu = g0->ng;
+            a.ng_d = d0->ng;
+            a.gshift_gu = __builtin_ctz(gs_gu / 32);
+            a.gshift_d = __builtin_ctz(gs_d / 32);
+            a.RP = RP;
+            a.RB = RB;
+            a.red_floats = kStreamRedBytes / 4;
+            cudaError_t e = launch_stream_decode(a, grid, st);
+            if (e != cudaSuccess) return cuda_fail(e, "decode expert-block launch");
+            count(1, 0);
+            return COLI_OK;
+        }
+    }
+
     // ---------------- decode, S = 1: activation slab in registers, one cooperative launch
     bool slab_ok = S == 1 && n_slots <= kMaxDecodeSlots && fmt != 3 && F % 32 == 0;
     for (int e = 0; e < n_experts && slab_ok; e++)
@@ -679,8 +737,8 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         e = launch_gather_planes(x, H, order, K, offsets + n_experts, n_slots, (int)H, H_pad, px,
                                  (long long)rows_alloc * H_pad, &flags[0], st);
         if (e != cudaSuccess) return cuda_fail(e, "activation planes launch");
-        alignas(64) unsigned char mapx[128], maph[128];
-        e = encode_planes_map(px, H_pad, 3LL * rows_alloc, mapx);
+        PlaneMapSet mapx, maph;
+        e = encode_plane_maps(px, H_pad, rows_alloc, &mapx);
         if (e != cudaSuccess) return cuda_fail(e, "activation tensor map");
         TcArgs a;
         memset(&a, 0, sizeof a);
@@ -705,7 +763,7 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         e = launch_silu_planes(gu, (int)F, offsets + n_experts, n_slots, F_pad, ph, (long long)rows_alloc * F_pad,
                                &flags[1], st);
         if (e != cudaSuccess) return cuda_fail(e, "silu planes launch");
-        e = encode_planes_map(ph, F_pad, 3LL * rows_alloc, maph);
+        e = encode_plane_maps(ph, F_pad, rows_alloc, &maph);
         if (e != cudaSuccess) return cuda_fail(e, "hidden tensor map");
         TcArgs d = a;
         d.mi = 2;

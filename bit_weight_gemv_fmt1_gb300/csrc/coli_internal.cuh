@@ -16,6 +16,7 @@
 // a shared-memory phase hit 8 different bank groups.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -513,13 +514,17 @@ struct TcArgs {
 bool tc_supported_fmt(int fmt, int gs);
 int tc_block_rows();
 cudaError_t encode_codes_map(const uint8_t *q, long long rs, long long O, void *out128);
-cudaError_t encode_planes_map(const void *planes, long long I_pad, long long total_rows, void *out128);
+// TMA maps of the activation planes (see encode_plane_maps); CUtensorMap blobs
+struct PlaneMapSet {
+    CUtensorMap m[6];
+};
+cudaError_t encode_plane_maps(const void *planes, long long I_pad, long long rows_alloc, PlaneMapSet *out);
 cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *order, int kdiv, const int32_t *n_valid,
                                  int n_rows, int I, int I_pad, void *planes, long long plane_elems, int *flag,
                                  cudaStream_t st);
 cudaError_t launch_silu_planes(const float *gu, int F, const int32_t *n_valid, int n_rows, int F_pad, void *planes,
                                long long plane_elems, int *flag, cudaStream_t st);
-cudaError_t launch_gemm_tc(const TcArgs &a, const void *planes_map128, int max_tiles, int n_sm, cudaStream_t st);
+cudaError_t launch_gemm_tc(const TcArgs &a, const PlaneMapSet &maps, int max_tiles, int n_sm, cudaStream_t st);
 
 cudaError_t launch_moe_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t smem, cudaStream_t st);
 cudaError_t moe_decode_occupancy(int fmt, size_t smem, int *per_sm);
@@ -531,6 +536,25 @@ cudaError_t launch_fmt1_encode(uint8_t *q, long long n, cudaStream_t st);
 size_t gemv_smem_bytes(int fmt, int cpr, int S, int I, bool generic);
 
 // S = 1 kernels with the activation slab in registers (slab.cu).
+// Streamed decode block (S = 1): weights arrive in shared memory by bulk
+// copies; see moe_decode_stream_kernel.
+struct StreamArgs {
+    MoeDecodeArgs m;          // x, ids, w, y, table, n_experts, K, H, F, cpr_gu, cpr_d, hbuf, bar, err, timeout_ns
+    int rs_gu, rs_d;          // bytes per gate/up row and per down row
+    int ng_gu, ng_d;          // scales per row
+    int gshift_gu, gshift_d;  // log2(gs / 32): chunk -> group
+    int RP, RB;               // gate/up row pairs per phase-A stage, down rows per phase-B stage
+    int red_floats;           // capacity of the per-CTA partial-sum buffer
+};
+constexpr int kStreamStageBytes = 27 * 1024;
+constexpr int kStreamStages = 5;
+constexpr int kStreamXhBytes = 64 * 1024;     // staged x (phase A) or h of the routed experts (phase B)
+constexpr int kStreamRedBytes = 12 * 1024;
+constexpr int kStreamConsumerWarps = 12;
+size_t stream_decode_smem();
+cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st);
+cudaError_t stream_decode_occupancy(int *per_sm);
+
 bool slab_supported(int fmt, int gs);
 size_t slab_gemv_smem(const GemvJob &job, int n_sm);
 cudaError_t launch_slab_gemv(const GemvJob &job, int n_sm, cudaStream_t st);

@@ -15,15 +15,18 @@
 // plane is loaded and multiplied.
 //
 // Warp roles (480 threads, persistent over a static tile schedule):
-//   warps 0-7   dequant: codes (smem) -> bf16 A tile, SW128 K-major layout;
-//               two threads per weight row, each half a K-block
+//   warps 0-7   dequant: codes (smem) -> bf16 A tile in TMEM (tcgen05.st),
+//               two threads per weight row, each half a K-block; keeping A
+//               out of shared memory leaves its bandwidth to the TMA streams
 //   warps 8-11  epilogue: TMEM -> registers, group scale, row scale, store
 //   warp  12    TMA producer of the codes: box [128 rows x 128 B] = 4 K-blocks
 //   warp  13    MMA issuer (one thread), tcgen05.mma kind::f16, M=128
-//   warp  14    TMA producer of the activation planes: 16-row boxes, only as
-//               many as the tile's rows need; a plane stage holds 64 rows per
-//               plane, so a tile of <= 16 rows takes 4 K-blocks per stage
-// With three planes they are stacked along N (N = 3 x the tile's padded rows)
+//   warp  14    TMA producer of the activation planes: one 4-D box per stage
+//               of R rows (16, 32 or 64: the tile's rows rounded up) x the
+//               planes x 64/R K-blocks, so small tiles take 4 K-blocks a copy
+// A TMA copy or an MMA costs the issuing thread about 130 or 56 cycles (N <= 64),
+// so each is made to carry as much of the tile as it can.
+// With three planes they are stacked along N (N = 3 x R)
 // so a K-step is one MMA whatever the plane count; the epilogue adds the three
 // column blocks.  A tcgen05.mma with N <= 64 costs the same issue time as one
 // with N = 64, so the issuing thread's loop is kept to the MMAs, the waits and
@@ -38,6 +41,7 @@
 #include <cudaTypedefs.h>
 
 #include "coli_internal.cuh"
+#include "mbarrier.cuh"
 
 namespace coli {
 
@@ -45,22 +49,20 @@ namespace {
 
 constexpr int BM = 128, BK = 64, BN = 64;
 constexpr int KB_PER_CS = 4;                          // K-blocks per codes stage: 128-byte row segments
-constexpr int NC = 4;                                 // codes stages (16 KB each): the HBM stream
-constexpr int NA = 3;                                 // dequantized A stages (16 KB each)
+constexpr int NC = 5;                                 // codes stages (16 KB each): the HBM stream
+constexpr int NA = 4;                                 // dequantized A stages, in TMEM (32 columns each)
 constexpr int NPL = 3;                                // activation planes
 constexpr int CODES_BYTES = BM * BK / 2 * KB_PER_CS;  // 16384: 128 rows x 128 B, 128-byte swizzle
-constexpr int A_BYTES = BM * BK * 2;                  // 16384
-constexpr int BOX_ROWS = 16;                          // activation rows per TMA box
-constexpr int BOX_BYTES = BOX_ROWS * BK * 2;          // 2048
 constexpr int PLANE_BYTES = BN * BK * 2;              // 8192: 64 rows x 128 B
-constexpr int B_RING = 4 * NPL * PLANE_BYTES;         // 96 KB
-constexpr int NB1 = B_RING / PLANE_BYTES;             // plane stages with one plane: 12
-constexpr int NB3 = B_RING / (NPL * PLANE_BYTES);     // with three planes: 4
+constexpr int B_RING = 5 * NPL * PLANE_BYTES;         // 120 KB
+constexpr int NB1 = B_RING / PLANE_BYTES;             // plane stages with one plane: 15
+constexpr int NB3 = B_RING / (NPL * PLANE_BYTES);     // with three planes: 5
 constexpr int NBMAX = NB1;
-constexpr int NACCMAX = 8;
+constexpr int NACCMAX = 6;
+constexpr uint32_t ACC_COLS = 384;                    // TMEM columns [0, 384): accumulators
+constexpr uint32_t A_COL0 = ACC_COLS;                 // [384, 512): NA A stages of 128 lanes x 64 bf16
 constexpr int OFF_B = 0;
-constexpr int OFF_A = OFF_B + B_RING;
-constexpr int OFF_CODES = OFF_A + NA * A_BYTES;
+constexpr int OFF_CODES = OFF_B + B_RING;
 constexpr int OFF_BAR = OFF_CODES + NC * CODES_BYTES;
 constexpr int N_BAR = 2 * NC + 2 * NBMAX + 2 * NA + 2 * NACCMAX + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;   // + alignment slack
@@ -71,43 +73,19 @@ constexpr int kTcThreads = 15 * 32;                   // <= 4 warps per SM sub-p
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_addr(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait: false once `deadline` (globaltimer ns) has passed or the CTA aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, uint64_t deadline, volatile int *abort) {
-    while (!mbar_try(b, parity)) {
-        if (*abort) return false;
-        if (global_ns() > deadline) return false;
-    }
-    return true;
-}
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
         ::"r"(smem_addr(dst)), "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
 }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        ::"r"(smem_addr(dst)), "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -126,12 +104,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
+// A from tensor memory (128 lanes = rows, 2 bf16 per column), B from shared memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t dtmem, uint32_t atmem, uint64_t bd, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(dtmem), "r"(atmem), "l"(bd), "r"(idesc), "r"(acc)
         : "memory");
 }
+// 16 consecutive TMEM columns of this thread's lane <- v; complete after tmem_wait_st().
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
@@ -184,36 +172,26 @@ __device__ __forceinline__ const MatDesc &mat_of(const TcArgs &a, const Tile &t)
     return a.table ? a.table[t.e].m[t.mi] : a.single;
 }
 
-// Bounded wait taken by a whole warp: every lane polls, lane 0 decides on
-// expiry, so the warp leaves together either way.
-__device__ __forceinline__ bool warp_wait(uint64_t *b, uint32_t parity, uint64_t deadline, volatile int *abort,
-                                          int lane) {
-    while (true) {
-        const bool done = mbar_try(b, parity);
-        if (__all_sync(0xffffffffu, done)) return true;
-        int stop = 0;
-        if (lane == 0) stop = (*abort != 0) || global_ns() > deadline;
-        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-    }
-}
-
 struct Bars {
     uint64_t *c_full, *c_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty, *done;
 };
 
-// Token rows per tile rounded to the MMA's N granule, and how many K-blocks
-// of activations share one plane stage (a stage holds 64 rows per plane).
-__device__ __forceinline__ int npad_of(const Tile &t) { return ((t.p1 - t.p0) + 15) & ~15; }
-__device__ __forceinline__ int kps_of(int npad) { return npad <= 16 ? 4 : (npad <= 32 ? 2 : 1); }
+// Row class of a tile: the activation rows one plane box carries (16, 32 or
+// 64, at least the tile's rows) and how many K-blocks one plane stage holds
+// (a stage is 64 rows x 64 inputs per plane).
+__device__ __forceinline__ int rcls_of(const Tile &t) {
+    const int n = t.p1 - t.p0;
+    return n <= 16 ? 0 : (n <= 32 ? 1 : 2);
+}
 
 // The warp roles for NT activation planes.  With NT = 3 the planes are
-// stacked along N: one MMA of N = 3 * npad multiplies all three, and the
+// stacked along N: one MMA of N = 3 * R multiplies all three, and the
 // epilogue adds the three column blocks.
 template <int NT>
-__device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &a, uint8_t *smem, const Bars &B,
+__device__ __forceinline__ void run_roles(const PlaneMapSet &tmx, const TcArgs &a, uint8_t *smem, const Bars &B,
                                           uint32_t tmem, volatile int &abort_flag, uint64_t deadline) {
     constexpr int NB = NT == 1 ? NB1 : NB3;
-    constexpr int NACC = NT == 1 ? 8 : 2;             // TMEM accumulators of NT * 64 columns
+    constexpr int NACC = NT == 1 ? 6 : 2;             // TMEM accumulators of NT * 64 columns
     constexpr int B_STAGE = NT * PLANE_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = a.tile_e ? *a.n_tiles : (a.P + BN - 1) / BN;
@@ -258,28 +236,23 @@ __device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &
             for (int k = max(0, it - NC); k < it; k++) mbar_wait(&B.c_full[k % NC], (k / NC) & 1, dl2, &no_abort);
         }
     } else if (warp == kPlanesWarp) {
-        // ---------------- TMA producer: activation planes, 16-row boxes, kps K-blocks per stage
+        // ---------------- TMA producer: activation planes, one box of kps K-blocks x NT planes x R rows per stage
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmx) : "memory");
+            for (int c = 0; c < 3; c++) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmx.m[c + (NT == 1 ? 0 : 3)]) : "memory");
             int it = 0, s = 0;
             uint32_t ph = 0;
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok && !abort_flag; L += gridDim.x) {
                 const Tile t = tile_of(a, L, n_tiles);
-                const int npad = npad_of(t), nbox = npad / BOX_ROWS, kps = kps_of(npad);
+                const int rc = rcls_of(t), kps = 4 >> rc;
+                const CUtensorMap *map = &tmx.m[rc + (NT == 1 ? 0 : 3)];
                 for (int kb0 = 0; kb0 < a.nkb; kb0 += kps) {
-                    const int nk = min(kps, a.nkb - kb0);
                     if (it >= NB && !mbar_wait(&B.b_empty[s], ph ^ 1, deadline, &abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(&B.b_full[s], nk * NT * nbox * BOX_BYTES);
-                    uint8_t *dst = smem + OFF_B + s * B_STAGE;
-                    for (int kk = 0; kk < nk; kk++)
-                        for (int pl = 0; pl < NT; pl++)
-                            for (int bx = 0; bx < nbox; bx++)
-                                tma_load_2d(dst + ((kk * NT + pl) * npad + bx * BOX_ROWS) * (BK * 2), &tmx,
-                                            (kb0 + kk) * BK, pl * a.rows_alloc + t.p0 + bx * BOX_ROWS, &B.b_full[s]);
+                    mbar_expect_tx(&B.b_full[s], B_STAGE);
+                    tma_load_4d(smem + OFF_B + s * B_STAGE, map, 0, t.p0, 0, kb0, &B.b_full[s]);
                     it++;
                     if (++s == NB) {
                         s = 0;
@@ -297,14 +270,13 @@ __device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &
         if (lane == 0) {
             int ai = 0, as = 0, bs = 0, gb = 0, g = 0;
             uint32_t aph = 0, bph = 0, gph = 0;
-            const uint64_t ad0 = sdesc_sw128(smem_addr(smem + OFF_A));
             const uint64_t bd0 = sdesc_sw128(smem_addr(smem + OFF_B));
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok && !abort_flag; L += gridDim.x) {
                 const Tile t = tile_of(a, L, n_tiles);
-                const int npad = npad_of(t), kps = kps_of(npad);
-                const uint32_t idesc = idesc_bf16(BM, NT * npad);
-                const uint32_t kstep = (uint32_t)(NT * npad * BK * 2) >> 4;   // one K-block inside a plane stage
+                const int rc = rcls_of(t), R = 16 << rc, kps = 4 >> rc;
+                const uint32_t idesc = idesc_bf16(BM, NT * R);
+                const uint32_t kstep = (uint32_t)(NT * R * BK * 2) >> 4;   // one K-block inside a plane stage
                 int kk = 0, kg = 0;
                 for (int kb = 0; kb < a.nkb; kb++) {
                     const bool first = kg == 0;
@@ -318,12 +290,12 @@ __device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = ad0 + (uint64_t)(as * (A_BYTES >> 4));
+                    const uint32_t at = tmem + A_COL0 + (uint32_t)(as * (BK / 2));
                     const uint64_t bd = bd0 + (uint64_t)(bs * (B_STAGE >> 4) + kk * kstep);
                     const uint32_t d = tmem + (uint32_t)(gb * NT * BN);
 #pragma unroll
                     for (int j = 0; j < BK / 16; j++)
-                        mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
+                        mma_bf16_ts(d, at + 8 * j, bd + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
                     mma_commit(&B.a_empty[as]);
                     ai++;
                     if (++as == NA) {
@@ -383,22 +355,23 @@ __device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &
                     ok = false;
                     break;
                 }
+                tc_fence_after();
                 const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-                uint8_t *arow = smem + OFF_A + as * A_BYTES + r * 128;
+                uint32_t q[16];
 #pragma unroll
                 for (int cc = 0; cc < 4; cc++) {
-                    uint32_t q[4];
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
                         uint32_t v = ((w[cc] >> (4 * k)) & 0x000F000Fu) | 0x43004300u;
                         __nv_bfloat162 hv = *reinterpret_cast<__nv_bfloat162 *>(&v);
                         hv = __hsub2(hv, off);
-                        q[k] = *reinterpret_cast<uint32_t *>(&hv);
+                        q[4 * cc + k] = *reinterpret_cast<uint32_t *>(&hv);
                     }
-                    *reinterpret_cast<uint4 *>(arow + (((4 * h + cc) ^ (r & 7)) << 4)) =
-                        make_uint4(q[0], q[1], q[2], q[3]);
                 }
-                fence_async_smem();
+                // lane r of TMEM, columns [A_COL0 + 32 as + 16 h, +16): inputs 32h..32h+31 of the K-block
+                tmem_st16(tmem + ((uint32_t)(warp & 3) << 21) + A_COL0 + (uint32_t)(as * (BK / 2) + h * 16), q);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.a_full[as]);
                 it++;
@@ -420,8 +393,8 @@ __device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &
             const Tile t = tile_of(a, L, n_tiles);
             const MatDesc &M = mat_of(a, t);
             const int n_tok = t.p1 - t.p0;
-            const int npad = npad_of(t);
-            const int nch = npad >> 4;
+            const int R = 16 << rcls_of(t);        // columns per plane block
+            const int nch = (n_tok + 15) >> 4;     // 16-column chunks holding this tile's rows
             const int o = t.mb * BM + m;
             const bool row_ok = o < a.O;
             float acc[BN];
@@ -474,7 +447,7 @@ __device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &
                             if (c8 >= 2 * nch) break;
                             uint32_t v[NT][8];
 #pragma unroll
-                            for (int pl = 0; pl < NT; pl++) tmem_ld8(base + pl * npad + c8 * 8, v[pl]);
+                            for (int pl = 0; pl < NT; pl++) tmem_ld8(base + pl * R + c8 * 8, v[pl]);
                             tmem_wait_ld();
 #pragma unroll
                             for (int k = 0; k < 8; k++) {
@@ -507,7 +480,7 @@ __device__ __forceinline__ void run_roles(const CUtensorMap &tmx, const TcArgs &
     }
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ PlaneMapSet tmx, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
@@ -671,18 +644,25 @@ cudaError_t encode_codes_map(const uint8_t *q, long long rs, long long O, void *
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t encode_planes_map(const void *planes, long long I_pad, long long total_rows, void *out128) {
-    CUtensorMap *out = (CUtensorMap *)out128;
+// Six 4-D maps over the planes [3][rows_alloc][I_pad] bf16, dimensions
+// (64 inputs, rows, plane, K-block): box (64, R, NTb, 64 / R) for R = 16, 32,
+// 64 and NTb = 1 (maps 0-2) or 3 (maps 3-5).  One box fills a plane stage in
+// the order [K-block][plane][row][64 inputs], 128-byte swizzled.
+cudaError_t encode_plane_maps(const void *planes, long long I_pad, long long rows_alloc, PlaneMapSet *out) {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {(cuuint64_t)I_pad, (cuuint64_t)total_rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(I_pad * 2)};
-    cuuint32_t box[2] = {BK, BOX_ROWS};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)planes, dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    cuuint64_t dims[4] = {(cuuint64_t)BK, (cuuint64_t)rows_alloc, (cuuint64_t)NPL, (cuuint64_t)(I_pad / BK)};
+    cuuint64_t strides[3] = {(cuuint64_t)(I_pad * 2), (cuuint64_t)(rows_alloc * I_pad * 2), (cuuint64_t)(BK * 2)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    for (int nt = 0; nt < 2; nt++)
+        for (int rc = 0; rc < 3; rc++) {
+            cuuint32_t box[4] = {BK, (cuuint32_t)(16 << rc), (cuuint32_t)(nt ? NPL : 1), (cuuint32_t)(4 >> rc)};
+            CUresult r = fn(&out->m[rc + 3 * nt], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)planes, dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        }
+    return cudaSuccess;
 }
 
 cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *order, int kdiv, const int32_t *n_valid,
@@ -702,8 +682,7 @@ cudaError_t launch_silu_planes(const float *gu, int F, const int32_t *n_valid, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(const TcArgs &a, const void *planes_map128, int max_tiles, int n_sm, cudaStream_t st) {
-    const CUtensorMap &tmx = *(const CUtensorMap *)planes_map128;
+cudaError_t launch_gemm_tc(const TcArgs &a, const PlaneMapSet &tmx, int max_tiles, int n_sm, cudaStream_t st) {
     const long long total = (long long)max_tiles * a.n_mblk;
     if (total <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);

@@ -16,7 +16,10 @@
 // The arithmetic per chunk is that of dot_rows: exact decode of each code into
 // the mantissa of 1.0 (or 2^23 for int8), exact offset removal, packed f32x2
 // FMA into bit-position classes that are rescaled by powers of two.
+#include <type_traits>
+
 #include "coli_internal.cuh"
+#include "mbarrier.cuh"
 
 namespace coli {
 
@@ -464,6 +467,397 @@ __global__ void __launch_bounds__(kSlabThreads, 2) moe_decode_slab_kernel(const 
     for (int rr = tid; rr < n_o; rr += blockDim.x) a.y[oc0 + rr] = yacc[rr];
 }
 
+
+// ------------------------------------------------------------------ decode block, S = 1, streamed
+// One CTA per SM.  Warp 12 streams the CTA's weight rows into a ring of
+// shared-memory stages with bulk copies (cp.async.bulk: whole rows, with
+// their group scales), five stages of 27 KB, so ~20 MB is in flight over the
+// GPU -- enough to cover HBM latency -- without any register cost.  Warps
+// 0-11 consume: warp w owns slab (w mod n_slab) of every row, keeps the
+// activations of that slab in registers (XReg), and reduces each (row, slab)
+// unit across the warp into a partial-sum buffer; sums over slabs, experts
+// and the SiLU are taken in a fixed order, so results do not depend on timing.
+//   phase A: stages of RP (gate row j, up row j) pairs of one routed expert;
+//            the CTA's pairs are a contiguous range of (expert, j);
+//            h[a][j] = silu(sum_s g) * sum_s u -> global scratch
+//   grid barrier (consumer warps only; the producer keeps streaming the
+//            phase-B rows, which do not depend on h)
+//   phase B: stages of RB down rows of one routed expert; the CTA owns rows
+//            [oc0, oc1) of y and adds the experts in ascending id order.
+// int4 chunk dot product without the offset-removal adds (streamed decode).
+// A code n at bit position p of a word, AND-ed out with no exponent bits, is
+// the f32 subnormal n * 2^(p-149), exactly.  Each lane holds its chunk's
+// activations scaled by 2^k (exact: a power of two), k chosen from the
+// chunk's largest |x| so that |x * 2^k| < 2^27; then every product
+// n * x * 2^(p-149+k) and every class sum is a normal f32 formed with the
+// usual single rounding of the FMA.  The classes are rescaled by 2^(49-p),
+// the sum by 2^(100-k), and the code offset 8 comes off as 8 * sum(x).  The
+// FMAs must keep subnormal inputs: plain fma.rn.f32x2, no flush to zero.
+__device__ __forceinline__ float exp2i(int e) {   // 2^e for -126 <= e <= 127
+    return __int_as_float((e + 127) << 23);
+}
+struct XRegS4 {
+    float4 v[8];        // x * 2^k, staged order of XReg<4>
+    float xsum;         // sum of the chunk's 32 activations
+    float f1, f2;       // 2^(100-k) = f1 * f2
+    __device__ __forceinline__ void load(const uint32_t *stage, int c) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(stage + (size_t)c * 32);
+        float t = 0.f, mx = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            v[j] = s4[j ^ (c & 7)];
+            t += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+        }
+        xsum = t;
+        // biased exponent eb of mx: mx < 2^(eb-126); k = 153 - eb, kept in [-126, 127]
+        const int eb = (__float_as_int(mx) >> 23) & 0xFF;
+        const int k = min(127, max(-126, 153 - eb));
+        const float s1 = exp2i(k / 2), s2 = exp2i(k - k / 2);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            v[j] = make_float4(v[j].x * s1 * s2, v[j].y * s1 * s2, v[j].z * s1 * s2, v[j].w * s1 * s2);
+        const int r = 100 - k;   // in [-27, 226]
+        f1 = exp2i(r / 2);
+        f2 = exp2i(r - r / 2);
+    }
+    __device__ __forceinline__ static float2 sub2(uint32_t a, uint32_t b) {
+        return make_float2(__uint_as_float(a), __uint_as_float(b));
+    }
+    __device__ __forceinline__ float dot(uint4 q) const {
+        float2 a01 = make_float2(0.f, 0.f), a25 = a01, a36 = a01, a47 = a01;
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint32_t w = w4[k], b = w >> 12;
+            ffma2(a01, sub2(w & 0xFu, w & 0xF0u), make_float2(v[2 * k].x, v[2 * k].y));
+            ffma2(a25, sub2(w & 0xF00u, b & 0xF00u), make_float2(v[2 * k].z, v[2 * k].w));
+            ffma2(a36, sub2(w & 0xF000u, b & 0xF000u), make_float2(v[2 * k + 1].x, v[2 * k + 1].y));
+            ffma2(a47, sub2(w & 0xF0000u, b & 0xF0000u), make_float2(v[2 * k + 1].z, v[2 * k + 1].w));
+        }
+        // classes p = 0, 4 | 8 | 12 | 16 -> factors 2^(49-p)
+        const float s = a01.x * 562949953421312.0f + a01.y * 35184372088832.0f + (a25.x + a25.y) * 2199023255552.0f +
+                        (a36.x + a36.y) * 137438953472.0f + (a47.x + a47.y) * 8589934592.0f;
+        return fmaf(-8.0f, xsum, (s * f1) * f2);
+    }
+};
+
+// Sums of four per-lane values over the warp with 6 shuffles: afterwards lane
+// 8k (k = 0..3) holds the total of value k.
+__device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v3, int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8;
+    float a0 = h16 ? v2 : v0, a1 = h16 ? v3 : v1;
+    const float b0 = h16 ? v0 : v2, b1 = h16 ? v1 : v3;
+    a0 += __shfl_xor_sync(0xffffffffu, b0, 16);
+    a1 += __shfl_xor_sync(0xffffffffu, b1, 16);
+    float k = h8 ? a1 : a0;
+    const float sd = h8 ? a0 : a1;
+    k += __shfl_xor_sync(0xffffffffu, sd, 8);
+    k += __shfl_xor_sync(0xffffffffu, k, 4);
+    k += __shfl_xor_sync(0xffffffffu, k, 2);
+    k += __shfl_xor_sync(0xffffffffu, k, 1);
+    return k;
+}
+
+struct StreamStage {
+    int kind;   // 0: phase A pairs, 1: phase B rows
+    int ai;     // routed-expert index (ascending expert id)
+    int row0, n;
+};
+struct StreamCursor {
+    long long pr, pr1;   // phase-A pair range still to issue
+    int bai, o, oc0, oc1, nact;
+    __device__ __forceinline__ bool next(const StreamArgs &a, StreamStage &st) {
+        if (pr < pr1) {
+            const int ai = (int)(pr / a.m.F);
+            const int j = (int)(pr - (long long)ai * a.m.F);
+            const int n = (int)min((long long)a.RP, min(pr1 - pr, (long long)(a.m.F - j)));
+            st = {0, ai, j, n};
+            pr += n;
+            return true;
+        }
+        if (bai < nact && o < oc1) {
+            const int n = min(a.RB, oc1 - o);
+            st = {1, bai, o, n};
+            o += n;
+            if (o >= oc1) {
+                o = oc0;
+                bai++;
+            }
+            return true;
+        }
+        return false;
+    }
+};
+
+template <int FMT>
+__global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode_stream_kernel(const StreamArgs a) {
+    constexpr int NWC = kStreamConsumerWarps, NCT = NWC * 32, NS = kStreamStages, SB = kStreamStageBytes;
+    extern __shared__ uint8_t sraw[];
+    uint8_t *ring = (uint8_t *)(((uintptr_t)sraw + 127) & ~(uintptr_t)127);
+    uint32_t *xh = reinterpret_cast<uint32_t *>(ring + NS * SB);
+    float *red = reinterpret_cast<float *>(ring + NS * SB + kStreamXhBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * SB + kStreamXhBytes + kStreamRedBytes);
+    uint64_t *empty = full + NS;
+    __shared__ int s_ids[kMaxDecodeSlots];
+    __shared__ float s_w[kMaxDecodeSlots];
+    __shared__ int s_exp[kMaxDecodeSlots];
+    __shared__ float s_ew[kMaxDecodeSlots];
+    __shared__ int s_nact, s_bad;
+    __shared__ volatile int abort_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const MoeDecodeArgs &m = a.m;
+    const int n = m.K;   // S = 1
+    const uint64_t deadline = global_ns() + (uint64_t)m.timeout_ns;
+
+    // ---- phase 0: distinct routed experts in ascending id order, weights summed
+    if (tid == 0) {
+        s_bad = 0;
+        abort_flag = 0;
+        for (int i = 0; i < NS; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid < n) {
+        const int e = m.ids[tid];
+        s_ids[tid] = e;
+        s_w[tid] = m.w[tid];
+        if (e < -1 || e >= m.n_experts) atomicOr(&s_bad, 1);
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (blockIdx.x == 0 && tid == 0) atomicCAS(m.err, 0, DEV_ERR_BAD_ID);
+        return;
+    }
+    if (tid == 0) {
+        int na = 0, last = -1;
+        for (;;) {
+            int best = 0x7fffffff;
+            for (int t = 0; t < n; t++)
+                if (s_ids[t] > last && s_ids[t] < best) best = s_ids[t];
+            if (best == 0x7fffffff) break;
+            float wsum = 0.f;
+            for (int t = 0; t < n; t++)
+                if (s_ids[t] == best) wsum += s_w[t];
+            s_exp[na] = best;
+            s_ew[na] = wsum;
+            na++;
+            last = best;
+        }
+        s_nact = na;
+    }
+    __syncthreads();
+    const int nact = s_nact;
+
+    // work of this CTA
+    const long long pairs = (long long)nact * m.F;
+    const long long ppc = (pairs + gridDim.x - 1) / gridDim.x;
+    const long long pr0 = min(pairs, (long long)blockIdx.x * ppc), pr1 = min(pairs, pr0 + ppc);
+    const int rpc = (m.H + gridDim.x - 1) / gridDim.x;
+    const int oc0 = min(m.H, (int)blockIdx.x * rpc), oc1 = min(m.H, oc0 + rpc);
+    StreamCursor cur;
+    cur.pr = pr0;
+    cur.pr1 = pr1;
+    cur.bai = 0;
+    cur.o = oc0;
+    cur.oc0 = oc0;
+    cur.oc1 = oc1;
+    cur.nact = nact;
+    const int offA_u = a.RP * a.rs_gu, offA_sg = 2 * a.RP * a.rs_gu, offA_su = offA_sg + a.RP * a.ng_gu * 4;
+    const int offB_s = a.RB * a.rs_d;
+
+    if (warp == NWC) {
+        // ---------------- producer: bulk copies of whole rows (and their scales) into the stage ring
+        if (lane == 0) {
+            int s = 0, it = 0;
+            uint32_t ph = 0;
+            StreamStage st;
+            while (cur.next(a, st)) {
+                if (it >= NS && !mbar_wait(&empty[s], ph ^ 1, deadline, &abort_flag)) {
+                    if (!abort_flag) {
+                        abort_flag = 1;
+                        atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                uint8_t *dst = ring + s * SB;
+                const ExpertDesc &E = m.table[s_exp[st.ai]];
+                if (st.kind == 0) {
+                    const uint32_t cb = (uint32_t)(st.n * a.rs_gu), sbytes = (uint32_t)(st.n * a.ng_gu * 4);
+                    mbar_expect_tx(&full[s], 2 * cb + 2 * sbytes);
+                    bulk_load(dst, E.m[0].q + (size_t)st.row0 * a.rs_gu, cb, &full[s]);
+                    bulk_load(dst + offA_u, E.m[1].q + (size_t)st.row0 * a.rs_gu, cb, &full[s]);
+                    bulk_load(dst + offA_sg, E.m[0].s + (size_t)st.row0 * a.ng_gu, sbytes, &full[s]);
+                    bulk_load(dst + offA_su, E.m[1].s + (size_t)st.row0 * a.ng_gu, sbytes, &full[s]);
+                } else {
+                    const uint32_t cb = (uint32_t)(st.n * a.rs_d), sbytes = (uint32_t)(st.n * a.ng_d * 4);
+                    mbar_expect_tx(&full[s], cb + sbytes);
+                    bulk_load(dst, E.m[2].q + (size_t)st.row0 * a.rs_d, cb, &full[s]);
+                    bulk_load(dst + offB_s, E.m[2].s + (size_t)st.row0 * a.ng_d, sbytes, &full[s]);
+                }
+                it++;
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            // every copy issued has landed before the CTA may exit
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int k = max(0, it - NS); k < it; k++) mbar_wait(&full[k % NS], (k / NS) & 1, dl2, &no_abort);
+        }
+        return;
+    }
+
+    // ---------------- consumers (warps 0..NWC-1); they sync among themselves only
+    const int nsA = (m.cpr_gu + 31) >> 5, nsB = (m.cpr_d + 31) >> 5;
+    const int GA = NWC / nsA, GB = NWC / nsB;
+    const int slA = warp % nsA, subA = warp / nsA, slB = warp % nsB, subB = warp / nsB;
+    const size_t xw_gu = staged_words(FMT, m.cpr_gu), xw_d = staged_words(FMT, m.cpr_d);
+    stage_vec<FMT>(reinterpret_cast<float *>(xh), m.x, m.H, (int)xw_gu, tid, NCT);
+    named_sync(1, NCT);
+    using XR = typename std::conditional<FMT == 4, XRegS4, XReg<FMT>>::type;
+    XR xr;
+    xr.load(xh, slA * 32 + lane);
+    int s = 0;
+    uint32_t ph = 0;
+    StreamStage st;
+    bool have = cur.next(a, st);
+    // phase A
+    while (have && st.kind == 0) {
+        if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
+            const uint8_t *src = ring + s * SB;
+            const int c = slA * 32 + lane;
+            const bool okc = c < m.cpr_gu;
+            const long long prb = (long long)st.ai * m.F + st.row0 - pr0;
+            // this warp's pairs of the stage: subA and subA + GA (RP <= 2 GA)
+            const int p0 = subA, p1 = subA + GA;
+            const bool ok0 = okc && p0 < st.n, ok1 = okc && p1 < st.n;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            const uint4 qg0 = ok0 ? *reinterpret_cast<const uint4 *>(src + p0 * a.rs_gu + c * 16) : z;
+            const uint4 qu0 = ok0 ? *reinterpret_cast<const uint4 *>(src + offA_u + p0 * a.rs_gu + c * 16) : z;
+            const uint4 qg1 = ok1 ? *reinterpret_cast<const uint4 *>(src + p1 * a.rs_gu + c * 16) : z;
+            const uint4 qu1 = ok1 ? *reinterpret_cast<const uint4 *>(src + offA_u + p1 * a.rs_gu + c * 16) : z;
+            const int gi0 = (p0 * a.ng_gu + (c >> a.gshift_gu)) * 4, gi1 = (p1 * a.ng_gu + (c >> a.gshift_gu)) * 4;
+            const float sg0 = ok0 ? *reinterpret_cast<const float *>(src + offA_sg + gi0) : 0.f;
+            const float su0 = ok0 ? *reinterpret_cast<const float *>(src + offA_su + gi0) : 0.f;
+            const float sg1 = ok1 ? *reinterpret_cast<const float *>(src + offA_sg + gi1) : 0.f;
+            const float su1 = ok1 ? *reinterpret_cast<const float *>(src + offA_su + gi1) : 0.f;
+            const float t = warp_sum4(xr.dot(qg0) * sg0, xr.dot(qu0) * su0, xr.dot(qg1) * sg1, xr.dot(qu1) * su1,
+                                      lane);
+            if ((lane & 7) == 0) {
+                const int k = lane >> 3;
+                const int pp = k < 2 ? p0 : p1;
+                if (pp < st.n) red[((prb + pp) * nsA + slA) * 2 + (k & 1)] = t;
+            }
+        } else if (!abort_flag && lane == 0) {
+            abort_flag = 1;
+            atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1;
+        }
+        have = cur.next(a, st);
+    }
+    named_sync(1, NCT);
+    for (long long prl = tid; prl < pr1 - pr0; prl += NCT) {
+        float g = 0.f, u = 0.f;
+        for (int k = 0; k < nsA; k++) {
+            g += red[(prl * nsA + k) * 2];
+            u += red[(prl * nsA + k) * 2 + 1];
+        }
+        m.hbuf[pr0 + prl] = g / (1.0f + expf(-g)) * u;
+    }
+    // grid barrier among the consumer warps of all CTAs
+    named_sync(1, NCT);
+    if (tid == 0 && !abort_flag) {
+        unsigned *bar = m.bar;
+        const unsigned gen = ld_acquire(bar + 1);
+        __threadfence();
+        const unsigned prev = atomicAdd(bar, 1u);
+        if (prev == gridDim.x - 1) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            atomicAdd(bar + 1, 1u);
+        } else {
+            while (ld_acquire(bar + 1) == gen) {
+                if (global_ns() > deadline) {
+                    atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
+                    abort_flag = 1;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+    }
+    named_sync(1, NCT);
+    // h of the routed experts, staged per expert in the order XReg reads
+    if (xw_d == (size_t)m.F) {
+        stage_vec<FMT>(reinterpret_cast<float *>(xh), m.hbuf, nact * m.F, nact * (int)xw_d, tid, NCT);
+    } else {
+        for (int ai = 0; ai < nact; ai++)
+            stage_vec<FMT>(reinterpret_cast<float *>(xh + (size_t)ai * xw_d), m.hbuf + (size_t)ai * m.F, m.F,
+                           (int)xw_d, tid, NCT);
+    }
+    named_sync(1, NCT);
+    // phase B
+    int cur_ai = -1;
+    while (have) {
+        if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
+            if (st.ai != cur_ai) {
+                cur_ai = st.ai;
+                xr.load(xh + (size_t)cur_ai * xw_d, slB * 32 + lane);
+            }
+            const uint8_t *src = ring + s * SB;
+            const int c = slB * 32 + lane;
+            const bool okc = c < m.cpr_d;
+            // this warp's rows of the stage: subB + k GB, k < 4 (RB <= 4 GB)
+            float v[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int r = subB + k * GB;
+                const bool ok = okc && r < st.n;
+                const uint4 q = ok ? *reinterpret_cast<const uint4 *>(src + r * a.rs_d + c * 16) : make_uint4(0, 0, 0, 0);
+                const float sc =
+                    ok ? *reinterpret_cast<const float *>(src + offB_s + (r * a.ng_d + (c >> a.gshift_d)) * 4) : 0.f;
+                v[k] = xr.dot(q) * sc;
+            }
+            const float t = warp_sum4(v[0], v[1], v[2], v[3], lane);
+            if ((lane & 7) == 0) {
+                const int r = subB + (lane >> 3) * GB;
+                if (r < st.n) red[((size_t)cur_ai * rpc + (st.row0 - oc0 + r)) * nsB + slB] = t;
+            }
+        } else if (!abort_flag && lane == 0) {
+            abort_flag = 1;
+            atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1;
+        }
+        have = cur.next(a, st);
+    }
+    named_sync(1, NCT);
+    for (int rr = tid; rr < oc1 - oc0; rr += NCT) {
+        float acc = 0.f;
+        for (int ai = 0; ai < nact; ai++) {
+            float d = 0.f;
+            for (int k = 0; k < nsB; k++) d += red[((size_t)ai * rpc + rr) * nsB + k];
+            acc = fmaf(s_ew[ai], d, acc);
+        }
+        m.y[oc0 + rr] = acc;
+    }
+}
+
 template <int FMT>
 cudaError_t slab_gemv_t(const GemvJob &job, int n_sm, int gshift, cudaStream_t st) {
     const int total = job.row_start[job.n];
@@ -513,6 +907,36 @@ int log2_exact(int v) {
 }
 
 }  // namespace
+
+size_t stream_decode_smem() {
+    return (size_t)kStreamStages * kStreamStageBytes + kStreamXhBytes + kStreamRedBytes + 2 * kStreamStages * 8 + 128;
+}
+
+cudaError_t stream_decode_occupancy(int *per_sm) {
+    auto kern = moe_decode_stream_kernel<4>;
+    const size_t smem = stream_decode_smem();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, (kStreamConsumerWarps + 1) * 32, smem);
+}
+
+cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st) {
+    auto kern = moe_decode_stream_kernel<4>;
+    const size_t smem = stream_decode_smem();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((kStreamConsumerWarps + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
 
 // gs (fmt=4) usable by the slab kernels: a power-of-two number of 32-input chunks.
 bool slab_supported(int fmt, int gs) {

@@ -57,6 +57,63 @@ def test_decode_block(fmt, gs, S, K):
     assert norm_err(got, ref) <= TOL
 
 
+@pytest.mark.parametrize("H,F,gs,K", [(3072, 1536, 64, 8), (6144, 2048, 128, 8), (1024, 512, 64, 3),
+                                      (2048, 1024, 32, 16)])
+def test_decode_streamed_shapes(H, F, gs, K):
+    """S = 1 int4 shapes taken by the bulk-copy decode kernel: several slabs per
+    row, pair ranges that straddle experts and CTAs, partial stages."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(4100 + H + F + gs + K)
+    host = _experts(g, H, F, 24, 4, gs, distinct=6)
+    x = wl.activations(g, 1, H)
+    ids, w = wl.routing_topk_softmax(g, 1, 24, K)
+    table = _device_table(coli, host)
+    got = _run_block(coli, torch, table, x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert norm_err(got, ref) <= TOL
+    again = _run_block(coli, torch, table, x, ids, w, H)
+    assert np.array_equal(got, again)
+
+
+def test_decode_streamed_duplicates_and_empty_slots():
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F = 1024, 512
+    g = wl.rng(4200)
+    host = _experts(g, H, F, 8, 4, 64)
+    table = _device_table(coli, host)
+    mats = _oracle_mats(host)
+    x = wl.activations(g, 1, H)
+    for ids in (np.array([[3, 3, -1, 5]], np.int32), np.array([[7, 0, 7, 7]], np.int32),
+                np.array([[-1, -1, -1, -1]], np.int32)):
+        w = g.uniform(0.05, 1.0, ids.shape).astype(np.float32)
+        got = _run_block(coli, torch, table, x, ids, w, H)
+        ref = orc.moe_block(H, F, mats, x, ids, w)
+        if np.all(ids < 0):
+            assert np.all(got == 0.0)
+        else:
+            assert norm_err(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("scale", [1e12, 2.0 ** 30, 1e-12])
+def test_decode_streamed_activation_magnitudes(scale):
+    """Activations far from unit size: the streamed kernel rescales each lane's
+    chunk by a power of two before multiplying, so large and tiny inputs keep
+    full f32 precision."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F = 2048, 1024
+    g = wl.rng(4300)
+    host = _experts(g, H, F, 8, 4, 64)
+    x = (wl.activations(g, 1, H) * scale).astype(np.float32)
+    ids, w = wl.routing_topk_softmax(g, 1, 8, 4)
+    got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert np.all(np.isfinite(got))
+    assert norm_err(got, ref) <= TOL
+
+
 def test_decode_ragged_routing_and_empty_slots():
     """Empty slots (-1), duplicate ids in a row, a row with no expert, the
     shared expert as one more weight-1 expert on every row."""
