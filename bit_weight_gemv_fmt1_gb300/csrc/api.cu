@@ -540,8 +540,10 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
     if (S == 1 && fmt == 4 && n_slots <= kMaxDecodeSlots) {
         const coli_tensor *d0 = experts[0].down;
         const int gs_gu = g0->gs, gs_d = d0->gs;
+        // whole 128-input blocks (so every lane's 32-input chunk is in range) and a 16-byte aligned x
         bool ok = gs_gu % 32 == 0 && gs_d % 32 == 0 && slab_supported(4, gs_gu) && slab_supported(4, gs_d) &&
-                  g0->ng % 4 == 0 && d0->ng % 4 == 0;
+                  g0->ng % 4 == 0 && d0->ng % 4 == 0 && H % 128 == 0 && F % 128 == 0 &&
+                  ((uintptr_t)x & 15) == 0;
         for (int e = 0; e < n_experts && ok; e++)
             ok = experts[e].gate->gs == gs_gu && experts[e].up->gs == gs_gu && experts[e].down->gs == gs_d;
         const int nsA = (cpr_gu + 31) / 32, nsB = (cpr_d + 31) / 32;

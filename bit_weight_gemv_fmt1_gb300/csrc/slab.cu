@@ -500,14 +500,18 @@ struct XRegS4 {
     float4 v[8];        // x * 2^k, staged order of XReg<4>
     float xsum;         // sum of the chunk's 32 activations
     float f1, f2;       // 2^(100-k) = f1 * f2
-    __device__ __forceinline__ void load(const uint32_t *stage, int c) {
-        const float4 *s4 = reinterpret_cast<const float4 *>(stage + (size_t)c * 32);
+    // raw[2k], raw[2k+1]: inputs 8k..8k+3, 8k+4..8k+7 of the chunk in natural order
+    __device__ __forceinline__ void set(const float4 (&raw)[8]) {
         float t = 0.f, mx = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            v[j] = s4[j ^ (c & 7)];
-            t += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+        for (int k = 0; k < 4; k++) {
+            const float4 a = raw[2 * k], b = raw[2 * k + 1];
+            // pairs matched to the code classes of dot(): x0 x1 x2 x5 | x3 x6 x4 x7
+            v[2 * k] = make_float4(a.x, a.y, a.z, b.y);
+            v[2 * k + 1] = make_float4(a.w, b.z, b.x, b.w);
+            t += ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+            mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                 fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w)))));
         }
         xsum = t;
         // biased exponent eb of mx: mx < 2^(eb-126); k = 153 - eb, kept in [-126, 127]
@@ -520,6 +524,24 @@ struct XRegS4 {
         const int r = 100 - k;   // in [-27, 226]
         f1 = exp2i(r / 2);
         f2 = exp2i(r - r / 2);
+    }
+    // chunk c of a vector staged by stage_vec<4> (permuted, swizzled, zero padded)
+    __device__ __forceinline__ void load_staged(const uint32_t *stage, int c) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(stage + (size_t)c * 32);
+        float4 raw[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            // undo the pair order so set() can apply it again
+            const float4 u = s4[j ^ (c & 7)];
+            raw[j] = u;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const float4 p0 = raw[2 * k], p1 = raw[2 * k + 1];   // x0 x1 x2 x5 | x3 x6 x4 x7
+            raw[2 * k] = make_float4(p0.x, p0.y, p0.z, p1.x);
+            raw[2 * k + 1] = make_float4(p1.z, p0.w, p1.y, p1.w);
+        }
+        set(raw);
     }
     __device__ __forceinline__ static float2 sub2(uint32_t a, uint32_t b) {
         return make_float2(__uint_as_float(a), __uint_as_float(b));
@@ -609,6 +631,17 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
     const MoeDecodeArgs &m = a.m;
     const int n = m.K;   // S = 1
     const uint64_t deadline = global_ns() + (uint64_t)m.timeout_ns;
+    // consumer lanes start loading their activation chunk now; it is used after phase 0
+    const int nsA = (m.cpr_gu + 31) >> 5, slA = warp % nsA;
+    // (lanes past the row's last chunk hold zeros)
+    float4 xraw[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp < NWC && slA * 32 + lane < m.cpr_gu) {
+        const float4 *p = reinterpret_cast<const float4 *>(m.x + (size_t)(slA * 32 + lane) * 32);
+#pragma unroll
+        for (int j = 0; j < 8; j++) xraw[j] = __ldg(p + j);
+    }
 
     // ---- phase 0: distinct routed experts in ascending id order, weights summed
     if (tid == 0) {
@@ -632,22 +665,31 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
         if (blockIdx.x == 0 && tid == 0) atomicCAS(m.err, 0, DEV_ERR_BAD_ID);
         return;
     }
-    if (tid == 0) {
-        int na = 0, last = -1;
-        for (;;) {
-            int best = 0x7fffffff;
-            for (int t = 0; t < n; t++)
-                if (s_ids[t] > last && s_ids[t] < best) best = s_ids[t];
-            if (best == 0x7fffffff) break;
-            float wsum = 0.f;
-            for (int t = 0; t < n; t++)
-                if (s_ids[t] == best) wsum += s_w[t];
-            s_exp[na] = best;
-            s_ew[na] = wsum;
-            na++;
-            last = best;
+    // slot t is the first of its id: its rank among the distinct ids gives its place
+    if (tid == 0) s_nact = 0;
+    __syncthreads();
+    if (tid < n) {
+        const int e = s_ids[tid];
+        bool first = e >= 0;
+        int rank = 0;
+        float wsum = 0.f;
+        for (int t = 0; t < n; t++) {
+            const int f = s_ids[t];
+            if (f == e) {
+                wsum += s_w[t];
+                if (t < tid) first = false;
+            }
+            if (f >= 0 && f < e) {
+                bool fst = true;   // count each smaller id once, at its first slot
+                for (int u = 0; u < t; u++) fst &= s_ids[u] != f;
+                rank += fst;
+            }
         }
-        s_nact = na;
+        if (first) {
+            s_exp[rank] = e;
+            s_ew[rank] = wsum;
+            atomicAdd(&s_nact, 1);
+        }
     }
     __syncthreads();
     const int nact = s_nact;
@@ -713,15 +755,11 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
     }
 
     // ---------------- consumers (warps 0..NWC-1); they sync among themselves only
-    const int nsA = (m.cpr_gu + 31) >> 5, nsB = (m.cpr_d + 31) >> 5;
+    const int nsB = (m.cpr_d + 31) >> 5;
     const int GA = NWC / nsA, GB = NWC / nsB;
-    const int slA = warp % nsA, subA = warp / nsA, slB = warp % nsB, subB = warp / nsB;
-    const size_t xw_gu = staged_words(FMT, m.cpr_gu), xw_d = staged_words(FMT, m.cpr_d);
-    stage_vec<FMT>(reinterpret_cast<float *>(xh), m.x, m.H, (int)xw_gu, tid, NCT);
-    named_sync(1, NCT);
-    using XR = typename std::conditional<FMT == 4, XRegS4, XReg<FMT>>::type;
-    XR xr;
-    xr.load(xh, slA * 32 + lane);
+    const int subA = warp / nsA, slB = warp % nsB, subB = warp / nsB;
+    XRegS4 xr;
+    xr.set(xraw);
     int s = 0;
     uint32_t ph = 0;
     StreamStage st;
@@ -798,13 +836,14 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
         __threadfence();
     }
     named_sync(1, NCT);
-    // h of the routed experts, staged per expert in the order XReg reads
+    // h of the routed experts, staged per expert in the order the warps read it
+    const size_t xw_d = staged_words(4, m.cpr_d);
     if (xw_d == (size_t)m.F) {
-        stage_vec<FMT>(reinterpret_cast<float *>(xh), m.hbuf, nact * m.F, nact * (int)xw_d, tid, NCT);
+        stage_vec<4>(reinterpret_cast<float *>(xh), m.hbuf, nact * m.F, nact * (int)xw_d, tid, NCT);
     } else {
         for (int ai = 0; ai < nact; ai++)
-            stage_vec<FMT>(reinterpret_cast<float *>(xh + (size_t)ai * xw_d), m.hbuf + (size_t)ai * m.F, m.F,
-                           (int)xw_d, tid, NCT);
+            stage_vec<4>(reinterpret_cast<float *>(xh + (size_t)ai * xw_d), m.hbuf + (size_t)ai * m.F, m.F, (int)xw_d,
+                         tid, NCT);
     }
     named_sync(1, NCT);
     // phase B
@@ -813,7 +852,7 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
         if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
             if (st.ai != cur_ai) {
                 cur_ai = st.ai;
-                xr.load(xh + (size_t)cur_ai * xw_d, slB * 32 + lane);
+                xr.load_staged(xh + (size_t)cur_ai * xw_d, slB * 32 + lane);
             }
             const uint8_t *src = ring + s * SB;
             const int c = slB * 32 + lane;

@@ -58,7 +58,7 @@ def test_decode_block(fmt, gs, S, K):
 
 
 @pytest.mark.parametrize("H,F,gs,K", [(3072, 1536, 64, 8), (6144, 2048, 128, 8), (1024, 512, 64, 3),
-                                      (2048, 1024, 32, 16)])
+                                      (2048, 1024, 32, 16), (1152, 640, 32, 8)])
 def test_decode_streamed_shapes(H, F, gs, K):
     """S = 1 int4 shapes taken by the bulk-copy decode kernel: several slabs per
     row, pair ranges that straddle experts and CTAs, partial stages."""
