@@ -496,7 +496,7 @@ def main():
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
-        traffic = json.load(open(tr_path)).get("moe_decode_kernel")
+        traffic = json.load(open(tr_path)).get("moe_decode_stream_kernel")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -525,7 +525,7 @@ def main():
             "hbm_frac_of_measured": value / peaks["hbm_gbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "peak_source": peaks["source"], "kernel": "moe_decode_kernel<4>",
+                         "peak_source": peaks["source"], "kernel": "moe_decode_stream_kernel<4>",
                          "avg_launch_us": avg_launch_s * 1e6, "timing": timing_mode},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": wk.h2d, "d2h_bytes_per_step": wk.d2h},

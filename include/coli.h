@@ -117,10 +117,14 @@ int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_
  * matmul for S > 1; PR #298 page, "metal: grouped-int4 (fmt=4) GEMV support"
  * commit message, Shader paragraph).
  *   W       uploaded tensor.
- *   x       device f32 [S][I], row-major, 16-byte aligned.
+ *   x       device f32 [S][I], row-major, 4-byte aligned (16-byte alignment
+ *           lets the kernels use vector loads).
  *   y       device f32 [S][O], row-major, overwritten; must not overlap x.
- *   S       rows, >= 1.  S <= 16 runs the bandwidth-bound CUDA-core kernels;
- *           larger S runs the tensor-core GEMM.
+ *   S       rows, >= 1.  S <= 8 (with the activations fitting shared memory)
+ *           runs the bandwidth-bound CUDA-core matvec kernels, S = 1 the
+ *           slab kernel for fmt 0/1/2/4; larger S runs the tensor-core GEMM
+ *           for fmt=2 and for fmt=4 with gs % 64 == 0, the tiled CUDA-core
+ *           GEMM otherwise.
  * Errors: COLI_EINVAL (NULL/misaligned pointer, S < 1), COLI_EDEVICE, COLI_ECUDA.
  */
 int coli_matmul(const coli_tensor *W, const float *x, float *y, int S, void *stream);
@@ -171,11 +175,16 @@ int coli_moe_route(const int32_t *ids, int S, int K, int n_experts, int32_t *off
  *   w        device f32 [S][K] routing weights, used as given.
  *   y        device f32 [S][H], overwritten; must not overlap x.
  *   S >= 1, 1 <= K <= 64.
- * S*K <= 64 runs the single-launch decode kernel (a cooperative grid with one
- * bounded grid-wide wait between the gate/up and down phases).  Larger S*K
- * runs the prefill pipeline (routing, gather, grouped gate/up, grouped down,
- * combine).  An id out of range is recorded for coli_sync_check(stream) and y
- * is then unspecified.
+ * S*K <= 64 runs a single-launch decode kernel (a cooperative grid with one
+ * bounded grid-wide wait between the gate/up and down phases): for S = 1 and
+ * fmt=4 (gs a power-of-two multiple of 32, a multiple of 4 groups per row,
+ * H and F multiples of 128, x 16-byte aligned, K*F*4 <= 64 KB) the kernel that
+ * streams the weights through shared memory with bulk copies; otherwise the
+ * slab kernel (S = 1) or the general decode kernel.  Larger S*K runs the
+ * prefill pipeline (routing, gather, grouped gate/up, grouped down, combine)
+ * on the tensor cores for int4 tables with gs % 64 == 0, on the CUDA cores
+ * otherwise.  An id out of range is recorded for coli_sync_check(stream) and
+ * y is then unspecified.
  * Errors: COLI_EINVAL, COLI_EFMT, COLI_EDEVICE, COLI_ENOMEM, COLI_ECUDA.
  */
 int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_experts,
