@@ -561,7 +561,8 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         int per_sm = 0;
         if (ok && stream_decode_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) {
             Workspace *ws = nullptr;
-            if (int rc = workspace(ds, st, (size_t)n_slots * F * sizeof(float), &ws)) return rc;
+            const size_t hstride = std::max((size_t)F, (size_t)staged_len(4, cpr_d));
+            if (int rc = workspace(ds, st, (size_t)n_slots * hstride * sizeof(float), &ws)) return rc;
             StreamArgs a;
             memset(&a, 0, sizeof a);
             a.m.x = x;

@@ -643,9 +643,17 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
         for (int j = 0; j < 8; j++) xraw[j] = __ldg(p + j);
     }
 
-    // ---- phase 0: distinct routed experts in ascending id order, weights summed
+    // ---- phase 0: distinct routed experts in ascending id order, weights summed.
+    // The producer warp reads the token's slots (its lane t holds slot t when
+    // K <= 32) while the consumer lanes' activation loads are in flight.
+    const int pl = tid - NWC * 32;   // producer-warp lane, or negative
+    int my_id = -1;
+    float my_w = 0.f;
+    if (pl >= 0 && pl < n) {
+        my_id = m.ids[pl];
+        my_w = m.w[pl];
+    }
     if (tid == 0) {
-        s_bad = 0;
         abort_flag = 0;
         for (int i = 0; i < NS; i++) {
             mbar_init(&full[i], 1);
@@ -653,45 +661,78 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncthreads();
-    if (tid < n) {
-        const int e = m.ids[tid];
-        s_ids[tid] = e;
-        s_w[tid] = m.w[tid];
-        if (e < -1 || e >= m.n_experts) atomicOr(&s_bad, 1);
+    if (n <= 32) {
+        if (warp == NWC) {
+            const bool valid = pl < n;
+            const bool bad = valid && (my_id < -1 || my_id >= m.n_experts);
+            const unsigned any_bad = __ballot_sync(0xffffffffu, bad);
+            bool first = valid && my_id >= 0;
+            int rank = 0;
+            float wsum = 0.f;
+            for (int t = 0; t < n; t++) {
+                const int f = __shfl_sync(0xffffffffu, my_id, t);
+                const float wt = __shfl_sync(0xffffffffu, my_w, t);
+                if (f == my_id) {
+                    wsum += wt;
+                    if (t < pl) first = false;
+                }
+                // count each smaller id once, at its first slot
+                const unsigned same_before = __ballot_sync(0xffffffffu, pl < t && my_id == f);
+                if (f >= 0 && f < my_id && same_before == 0u) rank++;
+            }
+            if (first && !any_bad) {
+                s_exp[rank] = my_id;
+                s_ew[rank] = wsum;
+            }
+            const unsigned nf = __popc(__ballot_sync(0xffffffffu, first));
+            if (lane == 0) {
+                s_bad = any_bad != 0u;
+                s_nact = (int)nf;
+            }
+        }
+        __syncthreads();
+    } else {
+        if (tid == 0) {
+            s_bad = 0;
+            s_nact = 0;
+        }
+        __syncthreads();
+        if (tid < n) {
+            const int e = m.ids[tid];
+            s_ids[tid] = e;
+            s_w[tid] = m.w[tid];
+            if (e < -1 || e >= m.n_experts) atomicOr(&s_bad, 1);
+        }
+        __syncthreads();
+        if (!s_bad && tid < n) {
+            const int e = s_ids[tid];
+            bool first = e >= 0;
+            int rank = 0;
+            float wsum = 0.f;
+            for (int t = 0; t < n; t++) {
+                const int f = s_ids[t];
+                if (f == e) {
+                    wsum += s_w[t];
+                    if (t < tid) first = false;
+                }
+                if (f >= 0 && f < e) {
+                    bool fst = true;   // count each smaller id once, at its first slot
+                    for (int u = 0; u < t; u++) fst &= s_ids[u] != f;
+                    rank += fst;
+                }
+            }
+            if (first) {
+                s_exp[rank] = e;
+                s_ew[rank] = wsum;
+                atomicAdd(&s_nact, 1);
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
     if (s_bad) {
         if (blockIdx.x == 0 && tid == 0) atomicCAS(m.err, 0, DEV_ERR_BAD_ID);
         return;
     }
-    // slot t is the first of its id: its rank among the distinct ids gives its place
-    if (tid == 0) s_nact = 0;
-    __syncthreads();
-    if (tid < n) {
-        const int e = s_ids[tid];
-        bool first = e >= 0;
-        int rank = 0;
-        float wsum = 0.f;
-        for (int t = 0; t < n; t++) {
-            const int f = s_ids[t];
-            if (f == e) {
-                wsum += s_w[t];
-                if (t < tid) first = false;
-            }
-            if (f >= 0 && f < e) {
-                bool fst = true;   // count each smaller id once, at its first slot
-                for (int u = 0; u < t; u++) fst &= s_ids[u] != f;
-                rank += fst;
-            }
-        }
-        if (first) {
-            s_exp[rank] = e;
-            s_ew[rank] = wsum;
-            atomicAdd(&s_nact, 1);
-        }
-    }
-    __syncthreads();
     const int nact = s_nact;
 
     // work of this CTA
@@ -804,13 +845,18 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
         have = cur.next(a, st);
     }
     named_sync(1, NCT);
+    // h[a][j] goes to hbuf in the order phase B stages it: expert a's block of
+    // xw_d floats, element j at stage_pos<4>(j) (chunks past F are never read)
+    const size_t xw_d = staged_words(4, m.cpr_d);
     for (long long prl = tid; prl < pr1 - pr0; prl += NCT) {
         float g = 0.f, u = 0.f;
         for (int k = 0; k < nsA; k++) {
             g += red[(prl * nsA + k) * 2];
             u += red[(prl * nsA + k) * 2 + 1];
         }
-        m.hbuf[pr0 + prl] = g / (1.0f + expf(-g)) * u;
+        const long long pr = pr0 + prl;
+        const int ai = (int)(pr / m.F), j = (int)(pr - (long long)ai * m.F);
+        m.hbuf[(size_t)ai * xw_d + stage_pos<4>(j)] = g / (1.0f + expf(-g)) * u;
     }
     // grid barrier among the consumer warps of all CTAs
     named_sync(1, NCT);
@@ -836,14 +882,24 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
         __threadfence();
     }
     named_sync(1, NCT);
-    // h of the routed experts, staged per expert in the order the warps read it
-    const size_t xw_d = staged_words(4, m.cpr_d);
-    if (xw_d == (size_t)m.F) {
-        stage_vec<4>(reinterpret_cast<float *>(xh), m.hbuf, nact * m.F, nact * (int)xw_d, tid, NCT);
-    } else {
-        for (int ai = 0; ai < nact; ai++)
-            stage_vec<4>(reinterpret_cast<float *>(xh + (size_t)ai * xw_d), m.hbuf + (size_t)ai * m.F, m.F, (int)xw_d,
-                         tid, NCT);
+    // h of the routed experts: already in staged order; chunks past F are zero
+    {
+        const float4 *src4 = reinterpret_cast<const float4 *>(m.hbuf);
+        float4 *dst4 = reinterpret_cast<float4 *>(xh);
+        const int n4 = nact * (int)xw_d / 4, c4 = (int)xw_d / 4;
+        constexpr int UN = 8;
+        for (int i0 = tid; i0 < n4; i0 += NCT * UN) {
+            float4 t[UN];
+#pragma unroll
+            for (int u = 0; u < UN; u++) {
+                const int i = i0 + u * NCT;
+                const bool live = i < n4 && ((i % c4) >> 3) * 32 < m.F;   // chunk (8 float4) inside F
+                t[u] = live ? __ldcg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < UN; u++)
+                if (i0 + u * NCT < n4) dst4[i0 + u * NCT] = t[u];
+        }
     }
     named_sync(1, NCT);
     // phase B
