@@ -124,8 +124,10 @@ int workspace(DeviceState *d, cudaStream_t st, size_t bytes, Workspace **out) {
     std::lock_guard<std::mutex> lk(d->mu);
     Workspace &w = d->ws[st];
     if (!w.bar) {
-        CU(cudaMalloc(&w.bar, 2 * sizeof(unsigned)), "cudaMalloc(barrier)");
-        CU(cudaMemset(w.bar, 0, 2 * sizeof(unsigned)), "cudaMemset(barrier)");
+        // words 0-1: counter and generation of the resetting grid barrier;
+        // bytes 128-135: the monotonic 64-bit arrival counter of the streamed decode
+        CU(cudaMalloc(&w.bar, kBarrierBytes), "cudaMalloc(barrier)");
+        CU(cudaMemset(w.bar, 0, kBarrierBytes), "cudaMemset(barrier)");
     }
     if (w.cap < bytes) {
         if (w.buf) {
@@ -877,7 +879,7 @@ int coli_sync_check(void *stream) {
     if (word == DEV_ERR_TIMEOUT) {
         std::lock_guard<std::mutex> lk(ds->mu);
         for (auto &kv : ds->ws)
-            if (kv.second.bar) cudaMemset(kv.second.bar, 0, 2 * sizeof(unsigned));
+            if (kv.second.bar) cudaMemset(kv.second.bar, 0, kBarrierBytes);
         return fail(COLI_ETIMEOUT, "a grid-wide wait in the expert block ran out of time");
     }
     if (word == DEV_ERR_BAD_ID) return fail(COLI_EINVAL, "a routing id was outside [-1, n_experts)");

@@ -546,6 +546,7 @@ struct StreamArgs {
     int RP, RB;               // gate/up row pairs per phase-A stage, down rows per phase-B stage
     int red_floats;           // capacity of the per-CTA partial-sum buffer
 };
+constexpr size_t kBarrierBytes = 256;           // per-workspace grid-barrier words (see workspace())
 constexpr int kStreamStageBytes = 27 * 1024;
 constexpr int kStreamStages = 5;
 constexpr int kStreamXhBytes = 64 * 1024;     // staged x (phase A) or h of the routed experts (phase B)

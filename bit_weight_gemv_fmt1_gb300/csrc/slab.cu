@@ -557,10 +557,33 @@ struct XRegS4 {
             ffma2(a36, sub2(w & 0xF000u, b & 0xF000u), make_float2(v[2 * k + 1].x, v[2 * k + 1].y));
             ffma2(a47, sub2(w & 0xF0000u, b & 0xF0000u), make_float2(v[2 * k + 1].z, v[2 * k + 1].w));
         }
+        return finish(a01, a25, a36, a47);
+    }
+    __device__ __forceinline__ float finish(float2 a01, float2 a25, float2 a36, float2 a47) const {
         // classes p = 0, 4 | 8 | 12 | 16 -> factors 2^(49-p)
         const float s = a01.x * 562949953421312.0f + a01.y * 35184372088832.0f + (a25.x + a25.y) * 2199023255552.0f +
                         (a36.x + a36.y) * 137438953472.0f + (a47.x + a47.y) * 8589934592.0f;
         return fmaf(-8.0f, xsum, (s * f1) * f2);
+    }
+    // four chunks against the same activations, interleaved word by word
+    __device__ __forceinline__ void dot4(const uint4 (&q)[4], float (&out)[4]) const {
+        float2 a01[4], a25[4], a36[4], a47[4];
+#pragma unroll
+        for (int d = 0; d < 4; d++) a01[d] = a25[d] = a36[d] = a47[d] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+#pragma unroll
+            for (int d = 0; d < 4; d++) {
+                const uint32_t w = k == 0 ? q[d].x : k == 1 ? q[d].y : k == 2 ? q[d].z : q[d].w;
+                const uint32_t b = w >> 12;
+                ffma2(a01[d], sub2(w & 0xFu, w & 0xF0u), make_float2(v[2 * k].x, v[2 * k].y));
+                ffma2(a25[d], sub2(w & 0xF00u, b & 0xF00u), make_float2(v[2 * k].z, v[2 * k].w));
+                ffma2(a36[d], sub2(w & 0xF000u, b & 0xF000u), make_float2(v[2 * k + 1].x, v[2 * k + 1].y));
+                ffma2(a47[d], sub2(w & 0xF0000u, b & 0xF0000u), make_float2(v[2 * k + 1].z, v[2 * k + 1].w));
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < 4; d++) out[d] = finish(a01[d], a25[d], a36[d], a47[d]);
     }
 };
 
@@ -825,8 +848,10 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
             const float su0 = ok0 ? *reinterpret_cast<const float *>(src + offA_su + gi0) : 0.f;
             const float sg1 = ok1 ? *reinterpret_cast<const float *>(src + offA_sg + gi1) : 0.f;
             const float su1 = ok1 ? *reinterpret_cast<const float *>(src + offA_su + gi1) : 0.f;
-            const float t = warp_sum4(xr.dot(qg0) * sg0, xr.dot(qu0) * su0, xr.dot(qg1) * sg1, xr.dot(qu1) * su1,
-                                      lane);
+            const uint4 qq[4] = {qg0, qu0, qg1, qu1};
+            float dd[4];
+            xr.dot4(qq, dd);
+            const float t = warp_sum4(dd[0] * sg0, dd[1] * su0, dd[2] * sg1, dd[3] * su1, lane);
             if ((lane & 7) == 0) {
                 const int k = lane >> 3;
                 const int pp = k < 2 ? p0 : p1;
@@ -860,24 +885,24 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
     }
     // grid barrier among the consumer warps of all CTAs
     named_sync(1, NCT);
+    // Arrivals count up a 64-bit counter that is never reset between calls:
+    // every launch of this kernel on the workspace has gridDim.x CTAs, so this
+    // call's CTAs wait until the count reaches the next multiple of gridDim.x.
     if (tid == 0 && !abort_flag) {
-        unsigned *bar = m.bar;
-        const unsigned gen = ld_acquire(bar + 1);
+        unsigned long long *ctr = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(m.bar) + 128);
         __threadfence();
-        const unsigned prev = atomicAdd(bar, 1u);
-        if (prev == gridDim.x - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
-        } else {
-            while (ld_acquire(bar + 1) == gen) {
-                if (global_ns() > deadline) {
-                    atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
-                    abort_flag = 1;
-                    break;
-                }
-                __nanosleep(64);
+        const unsigned long long old = atomicAdd(ctr, 1ull);
+        const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
+        for (;;) {
+            unsigned long long v;
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+            if (v >= target) break;
+            if (global_ns() > deadline) {
+                atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
+                abort_flag = 1;
+                break;
             }
+            __nanosleep(20);
         }
         __threadfence();
     }
@@ -914,17 +939,17 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
             const int c = slB * 32 + lane;
             const bool okc = c < m.cpr_d;
             // this warp's rows of the stage: subB + k GB, k < 4 (RB <= 4 GB)
-            float v[4];
+            uint4 qq[4];
+            float sc[4], dd[4];
 #pragma unroll
             for (int k = 0; k < 4; k++) {
                 const int r = subB + k * GB;
                 const bool ok = okc && r < st.n;
-                const uint4 q = ok ? *reinterpret_cast<const uint4 *>(src + r * a.rs_d + c * 16) : make_uint4(0, 0, 0, 0);
-                const float sc =
-                    ok ? *reinterpret_cast<const float *>(src + offB_s + (r * a.ng_d + (c >> a.gshift_d)) * 4) : 0.f;
-                v[k] = xr.dot(q) * sc;
+                qq[k] = ok ? *reinterpret_cast<const uint4 *>(src + r * a.rs_d + c * 16) : make_uint4(0, 0, 0, 0);
+                sc[k] = ok ? *reinterpret_cast<const float *>(src + offB_s + (r * a.ng_d + (c >> a.gshift_d)) * 4) : 0.f;
             }
-            const float t = warp_sum4(v[0], v[1], v[2], v[3], lane);
+            xr.dot4(qq, dd);
+            const float t = warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
             if ((lane & 7) == 0) {
                 const int r = subB + (lane >> 3) * GB;
                 if (r < st.n) red[((size_t)cur_ai * rpc + (st.row0 - oc0 + r)) * nsB + slB] = t;
