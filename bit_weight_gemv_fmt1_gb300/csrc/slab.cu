@@ -610,15 +610,19 @@ struct StreamStage {
     int row0, n;
 };
 struct StreamCursor {
-    long long pr, pr1;   // phase-A pair range still to issue
+    long long left;      // phase-A pairs still to issue
+    int ai, j;           // next phase-A pair: routed expert ai, row j (kept without division)
     int bai, o, oc0, oc1, nact;
     __device__ __forceinline__ bool next(const StreamArgs &a, StreamStage &st) {
-        if (pr < pr1) {
-            const int ai = (int)(pr / a.m.F);
-            const int j = (int)(pr - (long long)ai * a.m.F);
-            const int n = (int)min((long long)a.RP, min(pr1 - pr, (long long)(a.m.F - j)));
+        if (left > 0) {
+            const int n = (int)min((long long)min(a.RP, a.m.F - j), left);
             st = {0, ai, j, n};
-            pr += n;
+            left -= n;
+            j += n;
+            if (j == a.m.F) {
+                j = 0;
+                ai++;
+            }
             return true;
         }
         if (bai < nact && o < oc1) {
@@ -765,8 +769,9 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
     const int rpc = (m.H + gridDim.x - 1) / gridDim.x;
     const int oc0 = min(m.H, (int)blockIdx.x * rpc), oc1 = min(m.H, oc0 + rpc);
     StreamCursor cur;
-    cur.pr = pr0;
-    cur.pr1 = pr1;
+    cur.left = pr1 - pr0;
+    cur.ai = (int)(pr0 / m.F);
+    cur.j = (int)(pr0 - (long long)cur.ai * m.F);
     cur.bai = 0;
     cur.o = oc0;
     cur.oc0 = oc0;
@@ -834,7 +839,7 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
             const uint8_t *src = ring + s * SB;
             const int c = slA * 32 + lane;
             const bool okc = c < m.cpr_gu;
-            const long long prb = (long long)st.ai * m.F + st.row0 - pr0;
+            const int prb = (int)((long long)st.ai * m.F + st.row0 - pr0);   // local pair index of row0
             // this warp's pairs of the stage: subA and subA + GA (RP <= 2 GA)
             const int p0 = subA, p1 = subA + GA;
             const bool ok0 = okc && p0 < st.n, ok1 = okc && p1 < st.n;
