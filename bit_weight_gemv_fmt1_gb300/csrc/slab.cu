@@ -487,28 +487,29 @@ __global__ void __launch_bounds__(kSlabThreads, 2) moe_decode_slab_kernel(const 
 // int4 chunk dot product without the offset-removal adds (streamed decode).
 // A code n at bit position p of a word, AND-ed out with no exponent bits, is
 // the f32 subnormal n * 2^(p-149), exactly.  Each lane holds its chunk's
-// activations scaled by 2^k (exact: a power of two), k chosen from the
-// chunk's largest |x| so that |x * 2^k| < 2^27; then every product
-// n * x * 2^(p-149+k) and every class sum is a normal f32 formed with the
-// usual single rounding of the FMA.  The classes are rescaled by 2^(49-p),
-// the sum by 2^(100-k), and the code offset 8 comes off as 8 * sum(x).  The
-// FMAs must keep subnormal inputs: plain fma.rn.f32x2, no flush to zero.
+// activations multiplied by 2^(k-p), p the bit position its code will sit at
+// and k chosen from the chunk's largest |x| so that |x * 2^k| < 2^27 (exact:
+// powers of two).  Every product is then n * x * 2^(k-149), the same scale for
+// all positions, a normal f32 formed with the usual single rounding of the FMA,
+// so two accumulators per chunk suffice; the sum is rescaled by 2^(149-k) and
+// the code offset 8 comes off as 8 * sum(x).  The FMAs must keep subnormal
+// inputs: plain fma.rn.f32x2, no flush to zero.
 __device__ __forceinline__ float exp2i(int e) {   // 2^e for -126 <= e <= 127
     return __int_as_float((e + 127) << 23);
 }
+__device__ __forceinline__ float mul_exp2(float x, int e) {   // x * 2^e, -252 <= e <= 254, exact unless it under/overflows
+    return (x * exp2i(e / 2)) * exp2i(e - e / 2);
+}
 struct XRegS4 {
-    float4 v[8];        // x * 2^k, staged order of XReg<4>
+    float4 v[8];        // x * 2^(k-p), pairs in the order of dot()
     float xsum;         // sum of the chunk's 32 activations
-    float f1, f2;       // 2^(100-k) = f1 * f2
+    float f1, f2, f3;   // 2^(149-k) = f1 * f2 * f3
     // raw[2k], raw[2k+1]: inputs 8k..8k+3, 8k+4..8k+7 of the chunk in natural order
     __device__ __forceinline__ void set(const float4 (&raw)[8]) {
         float t = 0.f, mx = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const float4 a = raw[2 * k], b = raw[2 * k + 1];
-            // pairs matched to the code classes of dot(): x0 x1 x2 x5 | x3 x6 x4 x7
-            v[2 * k] = make_float4(a.x, a.y, a.z, b.y);
-            v[2 * k + 1] = make_float4(a.w, b.z, b.x, b.w);
             t += ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
             mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
                                  fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w)))));
@@ -516,28 +517,29 @@ struct XRegS4 {
         xsum = t;
         // biased exponent eb of mx: mx < 2^(eb-126); k = 153 - eb, kept in [-126, 127]
         const int eb = (__float_as_int(mx) >> 23) & 0xFF;
-        const int k = min(127, max(-126, 153 - eb));
-        const float s1 = exp2i(k / 2), s2 = exp2i(k - k / 2);
+        const int ks = min(127, max(-126, 153 - eb));
 #pragma unroll
-        for (int j = 0; j < 8; j++)
-            v[j] = make_float4(v[j].x * s1 * s2, v[j].y * s1 * s2, v[j].z * s1 * s2, v[j].w * s1 * s2);
-        const int r = 100 - k;   // in [-27, 226]
-        f1 = exp2i(r / 2);
-        f2 = exp2i(r - r / 2);
+        for (int k = 0; k < 4; k++) {
+            const float4 a = raw[2 * k], b = raw[2 * k + 1];
+            // x0 x1 x2 x5 at bit positions 0 4 8 8 | x3 x6 x4 x7 at 12 12 16 16
+            v[2 * k] = make_float4(mul_exp2(a.x, ks), mul_exp2(a.y, ks - 4), mul_exp2(a.z, ks - 8), mul_exp2(b.y, ks - 8));
+            v[2 * k + 1] = make_float4(mul_exp2(a.w, ks - 12), mul_exp2(b.z, ks - 12), mul_exp2(b.x, ks - 16),
+                                       mul_exp2(b.w, ks - 16));
+        }
+        const int r = 149 - ks;   // in [22, 275]
+        f1 = exp2i(r / 3);
+        f2 = exp2i(r / 3);
+        f3 = exp2i(r - 2 * (r / 3));
     }
     // chunk c of a vector staged by stage_vec<4> (permuted, swizzled, zero padded)
     __device__ __forceinline__ void load_staged(const uint32_t *stage, int c) {
         const float4 *s4 = reinterpret_cast<const float4 *>(stage + (size_t)c * 32);
         float4 raw[8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            // undo the pair order so set() can apply it again
-            const float4 u = s4[j ^ (c & 7)];
-            raw[j] = u;
-        }
+        for (int j = 0; j < 8; j++) raw[j] = s4[j ^ (c & 7)];
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            const float4 p0 = raw[2 * k], p1 = raw[2 * k + 1];   // x0 x1 x2 x5 | x3 x6 x4 x7
+            const float4 p0 = raw[2 * k], p1 = raw[2 * k + 1];   // staged: x0 x1 x2 x5 | x3 x6 x4 x7
             raw[2 * k] = make_float4(p0.x, p0.y, p0.z, p1.x);
             raw[2 * k + 1] = make_float4(p1.z, p0.w, p1.y, p1.w);
         }
@@ -546,44 +548,29 @@ struct XRegS4 {
     __device__ __forceinline__ static float2 sub2(uint32_t a, uint32_t b) {
         return make_float2(__uint_as_float(a), __uint_as_float(b));
     }
-    __device__ __forceinline__ float dot(uint4 q) const {
-        float2 a01 = make_float2(0.f, 0.f), a25 = a01, a36 = a01, a47 = a01;
-        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t w = w4[k], b = w >> 12;
-            ffma2(a01, sub2(w & 0xFu, w & 0xF0u), make_float2(v[2 * k].x, v[2 * k].y));
-            ffma2(a25, sub2(w & 0xF00u, b & 0xF00u), make_float2(v[2 * k].z, v[2 * k].w));
-            ffma2(a36, sub2(w & 0xF000u, b & 0xF000u), make_float2(v[2 * k + 1].x, v[2 * k + 1].y));
-            ffma2(a47, sub2(w & 0xF0000u, b & 0xF0000u), make_float2(v[2 * k + 1].z, v[2 * k + 1].w));
-        }
-        return finish(a01, a25, a36, a47);
-    }
-    __device__ __forceinline__ float finish(float2 a01, float2 a25, float2 a36, float2 a47) const {
-        // classes p = 0, 4 | 8 | 12 | 16 -> factors 2^(49-p)
-        const float s = a01.x * 562949953421312.0f + a01.y * 35184372088832.0f + (a25.x + a25.y) * 2199023255552.0f +
-                        (a36.x + a36.y) * 137438953472.0f + (a47.x + a47.y) * 8589934592.0f;
-        return fmaf(-8.0f, xsum, (s * f1) * f2);
+    __device__ __forceinline__ float finish(float2 a, float2 b) const {
+        const float s = (a.x + a.y) + (b.x + b.y);
+        return fmaf(-8.0f, xsum, ((s * f1) * f2) * f3);
     }
     // four chunks against the same activations, interleaved word by word
     __device__ __forceinline__ void dot4(const uint4 (&q)[4], float (&out)[4]) const {
-        float2 a01[4], a25[4], a36[4], a47[4];
+        float2 a[4], b[4];
 #pragma unroll
-        for (int d = 0; d < 4; d++) a01[d] = a25[d] = a36[d] = a47[d] = make_float2(0.f, 0.f);
+        for (int d = 0; d < 4; d++) a[d] = b[d] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; k++) {
 #pragma unroll
             for (int d = 0; d < 4; d++) {
                 const uint32_t w = k == 0 ? q[d].x : k == 1 ? q[d].y : k == 2 ? q[d].z : q[d].w;
-                const uint32_t b = w >> 12;
-                ffma2(a01[d], sub2(w & 0xFu, w & 0xF0u), make_float2(v[2 * k].x, v[2 * k].y));
-                ffma2(a25[d], sub2(w & 0xF00u, b & 0xF00u), make_float2(v[2 * k].z, v[2 * k].w));
-                ffma2(a36[d], sub2(w & 0xF000u, b & 0xF000u), make_float2(v[2 * k + 1].x, v[2 * k + 1].y));
-                ffma2(a47[d], sub2(w & 0xF0000u, b & 0xF0000u), make_float2(v[2 * k + 1].z, v[2 * k + 1].w));
+                const uint32_t hi = w >> 12;
+                ffma2(a[d], sub2(w & 0xFu, w & 0xF0u), make_float2(v[2 * k].x, v[2 * k].y));
+                ffma2(b[d], sub2(w & 0xF00u, hi & 0xF00u), make_float2(v[2 * k].z, v[2 * k].w));
+                ffma2(a[d], sub2(w & 0xF000u, hi & 0xF000u), make_float2(v[2 * k + 1].x, v[2 * k + 1].y));
+                ffma2(b[d], sub2(w & 0xF0000u, hi & 0xF0000u), make_float2(v[2 * k + 1].z, v[2 * k + 1].w));
             }
         }
 #pragma unroll
-        for (int d = 0; d < 4; d++) out[d] = finish(a01[d], a25[d], a36[d], a47[d]);
+        for (int d = 0; d < 4; d++) out[d] = finish(a[d], b[d]);
     }
 };
 
