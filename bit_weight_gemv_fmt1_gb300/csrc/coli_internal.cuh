@@ -414,6 +414,7 @@ struct GemvJob {
     int row_start[MAXM + 1];   // prefix of O over matrices
     int n, fmt, I, cpr, S;
     const float *x;
+    int *err;                  // device error word (streamed matvec only)
 };
 
 cudaError_t launch_gemv(const GemvJob &job, cudaStream_t st, int *n_launch);
@@ -553,6 +554,8 @@ constexpr int kStreamXhBytes = 64 * 1024;     // staged x (phase A) or h of the 
 constexpr int kStreamRedBytes = 12 * 1024;
 constexpr int kStreamConsumerWarps = 12;
 size_t stream_decode_smem();
+size_t stream_gemv_smem();
+cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st);
 cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st);
 cudaError_t stream_decode_occupancy(int *per_sm);
 

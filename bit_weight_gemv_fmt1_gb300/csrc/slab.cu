@@ -970,6 +970,137 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
     }
 }
 
+
+// ------------------------------------------------------------------ matvec, S = 1, int4, streamed
+// The same streaming scheme as the decode block's phase A for coli_matmul at
+// S = 1: rows of all matrices of the call form one index space, CTA b owns a
+// contiguous block of rpc rows, warp 12 copies stages of RG rows (codes and
+// scales) into the ring, warps 0-11 own one 512-byte slab each with the
+// activations in registers and form four row dot products per stage.  fmt=4
+// reads the group scale of each 32-input chunk, fmt=2 the row scale.
+template <int NWC>
+__global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const GemvJob job, int rpc, int RG,
+                                                                         int gshift, long long timeout_ns) {
+    constexpr int NCT = NWC * 32, NS = kStreamStages, SB = kStreamStageBytes;
+    extern __shared__ uint8_t sraw[];
+    uint8_t *ring = (uint8_t *)(((uintptr_t)sraw + 127) & ~(uintptr_t)127);
+    float *red = reinterpret_cast<float *>(ring + NS * SB);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * SB + kStreamRedBytes);
+    uint64_t *empty = full + NS;
+    __shared__ volatile int abort_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int total = job.row_start[job.n];
+    const int r0 = blockIdx.x * rpc, r1 = min(total, r0 + rpc);
+    if (r0 >= r1) return;
+    const uint64_t deadline = global_ns() + (uint64_t)timeout_ns;
+    const int ns = (job.cpr + 31) >> 5, sl = warp % ns, sub = warp / ns, G = NWC / ns;
+    float4 xraw[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp < NWC && sl * 32 + lane < job.cpr) {
+        const float4 *p = reinterpret_cast<const float4 *>(job.x + (size_t)(sl * 32 + lane) * 32);
+#pragma unroll
+        for (int j = 0; j < 8; j++) xraw[j] = __ldg(p + j);
+    }
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < NS; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int ng = job.fmt == 4 ? job.ng[0] : 1;
+    const long long rs = job.rs[0];
+    // stage cursor: next row r, its matrix m
+    int r = r0, m = 0;
+    while (r >= job.row_start[m + 1]) m++;
+    auto next = [&](int &st_m, int &st_o, int &st_n) -> bool {
+        if (r >= r1) return false;
+        while (r >= job.row_start[m + 1]) m++;
+        st_m = m;
+        st_o = r - job.row_start[m];
+        st_n = min(RG, min(r1, job.row_start[m + 1]) - r);
+        r += st_n;
+        return true;
+    };
+    int sm_, so, sn;
+    if (warp == NWC) {
+        if (lane == 0) {
+            int s = 0, it = 0;
+            uint32_t ph = 0;
+            while (next(sm_, so, sn)) {
+                if (it >= NS && !mbar_wait(&empty[s], ph ^ 1, deadline, &abort_flag)) {
+                    if (!abort_flag) {
+                        abort_flag = 1;
+                        atomicCAS(job.err, 0, DEV_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                uint8_t *dst = ring + s * SB;
+                const uint32_t cb = (uint32_t)(sn * rs), sbytes = (uint32_t)(sn * ng * 4);
+                mbar_expect_tx(&full[s], cb + sbytes);
+                bulk_load(dst, job.q[sm_] + (size_t)so * rs, cb, &full[s]);
+                bulk_load(dst + RG * rs, job.s[sm_] + (size_t)so * ng, sbytes, &full[s]);
+                it++;
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int k = max(0, it - NS); k < it; k++) mbar_wait(&full[k % NS], (k / NS) & 1, dl2, &no_abort);
+        }
+        return;
+    }
+    XRegS4 xr;
+    xr.set(xraw);
+    int s = 0;
+    uint32_t ph = 0;
+    const int c = sl * 32 + lane;
+    const bool okc = c < job.cpr;
+    while (next(sm_, so, sn)) {
+        if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
+            const uint8_t *src = ring + s * SB;
+            uint4 qq[4];
+            float sc[4], dd[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int rr = sub + k * G;
+                const bool ok = okc && rr < sn;
+                qq[k] = ok ? *reinterpret_cast<const uint4 *>(src + rr * rs + c * 16) : make_uint4(0, 0, 0, 0);
+                sc[k] = ok ? *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (c >> gshift)) * 4) : 0.f;
+            }
+            xr.dot4(qq, dd);
+            const float t = warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
+            if ((lane & 7) == 0) {
+                const int rr = sub + (lane >> 3) * G;
+                if (rr < sn) red[(job.row_start[sm_] + so + rr - r0) * ns + sl] = t;
+            }
+        } else if (!abort_flag && lane == 0) {
+            abort_flag = 1;
+            atomicCAS(job.err, 0, DEV_ERR_TIMEOUT);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+    named_sync(1, NCT);
+    for (int rr = tid; rr < r1 - r0; rr += NCT) {
+        float acc = 0.f;
+        for (int k = 0; k < ns; k++) acc += red[rr * ns + k];
+        const int rg = r0 + rr;
+        int mm = 0;
+        while (rg >= job.row_start[mm + 1]) mm++;
+        job.y[mm][rg - job.row_start[mm]] = acc;
+    }
+}
+
 template <int FMT>
 cudaError_t slab_gemv_t(const GemvJob &job, int n_sm, int gshift, cudaStream_t st) {
     const int total = job.row_start[job.n];
@@ -1048,6 +1179,18 @@ cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+size_t stream_gemv_smem() { return (size_t)kStreamStages * kStreamStageBytes + kStreamRedBytes + 2 * kStreamStages * 8 + 128; }
+
+// rpc: rows per CTA (a multiple of 4); RG: rows per stage; gshift: chunk -> scale index shift
+cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st) {
+    auto kern = stream_gemv_kernel<kStreamConsumerWarps>;
+    const size_t smem = stream_gemv_smem();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, (kStreamConsumerWarps + 1) * 32, smem, st>>>(job, rpc, RG, gshift, 2000000000LL);
+    return cudaGetLastError();
 }
 
 // gs (fmt=4) usable by the slab kernels: a power-of-two number of 32-input chunks.

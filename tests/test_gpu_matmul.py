@@ -151,3 +151,42 @@ def test_repeat_is_bitwise_stable():
     a = _run(coli, torch, m, x)
     b = _run(coli, torch, m, x)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (4, 32), (2, 0)])
+def test_streamed_matvec_exact_integers(fmt, gs):
+    """S = 1 int4 with I a multiple of 128 takes the bulk-copy matvec; with
+    power-of-two scales and integer x every step is exact, so the result must
+    equal the oracle bit for bit (pins its group index, code placement and the
+    removal of the code offset)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(600 + fmt + gs)
+    O, I = 204, 3072
+    m = wl.random_matrix(g, fmt, O, I, gs)
+    m.scales = (2.0 ** g.integers(-2, 3, m.scales.size)).astype(np.float32)
+    x = g.integers(-8, 9, (1, I)).astype(np.float32)
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(fmt, gs, O, I, m.data, m.scales, x)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("fmt,gs", [(2, 0), (4, 64)])
+def test_streamed_matvec_multi(fmt, gs):
+    """Eight 2048 x 6144 matrices sharing one input (the weight-streaming
+    layer) in one call: rows of all matrices in one index space, CTA row
+    blocks that straddle matrices."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(700 + fmt)
+    mats = [wl.random_matrix(g, fmt, 2048, 6144, gs) for _ in range(3)]
+    mats = [mats[i % 3] for i in range(8)]
+    x = wl.activations(g, 1, 6144)
+    Ws = [upload(coli, mm) for mm in mats]
+    xd = torch.from_numpy(x).cuda()
+    ys = [torch.full((1, 2048), float("nan"), device="cuda") for _ in mats]
+    coli.matmul_multi(Ws, xd, ys)
+    coli.sync_check()
+    refs = [orc.matmul(fmt, gs, 2048, 6144, mm.data, mm.scales, x) for mm in mats[:3]]
+    for i, y in enumerate(ys):
+        assert norm_err(y.cpu().numpy(), refs[i % 3]) <= TOL
