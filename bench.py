@@ -520,7 +520,8 @@ def main():
             "config": {"workload": "moe_decode_block", "hidden": wk.H, "intermediate": wk.F, "experts": wk.E,
                        "topk": wk.K, "fmt": 4, "gs": 64, "S": 1, "global_batch": world,
                        "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2: 5.4 GB expert pool, fresh top-8 routing every step",
+                       "l2": f"inputs larger than L2: {wk.E * wl.expert_bytes(wk.H, wk.F, 4, 64) / 1e9:.2f} GB expert pool, fresh top-{wk.K} "
+                             "routing every step",
                        "bytes_per_step": wk.bytes_per_step},
             "hbm_frac_of_measured": value / peaks["hbm_gbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
