@@ -50,7 +50,7 @@ namespace {
 constexpr int BM = 128, BK = 64, BN = 64;
 constexpr int KB_PER_CS = 4;                          // K-blocks per codes stage: 128-byte row segments
 constexpr int NC = 5;                                 // codes stages (16 KB each): the HBM stream
-constexpr int NA = 4;                                 // dequantized A stages, in TMEM (32 columns each)
+constexpr int NAMAX = 8;                              // dequantized A stages, in TMEM (32 columns each)
 constexpr int NPL = 3;                                // activation planes
 constexpr int CODES_BYTES = BM * BK / 2 * KB_PER_CS;  // 16384: 128 rows x 128 B, 128-byte swizzle
 constexpr int PLANE_BYTES = BN * BK * 2;              // 8192: 64 rows x 128 B
@@ -58,13 +58,13 @@ constexpr int B_RING = 5 * NPL * PLANE_BYTES;         // 120 KB
 constexpr int NB1 = B_RING / PLANE_BYTES;             // plane stages with one plane: 15
 constexpr int NB3 = B_RING / (NPL * PLANE_BYTES);     // with three planes: 5
 constexpr int NBMAX = NB1;
-constexpr int NACCMAX = 6;
-constexpr uint32_t ACC_COLS = 384;                    // TMEM columns [0, 384): accumulators
-constexpr uint32_t A_COL0 = ACC_COLS;                 // [384, 512): NA A stages of 128 lanes x 64 bf16
+constexpr int NACCMAX = 4;
+// TMEM (512 columns): accumulators first, then the A stages.  One plane:
+// 4 accumulators of 64 columns + 8 A stages; three planes: 2 of 192 + 4.
 constexpr int OFF_B = 0;
 constexpr int OFF_CODES = OFF_B + B_RING;
 constexpr int OFF_BAR = OFF_CODES + NC * CODES_BYTES;
-constexpr int N_BAR = 2 * NC + 2 * NBMAX + 2 * NA + 2 * NACCMAX + 1;
+constexpr int N_BAR = 2 * NC + 2 * NBMAX + 2 * NAMAX + 2 * NACCMAX + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;   // + alignment slack
 constexpr int kDqWarps = 8;                           // dequant warps: two per weight row (half a K-block each)
 constexpr int kEpWarps = 4;                           // epilogue warps 8-11, one per TMEM lane quarter
@@ -191,7 +191,10 @@ template <int NT>
 __device__ __forceinline__ void run_roles(const PlaneMapSet &tmx, const TcArgs &a, uint8_t *smem, const Bars &B,
                                           uint32_t tmem, volatile int &abort_flag, uint64_t deadline) {
     constexpr int NB = NT == 1 ? NB1 : NB3;
-    constexpr int NACC = NT == 1 ? 6 : 2;             // TMEM accumulators of NT * 64 columns
+    constexpr int NACC = NT == 1 ? 4 : 2;             // TMEM accumulators of NT * 64 columns
+    constexpr int NA = NT == 1 ? 8 : 4;               // A stages of 32 columns
+    constexpr uint32_t A_COL0 = NACC * NT * BN;       // first A column
+    static_assert(A_COL0 + NA * (BK / 2) <= TMEM_COLS, "TMEM budget");
     constexpr int B_STAGE = NT * PLANE_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = a.tile_e ? *a.n_tiles : (a.P + BN - 1) / BN;
@@ -490,8 +493,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     B.b_full = B.c_empty + NC;
     B.b_empty = B.b_full + NBMAX;
     B.a_full = B.b_empty + NBMAX;
-    B.a_empty = B.a_full + NA;
-    B.acc_full = B.a_empty + NA;
+    B.a_empty = B.a_full + NAMAX;
+    B.acc_full = B.a_empty + NAMAX;
     B.acc_empty = B.acc_full + NACCMAX;
     B.done = B.acc_empty + NACCMAX;
     uint32_t *tmem_slot = (uint32_t *)(bars + N_BAR);
@@ -510,7 +513,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             mbar_init(&B.b_full[i], 1);
             mbar_init(&B.b_empty[i], 1);
         }
-        for (int i = 0; i < NA; i++) {
+        for (int i = 0; i < NAMAX; i++) {
             mbar_init(&B.a_full[i], kDqWarps);
             mbar_init(&B.a_empty[i], 1);
         }
