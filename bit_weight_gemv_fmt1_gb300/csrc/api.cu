@@ -345,6 +345,31 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
                 return COLI_OK;
             }
         }
+        // S = 2..4 of the same int4 formats: half-chunk lanes keep all S activation rows in registers
+        // (measured crossover against the row-pair kernel: S = 2 from ~16 MB of weights, S = 3-4 from ~4 MB)
+        bool stream_s = S >= 2 && S <= 4 && (W0->fmt == 4 || W0->fmt == 2) && W0->I % 128 == 0 &&
+                        ((uintptr_t)x & 15) == 0 && wbytes >= (S == 2 ? (16u << 20) : (4u << 20));
+        for (int m = 0; m < n && stream_s; m++)
+            stream_s = W0->fmt == 4 ? (W[m]->gs == W0->gs && slab_supported(4, W[m]->gs) && W[m]->ng % 4 == 0)
+                                    : W[m]->O % 4 == 0;
+        const int nh = (2 * W0->cpr + 31) / 32;
+        stream_s = stream_s && kStreamConsumerWarps % nh == 0;
+        if (stream_s) {
+            const int ng = W0->fmt == 4 ? W0->ng : 1;
+            const int RG = (int)(kStreamStageBytes / (W0->rs + 4 * ng)) / 4 * 4;
+            const int total = job.row_start[n];
+            int rpc = (total + ds->n_sm - 1) / ds->n_sm;
+            rpc = (rpc + 3) / 4 * 4;
+            const int grid = (total + rpc - 1) / rpc;
+            const int gshift = W0->fmt == 4 ? __builtin_ctz(W0->gs / 16) : 30;
+            if (RG >= 4 && (size_t)rpc * S * nh * 4 <= (size_t)kStreamGemvRedBytes &&
+                stream_gemv_s_smem() <= ds->smem_optin) {
+                e = launch_stream_gemv_s(job, rpc, RG, gshift, grid, st);
+                if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
+                count(1, wbytes);
+                return COLI_OK;
+            }
+        }
         if (slab && slab_gemv_smem(job, ds->n_sm) <= ds->smem_optin) {
             e = launch_slab_gemv(job, ds->n_sm, st);
             nl = 1;

@@ -555,6 +555,9 @@ constexpr int kStreamRedBytes = 12 * 1024;
 constexpr int kStreamConsumerWarps = 12;
 size_t stream_decode_smem();
 size_t stream_gemv_smem();
+constexpr int kStreamGemvRedBytes = 64 * 1024;   // partial sums of the S = 2..4 streamed matvec
+size_t stream_gemv_s_smem();
+cudaError_t launch_stream_gemv_s(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st);
 cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st);
 cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st);
 cudaError_t stream_decode_occupancy(int *per_sm);

@@ -1101,6 +1101,215 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
     }
 }
 
+
+// ------------------------------------------------------------------ matvec, S = 2..4, int4, streamed
+// As stream_gemv_kernel, but every lane covers half a chunk (8 bytes = 16
+// inputs) so that the activations of all S rows fit in registers: a warp owns a
+// 256-byte half slab of every row, decodes each code once and multiplies it
+// into S accumulators.  Activations are pre-scaled per lane and per code
+// position exactly as in XRegS4.
+template <int S>
+struct XRegHalf {
+    float4 v[S][4];     // per row: x * 2^(k-p), pairs in the order of the dot product
+    float xsum[S], f1[S], f2[S], f3[S];
+    __device__ __forceinline__ void set(int row, const float4 (&raw)[4]) {
+        float t = 0.f, mx = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float4 a = raw[j];
+            t += (a.x + a.y) + (a.z + a.w);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+        }
+        xsum[row] = t;
+        const int eb = (__float_as_int(mx) >> 23) & 0xFF;
+        const int ks = min(127, max(-126, 153 - eb));
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const float4 a = raw[2 * k], b = raw[2 * k + 1];
+            v[row][2 * k] =
+                make_float4(mul_exp2(a.x, ks), mul_exp2(a.y, ks - 4), mul_exp2(a.z, ks - 8), mul_exp2(b.y, ks - 8));
+            v[row][2 * k + 1] = make_float4(mul_exp2(a.w, ks - 12), mul_exp2(b.z, ks - 12), mul_exp2(b.x, ks - 16),
+                                            mul_exp2(b.w, ks - 16));
+        }
+        const int r = 149 - ks;
+        f1[row] = exp2i(r / 3);
+        f2[row] = exp2i(r / 3);
+        f3[row] = exp2i(r - 2 * (r / 3));
+    }
+    // dot products of N code half-chunks with the S rows: out[d][s]
+    template <int N>
+    __device__ __forceinline__ void dots(const uint2 (&q)[N], float (&out)[N][S]) const {
+        float2 acc[N][S];
+#pragma unroll
+        for (int d = 0; d < N; d++)
+#pragma unroll
+            for (int r = 0; r < S; r++) acc[d][r] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+#pragma unroll
+            for (int d = 0; d < N; d++) {
+                const uint32_t w = k == 0 ? q[d].x : q[d].y, hi = w >> 12;
+                const float2 c01 = XRegS4::sub2(w & 0xFu, w & 0xF0u), c25 = XRegS4::sub2(w & 0xF00u, hi & 0xF00u);
+                const float2 c36 = XRegS4::sub2(w & 0xF000u, hi & 0xF000u);
+                const float2 c47 = XRegS4::sub2(w & 0xF0000u, hi & 0xF0000u);
+#pragma unroll
+                for (int r = 0; r < S; r++) {
+                    ffma2(acc[d][r], c01, make_float2(v[r][2 * k].x, v[r][2 * k].y));
+                    ffma2(acc[d][r], c25, make_float2(v[r][2 * k].z, v[r][2 * k].w));
+                    ffma2(acc[d][r], c36, make_float2(v[r][2 * k + 1].x, v[r][2 * k + 1].y));
+                    ffma2(acc[d][r], c47, make_float2(v[r][2 * k + 1].z, v[r][2 * k + 1].w));
+                }
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < N; d++)
+#pragma unroll
+            for (int r = 0; r < S; r++)
+                out[d][r] = fmaf(-8.0f, xsum[r], (((acc[d][r].x + acc[d][r].y) * f1[r]) * f2[r]) * f3[r]);
+    }
+};
+
+template <int NWC, int S>
+__global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_s_kernel(const GemvJob job, int rpc, int RG,
+                                                                           int gshift, long long timeout_ns) {
+    constexpr int NCT = NWC * 32, NS = kStreamStages, SB = kStreamStageBytes;
+    extern __shared__ uint8_t sraw[];
+    uint8_t *ring = (uint8_t *)(((uintptr_t)sraw + 127) & ~(uintptr_t)127);
+    float *red = reinterpret_cast<float *>(ring + NS * SB);   // [rpc][S][nh]
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * SB + kStreamGemvRedBytes);
+    uint64_t *empty = full + NS;
+    __shared__ volatile int abort_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int total = job.row_start[job.n];
+    const int r0 = blockIdx.x * rpc, r1 = min(total, r0 + rpc);
+    if (r0 >= r1) return;
+    const uint64_t deadline = global_ns() + (uint64_t)timeout_ns;
+    const int hcpr = job.cpr * 2;                        // 8-byte half chunks per row
+    const int nh = (hcpr + 31) >> 5, sl = warp % nh, sub = warp / nh, G = NWC / nh;
+    const int hc = sl * 32 + lane;                       // this lane's half chunk
+    const bool okc = hc < hcpr;
+    XRegHalf<S> xr;
+    if (warp < NWC) {
+#pragma unroll
+        for (int r = 0; r < S; r++) {
+            float4 raw[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                raw[j] = okc ? __ldg(reinterpret_cast<const float4 *>(job.x + (size_t)r * job.I + (size_t)hc * 16) + j)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            xr.set(r, raw);
+        }
+    }
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < NS; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int ng = job.fmt == 4 ? job.ng[0] : 1;
+    const long long rs = job.rs[0];
+    int r = r0, m = 0;
+    while (r >= job.row_start[m + 1]) m++;
+    auto next = [&](int &st_m, int &st_o, int &st_n) -> bool {
+        if (r >= r1) return false;
+        while (r >= job.row_start[m + 1]) m++;
+        st_m = m;
+        st_o = r - job.row_start[m];
+        st_n = min(RG, min(r1, job.row_start[m + 1]) - r);
+        r += st_n;
+        return true;
+    };
+    int sm_, so, sn;
+    if (warp == NWC) {
+        if (lane == 0) {
+            int s = 0, it = 0;
+            uint32_t ph = 0;
+            while (next(sm_, so, sn)) {
+                if (it >= NS && !mbar_wait(&empty[s], ph ^ 1, deadline, &abort_flag)) {
+                    if (!abort_flag) {
+                        abort_flag = 1;
+                        atomicCAS(job.err, 0, DEV_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                uint8_t *dst = ring + s * SB;
+                const uint32_t cb = (uint32_t)(sn * rs), sbytes = (uint32_t)(sn * ng * 4);
+                mbar_expect_tx(&full[s], cb + sbytes);
+                bulk_load(dst, job.q[sm_] + (size_t)so * rs, cb, &full[s]);
+                bulk_load(dst + RG * rs, job.s[sm_] + (size_t)so * ng, sbytes, &full[s]);
+                it++;
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int k = max(0, it - NS); k < it; k++) mbar_wait(&full[k % NS], (k / NS) & 1, dl2, &no_abort);
+        }
+        return;
+    }
+    int s = 0;
+    uint32_t ph = 0;
+    while (next(sm_, so, sn)) {
+        if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
+            const uint8_t *src = ring + s * SB;
+            // this warp's rows of the stage, two at a time
+            for (int rr0 = sub; rr0 < sn; rr0 += 2 * G) {
+                uint2 qq[2];
+                float sc[2];
+#pragma unroll
+                for (int d = 0; d < 2; d++) {
+                    const int rr = rr0 + d * G;
+                    const bool ok = okc && rr < sn;
+                    qq[d] = ok ? *reinterpret_cast<const uint2 *>(src + rr * rs + hc * 8) : make_uint2(0, 0);
+                    sc[d] = ok ? *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (hc >> gshift)) * 4) : 0.f;
+                }
+                float dd[2][S];
+                xr.template dots<2>(qq, dd);
+                // reduce the 2*S values in groups of four
+#pragma unroll
+                for (int g4 = 0; g4 < (2 * S + 3) / 4; g4++) {
+                    float v4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const int idx = g4 * 4 + k;   // idx = d * S + row
+                        v4[k] = idx < 2 * S ? dd[idx / S][idx % S] * sc[idx / S] : 0.f;
+                    }
+                    const float t = warp_sum4(v4[0], v4[1], v4[2], v4[3], lane);
+                    const int idx = g4 * 4 + (lane >> 3);
+                    if ((lane & 7) == 0 && idx < 2 * S) {
+                        const int rr = rr0 + (idx / S) * G;
+                        if (rr < sn) red[((job.row_start[sm_] + so + rr - r0) * S + idx % S) * nh + sl] = t;
+                    }
+                }
+            }
+        } else if (!abort_flag && lane == 0) {
+            abort_flag = 1;
+            atomicCAS(job.err, 0, DEV_ERR_TIMEOUT);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+    named_sync(1, NCT);
+    for (int t = tid; t < (r1 - r0) * S; t += NCT) {
+        const int rr = t / S, row = t - rr * S;
+        float acc = 0.f;
+        for (int k = 0; k < nh; k++) acc += red[(rr * S + row) * nh + k];
+        const int rg = r0 + rr;
+        int mm = 0;
+        while (rg >= job.row_start[mm + 1]) mm++;
+        job.y[mm][(size_t)row * job.O[mm] + rg - job.row_start[mm]] = acc;
+    }
+}
+
 template <int FMT>
 cudaError_t slab_gemv_t(const GemvJob &job, int n_sm, int gshift, cudaStream_t st) {
     const int total = job.row_start[job.n];
@@ -1191,6 +1400,26 @@ cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, 
     if (e != cudaSuccess) return e;
     kern<<<grid, (kStreamConsumerWarps + 1) * 32, smem, st>>>(job, rpc, RG, gshift, 2000000000LL);
     return cudaGetLastError();
+}
+
+size_t stream_gemv_s_smem() {
+    return (size_t)kStreamStages * kStreamStageBytes + kStreamGemvRedBytes + 2 * kStreamStages * 8 + 128;
+}
+
+cudaError_t launch_stream_gemv_s(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st) {
+    const size_t smem = stream_gemv_s_smem();
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, (kStreamConsumerWarps + 1) * 32, smem, st>>>(job, rpc, RG, gshift, 2000000000LL);
+        return cudaGetLastError();
+    };
+    switch (job.S) {
+    case 2: return go(stream_gemv_s_kernel<kStreamConsumerWarps, 2>);
+    case 3: return go(stream_gemv_s_kernel<kStreamConsumerWarps, 3>);
+    case 4: return go(stream_gemv_s_kernel<kStreamConsumerWarps, 4>);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 // gs (fmt=4) usable by the slab kernels: a power-of-two number of 32-input chunks.

@@ -190,3 +190,21 @@ def test_streamed_matvec_multi(fmt, gs):
     refs = [orc.matmul(fmt, gs, 2048, 6144, mm.data, mm.scales, x) for mm in mats[:3]]
     for i, y in enumerate(ys):
         assert norm_err(y.cpu().numpy(), refs[i % 3]) <= TOL
+
+
+@pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (2, 0)])
+@pytest.mark.parametrize("S", [2, 3, 4])
+def test_streamed_small_s_exact_integers(fmt, gs, S):
+    """S = 2..4 int4 with I a multiple of 128 and >= 4 MB of weights takes the
+    half-chunk streamed matvec; power-of-two scales and integer x make every
+    step exact, so the result must equal the oracle bit for bit."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(800 + fmt + gs + S)
+    O, I = 5460, 6144   # > 16 MB of int4 weights: the streamed path for every S
+    m = wl.random_matrix(g, fmt, O, I, gs)
+    m.scales = (2.0 ** g.integers(-2, 3, m.scales.size)).astype(np.float32)
+    x = g.integers(-8, 9, (S, I)).astype(np.float32)
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(fmt, gs, O, I, m.data, m.scales, x)
+    assert np.array_equal(got, ref)
