@@ -559,6 +559,8 @@ constexpr int kStreamGemvRedBytes = 64 * 1024;   // partial sums of the S = 2..4
 size_t stream_gemv_s_smem();
 cudaError_t launch_stream_gemv_s(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st);
 cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st);
+int stream_lane_bytes(int fmt);
+int stream_lane_inputs(int fmt);
 cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st);
 cudaError_t stream_decode_occupancy(int *per_sm);
 

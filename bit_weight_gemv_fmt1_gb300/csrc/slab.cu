@@ -501,6 +501,8 @@ __device__ __forceinline__ float mul_exp2(float x, int e) {   // x * 2^e, -252 <
     return (x * exp2i(e / 2)) * exp2i(e - e / 2);
 }
 struct XRegS4 {
+    static constexpr int LB = 16, NIN = 32;   // code bytes and inputs per lane
+    using Q = uint4;
     float4 v[8];        // x * 2^(k-p), pairs in the order of dot()
     float xsum;         // sum of the chunk's 32 activations
     float f1, f2, f3;   // 2^(149-k) = f1 * f2 * f3
@@ -552,15 +554,16 @@ struct XRegS4 {
         const float s = (a.x + a.y) + (b.x + b.y);
         return fmaf(-8.0f, xsum, ((s * f1) * f2) * f3);
     }
-    // four chunks against the same activations, interleaved word by word
-    __device__ __forceinline__ void dot4(const uint4 (&q)[4], float (&out)[4]) const {
-        float2 a[4], b[4];
+    // N chunks against the same activations, interleaved word by word
+    template <int N>
+    __device__ __forceinline__ void dotn(const uint4 (&q)[N], float (&out)[N]) const {
+        float2 a[N], b[N];
 #pragma unroll
-        for (int d = 0; d < 4; d++) a[d] = b[d] = make_float2(0.f, 0.f);
+        for (int d = 0; d < N; d++) a[d] = b[d] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; k++) {
 #pragma unroll
-            for (int d = 0; d < 4; d++) {
+            for (int d = 0; d < N; d++) {
                 const uint32_t w = k == 0 ? q[d].x : k == 1 ? q[d].y : k == 2 ? q[d].z : q[d].w;
                 const uint32_t hi = w >> 12;
                 ffma2(a[d], sub2(w & 0xFu, w & 0xF0u), make_float2(v[2 * k].x, v[2 * k].y));
@@ -570,7 +573,127 @@ struct XRegS4 {
             }
         }
 #pragma unroll
-        for (int d = 0; d < 4; d++) out[d] = finish(a[d], b[d]);
+        for (int d = 0; d < N; d++) out[d] = finish(a[d], b[d]);
+    }
+    __device__ __forceinline__ void dot4(const uint4 (&q)[4], float (&out)[4]) const { dotn<4>(q, out); }
+};
+
+
+// int8 (stored offset binary u = code + 128), 16 inputs per lane: bytes 0, 1 of
+// a word at bit positions 0 and 8, bytes 2, 3 the same after a 16-bit shift;
+// the offset comes off as 128 * sum(x).  Same scaling as XRegS4.
+struct XRegS1 {
+    static constexpr int LB = 16, NIN = 16;
+    using Q = uint4;
+    float4 v[4];
+    float xsum, f1, f2, f3;
+    __device__ __forceinline__ void set(const float4 (&raw)[4]) {
+        float t = 0.f, mx = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float4 a = raw[j];
+            t += (a.x + a.y) + (a.z + a.w);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+        }
+        xsum = t;
+        const int eb = (__float_as_int(mx) >> 23) & 0xFF;
+        const int ks = min(127, max(-126, 153 - eb));
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            v[j] = make_float4(mul_exp2(raw[j].x, ks), mul_exp2(raw[j].y, ks - 8), mul_exp2(raw[j].z, ks),
+                               mul_exp2(raw[j].w, ks - 8));
+        const int r = 149 - ks;
+        f1 = exp2i(r / 3);
+        f2 = exp2i(r / 3);
+        f3 = exp2i(r - 2 * (r / 3));
+    }
+    template <int N>
+    __device__ __forceinline__ void dotn(const uint4 (&q)[N], float (&out)[N]) const {
+        float2 a[N], b[N];
+#pragma unroll
+        for (int d = 0; d < N; d++) a[d] = b[d] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+#pragma unroll
+            for (int d = 0; d < N; d++) {
+                const uint32_t w = k == 0 ? q[d].x : k == 1 ? q[d].y : k == 2 ? q[d].z : q[d].w;
+                const uint32_t hi = w >> 16;
+                ffma2(a[d], XRegS4::sub2(w & 0xFFu, w & 0xFF00u), make_float2(v[k].x, v[k].y));
+                ffma2(b[d], XRegS4::sub2(hi & 0xFFu, hi & 0xFF00u), make_float2(v[k].z, v[k].w));
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < N; d++) {
+            const float sm = (a[d].x + a[d].y) + (b[d].x + b[d].y);
+            out[d] = fmaf(-128.0f, xsum, ((sm * f1) * f2) * f3);
+        }
+    }
+};
+
+// int2 (crumb - 2), 32 inputs per lane = 8 code bytes: crumbs 0..10 of a word at
+// their own bit positions, 11..15 after a 12-bit shift; the offset comes off as
+// 2 * sum(x).  Same scaling as XRegS4.
+struct XRegS3 {
+    static constexpr int LB = 8, NIN = 32;
+    using Q = uint2;
+    float2 v[16];       // pair j of word k: v[8k + j]
+    float xsum, f1, f2, f3;
+    __device__ __forceinline__ static int pos(int t) { return t <= 10 ? 2 * t : 2 * t - 12; }
+    __device__ __forceinline__ void set(const float4 (&raw)[8]) {
+        float xs[32];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            xs[4 * j] = raw[j].x;
+            xs[4 * j + 1] = raw[j].y;
+            xs[4 * j + 2] = raw[j].z;
+            xs[4 * j + 3] = raw[j].w;
+        }
+        float t = 0.f, mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+            t += xs[i];
+            mx = fmaxf(mx, fabsf(xs[i]));
+        }
+        xsum = t;
+        const int eb = (__float_as_int(mx) >> 23) & 0xFF;
+        const int ks = min(127, max(-126, 153 - eb));
+#pragma unroll
+        for (int k = 0; k < 2; k++)
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                v[8 * k + j] = make_float2(mul_exp2(xs[16 * k + 2 * j], ks - pos(2 * j)),
+                                           mul_exp2(xs[16 * k + 2 * j + 1], ks - pos(2 * j + 1)));
+        const int r = 149 - ks;
+        f1 = exp2i(r / 3);
+        f2 = exp2i(r / 3);
+        f3 = exp2i(r - 2 * (r / 3));
+    }
+    template <int N>
+    __device__ __forceinline__ void dotn(const uint2 (&q)[N], float (&out)[N]) const {
+        float2 a[N], b[N];
+#pragma unroll
+        for (int d = 0; d < N; d++) a[d] = b[d] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+#pragma unroll
+            for (int d = 0; d < N; d++) {
+                const uint32_t w = k == 0 ? q[d].x : q[d].y, hi = w >> 12;
+                const float2 *vk = v + 8 * k;
+                ffma2(a[d], XRegS4::sub2(w & 0x3u, w & 0xCu), vk[0]);
+                ffma2(b[d], XRegS4::sub2(w & 0x30u, w & 0xC0u), vk[1]);
+                ffma2(a[d], XRegS4::sub2(w & 0x300u, w & 0xC00u), vk[2]);
+                ffma2(b[d], XRegS4::sub2(w & 0x3000u, w & 0xC000u), vk[3]);
+                ffma2(a[d], XRegS4::sub2(w & 0x30000u, w & 0xC0000u), vk[4]);
+                ffma2(b[d], XRegS4::sub2(w & 0x300000u, hi & 0xC00u), vk[5]);
+                ffma2(a[d], XRegS4::sub2(hi & 0x3000u, hi & 0xC000u), vk[6]);
+                ffma2(b[d], XRegS4::sub2(hi & 0x30000u, hi & 0xC0000u), vk[7]);
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < N; d++) {
+            const float sm = (a[d].x + a[d].y) + (b[d].x + b[d].y);
+            out[d] = fmaf(-2.0f, xsum, ((sm * f1) * f2) * f3);
+        }
     }
 };
 
@@ -978,7 +1101,7 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
 // scales) into the ring, warps 0-11 own one 512-byte slab each with the
 // activations in registers and form four row dot products per stage.  fmt=4
 // reads the group scale of each 32-input chunk, fmt=2 the row scale.
-template <int NWC>
+template <int NWC, class XR>
 __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const GemvJob job, int rpc, int RG,
                                                                          int gshift, long long timeout_ns) {
     constexpr int NCT = NWC * 32, NS = kStreamStages, SB = kStreamStageBytes;
@@ -993,14 +1116,16 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
     const int r0 = blockIdx.x * rpc, r1 = min(total, r0 + rpc);
     if (r0 >= r1) return;
     const uint64_t deadline = global_ns() + (uint64_t)timeout_ns;
-    const int ns = (job.cpr + 31) >> 5, sl = warp % ns, sub = warp / ns, G = NWC / ns;
-    float4 xraw[8];
+    // lane units: XR::LB code bytes = XR::NIN inputs; a row has lpr of them
+    const int lpr = (job.I + XR::NIN - 1) / XR::NIN;
+    const int ns = (lpr + 31) >> 5, sl = warp % ns, sub = warp / ns, G = NWC / ns;
+    float4 xraw[XR::NIN / 4];
 #pragma unroll
-    for (int j = 0; j < 8; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (warp < NWC && sl * 32 + lane < job.cpr) {
-        const float4 *p = reinterpret_cast<const float4 *>(job.x + (size_t)(sl * 32 + lane) * 32);
+    for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp < NWC && sl * 32 + lane < lpr) {
+        const float4 *p = reinterpret_cast<const float4 *>(job.x + (size_t)(sl * 32 + lane) * XR::NIN);
 #pragma unroll
-        for (int j = 0; j < 8; j++) xraw[j] = __ldg(p + j);
+        for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = __ldg(p + j);
     }
     if (tid == 0) {
         abort_flag = 0;
@@ -1055,25 +1180,26 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
         }
         return;
     }
-    XRegS4 xr;
+    XR xr;
     xr.set(xraw);
     int s = 0;
     uint32_t ph = 0;
     const int c = sl * 32 + lane;
-    const bool okc = c < job.cpr;
+    const bool okc = c < lpr;
+    using Q = typename XR::Q;
     while (next(sm_, so, sn)) {
         if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
             const uint8_t *src = ring + s * SB;
-            uint4 qq[4];
+            Q qq[4];
             float sc[4], dd[4];
 #pragma unroll
             for (int k = 0; k < 4; k++) {
                 const int rr = sub + k * G;
                 const bool ok = okc && rr < sn;
-                qq[k] = ok ? *reinterpret_cast<const uint4 *>(src + rr * rs + c * 16) : make_uint4(0, 0, 0, 0);
+                qq[k] = ok ? *reinterpret_cast<const Q *>(src + rr * rs + c * XR::LB) : Q{};
                 sc[k] = ok ? *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (c >> gshift)) * 4) : 0.f;
             }
-            xr.dot4(qq, dd);
+            xr.template dotn<4>(qq, dd);
             const float t = warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
             if ((lane & 7) == 0) {
                 const int rr = sub + (lane >> 3) * G;
@@ -1394,13 +1520,25 @@ size_t stream_gemv_smem() { return (size_t)kStreamStages * kStreamStageBytes + k
 
 // rpc: rows per CTA (a multiple of 4); RG: rows per stage; gshift: chunk -> scale index shift
 cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st) {
-    auto kern = stream_gemv_kernel<kStreamConsumerWarps>;
     const size_t smem = stream_gemv_smem();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, (kStreamConsumerWarps + 1) * 32, smem, st>>>(job, rpc, RG, gshift, 2000000000LL);
-    return cudaGetLastError();
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, (kStreamConsumerWarps + 1) * 32, smem, st>>>(job, rpc, RG, gshift, 2000000000LL);
+        return cudaGetLastError();
+    };
+    switch (job.fmt) {
+    case 1: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS1>);
+    case 2:
+    case 4: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS4>);
+    case 3: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS3>);
+    default: return cudaErrorInvalidValue;
+    }
 }
+
+// code bytes and inputs of one lane of the streamed S = 1 matvec, per format (0: not streamed)
+int stream_lane_bytes(int fmt) { return fmt == 1 ? XRegS1::LB : fmt == 3 ? XRegS3::LB : (fmt == 2 || fmt == 4) ? XRegS4::LB : 0; }
+int stream_lane_inputs(int fmt) { return fmt == 1 ? XRegS1::NIN : fmt == 3 ? XRegS3::NIN : (fmt == 2 || fmt == 4) ? XRegS4::NIN : 0; }
 
 size_t stream_gemv_s_smem() {
     return (size_t)kStreamStages * kStreamStageBytes + kStreamGemvRedBytes + 2 * kStreamStages * 8 + 128;

@@ -153,7 +153,7 @@ def test_repeat_is_bitwise_stable():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (4, 32), (2, 0)])
+@pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (4, 32), (2, 0), (1, 0), (3, 0)])
 def test_streamed_matvec_exact_integers(fmt, gs):
     """S = 1 int4 with I a multiple of 128 takes the bulk-copy matvec; with
     power-of-two scales and integer x every step is exact, so the result must
@@ -162,7 +162,7 @@ def test_streamed_matvec_exact_integers(fmt, gs):
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
     g = wl.rng(600 + fmt + gs)
-    O, I = 204, 3072
+    O, I = {1: 700, 3: 2800}.get(fmt, 1404), 6144   # >= 4 MB of weights: the streamed path
     m = wl.random_matrix(g, fmt, O, I, gs)
     m.scales = (2.0 ** g.integers(-2, 3, m.scales.size)).astype(np.float32)
     x = g.integers(-8, 9, (1, I)).astype(np.float32)
@@ -171,7 +171,7 @@ def test_streamed_matvec_exact_integers(fmt, gs):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("fmt,gs", [(2, 0), (4, 64)])
+@pytest.mark.parametrize("fmt,gs", [(2, 0), (4, 64), (1, 0), (3, 0)])
 def test_streamed_matvec_multi(fmt, gs):
     """Eight 2048 x 6144 matrices sharing one input (the weight-streaming
     layer) in one call: rows of all matrices in one index space, CTA row
