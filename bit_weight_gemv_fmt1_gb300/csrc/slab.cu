@@ -697,6 +697,36 @@ struct XRegS3 {
     }
 };
 
+
+// f32 weights, 16 inputs per lane (64 contiguous bytes): plain f32x2 FMAs.
+struct Q4 {
+    uint4 v[4];
+};
+struct XRegF32 {
+    static constexpr int LB = 64, NIN = 16;
+    using Q = Q4;
+    float4 x[4];
+    __device__ __forceinline__ void set(const float4 (&raw)[4]) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) x[j] = raw[j];
+    }
+    template <int N>
+    __device__ __forceinline__ void dotn(const Q4 (&q)[N], float (&out)[N]) const {
+#pragma unroll
+        for (int d = 0; d < N; d++) {
+            float2 a = make_float2(0.f, 0.f), b = a;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                ffma2(a, make_float2(__uint_as_float(q[d].v[j].x), __uint_as_float(q[d].v[j].y)),
+                      make_float2(x[j].x, x[j].y));
+                ffma2(b, make_float2(__uint_as_float(q[d].v[j].z), __uint_as_float(q[d].v[j].w)),
+                      make_float2(x[j].z, x[j].w));
+            }
+            out[d] = (a.x + a.y) + (b.x + b.y);
+        }
+    }
+};
+
 // Sums of four per-lane values over the warp with 6 shuffles: afterwards lane
 // 8k (k = 0..3) holds the total of value k.
 __device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v3, int lane) {
@@ -1136,7 +1166,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const int ng = job.fmt == 4 ? job.ng[0] : 1;
+    const int ng = job.fmt == 4 ? job.ng[0] : job.fmt == 0 ? 0 : 1;   // scales per row (none for f32)
     const long long rs = job.rs[0];
     // stage cursor: next row r, its matrix m
     int r = r0, m = 0;
@@ -1167,7 +1197,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
                 const uint32_t cb = (uint32_t)(sn * rs), sbytes = (uint32_t)(sn * ng * 4);
                 mbar_expect_tx(&full[s], cb + sbytes);
                 bulk_load(dst, job.q[sm_] + (size_t)so * rs, cb, &full[s]);
-                bulk_load(dst + RG * rs, job.s[sm_] + (size_t)so * ng, sbytes, &full[s]);
+                if (sbytes) bulk_load(dst + RG * rs, job.s[sm_] + (size_t)so * ng, sbytes, &full[s]);
                 it++;
                 if (++s == NS) {
                     s = 0;
@@ -1197,7 +1227,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
                 const int rr = sub + k * G;
                 const bool ok = okc && rr < sn;
                 qq[k] = ok ? *reinterpret_cast<const Q *>(src + rr * rs + c * XR::LB) : Q{};
-                sc[k] = ok ? *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (c >> gshift)) * 4) : 0.f;
+                sc[k] = !ok ? 0.f : ng == 0 ? 1.f : *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (c >> gshift)) * 4);
             }
             xr.template dotn<4>(qq, dd);
             const float t = warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
@@ -1528,6 +1558,7 @@ cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, 
         return cudaGetLastError();
     };
     switch (job.fmt) {
+    case 0: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegF32>);
     case 1: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS1>);
     case 2:
     case 4: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS4>);
@@ -1537,8 +1568,12 @@ cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, 
 }
 
 // code bytes and inputs of one lane of the streamed S = 1 matvec, per format (0: not streamed)
-int stream_lane_bytes(int fmt) { return fmt == 1 ? XRegS1::LB : fmt == 3 ? XRegS3::LB : (fmt == 2 || fmt == 4) ? XRegS4::LB : 0; }
-int stream_lane_inputs(int fmt) { return fmt == 1 ? XRegS1::NIN : fmt == 3 ? XRegS3::NIN : (fmt == 2 || fmt == 4) ? XRegS4::NIN : 0; }
+int stream_lane_bytes(int fmt) {
+    return fmt == 0 ? XRegF32::LB : fmt == 1 ? XRegS1::LB : fmt == 3 ? XRegS3::LB : XRegS4::LB;
+}
+int stream_lane_inputs(int fmt) {
+    return fmt == 0 ? XRegF32::NIN : fmt == 1 ? XRegS1::NIN : fmt == 3 ? XRegS3::NIN : XRegS4::NIN;
+}
 
 size_t stream_gemv_s_smem() {
     return (size_t)kStreamStages * kStreamStageBytes + kStreamGemvRedBytes + 2 * kStreamStages * 8 + 128;

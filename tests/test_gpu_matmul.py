@@ -171,7 +171,7 @@ def test_streamed_matvec_exact_integers(fmt, gs):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("fmt,gs", [(2, 0), (4, 64), (1, 0), (3, 0)])
+@pytest.mark.parametrize("fmt,gs", [(2, 0), (4, 64), (1, 0), (3, 0), (0, 0)])
 def test_streamed_matvec_multi(fmt, gs):
     """Eight 2048 x 6144 matrices sharing one input (the weight-streaming
     layer) in one call: rows of all matrices in one index space, CTA row
