@@ -27,6 +27,10 @@
  *        scatter-add of the expert outputs.
  *   [E]  colibri-strix commit log, "fuse shared expert into GPU block": the
  *        shared expert is one more expert with weight 1.0 over all rows.
+ *   [R]  colibri-strix commit log, "metal: full decode layer in ONE command
+ *        buffer": the router is an f32 matvec followed by a sigmoid, then an
+ *        exact top-K selection -- greedy argmax over sigmoid + bias with the
+ *        CPU's tie order -- with top-p truncation, norm_topk and routed_scale.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   - element 2j of an int4 row is the LOW nibble of byte j;
@@ -36,7 +40,17 @@
  *   - group g covers inputs [g*gs, min((g+1)*gs, I)), ng = ceil(I/gs);
  *   - silu(g) = g / (1 + exp(-g));
  *   - routing weights are used as given; id -1 is an empty slot; y is
- *     overwritten; routing order is a stable sort of slots (s asc, k asc).
+ *     overwritten; routing order is a stable sort of slots (s asc, k asc);
+ *   - router top-K ([R]): the score of expert e is sigmoid(logit_e), computed
+ *     in double and rounded to f32; the selection key is score + bias in f32;
+ *     the greedy argmax breaks ties toward the lower id; a selected expert's
+ *     weight is its score (the bias only steers the choice); top-p keeps the
+ *     leading experts (selection order) while the f32 running sum of scores
+ *     before each is below top_p * (f32 sum of the K scores), top_p <= 0 or
+ *     >= 1 keeps all K; the rest become empty slots (id -1, weight 0);
+ *     norm_topk divides the kept weights by their f32 sum; routed_scale then
+ *     multiplies them.  Every decision and every weight is taken in f32, one
+ *     rounding per operation (this file is compiled without FMA contraction).
  */
 #include <math.h>
 #include <stddef.h>
@@ -371,4 +385,80 @@ int oracle_moe_block(int64_t H, int64_t F, int64_t S, int64_t K, int64_t n_exper
     free(acc);
     free(h);
     return ORACLE_OK;
+}
+
+/* Router top-K ([R]) for S rows of n_experts logits (f32 [S][E]); bias is
+ * f32 [E] or NULL.  ids/w receive [S][K].  See the reading in the header. */
+int oracle_moe_topk(const float *logits, const float *bias, int64_t S, int64_t E, int64_t K,
+                    float top_p, int norm_topk, float routed_scale, int32_t *ids, float *w)
+{
+    if (S < 0 || E < 1 || K < 1 || K > E)
+        return ORACLE_EINVAL;
+    float *score = (float *)malloc(sizeof(float) * (size_t)E);
+    float *key = (float *)malloc(sizeof(float) * (size_t)E);
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    if (!score || !key || !taken) {
+        free(score); free(key); free(taken);
+        return ORACLE_EINVAL;
+    }
+    for (int64_t s = 0; s < S; s++) {
+        const float *l = logits + s * E;
+        for (int64_t e = 0; e < E; e++) {
+            score[e] = (float)(1.0 / (1.0 + exp(-(double)l[e])));
+#if ORACLE_MUTATION == 9
+            key[e] = score[e];                              /* planted: bias ignored */
+#else
+            key[e] = score[e] + (bias ? bias[e] : 0.0f);
+#endif
+            taken[e] = 0;
+        }
+        int32_t *id = ids + s * K;
+        float *wt = w + s * K;
+        for (int64_t k = 0; k < K; k++) {                 /* greedy argmax */
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; e++) {
+                if (taken[e])
+                    continue;
+#if ORACLE_MUTATION == 8
+                if (best < 0 || key[e] >= key[best])        /* planted: ties go to the higher id */
+#else
+                if (best < 0 || key[e] > key[best])
+#endif
+                    best = e;
+            }
+            taken[best] = 1;
+            id[k] = (int32_t)best;
+            wt[k] = score[best];
+        }
+        int64_t keep = K;                                   /* top-p truncation */
+        if (top_p > 0.0f && top_p < 1.0f) {
+            float total = 0.0f;
+            for (int64_t k = 0; k < K; k++)
+                total = total + wt[k];
+            const float limit = top_p * total;
+            float cum = 0.0f;
+            keep = 0;
+            for (int64_t k = 0; k < K; k++) {
+                if (!(cum < limit))
+                    break;
+                cum = cum + wt[k];
+                keep++;
+            }
+        }
+        for (int64_t k = keep; k < K; k++) {
+            id[k] = -1;
+            wt[k] = 0.0f;
+        }
+        if (norm_topk) {
+            float sum = 0.0f;
+            for (int64_t k = 0; k < keep; k++)
+                sum = sum + wt[k];
+            for (int64_t k = 0; k < keep; k++)
+                wt[k] = wt[k] / sum;
+        }
+        for (int64_t k = 0; k < keep; k++)
+            wt[k] = wt[k] * routed_scale;
+    }
+    free(score); free(key); free(taken);
+    return 0;
 }

@@ -44,7 +44,7 @@ def build(mutation: int = 0, openmp: bool = True) -> str:
     if os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
         return out
     tmp = out + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm",
            f"-DORACLE_MUTATION={mutation}"]
     if openmp:
         cmd.insert(1, "-fopenmp")
@@ -74,6 +74,8 @@ def lib(mutation: int = 0) -> ctypes.CDLL:
             L.oracle_route.restype = _i64
             L.oracle_route.argtypes = [_ptr, _i64, _i64, _i64, _ptr, _ptr]
             L.oracle_moe_block.restype = ctypes.c_int
+            L.oracle_moe_topk.argtypes = [_ptr, _ptr, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int,
+                                          ctypes.c_float, _ptr, _ptr]
             L.oracle_moe_block.argtypes = [_i64, _i64, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, _ptr,
                                            _ptr, _ptr, _ptr]
             L.oracle_threads.restype = ctypes.c_int
@@ -192,3 +194,18 @@ def moe_block(H: int, F: int, experts, x, ids, w, mutation: int = 0, want=("y",)
     if rc:
         raise ValueError("oracle_moe_block rejected its arguments")
     return y if want == ("y",) else tuple({"y": y, "y64": y64}[k] for k in want)
+
+
+def moe_topk(logits, K: int, bias=None, top_p: float = 0.0, norm_topk: bool = False, routed_scale: float = 1.0,
+             mutation: int = 0):
+    """Router top-K of f32 logits [S, E]: (ids [S, K] int32, w [S, K] f32)."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    S, E = logits.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    ids = np.empty((S, K), dtype=np.int32)
+    w = np.empty((S, K), dtype=np.float32)
+    rc = lib(mutation).oracle_moe_topk(_p(logits), _p(b), S, E, K, float(top_p), int(bool(norm_topk)),
+                                       float(routed_scale), _p(ids), _p(w))
+    if rc:
+        raise ValueError("oracle_moe_topk rejected its arguments")
+    return ids, w

@@ -307,10 +307,65 @@ def pin_moe_invariants(mutation=0):
     return bool(np.allclose(yd[0], 2 * want, rtol=1e-12, atol=1e-12))
 
 
+def _sig32(l):
+    """sigmoid in double, rounded to f32 (math.exp, element by element)."""
+    return np.array([1.0 / (1.0 + math.exp(-float(v))) for v in np.ravel(l)], np.float32).reshape(np.shape(l))
+
+
+def pin_topk_worked_example(mutation=0):
+    """Five logits worked by hand: ties go to the lower id, the bias steers the
+    choice but not the weight, top-p keeps the smallest leading set that reaches
+    the mass, then norm_topk and routed_scale."""
+    l = np.array([[0.0, 1.0, 2.0, 2.0, -1.0]], np.float32)
+    sg = _sig32(l[0])
+    ids, w = orc.moe_topk(l, 3, mutation=mutation)
+    if ids.tolist() != [[2, 3, 1]] or not np.array_equal(w[0], sg[[2, 3, 1]]):
+        return False
+    ids, w = orc.moe_topk(l, 3, bias=np.array([0, 0, 0, 0, 1], np.float32), mutation=mutation)
+    if ids.tolist() != [[4, 2, 3]] or not np.array_equal(w[0], sg[[4, 2, 3]]):
+        return False
+    # mass of the three: 2*sig(2) + sig(1); half of it is reached after two
+    ids, w = orc.moe_topk(l, 3, top_p=0.5, norm_topk=True, routed_scale=2.5, mutation=mutation)
+    return ids.tolist() == [[2, 3, -1]] and np.array_equal(w[0], np.array([1.25, 1.25, 0.0], np.float32))
+
+
+def pin_topk_vs_sort(mutation=0):
+    """Greedy argmax equals a stable sort by (-key, id) (brute force), with
+    planted ties and a bias; top-p keeps exactly the shortest prefix whose score
+    mass reaches top_p of the K scores; norm_topk sums to one."""
+    g = wl.rng(77)
+    S, E, K = 40, 37, 6
+    l = g.normal(0, 1.5, (S, E)).astype(np.float32)
+    l[:, 5] = l[:, 9]                      # exact ties in every row
+    l[:, 20] = l[:, 11]
+    b = g.normal(0, 0.1, E).astype(np.float32)
+    b[9] = b[5]
+    b[20] = b[11]
+    ids, w = orc.moe_topk(l, K, bias=b, mutation=mutation)
+    sg = _sig32(l)
+    key = (sg + b[None, :]).astype(np.float32)
+    for s in range(S):
+        order = sorted(range(E), key=lambda e: (-float(key[s, e]), e))[:K]
+        if ids[s].tolist() != order or not np.array_equal(w[s], sg[s, order]):
+            return False
+    ids2, w2 = orc.moe_topk(l, K, bias=b, top_p=0.7, norm_topk=True, mutation=mutation)
+    for s in range(S):
+        sc = sg[s, ids[s]].astype(np.float64)
+        kept = int((ids2[s] >= 0).sum())
+        if kept < 1 or ids2[s, :kept].tolist() != ids[s, :kept].tolist() or np.any(ids2[s, kept:] != -1):
+            return False
+        total = sc.sum()
+        if sc[:kept].sum() < 0.7 * total * (1 - 1e-6) or sc[:kept - 1].sum() >= 0.7 * total * (1 + 1e-6):
+            return False
+        if abs(float(w2[s, :kept].astype(np.float64).sum()) - 1.0) > 1e-6 or np.any(w2[s, kept:] != 0):
+            return False
+    return True
+
+
 PINS = [pin_golden_layout, pin_expert_bytes, pin_all_bytes_brute, pin_exact_integer_cases,
         pin_random_vs_library, pin_int8_unit_scale, pin_fmt4_wide_group_is_fmt2, pin_inline_order,
         pin_scale_linearity, pin_partial_last_group, pin_silu_closed_form, pin_route_vs_sorted,
-        pin_moe_composition, pin_moe_invariants]
+        pin_moe_composition, pin_moe_invariants, pin_topk_worked_example, pin_topk_vs_sort]
 
 MUTATIONS = {
     1: "int4 nibble order swapped",
@@ -320,4 +375,6 @@ MUTATIONS = {
     5: "last term of the dot product dropped",
     6: "silu sign error",
     7: "routing weight dropped",
+    8: "router ties go to the higher id",
+    9: "router selection ignores the bias",
 }
