@@ -51,6 +51,8 @@ _lib.coli_matmul_multi.argtypes = [_int, ctypes.POINTER(_vp), _vp, ctypes.POINTE
 _lib.coli_moe_route.argtypes = [_vp, _int, _int, _int, _vp, _vp, _vp]
 _lib.coli_moe_block.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp]
 _lib.coli_moe_block_noalloc.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp, _vp]
+_lib.coli_moe_topk.argtypes = [_vp, _vp, _int, _int, _int, ctypes.c_float, _int, ctypes.c_float, _vp, _vp, _vp]
+_lib.coli_moe_router.argtypes = [_vp, _int, _vp, _vp, _int, ctypes.c_float, _int, ctypes.c_float, _vp, _vp, _vp]
 _lib.coli_sync_check.argtypes = [_vp]
 _lib.coli_get_stats.argtypes = [ctypes.POINTER(_Stats)]
 _lib.coli_get_stats.restype = None
@@ -59,8 +61,9 @@ _lib.coli_set_fail_after.argtypes = [_i64]
 _lib.coli_set_fail_after.restype = None
 
 EXPORTS = ("coli_tensor_upload", "coli_tensor_free", "coli_tensor_info", "coli_matmul", "coli_matmul_multi",
-           "coli_moe_route", "coli_moe_block", "coli_moe_block_noalloc", "coli_sync_check", "coli_last_error", "coli_get_stats",
-           "coli_reset_stats", "coli_set_fail_after", "coli_version")
+           "coli_moe_route", "coli_moe_topk", "coli_moe_router", "coli_moe_block", "coli_moe_block_noalloc",
+           "coli_sync_check", "coli_last_error", "coli_get_stats", "coli_reset_stats", "coli_set_fail_after",
+           "coli_version")
 
 
 class ColiError(RuntimeError):
@@ -151,6 +154,24 @@ def moe_route(ids, n_experts: int, offsets, order, stream=None):
     _check(_lib.coli_moe_route(_ptr(ids), int(S), int(K), int(n_experts), _ptr(offsets), _ptr(order),
                                _stream(stream)))
     return offsets, order
+
+
+def moe_topk(logits, K: int, ids, w, bias=None, top_p: float = 0.0, norm_topk: bool = False,
+             routed_scale: float = 1.0, stream=None):
+    """Router top-K of device f32 logits [S, E] into ids [S, K] int32 and w [S, K] f32 (see coli.h)."""
+    S, E = logits.shape
+    _check(_lib.coli_moe_topk(_ptr(logits), _ptr(bias), int(S), int(E), int(K), float(top_p), int(bool(norm_topk)),
+                              float(routed_scale), _ptr(ids), _ptr(w), _stream(stream)))
+    return ids, w
+
+
+def moe_router(x, router: Tensor, K: int, ids, w, bias=None, top_p: float = 0.0, norm_topk: bool = False,
+               routed_scale: float = 1.0, stream=None):
+    """logits = x @ router^T, then moe_topk (one call, see coli.h)."""
+    S = x.shape[0]
+    _check(_lib.coli_moe_router(_ptr(x), int(S), router.handle, _ptr(bias), int(K), float(top_p),
+                                int(bool(norm_topk)), float(routed_scale), _ptr(ids), _ptr(w), _stream(stream)))
+    return ids, w
 
 
 class ExpertTable:

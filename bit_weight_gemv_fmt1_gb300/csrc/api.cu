@@ -73,9 +73,11 @@ void count(int launches, uint64_t wbytes) {
 
 // ------------------------------------------------------------------ device state
 struct Workspace {
-    unsigned *bar = nullptr;      // grid barrier words [2]
+    unsigned *bar = nullptr;      // grid barrier words (kBarrierBytes)
     void *buf = nullptr;          // scratch
     size_t cap = 0;
+    void *rbuf = nullptr;         // router logits (kept apart from buf, which the router matvec may use)
+    size_t rcap = 0;
 };
 
 struct CachedTable {
@@ -115,6 +117,24 @@ int device_state(DeviceState **out) {
     d->smem_optin = (size_t)optin;
     g_dev[dev] = d;
     *out = d;
+    return COLI_OK;
+}
+
+// Router-logit scratch of at least `bytes` for this stream (grown like workspace()).
+int router_scratch(DeviceState *d, cudaStream_t st, size_t bytes, float **out) {
+    std::lock_guard<std::mutex> lk(d->mu);
+    Workspace &w = d->ws[st];
+    if (w.rcap < bytes) {
+        if (w.rbuf) {
+            CU(cudaDeviceSynchronize(), "cudaDeviceSynchronize(router scratch growth)");
+            CU(cudaFree(w.rbuf), "cudaFree(router scratch)");
+            w.rbuf = nullptr;
+            w.rcap = 0;
+        }
+        CU(cudaMalloc(&w.rbuf, bytes), "cudaMalloc(router scratch)");
+        w.rcap = bytes;
+    }
+    *out = (float *)w.rbuf;
     return COLI_OK;
 }
 
@@ -503,6 +523,49 @@ int coli_moe_route(const int32_t *ids, int S, int K, int n_experts, int32_t *off
     if (e != cudaSuccess) return cuda_fail(e, "routing launch");
     count(1, 0);
     return COLI_OK;
+}
+
+int coli_moe_topk(const float *logits, const float *bias, int S, int n_experts, int K, float top_p, int norm_topk,
+                  float routed_scale, int32_t *ids, float *w, void *stream) {
+    g_msg[0] = 0;
+    if (int rc = check_ptr(logits, "logits")) return rc;
+    if (bias && ((uintptr_t)bias & 3)) return fail(COLI_EINVAL, "bias is not 4-byte aligned");
+    if (int rc = check_ptr(ids, "ids")) return rc;
+    if (int rc = check_ptr(w, "w")) return rc;
+    if (n_experts < 1 || n_experts > 16384)
+        return fail(COLI_EINVAL, "n_experts must be in 1..16384 (got %d)", n_experts);
+    if (S < 1 || K < 1 || K > 64 || K > n_experts)
+        return fail(COLI_EINVAL, "need S >= 1 and 1 <= K <= min(64, n_experts) (got S=%d K=%d)", S, K);
+    if (!(top_p == top_p) || !(routed_scale == routed_scale))
+        return fail(COLI_EINVAL, "top_p and routed_scale must not be NaN");
+    if (int rc = injected()) return rc;
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    if (topk_smem(n_experts) > ds->smem_optin) return fail(COLI_EINVAL, "n_experts too large for one block");
+    cudaError_t e = launch_topk(logits, bias, S, n_experts, K, top_p, norm_topk, routed_scale, ids, w,
+                                (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "router top-K launch");
+    count(1, 0);
+    return COLI_OK;
+}
+
+int coli_moe_router(const float *x, int S, const coli_tensor *router, const float *bias, int K, float top_p,
+                    int norm_topk, float routed_scale, int32_t *ids, float *w, void *stream) {
+    g_msg[0] = 0;
+    if (int rc = check_tensor(router, "router")) return rc;
+    if (int rc = check_ptr(x, "x")) return rc;
+    if (router->O > 16384) return fail(COLI_EINVAL, "the router has more than 16384 experts");
+    if (S < 1) return fail(COLI_EINVAL, "S must be >= 1 (got %d)", S);
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    // logits go to a scratch buffer of their own (the stream's workspace is used by the matvec)
+    float *logits = nullptr;
+    if (int rc = router_scratch(ds, st, (size_t)S * router->O * sizeof(float), &logits)) return rc;
+    float *ys[1] = {logits};
+    const coli_tensor *Ws[1] = {router};
+    if (int rc = coli_matmul_multi(1, Ws, x, ys, S, stream)) return rc;
+    return coli_moe_topk(logits, bias, S, (int)router->O, K, top_p, norm_topk, routed_scale, ids, w, stream);
 }
 
 // ------------------------------------------------------------------ expert block

@@ -564,6 +564,10 @@ int stream_lane_inputs(int fmt);
 cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st);
 cudaError_t stream_decode_occupancy(int *per_sm);
 
+size_t topk_smem(int E);
+cudaError_t launch_topk(const float *logits, const float *bias, int S, int E, int K, float top_p, int norm_topk,
+                        float routed_scale, int32_t *ids, float *w, cudaStream_t st);
+
 bool slab_supported(int fmt, int gs);
 size_t slab_gemv_smem(const GemvJob &job, int n_sm);
 cudaError_t launch_slab_gemv(const GemvJob &job, int n_sm, cudaStream_t st);

@@ -160,6 +160,43 @@ int coli_moe_route(const int32_t *ids, int S, int K, int n_experts, int32_t *off
                    void *stream);
 
 /*
+ * Router top-K: the routing coli_moe_block consumes, computed on the device
+ * (colibri-strix commit log, "metal: full decode layer in ONE command buffer":
+ * sigmoid of the router logits, exact greedy top-K over sigmoid + bias with the
+ * CPU tie order, --topp truncation, norm_topk, routed_scale).  Per row s:
+ *   score_e = sigmoid(logits[s][e])        (double, rounded to f32)
+ *   key_e   = score_e + bias[e]            (f32; bias NULL means 0)
+ *   K rounds pick the largest remaining key, ties to the lower id;
+ *   ids[s][k] = the k-th pick, w[s][k] = its score (the bias only steers).
+ *   top_p in (0, 1): keep the leading picks while the f32 running sum of the
+ *   scores before each is below top_p * (f32 sum of the K scores); the rest
+ *   become empty slots (id -1, weight 0).  top_p <= 0 or >= 1 keeps all K.
+ *   norm_topk != 0: divide the kept weights by their f32 sum.
+ *   Then multiply the kept weights by routed_scale.
+ * Every decision and weight is the f32 value of these steps (one rounding per
+ * operation), so the result is the same on every run.
+ *   logits   device f32 [S][n_experts] (finite values).
+ *   bias     device f32 [n_experts] or NULL.
+ *   ids, w   device int32 / f32 [S][K], overwritten.
+ *   S >= 1, 1 <= n_experts <= 16384, 1 <= K <= min(64, n_experts).
+ * Errors: COLI_EINVAL (NULL/misaligned pointer, sizes, NaN top_p or
+ * routed_scale), COLI_EDEVICE, COLI_ECUDA.
+ */
+int coli_moe_topk(const float *logits, const float *bias, int S, int n_experts, int K, float top_p,
+                  int norm_topk, float routed_scale, int32_t *ids, float *w, void *stream);
+
+/*
+ * The router of the pages' decode layer in one call: logits = x * router^T
+ * (coli_matmul_multi with the uploaded router matrix, [n_experts][H], any
+ * format; the pages' router is f32, fmt=0), then coli_moe_topk.  The logits
+ * live in a library scratch buffer per stream.
+ *   x        device f32 [S][H].
+ *   Other arguments and errors as coli_moe_topk and coli_matmul.
+ */
+int coli_moe_router(const float *x, int S, const coli_tensor *router, const float *bias, int K, float top_p,
+                    int norm_topk, float routed_scale, int32_t *ids, float *w, void *stream);
+
+/*
  * The routed-expert block (colibri-strix commit log, "metal: batched
  * moe_block"; the shared expert is one more expert with weight 1 for every
  * row, "fuse shared expert into GPU block"):
