@@ -9,8 +9,8 @@ packed codes and scales of the 8 routed experts plus x and y, divided by the
 device time.  The 5.4 GB expert pool is far larger than L2 and every step
 routes to a fresh random set, so no step finds its weights in L2.
 
-Other workloads (--workload): gemv_single, gemv_sweep, moe_prefill,
-streaming.  --impl reference times the CPU oracle (the reference arm of this
+Other workloads (--workload): gemv_sweep, moe_prefill, streaming, router
+(all four are also in the by_workload part of a full run).  --impl reference times the CPU oracle (the reference arm of this
 benchmark) on a bounded sample of the same workload.
 
 Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
@@ -343,6 +343,59 @@ def bench_streaming(coli, torch, peaks, tokens=10):
     return res
 
 
+def bench_router(coli, torch, peaks, steps=200):
+    """Device-side router of the decode workload: logits of a 256 x 6144 f32
+    router, sigmoid + bias greedy top-8 with norm_topk (coli_moe_router), alone
+    and followed by the expert block (the whole routed-expert layer on the GPU,
+    no host step between)."""
+    c = wl.MOE_DECODE
+    g = wl.rng(c["seed"] + 100)
+    H, F, E, K = c["H"], c["F"], c["E"], c["K"]
+    Wr = g.normal(0.0, 0.05, (E, H)).astype(np.float32)
+    router = coli.tensor_upload(0, 0, E, H, Wr, None)
+    bias = torch.from_numpy(g.normal(0.0, 0.01, E).astype(np.float32)).cuda()
+    n_pool = 64
+    hosts = [wl.expert(g, H, F, c["fmt"], c["gs"]) for _ in range(8)]
+    dev = [tuple(coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in hosts[e % 8])
+           for e in range(n_pool)]
+    table = coli.ExpertTable(dev + [dev[e % n_pool] for e in range(E - n_pool)])
+    xs = torch.randn(steps, 1, H, device="cuda")
+    ids = torch.empty((1, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((1, K), device="cuda")
+    y = torch.empty((1, H), device="cuda")
+    st = torch.cuda.Stream()
+
+    def timed(fn):
+        with torch.cuda.stream(st):
+            for i in range(3):
+                fn(i)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            for i in range(steps):
+                fn(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            a.record(st)
+            graph.replay()
+            b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / steps
+
+    t_router = timed(lambda i: coli.moe_router(xs[i], router, K, ids, w, bias=bias, norm_topk=True, stream=st))
+    t_layer = timed(lambda i: (coli.moe_router(xs[i], router, K, ids, w, bias=bias, norm_topk=True, stream=st),
+                               coli.moe_block(xs[i], table, ids, w, y, stream=st)))
+    coli.sync_check()
+    rb = E * H * 4
+    return {"router_us": t_router * 1e6, "router_GB/s": rb / t_router / 1e9,
+            "router_plus_expert_block_us": t_layer * 1e6,
+            "note": "S=1, f32 router 256x6144, top-8 of sigmoid+bias with norm_topk; expert block over a "
+                    "64-expert resident pool (L2 sees part of it: the block time here is not the headline)"}
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle, timed as it stands, on a bounded
     sample of the default workload: one routed (row, expert) slot per step."""
@@ -414,7 +467,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--workload", default="moe_decode", choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming"),
+    ap.add_argument("--workload", default="moe_decode",
+                    choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming", "router"),
                     help="moe_decode is the headline line; the others print their own line (for profiling)")
     ap.add_argument("--experts-prefill", type=int, default=None, help="resident experts of the prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -442,6 +496,8 @@ def main():
             elif args.workload == "gemv_sweep":
                 l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
                 res = bench_gemv(coli, torch, peaks, l2)
+            elif args.workload == "router":
+                res = bench_router(coli, torch, peaks)
             else:
                 res = bench_streaming(coli, torch, peaks)
             print(json.dumps({"workload": args.workload, "result": res}), flush=True)
@@ -509,7 +565,7 @@ def main():
     if rank == 0 and not args.quick:
         l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
         by_wl = {"gemv": bench_gemv(coli, torch, peaks, l2), "moe_prefill": bench_prefill(coli, torch, peaks),
-                 "weight_streaming": bench_streaming(coli, torch, peaks)}
+                 "weight_streaming": bench_streaming(coli, torch, peaks), "router": bench_router(coli, torch, peaks)}
 
     if rank == 0:
         line = {
