@@ -31,6 +31,10 @@
  *        buffer": the router is an f32 matvec followed by a sigmoid, then an
  *        exact top-K selection -- greedy argmax over sigmoid + bias with the
  *        CPU's tie order -- with top-p truncation, norm_topk and routed_scale.
+ *   [P]  PR #298 page, commit message on qt_addrow / qt_matvec_rows (fmt=7):
+ *        an fp8 "passthrough" format holding one raw byte per element (the
+ *        byte convention of fmt=1) and ceil(O/128) * ceil(I/128) per-block
+ *        f32 scales; a [130,130] tensor has 4 blocks.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   - element 2j of an int4 row is the LOW nibble of byte j;
@@ -50,7 +54,13 @@
  *     >= 1 keeps all K; the rest become empty slots (id -1, weight 0);
  *     norm_topk divides the kept weights by their f32 sum; routed_scale then
  *     multiplies them.  Every decision and every weight is taken in f32, one
- *     rounding per operation (this file is compiled without FMA contraction).
+ *     rounding per operation (this file is compiled without FMA contraction);
+ *   - fmt=7 ([P]): the byte of element (o, i) is an OCP FP8 E4M3 number (sign,
+ *     4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal;
+ *     no infinities; S.1111.111 is NaN), multiplied by the scale of block
+ *     (o / 128, i / 128); the scales are stored block-row major,
+ *     s[(o / 128) * ceil(I / 128) + i / 128]; blocks at the right and bottom
+ *     edges are partial.  The gs argument is ignored for fmt=7.
  */
 #include <math.h>
 #include <stddef.h>
@@ -91,18 +101,20 @@ int64_t oracle_row_bytes(int fmt, int64_t I)
     case 2: return (I + 1) / 2;
     case 3: return (I + 3) / 4;
     case 4: return (I + 1) / 2;
+    case 7: return I;
     default: return -1;
     }
 }
 
 /* Number of f32 scales: none for fmt=0, one per row for fmt 1-3, O*ceil(I/gs)
- * for fmt=4 ([C]). */
+ * for fmt=4 ([C]), one per 128 x 128 block for fmt=7 ([P]). */
 int64_t oracle_scale_count(int fmt, int gs, int64_t O, int64_t I)
 {
     switch (fmt) {
     case 0: return 0;
     case 1: case 2: case 3: return O;
     case 4: return gs > 0 ? O * ((I + gs - 1) / gs) : -1;
+    case 7: return ((O + 127) / 128) * ((I + 127) / 128);
     default: return -1;
     }
 }
@@ -141,6 +153,26 @@ static int oracle_code(int fmt, int64_t I, const uint8_t *q, int64_t o, int64_t 
     }
 }
 
+/* Value of one OCP FP8 E4M3 byte, from the format's definition: normal
+ * numbers (-1)^s 2^(e-7) (1 + m/8), subnormals (-1)^s 2^-6 (m/8), NaN for
+ * exponent and mantissa all ones. */
+double oracle_fp8_value(int byte)
+{
+    const int sgn = (byte >> 7) & 1, e = (byte >> 3) & 15, m = byte & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+#if ORACLE_MUTATION == 11
+    v = ldexp(1.0 + m / 8.0, e - 7);                        /* planted: subnormals read as normals */
+#else
+    if (e == 0)
+        v = ldexp(m / 8.0, -6);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+#endif
+    return sgn ? -v : v;
+}
+
 /* Scale of element (o, i). */
 static double oracle_scale(int fmt, int gs, int64_t I, const float *s, int64_t o, int64_t i)
 {
@@ -158,6 +190,14 @@ static double oracle_scale(int fmt, int gs, int64_t I, const float *s, int64_t o
         return (double)s[o * ng + i / gs];
 #endif
     }
+    case 7: {
+        const int64_t nbr = (I + 127) / 128;               /* blocks per block-row */
+#if ORACLE_MUTATION == 10
+        return (double)s[(i / 128) * nbr + o / 128];       /* planted: transposed block index */
+#else
+        return (double)s[(o / 128) * nbr + i / 128];
+#endif
+    }
     default:
         return 1.0;
     }
@@ -170,12 +210,14 @@ static double oracle_weight(int fmt, int gs, int64_t I, const void *data, const 
 {
     if (fmt == 0)
         return (double)((const float *)data)[o * I + i];
+    if (fmt == 7)
+        return oracle_fp8_value(((const uint8_t *)data)[o * I + i]) * oracle_scale(fmt, gs, I, s, o, i);
     return (double)oracle_code(fmt, I, (const uint8_t *)data, o, i) * oracle_scale(fmt, gs, I, s, o, i);
 }
 
 static int oracle_check(int fmt, int gs, int64_t O, int64_t I)
 {
-    if (fmt < 0 || fmt > 4 || O < 1 || I < 1)
+    if (fmt < 0 || (fmt > 4 && fmt != 7) || O < 1 || I < 1)
         return ORACLE_EINVAL;
     if (fmt == 4 && (gs < 2 || (gs & 1)))
         return ORACLE_EINVAL;
@@ -226,7 +268,8 @@ int oracle_matmul(int fmt, int gs, int64_t O, int64_t I, const void *data, const
 /* The same product in the evaluation order the pages give for the kernels
  * ([M] Shader paragraph, [C]): fmt 1-3 multiply the row scale once after the
  * integer-code dot product; fmt=4 forms each group's code dot product and
- * folds the group scale in before summing over groups.  Mathematically equal
+ * folds the group scale in before summing over groups; fmt=7 does the same per
+ * 128-input block with the scale of the row's block.  Mathematically equal
  * to oracle_matmul; used to pin that equality. */
 int oracle_matmul_inline(int fmt, int gs, int64_t O, int64_t I, const void *data,
                          const float *scales, int64_t S, const float *x, double *y64)
@@ -251,6 +294,15 @@ int oracle_matmul_inline(int fmt, int gs, int64_t O, int64_t I, const void *data
                     for (int64_t i = i0; i < i1; i++)
                         part += (double)oracle_code(fmt, I, q, o, i) * (double)xs[i];
                     acc += (double)scales[o * ng + g] * part;
+                }
+            } else if (fmt == 7) {
+                const int64_t nb = (I + 127) / 128;
+                for (int64_t b = 0; b < nb; b++) {
+                    const int64_t i1 = (b * 128 + 128 < I) ? b * 128 + 128 : I;
+                    double part = 0.0;
+                    for (int64_t i = b * 128; i < i1; i++)
+                        part += oracle_fp8_value(q[o * I + i]) * (double)xs[i];
+                    acc += (double)scales[(o / 128) * nb + b] * part;
                 }
             } else {
                 double part = 0.0;

@@ -157,13 +157,17 @@ def pin_inline_order(mutation=0):
     """Group scale folded in per group equals dequantize-then-multiply, within
     1e-14 of the sum of |terms|."""
     g = wl.rng(15)
-    for fmt, gs, O, I in ((4, 64, 6, 500), (4, 16, 4, 97), (2, 0, 5, 99), (1, 0, 5, 77), (3, 0, 4, 70)):
-        codes = _raw(g, fmt, O, I)
-        sc = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(fmt, O, I, gs))
+    for fmt, gs, O, I in ((4, 64, 6, 500), (4, 16, 4, 97), (2, 0, 5, 99), (1, 0, 5, 77), (3, 0, 4, 70),
+                          (7, 0, 260, 300)):
+        if fmt == 7:
+            m = wl.random_matrix(g, 7, O, I)
+            data, sc = m.data, m.scales
+        else:
+            data = wl.pack(fmt, _raw(g, fmt, O, I))
+            sc = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(fmt, O, I, gs))
         x = g.standard_normal((2, I)).astype(np.float32)
-        y64, mag = orc.matmul(fmt, gs, O, I, wl.pack(fmt, codes), sc, x, mutation=mutation,
-                              want=("y64", "yabs"))
-        yi = orc.matmul_inline(fmt, gs, O, I, wl.pack(fmt, codes), sc, x, mutation=mutation)
+        y64, mag = orc.matmul(fmt, gs, O, I, data, sc, x, mutation=mutation, want=("y64", "yabs"))
+        yi = orc.matmul_inline(fmt, gs, O, I, data, sc, x, mutation=mutation)
         if not np.all(np.abs(y64 - yi) <= 1e-14 * mag):
             return False
     return True
@@ -362,10 +366,88 @@ def pin_topk_vs_sort(mutation=0):
     return True
 
 
+def _e4m3_library(b):
+    """FP8 E4M3 bytes decoded by PyTorch's float8_e4m3fn dtype (f64)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(b, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_fp8_block_count(mutation=0):
+    """tests/golden/fp8_blocks.txt: the scale count the pages print for fmt=7,
+    and one byte per element."""
+    for line in open(os.path.join(GOLDEN, "fp8_blocks.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        lhs, rhs = line.split("->")
+        O, I = (int(t) for t in lhs.split())
+        if orc.scale_count(7, 0, O, I, mutation) != int(rhs) or orc.row_bytes(7, I, mutation) != I:
+            return False
+    return True
+
+
+def pin_fp8_all_bytes(mutation=0):
+    """All 256 E4M3 bytes at unit scale against PyTorch's float8_e4m3fn
+    conversion (NaN at the same two bytes), plus the format's closed-form
+    landmarks: largest finite 448 (0x7E), smallest subnormal 2^-9 (0x01),
+    smallest normal 2^-6 (0x08), 1.0 (0x38), -2 (0xC0)."""
+    b = np.arange(256, dtype=np.uint8).reshape(1, -1)
+    got = orc.dequant(7, 0, 1, 256, b, np.ones(2, np.float32), mutation=mutation)[0]
+    want = _e4m3_library(b[0])
+    if not np.array_equal(np.isnan(got), np.isnan(want)) or not np.array_equal(got[~np.isnan(got)],
+                                                                               want[~np.isnan(want)]):
+        return False
+    marks = {0x7E: 448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0xC0: -2.0, 0x00: 0.0}
+    return all(got[k] == v for k, v in marks.items()) and bool(np.isnan(got[0x7F]) and np.isnan(got[0xFF]))
+
+
+def pin_fp8_block_structure(mutation=0):
+    """Brute force over the blocks of a 300 x 130 fmt=7 tensor (3 x 2 blocks,
+    partial at the bottom and right): with only block (bo, bi)'s scale set to
+    0.5, the dequantized matrix is 0.5 * the library-decoded bytes inside that
+    block and zero everywhere else."""
+    g = wl.rng(18)
+    O, I = 300, 130
+    m = wl.random_matrix(g, 7, O, I)
+    dec = _e4m3_library(m.data)
+    nbo, nbi = wl.n_groups(O, 128), wl.n_groups(I, 128)
+    for bo in range(nbo):
+        for bi in range(nbi):
+            sc = np.zeros(nbo * nbi, np.float32)
+            sc[bo * nbi + bi] = 0.5
+            got = orc.dequant(7, 0, O, I, m.data, sc, mutation=mutation)
+            want = np.zeros((O, I))
+            want[bo * 128:(bo + 1) * 128, bi * 128:(bi + 1) * 128] = 0.5 * dec[bo * 128:(bo + 1) * 128,
+                                                                               bi * 128:(bi + 1) * 128]
+            if not np.array_equal(got, want):
+                return False
+    return True
+
+
+def pin_fp8_unit_scale_vs_library(mutation=0):
+    """fmt=7 with every block scale 1 is a plain matvec of the decoded bytes:
+    numpy f64 over the library decode, within 1e-12 of the sum of |terms|;
+    scaling every block by 2 doubles y exactly."""
+    g = wl.rng(19)
+    O, I = 259, 385
+    m = wl.random_matrix(g, 7, O, I)
+    x = g.standard_normal((3, I)).astype(np.float32)
+    ones = np.ones(wl.scale_count(7, O, I, 0), np.float32)
+    dec = _e4m3_library(m.data)
+    y64, mag = orc.matmul(7, 0, O, I, m.data, ones, x, mutation=mutation, want=("y64", "yabs"))
+    want = x.astype(np.float64) @ dec.T
+    if not np.all(np.abs(y64 - want) <= 1e-12 * mag):
+        return False
+    y2, = orc.matmul(7, 0, O, I, m.data, 2 * ones, x, mutation=mutation, want=("y64",))
+    return bool(np.array_equal(y2, 2 * y64))
+
+
 PINS = [pin_golden_layout, pin_expert_bytes, pin_all_bytes_brute, pin_exact_integer_cases,
         pin_random_vs_library, pin_int8_unit_scale, pin_fmt4_wide_group_is_fmt2, pin_inline_order,
         pin_scale_linearity, pin_partial_last_group, pin_silu_closed_form, pin_route_vs_sorted,
-        pin_moe_composition, pin_moe_invariants, pin_topk_worked_example, pin_topk_vs_sort]
+        pin_moe_composition, pin_moe_invariants, pin_topk_worked_example, pin_topk_vs_sort,
+        pin_fp8_block_count, pin_fp8_all_bytes, pin_fp8_block_structure, pin_fp8_unit_scale_vs_library]
 
 MUTATIONS = {
     1: "int4 nibble order swapped",
@@ -377,4 +459,6 @@ MUTATIONS = {
     7: "routing weight dropped",
     8: "router ties go to the higher id",
     9: "router selection ignores the bias",
+    10: "fmt=7 block index transposed",
+    11: "fmt=7 subnormals read as normals",
 }

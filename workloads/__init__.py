@@ -14,7 +14,10 @@ Host byte layout (the library's upload input):
   fmt=3  int2 offset binary (value = crumb - 2), rows of ceil(I/4) bytes,
          element 4j+t in bits [2t, 2t+1] of byte j
   fmt=4  as fmt=2, plus f32 scales [O][ceil(I/gs)]
-Scales are f32: [O] for fmt 1-3, [O][ceil(I/gs)] for fmt=4, none for fmt=0.
+  fmt=7  one FP8 E4M3 byte per element, row-major [O][I], plus f32 scales
+         [ceil(O/128)][ceil(I/128)], one per 128 x 128 block
+Scales are f32: [O] for fmt 1-3, [O][ceil(I/gs)] for fmt=4, per block for
+fmt=7, none for fmt=0.
 """
 from __future__ import annotations
 
@@ -25,6 +28,8 @@ import numpy as np
 
 CODE_RANGE = {1: (-128, 127), 2: (0, 15), 3: (0, 3), 4: (0, 15)}
 OFFSET = {1: 0, 2: 8, 3: 2, 4: 8}
+FP8_BLOCK = 128                       # fmt=7 scale block edge (rows and inputs)
+FP8_NAN = (0x7F, 0xFF)                # the two E4M3 NaN bytes
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -32,7 +37,7 @@ def rng(seed: int) -> np.random.Generator:
 
 
 def row_bytes(fmt: int, I: int) -> int:
-    return {0: 4 * I, 1: I, 2: (I + 1) // 2, 3: (I + 3) // 4, 4: (I + 1) // 2}[fmt]
+    return {0: 4 * I, 1: I, 2: (I + 1) // 2, 3: (I + 3) // 4, 4: (I + 1) // 2, 7: I}[fmt]
 
 
 def n_groups(I: int, gs: int) -> int:
@@ -44,6 +49,8 @@ def scale_count(fmt: int, O: int, I: int, gs: int) -> int:
         return 0
     if fmt == 4:
         return O * n_groups(I, gs)
+    if fmt == 7:
+        return n_groups(O, FP8_BLOCK) * n_groups(I, FP8_BLOCK)
     return O
 
 
@@ -94,6 +101,11 @@ def random_matrix(g: np.random.Generator, fmt: int, O: int, I: int, gs: int = 0,
     f32 scales (the single-GEMV recipe); fmt=0 draws N(0, 0.02) weights."""
     if fmt == 0:
         return Matrix(0, 0, O, I, g.normal(0.0, 0.02, (O, I)).astype(np.float32), None)
+    if fmt == 7:
+        # uniform over the 254 non-NaN bytes: every finite E4M3 value, subnormals included
+        v = g.integers(0, 254, (O, I))
+        data = (v + (v >= 0x7F)).astype(np.uint8)   # 0..0x7E, 0x80..0xFE
+        return Matrix(7, 0, O, I, data, log_uniform(g, scale_lo, scale_hi, scale_count(7, O, I, 0)))
     if fmt in (2, 4):
         # two independent uniform nibbles per byte
         data = np.frombuffer(g.bytes(O * row_bytes(fmt, I)), dtype=np.uint8).reshape(O, -1).copy()
