@@ -264,6 +264,9 @@ def bench_gemv(coli, torch, peaks, l2_bytes):
     for fmt, gs in wl.GEMV_SWEEP["variants"]:
         name = f"sweep_fmt{fmt}" + (f"_g{gs}" if fmt == 4 else "")
         cases.append((name, fmt, gs, wl.GEMV_SWEEP["O"], wl.GEMV_SWEEP["I"], wl.GEMV_SWEEP["S"], wl.GEMV_SWEEP["seed"]))
+    # FP8 E4M3 with 128 x 128 block scales (uniform over the finite bytes), same shape
+    cases.append(("fp8_fmt7_b128", 7, 0, wl.GEMV_SWEEP["O"], wl.GEMV_SWEEP["I"], wl.GEMV_SWEEP["S"],
+                  wl.GEMV_SWEEP["seed"]))
     for name, fmt, gs, O, I, Ss, seed in cases:
         g = wl.rng(seed + fmt + gs)
         if name.startswith("sweep"):

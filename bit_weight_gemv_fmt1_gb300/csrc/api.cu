@@ -179,6 +179,7 @@ int64_t host_row_bytes(int fmt, int64_t I) {
     case 1: return I;
     case 2: case 4: return (I + 1) / 2;
     case 3: return (I + 3) / 4;
+    case 7: return I;
     default: return -1;
     }
 }
@@ -188,8 +189,8 @@ MatDesc desc_of(const coli_tensor *t) {
     m.q = t->q;
     m.s = t->s;
     m.rs = t->rs;
-    m.gs = t->fmt == 4 ? t->gs : 0;
-    m.ng = t->fmt == 4 ? t->ng : 1;
+    m.gs = t->fmt == 4 ? t->gs : t->fmt == 7 ? kFp8Block : 0;
+    m.ng = t->ng;
     m.tmap = t->tmap;
     return m;
 }
@@ -228,7 +229,8 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
     g_msg[0] = 0;
     if (!out) return fail(COLI_EINVAL, "out is NULL");
     *out = nullptr;
-    if (fmt < 0 || fmt > 4) return fail(COLI_EFMT, "unknown weight format %d (supported: 0..4)", fmt);
+    if (fmt < 0 || (fmt > 4 && fmt != 7))
+        return fail(COLI_EFMT, "unknown weight format %d (supported: 0..4, 7)", fmt);
     if (fmt == 4 && (gs < 2 || (gs & 1)))
         return fail(COLI_EFMT, "fmt=4 needs an even group size >= 2, got gs=%d", gs);
     if (O < 1 || I < 1) return fail(COLI_EINVAL, "O and I must be >= 1 (got O=%lld I=%lld)", (long long)O, (long long)I);
@@ -246,11 +248,14 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
     t->gs = fmt == 4 ? gs : 0;
     t->O = O;
     t->I = I;
-    t->ng = fmt == 4 ? (int)((I + gs - 1) / gs) : 1;
+    t->ng = fmt == 4 ? (int)((I + gs - 1) / gs) : fmt == 7 ? (int)((I + kFp8Block - 1) / kFp8Block) : 1;
     const int64_t hrb = host_row_bytes(fmt, I);
     t->rs = (hrb + 15) / 16 * 16;
     t->cpr = (int)((I + epc_of(fmt) - 1) / epc_of(fmt));
-    const int64_t n_scales = fmt == 0 ? 0 : (fmt == 4 ? O * t->ng : O);
+    const int64_t n_scales = fmt == 0   ? 0
+                             : fmt == 4 ? O * t->ng
+                             : fmt == 7 ? (O + kFp8Block - 1) / kFp8Block * t->ng
+                                        : O;
     t->alg_bytes = O * hrb + 4 * n_scales;
     t->dev_bytes = O * t->rs + 4 * n_scales;
     t->uid = g_uid++;

@@ -4,12 +4,14 @@
 //   q  : O rows of `rs` bytes, rs = row_bytes rounded up to 16; the padding is
 //        zero.  fmt=1 bytes are stored offset binary (b ^ 0x80) so that every
 //        integer format decodes as (unsigned code - offset).  fmt 2/3/4 keep
-//        the host nibble/crumb order; fmt=0 keeps the f32 values.
-//   s  : f32 scales exactly as on the host ([O] or [O][ng]); none for fmt=0.
+//        the host nibble/crumb order; fmt=0 keeps the f32 values; fmt=7
+//        keeps the host FP8 E4M3 bytes.
+//   s  : f32 scales exactly as on the host ([O], [O][ng], or for fmt=7
+//        [ceil(O/128)][ng] with ng = ceil(I/128)); none for fmt=0.
 //
 // The bandwidth-bound kernels stream each row as 16-byte chunks, lane l of a
 // warp taking chunks l, l+32, l+64, ...  A chunk holds EPC elements (4, 16,
-// 32, 64, 32 for fmt 0..4).  The activations are staged in shared memory in an
+// 32, 64, 32 for fmt 0..4, 16 for fmt 7).  The activations are staged in shared memory in an
 // order made for those chunks (see stage_vec): the four floats a lane needs
 // for one 32-bit word of codes are one 16-byte shared load, and the float4
 // units of a chunk are XOR-swizzled by the chunk index so that the 8 lanes of
@@ -17,6 +19,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -47,9 +50,20 @@ template <> struct Fmt<1> { static constexpr int EPC = 16; };
 template <> struct Fmt<2> { static constexpr int EPC = 32; };
 template <> struct Fmt<3> { static constexpr int EPC = 64; };
 template <> struct Fmt<4> { static constexpr int EPC = 32; };
+template <> struct Fmt<7> { static constexpr int EPC = 16; };
 
 __host__ __device__ inline int epc_of(int fmt) {
-    return fmt == 0 ? 4 : fmt == 1 ? 16 : fmt == 3 ? 64 : 32;
+    return fmt == 0 ? 4 : (fmt == 1 || fmt == 7) ? 16 : fmt == 3 ? 64 : 32;
+}
+
+// Formats whose scale changes along a row: fmt=4 (one scale per gs inputs)
+// and fmt=7 (one scale per 128 x 128 block).
+template <int FMT> constexpr bool kGrouped = FMT == 4 || FMT == 7;
+constexpr int kFp8Block = 128;   // fmt=7 block edge, rows and inputs
+
+// 16-byte chunks per scale group of a row: gs / 32 for fmt=4, 8 for fmt=7.
+__host__ __device__ inline int chunks_per_group(int fmt, int gs) {
+    return fmt == 7 ? kFp8Block / 16 : fmt == 4 ? gs / 32 : 1;
 }
 
 // Length (floats) of one staged activation vector for a row of `cpr` chunks:
@@ -64,7 +78,7 @@ template <int FMT>
 __device__ __forceinline__ int stage_pos(int e) {
     if constexpr (FMT == 0) {
         return e;
-    } else if constexpr (FMT == 1) {
+    } else if constexpr (FMT == 1 || FMT == 7) {
         const int c = e >> 4, r = e & 15;
         return c * 16 + (((r >> 2) ^ ((c >> 1) & 3)) << 2) + (r & 3);
     } else if constexpr (FMT == 2 || FMT == 4) {
@@ -239,6 +253,21 @@ __device__ __forceinline__ void view3(float2 &va, float2 &vb, uint32_t v) {
                make_float2(-__uint_as_float(M | (2u << 4)), -__uint_as_float(M | (2u << 6))));
 }
 
+// FP8 E4M3, 4 elements: the conversion instruction turns each byte pair into
+// an exact f16 pair (E4M3 values, subnormals and NaN included, are all f16
+// values), widened exactly to f32.  Accumulates into an Acc1.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t pair16) {
+    uint32_t h2;
+    asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h2) : "r"(pair16));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+}
+__device__ __forceinline__ Dec1 decode7(uint32_t w) {
+    Dec1 d;
+    d.v01 = e4m3x2_to_f32x2(w & 0xFFFFu);
+    d.v23 = e4m3x2_to_f32x2(w >> 16);
+    return d;
+}
+
 // f32 weights, 4 per chunk
 struct Acc0 { float2 a, b; };
 __device__ __forceinline__ void acc_zero(Acc0 &a) { a.a = a.b = make_float2(0.f, 0.f); }
@@ -250,6 +279,7 @@ template <> struct AccOf<1> { using T = Acc1; };
 template <> struct AccOf<2> { using T = Acc4; };
 template <> struct AccOf<3> { using T = Acc3; };
 template <> struct AccOf<4> { using T = Acc4; };
+template <> struct AccOf<7> { using T = Acc1; };
 
 // Multiply-accumulate one 16-byte chunk `q` of codes against the staged
 // activations of that chunk (xs4 points at the chunk's first float4 unit of
@@ -269,6 +299,11 @@ __device__ __forceinline__ void chunk_fma(typename AccOf<FMT>::T &acc, uint4 q, 
         const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int t = 0; t < 4; t++) fma1(acc, decode1(wv[t]), xs4[t ^ sw]);
+    } else if constexpr (FMT == 7) {
+        const int sw = (c >> 1) & 3;
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; t++) fma1(acc, decode7(wv[t]), xs4[t ^ sw]);
     } else if constexpr (FMT == 3) {
         const int sw = c & 7;
         const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
@@ -298,8 +333,9 @@ __device__ __forceinline__ void chunk_fma(typename AccOf<FMT>::T &acc, uint4 q, 
 
 // Dot products of R matrix rows against NS staged activation vectors, by one
 // warp.  rows[r] = row base pointers (16-byte aligned), scl[r] = the row's
-// scales (per-row formats: one float; fmt=4: ng floats), gpc[r] = chunks per
-// group of row r for fmt=4 (gs / 32).  xsv[n] = staged vector n.  Results are the
+// scales (per-row formats: one float; fmt=4: ng floats; fmt=7: the ng floats
+// of the row's block-row), gpc[r] = chunks per scale group of row r for the
+// grouped formats (chunks_per_group).  xsv[n] = staged vector n.  Results are the
 // warp-reduced sums, valid in every lane.
 template <int FMT, int R, int NS>
 __device__ __forceinline__ void dot_rows(const uint8_t *const (&rows)[R], const float *const (&scl)[R],
@@ -313,7 +349,7 @@ __device__ __forceinline__ void dot_rows(const uint8_t *const (&rows)[R], const 
 #pragma unroll
         for (int n = 0; n < NS; n++) y[r][n] = 0.f;
     Acc acc[R][NS];
-    if constexpr (FMT != 4) {
+    if constexpr (!kGrouped<FMT>) {
 #pragma unroll
         for (int r = 0; r < R; r++)
 #pragma unroll
@@ -330,7 +366,7 @@ __device__ __forceinline__ void dot_rows(const uint8_t *const (&rows)[R], const 
 #pragma unroll
             for (int r = 0; r < R; r++) {
                 q[u][r] = ok ? ld_stream(rows[r] + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
-                if constexpr (FMT == 4) sc[u][r] = ok ? __ldg(scl[r] + c / gpc[r]) : 0.f;
+                if constexpr (kGrouped<FMT>) sc[u][r] = ok ? __ldg(scl[r] + c / gpc[r]) : 0.f;
             }
         }
 #pragma unroll
@@ -338,7 +374,7 @@ __device__ __forceinline__ void dot_rows(const uint8_t *const (&rows)[R], const 
             if (it0 + u >= n_iter) break;
             const int c = (it0 + u) * 32 + lane;
             const int EPC = Fmt<FMT>::EPC;
-            if constexpr (FMT == 4) {
+            if constexpr (kGrouped<FMT>) {
 #pragma unroll
                 for (int r = 0; r < R; r++)
 #pragma unroll
@@ -350,7 +386,7 @@ __device__ __forceinline__ void dot_rows(const uint8_t *const (&rows)[R], const 
 #pragma unroll
                 for (int r = 0; r < R; r++) chunk_fma<FMT>(acc[r][n], q[u][r], xs4, c);
             }
-            if constexpr (FMT == 4) {
+            if constexpr (kGrouped<FMT>) {
 #pragma unroll
                 for (int r = 0; r < R; r++)
 #pragma unroll
@@ -365,7 +401,7 @@ __device__ __forceinline__ void dot_rows(const uint8_t *const (&rows)[R], const 
 #pragma unroll
         for (int n = 0; n < NS; n++) {
             float v;
-            if constexpr (FMT == 4) v = y[r][n];
+            if constexpr (kGrouped<FMT>) v = y[r][n];
             else if constexpr (FMT == 0) v = acc_combine(acc[r][n]);
             else v = rs * acc_combine(acc[r][n]);
             out[r][n] = warp_sum(v);
@@ -436,14 +472,28 @@ struct ExpertDesc {
     MatDesc m[3];
 };
 
+// Scales of row `row` of a matrix as dot_rows and decode_elem take them: the
+// row's own scale(s), or for fmt=7 the scales of the row's block-row.
+__device__ __forceinline__ const float *row_scales(int fmt, const MatDesc &m, int row) {
+    if (fmt == 0) return nullptr;
+    if (fmt == 4) return m.s + (size_t)row * m.ng;
+    if (fmt == 7) return m.s + (size_t)(row / kFp8Block) * m.ng;
+    return m.s + row;
+}
+
+// Value of one FP8 E4M3 byte (exact, through f16).
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) { return e4m3x2_to_f32x2(b).x; }
+
 // Decode one element (o fixed by `row`, input index i) of the device layout,
-// scale included.  Used by the tiled GEMM and the gather kernels.
+// scale included (rscale = row_scales of the row).  Used by the tiled GEMM
+// and the gather kernels.
 __device__ __forceinline__ float decode_elem(int fmt, const uint8_t *row, const float *rscale, int gs, int i) {
     switch (fmt) {
     case 0: return reinterpret_cast<const float *>(row)[i];
     case 1: return (float)((int)row[i] - 128) * rscale[0];
     case 2: { const uint8_t b = row[i >> 1]; return (float)(((i & 1) ? (b >> 4) : (b & 0xF)) - 8) * rscale[0]; }
     case 3: { const uint8_t b = row[i >> 2]; return (float)(((b >> (2 * (i & 3))) & 3) - 2) * rscale[0]; }
+    case 7: return e4m3_to_f32(row[i]) * rscale[i / kFp8Block];
     default: { const uint8_t b = row[i >> 1]; return (float)(((i & 1) ? (b >> 4) : (b & 0xF)) - 8) * rscale[i / gs]; }
     }
 }

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(NT) gemm_cc_kernel(const GemmArgs a) {
         for (int mtx = 0; mtx < (DUAL ? 2 : 1); mtx++) {
             const MatDesc &M = mtx ? W1 : W0;
             const uint8_t *row = lo < a.O ? M.q + (size_t)lo * M.rs : nullptr;
-            const float *rsc = (row && a.fmt != 0) ? (a.fmt == 4 ? M.s + (size_t)lo * M.ng : M.s + lo) : nullptr;
+            const float *rsc = row ? row_scales(a.fmt, M, lo) : nullptr;
 #pragma unroll
             for (int u = 0; u < 8; u++) {
                 const int i = k0 + lk + u;

@@ -3,7 +3,8 @@
 // y_m[s][o] = sum_i W_m[o][i] x[s][i] for one or several matrices W_m sharing
 // the activations x (PR #298 page, "metal: grouped-int4 (fmt=4) GEMV support"
 // commit message, Shader paragraph: per-row scale after the dot product for
-// fmt 1-3, the group scale folded in per group for fmt=4).
+// fmt 1-3, the group scale folded in per group for fmt=4; fmt=7 folds in the
+// scale of each 128 x 128 block the same way).
 //
 // One CTA stages x (all S rows) in shared memory once, then its warps stream
 // weight rows: a warp task is R consecutive rows of one matrix, each lane
@@ -58,8 +59,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvJob job) {
         for (int r = 0; r < R; r++) {
             const int o = min(o0 + r, Om - 1);
             rows[r] = job.q[m] + (size_t)o * job.rs[m];
-            scl[r] = FMT == 4 ? job.s[m] + (size_t)o * job.ng[m] : (FMT == 0 ? nullptr : job.s[m] + o);
-            gpc[r] = FMT == 4 ? job.gs[m] / 32 : 1;
+            scl[r] = FMT == 4   ? job.s[m] + (size_t)o * job.ng[m]
+                     : FMT == 7 ? job.s[m] + (size_t)(o / kFp8Block) * job.ng[m]
+                     : FMT == 0 ? nullptr
+                                : job.s[m] + o;
+            gpc[r] = chunks_per_group(FMT, job.gs[m]);
         }
         float out[R][S];
         dot_rows<FMT, R, S>(rows, scl, gpc, xsv, job.cpr, lane, out);
@@ -181,6 +185,7 @@ cudaError_t launch_gemv(const GemvJob &job, cudaStream_t st, int *n_launch) {
     case 2: return launch_f<2>(job, st, n_sm);
     case 3: return launch_f<3>(job, st, n_sm);
     case 4: return launch_f<4>(job, st, n_sm);
+    case 7: return launch_f<7>(job, st, n_sm);
     default: return cudaErrorInvalidValue;
     }
 }

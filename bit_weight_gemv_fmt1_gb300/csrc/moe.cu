@@ -58,19 +58,13 @@ __device__ bool grid_barrier(unsigned *bar, int *err, long long timeout_ns) {
     return ok != 0;
 }
 
-__device__ __forceinline__ const float *row_scales(int fmt, const MatDesc &m, int row) {
-    if (fmt == 4) return m.s + (size_t)row * m.ng;
-    if (fmt == 0) return nullptr;
-    return m.s + row;
-}
-
 template <int FMT, int NS>
 __device__ __forceinline__ void phase_a_item(const MatDesc &G, const MatDesc &U, int j, const float *xs,
                                              int xlen, const int *s_order, int p0, int K, int cpr, int lane,
                                              float *hbuf, int F) {
     const uint8_t *rows[2] = {G.q + (size_t)j * G.rs, U.q + (size_t)j * U.rs};
     const float *scl[2] = {row_scales(FMT, G, j), row_scales(FMT, U, j)};
-    const int gpc[2] = {max(G.gs / 32, 1), max(U.gs / 32, 1)};
+    const int gpc[2] = {chunks_per_group(FMT, G.gs), chunks_per_group(FMT, U.gs)};
     const float *xsv[NS];
 #pragma unroll
     for (int n = 0; n < NS; n++) xsv[n] = xs + (size_t)(s_order[p0 + n] / K) * xlen;
@@ -93,7 +87,7 @@ __device__ __forceinline__ void phase_b_item(const MatDesc &D, int o0, int H, co
         const int o = min(o0 + r, H - 1);
         rows[r] = D.q + (size_t)o * D.rs;
         scl[r] = row_scales(FMT, D, o);
-        gpc[r] = max(D.gs / 32, 1);
+        gpc[r] = chunks_per_group(FMT, D.gs);
     }
     const float *xsv[NS];
 #pragma unroll
@@ -405,6 +399,7 @@ cudaError_t moe_decode_occupancy(int fmt, size_t smem, int *per_sm) {
     case 2: return occ_t<2>(smem, per_sm);
     case 3: return occ_t<3>(smem, per_sm);
     case 4: return occ_t<4>(smem, per_sm);
+    case 7: return occ_t<7>(smem, per_sm);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -416,6 +411,7 @@ cudaError_t launch_moe_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t 
     case 2: return launch_decode_t<2>(a, grid, smem, st);
     case 3: return launch_decode_t<3>(a, grid, smem, st);
     case 4: return launch_decode_t<4>(a, grid, smem, st);
+    case 7: return launch_decode_t<7>(a, grid, smem, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -135,8 +135,8 @@ extern "C" int coli_moe_block_noalloc(const float *x, int S, const coli_expert *
             d.q = m[k]->q;
             d.s = m[k]->s;
             d.rs = m[k]->rs;
-            d.gs = m[k]->fmt == 4 ? m[k]->gs : 0;
-            d.ng = m[k]->fmt == 4 ? m[k]->ng : 1;
+            d.gs = m[k]->fmt == 4 ? m[k]->gs : m[k]->fmt == 7 ? kFp8Block : 0;
+            d.ng = m[k]->ng;
             d.tmap = m[k]->tmap;
         }
     }

@@ -4,7 +4,7 @@
  *
  * The operation (colibri project pages):
  *   - y[s][o] = sum_i w[o][i] * x[s][i] over a quantized weight matrix W [O][I]
- *     in one of five formats (PR #298 page, commit message "metal: grouped-int4
+ *     in one of six formats (PR #298 page, commit message "metal: grouped-int4
  *     (fmt=4) GEMV support": mm_gemv handled "fmt 0-3", fmt=4 added with one f32
  *     scale per gs inputs folded into the accumulation per group; commit message
  *     "CUDA backend had no fmt=4 case": per-row scale for fmt 1/2/3, per-group
@@ -27,6 +27,13 @@
  *   fmt=4  int4 as fmt=2; scales f32 [O][ceil(I/gs)], group g covering inputs
  *          [g*gs, min((g+1)*gs, I)) (PR #298 page, test_i4_grouped commit: the
  *          partial last group and gs > I).
+ *   fmt=7  FP8 E4M3 (OCP: sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ *          exponent 0 subnormal, no infinities, S.1111.111 NaN), one byte per
+ *          element, [O][I]; scales f32 [ceil(O/128)][ceil(I/128)], one per
+ *          128 x 128 block, w[o][i] = e4m3(byte) * s[o/128][i/128] (PR #298
+ *          page, qt_addrow / qt_matvec_rows commit message: fmt=7 keeps raw
+ *          bytes like fmt=1 and ceil(O/128)*ceil(I/128) per-block scales; the
+ *          E4M3 encoding is this library's reading of its "fp8 passthrough").
  * The int4 offset encoding and the extremes 0x00 -> -8, 0xFF -> +7 are printed
  * on the PR #298 page (test_i4_grouped commit message); the element order in a
  * byte, the int2 and int8 encodings are this library's documented readings.
@@ -86,9 +93,9 @@ typedef struct {
  * Upload one weight matrix W [O][I] (PR #298 page, "CUDA backend had no fmt=4
  * case" commit message: coli_cuda_tensor_upload_grouped takes gs and stores
  * O*ceil(I/gs) scales; this entry point is that upload for every format).
- *   fmt     0..4 as in the layout above.
+ *   fmt     0..4 or 7 as in the layout above.
  *   gs      fmt=4: group size, even and >= 2 (gs >= I means one group per row).
- *           Other formats: ignored.
+ *           Other formats: ignored (fmt=7 blocks are always 128 x 128).
  *   O, I    rows (outputs) and columns (inputs), each >= 1, I <= 2^30.
  *   data    HOST pointer to the packed codes in the host layout above.
  *   scales  HOST pointer to the f32 scales (NULL for fmt=0).
@@ -124,7 +131,7 @@ int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_
  *           runs the bandwidth-bound CUDA-core matvec kernels, S = 1 the
  *           slab kernel for fmt 0/1/2/4; larger S runs the tensor-core GEMM
  *           for fmt=2 and for fmt=4 with gs % 64 == 0, the tiled CUDA-core
- *           GEMM otherwise.
+ *           GEMM otherwise (fmt 0, 1, 3, 7).
  * Errors: COLI_EINVAL (NULL/misaligned pointer, S < 1), COLI_EDEVICE, COLI_ECUDA.
  */
 int coli_matmul(const coli_tensor *W, const float *x, float *y, int S, void *stream);

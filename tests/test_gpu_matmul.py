@@ -15,7 +15,7 @@ from oracle import oracle as orc
 
 pytestmark = pytest.mark.gpu
 
-FMT_CASES = [(0, 0), (1, 0), (2, 0), (3, 0), (4, 32), (4, 64), (4, 128)]
+FMT_CASES = [(0, 0), (1, 0), (2, 0), (3, 0), (4, 32), (4, 64), (4, 128), (7, 0)]
 
 
 def _run(coli, torch, m, x):
@@ -84,7 +84,7 @@ def test_fmt4_wide_group_equals_fmt2():
 
 
 @pytest.mark.parametrize("S", [9, 16, 33, 70])
-@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 10)])
+@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 10), (7, 0)])
 def test_large_s_gemm_path(fmt, gs, S):
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
@@ -94,6 +94,66 @@ def test_large_s_gemm_path(fmt, gs, S):
     got = _run(coli, torch, m, x)
     ref = orc.matmul(fmt, gs, 150, 700, m.data, m.scales, x)
     assert norm_err(got, ref) <= TOL
+
+
+def _fp8_library(b):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(b, dtype=np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("S", [1, 3, 9])
+def test_fp8_decode_table(S):
+    """Every FP8 E4M3 byte through the kernels (I = 1, x = 1, unit scales): y is
+    the decode table itself, NaN bytes included, bit for bit (matvec for
+    S <= 8, the tiled GEMM for S = 9)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    data = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    m = wl.Matrix(7, 0, 256, 1, data, np.ones(wl.scale_count(7, 256, 1, 0), np.float32))
+    x = np.ones((S, 1), np.float32)
+    got = _run(coli, torch, m, x).astype(np.float64)
+    ref = orc.matmul(7, 0, 256, 1, m.data, m.scales, x).astype(np.float64)
+    want = np.broadcast_to(_fp8_library(data[:, 0]), (S, 256))
+    for a in (ref, want):
+        assert np.array_equal(np.isnan(got), np.isnan(a))
+        assert np.array_equal(got[~np.isnan(got)], a[~np.isnan(a)])
+
+
+@pytest.mark.parametrize("O,I", [(300, 3000), (129, 385), (1, 17)])
+@pytest.mark.parametrize("S", [1, 4, 20])
+def test_fp8_exact_integer_cases(O, I, S):
+    """FP8 bytes whose values are multiples of 1/4 up to 8, power-of-two block
+    scales and integer x in [-4, 4]: every partial sum is exact in f32, so the
+    GPU must equal the oracle bit for bit (block index, partial blocks)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(31 * O + I + S)
+    vals = _fp8_library(np.arange(256, dtype=np.uint8))
+    ok = np.flatnonzero(np.isfinite(vals) & (np.abs(vals) <= 8) & (np.mod(vals * 4, 1) == 0)).astype(np.uint8)
+    data = g.choice(ok, (O, I))
+    sc = (2.0 ** g.integers(-2, 3, wl.scale_count(7, O, I, 0))).astype(np.float32)
+    m = wl.Matrix(7, 0, O, I, data, sc)
+    x = g.integers(-4, 5, (S, I)).astype(np.float32)
+    got = _run(coli, torch, m, x)
+    ref = orc.matmul(7, 0, O, I, m.data, m.scales, x)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_matmul_multi():
+    """Several FP8 matrices sharing one input (different O, partial blocks)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(92)
+    mats = [wl.random_matrix(g, 7, O, 1536) for O in (100, 257, 31, 512)]
+    x = wl.activations(g, 2, 1536)
+    Ws = [upload(coli, m) for m in mats]
+    xd = torch.from_numpy(x).cuda()
+    ys = [torch.empty(2, m.O, device="cuda") for m in mats]
+    coli.matmul_multi(Ws, xd, ys)
+    coli.sync_check()
+    for m, y in zip(mats, ys):
+        ref = orc.matmul(7, 0, m.O, 1536, m.data, m.scales, x)
+        assert norm_err(y.cpu().numpy(), ref) <= TOL
 
 
 def test_matmul_multi_shared_input():
