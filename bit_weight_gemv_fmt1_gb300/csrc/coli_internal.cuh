@@ -23,6 +23,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "coli.h"
 
 struct coli_tensor {
@@ -422,6 +424,20 @@ __device__ __forceinline__ float dot_row_fmt4_generic(const uint8_t *row, const 
     return warp_sum(acc);
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// The matvec kernels are launched with programmatic stream serialization: a
+// kernel lets the next one in the stream begin launching once every thread of
+// every CTA has finished its main loop (pdl_trigger; only the short epilogue
+// is left), and waits for the previous kernel to complete, with its writes
+// visible, before it reads activations or writes outputs (pdl_wait).
+// Weights and scales never change between kernels, so their loads may be
+// issued before the wait.  Triggering at the end of the main loop keeps at
+// most one kernel ahead resident; an early trigger let several waiting grids
+// pile up on the SMs and cut the running kernel's occupancy.  Without a
+// programmatic predecessor or dependent both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- timing
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
@@ -454,6 +470,22 @@ struct GemvJob {
 };
 
 cudaError_t launch_gemv(const GemvJob &job, cudaStream_t st, int *n_launch);
+
+// Launch `kern` with programmatic stream serialization allowed (see pdl_wait).
+template <class... P, class... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
 
 }  // namespace coli
 

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvJob job) {
     extern __shared__ float4 smem4[];
     float *xs = reinterpret_cast<float *>(smem4);
     const int xlen = staged_len(FMT, job.cpr);
+    pdl_wait();
 #pragma unroll
     for (int s = 0; s < S; s++)
         stage_vec<FMT>(xs + s * xlen, job.x + (size_t)s * job.I, job.I, xlen, threadIdx.x, blockDim.x);
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvJob job) {
             }
         }
     }
+    pdl_trigger();
 }
 
 // fmt=4 with gs not a multiple of 32: one warp per (matrix, row), plain
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvJob job) {
 __global__ void __launch_bounds__(kThreads) gemv_fmt4_generic_kernel(const GemvJob job) {
     extern __shared__ float4 smem4[];
     float *xs = reinterpret_cast<float *>(smem4);
+    pdl_wait();
     for (int e = threadIdx.x; e < job.S * job.I; e += blockDim.x) xs[e] = job.x[e];
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) gemv_fmt4_generic_kernel(const GemvJ
             if (lane == 0) job.y[m][(size_t)s * job.O[m] + o] = v;
         }
     }
+    pdl_trigger();
 }
 
 template <int FMT, int S, int R>
@@ -128,8 +132,7 @@ cudaError_t launch_t(const GemvJob &job, cudaStream_t st, int n_sm) {
     for (int m = 0; m < job.n; m++) n_tasks += (job.O[m] + R - 1) / R;
     const int want = (n_tasks + kThreads / 32 - 1) / (kThreads / 32);
     const int grid = max(1, min(want, per_sm * n_sm));
-    kern<<<grid, kThreads, smem, st>>>(job);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
 }
 
 template <int FMT, int S>
@@ -176,8 +179,7 @@ cudaError_t launch_gemv(const GemvJob &job, cudaStream_t st, int *n_launch) {
         if (e != cudaSuccess) return e;
         const int rows = job.row_start[job.n];
         const int grid = max(1, min((rows + 7) / 8, n_sm * 4));
-        gemv_fmt4_generic_kernel<<<grid, kThreads, smem, st>>>(job);
-        return cudaGetLastError();
+        return launch_pdl(gemv_fmt4_generic_kernel, dim3(grid), dim3(kThreads), smem, st, job);
     }
     switch (job.fmt) {
     case 0: return launch_f<0>(job, st, n_sm);

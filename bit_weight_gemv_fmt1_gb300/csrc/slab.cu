@@ -133,8 +133,6 @@ __global__ void __launch_bounds__(kSlabThreads, 2) slab_gemv_kernel(const GemvJo
     const int r0 = blockIdx.x * rpc;
     const int n_rows = min(rpc, total_rows - r0);
     if (n_rows <= 0) return;
-    stage_x<FMT>(xs, job.x, job.I, job.cpr);
-    __syncthreads();
 
     const int n_units = n_slab * n_rows;
     auto row_of = [&](int rr, int &m, int &o) {
@@ -162,6 +160,10 @@ __global__ void __launch_bounds__(kSlabThreads, 2) slab_gemv_kernel(const GemvJo
         else sb[i] = 1.f;
         if (ok) wl.step(nw, n_rows);
     }
+    // the first weight loads are in flight; the activations may come from the previous kernel
+    pdl_wait();
+    stage_x<FMT>(xs, job.x, job.I, job.cpr);
+    __syncthreads();
     XReg<FMT> xr;
     int cur_s = -1;
     for (int k0 = 0; warp + k0 * nw < n_units; k0 += P) {
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kSlabThreads, 2) slab_gemv_kernel(const GemvJo
             wc.step(nw, n_rows);
         }
     }
+    pdl_trigger();
     __syncthreads();
     for (int rr = threadIdx.x; rr < n_rows; rr += blockDim.x) {
         float acc = 0.f;
@@ -1145,18 +1148,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
     const int total = job.row_start[job.n];
     const int r0 = blockIdx.x * rpc, r1 = min(total, r0 + rpc);
     if (r0 >= r1) return;
-    const uint64_t deadline = global_ns() + (uint64_t)timeout_ns;
+    uint64_t deadline = global_ns() + (uint64_t)timeout_ns;
     // lane units: XR::LB code bytes = XR::NIN inputs; a row has lpr of them
     const int lpr = (job.I + XR::NIN - 1) / XR::NIN;
     const int ns = (lpr + 31) >> 5, sl = warp % ns, sub = warp / ns, G = NWC / ns;
-    float4 xraw[XR::NIN / 4];
-#pragma unroll
-    for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (warp < NWC && sl * 32 + lane < lpr) {
-        const float4 *p = reinterpret_cast<const float4 *>(job.x + (size_t)(sl * 32 + lane) * XR::NIN);
-#pragma unroll
-        for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = __ldg(p + j);
-    }
     if (tid == 0) {
         abort_flag = 0;
         for (int i = 0; i < NS; i++) {
@@ -1186,6 +1181,12 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
             int s = 0, it = 0;
             uint32_t ph = 0;
             while (next(sm_, so, sn)) {
+                if (it == NS) {
+                    // the ring is full of weights; from here on the consumers, which
+                    // waited for the previous kernel, pace the copies
+                    pdl_wait();
+                    deadline = global_ns() + (uint64_t)timeout_ns;
+                }
                 if (it >= NS && !mbar_wait(&empty[s], ph ^ 1, deadline, &abort_flag)) {
                     if (!abort_flag) {
                         abort_flag = 1;
@@ -1204,11 +1205,22 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
                     ph ^= 1;
                 }
             }
+            pdl_trigger();
             const uint64_t dl2 = global_ns() + 200000000ull;
             volatile int no_abort = 0;
             for (int k = max(0, it - NS); k < it; k++) mbar_wait(&full[k % NS], (k / NS) & 1, dl2, &no_abort);
         }
         return;
+    }
+    pdl_wait();
+    deadline = global_ns() + (uint64_t)timeout_ns;
+    float4 xraw[XR::NIN / 4];
+#pragma unroll
+    for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sl * 32 + lane < lpr) {
+        const float4 *p = reinterpret_cast<const float4 *>(job.x + (size_t)(sl * 32 + lane) * XR::NIN);
+#pragma unroll
+        for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = __ldg(p + j);
     }
     XR xr;
     xr.set(xraw);
@@ -1246,6 +1258,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
             ph ^= 1;
         }
     }
+    pdl_trigger();
     named_sync(1, NCT);
     for (int rr = tid; rr < r1 - r0; rr += NCT) {
         float acc = 0.f;
@@ -1339,23 +1352,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_s_kernel(const 
     const int total = job.row_start[job.n];
     const int r0 = blockIdx.x * rpc, r1 = min(total, r0 + rpc);
     if (r0 >= r1) return;
-    const uint64_t deadline = global_ns() + (uint64_t)timeout_ns;
+    uint64_t deadline = global_ns() + (uint64_t)timeout_ns;
     const int hcpr = job.cpr * 2;                        // 8-byte half chunks per row
     const int nh = (hcpr + 31) >> 5, sl = warp % nh, sub = warp / nh, G = NWC / nh;
     const int hc = sl * 32 + lane;                       // this lane's half chunk
     const bool okc = hc < hcpr;
-    XRegHalf<S> xr;
-    if (warp < NWC) {
-#pragma unroll
-        for (int r = 0; r < S; r++) {
-            float4 raw[4];
-#pragma unroll
-            for (int j = 0; j < 4; j++)
-                raw[j] = okc ? __ldg(reinterpret_cast<const float4 *>(job.x + (size_t)r * job.I + (size_t)hc * 16) + j)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-            xr.set(r, raw);
-        }
-    }
     if (tid == 0) {
         abort_flag = 0;
         for (int i = 0; i < NS; i++) {
@@ -1384,6 +1385,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_s_kernel(const 
             int s = 0, it = 0;
             uint32_t ph = 0;
             while (next(sm_, so, sn)) {
+                if (it == NS) {
+                    pdl_wait();
+                    deadline = global_ns() + (uint64_t)timeout_ns;
+                }
                 if (it >= NS && !mbar_wait(&empty[s], ph ^ 1, deadline, &abort_flag)) {
                     if (!abort_flag) {
                         abort_flag = 1;
@@ -1402,11 +1407,24 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_s_kernel(const 
                     ph ^= 1;
                 }
             }
+            pdl_trigger();
             const uint64_t dl2 = global_ns() + 200000000ull;
             volatile int no_abort = 0;
             for (int k = max(0, it - NS); k < it; k++) mbar_wait(&full[k % NS], (k / NS) & 1, dl2, &no_abort);
         }
         return;
+    }
+    pdl_wait();
+    deadline = global_ns() + (uint64_t)timeout_ns;
+    XRegHalf<S> xr;
+#pragma unroll
+    for (int r = 0; r < S; r++) {
+        float4 raw[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            raw[j] = okc ? __ldg(reinterpret_cast<const float4 *>(job.x + (size_t)r * job.I + (size_t)hc * 16) + j)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        xr.set(r, raw);
     }
     int s = 0;
     uint32_t ph = 0;
@@ -1454,6 +1472,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_s_kernel(const 
             ph ^= 1;
         }
     }
+    pdl_trigger();
     named_sync(1, NCT);
     for (int t = tid; t < (r1 - r0) * S; t += NCT) {
         const int rr = t / S, row = t - rr * S;
@@ -1478,8 +1497,7 @@ cudaError_t slab_gemv_t(const GemvJob &job, int n_sm, int gshift, cudaStream_t s
     auto kern = slab_gemv_kernel<FMT, 4>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kSlabThreads, smem, st>>>(job, rpc, gshift);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kSlabThreads), smem, st, job, rpc, gshift);
 }
 
 template <int FMT>
@@ -1554,8 +1572,8 @@ cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, 
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, (kStreamConsumerWarps + 1) * 32, smem, st>>>(job, rpc, RG, gshift, 2000000000LL);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3(grid), dim3((kStreamConsumerWarps + 1) * 32), smem, st, job, rpc, RG, gshift,
+                          2000000000LL);
     };
     switch (job.fmt) {
     case 0: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegF32>);
@@ -1584,8 +1602,8 @@ cudaError_t launch_stream_gemv_s(const GemvJob &job, int rpc, int RG, int gshift
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, (kStreamConsumerWarps + 1) * 32, smem, st>>>(job, rpc, RG, gshift, 2000000000LL);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3(grid), dim3((kStreamConsumerWarps + 1) * 32), smem, st, job, rpc, RG, gshift,
+                          2000000000LL);
     };
     switch (job.S) {
     case 2: return go(stream_gemv_s_kernel<kStreamConsumerWarps, 2>);

@@ -268,3 +268,94 @@ def test_streamed_small_s_exact_integers(fmt, gs, S):
     got = _run(coli, torch, m, x)
     ref = orc.matmul(fmt, gs, O, I, m.data, m.scales, x)
     assert np.array_equal(got, ref)
+
+
+def _chain_mats(g):
+    """A chain of matrices whose shapes compose (x[4096] -> ... -> [4096]) and
+    whose launches take different kernels: streamed (int4 groups, int8), the
+    register-slab kernel (small int4 matrices) and the generic kernel (FP8)."""
+    return [wl.random_matrix(g, 4, 4096, 4096, 64), wl.random_matrix(g, 7, 4096, 4096),
+            wl.random_matrix(g, 2, 1024, 4096), wl.random_matrix(g, 4, 4096, 1024, 128),
+            wl.random_matrix(g, 1, 4096, 4096)]
+
+
+def test_dependent_chain_in_graph():
+    """Each matvec reads the previous one's output (read after write across
+    back-to-back launches, replayed from a CUDA graph): stage k on the GPU
+    equals the oracle applied to the GPU's stage k-1 output.  The buffers are
+    filled with NaN before every replay, so a stage that read its input
+    before the producer finished would not match."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(93)
+    mats = _chain_mats(g)
+    Ws = [upload(coli, m) for m in mats]
+    x = torch.from_numpy(wl.activations(g, 1, 4096)).cuda()
+    ys = [torch.empty(1, m.O, device="cuda") for m in mats]
+    st = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        src = x
+        for W, y in zip(Ws, ys):
+            coli.matmul(W, src, y, stream=st)
+            src = y
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=st):
+        src = x
+        for W, y in zip(Ws, ys):
+            coli.matmul(W, src, y, stream=st)
+            src = y
+    for _ in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            graph.replay()
+        torch.cuda.synchronize()
+        coli.sync_check()
+        src = x.cpu().numpy()
+        for m, y in zip(mats, ys):
+            got = y.cpu().numpy()
+            ref = orc.matmul(m.fmt, m.gs, m.O, m.I, m.data, m.scales, src)
+            assert norm_err(got, ref) <= TOL
+            src = got
+
+
+def test_ping_pong_chain_in_graph():
+    """Two buffers used alternately (each launch overwrites the buffer the
+    launch before it read: write after read), replayed from a CUDA graph, against
+    the oracle chain in f64 (4 stages, tolerance 4x the per-stage one)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(94)
+    mats = [wl.random_matrix(g, 4, 4096, 4096, 64), wl.random_matrix(g, 2, 4096, 4096),
+            wl.random_matrix(g, 4, 4096, 4096, 128), wl.random_matrix(g, 1, 4096, 4096)]
+    Ws = [upload(coli, m) for m in mats]
+    x0 = wl.activations(g, 1, 4096)
+    bufs = [torch.empty(1, 4096, device="cuda"), torch.empty(1, 4096, device="cuda")]
+    st = torch.cuda.Stream()
+
+    def body():
+        for k, W in enumerate(Ws):
+            coli.matmul(W, bufs[k % 2], bufs[(k + 1) % 2], stream=st)
+
+    bufs[0].copy_(torch.from_numpy(x0))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        body()
+    ref = x0.astype(np.float64)
+    for m in mats:
+        ref = orc.matmul(m.fmt, m.gs, m.O, m.I, m.data, m.scales, ref.astype(np.float32), want=("y64",))[0]
+    for _ in range(3):
+        bufs[0].copy_(torch.from_numpy(x0))
+        bufs[1].fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            graph.replay()
+        torch.cuda.synchronize()
+        coli.sync_check()
+        assert norm_err(bufs[0].cpu().numpy(), ref) <= 4 * TOL
