@@ -237,10 +237,11 @@ def _time_loop(torch, fn, n, warm=5):
 def _time_graph(torch, fn, n, warm=3):
     """Average device time of fn(0..n-1) replayed from one CUDA graph (no
     Python launch overhead inside the timed region)."""
-    for i in range(warm):
-        fn(i)
-    torch.cuda.synchronize()
     st = torch.cuda.Stream()
+    with torch.cuda.stream(st):   # warm up on the capture stream: its scratch exists before capture
+        for i in range(warm):
+            fn(i)
+    torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=st):
         for i in range(n):
@@ -399,6 +400,75 @@ def bench_router(coli, torch, peaks, steps=200):
                     "64-expert resident pool (L2 sees part of it: the block time here is not the headline)"}
 
 
+def bench_host(coli, torch, peaks, l2_bytes, steps=100):
+    """Host-resident weights (coli_tensor_upload_host) read zero-copy over the
+    CPU-GPU link: (a) the link's copy bandwidth, pinned host -> HBM (torch copy),
+    as the reference; (b) a 2048x6144 int4 g64 matvec with its weights in host
+    memory, rotated over copies exceeding 4x L2; (c) the decode expert block
+    (H=6144, F=2048, int4 g64, S=1, K=8) with k of the 8 routed experts in host
+    memory and the rest in HBM, a fresh routing per call."""
+    out = {}
+    nb = 1 << 29
+    hsrc = torch.empty(nb, dtype=torch.uint8, pin_memory=True)
+    ddst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        ddst.copy_(hsrc, non_blocking=True)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(4):
+        ddst.copy_(hsrc, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    link = 4 * nb / (a.elapsed_time(b) / 1e3) / 1e9
+    out["h2d_copy_GB/s"] = link
+    del hsrc, ddst
+
+    c = wl.GEMV_SWEEP
+    O, I = c["O"], c["I"]
+    g = wl.rng(c["seed"] + 50)
+    m = wl.random_matrix(g, 4, O, I, 64)
+    ncopy = max(2, math.ceil(4 * l2_bytes / m.nbytes))
+    Ws = [coli.tensor_upload_host(m.fmt, m.gs, O, I, m.data, m.scales) for _ in range(ncopy)]
+    x = torch.randn(1, I, device="cuda")
+    y = torch.empty(1, O, device="cuda")
+    t = _time_graph(torch, lambda i: coli.matmul(Ws[i % ncopy], x, y), max(100, 2 * ncopy))
+    coli.sync_check()
+    out["matvec_host_fmt4_g64_S1"] = {"us": t * 1e6, "GB/s": m.nbytes / t / 1e9,
+                                      "frac_of_copy": m.nbytes / t / 1e9 / link, "copies": ncopy}
+    del Ws
+
+    d = wl.MOE_DECODE
+    H, F, K = d["H"], d["F"], d["K"]
+    g = wl.rng(d["seed"] + 200)
+    hosts = [wl.expert(g, H, F, d["fmt"], d["gs"]) for _ in range(8)]
+    n_dev, n_host = 64, 16
+    dev = [tuple(coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in hosts[e % 8])
+           for e in range(n_dev)]
+    hst = [tuple(coli.tensor_upload_host(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in hosts[e % 8])
+           for e in range(n_host)]
+    table = coli.ExpertTable(dev + hst)
+    xs = torch.randn(steps, 1, H, device="cuda")
+    w = torch.full((1, K), 1.0 / K, device="cuda")
+    yb = torch.empty(1, H, device="cuda")
+    per_expert = wl.expert_bytes(H, F, d["fmt"], d["gs"])
+    res = {}
+    for k in (0, 1, 2, 8):
+        ids = np.empty((steps, 1, K), np.int32)
+        for i in range(steps):
+            dv = [(i * 7 + j) % n_dev for j in range(K - k)]
+            hv = [n_dev + (i * 3 + j) % n_host for j in range(k)]
+            ids[i, 0] = dv + hv
+        idd = torch.from_numpy(ids).cuda()
+        t = _time_graph(torch, lambda i: coli.moe_block(xs[i], table, idd[i], w, yb), steps)
+        coli.sync_check()
+        res[f"k{k}"] = {"us": t * 1e6, "host_bytes": k * per_expert, "hbm_bytes": (K - k) * per_expert,
+                        "host_GB/s_if_link_bound": k * per_expert / t / 1e9}
+    out["decode_block_k_of_8_in_host_memory"] = res
+    return out
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle, timed as it stands, on a bounded
     sample of the default workload: one routed (row, expert) slot per step."""
@@ -471,7 +541,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default="moe_decode",
-                    choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming", "router"),
+                    choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming", "router", "host"),
                     help="moe_decode is the headline line; the others print their own line (for profiling)")
     ap.add_argument("--experts-prefill", type=int, default=None, help="resident experts of the prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -501,6 +571,9 @@ def main():
                 res = bench_gemv(coli, torch, peaks, l2)
             elif args.workload == "router":
                 res = bench_router(coli, torch, peaks)
+            elif args.workload == "host":
+                res = bench_host(coli, torch, peaks,
+                                 torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
             else:
                 res = bench_streaming(coli, torch, peaks)
             print(json.dumps({"workload": args.workload, "result": res}), flush=True)

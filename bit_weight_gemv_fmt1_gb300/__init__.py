@@ -43,6 +43,7 @@ class _Expert(ctypes.Structure):
 _lib.coli_version.restype = ctypes.c_char_p
 _lib.coli_last_error.restype = ctypes.c_char_p
 _lib.coli_tensor_upload.argtypes = [_int, _int, _i64, _i64, _vp, _vp, _vp, ctypes.POINTER(_vp)]
+_lib.coli_tensor_upload_host.argtypes = [_int, _int, _i64, _i64, _vp, _vp, ctypes.POINTER(_vp)]
 _lib.coli_tensor_free.argtypes = [_vp]
 _lib.coli_tensor_free.restype = None
 _lib.coli_tensor_info.argtypes = [_vp] + [ctypes.POINTER(_int)] * 2 + [ctypes.POINTER(_i64)] * 4
@@ -60,7 +61,7 @@ _lib.coli_reset_stats.restype = None
 _lib.coli_set_fail_after.argtypes = [_i64]
 _lib.coli_set_fail_after.restype = None
 
-EXPORTS = ("coli_tensor_upload", "coli_tensor_free", "coli_tensor_info", "coli_matmul", "coli_matmul_multi",
+EXPORTS = ("coli_tensor_upload", "coli_tensor_upload_host", "coli_tensor_free", "coli_tensor_info", "coli_matmul", "coli_matmul_multi",
            "coli_moe_route", "coli_moe_topk", "coli_moe_router", "coli_moe_block", "coli_moe_block_noalloc",
            "coli_sync_check", "coli_last_error", "coli_get_stats", "coli_reset_stats", "coli_set_fail_after",
            "coli_version")
@@ -130,6 +131,17 @@ def tensor_upload(fmt: int, gs: int, O: int, I: int, data: np.ndarray, scales: n
     out = _vp()
     _check(_lib.coli_tensor_upload(int(fmt), int(gs), int(O), int(I), data.ctypes.data,
                                    None if sc is None else sc.ctypes.data, _stream(stream), ctypes.byref(out)))
+    return Tensor(out.value, int(fmt), int(gs), int(O), int(I))
+
+
+def tensor_upload_host(fmt: int, gs: int, O: int, I: int, data: np.ndarray, scales: np.ndarray | None) -> Tensor:
+    """As tensor_upload, but the weights stay in pinned host memory and the
+    kernels read them zero-copy over the CPU-GPU link."""
+    data = np.ascontiguousarray(data)
+    sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.float32)
+    out = _vp()
+    _check(_lib.coli_tensor_upload_host(int(fmt), int(gs), int(O), int(I), data.ctypes.data,
+                                        None if sc is None else sc.ctypes.data, ctypes.byref(out)))
     return Tensor(out.value, int(fmt), int(gs), int(O), int(I))
 
 

@@ -224,9 +224,9 @@ void coli_reset_stats(void) {
 
 void coli_set_fail_after(int64_t n) { fail_after().store(n < 0 ? -1 : n); }
 
-int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
-                       void *stream, coli_tensor **out) {
-    g_msg[0] = 0;
+// Argument checks shared by both uploads.
+static int check_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
+                        coli_tensor **out) {
     if (!out) return fail(COLI_EINVAL, "out is NULL");
     *out = nullptr;
     if (fmt < 0 || (fmt > 4 && fmt != 7))
@@ -238,12 +238,12 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
         return fail(COLI_EINVAL, "matrix too large (O=%lld I=%lld)", (long long)O, (long long)I);
     if (!data) return fail(COLI_EINVAL, "data is NULL");
     if (fmt != 0 && !scales) return fail(COLI_EINVAL, "fmt=%d needs scales", fmt);
-    DeviceState *ds = nullptr;
-    if (int rc = device_state(&ds)) return rc;
-    cudaStream_t st = (cudaStream_t)stream;
+    return COLI_OK;
+}
 
+// A new tensor with the shape, layout and byte counts of (fmt, gs, O, I); no storage yet.
+static coli_tensor *new_tensor(int fmt, int gs, int64_t O, int64_t I, int64_t *n_scales) {
     coli_tensor *t = new coli_tensor();
-    CU(cudaGetDevice(&t->device), "cudaGetDevice");
     t->fmt = fmt;
     t->gs = fmt == 4 ? gs : 0;
     t->O = O;
@@ -252,13 +252,28 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
     const int64_t hrb = host_row_bytes(fmt, I);
     t->rs = (hrb + 15) / 16 * 16;
     t->cpr = (int)((I + epc_of(fmt) - 1) / epc_of(fmt));
-    const int64_t n_scales = fmt == 0   ? 0
-                             : fmt == 4 ? O * t->ng
-                             : fmt == 7 ? (O + kFp8Block - 1) / kFp8Block * t->ng
-                                        : O;
-    t->alg_bytes = O * hrb + 4 * n_scales;
-    t->dev_bytes = O * t->rs + 4 * n_scales;
+    *n_scales = fmt == 0   ? 0
+                : fmt == 4 ? O * t->ng
+                : fmt == 7 ? (O + kFp8Block - 1) / kFp8Block * t->ng
+                           : O;
+    t->alg_bytes = O * hrb + 4 * *n_scales;
+    t->dev_bytes = O * t->rs + 4 * *n_scales;
     t->uid = g_uid++;
+    return t;
+}
+
+int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
+                       void *stream, coli_tensor **out) {
+    g_msg[0] = 0;
+    if (int rc = check_upload(fmt, gs, O, I, data, scales, out)) return rc;
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    int64_t n_scales = 0;
+    coli_tensor *t = new_tensor(fmt, gs, O, I, &n_scales);
+    const int64_t hrb = host_row_bytes(fmt, I);
+    CU(cudaGetDevice(&t->device), "cudaGetDevice");
     cudaError_t e = cudaMalloc(&t->q, (size_t)(O * t->rs));
     if (e == cudaSuccess && n_scales) e = cudaMalloc(&t->s, (size_t)n_scales * 4);
     if (e == cudaSuccess) e = cudaMemsetAsync(t->q, 0, (size_t)(O * t->rs), st);
@@ -288,8 +303,53 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
     return COLI_OK;
 }
 
+int coli_tensor_upload_host(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
+                            coli_tensor **out) {
+    g_msg[0] = 0;
+    if (int rc = check_upload(fmt, gs, O, I, data, scales, out)) return rc;
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    int64_t n_scales = 0;
+    coli_tensor *t = new_tensor(fmt, gs, O, I, &n_scales);
+    const int64_t hrb = host_row_bytes(fmt, I);
+    t->host = 1;
+    t->dev_bytes = 0;
+    CU(cudaGetDevice(&t->device), "cudaGetDevice");
+    const unsigned flags = cudaHostAllocMapped | cudaHostAllocPortable;
+    cudaError_t e = cudaHostAlloc(&t->hq, (size_t)(O * t->rs), flags);
+    if (e == cudaSuccess && n_scales) e = cudaHostAlloc(&t->hs, (size_t)n_scales * 4, flags);
+    if (e == cudaSuccess) {
+        // the device layout, written by the CPU: rows padded to 16 bytes with zeros,
+        // int8 stored offset binary
+        uint8_t *q = (uint8_t *)t->hq;
+        const uint8_t *src = (const uint8_t *)data;
+        for (int64_t o = 0; o < O; o++) {
+            uint8_t *row = q + o * t->rs;
+            memcpy(row, src + o * hrb, (size_t)hrb);
+            memset(row + hrb, 0, (size_t)(t->rs - hrb));
+            if (fmt == 1)
+                for (int64_t i = 0; i < hrb; i++) row[i] ^= 0x80;
+        }
+        if (n_scales) memcpy(t->hs, scales, (size_t)n_scales * 4);
+        e = cudaHostGetDevicePointer((void **)&t->q, t->hq, 0);
+        if (e == cudaSuccess && n_scales) e = cudaHostGetDevicePointer((void **)&t->s, t->hs, 0);
+    }
+    if (e != cudaSuccess) {
+        coli_tensor_free(t);
+        return cuda_fail(e, "coli_tensor_upload_host");
+    }
+    *out = t;
+    return COLI_OK;
+}
+
 void coli_tensor_free(coli_tensor *t) {
     if (!t) return;
+    if (t->host) {
+        if (t->hq) cudaFreeHost(t->hq);
+        if (t->hs) cudaFreeHost(t->hs);
+        delete t;
+        return;
+    }
     if (t->q) cudaFree(t->q);
     if (t->s) cudaFree(t->s);
     if (t->tmap) cudaFree(t->tmap);
@@ -316,8 +376,10 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
     const coli_tensor *W0 = W[0];
     uint64_t wbytes = 0;
     for (int m = 0; m < n; m++) wbytes += (uint64_t)W[m]->alg_bytes;
-    bool generic = false;
+    bool generic = false, host_any = false;
     for (int m = 0; m < n; m++) generic |= (W0->fmt == 4 && (W[m]->gs % 32) != 0);
+    // host-resident weights are read with plain loads only (no bulk copies, no TMA)
+    for (int m = 0; m < n; m++) host_any |= W[m]->host != 0;
     const size_t smem = gemv_smem_bytes(W0->fmt, W0->cpr, S, (int)W0->I, generic);
     bool slab = S == 1 && !generic;
     for (int m = 0; m < n && slab; m++) slab = slab_supported(W[m]->fmt, W[m]->gs) && W[m]->gs == W0->gs;
@@ -348,7 +410,7 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
         // groups per row; fmt 1-3: every O a multiple of 4, for the row-scale copies):
         // weights streamed by bulk copies (below ~4 MB the slab kernel's shorter start-up wins)
         const int fmt0 = W0->fmt;
-        bool stream = S == 1 && fmt0 >= 0 && fmt0 <= 4 && W0->I % 128 == 0 && ((uintptr_t)x & 15) == 0 &&
+        bool stream = S == 1 && !host_any && fmt0 >= 0 && fmt0 <= 4 && W0->I % 128 == 0 && ((uintptr_t)x & 15) == 0 &&
                       wbytes >= (4u << 20);
         for (int m = 0; m < n && stream; m++)
             stream = fmt0 == 4 ? (W[m]->gs == W0->gs && slab_supported(4, W[m]->gs) && W[m]->ng % 4 == 0)
@@ -377,7 +439,7 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
         }
         // S = 2..4 of the same int4 formats: half-chunk lanes keep all S activation rows in registers
         // (measured crossover against the row-pair kernel: S = 2 from ~16 MB of weights, S = 3-4 from ~4 MB)
-        bool stream_s = S >= 2 && S <= 4 && (W0->fmt == 4 || W0->fmt == 2) && W0->I % 128 == 0 &&
+        bool stream_s = S >= 2 && S <= 4 && !host_any && (W0->fmt == 4 || W0->fmt == 2) && W0->I % 128 == 0 &&
                         ((uintptr_t)x & 15) == 0 && wbytes >= (S == 2 ? (16u << 20) : (4u << 20));
         for (int m = 0; m < n && stream_s; m++)
             stream_s = W0->fmt == 4 ? (W[m]->gs == W0->gs && slab_supported(4, W[m]->gs) && W[m]->ng % 4 == 0)
@@ -658,13 +720,15 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
 
     const int n_slots = S * K;
     const int cpr_gu = g0->cpr, cpr_d = experts[0].down->cpr;
-    bool gs_ok = true;
+    bool gs_ok = true, host_any = false;
+    for (int e = 0; e < n_experts; e++)
+        host_any |= experts[e].gate->host || experts[e].up->host || experts[e].down->host;
     if (fmt == 4)
         for (int e = 0; e < n_experts && gs_ok; e++)
             gs_ok = experts[e].gate->gs % 32 == 0 && experts[e].up->gs % 32 == 0 && experts[e].down->gs % 32 == 0;
 
     // ---------------- decode, S = 1, int4 groups: weights streamed by bulk copies, one cooperative launch
-    if (S == 1 && fmt == 4 && n_slots <= kMaxDecodeSlots) {
+    if (S == 1 && fmt == 4 && n_slots <= kMaxDecodeSlots && !host_any) {
         const coli_tensor *d0 = experts[0].down;
         const int gs_gu = g0->gs, gs_d = d0->gs;
         // whole 128-input blocks (so every lane's 32-input chunk is in range) and a 16-byte aligned x

@@ -37,6 +37,9 @@ struct coli_tensor {
     int64_t dev_bytes, alg_bytes;
     uint64_t uid;        // unique per upload, never reused
     void *tmap;          // device copy of the codes' TMA descriptor (int4 formats), else NULL
+    int host;            // 1: codes and scales live in pinned host memory (q, s are the
+                         //    device-side addresses of that mapping; hq, hs the host ones)
+    void *hq, *hs;
 };
 
 namespace coli {

@@ -110,6 +110,25 @@ typedef struct {
 int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data,
                        const float *scales, void *stream, coli_tensor **out);
 
+/*
+ * Upload one weight matrix that STAYS IN HOST MEMORY (colibri-strix commit log:
+ * "metal: backend infrastructure" and "metal: batched moe_block + zero-copy
+ * slab registry" read expert slabs zero-copy from unified memory; "metal:
+ * overlap disk loads with GPU compute" computes resident experts while the
+ * others arrive).  The codes and scales are written, in the same padded layout
+ * the device copy uses, into pinned host memory mapped into the GPU's address
+ * space; the kernels read them over the CPU-GPU link (NVLink-C2C on Grace)
+ * every call, with plain loads, while device-resident matrices of the same
+ * call stream from HBM.
+ *   Arguments, layout and errors as coli_tensor_upload (no stream: nothing is
+ *   queued on the GPU).  data and scales may be freed when the call returns.
+ *   The tensor is used exactly like a device one (coli_matmul, expert tables,
+ *   mixed with device tensors); calls that touch one avoid the bulk-copy
+ *   kernels.  coli_tensor_info reports device_bytes = 0.
+ */
+int coli_tensor_upload_host(int fmt, int gs, int64_t O, int64_t I, const void *data,
+                            const float *scales, coli_tensor **out);
+
 /* Free a tensor (NULL is ignored).  The caller must make sure no queued work
  * still reads it (synchronize the streams that used it first). */
 void coli_tensor_free(coli_tensor *t);

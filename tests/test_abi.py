@@ -54,6 +54,10 @@ def test_upload_refuses_bad_format(lib, fmt, gs, code):
     assert rc == code
     assert out.value is None
     assert lib.coli_last_error()
+    out = ctypes.c_void_p(123)
+    rc = lib.coli_tensor_upload_host(fmt, gs, ctypes.c_int64(4), ctypes.c_int64(8), buf, sc, ctypes.byref(out))
+    assert rc == code
+    assert out.value is None
 
 
 def test_upload_refuses_bad_sizes(lib):
@@ -64,6 +68,9 @@ def test_upload_refuses_bad_sizes(lib):
     assert lib.coli_tensor_upload(2, 0, ctypes.c_int64(4), ctypes.c_int64(8), None, sc, None, ctypes.byref(out)) == -1
     assert lib.coli_tensor_upload(2, 0, ctypes.c_int64(4), ctypes.c_int64(8), buf, None, None, ctypes.byref(out)) == -1
     assert lib.coli_tensor_upload(2, 0, ctypes.c_int64(4), ctypes.c_int64(8), buf, sc, None, None) == -1
+    assert lib.coli_tensor_upload_host(2, 0, ctypes.c_int64(0), ctypes.c_int64(8), buf, sc, ctypes.byref(out)) == -1
+    assert lib.coli_tensor_upload_host(2, 0, ctypes.c_int64(4), ctypes.c_int64(8), None, sc, ctypes.byref(out)) == -1
+    assert lib.coli_tensor_upload_host(2, 0, ctypes.c_int64(4), ctypes.c_int64(8), buf, None, ctypes.byref(out)) == -1
 
 
 def test_compute_calls_refuse_null(lib):
