@@ -410,26 +410,28 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
         // groups per row; fmt 1-3: every O a multiple of 4, for the row-scale copies):
         // weights streamed by bulk copies (below ~4 MB the slab kernel's shorter start-up wins)
         const int fmt0 = W0->fmt;
-        bool stream = S == 1 && !host_any && fmt0 >= 0 && fmt0 <= 4 && W0->I % 128 == 0 && ((uintptr_t)x & 15) == 0 &&
-                      wbytes >= (4u << 20);
+        // (fmt 0 and 7 copy no scales with the rows: f32 has none, FP8 block scales are read from global)
+        const bool no_row_scales = fmt0 == 0 || fmt0 == 7;
+        bool stream = S == 1 && !host_any && ((fmt0 >= 0 && fmt0 <= 4) || fmt0 == 7) && W0->I % 128 == 0 &&
+                      ((uintptr_t)x & 15) == 0 && wbytes >= (4u << 20);
         for (int m = 0; m < n && stream; m++)
             stream = fmt0 == 4 ? (W[m]->gs == W0->gs && slab_supported(4, W[m]->gs) && W[m]->ng % 4 == 0)
-                               : (fmt0 == 0 || W[m]->O % 4 == 0);
+                               : (no_row_scales || W[m]->O % 4 == 0);
         const int lpr = stream ? (int)(W0->I / stream_lane_inputs(fmt0)) : 1;
         const int ns = (lpr + 31) / 32;
         stream = stream && kStreamConsumerWarps % ns == 0;
         if (stream) {
-            const int ng = fmt0 == 4 ? W0->ng : fmt0 == 0 ? 0 : 1;
+            const int ng = fmt0 == 4 ? W0->ng : no_row_scales ? 0 : 1;
             const int G = kStreamConsumerWarps / ns;
             int RG = std::min(4 * G, (int)(kStreamStageBytes / (W0->rs + 4 * ng)));
-            if (fmt0 != 0) RG = RG / 4 * 4;   // row-scale copies need whole groups of 4 rows
-            else RG = std::max(RG, 0);
+            if (!no_row_scales) RG = RG / 4 * 4;   // row-scale copies need whole groups of 4 rows
             const int total = job.row_start[n];
             int rpc = (total + ds->n_sm - 1) / ds->n_sm;
-            if (fmt0 != 0) rpc = (rpc + 3) / 4 * 4;   // CTA row blocks start on whole groups of 4 row scales
+            if (!no_row_scales) rpc = (rpc + 3) / 4 * 4;   // CTA row blocks start on whole groups of 4 row scales
             const int grid = (total + rpc - 1) / rpc;
-            const int gshift = fmt0 == 4 ? __builtin_ctz(W0->gs / 32) : 30;
-            if (RG >= (fmt0 == 0 ? 1 : 4) && (size_t)rpc * ns * 4 <= (size_t)kStreamRedBytes &&
+            // chunk -> scale index: fmt=4 groups of gs/32 chunks, FP8 blocks of 8 16-byte chunks
+            const int gshift = fmt0 == 4 ? __builtin_ctz(W0->gs / 32) : fmt0 == 7 ? 3 : 30;
+            if (RG >= (no_row_scales ? 1 : 4) && (size_t)rpc * ns * 4 <= (size_t)kStreamRedBytes &&
                 stream_gemv_smem() <= ds->smem_optin) {
                 e = launch_stream_gemv(job, rpc, RG, gshift, grid, st);
                 if (e != cudaSuccess) return cuda_fail(e, "matvec launch");

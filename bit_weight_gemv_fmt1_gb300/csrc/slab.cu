@@ -730,6 +730,41 @@ struct XRegF32 {
     }
 };
 
+// FP8 E4M3 (fmt=7), 16 inputs per lane: each byte pair converts exactly to an
+// f16 pair and then to f32 (no offset, no scaling); the 128 x 128 block scale
+// is applied per lane chunk by the caller (BlockScaled).
+struct XRegF8 {
+    static constexpr int LB = 16, NIN = 16;
+    using Q = uint4;
+    float4 v[4];   // inputs 4k..4k+3 of the lane's 16, natural order
+    __device__ __forceinline__ void set(const float4 (&raw)[4]) {
+#pragma unroll
+        for (int k = 0; k < 4; k++) v[k] = raw[k];
+    }
+    template <int N>
+    __device__ __forceinline__ void dotn(const uint4 (&q)[N], float (&out)[N]) const {
+        float2 a[N], b[N];
+#pragma unroll
+        for (int d = 0; d < N; d++) a[d] = b[d] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+#pragma unroll
+            for (int d = 0; d < N; d++) {
+                const uint32_t w = k == 0 ? q[d].x : k == 1 ? q[d].y : k == 2 ? q[d].z : q[d].w;
+                ffma2(a[d], e4m3x2_to_f32x2(w & 0xFFFFu), make_float2(v[k].x, v[k].y));
+                ffma2(b[d], e4m3x2_to_f32x2(w >> 16), make_float2(v[k].z, v[k].w));
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < N; d++) out[d] = (a[d].x + a[d].y) + (b[d].x + b[d].y);
+    }
+};
+
+// Decoders whose scale is per 128 x 128 block (read from global memory by the
+// consumer) instead of per row or per row group (copied with the rows).
+template <class XR> struct BlockScaled { static constexpr bool value = false; };
+template <> struct BlockScaled<XRegF8> { static constexpr bool value = true; };
+
 // Sums of four per-lane values over the warp with 6 shuffles: afterwards lane
 // 8k (k = 0..3) holds the total of value k.
 __device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v3, int lane) {
@@ -1127,13 +1162,15 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode
 }
 
 
-// ------------------------------------------------------------------ matvec, S = 1, int4, streamed
+// ------------------------------------------------------------------ matvec, S = 1, streamed
 // The same streaming scheme as the decode block's phase A for coli_matmul at
 // S = 1: rows of all matrices of the call form one index space, CTA b owns a
 // contiguous block of rpc rows, warp 12 copies stages of RG rows (codes and
 // scales) into the ring, warps 0-11 own one 512-byte slab each with the
 // activations in registers and form four row dot products per stage.  fmt=4
-// reads the group scale of each 32-input chunk, fmt=2 the row scale.
+// reads the group scale of each 32-input chunk, fmt 1-3 the row scale (both
+// copied with the rows), fmt=7 the scale of the chunk's 128 x 128 block (from
+// global memory, where the whole scale grid stays cached).
 template <int NWC, class XR>
 __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const GemvJob job, int rpc, int RG,
                                                                          int gshift, long long timeout_ns) {
@@ -1161,7 +1198,8 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const int ng = job.fmt == 4 ? job.ng[0] : job.fmt == 0 ? 0 : 1;   // scales per row (none for f32)
+    // scales copied with each row: none for f32 and for block-scaled FP8
+    const int ng = job.fmt == 4 ? job.ng[0] : (job.fmt == 0 || BlockScaled<XR>::value) ? 0 : 1;
     const long long rs = job.rs[0];
     // stage cursor: next row r, its matrix m
     int r = r0, m = 0;
@@ -1239,7 +1277,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
                 const int rr = sub + k * G;
                 const bool ok = okc && rr < sn;
                 qq[k] = ok ? *reinterpret_cast<const Q *>(src + rr * rs + c * XR::LB) : Q{};
-                sc[k] = !ok ? 0.f : ng == 0 ? 1.f : *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (c >> gshift)) * 4);
+                if constexpr (BlockScaled<XR>::value)
+                    sc[k] = ok ? __ldg(job.s[sm_] + (size_t)((so + rr) / kFp8Block) * job.ng[sm_] + (c >> gshift)) : 0.f;
+                else
+                    sc[k] = !ok ? 0.f : ng == 0 ? 1.f : *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (c >> gshift)) * 4);
             }
             xr.template dotn<4>(qq, dd);
             const float t = warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
@@ -1581,16 +1622,18 @@ cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, 
     case 2:
     case 4: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS4>);
     case 3: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS3>);
+    case 7: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegF8>);
     default: return cudaErrorInvalidValue;
     }
 }
 
 // code bytes and inputs of one lane of the streamed S = 1 matvec, per format (0: not streamed)
 int stream_lane_bytes(int fmt) {
-    return fmt == 0 ? XRegF32::LB : fmt == 1 ? XRegS1::LB : fmt == 3 ? XRegS3::LB : XRegS4::LB;
+    return fmt == 0 ? XRegF32::LB : fmt == 1 ? XRegS1::LB : fmt == 3 ? XRegS3::LB : fmt == 7 ? XRegF8::LB : XRegS4::LB;
 }
 int stream_lane_inputs(int fmt) {
-    return fmt == 0 ? XRegF32::NIN : fmt == 1 ? XRegS1::NIN : fmt == 3 ? XRegS3::NIN : XRegS4::NIN;
+    return fmt == 0 ? XRegF32::NIN : fmt == 1 ? XRegS1::NIN : fmt == 3 ? XRegS3::NIN : fmt == 7 ? XRegF8::NIN
+                                                                                       : XRegS4::NIN;
 }
 
 size_t stream_gemv_s_smem() {

@@ -119,7 +119,7 @@ def test_fp8_decode_table(S):
         assert np.array_equal(got[~np.isnan(got)], a[~np.isnan(a)])
 
 
-@pytest.mark.parametrize("O,I", [(300, 3000), (129, 385), (1, 17)])
+@pytest.mark.parametrize("O,I", [(300, 3000), (129, 385), (1, 17), (1000, 6144), (777, 6144)])
 @pytest.mark.parametrize("S", [1, 4, 20])
 def test_fp8_exact_integer_cases(O, I, S):
     """FP8 bytes whose values are multiples of 1/4 up to 8, power-of-two block
@@ -231,7 +231,7 @@ def test_streamed_matvec_exact_integers(fmt, gs):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("fmt,gs", [(2, 0), (4, 64), (1, 0), (3, 0), (0, 0)])
+@pytest.mark.parametrize("fmt,gs", [(2, 0), (4, 64), (1, 0), (3, 0), (0, 0), (7, 0)])
 def test_streamed_matvec_multi(fmt, gs):
     """Eight 2048 x 6144 matrices sharing one input (the weight-streaming
     layer) in one call: rows of all matrices in one index space, CTA row
