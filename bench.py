@@ -257,7 +257,7 @@ def _time_graph(torch, fn, n, warm=3):
     return a.elapsed_time(b) / 1e3 / n
 
 
-def bench_gemv(coli, torch, peaks, l2_bytes):
+def bench_gemv(coli, torch, peaks, l2_bytes, only=None):
     """Single fmt=4 GEMV and the format sweep, each over enough distinct copies
     of the matrix that the rotation exceeds 4x L2 (no call finds its weights in L2)."""
     out = {}
@@ -268,6 +268,10 @@ def bench_gemv(coli, torch, peaks, l2_bytes):
     # FP8 E4M3 with 128 x 128 block scales (uniform over the finite bytes), same shape
     cases.append(("fp8_fmt7_b128", 7, 0, wl.GEMV_SWEEP["O"], wl.GEMV_SWEEP["I"], wl.GEMV_SWEEP["S"],
                   wl.GEMV_SWEEP["seed"]))
+    if only:
+        cases = [c for c in cases if c[0] == only]
+        if not cases:
+            raise SystemExit(f"unknown --gemv-case {only}")
     for name, fmt, gs, O, I, Ss, seed in cases:
         g = wl.rng(seed + fmt + gs)
         if name.startswith("sweep"):
@@ -548,6 +552,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--experts", type=int, default=None, help="resident experts of the decode workload (default 256)")
     ap.add_argument("--quick", action="store_true", help="headline workload only (no by_workload sweep)")
+    ap.add_argument("--gemv-case", default=None,
+                    help="--workload gemv_sweep: run only this case (e.g. sweep_fmt4_g64, fp8_fmt7_b128)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()
@@ -568,7 +574,7 @@ def main():
                 res = bench_prefill(coli, torch, peaks, steps=max(1, args.steps), n_experts=args.experts_prefill)
             elif args.workload == "gemv_sweep":
                 l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
-                res = bench_gemv(coli, torch, peaks, l2)
+                res = bench_gemv(coli, torch, peaks, l2, only=args.gemv_case)
             elif args.workload == "router":
                 res = bench_router(coli, torch, peaks)
             elif args.workload == "host":
