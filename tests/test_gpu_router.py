@@ -116,3 +116,28 @@ def test_topk_refusals():
         coli.moe_topk(l, 0, ids, w)            # K < 1
     with pytest.raises(coli.ColiError):
         coli.moe_topk(l, 2, ids, w, top_p=float("nan"))
+
+
+def test_router_fp8_weights_exact():
+    """A router stored as FP8 (fmt=7, 128x128 block scales) with values that
+    make every logit exact in f32 (multiples of 1/4 up to 8, power-of-two block
+    scales, integer x): the routing equals the oracle's bit for bit."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(9200)
+    E, H, S, K = 256, 6144, 3, 8
+    vals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ok = np.flatnonzero(np.isfinite(vals) & (np.abs(vals) <= 8) & (np.mod(vals * 4, 1) == 0)).astype(np.uint8)
+    data = g.choice(ok, (E, H))
+    sc = (2.0 ** g.integers(-2, 3, wl.scale_count(7, E, H, 0))).astype(np.float32)
+    x = g.integers(-4, 5, (S, H)).astype(np.float32)
+    b = (g.integers(-8, 9, E) / 256.0).astype(np.float32)
+    Rt = coli.tensor_upload(7, 0, E, H, data, sc)
+    ids = torch.empty((S, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((S, K), device="cuda")
+    coli.moe_router(torch.from_numpy(x).cuda(), Rt, K, ids, w, bias=torch.from_numpy(b).cuda(), norm_topk=True)
+    coli.sync_check()
+    logits = orc.matmul(7, 0, E, H, data, sc, x)
+    rid, rw = orc.moe_topk(logits, K, bias=b, norm_topk=True)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=0.0)

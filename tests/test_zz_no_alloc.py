@@ -17,13 +17,13 @@ def _setup(coli, g, H, F, E, fmt, gs):
     return coli.ExpertTable([tuple(upload(coli, m) for m in trip) for trip in host])
 
 
-@pytest.mark.parametrize("S,K", [(1, 8), (4, 8)])
-def test_noalloc_matches_allocating_entry_point(S, K):
+@pytest.mark.parametrize("S,K,fmt,gs", [(1, 8, 4, 64), (4, 8, 4, 64), (1, 8, 7, 0), (3, 4, 7, 0)])
+def test_noalloc_matches_allocating_entry_point(S, K, fmt, gs):
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
     H, F, E = 1024, 512, 16
-    g = wl.rng(700 + S)
-    table = _setup(coli, g, H, F, E, 4, 64)
+    g = wl.rng(700 + S + fmt)
+    table = _setup(coli, g, H, F, E, fmt, gs)
     err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for call in range(2):
         x = torch.from_numpy(wl.activations(g, S, H)).cuda()
@@ -37,6 +37,30 @@ def test_noalloc_matches_allocating_entry_point(S, K):
         torch.cuda.synchronize()
         assert int(err.item()) == 0, f"call {call}: device error {int(err.item())}"
         assert norm_err(y.cpu().numpy(), y_ref.cpu().numpy()) <= TOL, f"call {call}"
+
+
+def test_noalloc_with_host_resident_experts():
+    """Half of the experts in pinned host memory: the no-allocation block
+    equals the allocating one."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E, S, K = 1024, 512, 8, 2, 8
+    g = wl.rng(705)
+    host = [wl.expert(g, H, F, 4, 64) for _ in range(E)]
+    table = coli.ExpertTable([tuple((coli.tensor_upload_host(m.fmt, m.gs, m.O, m.I, m.data, m.scales) if e % 2
+                                     else upload(coli, m)) for m in trip) for e, trip in enumerate(host)])
+    x = torch.from_numpy(wl.activations(g, S, H)).cuda()
+    ids_h, w_h = wl.routing_topk_softmax(g, S, E, K)
+    ids, w = torch.from_numpy(ids_h).cuda(), torch.from_numpy(w_h).cuda()
+    y_ref = torch.empty(S, H, device="cuda")
+    coli.moe_block(x, table, ids, w, y_ref)
+    coli.sync_check()
+    y = torch.full((S, H), float("nan"), device="cuda")
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    coli.moe_block_noalloc(x, table, ids, w, y, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert norm_err(y.cpu().numpy(), y_ref.cpu().numpy()) <= TOL
 
 
 def test_noalloc_allocates_nothing_after_first_call():
