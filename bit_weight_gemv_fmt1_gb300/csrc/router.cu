@@ -40,6 +40,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *logits,
     const int s = blockIdx.x;
     if (s >= S) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // launched as a programmatic dependent of the router matvec: its logits are
+    // visible once the wait returns
+    pdl_wait();
     const float *l = logits + (size_t)s * E;
     for (int e = tid; e < E; e += blockDim.x) {
         const float sc = (float)(1.0 / (1.0 + exp(-(double)l[e])));
@@ -83,6 +86,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *logits,
         }
         __syncthreads();
     }
+    pdl_trigger();
     if (tid == 0) {
         float wt[64];
         for (int k = 0; k < K; k++) wt[k] = score[s_sel[k]];
@@ -124,8 +128,8 @@ cudaError_t launch_topk(const float *logits, const float *bias, int S, int E, in
     const size_t smem = topk_smem(E);
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_kernel<<<S, kTopkThreads, smem, st>>>(logits, bias, S, E, K, top_p, norm_topk, routed_scale, ids, w);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3(S), dim3(kTopkThreads), smem, st, logits, bias, S, E, K, top_p, norm_topk,
+                      routed_scale, ids, w);
 }
 
 }  // namespace coli
