@@ -31,6 +31,10 @@
  *        buffer": the router is an f32 matvec followed by a sigmoid, then an
  *        exact top-K selection -- greedy argmax over sigmoid + bias with the
  *        CPU's tie order -- with top-p truncation, norm_topk and routed_scale.
+ *   [A]  PR #298 page, commit message on qt_addrow / qt_matvec_rows: the two
+ *        functions serve the kv_b MLA-absorption path; qt_matvec_rows is a
+ *        matvec over a range of rows of a quantized matrix, qt_addrow adds a
+ *        coefficient times one dequantized row into an accumulator.
  *   [P]  PR #298 page, commit message on qt_addrow / qt_matvec_rows (fmt=7):
  *        an fp8 "passthrough" format holding one raw byte per element (the
  *        byte convention of fmt=1) and ceil(O/128) * ceil(I/128) per-block
@@ -60,7 +64,12 @@
  *     no infinities; S.1111.111 is NaN), multiplied by the scale of block
  *     (o / 128, i / 128); the scales are stored block-row major,
  *     s[(o / 128) * ceil(I / 128) + i / 128]; blocks at the right and bottom
- *     edges are partial.  The gs argument is ignored for fmt=7.
+ *     edges are partial.  The gs argument is ignored for fmt=7;
+ *   - absorption ([A]): head h of n_heads owns rows o0 + h*stride + j,
+ *     j < n_rows; the row-range matvec gives each head its own input vector,
+ *     y[s][h][j] = sum_i w[o0+h*stride+j][i] x[s][h][i]; the transposed form
+ *     accumulates addrow over the head's rows in ascending row order,
+ *     y[s][h][i] = sum_j x[s][h][j] w[o0+h*stride+j][i]; y is overwritten.
  */
 #include <math.h>
 #include <stddef.h>
@@ -513,4 +522,67 @@ int oracle_moe_topk(const float *logits, const float *bias, int64_t S, int64_t E
     }
     free(score); free(key); free(taken);
     return 0;
+}
+
+/* Row-range matvec of the absorption path ([A], qt_matvec_rows), per head:
+ * y[s][h][j] = sum_i w[o0 + h*stride + j][i] * x[s][h][i], double accumulation
+ * in ascending i, rounded to f32 once.  x is [S][n_heads][I], y is
+ * [S][n_heads][n_rows]. */
+int oracle_matmul_rows(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
+                       int64_t o0, int64_t stride, int64_t n_rows, int64_t n_heads, int64_t S,
+                       const float *x, float *y)
+{
+    if (oracle_check(fmt, gs, O, I) || o0 < 0 || n_rows < 1 || n_heads < 1 || stride < 0 || S < 0 ||
+        o0 + (n_heads - 1) * stride + n_rows > O)
+        return ORACLE_EINVAL;
+#pragma omp parallel for collapse(3) schedule(static)
+    for (int64_t s = 0; s < S; s++)
+        for (int64_t h = 0; h < n_heads; h++)
+            for (int64_t j = 0; j < n_rows; j++) {
+                const int64_t o = o0 + h * stride + j;
+                const float *xv = x + (s * n_heads + h) * I;
+                double acc = 0.0;
+                for (int64_t i = 0; i < I; i++)
+                    acc += oracle_weight(fmt, gs, I, data, scales, o, i) * (double)xv[i];
+                y[(s * n_heads + h) * n_rows + j] = (float)acc;
+            }
+    return ORACLE_OK;
+}
+
+/* Transposed row-range product of the absorption path ([A], qt_addrow summed
+ * over a head's rows): y[s][h][i] = sum_j x[s][h][j] * w[o0 + h*stride + j][i],
+ * each row added in ascending j in double, rounded to f32 once.  x is
+ * [S][n_heads][n_rows], y is [S][n_heads][I]. */
+int oracle_matmul_rows_t(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
+                         int64_t o0, int64_t stride, int64_t n_rows, int64_t n_heads, int64_t S,
+                         const float *x, float *y)
+{
+    if (oracle_check(fmt, gs, O, I) || o0 < 0 || n_rows < 1 || n_heads < 1 || stride < 0 || S < 0 ||
+        o0 + (n_heads - 1) * stride + n_rows > O)
+        return ORACLE_EINVAL;
+    int rc = ORACLE_OK;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t s = 0; s < S; s++)
+        for (int64_t h = 0; h < n_heads; h++) {
+            double *acc = (double *)calloc((size_t)I, sizeof(double));
+            const float *xv = x + (s * n_heads + h) * n_rows;
+            if (!acc) {
+                rc = ORACLE_EINVAL;
+                continue;
+            }
+            for (int64_t j = 0; j < n_rows; j++) {
+#if ORACLE_MUTATION == 12
+                const int64_t o = o0 + h * n_rows + j;          /* planted: heads packed at n_rows, not stride */
+#else
+                const int64_t o = o0 + h * stride + j;
+#endif
+                const double c = (double)xv[j];
+                for (int64_t i = 0; i < I; i++)
+                    acc[i] += c * oracle_weight(fmt, gs, I, data, scales, o, i);   /* addrow */
+            }
+            for (int64_t i = 0; i < I; i++)
+                y[(s * n_heads + h) * I + i] = (float)acc[i];
+            free(acc);
+        }
+    return rc;
 }

@@ -73,6 +73,10 @@ def lib(mutation: int = 0) -> ctypes.CDLL:
             L.oracle_silu.argtypes = [ctypes.c_double]
             L.oracle_route.restype = _i64
             L.oracle_route.argtypes = [_ptr, _i64, _i64, _i64, _ptr, _ptr]
+            for fn in (L.oracle_matmul_rows, L.oracle_matmul_rows_t):
+                fn.restype = ctypes.c_int
+                fn.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _ptr, _ptr, _i64, _i64, _i64, _i64, _i64,
+                               _ptr, _ptr]
             L.oracle_moe_block.restype = ctypes.c_int
             L.oracle_moe_topk.argtypes = [_ptr, _ptr, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int,
                                           ctypes.c_float, _ptr, _ptr]
@@ -209,3 +213,29 @@ def moe_topk(logits, K: int, bias=None, top_p: float = 0.0, norm_topk: bool = Fa
     if rc:
         raise ValueError("oracle_moe_topk rejected its arguments")
     return ids, w
+
+
+def matmul_rows(fmt: int, gs: int, O: int, I: int, data, scales, o0: int, stride: int, n_rows: int, n_heads: int,
+                x, mutation: int = 0) -> np.ndarray:
+    """Per-head row-range matvec of the absorption path: x [S][n_heads][I] -> y [S][n_heads][n_rows]."""
+    d, s = _data(fmt, data), _scales(scales)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, n_heads, I)
+    y = np.empty((x.shape[0], n_heads, n_rows), dtype=np.float32)
+    rc = lib(mutation).oracle_matmul_rows(fmt, gs, O, I, _p(d), _p(s), o0, stride, n_rows, n_heads, x.shape[0],
+                                          _p(x), _p(y))
+    if rc:
+        raise ValueError("oracle_matmul_rows rejected its arguments")
+    return y
+
+
+def matmul_rows_t(fmt: int, gs: int, O: int, I: int, data, scales, o0: int, stride: int, n_rows: int, n_heads: int,
+                  x, mutation: int = 0) -> np.ndarray:
+    """Transposed per-head row-range product: x [S][n_heads][n_rows] -> y [S][n_heads][I]."""
+    d, s = _data(fmt, data), _scales(scales)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, n_heads, n_rows)
+    y = np.empty((x.shape[0], n_heads, I), dtype=np.float32)
+    rc = lib(mutation).oracle_matmul_rows_t(fmt, gs, O, I, _p(d), _p(s), o0, stride, n_rows, n_heads, x.shape[0],
+                                            _p(x), _p(y))
+    if rc:
+        raise ValueError("oracle_matmul_rows_t rejected its arguments")
+    return y

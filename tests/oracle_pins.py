@@ -443,11 +443,92 @@ def pin_fp8_unit_scale_vs_library(mutation=0):
     return bool(np.array_equal(y2, 2 * y64))
 
 
+def _absorb_cases(g):
+    """(fmt, gs, matrix, dequantized f64 matrix from raw codes / library decode)."""
+    out = []
+    O, I = 60, 70
+    for fmt, gs in ((0, 0), (1, 0), (2, 0), (3, 0), (4, 16), (4, 6), (7, 0)):
+        if fmt == 0:
+            m = wl.random_matrix(g, 0, O, I)
+            deq = m.data.astype(np.float64)
+        elif fmt == 7:
+            m = wl.random_matrix(g, 7, O, I)
+            deq = _e4m3_library(m.data) * np.repeat(np.repeat(m.scales.astype(np.float64).reshape(1, 1), O, 0), I, 1)
+        else:
+            codes = _raw(g, fmt, O, I)
+            sc = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(fmt, O, I, gs))
+            m = wl.Matrix(fmt, gs, O, I, wl.pack(fmt, codes), sc)
+            deq = _deq_from_raw(fmt, gs, codes, sc)
+        out.append((fmt, gs, m, deq))
+    return out
+
+
+def pin_absorb_vs_library(mutation=0):
+    """Absorption products ([A]) on heads with a row stride larger than the rows
+    per head: numpy over the matrix dequantized from raw codes (FP8: the
+    library decode; its 60 x 70 shape is one scale block), forward and
+    transposed, within f32 rounding."""
+    g = wl.rng(20)
+    o0, stride, n_rows, n_heads, S = 3, 17, 9, 3, 2
+    for fmt, gs, m, deq in _absorb_cases(g):
+        rows = np.array([[o0 + h * stride + j for j in range(n_rows)] for h in range(n_heads)])
+        xf = g.standard_normal((S, n_heads, m.I)).astype(np.float32)
+        xt = g.standard_normal((S, n_heads, n_rows)).astype(np.float32)
+        want_f = np.einsum("hji,shi->shj", deq[rows], xf.astype(np.float64))
+        want_t = np.einsum("hji,shj->shi", deq[rows], xt.astype(np.float64))
+        mag_f = np.einsum("hji,shi->shj", np.abs(deq[rows]), np.abs(xf.astype(np.float64)))
+        mag_t = np.einsum("hji,shj->shi", np.abs(deq[rows]), np.abs(xt.astype(np.float64)))
+        got_f = orc.matmul_rows(fmt, gs, m.O, m.I, m.data, m.scales, o0, stride, n_rows, n_heads, xf,
+                                mutation=mutation).astype(np.float64)
+        got_t = orc.matmul_rows_t(fmt, gs, m.O, m.I, m.data, m.scales, o0, stride, n_rows, n_heads, xt,
+                                  mutation=mutation).astype(np.float64)
+        if not (np.all(np.abs(got_f - want_f) <= 2.0 ** -23 * np.abs(want_f) + 1e-12 * mag_f) and
+                np.all(np.abs(got_t - want_t) <= 2.0 ** -23 * np.abs(want_t) + 1e-12 * mag_t)):
+            return False
+    return True
+
+
+def pin_absorb_addrow_single(mutation=0):
+    """One head of one row with coefficient c: the transposed product is
+    c times that dequantized row (qt_addrow), element for element."""
+    g = wl.rng(21)
+    for fmt, gs, m, deq in _absorb_cases(g):
+        for row in (0, 31, m.O - 1):
+            c = np.float32(g.standard_normal())
+            got = orc.matmul_rows_t(fmt, gs, m.O, m.I, m.data, m.scales, row, 0, 1, 1, np.array([[[c]]], np.float32),
+                                    mutation=mutation)[0, 0].astype(np.float64)
+            if not np.array_equal(got, (float(c) * deq[row]).astype(np.float32).astype(np.float64)):
+                return False
+    return True
+
+
+def pin_absorb_adjoint(mutation=0):
+    """The two absorption products are adjoint: <x_f, T(x_t)> = <F(x_f), x_t>
+    for every head, within the rounding of the f32 outputs."""
+    g = wl.rng(22)
+    o0, stride, n_rows, n_heads = 5, 11, 11, 4
+    for fmt, gs, m, _ in _absorb_cases(g):
+        xf = g.standard_normal((1, n_heads, m.I)).astype(np.float32)
+        xt = g.standard_normal((1, n_heads, n_rows)).astype(np.float32)
+        yf = orc.matmul_rows(fmt, gs, m.O, m.I, m.data, m.scales, o0, stride, n_rows, n_heads, xf,
+                             mutation=mutation).astype(np.float64)
+        yt = orc.matmul_rows_t(fmt, gs, m.O, m.I, m.data, m.scales, o0, stride, n_rows, n_heads, xt,
+                               mutation=mutation).astype(np.float64)
+        a = np.einsum("shi,shi->sh", xf.astype(np.float64), yt)
+        b = np.einsum("shj,shj->sh", yf, xt.astype(np.float64))
+        scale = np.einsum("shi,shi->sh", np.abs(xf.astype(np.float64)), np.abs(yt)) + \
+            np.einsum("shj,shj->sh", np.abs(yf), np.abs(xt.astype(np.float64)))
+        if not np.all(np.abs(a - b) <= 1e-5 * scale):
+            return False
+    return True
+
+
 PINS = [pin_golden_layout, pin_expert_bytes, pin_all_bytes_brute, pin_exact_integer_cases,
         pin_random_vs_library, pin_int8_unit_scale, pin_fmt4_wide_group_is_fmt2, pin_inline_order,
         pin_scale_linearity, pin_partial_last_group, pin_silu_closed_form, pin_route_vs_sorted,
         pin_moe_composition, pin_moe_invariants, pin_topk_worked_example, pin_topk_vs_sort,
-        pin_fp8_block_count, pin_fp8_all_bytes, pin_fp8_block_structure, pin_fp8_unit_scale_vs_library]
+        pin_fp8_block_count, pin_fp8_all_bytes, pin_fp8_block_structure, pin_fp8_unit_scale_vs_library,
+        pin_absorb_vs_library, pin_absorb_addrow_single, pin_absorb_adjoint]
 
 MUTATIONS = {
     1: "int4 nibble order swapped",
@@ -461,4 +542,5 @@ MUTATIONS = {
     9: "router selection ignores the bias",
     10: "fmt=7 block index transposed",
     11: "fmt=7 subnormals read as normals",
+    12: "absorption heads packed at n_rows instead of the row stride",
 }
