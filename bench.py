@@ -478,6 +478,33 @@ def bench_host(coli, torch, peaks, l2_bytes, steps=100):
     return out
 
 
+def bench_absorb(coli, torch, peaks, l2_bytes):
+    """kv_b absorption products at an MLA decode shape: kv_b of 128 heads x
+    (128 key + 128 value rows) x 512 latent inputs, int4 g64; per token the
+    transposed product over each head's key rows and the forward product over
+    its value rows, S = 1, rotated over copies exceeding 4x L2."""
+    n_heads, per_head, n_rows, I = 128, 256, 128, 512
+    g = wl.rng(4321)
+    m = wl.random_matrix(g, 4, n_heads * per_head, I, 64)
+    ncopy = max(2, math.ceil(4 * l2_bytes / m.nbytes))
+    Ws = [coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for _ in range(ncopy)]
+    half = m.nbytes / 2   # each product touches half of the rows
+    xt = torch.randn(1, n_heads, n_rows, device="cuda")
+    yt = torch.empty(1, n_heads, I, device="cuda")
+    xf = torch.randn(1, n_heads, I, device="cuda")
+    yf = torch.empty(1, n_heads, n_rows, device="cuda")
+    n = max(200, 2 * ncopy)
+    t_t = _time_graph(torch, lambda i: coli.matmul_rows_t(Ws[i % ncopy], 0, per_head, n_rows, n_heads, xt, yt), n)
+    t_f = _time_graph(torch, lambda i: coli.matmul_rows(Ws[i % ncopy], n_rows, per_head, n_rows, n_heads, xf, yf), n)
+    coli.sync_check()
+    res = {}
+    for name, t in (("key_rows_transposed", t_t), ("value_rows_forward", t_f)):
+        res[name] = {"us": t * 1e6, "GB/s": half / t / 1e9, "frac_hbm": half / t / 1e9 / peaks["hbm_gbs"]}
+    res["note"] = (f"kv_b {n_heads}x{per_head} rows x {I} inputs, int4 g64 ({m.nbytes / 1e6:.1f} MB, "
+                   f"{ncopy} copies); each product reads half of it")
+    return res
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle, timed as it stands, on a bounded
     sample of the default workload: one routed (row, expert) slot per step."""
@@ -550,7 +577,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default="moe_decode",
-                    choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming", "router", "host"),
+                    choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming", "router", "host", "absorb"),
                     help="moe_decode is the headline line; the others print their own line (for profiling)")
     ap.add_argument("--experts-prefill", type=int, default=None, help="resident experts of the prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -582,6 +609,9 @@ def main():
                 res = bench_gemv(coli, torch, peaks, l2, only=args.gemv_case)
             elif args.workload == "router":
                 res = bench_router(coli, torch, peaks)
+            elif args.workload == "absorb":
+                res = bench_absorb(coli, torch, peaks,
+                                   torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
             elif args.workload == "host":
                 res = bench_host(coli, torch, peaks,
                                  torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)

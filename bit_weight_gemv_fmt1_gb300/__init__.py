@@ -49,6 +49,8 @@ _lib.coli_tensor_free.restype = None
 _lib.coli_tensor_info.argtypes = [_vp] + [ctypes.POINTER(_int)] * 2 + [ctypes.POINTER(_i64)] * 4
 _lib.coli_matmul.argtypes = [_vp, _vp, _vp, _int, _vp]
 _lib.coli_matmul_multi.argtypes = [_int, ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp), _int, _vp]
+_lib.coli_matmul_rows.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _int, _vp]
+_lib.coli_matmul_rows_t.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _int, _vp]
 _lib.coli_moe_route.argtypes = [_vp, _int, _int, _int, _vp, _vp, _vp]
 _lib.coli_moe_block.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp]
 _lib.coli_moe_block_noalloc.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp, _vp]
@@ -62,6 +64,7 @@ _lib.coli_set_fail_after.argtypes = [_i64]
 _lib.coli_set_fail_after.restype = None
 
 EXPORTS = ("coli_tensor_upload", "coli_tensor_upload_host", "coli_tensor_free", "coli_tensor_info", "coli_matmul", "coli_matmul_multi",
+           "coli_matmul_rows", "coli_matmul_rows_t",
            "coli_moe_route", "coli_moe_topk", "coli_moe_router", "coli_moe_block", "coli_moe_block_noalloc",
            "coli_sync_check", "coli_last_error", "coli_get_stats", "coli_reset_stats", "coli_set_fail_after",
            "coli_version")
@@ -149,6 +152,26 @@ def matmul(W: Tensor, x, y, S: int | None = None, stream=None):
     """y[S, O] = x[S, I] @ W^T (x, y: contiguous float32 CUDA tensors)."""
     S = x.shape[0] if S is None else S
     _check(_lib.coli_matmul(W.handle, _ptr(x), _ptr(y), int(S), _stream(stream)))
+    return y
+
+
+def matmul_rows(W: Tensor, o0: int, stride: int, n_rows: int, n_heads: int, x, y, S: int | None = None,
+                stream=None):
+    """Per-head row-range matvec of the kv_b absorption path:
+    y[s, h, j] = sum_i W[o0 + h*stride + j, i] * x[s, h, i]  (x [S, n_heads, I], y [S, n_heads, n_rows])."""
+    S = x.shape[0] if S is None else S
+    _check(_lib.coli_matmul_rows(W.handle, int(o0), int(stride), int(n_rows), int(n_heads), _ptr(x), _ptr(y), int(S),
+                                 _stream(stream)))
+    return y
+
+
+def matmul_rows_t(W: Tensor, o0: int, stride: int, n_rows: int, n_heads: int, x, y, S: int | None = None,
+                  stream=None):
+    """Transposed per-head product: y[s, h, i] = sum_j x[s, h, j] * W[o0 + h*stride + j, i]
+    (x [S, n_heads, n_rows], y [S, n_heads, I])."""
+    S = x.shape[0] if S is None else S
+    _check(_lib.coli_matmul_rows_t(W.handle, int(o0), int(stride), int(n_rows), int(n_heads), _ptr(x), _ptr(y),
+                                   int(S), _stream(stream)))
     return y
 
 

@@ -564,6 +564,47 @@ int coli_matmul_multi(int n, const coli_tensor *const *W, const float *x, float 
     return run_matmul(n, W, x, y, S, (cudaStream_t)stream);
 }
 
+// ------------------------------------------------------------------ absorption
+static int run_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_rows, int n_heads, const float *x,
+                    float *y, int S, void *stream, bool transposed) {
+    g_msg[0] = 0;
+    if (int rc = check_tensor(W, "W")) return rc;
+    if (int rc = check_ptr(x, "x")) return rc;
+    if (int rc = check_ptr(y, "y")) return rc;
+    if (S < 1) return fail(COLI_EINVAL, "S must be >= 1 (got %d)", S);
+    if (n_heads < 1 || n_rows < 1 || n_rows > (1 << 30) || o0 < 0 || stride < 0)
+        return fail(COLI_EINVAL, "need n_heads >= 1, 1 <= n_rows <= 2^30, o0 >= 0, stride >= 0");
+    if (o0 + (int64_t)(n_heads - 1) * stride + n_rows > W->O)
+        return fail(COLI_EINVAL, "head rows run past the matrix: o0 + (n_heads-1)*stride + n_rows = %lld > O = %lld",
+                    (long long)(o0 + (int64_t)(n_heads - 1) * stride + n_rows), (long long)W->O);
+    if (int rc = injected()) return rc;
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    const int fmt = W->fmt;
+    const int N = fmt == 0 ? 2 : (fmt == 1 || fmt == 7) ? 8 : fmt == 3 ? 32 : 16;   // elements per 8-byte unit
+    const int units = (int)((W->I + N - 1) / N);
+    if (absorb_smem(fmt, transposed, units, (int)n_rows, S) > (size_t)ds->smem_optin)
+        return fail(COLI_EINVAL, "%s: the shared-memory stage (%zu bytes) exceeds the device limit",
+                    transposed ? "coli_matmul_rows_t" : "coli_matmul_rows",
+                    absorb_smem(fmt, transposed, units, (int)n_rows, S));
+    int nl = 0;
+    cudaError_t e = launch_absorb(desc_of(W), fmt, (int)W->I, units, o0, stride, (int)n_rows, n_heads, S, x, y,
+                                  transposed, (cudaStream_t)stream, &nl);
+    if (e != cudaSuccess) return cuda_fail(e, transposed ? "coli_matmul_rows_t" : "coli_matmul_rows");
+    count(nl, (uint64_t)n_heads * (uint64_t)n_rows * (uint64_t)W->rs);
+    return COLI_OK;
+}
+
+int coli_matmul_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_rows, int n_heads, const float *x,
+                     float *y, int S, void *stream) {
+    return run_rows(W, o0, stride, n_rows, n_heads, x, y, S, stream, false);
+}
+
+int coli_matmul_rows_t(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_rows, int n_heads, const float *x,
+                       float *y, int S, void *stream) {
+    return run_rows(W, o0, stride, n_rows, n_heads, x, y, S, stream, true);
+}
+
 // ------------------------------------------------------------------ routing
 int coli_moe_route(const int32_t *ids, int S, int K, int n_experts, int32_t *offsets, int32_t *order,
                    void *stream) {

@@ -649,6 +649,12 @@ int stream_lane_inputs(int fmt);
 cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st);
 cudaError_t stream_decode_occupancy(int *per_sm);
 
+// kv_b absorption products (absorb.cu)
+size_t absorb_smem(int fmt, bool transposed, int units, int n_rows, int S);
+cudaError_t launch_absorb(const MatDesc &m, int fmt, int I, int units, long long o0, long long stride, int n_rows,
+                          int n_heads, int S, const float *x, float *y, bool transposed, cudaStream_t st,
+                          int *n_launch);
+
 size_t topk_smem(int E);
 cudaError_t launch_topk(const float *logits, const float *bias, int S, int E, int K, float top_p, int norm_topk,
                         float routed_scale, int32_t *ids, float *w, cudaStream_t st);

@@ -170,6 +170,28 @@ int coli_matmul_multi(int n, const coli_tensor *const *W, const float *x, float 
                       void *stream);
 
 /*
+ * The two quantized products of the kv_b MLA-absorption path, batched over
+ * attention heads (PR #298 page, commit message on qt_addrow / qt_matvec_rows:
+ * a matvec over a range of rows of one quantized matrix, and the accumulation
+ * of coefficient times dequantized row).  Head h owns rows
+ * o0 + h*stride + j, j < n_rows, of W [O][I]:
+ *   coli_matmul_rows    y[s][h][j] = sum_i W[o0 + h*stride + j][i] * x[s][h][i]
+ *                       x: device f32 [S][n_heads][I]; y: [S][n_heads][n_rows]
+ *   coli_matmul_rows_t  y[s][h][i] = sum_j x[s][h][j] * W[o0 + h*stride + j][i]
+ *                       x: device f32 [S][n_heads][n_rows]; y: [S][n_heads][I]
+ *   W       any format (device or host resident); y overwritten, must not overlap x.
+ *   o0, stride, n_rows, n_heads  o0 >= 0, stride >= 0 (heads may share rows),
+ *           1 <= n_rows <= 2^30, n_heads >= 1, o0 + (n_heads-1)*stride + n_rows <= O.
+ *   S       rows of activations, >= 1 (each weight row is read once per 4 of them).
+ * Errors: COLI_EINVAL (pointers, ranges, a head's activations too long for the
+ * shared-memory stage), COLI_EDEVICE, COLI_ECUDA.
+ */
+int coli_matmul_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_rows, int n_heads,
+                     const float *x, float *y, int S, void *stream);
+int coli_matmul_rows_t(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_rows, int n_heads,
+                       const float *x, float *y, int S, void *stream);
+
+/*
  * Routing inversion: a stable counting sort of the slots (s, k), s < S, k < K,
  * by expert id ids[s*K+k] (colibri-strix commit log, "metal: batched
  * moe_block": per-row ragged routing; id -1 is an empty slot).
