@@ -269,11 +269,13 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
     DeviceState *ds = nullptr;
     if (int rc = device_state(&ds)) return rc;
     cudaStream_t st = (cudaStream_t)stream;
+    int device = 0;
+    CU(cudaGetDevice(&device), "cudaGetDevice");
 
     int64_t n_scales = 0;
     coli_tensor *t = new_tensor(fmt, gs, O, I, &n_scales);
     const int64_t hrb = host_row_bytes(fmt, I);
-    CU(cudaGetDevice(&t->device), "cudaGetDevice");
+    t->device = device;
     cudaError_t e = cudaMalloc(&t->q, (size_t)(O * t->rs));
     if (e == cudaSuccess && n_scales) e = cudaMalloc(&t->s, (size_t)n_scales * 4);
     if (e == cudaSuccess) e = cudaMemsetAsync(t->q, 0, (size_t)(O * t->rs), st);
@@ -309,12 +311,14 @@ int coli_tensor_upload_host(int fmt, int gs, int64_t O, int64_t I, const void *d
     if (int rc = check_upload(fmt, gs, O, I, data, scales, out)) return rc;
     DeviceState *ds = nullptr;
     if (int rc = device_state(&ds)) return rc;
+    int device = 0;
+    CU(cudaGetDevice(&device), "cudaGetDevice");
     int64_t n_scales = 0;
     coli_tensor *t = new_tensor(fmt, gs, O, I, &n_scales);
     const int64_t hrb = host_row_bytes(fmt, I);
     t->host = 1;
     t->dev_bytes = 0;
-    CU(cudaGetDevice(&t->device), "cudaGetDevice");
+    t->device = device;
     const unsigned flags = cudaHostAllocMapped | cudaHostAllocPortable;
     cudaError_t e = cudaHostAlloc(&t->hq, (size_t)(O * t->rs), flags);
     if (e == cudaSuccess && n_scales) e = cudaHostAlloc(&t->hs, (size_t)n_scales * 4, flags);
