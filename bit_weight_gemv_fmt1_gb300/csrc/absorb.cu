@@ -8,10 +8,10 @@
 //
 // Both kernels read the device layout in 8-byte units (2 f32, 8 int8/FP8, 16
 // int4, 32 int2 values), decode them exactly and accumulate in f32.  The
-// forward kernel gives each warp four head rows at once (lanes over the rows'
+// forward kernel gives each warp eight head rows at once (lanes over the rows'
 // units, the head's activations staged in shared memory, shuffle reductions);
 // the transposed kernel gives each lane one unit column of the head and a
-// slice of its rows, eight rows' loads in flight at a time, keeps the
+// slice of its rows, sixteen rows' loads in flight at a time, keeps the
 // coefficients in shared memory and reduces the row slices through shared
 // memory.  Weight loads that need nothing from the previous kernel are issued
 // before the dependency wait.  Rows are read exactly once per call for S <= 4.
@@ -94,7 +94,7 @@ struct AbsorbArgs {
 template <int FMT, int S_T, bool PS>
 __global__ void __launch_bounds__(kAbsorbThreads) absorb_fwd_kernel(const AbsorbArgs a, int s0) {
     extern __shared__ float xs[];   // [S_T][units * N]
-    constexpr int N = Unit<FMT>::N, RU = 4;
+    constexpr int N = Unit<FMT>::N, RU = 8;
     const int h = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int xlen = a.units * N;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_fwd_kernel(const Absorb
 template <int FMT, int S_T, bool PS>
 __global__ void __launch_bounds__(kAbsorbThreads) absorb_t_kernel(const AbsorbArgs a, int s0) {
     extern __shared__ float sm[];   // coef [S_T][n_rows], then partials [P][S_T][N][32]
-    constexpr int N = Unit<FMT>::N, RT = 8;
+    constexpr int N = Unit<FMT>::N, RT = 16;
     const int h = blockIdx.x;
     const int lane = threadIdx.x & 31, p = threadIdx.x >> 5, P = blockDim.x >> 5;
     float *coef = sm;
@@ -248,7 +248,7 @@ cudaError_t launch_one(const AbsorbArgs &a, bool transposed, int s0, cudaStream_
         auto kern = absorb_fwd_kernel<FMT, S_T, PS>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        const int rows_per_cta = (kAbsorbThreads / 32) * 4;   // RU rows per warp
+        const int rows_per_cta = (kAbsorbThreads / 32) * 8;   // RU rows per warp
         const dim3 grid(a.n_heads, (a.n_rows + rows_per_cta - 1) / rows_per_cta);
         return launch_pdl(kern, grid, dim3(kAbsorbThreads), smem, st, a, s0);
     }
