@@ -77,6 +77,11 @@ def test_compute_calls_refuse_null(lib):
     assert lib.coli_matmul(None, None, None, 1, None) == -1
     assert lib.coli_moe_route(None, 1, 8, 256, None, None, None) == -1
     assert lib.coli_moe_block(None, 1, None, 1, None, None, 8, None, None) == -1
+    i64 = ctypes.c_int64
+    assert lib.coli_matmul_rows(None, i64(0), i64(0), i64(1), 1, None, None, 1, None) == -1
+    assert lib.coli_matmul_rows_t(None, i64(0), i64(0), i64(1), 1, None, None, 1, None) == -1
+    assert lib.coli_moe_topk(None, None, 1, 8, 2, ctypes.c_float(0.0), 0, ctypes.c_float(1.0), None, None,
+                             None) == -1
 
 
 def test_fail_after_is_host_side(lib):
