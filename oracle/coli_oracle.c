@@ -247,7 +247,7 @@ int oracle_dequant_row(int fmt, int gs, int64_t O, int64_t I, const void *data,
 /* y[s][o] = sum_i w[o][i] * x[s][i], dequantize-then-multiply, accumulated in
  * double over i in ascending order and rounded to f32 once at the end.
  * y64 (optional) receives the double result, yabs (optional) the sum of
- * |w[o][i] * x[s][i]| that the pages use to judge rounding ([T], tolerance
+ * |w[o][i] * x[s][i]| that the pages use to assess rounding ([T], tolerance
  * paragraph). */
 int oracle_matmul(int fmt, int gs, int64_t O, int64_t I, const void *data, const float *scales,
                   int64_t S, const float *x, float *y, double *y64, double *yabs)
