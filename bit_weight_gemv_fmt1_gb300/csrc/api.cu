@@ -587,6 +587,10 @@ static int run_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_
     const int fmt = W->fmt;
     const int N = fmt == 0 ? 2 : (fmt == 1 || fmt == 7) ? 8 : fmt == 3 ? 32 : 16;   // elements per 8-byte unit
     const int units = (int)((W->I + N - 1) / N);
+    // grid y: 64-row blocks of a head (forward) or 32-unit column blocks (transposed)
+    if ((transposed ? (units + 31) / 32 : (n_rows + 63) / 64) > 65535)
+        return fail(COLI_EINVAL, "%s: %s too large for one launch",
+                    transposed ? "coli_matmul_rows_t" : "coli_matmul_rows", transposed ? "I" : "n_rows");
     if (absorb_smem(fmt, transposed, units, (int)n_rows, S) > (size_t)ds->smem_optin)
         return fail(COLI_EINVAL, "%s: the shared-memory stage (%zu bytes) exceeds the device limit",
                     transposed ? "coli_matmul_rows_t" : "coli_matmul_rows",
