@@ -505,6 +505,36 @@ def bench_absorb(coli, torch, peaks, l2_bytes):
     return res
 
 
+def bench_decode_formats(coli, torch, peaks, steps=200):
+    """The decode expert block (H=6144, F=2048, S=1, top-8, a fresh routing per
+    call) for expert tables of other formats than the headline's int4 g64:
+    FP8 E4M3 with 128x128 block scales and int8; a 64-expert resident pool
+    (every pool > 2 GB, so L2 holds a small part of it)."""
+    d = wl.MOE_DECODE
+    H, F, K = d["H"], d["F"], d["K"]
+    out = {}
+    for name, fmt, gs in (("fp8_fmt7_b128", 7, 0), ("int8_fmt1", 1, 0)):
+        g = wl.rng(d["seed"] + 300 + fmt)
+        hosts = [wl.expert(g, H, F, fmt, gs) for _ in range(8)]
+        n_pool = 64
+        dev = [tuple(coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in hosts[e % 8])
+               for e in range(n_pool)]
+        table = coli.ExpertTable(dev)
+        ids_h, w_h = wl.routing_topk_softmax(g, steps, n_pool, K)
+        ids = torch.from_numpy(ids_h).cuda()
+        w = torch.from_numpy(w_h).cuda()
+        xs = torch.randn(steps, 1, H, device="cuda")
+        y = torch.empty(1, H, device="cuda")
+        t = _time_graph(torch, lambda i: coli.moe_block(xs[i], table, ids[i: i + 1], w[i: i + 1], y), steps)
+        coli.sync_check()
+        nbytes = K * wl.expert_bytes(H, F, fmt, gs)
+        out[name] = {"us": t * 1e6, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+                     "pool_GB": n_pool * wl.expert_bytes(H, F, fmt, gs) / 1e9}
+        del dev, table
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle, timed as it stands, on a bounded
     sample of the default workload: one routed (row, expert) slot per step."""
@@ -577,7 +607,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default="moe_decode",
-                    choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming", "router", "host", "absorb"),
+                    choices=("moe_decode", "moe_prefill", "gemv_sweep", "streaming", "router", "host", "absorb",
+                             "decode_formats"),
                     help="moe_decode is the headline line; the others print their own line (for profiling)")
     ap.add_argument("--experts-prefill", type=int, default=None, help="resident experts of the prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -609,6 +640,8 @@ def main():
                 res = bench_gemv(coli, torch, peaks, l2, only=args.gemv_case)
             elif args.workload == "router":
                 res = bench_router(coli, torch, peaks)
+            elif args.workload == "decode_formats":
+                res = bench_decode_formats(coli, torch, peaks)
             elif args.workload == "absorb":
                 res = bench_absorb(coli, torch, peaks,
                                    torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
