@@ -78,6 +78,8 @@ struct Workspace {
     size_t cap = 0;
     void *rbuf = nullptr;         // router logits (kept apart from buf, which the router matvec may use)
     size_t rcap = 0;
+    unsigned *cnt = nullptr;      // counters of the streamed decode block (zero between calls)
+    size_t cnt_cap = 0;           // words
 };
 
 struct CachedTable {
@@ -144,8 +146,7 @@ int workspace(DeviceState *d, cudaStream_t st, size_t bytes, Workspace **out) {
     std::lock_guard<std::mutex> lk(d->mu);
     Workspace &w = d->ws[st];
     if (!w.bar) {
-        // words 0-1: counter and generation of the resetting grid barrier;
-        // bytes 128-135: the monotonic 64-bit arrival counter of the streamed decode
+        // words 0-1: counter and generation of the resetting grid barrier
         CU(cudaMalloc(&w.bar, kBarrierBytes), "cudaMalloc(barrier)");
         CU(cudaMemset(w.bar, 0, kBarrierBytes), "cudaMemset(barrier)");
     }
@@ -161,6 +162,27 @@ int workspace(DeviceState *d, cudaStream_t st, size_t bytes, Workspace **out) {
         w.cap = want;
     }
     *out = &w;
+    return COLI_OK;
+}
+
+// Counter words of the streamed decode block for this stream, zero at
+// allocation; the kernel leaves them zero at the end of every call.
+int decode_counters(DeviceState *d, cudaStream_t st, size_t words, unsigned **out) {
+    std::lock_guard<std::mutex> lk(d->mu);
+    Workspace &w = d->ws[st];
+    if (w.cnt_cap < words) {
+        if (w.cnt) {
+            CU(cudaDeviceSynchronize(), "cudaDeviceSynchronize(counter growth)");
+            CU(cudaFree(w.cnt), "cudaFree(counters)");
+            w.cnt = nullptr;
+            w.cnt_cap = 0;
+        }
+        const size_t want = std::max<size_t>(words, 4096);
+        CU(cudaMalloc(&w.cnt, want * sizeof(unsigned)), "cudaMalloc(counters)");
+        CU(cudaMemset(w.cnt, 0, want * sizeof(unsigned)), "cudaMemset(counters)");
+        w.cnt_cap = want;
+    }
+    *out = w.cnt;
     return COLI_OK;
 }
 
@@ -778,61 +800,38 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         for (int e = 0; e < n_experts && gs_ok; e++)
             gs_ok = experts[e].gate->gs % 32 == 0 && experts[e].up->gs % 32 == 0 && experts[e].down->gs % 32 == 0;
 
-    // ---------------- decode, S = 1, int4 groups: weights streamed by bulk copies, one cooperative launch
-    if (S == 1 && fmt == 4 && n_slots <= kMaxDecodeSlots && !host_any) {
+    // ---------------- decode, S = 1, int4 / int8 tables: weights streamed by bulk copies, dp4a decode,
+    // one cooperative launch
+    if (S == 1 && (fmt == 1 || fmt == 2 || fmt == 4) && n_slots <= kMaxDecodeSlots && !host_any) {
         const coli_tensor *d0 = experts[0].down;
         const int gs_gu = g0->gs, gs_d = d0->gs;
-        // whole 128-input blocks (so every lane's 32-input chunk is in range) and a 16-byte aligned x
-        bool ok = gs_gu % 32 == 0 && gs_d % 32 == 0 && slab_supported(4, gs_gu) && slab_supported(4, gs_d) &&
-                  g0->ng % 4 == 0 && d0->ng % 4 == 0 && H % 128 == 0 && F % 128 == 0 &&
-                  ((uintptr_t)x & 15) == 0;
-        for (int e = 0; e < n_experts && ok; e++)
+        // one gs per role, a power-of-two number of 16-byte chunks per group
+        bool ok = fmt != 4 || (slab_supported(4, gs_gu) && slab_supported(4, gs_d));
+        for (int e = 0; e < n_experts && ok && fmt == 4; e++)
             ok = experts[e].gate->gs == gs_gu && experts[e].up->gs == gs_gu && experts[e].down->gs == gs_d;
-        const int nsA = (cpr_gu + 31) / 32, nsB = (cpr_d + 31) / 32;
-        ok = ok && kStreamConsumerWarps % nsA == 0 && kStreamConsumerWarps % nsB == 0;
-        const int rs_gu = (int)g0->rs, rs_d = (int)d0->rs;
-        // each consumer warp takes at most 2 pairs (phase A) or 4 rows (phase B) of a stage
-        const int RP = std::min(kStreamStageBytes / (2 * (rs_gu + 4 * g0->ng)), 2 * (kStreamConsumerWarps / nsA));
-        const int RB = std::min(kStreamStageBytes / (rs_d + 4 * d0->ng), 4 * (kStreamConsumerWarps / nsB));
-        const int grid = ds->n_sm;
-        const long long ppc = ((long long)K * F + grid - 1) / grid, rpc = (H + grid - 1) / grid;
-        ok = ok && RP >= 1 && RB >= 1 && (long long)staged_len(4, cpr_gu) * 4 <= kStreamXhBytes &&
-             (long long)K * staged_len(4, cpr_d) * 4 <= kStreamXhBytes &&
-             ppc * nsA * 2 * 4 <= kStreamRedBytes && (long long)K * rpc * nsB * 4 <= kStreamRedBytes &&
-             stream_decode_smem() <= (size_t)ds->smem_optin;
+        SdArgs a;
+        size_t smem = 0;
         int per_sm = 0;
-        if (ok && stream_decode_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) {
+        if (ok && sd_plan(fmt, (int)H, (int)F, K, cpr_gu, cpr_d, (int)g0->rs, (int)d0->rs, g0->ng, d0->ng, ds->n_sm,
+                          (size_t)ds->smem_optin, &a, &smem) &&
+            sd_occupancy(a, smem, &per_sm) == cudaSuccess && per_sm >= 1) {
             Workspace *ws = nullptr;
-            const size_t hstride = std::max((size_t)F, (size_t)staged_len(4, cpr_d));
-            if (int rc = workspace(ds, st, (size_t)n_slots * hstride * sizeof(float), &ws)) return rc;
-            StreamArgs a;
-            memset(&a, 0, sizeof a);
-            a.m.x = x;
-            a.m.ids = ids;
-            a.m.w = w;
-            a.m.y = y;
-            a.m.table = table;
-            a.m.n_experts = n_experts;
-            a.m.S = 1;
-            a.m.K = K;
-            a.m.H = (int)H;
-            a.m.F = (int)F;
-            a.m.cpr_gu = cpr_gu;
-            a.m.cpr_d = cpr_d;
-            a.m.hbuf = (float *)ws->buf;
-            a.m.bar = ws->bar;
-            a.m.err = ds->err;
-            a.m.timeout_ns = 2000000000LL;
-            a.rs_gu = rs_gu;
-            a.rs_d = rs_d;
-            a.ng_gu = g0->ng;
-            a.ng_d = d0->ng;
-            a.gshift_gu = __builtin_ctz(gs_gu / 32);
-            a.gshift_d = __builtin_ctz(gs_d / 32);
-            a.RP = RP;
-            a.RB = RB;
-            a.red_floats = kStreamRedBytes / 4;
-            cudaError_t e = launch_stream_decode(a, grid, st);
+            if (int rc = workspace(ds, st, sd_scratch_bytes(a), &ws)) return rc;
+            unsigned *ctr = nullptr;
+            if (int rc = decode_counters(ds, st, sd_counter_words(a), &ctr)) return rc;
+            a.x = x;
+            a.ids = ids;
+            a.w = w;
+            a.y = y;
+            a.table = table;
+            a.n_experts = n_experts;
+            a.gshift_gu = fmt == 4 ? __builtin_ctz(gs_gu / 32) : 0;
+            a.gshift_d = fmt == 4 ? __builtin_ctz(gs_d / 32) : 0;
+            a.hbuf = (float *)ws->buf;
+            a.ctr = ctr;
+            a.err = ds->err;
+            a.timeout_ns = 2000000000LL;
+            cudaError_t e = launch_stream_decode(a, ds->n_sm, smem, st);
             if (e != cudaSuccess) return cuda_fail(e, "decode expert-block launch");
             count(1, 0);
             return COLI_OK;

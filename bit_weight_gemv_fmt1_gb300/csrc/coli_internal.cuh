@@ -621,24 +621,47 @@ cudaError_t launch_combine(const float *slot_out, const int32_t *inv, const floa
 cudaError_t launch_fmt1_encode(uint8_t *q, long long n, cudaStream_t st);
 size_t gemv_smem_bytes(int fmt, int cpr, int S, int I, bool generic);
 
-// S = 1 kernels with the activation slab in registers (slab.cu).
-// Streamed decode block (S = 1): weights arrive in shared memory by bulk
-// copies; see moe_decode_stream_kernel.
-struct StreamArgs {
-    MoeDecodeArgs m;          // x, ids, w, y, table, n_experts, K, H, F, cpr_gu, cpr_d, hbuf, bar, err, timeout_ns
-    int rs_gu, rs_d;          // bytes per gate/up row and per down row
-    int ng_gu, ng_d;          // scales per row
-    int gshift_gu, gshift_d;  // log2(gs / 32): chunk -> group
-    int RP, RB;               // gate/up row pairs per phase-A stage, down rows per phase-B stage
-    int red_floats;           // capacity of the per-CTA partial-sum buffer
+// Streamed decode expert block, S = 1, int4 (fmt 2/4) and int8 (fmt 1) tables
+// (stream_decode.cu): weights arrive in shared memory by bulk copies, the
+// activations live in registers as dp4a limbs.  sd_plan fills the geometry.
+struct SdArgs {
+    const float *x;
+    const int32_t *ids;
+    const float *w;
+    float *y;
+    const ExpertDesc *table;
+    int n_experts, K, H, F;
+    int fmt;
+    int nc;                    // consumer warps (the producer is one more)
+    int n_groups, group_warps; // consumer groups (stage k goes to group k mod n_groups) and warps per group
+    int nsA, nsB;              // 512-byte slabs per gate/up row and per down row
+    int cpr_gu, cpr_d;         // 16-byte chunks per gate/up row and per down row
+    int rs_gu, rs_d;           // device row strides (bytes)
+    int ng_gu, ng_d;           // scales per row (1 for per-row formats)
+    int gshift_gu, gshift_d;   // chunk -> group index shift (grouped formats)
+    int grouped;               // 1: per-group scales copied with the rows; 0: one scale per row
+    int RP, RB;                // gate/up pairs per phase-A stage, down rows per expert and phase-B stage
+    int stage_bytes, n_stages;
+    int off_redA, off_redB, off_desc, off_bar;   // dynamic shared-memory layout (bytes)
+    float *hbuf;               // [K][F] scratch: h
+    unsigned *ctr;             // zeroed counters: unused, CTAs out, barrier arrivals
+    int *err;                  // device error word
+    long long timeout_ns;      // bound of every wait
 };
+bool sd_plan(int fmt, int H, int F, int K, int cpr_gu, int cpr_d, int rs_gu, int rs_d, int ng_gu, int ng_d,
+             int n_sm, size_t smem_max, SdArgs *a, size_t *smem);
+cudaError_t sd_occupancy(const SdArgs &a, size_t smem, int *per_sm);
+size_t sd_scratch_bytes(const SdArgs &a);
+size_t sd_counter_words(const SdArgs &a);
+cudaError_t launch_stream_decode(const SdArgs &a, int grid, size_t smem, cudaStream_t st);
+
+// Streamed S = 1 matvec (slab.cu): the same bulk-copy ring over the rows of all
+// matrices of the call.
 constexpr size_t kBarrierBytes = 256;           // per-workspace grid-barrier words (see workspace())
 constexpr int kStreamStageBytes = 27 * 1024;
 constexpr int kStreamStages = 5;
-constexpr int kStreamXhBytes = 64 * 1024;     // staged x (phase A) or h of the routed experts (phase B)
 constexpr int kStreamRedBytes = 12 * 1024;
 constexpr int kStreamConsumerWarps = 12;
-size_t stream_decode_smem();
 size_t stream_gemv_smem();
 constexpr int kStreamGemvRedBytes = 64 * 1024;   // partial sums of the S = 2..4 streamed matvec
 size_t stream_gemv_s_smem();
@@ -646,8 +669,6 @@ cudaError_t launch_stream_gemv_s(const GemvJob &job, int rpc, int RG, int gshift
 cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, int grid, cudaStream_t st);
 int stream_lane_bytes(int fmt);
 int stream_lane_inputs(int fmt);
-cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st);
-cudaError_t stream_decode_occupancy(int *per_sm);
 
 // kv_b absorption products (absorb.cu)
 size_t absorb_smem(int fmt, bool transposed, int units, int n_rows, int S);

@@ -471,23 +471,8 @@ __global__ void __launch_bounds__(kSlabThreads, 2) moe_decode_slab_kernel(const 
 }
 
 
-// ------------------------------------------------------------------ decode block, S = 1, streamed
-// One CTA per SM.  Warp 12 streams the CTA's weight rows into a ring of
-// shared-memory stages with bulk copies (cp.async.bulk: whole rows, with
-// their group scales), five stages of 27 KB, so ~20 MB is in flight over the
-// GPU -- enough to cover HBM latency -- without any register cost.  Warps
-// 0-11 consume: warp w owns slab (w mod n_slab) of every row, keeps the
-// activations of that slab in registers (XReg), and reduces each (row, slab)
-// unit across the warp into a partial-sum buffer; sums over slabs, experts
-// and the SiLU are taken in a fixed order, so results do not depend on timing.
-//   phase A: stages of RP (gate row j, up row j) pairs of one routed expert;
-//            the CTA's pairs are a contiguous range of (expert, j);
-//            h[a][j] = silu(sum_s g) * sum_s u -> global scratch
-//   grid barrier (consumer warps only; the producer keeps streaming the
-//            phase-B rows, which do not depend on h)
-//   phase B: stages of RB down rows of one routed expert; the CTA owns rows
-//            [oc0, oc1) of y and adds the experts in ascending id order.
-// int4 chunk dot product without the offset-removal adds (streamed decode).
+// ------------------------------------------------------------------ lane decoders of the streamed matvec
+// int4 chunk dot product without the offset-removal adds.
 // A code n at bit position p of a word, AND-ed out with no exponent bits, is
 // the f32 subnormal n * 2^(p-149), exactly.  Each lane holds its chunk's
 // activations multiplied by 2^(k-p), p the bit position its code will sit at
@@ -781,386 +766,6 @@ __device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v
     k += __shfl_xor_sync(0xffffffffu, k, 1);
     return k;
 }
-
-struct StreamStage {
-    int kind;   // 0: phase A pairs, 1: phase B rows
-    int ai;     // routed-expert index (ascending expert id)
-    int row0, n;
-};
-struct StreamCursor {
-    long long left;      // phase-A pairs still to issue
-    int ai, j;           // next phase-A pair: routed expert ai, row j (kept without division)
-    int bai, o, oc0, oc1, nact;
-    __device__ __forceinline__ bool next(const StreamArgs &a, StreamStage &st) {
-        if (left > 0) {
-            const int n = (int)min((long long)min(a.RP, a.m.F - j), left);
-            st = {0, ai, j, n};
-            left -= n;
-            j += n;
-            if (j == a.m.F) {
-                j = 0;
-                ai++;
-            }
-            return true;
-        }
-        if (bai < nact && o < oc1) {
-            const int n = min(a.RB, oc1 - o);
-            st = {1, bai, o, n};
-            o += n;
-            if (o >= oc1) {
-                o = oc0;
-                bai++;
-            }
-            return true;
-        }
-        return false;
-    }
-};
-
-template <int FMT>
-__global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 1) moe_decode_stream_kernel(const StreamArgs a) {
-    constexpr int NWC = kStreamConsumerWarps, NCT = NWC * 32, NS = kStreamStages, SB = kStreamStageBytes;
-    extern __shared__ uint8_t sraw[];
-    uint8_t *ring = (uint8_t *)(((uintptr_t)sraw + 127) & ~(uintptr_t)127);
-    uint32_t *xh = reinterpret_cast<uint32_t *>(ring + NS * SB);
-    float *red = reinterpret_cast<float *>(ring + NS * SB + kStreamXhBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + NS * SB + kStreamXhBytes + kStreamRedBytes);
-    uint64_t *empty = full + NS;
-    __shared__ int s_ids[kMaxDecodeSlots];
-    __shared__ float s_w[kMaxDecodeSlots];
-    __shared__ int s_exp[kMaxDecodeSlots];
-    __shared__ float s_ew[kMaxDecodeSlots];
-    __shared__ int s_nact, s_bad;
-    __shared__ volatile int abort_flag;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const MoeDecodeArgs &m = a.m;
-    const int n = m.K;   // S = 1
-    const uint64_t deadline = global_ns() + (uint64_t)m.timeout_ns;
-    // consumer lanes start loading their activation chunk now; it is used after phase 0
-    const int nsA = (m.cpr_gu + 31) >> 5, slA = warp % nsA;
-    // (lanes past the row's last chunk hold zeros)
-    float4 xraw[8];
-#pragma unroll
-    for (int j = 0; j < 8; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (warp < NWC && slA * 32 + lane < m.cpr_gu) {
-        const float4 *p = reinterpret_cast<const float4 *>(m.x + (size_t)(slA * 32 + lane) * 32);
-#pragma unroll
-        for (int j = 0; j < 8; j++) xraw[j] = __ldg(p + j);
-    }
-
-    // ---- phase 0: distinct routed experts in ascending id order, weights summed.
-    // The producer warp reads the token's slots (its lane t holds slot t when
-    // K <= 32) while the consumer lanes' activation loads are in flight.
-    const int pl = tid - NWC * 32;   // producer-warp lane, or negative
-    int my_id = -1;
-    float my_w = 0.f;
-    if (pl >= 0 && pl < n) {
-        my_id = m.ids[pl];
-        my_w = m.w[pl];
-    }
-    if (tid == 0) {
-        abort_flag = 0;
-        for (int i = 0; i < NS; i++) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NWC);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (n <= 32) {
-        if (warp == NWC) {
-            const bool valid = pl < n;
-            const bool bad = valid && (my_id < -1 || my_id >= m.n_experts);
-            const unsigned any_bad = __ballot_sync(0xffffffffu, bad);
-            bool first = valid && my_id >= 0;
-            int rank = 0;
-            float wsum = 0.f;
-            for (int t = 0; t < n; t++) {
-                const int f = __shfl_sync(0xffffffffu, my_id, t);
-                const float wt = __shfl_sync(0xffffffffu, my_w, t);
-                if (f == my_id) {
-                    wsum += wt;
-                    if (t < pl) first = false;
-                }
-                // count each smaller id once, at its first slot
-                const unsigned same_before = __ballot_sync(0xffffffffu, pl < t && my_id == f);
-                if (f >= 0 && f < my_id && same_before == 0u) rank++;
-            }
-            if (first && !any_bad) {
-                s_exp[rank] = my_id;
-                s_ew[rank] = wsum;
-            }
-            const unsigned nf = __popc(__ballot_sync(0xffffffffu, first));
-            if (lane == 0) {
-                s_bad = any_bad != 0u;
-                s_nact = (int)nf;
-            }
-        }
-        __syncthreads();
-    } else {
-        if (tid == 0) {
-            s_bad = 0;
-            s_nact = 0;
-        }
-        __syncthreads();
-        if (tid < n) {
-            const int e = m.ids[tid];
-            s_ids[tid] = e;
-            s_w[tid] = m.w[tid];
-            if (e < -1 || e >= m.n_experts) atomicOr(&s_bad, 1);
-        }
-        __syncthreads();
-        if (!s_bad && tid < n) {
-            const int e = s_ids[tid];
-            bool first = e >= 0;
-            int rank = 0;
-            float wsum = 0.f;
-            for (int t = 0; t < n; t++) {
-                const int f = s_ids[t];
-                if (f == e) {
-                    wsum += s_w[t];
-                    if (t < tid) first = false;
-                }
-                if (f >= 0 && f < e) {
-                    bool fst = true;   // count each smaller id once, at its first slot
-                    for (int u = 0; u < t; u++) fst &= s_ids[u] != f;
-                    rank += fst;
-                }
-            }
-            if (first) {
-                s_exp[rank] = e;
-                s_ew[rank] = wsum;
-                atomicAdd(&s_nact, 1);
-            }
-        }
-        __syncthreads();
-    }
-    if (s_bad) {
-        if (blockIdx.x == 0 && tid == 0) atomicCAS(m.err, 0, DEV_ERR_BAD_ID);
-        return;
-    }
-    const int nact = s_nact;
-
-    // work of this CTA
-    const long long pairs = (long long)nact * m.F;
-    const long long ppc = (pairs + gridDim.x - 1) / gridDim.x;
-    const long long pr0 = min(pairs, (long long)blockIdx.x * ppc), pr1 = min(pairs, pr0 + ppc);
-    const int rpc = (m.H + gridDim.x - 1) / gridDim.x;
-    const int oc0 = min(m.H, (int)blockIdx.x * rpc), oc1 = min(m.H, oc0 + rpc);
-    StreamCursor cur;
-    cur.left = pr1 - pr0;
-    cur.ai = (int)(pr0 / m.F);
-    cur.j = (int)(pr0 - (long long)cur.ai * m.F);
-    cur.bai = 0;
-    cur.o = oc0;
-    cur.oc0 = oc0;
-    cur.oc1 = oc1;
-    cur.nact = nact;
-    const int offA_u = a.RP * a.rs_gu, offA_sg = 2 * a.RP * a.rs_gu, offA_su = offA_sg + a.RP * a.ng_gu * 4;
-    const int offB_s = a.RB * a.rs_d;
-
-    if (warp == NWC) {
-        // ---------------- producer: bulk copies of whole rows (and their scales) into the stage ring
-        if (lane == 0) {
-            int s = 0, it = 0;
-            uint32_t ph = 0;
-            StreamStage st;
-            while (cur.next(a, st)) {
-                if (it >= NS && !mbar_wait(&empty[s], ph ^ 1, deadline, &abort_flag)) {
-                    if (!abort_flag) {
-                        abort_flag = 1;
-                        atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
-                    }
-                    break;
-                }
-                uint8_t *dst = ring + s * SB;
-                const ExpertDesc &E = m.table[s_exp[st.ai]];
-                if (st.kind == 0) {
-                    const uint32_t cb = (uint32_t)(st.n * a.rs_gu), sbytes = (uint32_t)(st.n * a.ng_gu * 4);
-                    mbar_expect_tx(&full[s], 2 * cb + 2 * sbytes);
-                    bulk_load(dst, E.m[0].q + (size_t)st.row0 * a.rs_gu, cb, &full[s]);
-                    bulk_load(dst + offA_u, E.m[1].q + (size_t)st.row0 * a.rs_gu, cb, &full[s]);
-                    bulk_load(dst + offA_sg, E.m[0].s + (size_t)st.row0 * a.ng_gu, sbytes, &full[s]);
-                    bulk_load(dst + offA_su, E.m[1].s + (size_t)st.row0 * a.ng_gu, sbytes, &full[s]);
-                } else {
-                    const uint32_t cb = (uint32_t)(st.n * a.rs_d), sbytes = (uint32_t)(st.n * a.ng_d * 4);
-                    mbar_expect_tx(&full[s], cb + sbytes);
-                    bulk_load(dst, E.m[2].q + (size_t)st.row0 * a.rs_d, cb, &full[s]);
-                    bulk_load(dst + offB_s, E.m[2].s + (size_t)st.row0 * a.ng_d, sbytes, &full[s]);
-                }
-                it++;
-                if (++s == NS) {
-                    s = 0;
-                    ph ^= 1;
-                }
-            }
-            // every copy issued has landed before the CTA may exit
-            const uint64_t dl2 = global_ns() + 200000000ull;
-            volatile int no_abort = 0;
-            for (int k = max(0, it - NS); k < it; k++) mbar_wait(&full[k % NS], (k / NS) & 1, dl2, &no_abort);
-        }
-        return;
-    }
-
-    // ---------------- consumers (warps 0..NWC-1); they sync among themselves only
-    const int nsB = (m.cpr_d + 31) >> 5;
-    const int GA = NWC / nsA, GB = NWC / nsB;
-    const int subA = warp / nsA, slB = warp % nsB, subB = warp / nsB;
-    XRegS4 xr;
-    xr.set(xraw);
-    int s = 0;
-    uint32_t ph = 0;
-    StreamStage st;
-    bool have = cur.next(a, st);
-    // phase A
-    while (have && st.kind == 0) {
-        if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
-            const uint8_t *src = ring + s * SB;
-            const int c = slA * 32 + lane;
-            const bool okc = c < m.cpr_gu;
-            const int prb = (int)((long long)st.ai * m.F + st.row0 - pr0);   // local pair index of row0
-            // this warp's pairs of the stage: subA and subA + GA (RP <= 2 GA)
-            const int p0 = subA, p1 = subA + GA;
-            const bool ok0 = okc && p0 < st.n, ok1 = okc && p1 < st.n;
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            const uint4 qg0 = ok0 ? *reinterpret_cast<const uint4 *>(src + p0 * a.rs_gu + c * 16) : z;
-            const uint4 qu0 = ok0 ? *reinterpret_cast<const uint4 *>(src + offA_u + p0 * a.rs_gu + c * 16) : z;
-            const uint4 qg1 = ok1 ? *reinterpret_cast<const uint4 *>(src + p1 * a.rs_gu + c * 16) : z;
-            const uint4 qu1 = ok1 ? *reinterpret_cast<const uint4 *>(src + offA_u + p1 * a.rs_gu + c * 16) : z;
-            const int gi0 = (p0 * a.ng_gu + (c >> a.gshift_gu)) * 4, gi1 = (p1 * a.ng_gu + (c >> a.gshift_gu)) * 4;
-            const float sg0 = ok0 ? *reinterpret_cast<const float *>(src + offA_sg + gi0) : 0.f;
-            const float su0 = ok0 ? *reinterpret_cast<const float *>(src + offA_su + gi0) : 0.f;
-            const float sg1 = ok1 ? *reinterpret_cast<const float *>(src + offA_sg + gi1) : 0.f;
-            const float su1 = ok1 ? *reinterpret_cast<const float *>(src + offA_su + gi1) : 0.f;
-            const uint4 qq[4] = {qg0, qu0, qg1, qu1};
-            float dd[4];
-            xr.dot4(qq, dd);
-            const float t = warp_sum4(dd[0] * sg0, dd[1] * su0, dd[2] * sg1, dd[3] * su1, lane);
-            if ((lane & 7) == 0) {
-                const int k = lane >> 3;
-                const int pp = k < 2 ? p0 : p1;
-                if (pp < st.n) red[((prb + pp) * nsA + slA) * 2 + (k & 1)] = t;
-            }
-        } else if (!abort_flag && lane == 0) {
-            abort_flag = 1;
-            atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == NS) {
-            s = 0;
-            ph ^= 1;
-        }
-        have = cur.next(a, st);
-    }
-    named_sync(1, NCT);
-    // h[a][j] goes to hbuf in the order phase B stages it: expert a's block of
-    // xw_d floats, element j at stage_pos<4>(j) (chunks past F are never read)
-    const size_t xw_d = staged_words(4, m.cpr_d);
-    for (long long prl = tid; prl < pr1 - pr0; prl += NCT) {
-        float g = 0.f, u = 0.f;
-        for (int k = 0; k < nsA; k++) {
-            g += red[(prl * nsA + k) * 2];
-            u += red[(prl * nsA + k) * 2 + 1];
-        }
-        const long long pr = pr0 + prl;
-        const int ai = (int)(pr / m.F), j = (int)(pr - (long long)ai * m.F);
-        m.hbuf[(size_t)ai * xw_d + stage_pos<4>(j)] = g / (1.0f + expf(-g)) * u;
-    }
-    // grid barrier among the consumer warps of all CTAs
-    named_sync(1, NCT);
-    // Arrivals count up a 64-bit counter that is never reset between calls:
-    // every launch of this kernel on the workspace has gridDim.x CTAs, so this
-    // call's CTAs wait until the count reaches the next multiple of gridDim.x.
-    if (tid == 0 && !abort_flag) {
-        unsigned long long *ctr = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(m.bar) + 128);
-        __threadfence();
-        const unsigned long long old = atomicAdd(ctr, 1ull);
-        const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
-        for (;;) {
-            unsigned long long v;
-            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
-            if (v >= target) break;
-            if (global_ns() > deadline) {
-                atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
-                abort_flag = 1;
-                break;
-            }
-            __nanosleep(20);
-        }
-        __threadfence();
-    }
-    named_sync(1, NCT);
-    // h of the routed experts: already in staged order; chunks past F are zero
-    {
-        const float4 *src4 = reinterpret_cast<const float4 *>(m.hbuf);
-        float4 *dst4 = reinterpret_cast<float4 *>(xh);
-        const int n4 = nact * (int)xw_d / 4, c4 = (int)xw_d / 4;
-        constexpr int UN = 8;
-        for (int i0 = tid; i0 < n4; i0 += NCT * UN) {
-            float4 t[UN];
-#pragma unroll
-            for (int u = 0; u < UN; u++) {
-                const int i = i0 + u * NCT;
-                const bool live = i < n4 && ((i % c4) >> 3) * 32 < m.F;   // chunk (8 float4) inside F
-                t[u] = live ? __ldcg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < UN; u++)
-                if (i0 + u * NCT < n4) dst4[i0 + u * NCT] = t[u];
-        }
-    }
-    named_sync(1, NCT);
-    // phase B
-    int cur_ai = -1;
-    while (have) {
-        if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
-            if (st.ai != cur_ai) {
-                cur_ai = st.ai;
-                xr.load_staged(xh + (size_t)cur_ai * xw_d, slB * 32 + lane);
-            }
-            const uint8_t *src = ring + s * SB;
-            const int c = slB * 32 + lane;
-            const bool okc = c < m.cpr_d;
-            // this warp's rows of the stage: subB + k GB, k < 4 (RB <= 4 GB)
-            uint4 qq[4];
-            float sc[4], dd[4];
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int r = subB + k * GB;
-                const bool ok = okc && r < st.n;
-                qq[k] = ok ? *reinterpret_cast<const uint4 *>(src + r * a.rs_d + c * 16) : make_uint4(0, 0, 0, 0);
-                sc[k] = ok ? *reinterpret_cast<const float *>(src + offB_s + (r * a.ng_d + (c >> a.gshift_d)) * 4) : 0.f;
-            }
-            xr.dot4(qq, dd);
-            const float t = warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
-            if ((lane & 7) == 0) {
-                const int r = subB + (lane >> 3) * GB;
-                if (r < st.n) red[((size_t)cur_ai * rpc + (st.row0 - oc0 + r)) * nsB + slB] = t;
-            }
-        } else if (!abort_flag && lane == 0) {
-            abort_flag = 1;
-            atomicCAS(m.err, 0, DEV_ERR_TIMEOUT);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == NS) {
-            s = 0;
-            ph ^= 1;
-        }
-        have = cur.next(a, st);
-    }
-    named_sync(1, NCT);
-    for (int rr = tid; rr < oc1 - oc0; rr += NCT) {
-        float acc = 0.f;
-        for (int ai = 0; ai < nact; ai++) {
-            float d = 0.f;
-            for (int k = 0; k < nsB; k++) d += red[((size_t)ai * rpc + rr) * nsB + k];
-            acc = fmaf(s_ew[ai], d, acc);
-        }
-        m.y[oc0 + rr] = acc;
-    }
-}
-
 
 // ------------------------------------------------------------------ matvec, S = 1, streamed
 // The same streaming scheme as the decode block's phase A for coli_matmul at
@@ -1574,36 +1179,6 @@ int log2_exact(int v) {
 }
 
 }  // namespace
-
-size_t stream_decode_smem() {
-    return (size_t)kStreamStages * kStreamStageBytes + kStreamXhBytes + kStreamRedBytes + 2 * kStreamStages * 8 + 128;
-}
-
-cudaError_t stream_decode_occupancy(int *per_sm) {
-    auto kern = moe_decode_stream_kernel<4>;
-    const size_t smem = stream_decode_smem();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, (kStreamConsumerWarps + 1) * 32, smem);
-}
-
-cudaError_t launch_stream_decode(const StreamArgs &a, int grid, cudaStream_t st) {
-    auto kern = moe_decode_stream_kernel<4>;
-    const size_t smem = stream_decode_smem();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3((kStreamConsumerWarps + 1) * 32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
-}
 
 size_t stream_gemv_smem() { return (size_t)kStreamStages * kStreamStageBytes + kStreamRedBytes + 2 * kStreamStages * 8 + 128; }
 

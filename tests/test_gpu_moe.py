@@ -57,15 +57,19 @@ def test_decode_block(fmt, gs, S, K):
     assert norm_err(got, ref) <= TOL
 
 
+@pytest.mark.parametrize("fmt", [4, 2, 1])
 @pytest.mark.parametrize("H,F,gs,K", [(3072, 1536, 64, 8), (6144, 2048, 128, 8), (1024, 512, 64, 3),
-                                      (2048, 1024, 32, 16), (1152, 640, 32, 8)])
-def test_decode_streamed_shapes(H, F, gs, K):
-    """S = 1 int4 shapes taken by the bulk-copy decode kernel: several slabs per
-    row, pair ranges that straddle experts and CTAs, partial stages."""
+                                      (2048, 1024, 32, 16), (1152, 640, 32, 8), (1000, 744, 64, 5),
+                                      (6144, 2048, 64, 9)])
+def test_decode_streamed_shapes(fmt, H, F, gs, K):
+    """S = 1 int4 / int8 shapes taken by the bulk-copy decode kernel: several
+    slabs per row, pair ranges that straddle experts and CTAs, partial stages,
+    rows whose last 16-byte chunk is partly padding (H, F not multiples of 32),
+    the shared expert's ninth slot."""
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
-    g = wl.rng(4100 + H + F + gs + K)
-    host = _experts(g, H, F, 24, 4, gs, distinct=6)
+    g = wl.rng(4100 + H + F + gs + K + 11 * fmt)
+    host = _experts(g, H, F, 24, fmt, gs if fmt == 4 else 0, distinct=6)
     x = wl.activations(g, 1, H)
     ids, w = wl.routing_topk_softmax(g, 1, 24, K)
     table = _device_table(coli, host)
