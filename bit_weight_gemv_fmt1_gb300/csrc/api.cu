@@ -800,6 +800,42 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         for (int e = 0; e < n_experts && gs_ok; e++)
             gs_ok = experts[e].gate->gs % 32 == 0 && experts[e].up->gs % 32 == 0 && experts[e].down->gs % 32 == 0;
 
+    // ---------------- decode, S = 1, int4 tables (gs a power-of-two multiple of 64): weights streamed by
+    // bulk copies, dot products on the tensor cores, one cooperative launch
+    if (S == 1 && (fmt == 2 || fmt == 4) && n_slots <= kMaxDecodeSlots && !host_any) {
+        const coli_tensor *d0 = experts[0].down;
+        const int gs_gu = g0->gs, gs_d = d0->gs;
+        bool ok = true;
+        for (int e = 0; e < n_experts && ok && fmt == 4; e++)
+            ok = experts[e].gate->gs == gs_gu && experts[e].up->gs == gs_gu && experts[e].down->gs == gs_d;
+        MdArgs a;
+        size_t smem = 0;
+        int per_sm = 0;
+        if (ok && md_plan(fmt, (int)H, (int)F, K, (int)g0->rs, (int)d0->rs, g0->ng, d0->ng, gs_gu, gs_d, ds->n_sm,
+                          (size_t)ds->smem_optin, &a, &smem) &&
+            md_occupancy(a, smem, &per_sm) == cudaSuccess && per_sm >= 1) {
+            Workspace *ws = nullptr;
+            if (int rc = workspace(ds, st, md_scratch_bytes(a), &ws)) return rc;
+            unsigned *ctr = nullptr;
+            if (int rc = decode_counters(ds, st, md_counter_words(), &ctr)) return rc;
+            a.x = x;
+            a.ids = ids;
+            a.w = w;
+            a.y = y;
+            a.table = table;
+            a.n_experts = n_experts;
+            a.hbuf = (float *)ws->buf;
+            a.part = a.hbuf + (size_t)K * F;
+            a.ctr = ctr;
+            a.err = ds->err;
+            a.timeout_ns = 2000000000LL;
+            cudaError_t e = launch_decode_mma(a, ds->n_sm, smem, st);
+            if (e != cudaSuccess) return cuda_fail(e, "decode expert-block launch");
+            count(1, 0);
+            return COLI_OK;
+        }
+    }
+
     // ---------------- decode, S = 1, int4 / int8 tables: weights streamed by bulk copies, dp4a decode,
     // one cooperative launch
     if (S == 1 && (fmt == 1 || fmt == 2 || fmt == 4) && n_slots <= kMaxDecodeSlots && !host_any) {

@@ -655,6 +655,40 @@ size_t sd_scratch_bytes(const SdArgs &a);
 size_t sd_counter_words(const SdArgs &a);
 cudaError_t launch_stream_decode(const SdArgs &a, int grid, size_t smem, cudaStream_t st);
 
+// Decode expert block, S = 1, int4 tables on the tensor cores (decode_mma.cu):
+// weights streamed into shared memory by bulk copies, decoded to f16
+// subnormals, mma.sync against hi/lo f16 activations.  md_plan fills the
+// geometry.
+struct MdArgs {
+    const float *x;
+    const int32_t *ids;
+    const float *w;
+    float *y;
+    const ExpertDesc *table;
+    int n_experts, K, H, F;
+    int fmt;
+    int rs_gu, rs_d;           // device row strides (bytes)
+    int ng_gu, ng_d;           // scales per row (fmt 4)
+    int gsh_gu, gsh_d;         // segment -> scale group shift: log2(gs / 64)
+    int nsegA, nsegB;          // 64-input segments per gate/up row and per down row
+    int spwA, spwB;            // segments per consumer warp
+    int bsA, ssA, soA;         // phase-A stage: code-block stride, scale-block stride, scale offset (bytes)
+    int bsB, ssB, soB;         // phase-B stage
+    int slot_bytes;
+    int off_red, off_bar;      // dynamic shared-memory layout (bytes)
+    float *hbuf;               // [K][F] scratch: h
+    float *part;               // [K][H] scratch: each routed expert's down output
+    unsigned *ctr;             // zeroed counters (md_counter_words)
+    int *err;                  // device error word
+    long long timeout_ns;      // bound of every wait
+};
+bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int ng_d, int gs_gu, int gs_d, int n_sm,
+             size_t smem_max, MdArgs *a, size_t *smem);
+cudaError_t md_occupancy(const MdArgs &a, size_t smem, int *per_sm);
+size_t md_scratch_bytes(const MdArgs &a);
+size_t md_counter_words();
+cudaError_t launch_decode_mma(const MdArgs &a, int grid, size_t smem, cudaStream_t st);
+
 // Streamed S = 1 matvec (slab.cu): the same bulk-copy ring over the rows of all
 // matrices of the call.
 constexpr size_t kBarrierBytes = 256;           // per-workspace grid-barrier words (see workspace())

@@ -1,0 +1,922 @@
+// decode_mma.cu -- the decode expert block at S = 1 (one token, top-K routed
+// experts) for int4 expert tables (fmt 2, and fmt 4 with groups of a
+// power-of-two multiple of 64 inputs), in one cooperative launch with one CTA
+// per SM (colibri-strix commit log, "metal: batched moe_block": gate/up GEMV,
+// SiLU * mul, down GEMV and the weighted sum over the routed experts as a
+// single GPU pass).
+//
+// Arithmetic.  The dot products run on the tensor cores as register-operand
+// mma.sync m16n8k16 (f16 inputs, f32 accumulate); this is a matrix-vector
+// product, so the operands come straight from registers and only two of the
+// eight B columns carry data.
+//   A (weights): a 4-bit code n placed in the low mantissa bits of an f16
+//     with a zero exponent field is the subnormal n * 2^-24, exact.  One AND
+//     of a 32-bit word of eight codes with 0x000F000F gives the f16 pair
+//     (n0, n4), with 0x00F000F0 the pair (16 n1, 16 n5); the word shifted
+//     right by 8 gives (n2, n6) and (16 n3, 16 n7) the same way.  So one
+//     word is four A registers for five integer operations.
+//   B (activations): the warp scales its inputs by a power of two 2^k (the
+//     largest magnitude lands in [2^14, 2^15)) and splits each into
+//     hi = f16(v) and lo = f16((v - hi) * 2^11): column 0 holds hi, column 1
+//     lo, so the pair carries 22 significant bits.  Inputs facing a 16 n code
+//     are stored divided by 16.
+//   The offset binary code value is n - 8: each chain of mma starts from
+//   C = -8 * 2^-24 * (sum of the B values of its inputs), so the result is
+//   2^-24 * sum (n - 8) v.  Per group (fmt 4) the chain result is multiplied
+//   by the group's scale; per row (fmt 2) the row's scale is applied to the
+//   finished dot product.
+//
+// Roles.  Warps 0..15 consume, warp 16 produces: its lane 0 streams stages
+// into kMdSlots shared-memory slots with bulk copies (cp.async.bulk) and a
+// descriptor per slot.  Warp 17 finishes every stage (below); warp 18 publishes
+// the h it writes to the other CTAs.  A stage holds whole rows in four blocks of rows; the
+// blocks start 32 bytes apart modulo 128, and the 16 rows of an mma tile take
+// row r of all four blocks for r = 0..3, so the 8-byte code loads of a
+// half-warp fall in four different bank quarters.  Warp w owns the 64-input
+// segments [w S, (w + 1) S) of every row and keeps their B fragments in
+// registers.
+//   phase 0: the token's routed experts, distinct and in ascending id order,
+//            duplicate slots' weights summed (decode_route.cuh).
+//   phase A: stages of 8 (gate, up) row pairs of one routed expert, dealt
+//            round robin over the CTAs.  Every consumer warp writes its
+//            segments' share of the 16 rows to the slot's partial-sum table
+//            and moves on; warp 17 sums the table in warp order, writes
+//            h[a][j] = silu(gate) * up to global scratch and frees the slot.
+//   grid barrier (the producer meanwhile copies the first phase-B stages).
+//   phase B: the CTA owns output rows [oc0, oc1); one stage per routed expert
+//            holds those rows of its down matrix.  Each warp builds the B
+//            fragments of its segments of that expert's h and accumulates
+//            w_a * (its share of down_a . h_a) per row in registers across
+//            the experts; at the end the 16 warps' shares are summed in warp
+//            order: y[o] is written once.
+// Results do not depend on timing or on the number of SMs.  Every wait is
+// bounded (mbarrier.cuh); on expiry the kernel records DEV_ERR_TIMEOUT and
+// returns.  The last CTA to leave resets the call's barrier counter.
+#include <algorithm>
+#include <cstring>
+
+#include "coli_internal.cuh"
+#include "decode_route.cuh"
+#include "mbarrier.cuh"
+
+namespace coli {
+
+namespace {
+
+constexpr int kMdWarps = 16;     // consumer warps; then the producer, epilogue and signal warps
+constexpr int kMdThreads = (kMdWarps + 3) * 32;
+constexpr int kMdQueue = 16;     // entries of the epilogue -> signal queue
+constexpr int kMdSlots = 3;      // shared-memory slots of the stage ring
+constexpr int kMdSegMax = 6;     // 64-input segments per warp and row (H, F <= 6144)
+constexpr int kMdTiles = 3;                   // 16-row mma tiles of a phase-B stage
+constexpr int kMdBlockRows = 4 * kMdTiles;     // rows of each of a phase-B stage's four blocks
+constexpr int kMdStageRows = 4 * kMdBlockRows; // down rows of a phase-B stage (48)
+constexpr int kMdMaxBlocks = 128;              // 64-row blocks of y (H <= 8192)
+constexpr int kMdCtrReady = 4;                 // counter words: [1] CTAs out, [4..68) ready, [68..) blocks
+constexpr int kMdCtrBlocks = kMdCtrReady + kMaxDecodeSlots;
+
+enum : int { MD_A = 0, MD_B = 1, MD_END = 2 };
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float md_ldsf(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// d += A B on the tensor cores, m16n8k16, f16 operands, f32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d = A B + c (the start of a chain: c and d are different registers).
+__device__ __forceinline__ void mma16816c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1, float4 c) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+// One 64-input segment of a 16-row tile: cg / ch are the thread's two code
+// words of its rows g and g + 8 (inputs 16 t + 0..7 and 16 t + 8..15 of the
+// segment), bf the segment's eight B registers.  d = c + the segment's four
+// products (md_segment_c) or d += them (md_segment).
+__device__ __forceinline__ void md_segment_c(float (&d)[4], uint2 cg, uint2 ch, const uint32_t (&bf)[8], float4 c) {
+    // two chains of two (operands P and Q), so that two mma are in flight
+    const uint32_t L = 0x000F000Fu, Hm = 0x00F000F0u;
+    float e[4];
+    mma16816c(d, cg.x & L, ch.x & L, cg.x & Hm, ch.x & Hm, bf[0], bf[1], c);
+    const uint32_t ug = cg.x >> 8, uh = ch.x >> 8;
+    mma16816c(e, ug & L, uh & L, ug & Hm, uh & Hm, bf[2], bf[3], make_float4(0.f, 0.f, 0.f, 0.f));
+    mma16816(d, cg.y & L, ch.y & L, cg.y & Hm, ch.y & Hm, bf[4], bf[5]);
+    const uint32_t vg = cg.y >> 8, vh = ch.y >> 8;
+    mma16816(e, vg & L, vh & L, vg & Hm, vh & Hm, bf[6], bf[7]);
+    d[0] += e[0];
+    d[1] += e[1];
+    d[2] += e[2];
+    d[3] += e[3];
+}
+__device__ __forceinline__ void md_segment(float (&d)[4], uint2 cg, uint2 ch, const uint32_t (&bf)[8]) {
+    const uint32_t L = 0x000F000Fu, Hm = 0x00F000F0u;
+    mma16816(d, cg.x & L, ch.x & L, cg.x & Hm, ch.x & Hm, bf[0], bf[1]);
+    const uint32_t ug = cg.x >> 8, uh = ch.x >> 8;
+    mma16816(d, ug & L, uh & L, ug & Hm, uh & Hm, bf[2], bf[3]);
+    mma16816(d, cg.y & L, ch.y & L, cg.y & Hm, ch.y & Hm, bf[4], bf[5]);
+    const uint32_t vg = cg.y >> 8, vh = ch.y >> 8;
+    mma16816(d, vg & L, vh & L, vg & Hm, vh & Hm, bf[6], bf[7]);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// The value lane `lane` loads for round r: inputs 64 q0 + 128 r + 4 lane + 0..3
+// of v (length n); zero past n or past the warp's nq segments.
+__device__ __forceinline__ float4 md_load4(const float *v, int n, int q0, int nq, int r, int lane, bool cg) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int seg = 2 * r + (lane >> 4);
+    if (seg >= nq) return f;
+    const long long i0 = (long long)(q0 + seg) * 64 + 4 * ((lane & 15));
+    if (i0 + 4 <= n && ((reinterpret_cast<uintptr_t>(v + i0) & 15) == 0)) {
+        f = cg ? __ldcg(reinterpret_cast<const float4 *>(v + i0)) : __ldg(reinterpret_cast<const float4 *>(v + i0));
+    } else {
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if (i0 + j < n) t[j] = cg ? __ldcg(v + i0 + j) : __ldg(v + i0 + j);
+        f = make_float4(t[0], t[1], t[2], t[3]);
+    }
+    return f;
+}
+
+// The warp's scale for its values (all rounds): 2^k with the largest
+// magnitude times 2^k in [2^14, 2^15), k clamped so that 2^k and 2^-k are
+// normal floats; unscale = 2^-k, or NaN when an input is not finite.
+struct MdScale {
+    float s2k, unscale;
+};
+template <int NR>
+__device__ __forceinline__ MdScale md_scale(const float4 (&ld)[NR]) {
+    uint32_t mb = 0;
+#pragma unroll
+    for (int r = 0; r < NR; r++) {
+        mb = max(mb, __float_as_uint(ld[r].x) & 0x7fffffffu);
+        mb = max(mb, __float_as_uint(ld[r].y) & 0x7fffffffu);
+        mb = max(mb, __float_as_uint(ld[r].z) & 0x7fffffffu);
+        mb = max(mb, __float_as_uint(ld[r].w) & 0x7fffffffu);
+    }
+    mb = __reduce_max_sync(0xffffffffu, mb);
+    const int k = min(141 - (int)(mb >> 23), 126);
+    MdScale sc;
+    sc.s2k = __uint_as_float((uint32_t)(k + 127) << 23);
+    sc.unscale = mb >= 0x7f800000u ? __uint_as_float(0x7fc00000u) : __uint_as_float((uint32_t)(127 - k) << 23);
+    return sc;
+}
+
+// B fragments and chain starts of one round (two segments) of the warp's
+// inputs, from the four values each lane loaded for it (md_load4: lane L holds
+// inputs 4 L + 0..3 of the round).  nq = the warp's segments left from this
+// round on.
+//   Each lane converts its values to the hi / lo f16 halves and stores them
+//   into the warp's staging area `stg` (512 bytes) as the rows of the
+//   transposed B operands: for every B operand (segment, k-step, P or Q) and
+//   every half of its 16 k-slots, row 0 holds the hi column and row 1 the lo
+//   column, 8 slots of 2 bytes each.  ldmatrix then hands every lane its
+//   fragment; the lanes of the six all-zero columns read `zrow`.
+//   Input 16 t + 8 i + j of a segment feeds k-step i, operand P (j & 2 == 0)
+//   or Q, k-slot 2 t + j / 4 + 8 (j & 1): the slots of 16 n codes, j odd,
+//   hold the input divided by 16.
+//   b0 / b1: the eight B registers of the round's segments (k-step i:
+//   P b0b1, P b2b3, Q b0b1, Q b2b3 at 4 i + 0..3), zero for segments >= nq.
+//   c0 / c1: -8 * 2^-24 * sum of the segment's B values, as the accumulator
+//   quad (hi, lo, hi, lo) of the tile rows: four mma of the fragments with the
+//   constant A = -8 * 2^-24 (-128 * 2^-24 on the 16 n slots), exact f16
+//   subnormals.
+__device__ __forceinline__ void md_frags(float4 ld, MdScale sc, int nq, int lane, uint32_t stg, uint32_t zrow,
+                                         uint32_t (&b0)[8], uint32_t (&b1)[8], float4 &c0, float4 &c1) {
+    // store: lane L = 16 seg + 4 t + 2 i + h holds j = 4 h + 0..3
+    {
+        const int seg = lane >> 4, t = (lane >> 2) & 3, i = (lane >> 1) & 1, h = lane & 1;
+        const uint32_t wb = stg + (uint32_t)(((seg * 2 + i) * 2) * 64 + (2 * t + h) * 2);
+        const float v[4] = {ld.x, ld.y, ld.z, ld.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            // q = j % 4: operand P (q < 2) or Q, slot half q % 2 (the 16 n slots for odd q)
+            const float sv = v[q] * sc.s2k * ((q & 1) ? 0.0625f : 1.f);
+            const __half hi = __float2half_rn(sv);
+            const __half lo = __float2half_rn((sv - __half2float(hi)) * 2048.f);
+            const uint32_t ad = wb + (uint32_t)((((q >> 1) * 2 + (q & 1)) * 2) * 16);
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(ad), "h"(__half_as_ushort(hi)));
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(ad + 16), "h"(__half_as_ushort(lo)));
+        }
+    }
+    __syncwarp();
+    // load: matrix q of ldmatrix.x4 = (operand q / 2, slot half q % 2); lane L
+    // gives row L % 8 of matrix L / 8: column 0 (hi) or 1 (lo), else zeros
+    const int mq = lane >> 3, mr = lane & 7;
+#pragma unroll
+    for (int sg = 0; sg < 2; sg++) {
+        uint32_t(&bf)[8] = sg ? b1 : b0;
+        const bool on = sg < nq;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const uint32_t ra = mr < 2 ? stg + (uint32_t)(((((sg * 2 + i) * 2 + (mq >> 1)) * 2 + (mq & 1)) * 2 + mr) * 16)
+                                       : zrow;
+            uint32_t r0, r1, r2, r3;
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                         : "r"(ra));
+            bf[4 * i + 0] = on ? r0 : 0u;
+            bf[4 * i + 1] = on ? r1 : 0u;
+            bf[4 * i + 2] = on ? r2 : 0u;
+            bf[4 * i + 3] = on ? r3 : 0u;
+        }
+    }
+    __syncwarp();   // the staging area may be rewritten after this
+    const uint32_t e8 = 0x80088008u, e128 = 0x80808080u;   // -8 and -128 times 2^-24, two f16 each
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        mma16816(d0, e8, e8, e128, e128, b0[2 * k], b0[2 * k + 1]);
+        mma16816(d1, e8, e8, e128, e128, b1[2 * k], b1[2 * k + 1]);
+    }
+    c0 = make_float4(d0[0], d0[1], d0[2], d0[3]);
+    c1 = make_float4(d1[0], d1[1], d1[2], d1[3]);
+}
+
+// A warp's share of one phase-A stage: its segments of the 16 tile rows.
+//   cq: shared address of the thread's code word of row g in segment 0; rs2:
+//   bytes from row g to row g + 8; cfs: the warp's chain starts, one float4
+//   (hi, lo, hi, lo) per segment and one more for the sum over segments;
+//   sq: scale of row g for segment 0, sr2: bytes to row g + 8's scale.
+// FULL: the warp owns all kMdSegMax segments (no per-segment tests).
+template <bool GROUPED, int GSH, bool FULL>
+__device__ __forceinline__ void md_tileA(float (&y)[4], uint32_t cq, uint32_t rs2, uint32_t cfs, uint32_t sq,
+                                         uint32_t sr2, int nq, const uint32_t (&bf)[kMdSegMax][8]) {
+    if (GROUPED) {
+        y[0] = y[1] = y[2] = y[3] = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMdSegMax; q++) {
+            if (FULL || q < nq) {
+                const uint2 cg = lds64(cq + 32 * q), ch = lds64(cq + rs2 + 32 * q);
+                float dd[4];
+                md_segment_c(dd, cg, ch, bf[q], lds128f(cfs + 16 * q));
+                const float sg = md_ldsf(sq + 4 * (q >> GSH)), sh = md_ldsf(sq + sr2 + 4 * (q >> GSH));
+                y[0] = fmaf(sg, dd[0], y[0]);
+                y[1] = fmaf(sg, dd[1], y[1]);
+                y[2] = fmaf(sh, dd[2], y[2]);
+                y[3] = fmaf(sh, dd[3], y[3]);
+            }
+        }
+    } else {
+        // two chains (even and odd segments) over the row
+        float z[4];
+        const uint2 cg0 = lds64(cq), ch0 = lds64(cq + rs2);
+        md_segment_c(y, cg0, ch0, bf[0], lds128f(cfs + 16 * kMdSegMax));
+        if (FULL || nq > 1) {
+            const uint2 cg1 = lds64(cq + 32), ch1 = lds64(cq + rs2 + 32);
+            md_segment_c(z, cg1, ch1, bf[1], make_float4(0.f, 0.f, 0.f, 0.f));
+        } else {
+            z[0] = z[1] = z[2] = z[3] = 0.f;
+        }
+#pragma unroll
+        for (int q = 2; q < kMdSegMax; q++) {
+            if (FULL || q < nq) {
+                const uint2 cg = lds64(cq + 32 * q), ch = lds64(cq + rs2 + 32 * q);
+                md_segment((q & 1) ? z : y, cg, ch, bf[q]);
+            }
+        }
+        y[0] += z[0];
+        y[1] += z[1];
+        y[2] += z[2];
+        y[3] += z[3];
+    }
+}
+
+// The epilogue's release of a slot: one arrival that counts for all the
+// consumer warps.
+__device__ __forceinline__ void md_release(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(kMdWarps)
+                 : "memory");
+}
+
+// A warp's bounded wait for a stage (every lane polls; false for the whole
+// warp once any lane hit the deadline or the CTA aborted).
+__device__ __forceinline__ bool md_wait(uint64_t *bar, uint32_t parity, uint64_t deadline, volatile int *abort) {
+    bool ok = true;
+    while (!mbar_try(bar, parity)) {
+        if (*abort || global_ns() > deadline) {
+            ok = false;
+            break;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// GSH: log2(gs / 64), segments per scale group (fmt 4); 0 for fmt 2.
+template <bool GROUPED, int GSH>
+__global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdArgs a) {
+    extern __shared__ uint8_t sraw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)sraw + 127) & ~(uintptr_t)127);
+    float *red = reinterpret_cast<float *>(base + a.off_red);   // [slot][warp][48]: partial sums of a stage
+    int4 *desc = reinterpret_cast<int4 *>(base + a.off_bar);    // [slot]
+    uint64_t *full = reinterpret_cast<uint64_t *>(desc + kMdSlots);
+    uint64_t *empty = full + kMdSlots;
+    uint64_t *redfull = empty + kMdSlots;   // every consumer warp wrote its partial sums of the stage
+    __shared__ DecodeRouting rt;
+    __shared__ volatile int abort_flag;
+    __shared__ float4 s_cf[kMdWarps][kMdSegMax + 1];   // phase-A chain starts of each warp's segments, their sum
+    __shared__ __align__(16) uint8_t s_stg[kMdWarps][512];   // B-fragment staging, one area per consumer warp
+    __shared__ __align__(16) uint32_t s_zrow[4];             // the all-zero B columns
+    __shared__ int s_done[kMdMaxBlocks];                     // output blocks this CTA completes
+    __shared__ int s_ndone;
+    __shared__ int2 s_q[kMdQueue];                           // (expert, pairs) of h written, for the signal warp
+    __shared__ unsigned s_qn, s_qdone;                       // entries written / published
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int SB = a.slot_bytes;
+    const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
+    unsigned *exitc = a.ctr + 1;
+    unsigned *ready = a.ctr + kMdCtrReady;   // [routed expert]: pairs of h written
+    unsigned *blkc = a.ctr + kMdCtrBlocks;   // [64-row block of y]: expert rows summed into part
+
+    // consumers load their x values now; the fragments are built after routing
+    const int q0A = warp * a.spwA, nqA = min(a.spwA, a.nsegA - q0A);
+    constexpr int NR = (kMdSegMax + 1) / 2;
+    float4 ldA[NR];
+    if (warp < kMdWarps) {
+#pragma unroll
+        for (int r = 0; r < NR; r++) ldA[r] = md_load4(a.x, a.H, q0A, nqA, r, lane, false);
+    }
+
+    if (tid < 4) s_zrow[tid] = 0u;
+    if (tid == 0) {
+        abort_flag = 0;
+        s_ndone = 0;
+        s_qn = 0u;
+        s_qdone = 0u;
+        for (int i = 0; i < kMdSlots; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kMdWarps);
+            mbar_init(&redfull[i], kMdWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    decode_route(rt, a.ids, a.w, a.K, a.n_experts, a.table, kMdWarps);
+    if (rt.bad) {
+        if (blockIdx.x == 0 && tid == 0) atomicCAS(a.err, 0, DEV_ERR_BAD_ID);
+        return;
+    }
+    const int nact = rt.nact;
+    if (nact == 0) {   // no routed expert: y = 0
+        const int rpc = (a.H + gridDim.x - 1) / gridDim.x;
+        for (int r = tid; r < rpc; r += kMdThreads)
+            if ((int)blockIdx.x * rpc + r < a.H) a.y[blockIdx.x * rpc + r] = 0.f;
+        return;
+    }
+    // phase B: this CTA's routed expert eB (the CTAs of an expert split its
+    // down rows evenly) and its rows [rb0, rb1)
+    const int G = gridDim.x;
+    const int eB = (int)(((long long)blockIdx.x * nact) / G);
+    const int cb0 = (int)(((long long)eB * G + nact - 1) / nact), cb1 = (int)(((long long)(eB + 1) * G + nact - 1) / nact);
+    const int rb0 = (int)((long long)a.H * (blockIdx.x - cb0) / (cb1 - cb0));
+    const int rb1 = (int)((long long)a.H * (blockIdx.x - cb0 + 1) / (cb1 - cb0));
+
+    if (warp == kMdWarps) {
+        // ---------------- producer: lane 0 issues every stage of the CTA.  Phase-A
+        // units are dealt round robin, the last routed expert's first, so that
+        // the final round (a partial one) belongs to expert 0
+        if (lane == 0) {
+            const int spe = (a.F + 7) / 8;   // phase-A stages per routed expert
+            const unsigned totalA = (unsigned)(nact * spe);
+            const int nB = (rb1 - rb0 + kMdStageRows - 1) / kMdStageRows;
+            const int rsA = a.rs_gu, rsB = a.rs_d;
+            unsigned idx = blockIdx.x;
+            int jB = 0, i = 0;
+            while (true) {
+                const int s = i % kMdSlots;
+                if (i >= kMdSlots && !mbar_wait(&empty[s], ((i / kMdSlots) & 1) ^ 1, deadline, &abort_flag)) {
+                    if (!abort_flag) {
+                        abort_flag = 1;
+                        atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                uint8_t *dst = base + (size_t)s * SB;
+                if (idx < totalA) {
+                    const int ai = nact - 1 - (int)(idx / spe), j0 = (int)(idx % spe) * 8;
+                    const int w = min(8, a.F - j0);
+                    desc[s] = make_int4(MD_A, ai, j0, w);
+                    uint32_t tx = 0;
+                    int cnt[4];
+#pragma unroll
+                    for (int b = 0; b < 4; b++) {
+                        cnt[b] = max(0, min(4, w - 4 * (b & 1)));
+                        tx += (uint32_t)cnt[b] * (uint32_t)(rsA + (GROUPED ? 4 * a.ng_gu : 0));
+                    }
+                    mbar_expect_tx(&full[s], tx);
+#pragma unroll
+                    for (int b = 0; b < 4; b++) {
+                        if (cnt[b] == 0) continue;
+                        const int pr0 = j0 + 4 * (b & 1), m = b >> 1;
+                        bulk_load(dst + b * (a.bsA + 32), rt.q[ai][m] + (size_t)pr0 * rsA, (uint32_t)(cnt[b] * rsA),
+                                  &full[s]);
+                        if (GROUPED)
+                            bulk_load(dst + a.soA + b * a.ssA, rt.s[ai][m] + (size_t)pr0 * a.ng_gu,
+                                      (uint32_t)(cnt[b] * a.ng_gu * 4), &full[s]);
+                    }
+                    idx += G;
+                } else if (jB < nB) {
+                    const int r0 = rb0 + jB * kMdStageRows, nr = min(kMdStageRows, rb1 - r0);
+                    desc[s] = make_int4(MD_B, eB, r0, nr);
+                    uint32_t tx = 0;
+                    int cnt[4];
+#pragma unroll
+                    for (int b = 0; b < 4; b++) {
+                        cnt[b] = max(0, min(kMdBlockRows, nr - b * kMdBlockRows));
+                        tx += (uint32_t)cnt[b] * (uint32_t)(rsB + (GROUPED ? 4 * a.ng_d : 0));
+                    }
+                    mbar_expect_tx(&full[s], tx);
+#pragma unroll
+                    for (int b = 0; b < 4; b++) {
+                        if (cnt[b] == 0) continue;
+                        const size_t rr = (size_t)r0 + (size_t)b * kMdBlockRows;
+                        bulk_load(dst + b * (a.bsB + 32), rt.q[eB][2] + rr * rsB, (uint32_t)(cnt[b] * rsB), &full[s]);
+                        if (GROUPED)
+                            bulk_load(dst + a.soB + b * a.ssB, rt.s[eB][2] + rr * a.ng_d,
+                                      (uint32_t)(cnt[b] * a.ng_d * 4), &full[s]);
+                    }
+                    jB++;
+                } else {
+                    desc[s] = make_int4(MD_END, 0, 0, 0);
+                    mbar_arrive(&full[s]);   // end marker: no bytes
+                    i++;
+                    break;
+                }
+                i++;
+            }
+            // every copy issued has landed before the CTA may exit
+            const uint64_t dl2 = global_ns() + 200000000ull;
+            volatile int no_abort = 0;
+            for (int q = max(0, i - kMdSlots); q < i; q++)
+                mbar_wait(&full[q % kMdSlots], (q / kMdSlots) & 1, dl2, &no_abort);
+        }
+        return;
+    }
+
+    if (warp == kMdWarps + 1) {
+        // ---------------- epilogue: sums the consumer warps' partials of each stage
+        // in warp order, then frees the slot.  Phase A: h = silu(gate) * up and the
+        // expert's ready count; phase B: the expert's rows of part
+        int i = 0;
+        bool ok = true;
+        // the h of a stage is handed to the signal warp, which publishes it (the
+        // gpu-scope fence that takes is then off this warp's path)
+        unsigned qn = 0;
+        bool qopen = true;
+        auto push = [&](int e, int w) {
+            __syncwarp();
+            if (lane == 0) {
+                while (qn - *(volatile unsigned *)&s_qdone >= (unsigned)kMdQueue) {
+                    if (abort_flag || global_ns() > deadline) break;
+                    __nanosleep(32);
+                }
+                s_q[qn % kMdQueue] = make_int2(e, w);
+                asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_addr(&s_qn)), "r"(qn + 1) : "memory");
+            }
+            qn++;
+        };
+        while (true) {
+            const int s = i % kMdSlots;
+            const uint32_t par = (uint32_t)((i / kMdSlots) & 1);
+            if (!md_wait(&full[s], par, deadline, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            const int4 d = desc[s];
+            if (d.x != MD_A && qopen) {
+                push(-1, 0);   // phase A is over for this CTA
+                qopen = false;
+            }
+            if (d.x == MD_END) break;
+            if (!md_wait(&redfull[s], par, deadline, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            const float *rd = red + s * kMdWarps * kMdStageRows;
+            if (d.x == MD_A) {
+                // row m = lane % 16 summed over warps 8 (lane / 16) .. + 7, then the two halves
+                const float *rp = rd + (lane >> 4) * 8 * kMdStageRows + (lane & 15);
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; w++) v += rp[w * kMdStageRows];
+                // the slot is free once its partial sums are read
+                __syncwarp();
+                if (lane == 0) md_release(&empty[s]);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                // tile row of gate pair p: block p / 4, row p % 4 -> 4 (p % 4) + p / 4; up: + 2
+                const int p = lane & 7;
+                const int mg = 4 * (p & 3) + (p >> 2);
+                float gv = __shfl_sync(0xffffffffu, v, mg), uv = __shfl_sync(0xffffffffu, v, mg + 2);
+                if (lane < d.w) {
+                    if (!GROUPED) {
+                        gv *= __ldg(rt.s[d.y][0] + d.z + lane);
+                        uv *= __ldg(rt.s[d.y][1] + d.z + lane);
+                    }
+                    a.hbuf[(size_t)d.y * a.F + d.z + lane] = gv / (1.0f + expf(-gv)) * uv;
+                }
+                push(d.y, d.w);
+            } else {
+                // stage row rr: block rr / 12, row rin = rr % 12 of it = tile rin / 4, tile row 4 (rin % 4) + block
+                float v[2] = {0.f, 0.f};
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int rr = lane + 32 * h;
+                    if (rr < d.w) {
+                        const int b = rr / kMdBlockRows, rin = rr - b * kMdBlockRows;
+                        const int col = (rin >> 2) * 16 + 4 * (rin & 3) + b;
+#pragma unroll
+                        for (int w = 0; w < kMdWarps; w++) v[h] += rd[w * kMdStageRows + col];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) md_release(&empty[s]);
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int rr = lane + 32 * h;
+                    if (rr < d.w) {
+                        if (!GROUPED) v[h] *= __ldg(rt.s[d.y][2] + d.z + rr);
+                        a.part[(size_t)d.y * a.H + d.z + rr] = v[h];
+                    }
+                }
+            }
+            i++;
+        }
+        if (qopen) push(-1, 0);
+        if (!ok && lane == 0 && !abort_flag) {
+            abort_flag = 1;
+            atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+        }
+        // the CTA's expert rows are in part: count them into their 64-row blocks of
+        // y; the CTA that completes a block sums it (below)
+        if (ok && rb1 > rb0) {
+            __threadfence();
+            __syncwarp();
+            for (int blk = rb0 / 64 + lane; blk * 64 < rb1; blk += 32) {
+                const int lo = max(rb0, blk * 64), hi = min(rb1, blk * 64 + 64);
+                const unsigned need = (unsigned)nact * (unsigned)(min(a.H, blk * 64 + 64) - blk * 64);
+                if (atomicAdd(&blkc[blk], (unsigned)(hi - lo)) + (unsigned)(hi - lo) == need)
+                    s_done[atomicAdd(&s_ndone, 1)] = blk;
+            }
+            __threadfence();
+        }
+        named_sync(2, (kMdWarps + 1) * 32);
+    } else if (warp == kMdWarps + 2) {
+        // ---------------- signal: publishes the h the epilogue wrote.  The acquire of
+        // the queue count orders the epilogue's h stores before this lane's
+        // gpu-scope fence, which orders them before the ready counts it raises
+        if (lane == 0) {
+            unsigned k = 0;
+            bool more = true;
+            while (more) {
+                unsigned n;
+                asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(n) : "r"(smem_addr(&s_qn)) : "memory");
+                if (n == k) {
+                    if (abort_flag || global_ns() > deadline) break;
+                    __nanosleep(64);
+                    continue;
+                }
+                __threadfence();
+                for (; k < n && more; k++) {
+                    const int2 q = s_q[k % kMdQueue];
+                    if (q.x < 0) more = false;
+                    else atomicAdd(&ready[q.x], (unsigned)q.y);
+                }
+                *(volatile unsigned *)&s_qdone = k;
+            }
+        }
+        return;
+    } else {
+        // ---------------- consumers
+        const uint32_t ring_s = smem_addr(base);
+        const int g = lane >> 2, t = lane & 3;
+        const int blk = g & 3, rib = g >> 2;   // block and row in block of tile row g (row g + 8: rib + 2)
+        const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(s_zrow);
+        int i = 0;                              // stage counter
+        bool live = true;
+        {
+            // phase A
+            uint32_t bf[kMdSegMax][8];
+            const MdScale scA = md_scale<NR>(ldA);
+            const float unA = scA.unscale * 0x1p24f;
+            float4 cft = make_float4(0.f, 0.f, 0.f, 0.f);   // per-row formats: the chain start of the whole row
+#pragma unroll
+            for (int r = 0; r < NR; r++) {
+                float4 c0, c1;
+                md_frags(ldA[r], scA, nqA - 2 * r, lane, stg, zrow, bf[2 * r], bf[2 * r + 1], c0, c1);
+                if (lane == 0) {
+                    s_cf[warp][2 * r] = c0;
+                    s_cf[warp][2 * r + 1] = c1;
+                }
+                cft.x += c0.x + c1.x;
+                cft.y += c0.y + c1.y;
+                cft.z += c0.z + c1.z;
+                cft.w += c0.w + c1.w;
+            }
+            // lane 0 holds the hi / lo quads of tile row 0; every row's start is the same
+            if (lane == 0) s_cf[warp][kMdSegMax] = cft;
+            __syncwarp();
+            const uint32_t rs2 = 2u * (uint32_t)a.rs_gu;
+            const uint32_t cofs = (uint32_t)(blk * (a.bsA + 32) + rib * a.rs_gu + 32 * q0A + 8 * t);
+            const uint32_t sofs = (uint32_t)(a.soA + blk * a.ssA + rib * a.ng_gu * 4 + (q0A >> GSH) * 4);
+            const uint32_t sr2 = 8u * (uint32_t)a.ng_gu;
+            const uint32_t cfs = smem_addr(&s_cf[warp][0]);
+            const bool fullA = nqA == kMdSegMax;
+            while (true) {
+                const int s = i % kMdSlots;
+                if (!md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag)) {
+                    if (lane == 0 && !abort_flag) {
+                        abort_flag = 1;
+                        atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+                    }
+                    live = false;
+                    break;
+                }
+                const int4 d = desc[s];
+                if (d.x != MD_A) break;   // stage i belongs to phase B (or is the end marker)
+                const uint32_t sb = ring_s + (uint32_t)(s * SB);
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                if (fullA)
+                    md_tileA<GROUPED, GSH, true>(y, sb + cofs, rs2, cfs, sb + sofs, sr2, nqA, bf);
+                else if (nqA > 0)
+                    md_tileA<GROUPED, GSH, false>(y, sb + cofs, rs2, cfs, sb + sofs, sr2, nqA, bf);
+                float *rw = red + (s * kMdWarps + warp) * kMdStageRows;
+                if (t == 0) {
+                    const bool on = nqA > 0;
+                    rw[g] = on ? fmaf(y[1], 0x1p-11f, y[0]) * unA : 0.f;
+                    rw[g + 8] = on ? fmaf(y[3], 0x1p-11f, y[2]) * unA : 0.f;
+                }
+                // the epilogue warp turns the stage into h and frees the slot
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&redfull[s]);
+                i++;
+            }
+        }
+        // phase B: wait until every pair of h of expert eB is written (one thread
+        // polls the expert's ready count), build the B fragments of the warp's
+        // segments of it once, then stream the CTA's rows of down[eB]
+        // (every consumer warp reaches this point, so the barrier below is CTA-uniform)
+        if (rb1 > rb0) {
+            if (tid == 0) {
+                while (true) {
+                    unsigned v;
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ready + eB) : "memory");
+                    if (v >= (unsigned)a.F) break;
+                    if (abort_flag || global_ns() > deadline) {
+                        if (!abort_flag) {
+                            abort_flag = 1;
+                            atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+                        }
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            named_sync(3, kMdWarps * 32);
+            live = live && !abort_flag;
+        }
+        if (live && rb1 > rb0) {
+            const int q0B = warp * a.spwB, nqB = min(a.spwB, a.nsegB - q0B);
+            const int rs = a.rs_d;
+            const uint32_t cofs = (uint32_t)(blk * (a.bsB + 32) + rib * rs + 32 * q0B + 8 * t);
+            const uint32_t sofs = (uint32_t)(a.soB + blk * a.ssB + rib * a.ng_d * 4 + (q0B >> GSH) * 4);
+            uint32_t bf[2][8];
+            float4 cq[2];
+            float unB = 0.f;
+            {
+                float4 ld[1] = {md_load4(a.hbuf + (size_t)eB * a.F, a.F, q0B, nqB, 0, lane, true)};
+                const MdScale scB = md_scale<1>(ld);
+                unB = scB.unscale * 0x1p24f;
+                md_frags(ld[0], scB, nqB, lane, stg, zrow, bf[0], bf[1], cq[0], cq[1]);
+            }
+            const bool fullB = nqB == 2;
+            while (true) {
+                const int s = i % kMdSlots;
+                if (!md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag)) {
+                    if (lane == 0 && !abort_flag) {
+                        abort_flag = 1;
+                        atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                const int4 d = desc[s];
+                if (d.x != MD_B) {   // end marker
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                    break;
+                }
+                const uint32_t sb = ring_s + (uint32_t)(s * SB);
+                float *rw = red + (s * kMdWarps + warp) * kMdStageRows;
+#pragma unroll
+                for (int T = 0; T < kMdTiles; T++) {
+                    float y[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (nqB > 0) {
+                        const uint32_t tofs = sb + cofs + (uint32_t)(4 * T * rs);
+                        const uint32_t tsc = sb + sofs + (uint32_t)(4 * T * a.ng_d * 4);
+#pragma unroll
+                        for (int sg = 0; sg < 2; sg++) {
+                            if (fullB || sg < nqB) {
+                                const uint2 cg = lds64(tofs + 32 * sg), ch = lds64(tofs + 2 * rs + 32 * sg);
+                                if (GROUPED) {
+                                    float dd[4];
+                                    md_segment_c(dd, cg, ch, bf[sg], cq[sg]);
+                                    const uint32_t sa = tsc + 4 * (sg >> GSH);
+                                    const float sgv = md_ldsf(sa), shv = md_ldsf(sa + 2 * a.ng_d * 4);
+                                    y[0] = fmaf(sgv, dd[0], y[0]);
+                                    y[1] = fmaf(sgv, dd[1], y[1]);
+                                    y[2] = fmaf(shv, dd[2], y[2]);
+                                    y[3] = fmaf(shv, dd[3], y[3]);
+                                } else {
+                                    y[0] += cq[sg].x;
+                                    y[1] += cq[sg].y;
+                                    y[2] += cq[sg].z;
+                                    y[3] += cq[sg].w;
+                                    md_segment(y, cg, ch, bf[sg]);
+                                }
+                            }
+                        }
+                    }
+                    if (t == 0) {
+                        const bool on = nqB > 0;
+                        rw[T * 16 + g] = on ? fmaf(y[1], 0x1p-11f, y[0]) * unB : 0.f;
+                        rw[T * 16 + g + 8] = on ? fmaf(y[3], 0x1p-11f, y[2]) * unB : 0.f;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&redfull[s]);
+                i++;
+            }
+        } else if (live) {
+            // no phase-B rows: pass the end marker
+            const int s = i % kMdSlots;
+            if (md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag)) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+        }
+        named_sync(2, (kMdWarps + 1) * 32);
+        // y of the blocks this CTA completed: sum over the routed experts in order
+        if (!abort_flag) {
+            for (int k = tid; k < s_ndone * 64; k += kMdWarps * 32) {
+                const int row = s_done[k >> 6] * 64 + (k & 63);
+                if (row < a.H) {
+                    float v = 0.f;
+                    for (int e = 0; e < nact; e++) v = fmaf(rt.ew[e], __ldcg(a.part + (size_t)e * a.H + row), v);
+                    a.y[row] = v;
+                }
+            }
+        }
+        // the last CTA out zeroes the call's counters for the next call
+        if (tid == 0) {
+            __threadfence();
+            if (atomicAdd(exitc, 1u) == gridDim.x - 1) {
+                for (int e = 0; e < a.K; e++) ready[e] = 0u;
+                for (int b = 0; b < (a.H + 63) / 64; b++) blkc[b] = 0u;
+                *exitc = 0u;
+                __threadfence();
+            }
+        }
+    }
+}
+
+size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+int log2_exact(int v) {
+    int k = 0;
+    while ((1 << k) < v) k++;
+    return (1 << k) == v ? k : -1;
+}
+
+}  // namespace
+
+// Geometry of the tensor-core decode block for an int4 expert table.  fmt=4
+// needs gs_gu and gs_d to be 64 times a power of two and a multiple of 4
+// scales per row (16-byte scale copies); H and F up to 16 * 6 * 64 = 6144.
+// Returns false when the table does not fit this kernel.
+bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int ng_d, int gs_gu, int gs_d, int n_sm,
+             size_t smem_max, MdArgs *a, size_t *smem) {
+    if (fmt != 2 && fmt != 4) return false;
+    const bool grouped = fmt == 4;
+    int gsh_gu = 0, gsh_d = 0;
+    if (grouped) {
+        if (gs_gu % 64 != 0 || gs_d % 64 != 0) return false;
+        gsh_gu = log2_exact(gs_gu / 64);
+        gsh_d = log2_exact(gs_d / 64);
+        // one shift for both roles, 64 or 128 inputs per group
+        if (gsh_gu < 0 || gsh_gu > 1 || gsh_d != gsh_gu || ng_gu % 4 != 0 || ng_d % 4 != 0) return false;
+    }
+    if (H < 1 || F < 1 || n_sm < 1 || K < 1 || K > kMaxDecodeSlots) return false;
+    const int nsegA = (H + 63) / 64, nsegB = (F + 63) / 64;
+    // segments per warp: a multiple of the segments per scale group, so that
+    // every warp starts at a group boundary
+    const int gm = 1 << gsh_gu;
+    const int spwA = ((nsegA + kMdWarps - 1) / kMdWarps + gm - 1) / gm * gm;
+    const int spwB = ((nsegB + kMdWarps - 1) / kMdWarps + gm - 1) / gm * gm;
+    if (spwA > kMdSegMax || spwB > kMdSegMax) return false;
+    // phase B: every routed expert has CTAs of its own (at most K experts)
+    if (n_sm < K || spwB > 2 || (H + 63) / 64 > kMdMaxBlocks) return false;
+    // slot layouts: four code blocks 32 bytes apart modulo 128 (each followed
+    // by room for the 32-byte read past a row's last segment), then four
+    // scale blocks 16 bytes apart modulo 128
+    const size_t bsA = round_up((size_t)4 * rs_gu + 32, 128), soA = 4 * bsA + 128;
+    const size_t ssA = grouped ? (size_t)16 * ng_gu + 16 : 0;
+    const size_t bsB = round_up((size_t)kMdBlockRows * rs_d + 32, 128), soB = 4 * bsB + 128;
+    const size_t ssB = grouped ? (size_t)kMdBlockRows * ng_d * 4 + 16 : 0;
+    const size_t SB = round_up(std::max(soA + 4 * ssA, soB + 4 * ssB), 128);
+    const size_t off_red = kMdSlots * SB;
+    const size_t red_bytes = (size_t)kMdSlots * kMdWarps * kMdStageRows * 4;
+    const size_t off_bar = off_red + red_bytes;
+    const size_t total = off_bar + kMdSlots * 16 + 3 * kMdSlots * 8 + 128;   // + alignment slack
+    // static shared memory of the kernel: about 15 KB
+    if (total + 16 * 1024 > smem_max || SB > (1u << 30)) return false;
+    memset(a, 0, sizeof *a);
+    a->K = K;
+    a->H = H;
+    a->F = F;
+    a->fmt = fmt;
+    a->rs_gu = rs_gu;
+    a->rs_d = rs_d;
+    a->ng_gu = grouped ? ng_gu : 0;
+    a->ng_d = grouped ? ng_d : 0;
+    a->gsh_gu = gsh_gu;
+    a->gsh_d = gsh_d;
+    a->nsegA = nsegA;
+    a->nsegB = nsegB;
+    a->spwA = spwA;
+    a->spwB = spwB;
+    a->bsA = (int)bsA;
+    a->ssA = (int)ssA;
+    a->soA = (int)soA;
+    a->bsB = (int)bsB;
+    a->ssB = (int)ssB;
+    a->soB = (int)soB;
+    a->slot_bytes = (int)SB;
+    a->off_red = (int)off_red;
+    a->off_bar = (int)off_bar;
+    *smem = total;
+    return true;
+}
+
+// Scratch of one call: h [K][F] and the experts' down outputs part [K][H], floats.
+size_t md_scratch_bytes(const MdArgs &a) { return (size_t)a.K * ((size_t)a.F + a.H) * 4; }
+// Counter words of one call (zero between calls).
+size_t md_counter_words() { return kMdCtrBlocks + kMdMaxBlocks; }
+
+// The kernel instance of a plan: fmt and group shift.
+template <class Fn>
+cudaError_t md_dispatch(const MdArgs &a, Fn &&fn) {
+    if (a.fmt == 2) return fn(moe_decode_mma_kernel<false, 0>);
+    return a.gsh_gu == 0 ? fn(moe_decode_mma_kernel<true, 0>) : fn(moe_decode_mma_kernel<true, 1>);
+}
+
+cudaError_t md_occupancy(const MdArgs &a, size_t smem, int *per_sm) {
+    return md_dispatch(a, [&](auto kern) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, kMdThreads, smem);
+    });
+}
+
+cudaError_t launch_decode_mma(const MdArgs &a, int grid, size_t smem, cudaStream_t st) {
+    return md_dispatch(a, [&](auto kern) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kMdThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, a);
+    });
+}
+
+}  // namespace coli

@@ -35,12 +35,15 @@
 #include <cstring>
 
 #include "coli_internal.cuh"
+#include "decode_route.cuh"
 #include "dp4a.cuh"
 #include "mbarrier.cuh"
 
 namespace coli {
 
 namespace {
+
+constexpr int kSdSlotsPerGroup = 2;   // a group streams into one slot while it consumes the other
 
 // Stage descriptor, written by the producer into shared memory before it arms
 // the stage's full barrier (the consumers read it after their wait).
@@ -99,17 +102,11 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
     int *slot_cnt = reinterpret_cast<int *>(base + a.off_desc + 16 * a.n_stages);   // [slot]
     uint64_t *full = reinterpret_cast<uint64_t *>(base + a.off_bar);
     uint64_t *empty = full + a.n_stages;
-    __shared__ int s_ids[kMaxDecodeSlots];
-    __shared__ float s_w[kMaxDecodeSlots];
-    __shared__ int s_exp[kMaxDecodeSlots];
-    __shared__ float s_ew[kMaxDecodeSlots];
-    __shared__ const uint8_t *s_q[kMaxDecodeSlots][3];   // routed expert's gate, up, down codes
-    __shared__ const float *s_s[kMaxDecodeSlots][3];     // and scales
-    __shared__ int s_nact, s_bad;
+    __shared__ DecodeRouting rt;
     __shared__ volatile int abort_flag;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NC = a.nc, NCT = NC * 32, NS = a.n_stages, SB = a.stage_bytes, NG = a.n_groups, GW = a.group_warps;
-    const int SPG = NS / NG;
+    constexpr int SPG = kSdSlotsPerGroup;
     const int n = a.K;   // S = 1: the token's K slots
     const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
     constexpr bool grouped = GROUPED;
@@ -126,13 +123,6 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
         d4_load_chunk<D::NIN>(a.x, a.H, okA ? cA : (long long)a.cpr_gu + 1, xv, [](const auto *p) { return __ldg(p); });
 
     // ---- phase 0: distinct routed experts in ascending id order, weights summed
-    const int pl = tid - NC * 32;   // producer-warp lane, or negative
-    int my_id = -1;
-    float my_w = 0.f;
-    if (pl >= 0 && pl < n) {
-        my_id = a.ids[pl];
-        my_w = a.w[pl];
-    }
     if (tid == 0) {
         abort_flag = 0;
         for (int i = 0; i < NS; i++) {
@@ -145,91 +135,12 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (n <= 32) {
-        if (warp == NC) {
-            const bool valid = pl < n;
-            const bool bad = valid && (my_id < -1 || my_id >= a.n_experts);
-            const unsigned any_bad = __ballot_sync(0xffffffffu, bad);
-            bool first = valid && my_id >= 0;
-            int rank = 0;
-            float wsum = 0.f;
-            for (int t = 0; t < n; t++) {
-                const int f = __shfl_sync(0xffffffffu, my_id, t);
-                const float wt = __shfl_sync(0xffffffffu, my_w, t);
-                if (f == my_id) {
-                    wsum += wt;
-                    if (t < pl) first = false;
-                }
-                // count each smaller id once, at its first slot
-                const unsigned same_before = __ballot_sync(0xffffffffu, pl < t && my_id == f);
-                if (f >= 0 && f < my_id && same_before == 0u) rank++;
-            }
-            if (first && !any_bad) {
-                s_exp[rank] = my_id;
-                s_ew[rank] = wsum;
-                const ExpertDesc &E = a.table[my_id];
-#pragma unroll
-                for (int r = 0; r < 3; r++) {
-                    s_q[rank][r] = E.m[r].q;
-                    s_s[rank][r] = E.m[r].s;
-                }
-            }
-            const unsigned nf = __popc(__ballot_sync(0xffffffffu, first));
-            if (lane == 0) {
-                s_bad = any_bad != 0u;
-                s_nact = (int)nf;
-            }
-        }
-        __syncthreads();
-    } else {
-        if (tid == 0) {
-            s_bad = 0;
-            s_nact = 0;
-        }
-        __syncthreads();
-        if (tid < n) {
-            const int e = a.ids[tid];
-            s_ids[tid] = e;
-            s_w[tid] = a.w[tid];
-            if (e < -1 || e >= a.n_experts) atomicOr(&s_bad, 1);
-        }
-        __syncthreads();
-        if (!s_bad && tid < n) {
-            const int e = s_ids[tid];
-            bool first = e >= 0;
-            int rank = 0;
-            float wsum = 0.f;
-            for (int t = 0; t < n; t++) {
-                const int f = s_ids[t];
-                if (f == e) {
-                    wsum += s_w[t];
-                    if (t < tid) first = false;
-                }
-                if (f >= 0 && f < e) {
-                    bool fst = true;   // count each smaller id once, at its first slot
-                    for (int u = 0; u < t; u++) fst &= s_ids[u] != f;
-                    rank += fst;
-                }
-            }
-            if (first) {
-                s_exp[rank] = e;
-                s_ew[rank] = wsum;
-                const ExpertDesc &E = a.table[e];
-#pragma unroll
-                for (int r = 0; r < 3; r++) {
-                    s_q[rank][r] = E.m[r].q;
-                    s_s[rank][r] = E.m[r].s;
-                }
-                atomicAdd(&s_nact, 1);
-            }
-        }
-        __syncthreads();
-    }
-    if (s_bad) {
+    decode_route(rt, a.ids, a.w, n, a.n_experts, a.table, NC);
+    if (rt.bad) {
         if (blockIdx.x == 0 && tid == 0) atomicCAS(a.err, 0, DEV_ERR_BAD_ID);
         return;
     }
-    const int nact = s_nact;
+    const int nact = rt.nact;
     const int rpcB = (a.H + gridDim.x - 1) / gridDim.x;
     const int oc0 = min(a.H, (int)blockIdx.x * rpcB), oc1 = min(a.H, oc0 + rpcB);
     // slot layouts: A = [gate codes RP rows][up codes RP rows][gate scales][up scales];
@@ -269,11 +180,11 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
                     const uint32_t cb = (uint32_t)(w * a.rs_gu);
                     const uint32_t sb = grouped ? (uint32_t)(w * a.ng_gu * 4) : 0u;
                     mbar_expect_tx(&full[s], 2 * cb + 2 * sb);
-                    bulk_load(dst, s_q[ai][0] + (size_t)j0 * a.rs_gu, cb, &full[s]);
-                    bulk_load(dst + offA_u, s_q[ai][1] + (size_t)j0 * a.rs_gu, cb, &full[s]);
+                    bulk_load(dst, rt.q[ai][0] + (size_t)j0 * a.rs_gu, cb, &full[s]);
+                    bulk_load(dst + offA_u, rt.q[ai][1] + (size_t)j0 * a.rs_gu, cb, &full[s]);
                     if (sb) {
-                        bulk_load(dst + offA_sg, s_s[ai][0] + (size_t)j0 * a.ng_gu, sb, &full[s]);
-                        bulk_load(dst + offA_su, s_s[ai][1] + (size_t)j0 * a.ng_gu, sb, &full[s]);
+                        bulk_load(dst + offA_sg, rt.s[ai][0] + (size_t)j0 * a.ng_gu, sb, &full[s]);
+                        bulk_load(dst + offA_su, rt.s[ai][1] + (size_t)j0 * a.ng_gu, sb, &full[s]);
                     }
                     idx += V;
                 } else if (jB < nstB) {
@@ -284,9 +195,9 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
                         mbar_expect_tx(&full[s], (uint32_t)ne * (cb + sb));
                         for (int m = 0; m < ne; m++) {
                             const int ai = g + m * NG;
-                            bulk_load(dst + (size_t)m * cb, s_q[ai][2] + (size_t)r0 * a.rs_d, cb, &full[s]);
+                            bulk_load(dst + (size_t)m * cb, rt.q[ai][2] + (size_t)r0 * a.rs_d, cb, &full[s]);
                             if (sb)
-                                bulk_load(dst + (size_t)ne * cb + (size_t)m * sb, s_s[ai][2] + (size_t)r0 * a.ng_d, sb,
+                                bulk_load(dst + (size_t)ne * cb + (size_t)m * sb, rt.s[ai][2] + (size_t)r0 * a.ng_d, sb,
                                           &full[s]);
                         }
                     } else {
@@ -322,7 +233,9 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
         // base run with the iteration; lanes past the end of a row read row 0's
         // codes (their limbs are zero) and the slot's zero scale.
         D xd;
-        xd.set(xv);
+        const uint32_t mbA = d4_warp_maxbits<D::NIN>(xv);
+        xd.set(xv, d4_exp(mbA));
+        const float invA = d4_unscale(mbA, D::UNSCALE_EXTRA);   // back to units of x, after the reduction
         const int rs = a.rs_gu, ng4 = a.ng_gu * 4;
         const int q0 = okA ? subA * rs + cA * 16 : 0, q1 = okA ? GA * rs : 0, dq = okA ? 2 * GA * rs : 0;
         const int giA = okA ? (cA >> a.gshift_gu) : 0;
@@ -347,30 +260,50 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
             float *red = redA + s * a.RP * nsA * 2 + r0;
             uint32_t qa = sb + q0, sa = sb + s0;
             int pp = pk;
-            for (int p0 = subA; p0 < d.w; p0 += 2 * GA) {
+            // two iterations per trip (the second one dropped past the stage's
+            // pairs), so the two reductions overlap with each other and with
+            // the dot products
+            for (int p0 = subA; p0 < d.w; p0 += 4 * GA) {
+                const bool two = p0 + 2 * GA < d.w;
+                const uint32_t qb = two ? qa + dq : qa, sb2 = two ? sa + ds : sa;
                 const uint4 qq[4] = {lds128(qa), lds128(qa + offA_u), lds128(qa + q1), lds128(qa + q1 + offA_u)};
-                float sc[4];
+                const uint4 qr[4] = {lds128(qb), lds128(qb + offA_u), lds128(qb + q1), lds128(qb + q1 + offA_u)};
+                float sc[4], sd[4];
                 if constexpr (GROUPED) {
                     sc[0] = ldsf(sa);
                     sc[1] = ldsf(sa + su);
                     sc[2] = ldsf(sa + s1);
                     sc[3] = ldsf(sa + s1 + su);
+                    sd[0] = ldsf(sb2);
+                    sd[1] = ldsf(sb2 + su);
+                    sd[2] = ldsf(sb2 + s1);
+                    sd[3] = ldsf(sb2 + s1 + su);
                 } else {
-                    const int ra = d.z + p0, rb = d.z + min(p0 + GA, d.w - 1);
                     const float z = okA ? 1.f : 0.f;
-                    sc[0] = __ldg(s_s[d.y][0] + ra) * z;
-                    sc[1] = __ldg(s_s[d.y][1] + ra) * z;
-                    sc[2] = __ldg(s_s[d.y][0] + rb) * z;
-                    sc[3] = __ldg(s_s[d.y][1] + rb) * z;
+                    const int ra = d.z + min(p0, d.w - 1), rb = d.z + min(p0 + GA, d.w - 1);
+                    const int rc = d.z + min(p0 + 2 * GA, d.w - 1), rd = d.z + min(p0 + 3 * GA, d.w - 1);
+                    sc[0] = __ldg(rt.s[d.y][0] + ra) * z;
+                    sc[1] = __ldg(rt.s[d.y][1] + ra) * z;
+                    sc[2] = __ldg(rt.s[d.y][0] + rb) * z;
+                    sc[3] = __ldg(rt.s[d.y][1] + rb) * z;
+                    sd[0] = __ldg(rt.s[d.y][0] + rc) * z;
+                    sd[1] = __ldg(rt.s[d.y][1] + rc) * z;
+                    sd[2] = __ldg(rt.s[d.y][0] + rd) * z;
+                    sd[3] = __ldg(rt.s[d.y][1] + rd) * z;
                 }
-                float dd[4];
+                float dd[4], de[4];
                 xd.template dotn<4>(qq, dd);
+                xd.template dotn<4>(qr, de);
                 const float t = sd_warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
-                if ((lane & 7) == 0 && pp < d.w) *red = t;
-                qa += dq;
-                sa += ds;
-                red += dr;
-                pp += 2 * GA;
+                const float t2 = sd_warp_sum4(de[0] * sd[0], de[1] * sd[1], de[2] * sd[2], de[3] * sd[3], lane);
+                if ((lane & 7) == 0) {
+                    if (pp < d.w) red[0] = t * invA;
+                    if (pp + 2 * GA < d.w) red[dr] = t2 * invA;
+                }
+                qa += 2 * dq;
+                sa += 2 * ds;
+                red += 2 * dr;
+                pp += 4 * GA;
             }
             // the last warp of the group to finish the stage turns its pairs into
             // h = silu(g) * u (plain stores; the grid barrier publishes them)
@@ -402,22 +335,7 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
     // grid barrier among the consumers of all CTAs: every h is in global memory
     // after it (the producer keeps copying phase-B stages meanwhile)
     named_sync(1, NCT);
-    if (tid == 0 && !abort_flag) {
-        __threadfence();
-        atomicAdd(arrived, 1u);
-        while (true) {
-            unsigned v;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(arrived) : "memory");
-            if (v >= gridDim.x) break;
-            if (global_ns() > deadline) {
-                atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
-                abort_flag = 1;
-                break;
-            }
-            __nanosleep(32);
-        }
-        __threadfence();
-    }
+    if (tid == 0 && !abort_flag && !decode_grid_barrier(arrived, deadline, a.err)) abort_flag = 1;
     named_sync(1, NCT);
     // phase B: warp gi of group grp owns expert ai = grp + NG (gi / nsBW) and the
     // slabs SPW (gi % nsBW) ..; its h limbs are converted here, once
@@ -426,6 +344,7 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
         const int ai = grp + NG * m;
         const bool active = ai < nact;
         D xb[D::SPW];
+        float invB[D::SPW];
         bool okB[D::SPW];
         int qoffB[D::SPW], giB[D::SPW];
 #pragma unroll
@@ -436,9 +355,13 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
             qoffB[u] = okB[u] ? cB * 16 : 0;
             giB[u] = okB[u] ? (cB >> a.gshift_d) : 0;
             float v[D::NIN];
+            // L1-allocating loads: a lane reads all 128 bytes of one line, and the
+            // grid barrier's acquire has dropped any older copy from this SM's L1
             d4_load_chunk<D::NIN>(a.hbuf + (size_t)(active ? ai : 0) * a.F, a.F, okB[u] ? cB : (long long)a.cpr_d + 1,
-                                  v, [](const auto *p) { return __ldcg(p); });
-            xb[u].set(v);
+                                  v, [](const auto *p) { return __ldca(p); });
+            const uint32_t mb = d4_warp_maxbits<D::NIN>(v);
+            xb[u].set(v, d4_exp(mb));
+            invB[u] = d4_unscale(mb, D::UNSCALE_EXTRA);
         }
         const int rsd = a.rs_d, ngd4 = a.ng_d * 4;
         while (true) {
@@ -472,6 +395,34 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
                     const int dq = okB[u] ? rsd : 0, dsc = okB[u] ? ngd4 : 0;
                     float *rr = rb + slab;
                     int r0 = 0;
+                    // eight rows per trip: two independent dot products and reductions
+                    for (; r0 + 8 <= nr; r0 += 8) {
+                        const uint4 qq[4] = {lds128(qa), lds128(qa + dq), lds128(qa + 2 * dq), lds128(qa + 3 * dq)};
+                        const uint4 qr[4] = {lds128(qa + 4 * dq), lds128(qa + 5 * dq), lds128(qa + 6 * dq),
+                                             lds128(qa + 7 * dq)};
+                        float sc[8];
+                        if constexpr (GROUPED) {
+#pragma unroll
+                            for (int q = 0; q < 8; q++) sc[q] = ldsf(sa + q * dsc);
+                        } else {
+                            const float *ps = rt.s[ai][2] + d.z + r0;
+                            const float z = okB[u] ? 1.f : 0.f;
+#pragma unroll
+                            for (int q = 0; q < 8; q++) sc[q] = __ldg(ps + q) * z;
+                        }
+                        float dd[4], de[4];
+                        xb[u].template dotn<4>(qq, dd);
+                        xb[u].template dotn<4>(qr, de);
+                        const float t = sd_warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
+                        const float t2 = sd_warp_sum4(de[0] * sc[4], de[1] * sc[5], de[2] * sc[6], de[3] * sc[7], lane);
+                        if ((lane & 7) == 0) {
+                            rr[0] = t * invB[u];
+                            rr[4 * nsB] = t2 * invB[u];
+                        }
+                        qa += 8 * dq;
+                        sa += 8 * dsc;
+                        rr += 8 * nsB;
+                    }
                     for (; r0 + 4 <= nr; r0 += 4) {
                         const uint4 qq[4] = {lds128(qa), lds128(qa + dq), lds128(qa + 2 * dq), lds128(qa + 3 * dq)};
                         float sc[4];
@@ -481,7 +432,7 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
                             sc[2] = ldsf(sa + 2 * dsc);
                             sc[3] = ldsf(sa + 3 * dsc);
                         } else {
-                            const float *ps = s_s[ai][2] + d.z + r0;
+                            const float *ps = rt.s[ai][2] + d.z + r0;
                             const float z = okB[u] ? 1.f : 0.f;
                             sc[0] = __ldg(ps) * z;
                             sc[1] = __ldg(ps + 1) * z;
@@ -491,7 +442,7 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
                         float dd[4];
                         xb[u].template dotn<4>(qq, dd);
                         const float t = sd_warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
-                        if ((lane & 7) == 0) *rr = t;
+                        if ((lane & 7) == 0) *rr = t * invB[u];
                         qa += 4 * dq;
                         sa += 4 * dsc;
                         rr += 4 * nsB;
@@ -504,7 +455,7 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
                         for (int q = 0; q < 3; q++) {
                             const int rq = min(q, rem - 1);
                             if constexpr (GROUPED) sc[q] = ldsf(sa + rq * dsc);
-                            else sc[q] = okB[u] ? __ldg(s_s[ai][2] + d.z + r0 + rq) : 0.f;
+                            else sc[q] = okB[u] ? __ldg(rt.s[ai][2] + d.z + r0 + rq) : 0.f;
                         }
                         if (rem == 1) {
                             const uint4 q1[1] = {lds128(qa)};
@@ -526,7 +477,7 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
                             v4[2] = d3[2] * sc[2];
                         }
                         const float t = sd_warp_sum4(v4[0], v4[1], v4[2], v4[3], lane);
-                        if ((lane & 7) == 0 && kk < rem) *rr = t;
+                        if ((lane & 7) == 0 && kk < rem) *rr = t * invB[u];
                     }
                 }
             }
@@ -541,20 +492,13 @@ __global__ void __launch_bounds__((NCMAX + 1) * 32, 1) moe_decode_stream_kernel(
         for (int ai = 0; ai < nact; ai++) {
             float dsum = 0.f;
             for (int q = 0; q < nsB; q++) dsum += redB[(ai * rpcB + rr) * nsB + q];
-            acc = fmaf(s_ew[ai], dsum, acc);
+            acc = fmaf(rt.ew[ai], dsum, acc);
         }
         a.y[oc0 + rr] = acc;
     }
     // the last CTA out resets the barrier counter for the next call, also after
     // an aborted call
-    if (tid == 0) {
-        __threadfence();
-        if (atomicAdd(exitc, 1u) == gridDim.x - 1) {
-            *arrived = 0u;
-            *exitc = 0u;
-            __threadfence();
-        }
-    }
+    if (tid == 0) decode_exit(exitc, arrived);
 }
 
 template <class D, bool GROUPED, int NCMAX>
@@ -609,8 +553,7 @@ bool sd_plan(int fmt, int H, int F, int K, int cpr_gu, int cpr_d, int rs_gu, int
     if (L > ncmax) return false;
     const int NG = std::min(3, ncmax / L);
     const int GW = (ncmax / NG) / L * L;
-    const int SPG = 2;   // slots per group
-    const int NS = SPG * NG;
+    const int NS = kSdSlotsPerGroup * NG;
     const int GA = GW / nsA;
     // phase B: every routed expert of a group needs nsBW warps of it
     const int ne_max = (K + NG - 1) / NG;
