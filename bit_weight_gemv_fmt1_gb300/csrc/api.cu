@@ -817,15 +817,14 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
             Workspace *ws = nullptr;
             if (int rc = workspace(ds, st, md_scratch_bytes(a), &ws)) return rc;
             unsigned *ctr = nullptr;
-            if (int rc = decode_counters(ds, st, md_counter_words(), &ctr)) return rc;
+            if (int rc = decode_counters(ds, st, md_counter_words(a), &ctr)) return rc;
             a.x = x;
             a.ids = ids;
             a.w = w;
             a.y = y;
             a.table = table;
             a.n_experts = n_experts;
-            a.hbuf = (float *)ws->buf;
-            a.part = a.hbuf + (size_t)K * F;
+            a.part = (float *)ws->buf;
             a.ctr = ctr;
             a.err = ds->err;
             a.timeout_ns = 2000000000LL;

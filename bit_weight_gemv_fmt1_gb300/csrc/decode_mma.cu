@@ -28,8 +28,7 @@
 //
 // Roles.  Warps 0..15 consume, warp 16 produces: its lane 0 streams stages
 // into kMdSlots shared-memory slots with bulk copies (cp.async.bulk) and a
-// descriptor per slot.  Warp 17 finishes every stage (below); warp 18 publishes
-// the h it writes to the other CTAs.  A stage holds whole rows in four blocks of rows; the
+// descriptor per slot.  Warp 17 finishes every stage (below).  A stage holds whole rows in four blocks of rows; the
 // blocks start 32 bytes apart modulo 128, and the 16 rows of an mma tile take
 // row r of all four blocks for r = 0..3, so the 8-byte code loads of a
 // half-warp fall in four different bank quarters.  Warp w owns the 64-input
@@ -38,20 +37,25 @@
 //   phase 0: the token's routed experts, distinct and in ascending id order,
 //            duplicate slots' weights summed (decode_route.cuh).
 //   phase A: stages of 8 (gate, up) row pairs of one routed expert, dealt
-//            round robin over the CTAs.  Every consumer warp writes its
-//            segments' share of the 16 rows to the slot's partial-sum table
-//            and moves on; warp 17 sums the table in warp order, writes
-//            h[a][j] = silu(gate) * up to global scratch and frees the slot.
-//   grid barrier (the producer meanwhile copies the first phase-B stages).
-//   phase B: the CTA owns output rows [oc0, oc1); one stage per routed expert
-//            holds those rows of its down matrix.  Each warp builds the B
-//            fragments of its segments of that expert's h and accumulates
-//            w_a * (its share of down_a . h_a) per row in registers across
-//            the experts; at the end the 16 warps' shares are summed in warp
-//            order: y[o] is written once.
+//            round robin over the CTAs, the last routed expert's first.
+//            Every consumer warp writes its segments' share of the 16 rows to
+//            the slot's partial-sum table and moves on; warp 17 sums the table
+//            in warp order and writes h[a][j] = silu(gate) * up to global
+//            memory, each value as one 64-bit word under the call's tag.
+//   phase B: the CTAs of the grid are split evenly among the routed
+//            experts; a CTA owns a range of whole 48-row stages of its
+//            expert's down rows.  Each warp polls until the h
+//            values of its segments carry the call's tag (no fence or grid
+//            barrier: a 64-bit store is seen whole), builds their B fragments
+//            once and streams the CTA's rows in stages of 48; warp 17 sums the
+//            warps' shares of each row in warp order into part[a][o].
+//   y:       the CTA whose rows complete a 64-row block of y (counted with
+//            atomics after a fence) sums part over the routed experts in
+//            order, with their routing weights: y[o] is written once.
 // Results do not depend on timing or on the number of SMs.  Every wait is
 // bounded (mbarrier.cuh); on expiry the kernel records DEV_ERR_TIMEOUT and
-// returns.  The last CTA to leave resets the call's barrier counter.
+// returns.  The last CTA to leave clears the block counts and moves the tag
+// on for the next call.
 #include <algorithm>
 #include <cstring>
 
@@ -63,17 +67,25 @@ namespace coli {
 
 namespace {
 
-constexpr int kMdWarps = 16;     // consumer warps; then the producer, epilogue and signal warps
-constexpr int kMdThreads = (kMdWarps + 3) * 32;
-constexpr int kMdQueue = 16;     // entries of the epilogue -> signal queue
+constexpr int kMdWarps = 16;     // consumer warps; then the producer warp and the epilogue warp
+constexpr int kMdThreads = (kMdWarps + 2) * 32;
 constexpr int kMdSlots = 3;      // shared-memory slots of the stage ring
+// back-off (ns) of a waiting warp: consumer, epilogue, producer
+constexpr uint32_t kMdNapC = 0, kMdNapE = 64, kMdNapP = 64;
 constexpr int kMdSegMax = 6;     // 64-input segments per warp and row (H, F <= 6144)
 constexpr int kMdTiles = 3;                   // 16-row mma tiles of a phase-B stage
 constexpr int kMdBlockRows = 4 * kMdTiles;     // rows of each of a phase-B stage's four blocks
 constexpr int kMdStageRows = 4 * kMdBlockRows; // down rows of a phase-B stage (48)
 constexpr int kMdMaxBlocks = 128;              // 64-row blocks of y (H <= 8192)
-constexpr int kMdCtrReady = 4;                 // counter words: [1] CTAs out, [4..68) ready, [68..) blocks
-constexpr int kMdCtrBlocks = kMdCtrReady + kMaxDecodeSlots;
+// partial sums of a stage: phase A [warp][48] (16 rows used), phase B
+// [row][20] (16 warps, padded so that a lane's row is one conflict-free
+// 128-bit load per 4 warps)
+constexpr int kMdRedB = 20;
+constexpr int kMdRedSlot = kMdStageRows * kMdRedB;
+// state words of a call (zero before the first call): [1] CTAs out, [3] epoch,
+// [4 ..) 64-row block counts of y, then the tagged h [K][F] (8 bytes each)
+constexpr int kMdCtrBlocks = 4;
+constexpr int kMdCtrH = kMdCtrBlocks + kMdMaxBlocks;
 
 enum : int { MD_A = 0, MD_B = 1, MD_END = 2 };
 
@@ -308,6 +320,49 @@ __device__ __forceinline__ void md_tileA(float (&y)[4], uint32_t cq, uint32_t rs
     }
 }
 
+// The CTAs that own routed expert e in the down phase: [cb(e), cb(e + 1))
+// with cb(e) = ceil(e G / nact).  eB: the expert of CTA c, [cb0, cb1) its CTAs.
+__device__ __forceinline__ void md_owner(int c, int nact, int G, int *eB, int *cb0, int *cb1) {
+    auto cb = [&](int e) -> int { return (int)(((long long)e * G + nact - 1) / nact); };
+    int e = (int)(((long long)c * nact) / G);
+    while (e > 0 && cb(e) > c) e--;
+    while (e + 1 < nact && cb(e + 1) <= c) e++;
+    *eB = e;
+    *cb0 = cb(e);
+    *cb1 = cb(e + 1);
+}
+
+// The h values lane `lane` of a phase-B warp needs (inputs 64 q0 + 4 lane +
+// 0..3 of the warp's segments, as md_load4): each is the f32 bits under the
+// call's tag in a 64-bit word.  Polls until every value of the warp carries
+// `tag`; false (for the whole warp) once the deadline passed or the CTA
+// aborted.
+__device__ __forceinline__ bool md_load_h(const unsigned long long *h, int n, int q0, int nq, int lane, unsigned tag,
+                                          uint64_t deadline, volatile int *abort, float4 *out) {
+    const int seg = lane >> 4;
+    const long long i0 = (long long)(q0 + seg) * 64 + 4 * (lane & 15);
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    while (true) {
+        bool ok = true;
+        if (seg < nq) {
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                if (i0 + j < n) {
+                    unsigned long long w;
+                    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(h + i0 + j) : "memory");
+                    ok &= (unsigned)(w >> 32) == tag;
+                    v[j] = __uint_as_float((unsigned)w);
+                }
+            }
+        }
+        if (__all_sync(0xffffffffu, ok)) break;
+        if (__any_sync(0xffffffffu, *abort != 0 || global_ns() > deadline)) return false;
+        __nanosleep(128);
+    }
+    *out = make_float4(v[0], v[1], v[2], v[3]);
+    return true;
+}
+
 // The epilogue's release of a slot: one arrival that counts for all the
 // consumer warps.
 __device__ __forceinline__ void md_release(uint64_t *bar) {
@@ -317,15 +372,28 @@ __device__ __forceinline__ void md_release(uint64_t *bar) {
 
 // A warp's bounded wait for a stage (every lane polls; false for the whole
 // warp once any lane hit the deadline or the CTA aborted).
-__device__ __forceinline__ bool md_wait(uint64_t *bar, uint32_t parity, uint64_t deadline, volatile int *abort) {
+// After a failed try the warp sleeps `nap` ns (0: none), so that a waiting
+// warp leaves the issue slots of its SM sub-partition to the working ones.
+__device__ __forceinline__ bool md_wait(uint64_t *bar, uint32_t parity, uint64_t deadline, volatile int *abort,
+                                        uint32_t nap) {
     bool ok = true;
     while (!mbar_try(bar, parity)) {
         if (*abort || global_ns() > deadline) {
             ok = false;
             break;
         }
+        if (nap) __nanosleep(nap);
     }
     return __all_sync(0xffffffffu, ok);
+}
+// The producer lane's wait for a free slot, with the same back-off.
+__device__ __forceinline__ bool md_wait1(uint64_t *bar, uint32_t parity, uint64_t deadline, volatile int *abort,
+                                         uint32_t nap) {
+    while (!mbar_try(bar, parity)) {
+        if (*abort || global_ns() > deadline) return false;
+        if (nap) __nanosleep(nap);
+    }
+    return true;
 }
 
 // GSH: log2(gs / 64), segments per scale group (fmt 4); 0 for fmt 2.
@@ -333,7 +401,7 @@ template <bool GROUPED, int GSH>
 __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdArgs a) {
     extern __shared__ uint8_t sraw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)sraw + 127) & ~(uintptr_t)127);
-    float *red = reinterpret_cast<float *>(base + a.off_red);   // [slot][warp][48]: partial sums of a stage
+    float *red = reinterpret_cast<float *>(base + a.off_red);   // [slot][kMdRedSlot]: partial sums of a stage
     int4 *desc = reinterpret_cast<int4 *>(base + a.off_bar);    // [slot]
     uint64_t *full = reinterpret_cast<uint64_t *>(desc + kMdSlots);
     uint64_t *empty = full + kMdSlots;
@@ -341,18 +409,18 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     __shared__ DecodeRouting rt;
     __shared__ volatile int abort_flag;
     __shared__ float4 s_cf[kMdWarps][kMdSegMax + 1];   // phase-A chain starts of each warp's segments, their sum
-    __shared__ __align__(16) uint8_t s_stg[kMdWarps][512];   // B-fragment staging, one area per consumer warp
-    __shared__ __align__(16) uint32_t s_zrow[4];             // the all-zero B columns
+    __shared__ __align__(16) uint8_t s_stg[kMdWarps][528];   // B-fragment staging of each consumer warp, + a zero row
     __shared__ int s_done[kMdMaxBlocks];                     // output blocks this CTA completes
     __shared__ int s_ndone;
-    __shared__ int2 s_q[kMdQueue];                           // (expert, pairs) of h written, for the signal warp
-    __shared__ unsigned s_qn, s_qdone;                       // entries written / published
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int SB = a.slot_bytes;
     const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
     unsigned *exitc = a.ctr + 1;
-    unsigned *ready = a.ctr + kMdCtrReady;   // [routed expert]: pairs of h written
     unsigned *blkc = a.ctr + kMdCtrBlocks;   // [64-row block of y]: expert rows summed into part
+    // h values carry the call's tag in their high word: a 64-bit store is seen
+    // whole or not at all, so a reader knows a value is this call's without a fence
+    unsigned long long *htag = reinterpret_cast<unsigned long long *>(a.ctr + kMdCtrH);
+    const unsigned tag = *(volatile unsigned *)(a.ctr + 3) + 1u;
 
     // consumers load their x values now; the fragments are built after routing
     const int q0A = warp * a.spwA, nqA = min(a.spwA, a.nsegA - q0A);
@@ -363,20 +431,61 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
         for (int r = 0; r < NR; r++) ldA[r] = md_load4(a.x, a.H, q0A, nqA, r, lane, false);
     }
 
-    if (tid < 4) s_zrow[tid] = 0u;
-    if (tid == 0) {
+    // routing: by the producer warp alone for K <= 32 (the consumers build their
+    // phase-A fragments meanwhile), else by the whole CTA
+    auto md_init = [&]() {
         abort_flag = 0;
         s_ndone = 0;
-        s_qn = 0u;
-        s_qdone = 0u;
         for (int i = 0; i < kMdSlots; i++) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kMdWarps);
             mbar_init(&redfull[i], kMdWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    };
+    const bool wroute = a.K <= 32;
+    if (!wroute) {
+        if (tid == 0) md_init();
+        decode_route(rt, a.ids, a.w, a.K, a.n_experts, a.table, kMdWarps);
+    } else if (warp == kMdWarps) {
+        decode_route_warp(rt, a.ids, a.w, a.K, a.n_experts, a.table);
+        if (lane == 0) md_init();
+        __syncwarp();
     }
-    decode_route(rt, a.ids, a.w, a.K, a.n_experts, a.table, kMdWarps);
+    // phase-A B fragments of the consumer warps (the token's x: no routing needed)
+    uint32_t bfA[kMdSegMax][8];
+    float unA = 0.f;
+    if (warp < kMdWarps) {
+        uint32_t *zr = reinterpret_cast<uint32_t *>(&s_stg[warp][512]);
+        if (lane < 4) zr[lane] = 0u;
+        __syncwarp();
+        const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(zr);
+        const MdScale scA = md_scale<NR>(ldA);
+        unA = scA.unscale * 0x1p24f;
+        float4 cft = make_float4(0.f, 0.f, 0.f, 0.f);   // per-row formats: the chain start of the whole row
+#pragma unroll
+        for (int r = 0; r < NR; r++) {
+            float4 c0, c1;
+            md_frags(ldA[r], scA, nqA - 2 * r, lane, stg, zrow, bfA[2 * r], bfA[2 * r + 1], c0, c1);
+            if (lane == 0) {
+                s_cf[warp][2 * r] = c0;
+                s_cf[warp][2 * r + 1] = c1;
+            }
+            cft.x += c0.x + c1.x;
+            cft.y += c0.y + c1.y;
+            cft.z += c0.z + c1.z;
+            cft.w += c0.w + c1.w;
+        }
+        // lane 0 holds the hi / lo quads of tile row 0; every row's start is the same
+        if (lane == 0) s_cf[warp][kMdSegMax] = cft;
+        __syncwarp();
+    }
+    // the routing and the shared state are visible to every warp after this
+    // barrier; the producer passes it without waiting
+    if (warp == kMdWarps)
+        asm volatile("bar.arrive 5, %0;" ::"r"(kMdThreads) : "memory");
+    else
+        named_sync(5, kMdThreads);
     if (rt.bad) {
         if (blockIdx.x == 0 && tid == 0) atomicCAS(a.err, 0, DEV_ERR_BAD_ID);
         return;
@@ -391,10 +500,12 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     // phase B: this CTA's routed expert eB (the CTAs of an expert split its
     // down rows evenly) and its rows [rb0, rb1)
     const int G = gridDim.x;
-    const int eB = (int)(((long long)blockIdx.x * nact) / G);
-    const int cb0 = (int)(((long long)eB * G + nact - 1) / nact), cb1 = (int)(((long long)(eB + 1) * G + nact - 1) / nact);
-    const int rb0 = (int)((long long)a.H * (blockIdx.x - cb0) / (cb1 - cb0));
-    const int rb1 = (int)((long long)a.H * (blockIdx.x - cb0 + 1) / (cb1 - cb0));
+    int eB = 0, cb0 = 0, cb1 = G;
+    md_owner(blockIdx.x, nact, G, &eB, &cb0, &cb1);
+    // whole 48-row stages of the expert's rows, split evenly among its CTAs
+    const int nsE = (a.H + kMdStageRows - 1) / kMdStageRows, kB = blockIdx.x - cb0, nB_ = cb1 - cb0;
+    const int rb0 = min(a.H, kMdStageRows * (int)((long long)nsE * kB / nB_));
+    const int rb1 = min(a.H, kMdStageRows * (int)((long long)nsE * (kB + 1) / nB_));
 
     if (warp == kMdWarps) {
         // ---------------- producer: lane 0 issues every stage of the CTA.  Phase-A
@@ -409,7 +520,13 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             int jB = 0, i = 0;
             while (true) {
                 const int s = i % kMdSlots;
-                if (i >= kMdSlots && !mbar_wait(&empty[s], ((i / kMdSlots) & 1) ^ 1, deadline, &abort_flag)) {
+                // the first stage is copied alone (its bytes are then not interleaved
+                // with the next stages'), so that the consumers can start early
+                if (i == 1) {
+                    volatile int no_abort = 0;
+                    mbar_wait(&full[0], 0, global_ns() + 4000, &no_abort);
+                }
+                if (i >= kMdSlots && !md_wait1(&empty[s], ((i / kMdSlots) & 1) ^ 1, deadline, &abort_flag, kMdNapP)) {
                     if (!abort_flag) {
                         abort_flag = 1;
                         atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
@@ -480,44 +597,24 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
 
     if (warp == kMdWarps + 1) {
         // ---------------- epilogue: sums the consumer warps' partials of each stage
-        // in warp order, then frees the slot.  Phase A: h = silu(gate) * up and the
-        // expert's ready count; phase B: the expert's rows of part
+        // in warp order, then frees the slot.  Phase A: h = silu(gate) * up, stored
+        // under the call's tag; phase B: the expert's rows of part
         int i = 0;
         bool ok = true;
-        // the h of a stage is handed to the signal warp, which publishes it (the
-        // gpu-scope fence that takes is then off this warp's path)
-        unsigned qn = 0;
-        bool qopen = true;
-        auto push = [&](int e, int w) {
-            __syncwarp();
-            if (lane == 0) {
-                while (qn - *(volatile unsigned *)&s_qdone >= (unsigned)kMdQueue) {
-                    if (abort_flag || global_ns() > deadline) break;
-                    __nanosleep(32);
-                }
-                s_q[qn % kMdQueue] = make_int2(e, w);
-                asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_addr(&s_qn)), "r"(qn + 1) : "memory");
-            }
-            qn++;
-        };
         while (true) {
             const int s = i % kMdSlots;
             const uint32_t par = (uint32_t)((i / kMdSlots) & 1);
-            if (!md_wait(&full[s], par, deadline, &abort_flag)) {
+            if (!md_wait(&full[s], par, deadline, &abort_flag, kMdNapE)) {
                 ok = false;
                 break;
             }
             const int4 d = desc[s];
-            if (d.x != MD_A && qopen) {
-                push(-1, 0);   // phase A is over for this CTA
-                qopen = false;
-            }
             if (d.x == MD_END) break;
-            if (!md_wait(&redfull[s], par, deadline, &abort_flag)) {
+            if (!md_wait(&redfull[s], par, deadline, &abort_flag, kMdNapE)) {
                 ok = false;
                 break;
             }
-            const float *rd = red + s * kMdWarps * kMdStageRows;
+            const float *rd = red + s * kMdRedSlot;
             if (d.x == MD_A) {
                 // row m = lane % 16 summed over warps 8 (lane / 16) .. + 7, then the two halves
                 const float *rp = rd + (lane >> 4) * 8 * kMdStageRows + (lane & 15);
@@ -537,20 +634,28 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                         gv *= __ldg(rt.s[d.y][0] + d.z + lane);
                         uv *= __ldg(rt.s[d.y][1] + d.z + lane);
                     }
-                    a.hbuf[(size_t)d.y * a.F + d.z + lane] = gv / (1.0f + expf(-gv)) * uv;
+                    const float h = gv / (1.0f + expf(-gv)) * uv;
+                    const unsigned long long hv = ((unsigned long long)tag << 32) | __float_as_uint(h);
+                    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(htag + (size_t)d.y * a.F + d.z + lane),
+                                 "l"(hv)
+                                 : "memory");
                 }
-                push(d.y, d.w);
             } else {
-                // stage row rr: block rr / 12, row rin = rr % 12 of it = tile rin / 4, tile row 4 (rin % 4) + block
+                // stage row rr = lane (+ 32): the 16 warps' shares in warp order
                 float v[2] = {0.f, 0.f};
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     const int rr = lane + 32 * h;
                     if (rr < d.w) {
-                        const int b = rr / kMdBlockRows, rin = rr - b * kMdBlockRows;
-                        const int col = (rin >> 2) * 16 + 4 * (rin & 3) + b;
+                        const float4 *rr4 = reinterpret_cast<const float4 *>(rd + rr * kMdRedB);
 #pragma unroll
-                        for (int w = 0; w < kMdWarps; w++) v[h] += rd[w * kMdStageRows + col];
+                        for (int w4 = 0; w4 < kMdWarps / 4; w4++) {
+                            const float4 q = rr4[w4];
+                            v[h] += q.x;
+                            v[h] += q.y;
+                            v[h] += q.z;
+                            v[h] += q.w;
+                        }
                     }
                 }
                 __syncwarp();
@@ -566,7 +671,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             }
             i++;
         }
-        if (qopen) push(-1, 0);
         if (!ok && lane == 0 && !abort_flag) {
             abort_flag = 1;
             atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
@@ -585,61 +689,17 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             __threadfence();
         }
         named_sync(2, (kMdWarps + 1) * 32);
-    } else if (warp == kMdWarps + 2) {
-        // ---------------- signal: publishes the h the epilogue wrote.  The acquire of
-        // the queue count orders the epilogue's h stores before this lane's
-        // gpu-scope fence, which orders them before the ready counts it raises
-        if (lane == 0) {
-            unsigned k = 0;
-            bool more = true;
-            while (more) {
-                unsigned n;
-                asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(n) : "r"(smem_addr(&s_qn)) : "memory");
-                if (n == k) {
-                    if (abort_flag || global_ns() > deadline) break;
-                    __nanosleep(64);
-                    continue;
-                }
-                __threadfence();
-                for (; k < n && more; k++) {
-                    const int2 q = s_q[k % kMdQueue];
-                    if (q.x < 0) more = false;
-                    else atomicAdd(&ready[q.x], (unsigned)q.y);
-                }
-                *(volatile unsigned *)&s_qdone = k;
-            }
-        }
-        return;
     } else {
         // ---------------- consumers
         const uint32_t ring_s = smem_addr(base);
         const int g = lane >> 2, t = lane & 3;
         const int blk = g & 3, rib = g >> 2;   // block and row in block of tile row g (row g + 8: rib + 2)
-        const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(s_zrow);
+        const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(&s_stg[warp][512]);
         int i = 0;                              // stage counter
         bool live = true;
         {
             // phase A
-            uint32_t bf[kMdSegMax][8];
-            const MdScale scA = md_scale<NR>(ldA);
-            const float unA = scA.unscale * 0x1p24f;
-            float4 cft = make_float4(0.f, 0.f, 0.f, 0.f);   // per-row formats: the chain start of the whole row
-#pragma unroll
-            for (int r = 0; r < NR; r++) {
-                float4 c0, c1;
-                md_frags(ldA[r], scA, nqA - 2 * r, lane, stg, zrow, bf[2 * r], bf[2 * r + 1], c0, c1);
-                if (lane == 0) {
-                    s_cf[warp][2 * r] = c0;
-                    s_cf[warp][2 * r + 1] = c1;
-                }
-                cft.x += c0.x + c1.x;
-                cft.y += c0.y + c1.y;
-                cft.z += c0.z + c1.z;
-                cft.w += c0.w + c1.w;
-            }
-            // lane 0 holds the hi / lo quads of tile row 0; every row's start is the same
-            if (lane == 0) s_cf[warp][kMdSegMax] = cft;
-            __syncwarp();
+            uint32_t(&bf)[kMdSegMax][8] = bfA;
             const uint32_t rs2 = 2u * (uint32_t)a.rs_gu;
             const uint32_t cofs = (uint32_t)(blk * (a.bsA + 32) + rib * a.rs_gu + 32 * q0A + 8 * t);
             const uint32_t sofs = (uint32_t)(a.soA + blk * a.ssA + rib * a.ng_gu * 4 + (q0A >> GSH) * 4);
@@ -648,7 +708,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             const bool fullA = nqA == kMdSegMax;
             while (true) {
                 const int s = i % kMdSlots;
-                if (!md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag)) {
+                if (!md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag, kMdNapC)) {
                     if (lane == 0 && !abort_flag) {
                         abort_flag = 1;
                         atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
@@ -664,7 +724,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                     md_tileA<GROUPED, GSH, true>(y, sb + cofs, rs2, cfs, sb + sofs, sr2, nqA, bf);
                 else if (nqA > 0)
                     md_tileA<GROUPED, GSH, false>(y, sb + cofs, rs2, cfs, sb + sofs, sr2, nqA, bf);
-                float *rw = red + (s * kMdWarps + warp) * kMdStageRows;
+                float *rw = red + s * kMdRedSlot + warp * kMdStageRows;
                 if (t == 0) {
                     const bool on = nqA > 0;
                     rw[g] = on ? fmaf(y[1], 0x1p-11f, y[0]) * unA : 0.f;
@@ -676,29 +736,8 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                 i++;
             }
         }
-        // phase B: wait until every pair of h of expert eB is written (one thread
-        // polls the expert's ready count), build the B fragments of the warp's
-        // segments of it once, then stream the CTA's rows of down[eB]
-        // (every consumer warp reaches this point, so the barrier below is CTA-uniform)
-        if (rb1 > rb0) {
-            if (tid == 0) {
-                while (true) {
-                    unsigned v;
-                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ready + eB) : "memory");
-                    if (v >= (unsigned)a.F) break;
-                    if (abort_flag || global_ns() > deadline) {
-                        if (!abort_flag) {
-                            abort_flag = 1;
-                            atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
-                        }
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
-            named_sync(3, kMdWarps * 32);
-            live = live && !abort_flag;
-        }
+        // phase B: the warp's h values of expert eB (this call's tag on every one),
+        // its B fragments built once, then the CTA's rows of down[eB]
         if (live && rb1 > rb0) {
             const int q0B = warp * a.spwB, nqB = min(a.spwB, a.nsegB - q0B);
             const int rs = a.rs_d;
@@ -708,15 +747,31 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             float4 cq[2];
             float unB = 0.f;
             {
-                float4 ld[1] = {md_load4(a.hbuf + (size_t)eB * a.F, a.F, q0B, nqB, 0, lane, true)};
-                const MdScale scB = md_scale<1>(ld);
+                float4 ld = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!md_load_h(htag + (size_t)eB * a.F, a.F, q0B, nqB, lane, tag, deadline, &abort_flag, &ld)) {
+                    if (lane == 0 && !abort_flag) {
+                        abort_flag = 1;
+                        atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+                    }
+                    live = false;
+                }
+                float4 lda[1] = {ld};
+                const MdScale scB = md_scale<1>(lda);
                 unB = scB.unscale * 0x1p24f;
-                md_frags(ld[0], scB, nqB, lane, stg, zrow, bf[0], bf[1], cq[0], cq[1]);
+                md_frags(ld, scB, nqB, lane, stg, zrow, bf[0], bf[1], cq[0], cq[1]);
             }
             const bool fullB = nqB == 2;
-            while (true) {
+            // offsets of the tiles' code words and scales (rows 4 T + rib of each block)
+            uint32_t tco[kMdTiles], tso[kMdTiles];
+#pragma unroll
+            for (int T = 0; T < kMdTiles; T++) {
+                tco[T] = cofs + (uint32_t)(4 * T * rs);
+                tso[T] = sofs + (uint32_t)(4 * T * a.ng_d * 4);
+            }
+            const uint32_t rs2 = 2u * (uint32_t)rs, sr2 = 8u * (uint32_t)a.ng_d;
+            while (live) {
                 const int s = i % kMdSlots;
-                if (!md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag)) {
+                if (!md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag, kMdNapC)) {
                     if (lane == 0 && !abort_flag) {
                         abort_flag = 1;
                         atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
@@ -730,22 +785,22 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                     break;
                 }
                 const uint32_t sb = ring_s + (uint32_t)(s * SB);
-                float *rw = red + (s * kMdWarps + warp) * kMdStageRows;
+                // tile row m = g, g + 8 of tile T is stage row 12 (m % 4) + 4 T + m / 4
+                float *rw = red + s * kMdRedSlot + (blk * kMdBlockRows + rib) * kMdRedB + warp;
 #pragma unroll
                 for (int T = 0; T < kMdTiles; T++) {
                     float y[4] = {0.f, 0.f, 0.f, 0.f};
                     if (nqB > 0) {
-                        const uint32_t tofs = sb + cofs + (uint32_t)(4 * T * rs);
-                        const uint32_t tsc = sb + sofs + (uint32_t)(4 * T * a.ng_d * 4);
+                        const uint32_t tofs = sb + tco[T], tsc = sb + tso[T];
 #pragma unroll
                         for (int sg = 0; sg < 2; sg++) {
                             if (fullB || sg < nqB) {
-                                const uint2 cg = lds64(tofs + 32 * sg), ch = lds64(tofs + 2 * rs + 32 * sg);
+                                const uint2 cg = lds64(tofs + 32 * sg), ch = lds64(tofs + rs2 + 32 * sg);
                                 if (GROUPED) {
                                     float dd[4];
                                     md_segment_c(dd, cg, ch, bf[sg], cq[sg]);
                                     const uint32_t sa = tsc + 4 * (sg >> GSH);
-                                    const float sgv = md_ldsf(sa), shv = md_ldsf(sa + 2 * a.ng_d * 4);
+                                    const float sgv = md_ldsf(sa), shv = md_ldsf(sa + sr2);
                                     y[0] = fmaf(sgv, dd[0], y[0]);
                                     y[1] = fmaf(sgv, dd[1], y[1]);
                                     y[2] = fmaf(shv, dd[2], y[2]);
@@ -762,18 +817,19 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                     }
                     if (t == 0) {
                         const bool on = nqB > 0;
-                        rw[T * 16 + g] = on ? fmaf(y[1], 0x1p-11f, y[0]) * unB : 0.f;
-                        rw[T * 16 + g + 8] = on ? fmaf(y[3], 0x1p-11f, y[2]) * unB : 0.f;
+                        rw[4 * T * kMdRedB] = on ? fmaf(y[1], 0x1p-11f, y[0]) * unB : 0.f;
+                        rw[(4 * T + 2) * kMdRedB] = on ? fmaf(y[3], 0x1p-11f, y[2]) * unB : 0.f;
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&redfull[s]);
                 i++;
             }
-        } else if (live) {
+        }
+        if (live && rb1 <= rb0) {
             // no phase-B rows: pass the end marker
             const int s = i % kMdSlots;
-            if (md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag)) {
+            if (md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag, kMdNapC)) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
@@ -790,11 +846,11 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                 }
             }
         }
-        // the last CTA out zeroes the call's counters for the next call
+        // the last CTA out zeroes the block counts and moves the tag on for the next call
         if (tid == 0) {
             __threadfence();
             if (atomicAdd(exitc, 1u) == gridDim.x - 1) {
-                for (int e = 0; e < a.K; e++) ready[e] = 0u;
+                *(a.ctr + 3) += 1u;   // the next call's tag
                 for (int b = 0; b < (a.H + 63) / 64; b++) blkc[b] = 0u;
                 *exitc = 0u;
                 __threadfence();
@@ -848,7 +904,7 @@ bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int n
     const size_t ssB = grouped ? (size_t)kMdBlockRows * ng_d * 4 + 16 : 0;
     const size_t SB = round_up(std::max(soA + 4 * ssA, soB + 4 * ssB), 128);
     const size_t off_red = kMdSlots * SB;
-    const size_t red_bytes = (size_t)kMdSlots * kMdWarps * kMdStageRows * 4;
+    const size_t red_bytes = (size_t)kMdSlots * kMdRedSlot * 4;
     const size_t off_bar = off_red + red_bytes;
     const size_t total = off_bar + kMdSlots * 16 + 3 * kMdSlots * 8 + 128;   // + alignment slack
     // static shared memory of the kernel: about 15 KB
@@ -881,10 +937,11 @@ bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int n
     return true;
 }
 
-// Scratch of one call: h [K][F] and the experts' down outputs part [K][H], floats.
-size_t md_scratch_bytes(const MdArgs &a) { return (size_t)a.K * ((size_t)a.F + a.H) * 4; }
-// Counter words of one call (zero between calls).
-size_t md_counter_words() { return kMdCtrBlocks + kMdMaxBlocks; }
+// Scratch of one call: the experts' down outputs part [K][H], floats.
+size_t md_scratch_bytes(const MdArgs &a) { return (size_t)a.K * a.H * 4; }
+// State words of the kernel (zero before its first call): counters, epoch and
+// the tagged h [K][F].
+size_t md_counter_words(const MdArgs &a) { return kMdCtrH + 2 * (size_t)a.K * a.F; }
 
 // The kernel instance of a plan: fmt and group shift.
 template <class Fn>

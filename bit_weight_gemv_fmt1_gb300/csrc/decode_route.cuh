@@ -23,64 +23,71 @@ struct DecodeRouting {
     int nact, bad;
 };
 
+// Phase 0 by one warp, for n <= 32 slots: the lanes rank the slots with
+// shuffles and ballots.  Ids outside [-1, n_experts) set r.bad.  The results
+// are in shared memory once the warp has passed a barrier with the readers.
+__device__ __forceinline__ void decode_route_warp(DecodeRouting &r, const int32_t *ids, const float *w, int n,
+                                                  int n_experts, const ExpertDesc *table) {
+    const int lane = threadIdx.x & 31;
+    const bool valid = lane < n;
+    int my_id = -1;
+    float my_w = 0.f;
+    if (valid) {
+        my_id = ids[lane];
+        my_w = w[lane];
+    }
+    const bool bad = valid && (my_id < -1 || my_id >= n_experts);
+    // the slot's expert pointers are fetched while the ranks are formed
+    const uint8_t *eq[3] = {nullptr, nullptr, nullptr};
+    const float *es[3] = {nullptr, nullptr, nullptr};
+    if (valid && !bad && my_id >= 0) {
+        const ExpertDesc &E = table[my_id];
+#pragma unroll
+        for (int m = 0; m < 3; m++) {
+            eq[m] = E.m[m].q;
+            es[m] = E.m[m].s;
+        }
+    }
+    const unsigned any_bad = __ballot_sync(0xffffffffu, bad);
+    bool first = valid && my_id >= 0;
+    int rank = 0;
+    float wsum = 0.f;
+    for (int t = 0; t < n; t++) {
+        const int f = __shfl_sync(0xffffffffu, my_id, t);
+        const float wt = __shfl_sync(0xffffffffu, my_w, t);
+        if (f == my_id) {
+            wsum += wt;
+            if (t < lane) first = false;
+        }
+        // count each smaller id once, at its first slot
+        const unsigned same_before = __ballot_sync(0xffffffffu, lane < t && my_id == f);
+        if (f >= 0 && f < my_id && same_before == 0u) rank++;
+    }
+    if (first && !any_bad) {
+        r.exp[rank] = my_id;
+        r.ew[rank] = wsum;
+#pragma unroll
+        for (int m = 0; m < 3; m++) {
+            r.q[rank][m] = eq[m];
+            r.s[rank][m] = es[m];
+        }
+    }
+    const unsigned nf = __popc(__ballot_sync(0xffffffffu, first));
+    if (lane == 0) {
+        r.bad = any_bad != 0u;
+        r.nact = (int)nf;
+    }
+}
+
 // Phase 0, called by every thread of the CTA (it contains __syncthreads).
-// For n <= 32 slots warp `rw` ranks the slots with shuffles and ballots while
-// the rest of the CTA goes on; above that the first n threads rank through
-// shared memory.  Ids outside [-1, n_experts) set r.bad.
+// For n <= 32 slots warp `rw` ranks the slots (decode_route_warp) while the
+// rest of the CTA waits; above that the first n threads rank through shared
+// memory.  Ids outside [-1, n_experts) set r.bad.
 __device__ __forceinline__ void decode_route(DecodeRouting &r, const int32_t *ids, const float *w, int n,
                                              int n_experts, const ExpertDesc *table, int rw) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     if (n <= 32) {
-        if (warp == rw) {
-            const bool valid = lane < n;
-            int my_id = -1;
-            float my_w = 0.f;
-            if (valid) {
-                my_id = ids[lane];
-                my_w = w[lane];
-            }
-            const bool bad = valid && (my_id < -1 || my_id >= n_experts);
-            // the slot's expert pointers are fetched while the ranks are formed
-            const uint8_t *eq[3] = {nullptr, nullptr, nullptr};
-            const float *es[3] = {nullptr, nullptr, nullptr};
-            if (valid && !bad && my_id >= 0) {
-                const ExpertDesc &E = table[my_id];
-#pragma unroll
-                for (int m = 0; m < 3; m++) {
-                    eq[m] = E.m[m].q;
-                    es[m] = E.m[m].s;
-                }
-            }
-            const unsigned any_bad = __ballot_sync(0xffffffffu, bad);
-            bool first = valid && my_id >= 0;
-            int rank = 0;
-            float wsum = 0.f;
-            for (int t = 0; t < n; t++) {
-                const int f = __shfl_sync(0xffffffffu, my_id, t);
-                const float wt = __shfl_sync(0xffffffffu, my_w, t);
-                if (f == my_id) {
-                    wsum += wt;
-                    if (t < lane) first = false;
-                }
-                // count each smaller id once, at its first slot
-                const unsigned same_before = __ballot_sync(0xffffffffu, lane < t && my_id == f);
-                if (f >= 0 && f < my_id && same_before == 0u) rank++;
-            }
-            if (first && !any_bad) {
-                r.exp[rank] = my_id;
-                r.ew[rank] = wsum;
-#pragma unroll
-                for (int m = 0; m < 3; m++) {
-                    r.q[rank][m] = eq[m];
-                    r.s[rank][m] = es[m];
-                }
-            }
-            const unsigned nf = __popc(__ballot_sync(0xffffffffu, first));
-            if (lane == 0) {
-                r.bad = any_bad != 0u;
-                r.nact = (int)nf;
-            }
-        }
+        if (warp == rw) decode_route_warp(r, ids, w, n, n_experts, table);
         __syncthreads();
         return;
     }
