@@ -814,8 +814,6 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         if (ok && md_plan(fmt, (int)H, (int)F, K, (int)g0->rs, (int)d0->rs, g0->ng, d0->ng, gs_gu, gs_d, ds->n_sm,
                           (size_t)ds->smem_optin, &a, &smem) &&
             md_occupancy(a, smem, &per_sm) == cudaSuccess && per_sm >= 1) {
-            Workspace *ws = nullptr;
-            if (int rc = workspace(ds, st, md_scratch_bytes(a), &ws)) return rc;
             unsigned *ctr = nullptr;
             if (int rc = decode_counters(ds, st, md_counter_words(a), &ctr)) return rc;
             a.x = x;
@@ -824,7 +822,6 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
             a.y = y;
             a.table = table;
             a.n_experts = n_experts;
-            a.part = (float *)ws->buf;
             a.ctr = ctr;
             a.err = ds->err;
             a.timeout_ns = 2000000000LL;

@@ -676,7 +676,6 @@ struct MdArgs {
     int bsB, ssB, soB;         // phase-B stage
     int slot_bytes;
     int off_red, off_bar;      // dynamic shared-memory layout (bytes)
-    float *part;               // [K][H] scratch: each routed expert's down output
     unsigned *ctr;             // kernel state, zero before the first call (md_counter_words)
     int *err;                  // device error word
     long long timeout_ns;      // bound of every wait
@@ -684,7 +683,6 @@ struct MdArgs {
 bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int ng_d, int gs_gu, int gs_d, int n_sm,
              size_t smem_max, MdArgs *a, size_t *smem);
 cudaError_t md_occupancy(const MdArgs &a, size_t smem, int *per_sm);
-size_t md_scratch_bytes(const MdArgs &a);
 size_t md_counter_words(const MdArgs &a);
 cudaError_t launch_decode_mma(const MdArgs &a, int grid, size_t smem, cudaStream_t st);
 

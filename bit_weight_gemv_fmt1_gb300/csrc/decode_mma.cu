@@ -49,13 +49,13 @@
 //            barrier: a 64-bit store is seen whole), builds their B fragments
 //            once and streams the CTA's rows in stages of 48; warp 17 sums the
 //            warps' shares of each row in warp order into part[a][o].
-//   y:       the CTA whose rows complete a 64-row block of y (counted with
-//            atomics after a fence) sums part over the routed experts in
-//            order, with their routing weights: y[o] is written once.
+//            The sums go out as tagged 64-bit words too.
+//   y:       CTA c sums the 64-row blocks c, c + G, ... of y over the routed
+//            experts in order, with their routing weights, once every part
+//            value of the block carries the call's tag: y[o] is written once.
 // Results do not depend on timing or on the number of SMs.  Every wait is
 // bounded (mbarrier.cuh); on expiry the kernel records DEV_ERR_TIMEOUT and
-// returns.  The last CTA to leave clears the block counts and moves the tag
-// on for the next call.
+// returns.  The last CTA to leave moves the tag on for the next call.
 #include <algorithm>
 #include <cstring>
 
@@ -76,16 +76,14 @@ constexpr int kMdSegMax = 6;     // 64-input segments per warp and row (H, F <= 
 constexpr int kMdTiles = 3;                   // 16-row mma tiles of a phase-B stage
 constexpr int kMdBlockRows = 4 * kMdTiles;     // rows of each of a phase-B stage's four blocks
 constexpr int kMdStageRows = 4 * kMdBlockRows; // down rows of a phase-B stage (48)
-constexpr int kMdMaxBlocks = 128;              // 64-row blocks of y (H <= 8192)
 // partial sums of a stage: phase A [warp][48] (16 rows used), phase B
 // [row][20] (16 warps, padded so that a lane's row is one conflict-free
 // 128-bit load per 4 warps)
 constexpr int kMdRedB = 20;
 constexpr int kMdRedSlot = kMdStageRows * kMdRedB;
-// state words of a call (zero before the first call): [1] CTAs out, [3] epoch,
-// [4 ..) 64-row block counts of y, then the tagged h [K][F] (8 bytes each)
-constexpr int kMdCtrBlocks = 4;
-constexpr int kMdCtrH = kMdCtrBlocks + kMdMaxBlocks;
+// state words of the kernel (zero before the first call): [1] CTAs out,
+// [3] epoch, then the tagged h [K][F] and part [K][H] (8 bytes each)
+constexpr int kMdCtrH = 4;
 
 enum : int { MD_A = 0, MD_B = 1, MD_END = 2 };
 
@@ -322,9 +320,10 @@ __device__ __forceinline__ void md_tileA(float (&y)[4], uint32_t cq, uint32_t rs
 
 // The CTAs that own routed expert e in the down phase: [cb(e), cb(e + 1))
 // with cb(e) = ceil(e G / nact).  eB: the expert of CTA c, [cb0, cb1) its CTAs.
+// (32-bit arithmetic: G <= 1024 CTAs and nact <= 64, so the products fit.)
 __device__ __forceinline__ void md_owner(int c, int nact, int G, int *eB, int *cb0, int *cb1) {
-    auto cb = [&](int e) -> int { return (int)(((long long)e * G + nact - 1) / nact); };
-    int e = (int)(((long long)c * nact) / G);
+    auto cb = [&](int e) -> int { return (e * G + nact - 1) / nact; };
+    int e = c * nact / G;
     while (e > 0 && cb(e) > c) e--;
     while (e + 1 < nact && cb(e + 1) <= c) e++;
     *eB = e;
@@ -410,16 +409,15 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     __shared__ volatile int abort_flag;
     __shared__ float4 s_cf[kMdWarps][kMdSegMax + 1];   // phase-A chain starts of each warp's segments, their sum
     __shared__ __align__(16) uint8_t s_stg[kMdWarps][528];   // B-fragment staging of each consumer warp, + a zero row
-    __shared__ int s_done[kMdMaxBlocks];                     // output blocks this CTA completes
-    __shared__ int s_ndone;
+    __shared__ float s_part[kMdWarps * 32];                  // the final sum: one (expert, row) per thread
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int SB = a.slot_bytes;
     const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
     unsigned *exitc = a.ctr + 1;
-    unsigned *blkc = a.ctr + kMdCtrBlocks;   // [64-row block of y]: expert rows summed into part
     // h values carry the call's tag in their high word: a 64-bit store is seen
     // whole or not at all, so a reader knows a value is this call's without a fence
     unsigned long long *htag = reinterpret_cast<unsigned long long *>(a.ctr + kMdCtrH);
+    unsigned long long *ptag = htag + (size_t)a.K * a.F;
     const unsigned tag = *(volatile unsigned *)(a.ctr + 3) + 1u;
 
     // consumers load their x values now; the fragments are built after routing
@@ -435,7 +433,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     // phase-A fragments meanwhile), else by the whole CTA
     auto md_init = [&]() {
         abort_flag = 0;
-        s_ndone = 0;
         for (int i = 0; i < kMdSlots; i++) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kMdWarps);
@@ -480,18 +477,19 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
         if (lane == 0) s_cf[warp][kMdSegMax] = cft;
         __syncwarp();
     }
-    // the routing and the shared state are visible to every warp after this
-    // barrier; the producer passes it without waiting
-    if (warp == kMdWarps)
-        asm volatile("bar.arrive 5, %0;" ::"r"(kMdThreads) : "memory");
-    else
-        named_sync(5, kMdThreads);
+    // the routing and the shared state are visible to every warp after barrier
+    // 5; the producer passes it without waiting, once it has issued the first
+    // stage (the other warps wait in the barrier, not spinning on the stage)
+    auto release_others = [&]() { asm volatile("bar.arrive 5, %0;" ::"r"(kMdThreads) : "memory"); };
+    if (warp != kMdWarps) named_sync(5, kMdThreads);
     if (rt.bad) {
+        if (warp == kMdWarps) release_others();
         if (blockIdx.x == 0 && tid == 0) atomicCAS(a.err, 0, DEV_ERR_BAD_ID);
         return;
     }
     const int nact = rt.nact;
     if (nact == 0) {   // no routed expert: y = 0
+        if (warp == kMdWarps) release_others();
         const int rpc = (a.H + gridDim.x - 1) / gridDim.x;
         for (int r = tid; r < rpc; r += kMdThreads)
             if ((int)blockIdx.x * rpc + r < a.H) a.y[blockIdx.x * rpc + r] = 0.f;
@@ -504,88 +502,95 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     md_owner(blockIdx.x, nact, G, &eB, &cb0, &cb1);
     // whole 48-row stages of the expert's rows, split evenly among its CTAs
     const int nsE = (a.H + kMdStageRows - 1) / kMdStageRows, kB = blockIdx.x - cb0, nB_ = cb1 - cb0;
-    const int rb0 = min(a.H, kMdStageRows * (int)((long long)nsE * kB / nB_));
-    const int rb1 = min(a.H, kMdStageRows * (int)((long long)nsE * (kB + 1) / nB_));
+    const int rb0 = min(a.H, kMdStageRows * (nsE * kB / nB_));
+    const int rb1 = min(a.H, kMdStageRows * (nsE * (kB + 1) / nB_));
 
     if (warp == kMdWarps) {
         // ---------------- producer: lane 0 issues every stage of the CTA.  Phase-A
         // units are dealt round robin, the last routed expert's first, so that
         // the final round (a partial one) belongs to expert 0
-        if (lane == 0) {
-            const int spe = (a.F + 7) / 8;   // phase-A stages per routed expert
-            const unsigned totalA = (unsigned)(nact * spe);
-            const int nB = (rb1 - rb0 + kMdStageRows - 1) / kMdStageRows;
-            const int rsA = a.rs_gu, rsB = a.rs_d;
-            unsigned idx = blockIdx.x;
-            int jB = 0, i = 0;
-            while (true) {
-                const int s = i % kMdSlots;
-                // the first stage is copied alone (its bytes are then not interleaved
-                // with the next stages'), so that the consumers can start early
-                if (i == 1) {
-                    volatile int no_abort = 0;
-                    mbar_wait(&full[0], 0, global_ns() + 4000, &no_abort);
-                }
-                if (i >= kMdSlots && !md_wait1(&empty[s], ((i / kMdSlots) & 1) ^ 1, deadline, &abort_flag, kMdNapP)) {
-                    if (!abort_flag) {
-                        abort_flag = 1;
-                        atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
-                    }
-                    break;
-                }
-                uint8_t *dst = base + (size_t)s * SB;
-                if (idx < totalA) {
-                    const int ai = nact - 1 - (int)(idx / spe), j0 = (int)(idx % spe) * 8;
-                    const int w = min(8, a.F - j0);
-                    desc[s] = make_int4(MD_A, ai, j0, w);
-                    uint32_t tx = 0;
-                    int cnt[4];
-#pragma unroll
-                    for (int b = 0; b < 4; b++) {
-                        cnt[b] = max(0, min(4, w - 4 * (b & 1)));
-                        tx += (uint32_t)cnt[b] * (uint32_t)(rsA + (GROUPED ? 4 * a.ng_gu : 0));
-                    }
-                    mbar_expect_tx(&full[s], tx);
-#pragma unroll
-                    for (int b = 0; b < 4; b++) {
-                        if (cnt[b] == 0) continue;
-                        const int pr0 = j0 + 4 * (b & 1), m = b >> 1;
-                        bulk_load(dst + b * (a.bsA + 32), rt.q[ai][m] + (size_t)pr0 * rsA, (uint32_t)(cnt[b] * rsA),
-                                  &full[s]);
-                        if (GROUPED)
-                            bulk_load(dst + a.soA + b * a.ssA, rt.s[ai][m] + (size_t)pr0 * a.ng_gu,
-                                      (uint32_t)(cnt[b] * a.ng_gu * 4), &full[s]);
-                    }
-                    idx += G;
-                } else if (jB < nB) {
-                    const int r0 = rb0 + jB * kMdStageRows, nr = min(kMdStageRows, rb1 - r0);
-                    desc[s] = make_int4(MD_B, eB, r0, nr);
-                    uint32_t tx = 0;
-                    int cnt[4];
-#pragma unroll
-                    for (int b = 0; b < 4; b++) {
-                        cnt[b] = max(0, min(kMdBlockRows, nr - b * kMdBlockRows));
-                        tx += (uint32_t)cnt[b] * (uint32_t)(rsB + (GROUPED ? 4 * a.ng_d : 0));
-                    }
-                    mbar_expect_tx(&full[s], tx);
-#pragma unroll
-                    for (int b = 0; b < 4; b++) {
-                        if (cnt[b] == 0) continue;
-                        const size_t rr = (size_t)r0 + (size_t)b * kMdBlockRows;
-                        bulk_load(dst + b * (a.bsB + 32), rt.q[eB][2] + rr * rsB, (uint32_t)(cnt[b] * rsB), &full[s]);
-                        if (GROUPED)
-                            bulk_load(dst + a.soB + b * a.ssB, rt.s[eB][2] + rr * a.ng_d,
-                                      (uint32_t)(cnt[b] * a.ng_d * 4), &full[s]);
-                    }
-                    jB++;
-                } else {
-                    desc[s] = make_int4(MD_END, 0, 0, 0);
-                    mbar_arrive(&full[s]);   // end marker: no bytes
-                    i++;
-                    break;
-                }
-                i++;
+        const int spe = (a.F + 7) / 8;   // phase-A stages per routed expert
+        const unsigned totalA = (unsigned)(nact * spe);
+        const int nB = (rb1 - rb0 + kMdStageRows - 1) / kMdStageRows;
+        const int rsA = a.rs_gu, rsB = a.rs_d;
+        unsigned idx = blockIdx.x;
+        int jB = 0, i = 0;
+        bool more = true;
+        // stage i into slot i % kMdSlots; false after the end marker or an abort
+        auto issue = [&]() -> bool {
+            const int s = i % kMdSlots;
+            // the first stage is copied alone (its bytes are then not interleaved
+            // with the next stages'), so that the consumers can start early
+            if (i == 1) {
+                volatile int no_abort = 0;
+                mbar_wait(&full[0], 0, global_ns() + 4000, &no_abort);
             }
+            if (i >= kMdSlots && !md_wait1(&empty[s], ((i / kMdSlots) & 1) ^ 1, deadline, &abort_flag, kMdNapP)) {
+                if (!abort_flag) {
+                    abort_flag = 1;
+                    atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+                }
+                return false;
+            }
+            uint8_t *dst = base + (size_t)s * SB;
+            if (idx < totalA) {
+                const int ai = nact - 1 - (int)(idx / spe), j0 = (int)(idx % spe) * 8;
+                const int w = min(8, a.F - j0);
+                desc[s] = make_int4(MD_A, ai, j0, w);
+                uint32_t tx = 0;
+                int cnt[4];
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    cnt[b] = max(0, min(4, w - 4 * (b & 1)));
+                    tx += (uint32_t)cnt[b] * (uint32_t)(rsA + (GROUPED ? 4 * a.ng_gu : 0));
+                }
+                mbar_expect_tx(&full[s], tx);
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    if (cnt[b] == 0) continue;
+                    const int pr0 = j0 + 4 * (b & 1), m = b >> 1;
+                    bulk_load(dst + b * (a.bsA + 32), rt.q[ai][m] + (size_t)pr0 * rsA, (uint32_t)(cnt[b] * rsA),
+                              &full[s]);
+                    if (GROUPED)
+                        bulk_load(dst + a.soA + b * a.ssA, rt.s[ai][m] + (size_t)pr0 * a.ng_gu,
+                                  (uint32_t)(cnt[b] * a.ng_gu * 4), &full[s]);
+                }
+                idx += G;
+            } else if (jB < nB) {
+                const int r0 = rb0 + jB * kMdStageRows, nr = min(kMdStageRows, rb1 - r0);
+                desc[s] = make_int4(MD_B, eB, r0, nr);
+                uint32_t tx = 0;
+                int cnt[4];
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    cnt[b] = max(0, min(kMdBlockRows, nr - b * kMdBlockRows));
+                    tx += (uint32_t)cnt[b] * (uint32_t)(rsB + (GROUPED ? 4 * a.ng_d : 0));
+                }
+                mbar_expect_tx(&full[s], tx);
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    if (cnt[b] == 0) continue;
+                    const size_t rr = (size_t)r0 + (size_t)b * kMdBlockRows;
+                    bulk_load(dst + b * (a.bsB + 32), rt.q[eB][2] + rr * rsB, (uint32_t)(cnt[b] * rsB), &full[s]);
+                    if (GROUPED)
+                        bulk_load(dst + a.soB + b * a.ssB, rt.s[eB][2] + rr * a.ng_d, (uint32_t)(cnt[b] * a.ng_d * 4),
+                                  &full[s]);
+                }
+                jB++;
+            } else {
+                desc[s] = make_int4(MD_END, 0, 0, 0);
+                mbar_arrive(&full[s]);   // end marker: no bytes
+                i++;
+                return false;
+            }
+            i++;
+            return true;
+        };
+        if (lane == 0) more = issue();
+        __syncwarp();
+        release_others();
+        if (lane == 0) {
+            while (more) more = issue();
             // every copy issued has landed before the CTA may exit
             const uint64_t dl2 = global_ns() + 200000000ull;
             volatile int no_abort = 0;
@@ -665,7 +670,10 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                     const int rr = lane + 32 * h;
                     if (rr < d.w) {
                         if (!GROUPED) v[h] *= __ldg(rt.s[d.y][2] + d.z + rr);
-                        a.part[(size_t)d.y * a.H + d.z + rr] = v[h];
+                        const unsigned long long pv = ((unsigned long long)tag << 32) | __float_as_uint(v[h]);
+                        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(ptag + (size_t)d.y * a.H + d.z + rr),
+                                     "l"(pv)
+                                     : "memory");
                     }
                 }
             }
@@ -674,19 +682,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
         if (!ok && lane == 0 && !abort_flag) {
             abort_flag = 1;
             atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
-        }
-        // the CTA's expert rows are in part: count them into their 64-row blocks of
-        // y; the CTA that completes a block sums it (below)
-        if (ok && rb1 > rb0) {
-            __threadfence();
-            __syncwarp();
-            for (int blk = rb0 / 64 + lane; blk * 64 < rb1; blk += 32) {
-                const int lo = max(rb0, blk * 64), hi = min(rb1, blk * 64 + 64);
-                const unsigned need = (unsigned)nact * (unsigned)(min(a.H, blk * 64 + 64) - blk * 64);
-                if (atomicAdd(&blkc[blk], (unsigned)(hi - lo)) + (unsigned)(hi - lo) == need)
-                    s_done[atomicAdd(&s_ndone, 1)] = blk;
-            }
-            __threadfence();
         }
         named_sync(2, (kMdWarps + 1) * 32);
     } else {
@@ -835,23 +830,51 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             }
         }
         named_sync(2, (kMdWarps + 1) * 32);
-        // y of the blocks this CTA completed: sum over the routed experts in order
-        if (!abort_flag) {
-            for (int k = tid; k < s_ndone * 64; k += kMdWarps * 32) {
-                const int row = s_done[k >> 6] * 64 + (k & 63);
-                if (row < a.H) {
-                    float v = 0.f;
-                    for (int e = 0; e < nact; e++) v = fmaf(rt.ew[e], __ldcg(a.part + (size_t)e * a.H + row), v);
-                    a.y[row] = v;
+        // y: CTA c sums the 64-row blocks c, c + G, ...: each thread polls one
+        // (expert, row) of part until it carries the call's tag, then the rows are
+        // summed over the routed experts in order, with their routing weights
+        const int nblk = (a.H + 63) / 64;
+        // (every consumer thread runs the same passes: the named barriers inside
+        // stay matched; an abort only cuts the polling short)
+        for (int blkI = blockIdx.x; blkI < nblk; blkI += G) {
+            const int rows = min(64, a.H - blkI * 64);
+            const int per = kMdWarps * 32 / 64;   // experts per pass
+            float v = 0.f;
+            for (int e0 = 0; e0 < nact; e0 += per) {
+                const int e = e0 + (tid >> 6), row = blkI * 64 + (tid & 63);
+                bool okp = true;
+                if (e < nact && (tid & 63) < rows) {
+                    const unsigned long long *pp = ptag + (size_t)e * a.H + row;
+                    while (true) {
+                        unsigned long long w;
+                        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(pp) : "memory");
+                        if ((unsigned)(w >> 32) == tag) {
+                            s_part[tid] = __uint_as_float((unsigned)w);
+                            break;
+                        }
+                        if (abort_flag || global_ns() > deadline) {
+                            okp = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
                 }
+                if (!okp && !abort_flag) {
+                    abort_flag = 1;
+                    atomicCAS(a.err, 0, DEV_ERR_TIMEOUT);
+                }
+                named_sync(3, kMdWarps * 32);
+                if (tid < rows)
+                    for (int k = 0; k < per && e0 + k < nact; k++) v = fmaf(rt.ew[e0 + k], s_part[k * 64 + tid], v);
+                named_sync(3, kMdWarps * 32);
             }
+            if (tid < rows && !abort_flag) a.y[blkI * 64 + tid] = v;
         }
-        // the last CTA out zeroes the block counts and moves the tag on for the next call
+        // the last CTA out moves the tag on for the next call
         if (tid == 0) {
             __threadfence();
             if (atomicAdd(exitc, 1u) == gridDim.x - 1) {
-                *(a.ctr + 3) += 1u;   // the next call's tag
-                for (int b = 0; b < (a.H + 63) / 64; b++) blkc[b] = 0u;
+                *(a.ctr + 3) += 1u;
                 *exitc = 0u;
                 __threadfence();
             }
@@ -894,7 +917,7 @@ bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int n
     const int spwB = ((nsegB + kMdWarps - 1) / kMdWarps + gm - 1) / gm * gm;
     if (spwA > kMdSegMax || spwB > kMdSegMax) return false;
     // phase B: every routed expert has CTAs of its own (at most K experts)
-    if (n_sm < K || spwB > 2 || (H + 63) / 64 > kMdMaxBlocks) return false;
+    if (n_sm < K || spwB > 2) return false;
     // slot layouts: four code blocks 32 bytes apart modulo 128 (each followed
     // by room for the 32-byte read past a row's last segment), then four
     // scale blocks 16 bytes apart modulo 128
@@ -937,11 +960,10 @@ bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int n
     return true;
 }
 
-// Scratch of one call: the experts' down outputs part [K][H], floats.
-size_t md_scratch_bytes(const MdArgs &a) { return (size_t)a.K * a.H * 4; }
+
 // State words of the kernel (zero before its first call): counters, epoch and
 // the tagged h [K][F].
-size_t md_counter_words(const MdArgs &a) { return kMdCtrH + 2 * (size_t)a.K * a.F; }
+size_t md_counter_words(const MdArgs &a) { return kMdCtrH + 2 * (size_t)a.K * ((size_t)a.F + a.H); }
 
 // The kernel instance of a plan: fmt and group shift.
 template <class Fn>
