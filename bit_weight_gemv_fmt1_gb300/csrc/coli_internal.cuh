@@ -677,6 +677,7 @@ struct MdArgs {
     int slot_bytes;
     int off_red, off_bar;      // dynamic shared-memory layout (bytes)
     unsigned *ctr;             // kernel state, zero before the first call (md_counter_words)
+    int m0[65];                // [routed experts <= 64]: CTAs of the expert finished last in the down phase
     int *err;                  // device error word
     long long timeout_ns;      // bound of every wait
 };

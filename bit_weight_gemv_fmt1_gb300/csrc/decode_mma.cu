@@ -42,15 +42,16 @@
 //            the slot's partial-sum table and moves on; warp 17 sums the table
 //            in warp order and writes h[a][j] = silu(gate) * up to global
 //            memory, each value as one 64-bit word under the call's tag.
-//   phase B: the CTAs of the grid are split evenly among the routed
-//            experts; a CTA owns a range of whole 48-row stages of its
-//            expert's down rows.  Each warp polls until the h
+//   phase B: each CTA owns one routed expert and a range of whole 48-row
+//            stages of its down rows (md_share: expert 0, whose h is finished
+//            last, gets more CTAs; the others are interleaved so that every
+//            CTA's gate/up units plus down stages come out even).  Each warp polls until the h
 //            values of its segments carry the call's tag (no fence or grid
 //            barrier: a 64-bit store is seen whole), builds their B fragments
 //            once and streams the CTA's rows in stages of 48; warp 17 sums the
 //            warps' shares of each row in warp order into part[a][o].
 //            The sums go out as tagged 64-bit words too.
-//   y:       CTA c sums the 64-row blocks c, c + G, ... of y over the routed
+//   y:       CTA G - 1 - c sums the 64-row blocks c, c + G, ... of y over the routed
 //            experts in order, with their routing weights, once every part
 //            value of the block carries the call's tag: y[o] is written once.
 // Results do not depend on timing or on the number of SMs.  Every wait is
@@ -86,6 +87,7 @@ constexpr int kMdRedSlot = kMdStageRows * kMdRedB;
 constexpr int kMdCtrH = 4;
 
 enum : int { MD_A = 0, MD_B = 1, MD_END = 2 };
+static_assert(kMaxDecodeSlots + 1 <= (int)(sizeof(MdArgs::m0) / sizeof(int)), "MdArgs::m0 covers every routed-expert count");
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 v;
@@ -318,17 +320,60 @@ __device__ __forceinline__ void md_tileA(float (&y)[4], uint32_t cq, uint32_t rs
     }
 }
 
-// The CTAs that own routed expert e in the down phase: [cb(e), cb(e + 1))
-// with cb(e) = ceil(e G / nact).  eB: the expert of CTA c, [cb0, cb1) its CTAs.
-// (32-bit arithmetic: G <= 1024 CTAs and nact <= 64, so the products fit.)
-__device__ __forceinline__ void md_owner(int c, int nact, int G, int *eB, int *cb0, int *cb1) {
-    auto cb = [&](int e) -> int { return (e * G + nact - 1) / nact; };
-    int e = c * nact / G;
-    while (e > 0 && cb(e) > c) e--;
-    while (e + 1 < nact && cb(e + 1) <= c) e++;
+// Stages [s0, s1) of member j of a group of M CTAs that split nsE stages,
+// where members j < Hh carry q + 1 gate/up units and the others q: units +
+// stages come out T or T + 1 for every member, the + 1 going to members with
+// fewer units first; when the stages are too few for that, an even split.
+__device__ __forceinline__ void md_split(int j, int M, int Hh, int q, int nsE, int *s0, int *s1) {
+    const int Lt = M * q + Hh + nsE;
+    const int T = Lt / M, r = Lt % M;
+    if (T < q + 1) {
+        *s0 = nsE * j / M;
+        *s1 = nsE * (j + 1) / M;
+        return;
+    }
+    const int light = M - Hh;
+    auto plus_before = [&](int jj) -> int {   // + 1s among members 0 .. jj - 1
+        if (r <= light) return min(max(jj - Hh, 0), r);
+        return max(jj - Hh, 0) + min(jj, r - light);
+    };
+    auto units_before = [&](int jj) -> int { return jj * q + min(jj, Hh); };
+    *s0 = j * T - units_before(j) + plus_before(j);
+    *s1 = (j + 1) * T - units_before(j + 1) + plus_before(j + 1);
+}
+
+// The down-phase share of CTA c: its routed expert eB and the stages [s0, s1)
+// of that expert's nsE stages of 48 down rows.  Gate/up units are dealt round
+// robin (CTA c gets q + 1 of them for c < rA, else q), the last routed
+// expert's first, so expert 0's h is finished last: at the end of the final
+// (partial) round, and it reaches its owners about one unit's time later.
+// Expert 0 therefore gets the first M0 CTAs (those with q + 1 units, busy to
+// the end anyway), M0 = md_m0(...) computed with the plan, so that its owners
+// (starting at q + 2 units, even split) and the others (interleaved over CTAs
+// M0 .. G - 1, md_split) finish together; with one routed expert every CTA
+// owns it (md_split).
+// (32-bit arithmetic: G <= 1024 CTAs, nact <= 64, fewer than 2^20 units.)
+__device__ __forceinline__ void md_share(int c, int nact, int G, int totalA, int nsE, int M0, int *eB, int *s0,
+                                         int *s1) {
+    const int q = totalA / G, rA = totalA % G;
+    if (nact == 1) {
+        *eB = 0;
+        md_split(c, G, rA, q, nsE, s0, s1);
+        return;
+    }
+    const int no = nact - 1;
+    if (c < M0) {
+        *eB = 0;
+        *s0 = nsE * c / M0;
+        *s1 = nsE * (c + 1) / M0;
+        return;
+    }
+    const int cc = c - M0, e = 1 + cc % no, j = cc / no;
+    const int base = M0 + (e - 1);                           // the group's member j is CTA base + j no
+    const int M = (G - base + no - 1) / no;
+    const int Hh = rA > base ? min(M, (rA - base + no - 1) / no) : 0;
     *eB = e;
-    *cb0 = cb(e);
-    *cb1 = cb(e + 1);
+    md_split(j, M, Hh, q, nsE, s0, s1);
 }
 
 // The h values lane `lane` of a phase-B warp needs (inputs 64 q0 + 4 lane +
@@ -498,18 +543,16 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     // phase B: this CTA's routed expert eB (the CTAs of an expert split its
     // down rows evenly) and its rows [rb0, rb1)
     const int G = gridDim.x;
-    int eB = 0, cb0 = 0, cb1 = G;
-    md_owner(blockIdx.x, nact, G, &eB, &cb0, &cb1);
-    // whole 48-row stages of the expert's rows, split evenly among its CTAs
-    const int nsE = (a.H + kMdStageRows - 1) / kMdStageRows, kB = blockIdx.x - cb0, nB_ = cb1 - cb0;
-    const int rb0 = min(a.H, kMdStageRows * (nsE * kB / nB_));
-    const int rb1 = min(a.H, kMdStageRows * (nsE * (kB + 1) / nB_));
+    const int spe = (a.F + 7) / 8;   // phase-A stages per routed expert
+    const int nsE = (a.H + kMdStageRows - 1) / kMdStageRows;   // 48-row stages of a down matrix
+    int eB = 0, sB0 = 0, sB1 = 0;
+    md_share(blockIdx.x, nact, G, nact * spe, nsE, a.m0[nact], &eB, &sB0, &sB1);
+    const int rb0 = min(a.H, kMdStageRows * sB0), rb1 = min(a.H, kMdStageRows * sB1);
 
     if (warp == kMdWarps) {
         // ---------------- producer: lane 0 issues every stage of the CTA.  Phase-A
         // units are dealt round robin, the last routed expert's first, so that
         // the final round (a partial one) belongs to expert 0
-        const int spe = (a.F + 7) / 8;   // phase-A stages per routed expert
         const unsigned totalA = (unsigned)(nact * spe);
         const int nB = (rb1 - rb0 + kMdStageRows - 1) / kMdStageRows;
         const int rsA = a.rs_gu, rsB = a.rs_d;
@@ -830,13 +873,14 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             }
         }
         named_sync(2, (kMdWarps + 1) * 32);
-        // y: CTA c sums the 64-row blocks c, c + G, ...: each thread polls one
+        // y: CTA G - 1 - c sums the 64-row blocks c, c + G, ... (the CTAs at the end
+        // of the grid have one gate/up unit fewer): each thread polls one
         // (expert, row) of part until it carries the call's tag, then the rows are
         // summed over the routed experts in order, with their routing weights
         const int nblk = (a.H + 63) / 64;
         // (every consumer thread runs the same passes: the named barriers inside
         // stay matched; an abort only cuts the polling short)
-        for (int blkI = blockIdx.x; blkI < nblk; blkI += G) {
+        for (int blkI = G - 1 - (int)blockIdx.x; blkI < nblk; blkI += G) {
             const int rows = min(64, a.H - blkI * 64);
             const int per = kMdWarps * 32 / 64;   // experts per pass
             float v = 0.f;
@@ -933,6 +977,29 @@ bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int n
     // static shared memory of the kernel: about 15 KB
     if (total + 16 * 1024 > smem_max || SB > (1u << 30)) return false;
     memset(a, 0, sizeof *a);
+    // CTAs of the expert finished last (md_share), for each possible number of
+    // routed experts: the balance of expert 0's owners, which start at q + 2
+    // units, against the others' units and stages
+    {
+        const int spe = (F + 7) / 8, nsE = (H + kMdStageRows - 1) / kMdStageRows, G = n_sm;
+        for (int nact = 2; nact <= K; nact++) {
+            const int totalA = nact * spe, q = totalA / G, rA = totalA % G, no = nact - 1;
+            const long long start0 = q + (rA > 0 ? 1 : 0) + 1;
+            int M0 = 1;
+            long long best = -1;
+            for (int m = 1; m <= G - no; m++) {
+                const long long Ao = (long long)(G - m) * q + std::max(rA - m, 0);
+                const long long lhs = start0 * m * (G - m) + (long long)nsE * (G - m);
+                const long long rhs = Ao * m + (long long)no * nsE * m;
+                const long long d = lhs > rhs ? lhs - rhs : rhs - lhs;
+                if (best < 0 || d < best) {
+                    best = d;
+                    M0 = m;
+                }
+            }
+            a->m0[nact] = M0;
+        }
+    }
     a->K = K;
     a->H = H;
     a->F = F;
