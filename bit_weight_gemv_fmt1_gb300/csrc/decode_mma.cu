@@ -562,12 +562,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
         // stage i into slot i % kMdSlots; false after the end marker or an abort
         auto issue = [&]() -> bool {
             const int s = i % kMdSlots;
-            // the first stage is copied alone (its bytes are then not interleaved
-            // with the next stages'), so that the consumers can start early
-            if (i == 1) {
-                volatile int no_abort = 0;
-                mbar_wait(&full[0], 0, global_ns() + 4000, &no_abort);
-            }
             if (i >= kMdSlots && !md_wait1(&empty[s], ((i / kMdSlots) & 1) ^ 1, deadline, &abort_flag, kMdNapP)) {
                 if (!abort_flag) {
                     abort_flag = 1;
