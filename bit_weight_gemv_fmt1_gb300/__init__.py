@@ -54,6 +54,10 @@ _lib.coli_matmul_rows_t.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _int,
 _lib.coli_moe_route.argtypes = [_vp, _int, _int, _int, _vp, _vp, _vp]
 _lib.coli_moe_block.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp]
 _lib.coli_moe_block_noalloc.argtypes = [_vp, _int, ctypes.POINTER(_Expert), _int, _vp, _vp, _int, _vp, _vp, _vp]
+_lib.coli_expert_table_create.argtypes = [ctypes.POINTER(_Expert), _int, ctypes.POINTER(_vp)]
+_lib.coli_expert_table_free.argtypes = [_vp]
+_lib.coli_expert_table_free.restype = None
+_lib.coli_moe_block_t.argtypes = [_vp, _int, _vp, _vp, _vp, _int, _vp, _vp]
 _lib.coli_moe_topk.argtypes = [_vp, _vp, _int, _int, _int, ctypes.c_float, _int, ctypes.c_float, _vp, _vp, _vp]
 _lib.coli_moe_router.argtypes = [_vp, _int, _vp, _vp, _int, ctypes.c_float, _int, ctypes.c_float, _vp, _vp, _vp]
 _lib.coli_sync_check.argtypes = [_vp]
@@ -66,6 +70,7 @@ _lib.coli_set_fail_after.restype = None
 EXPORTS = ("coli_tensor_upload", "coli_tensor_upload_host", "coli_tensor_free", "coli_tensor_info", "coli_matmul", "coli_matmul_multi",
            "coli_matmul_rows", "coli_matmul_rows_t",
            "coli_moe_route", "coli_moe_topk", "coli_moe_router", "coli_moe_block", "coli_moe_block_noalloc",
+           "coli_expert_table_create", "coli_expert_table_free", "coli_moe_block_t",
            "coli_sync_check", "coli_last_error", "coli_get_stats", "coli_reset_stats", "coli_set_fail_after",
            "coli_version")
 
@@ -210,18 +215,42 @@ def moe_router(x, router: Tensor, K: int, ids, w, bias=None, top_p: float = 0.0,
 
 
 class ExpertTable:
-    """Host array of coli_expert descriptors (keeps the tensors alive)."""
+    """An expert table: the host array of coli_expert descriptors (keeps the
+    tensors alive) and, from the first block call on, the library's checked
+    device copy (coli_expert_table_create), freed with the object."""
 
     def __init__(self, experts):
         self.experts = list(experts)
         self.arr = (_Expert * len(self.experts))(*[_Expert(g.handle, u.handle, d.handle)
                                                    for (g, u, d) in self.experts])
+        self._t = None
 
     def __len__(self):
         return len(self.experts)
 
+    def handle(self) -> int:
+        if self._t is None:
+            h = _vp()
+            _check(_lib.coli_expert_table_create(self.arr, len(self.experts), ctypes.byref(h)))
+            self._t = h.value
+        return self._t
+
+    def __del__(self):
+        if getattr(self, "_t", None):
+            _lib.coli_expert_table_free(self._t)
+            self._t = None
+
 
 def moe_block(x, table: ExpertTable, ids, w, y, stream=None):
+    """coli_moe_block_t on the table's device copy."""
+    S, K = ids.shape
+    _check(_lib.coli_moe_block_t(_ptr(x), int(S), table.handle(), _ptr(ids), _ptr(w), int(K), _ptr(y),
+                                 _stream(stream)))
+    return y
+
+
+def moe_block_array(x, table: ExpertTable, ids, w, y, stream=None):
+    """coli_moe_block on the host array (the table is checked on every call)."""
     S, K = ids.shape
     _check(_lib.coli_moe_block(_ptr(x), int(S), table.arr, len(table), _ptr(ids), _ptr(w), int(K), _ptr(y),
                                _stream(stream)))

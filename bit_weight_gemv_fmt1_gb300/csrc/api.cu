@@ -222,6 +222,9 @@ MatDesc desc_of(const coli_tensor *t) {
 namespace coli {
 // Record `msg` as this thread's last error (for coli_last_error) and return code.
 int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+void clear_last_error() { g_msg[0] = 0; }
+int injected_gate() { return injected(); }
+void count_call(int launches, uint64_t weight_bytes) { count(launches, weight_bytes); }
 }  // namespace coli
 
 // =================================================================== ABI
@@ -751,6 +754,79 @@ static int expert_table(DeviceState *ds, const coli_expert *ex, int n, cudaStrea
     return COLI_OK;
 }
 
+// What the expert block's dispatch needs to know about an expert table,
+// found in one pass over it (coli_moe_block: on every call;
+// coli_expert_table_create: once).
+struct MoeInfo {
+    int n, fmt, device;
+    int64_t H, F;
+    const coli_tensor *g0, *d0;   // expert 0's gate and down: the shapes and gs of every expert's
+    bool host_any;                // some matrix lives in pinned host memory
+    bool gs_ok;                   // fmt=4: every gs a multiple of 32
+    bool gs_uniform;              // every gate/up gs equals g0's, every down gs d0's
+    bool slab_gs;                 // every gs taken by the slab kernels
+    bool tc_all;                  // every matrix taken by the tensor-core GEMM, with its TMA map
+};
+
+static int moe_info(const coli_expert *experts, int n_experts, MoeInfo *mi) {
+    if (!experts) return fail(COLI_EINVAL, "experts is NULL");
+    if (n_experts < 1 || n_experts > 8192)
+        return fail(COLI_EINVAL, "n_experts must be in 1..8192 (got %d)", n_experts);
+    int dev = 0;
+    CU(cudaGetDevice(&dev), "cudaGetDevice");
+    const coli_tensor *g0 = experts[0].gate, *d0 = experts[0].down;
+    if (!g0) return fail(COLI_EINVAL, "experts[0].gate is NULL");
+    if (!d0) return fail(COLI_EINVAL, "experts[0].down is NULL");
+    const int64_t F = g0->O, H = g0->I;
+    const int fmt = g0->fmt;
+    if (F > (1 << 30) || H > (1 << 30)) return fail(COLI_EINVAL, "expert dimensions too large");
+    MoeInfo r;
+    r.n = n_experts;
+    r.fmt = fmt;
+    r.device = dev;
+    r.H = H;
+    r.F = F;
+    r.g0 = g0;
+    r.d0 = d0;
+    r.host_any = false;
+    r.gs_ok = r.gs_uniform = r.slab_gs = r.tc_all = true;
+    const char *nm[3] = {"gate", "up", "down"};
+    for (int e = 0; e < n_experts; e++) {
+        const coli_tensor *m[3] = {experts[e].gate, experts[e].up, experts[e].down};
+        for (int k = 0; k < 3; k++) {
+            if (!m[k]) return fail(COLI_EINVAL, "expert %d %s is NULL", e, nm[k]);
+            if (m[k]->device != dev)
+                return fail(COLI_EDEVICE, "expert %d %s lives on device %d but device %d is current", e, nm[k],
+                            m[k]->device, dev);
+            if (m[k]->fmt != fmt)
+                return fail(COLI_EFMT, "expert %d %s has fmt=%d but expert 0 gate has fmt=%d; one format per "
+                                       "expert table is supported", e, nm[k], m[k]->fmt, fmt);
+            r.host_any |= m[k]->host != 0;
+            r.gs_ok &= fmt != 4 || m[k]->gs % 32 == 0;
+            r.gs_uniform &= m[k]->gs == (k == 2 ? d0->gs : g0->gs);
+            r.slab_gs &= slab_supported(fmt, m[k]->gs);
+            r.tc_all &= tc_supported_fmt(fmt, m[k]->gs) && m[k]->tmap != nullptr;
+        }
+        if (m[0]->O != F || m[0]->I != H || m[1]->O != F || m[1]->I != H || m[2]->O != H || m[2]->I != F)
+            return fail(COLI_EINVAL, "expert %d: gate/up must be [%lld][%lld] and down [%lld][%lld]", e,
+                        (long long)F, (long long)H, (long long)H, (long long)F);
+    }
+    *mi = r;
+    return COLI_OK;
+}
+
+// The tensor-core decode plan of a table for one K, kept by
+// coli_expert_table_create's tables between calls.
+struct MdPlanCache {
+    int K = -1;
+    bool ok = false;
+    MdArgs a;
+    size_t smem = 0;
+};
+
+static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, const float *x, int S,
+                   const int32_t *ids, const float *w, int K, float *y, cudaStream_t st, MdPlanCache *pc);
+
 int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_experts, const int32_t *ids,
                    const float *w, int K, float *y, void *stream) {
     g_msg[0] = 0;
@@ -758,62 +834,117 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
     if (int rc = check_ptr(y, "y")) return rc;
     if (int rc = check_ptr(ids, "ids")) return rc;
     if (int rc = check_ptr(w, "w")) return rc;
-    if (!experts) return fail(COLI_EINVAL, "experts is NULL");
     if (S < 1 || K < 1 || K > 64) return fail(COLI_EINVAL, "need S >= 1 and 1 <= K <= 64 (got S=%d K=%d)", S, K);
-    if (n_experts < 1 || n_experts > 8192)
-        return fail(COLI_EINVAL, "n_experts must be in 1..8192 (got %d)", n_experts);
-    const coli_tensor *g0 = experts[0].gate;
-    if (int rc = check_tensor(g0, "experts[0].gate")) return rc;
-    const int64_t F = g0->O, H = g0->I;
-    const int fmt = g0->fmt;
-    if (F > (1 << 30) || H > (1 << 30)) return fail(COLI_EINVAL, "expert dimensions too large");
-    for (int e = 0; e < n_experts; e++) {
-        const coli_tensor *m[3] = {experts[e].gate, experts[e].up, experts[e].down};
-        const char *nm[3] = {"gate", "up", "down"};
-        for (int k = 0; k < 3; k++) {
-            if (int rc = check_tensor(m[k], nm[k])) {
-                char why[256];
-                snprintf(why, sizeof why, "%s", g_msg);
-                return fail(rc, "expert %d %s: %s", e, nm[k], why);
-            }
-            if (m[k]->fmt != fmt)
-                return fail(COLI_EFMT, "expert %d %s has fmt=%d but expert 0 gate has fmt=%d; one format per "
-                                       "expert table is supported", e, nm[k], m[k]->fmt, fmt);
-        }
-        if (m[0]->O != F || m[0]->I != H || m[1]->O != F || m[1]->I != H || m[2]->O != H || m[2]->I != F)
-            return fail(COLI_EINVAL, "expert %d: gate/up must be [%lld][%lld] and down [%lld][%lld]", e,
-                        (long long)F, (long long)H, (long long)H, (long long)F);
-    }
+    MoeInfo mi;
+    if (int rc = moe_info(experts, n_experts, &mi)) return rc;
     if (int rc = injected()) return rc;
     DeviceState *ds = nullptr;
     if (int rc = device_state(&ds)) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     const ExpertDesc *table = nullptr;
     if (int rc = expert_table(ds, experts, n_experts, st, &table)) return rc;
+    return moe_run(mi, table, ds, x, S, ids, w, K, y, st, nullptr);
+}
 
+}  // extern "C"
+
+// A table made once by coli_expert_table_create.
+struct coli_expert_table {
+    MoeInfo mi;
+    ExpertDesc *d = nullptr;   // device copy of the descriptors
+    std::mutex mu;             // guards pc
+    MdPlanCache pc;
+};
+
+extern "C" {
+
+int coli_expert_table_create(const coli_expert *experts, int n_experts, coli_expert_table **out) {
+    g_msg[0] = 0;
+    if (!out) return fail(COLI_EINVAL, "out is NULL");
+    *out = nullptr;
+    MoeInfo mi;
+    if (int rc = moe_info(experts, n_experts, &mi)) return rc;
+    std::vector<ExpertDesc> h((size_t)n_experts);
+    for (int e = 0; e < n_experts; e++) {
+        h[e].m[0] = desc_of(experts[e].gate);
+        h[e].m[1] = desc_of(experts[e].up);
+        h[e].m[2] = desc_of(experts[e].down);
+    }
+    coli_expert_table *t = new coli_expert_table();
+    t->mi = mi;
+    CU(cudaMalloc(&t->d, sizeof(ExpertDesc) * (size_t)n_experts), "cudaMalloc(expert table)");
+    const cudaError_t e = cudaMemcpy(t->d, h.data(), sizeof(ExpertDesc) * (size_t)n_experts, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(t->d);
+        delete t;
+        return cuda_fail(e, "expert table upload");
+    }
+    *out = t;
+    return COLI_OK;
+}
+
+void coli_expert_table_free(coli_expert_table *t) {
+    if (!t) return;
+    cudaFree(t->d);
+    delete t;
+}
+
+int coli_moe_block_t(const float *x, int S, const coli_expert_table *table, const int32_t *ids, const float *w,
+                     int K, float *y, void *stream) {
+    g_msg[0] = 0;
+    if (int rc = check_ptr(x, "x")) return rc;
+    if (int rc = check_ptr(y, "y")) return rc;
+    if (int rc = check_ptr(ids, "ids")) return rc;
+    if (int rc = check_ptr(w, "w")) return rc;
+    if (!table) return fail(COLI_EINVAL, "table is NULL");
+    if (S < 1 || K < 1 || K > 64) return fail(COLI_EINVAL, "need S >= 1 and 1 <= K <= 64 (got S=%d K=%d)", S, K);
+    int dev = 0;
+    CU(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev != table->mi.device)
+        return fail(COLI_EDEVICE, "the table lives on device %d but device %d is current", table->mi.device, dev);
+    if (int rc = injected()) return rc;
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(&ds)) return rc;
+    coli_expert_table *t = const_cast<coli_expert_table *>(table);
+    std::lock_guard<std::mutex> lk(t->mu);
+    return moe_run(t->mi, t->d, ds, x, S, ids, w, K, y, (cudaStream_t)stream, &t->pc);
+}
+
+static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, const float *x, int S,
+                   const int32_t *ids, const float *w, int K, float *y, cudaStream_t st, MdPlanCache *pc) {
+    const int n_experts = mi.n, fmt = mi.fmt;
+    const int64_t H = mi.H, F = mi.F;
+    const coli_tensor *g0 = mi.g0;
     const int n_slots = S * K;
-    const int cpr_gu = g0->cpr, cpr_d = experts[0].down->cpr;
-    bool gs_ok = true, host_any = false;
-    for (int e = 0; e < n_experts; e++)
-        host_any |= experts[e].gate->host || experts[e].up->host || experts[e].down->host;
-    if (fmt == 4)
-        for (int e = 0; e < n_experts && gs_ok; e++)
-            gs_ok = experts[e].gate->gs % 32 == 0 && experts[e].up->gs % 32 == 0 && experts[e].down->gs % 32 == 0;
+    const int cpr_gu = g0->cpr, cpr_d = mi.d0->cpr;
+    const bool gs_ok = mi.gs_ok, host_any = mi.host_any;
 
     // ---------------- decode, S = 1, int4 tables (gs a power-of-two multiple of 64): weights streamed by
     // bulk copies, dot products on the tensor cores, one cooperative launch
     if (S == 1 && (fmt == 2 || fmt == 4) && n_slots <= kMaxDecodeSlots && !host_any) {
-        const coli_tensor *d0 = experts[0].down;
+        const coli_tensor *d0 = mi.d0;
         const int gs_gu = g0->gs, gs_d = d0->gs;
-        bool ok = true;
-        for (int e = 0; e < n_experts && ok && fmt == 4; e++)
-            ok = experts[e].gate->gs == gs_gu && experts[e].up->gs == gs_gu && experts[e].down->gs == gs_d;
         MdArgs a;
         size_t smem = 0;
-        int per_sm = 0;
-        if (ok && md_plan(fmt, (int)H, (int)F, K, (int)g0->rs, (int)d0->rs, g0->ng, d0->ng, gs_gu, gs_d, ds->n_sm,
-                          (size_t)ds->smem_optin, &a, &smem) &&
-            md_occupancy(a, smem, &per_sm) == cudaSuccess && per_sm >= 1) {
+        bool planned;
+        if (pc && pc->K == K) {   // the table's plan for this K
+            planned = pc->ok;
+            a = pc->a;
+            smem = pc->smem;
+        } else {
+            int per_sm = 0;
+            planned = (fmt == 2 || mi.gs_uniform) &&
+                      md_plan(fmt, (int)H, (int)F, K, (int)g0->rs, (int)d0->rs, g0->ng, d0->ng, gs_gu, gs_d, ds->n_sm,
+                              (size_t)ds->smem_optin, &a, &smem) &&
+                      md_occupancy(a, smem, &per_sm) == cudaSuccess && per_sm >= 1;
+            if (pc) {
+                pc->K = K;
+                pc->ok = planned;
+                pc->a = a;
+                pc->smem = smem;
+            }
+        }
+        if (planned) {
             unsigned *ctr = nullptr;
             if (int rc = decode_counters(ds, st, md_counter_words(a), &ctr)) return rc;
             a.x = x;
@@ -835,12 +966,10 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
     // ---------------- decode, S = 1, int4 / int8 tables: weights streamed by bulk copies, dp4a decode,
     // one cooperative launch
     if (S == 1 && (fmt == 1 || fmt == 2 || fmt == 4) && n_slots <= kMaxDecodeSlots && !host_any) {
-        const coli_tensor *d0 = experts[0].down;
+        const coli_tensor *d0 = mi.d0;
         const int gs_gu = g0->gs, gs_d = d0->gs;
         // one gs per role, a power-of-two number of 16-byte chunks per group
-        bool ok = fmt != 4 || (slab_supported(4, gs_gu) && slab_supported(4, gs_d));
-        for (int e = 0; e < n_experts && ok && fmt == 4; e++)
-            ok = experts[e].gate->gs == gs_gu && experts[e].up->gs == gs_gu && experts[e].down->gs == gs_d;
+        const bool ok = fmt != 4 || (slab_supported(4, gs_gu) && slab_supported(4, gs_d) && mi.gs_uniform);
         SdArgs a;
         size_t smem = 0;
         int per_sm = 0;
@@ -871,11 +1000,7 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
     }
 
     // ---------------- decode, S = 1: activation slab in registers, one cooperative launch
-    bool slab_ok = S == 1 && n_slots <= kMaxDecodeSlots && fmt != 3 && F % 32 == 0;
-    for (int e = 0; e < n_experts && slab_ok; e++)
-        slab_ok = slab_supported(fmt, experts[e].gate->gs) && experts[e].gate->gs == g0->gs &&
-                  experts[e].up->gs == g0->gs && slab_supported(fmt, experts[e].down->gs) &&
-                  experts[e].down->gs == experts[0].down->gs;
+    const bool slab_ok = S == 1 && n_slots <= kMaxDecodeSlots && fmt != 3 && F % 32 == 0 && mi.slab_gs && mi.gs_uniform;
     if (slab_ok) {
         const int grid_min = ds->n_sm;
         int sb = std::min(n_slots, 8);
@@ -910,7 +1035,7 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
             a.rpc = (int)((H + grid - 1) / grid);
             a.timeout_ns = 2000000000LL;
             cudaError_t e = launch_slab_decode(a, fmt, grid, smem, fmt == 4 ? g0->gs : 32,
-                                               fmt == 4 ? experts[0].down->gs : 32, st);
+                                               fmt == 4 ? mi.d0->gs : 32, st);
             if (e != cudaSuccess) return cuda_fail(e, "decode expert-block launch");
             count(1, 0);
             return COLI_OK;
@@ -965,13 +1090,7 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
     }
 
     // ---------------- prefill on the tensor cores (int4 formats with one gs per role)
-    bool tc_ok = fmt == 2 || fmt == 4;
-    for (int e = 0; e < n_experts && tc_ok; e++) {
-        tc_ok = tc_supported_fmt(fmt, experts[e].gate->gs) && experts[e].gate->gs == g0->gs &&
-                experts[e].up->gs == g0->gs && experts[e].down->gs == experts[0].down->gs &&
-                tc_supported_fmt(fmt, experts[e].down->gs) && experts[e].gate->tmap && experts[e].up->tmap &&
-                experts[e].down->tmap;
-    }
+    const bool tc_ok = (fmt == 2 || fmt == 4) && mi.tc_all && mi.gs_uniform;
     if (tc_ok) {
         const int TR = tc_block_rows();
         const int max_tiles = (n_slots + TR - 1) / TR + std::min(n_experts, n_slots);
@@ -1047,7 +1166,7 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
         d.O = (int)H;
         d.I = (int)F;
         d.nkb = F_pad / 64;
-        d.gkb = fmt == 4 ? experts[0].down->gs / 64 : d.nkb;
+        d.gkb = fmt == 4 ? mi.d0->gs / 64 : d.nkb;
         d.n_mblk = (int)((H + 127) / 128);
         d.nterm_flag = &flags[1];
         d.out = slot_out;

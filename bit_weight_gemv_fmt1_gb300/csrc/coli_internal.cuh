@@ -722,6 +722,16 @@ cudaError_t launch_slab_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t
 
 // Record `msg` as the calling thread's last error (coli_last_error) and return code.
 int set_last_error(int code, const char *msg);
+// Clear the calling thread's last error message (an entry point's first step).
+void clear_last_error();
+// The host-side fault-injection gate of compute calls (coli_set_fail_after):
+// COLI_EINJECTED once the counter has run out, else COLI_OK.
+int injected_gate();
+// Count one compute call with its launches and weight bytes (coli_get_stats).
+void count_call(int launches, uint64_t weight_bytes);
+// Copy n expert descriptors, passed by value in kernel parameters, to the
+// device table dst (stream-ordered, no host memory involved).
+cudaError_t launch_table_fill(ExpertDesc *dst, const ExpertDesc *src, int n, cudaStream_t st);
 
 constexpr int kDecodeThreads = 256;
 constexpr int kMaxDecodeSlots = 64;

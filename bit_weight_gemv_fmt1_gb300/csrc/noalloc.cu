@@ -2,28 +2,30 @@
 // device memory.
 //
 // Some callers must not call cudaMalloc/cudaFree (or anything that does):
-// code that records CUDA graphs, where an allocation inside the capture is an
-// error or silently becomes part of the graph; latency-critical decode loops,
-// because cudaMalloc/cudaFree synchronise the whole device; and processes in
-// which another allocator (a framework's caching allocator, a pre-reserved
-// pool) already owns the GPU memory, so a surprise allocation can fail.
-// coli_moe_block allocates its scratch (per stream) and its expert-table copy
-// (per device) on first use; this variant keeps them in one file-scope
-// device array instead, sized for the decode path only.
+// latency-critical decode loops, because cudaMalloc/cudaFree synchronise the
+// whole device, and processes in which another allocator (a framework's
+// caching allocator, a pre-reserved pool) already owns the GPU memory, so a
+// surprise allocation can fail.  coli_moe_block allocates its scratch (per
+// stream) and its expert-table copy (per device) on first use; this variant
+// keeps them in one file-scope device array instead, sized for the decode path
+// only.
 //
 // The scratch array lives in every GPU that loads the library until the
 // process exits.  Its device address is looked up once per device with
-// cudaGetSymbolAddress, by the first call on that device (so make that first
-// call before any stream capture).  All calls share the array: calls that may
-// overlap on the GPU (different streams without ordering, several host threads)
-// race and must be serialised by the caller.  The barrier words are cleared
-// at the start of every call; the other regions are fully written before they
-// are read.
+// cudaGetSymbolAddress, by the first call on that device.  All calls share the
+// array: calls that may overlap on the GPU (different streams without
+// ordering, several host threads) race and must be serialised by the caller.
+// The expert descriptors reach the array through the parameters of a small
+// copy kernel (no host buffer is read by the GPU), and only when they differ
+// from the ones the previous call on the device left there.  The barrier words
+// are cleared at the start of every call; the other regions are fully written
+// before they are read.
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "coli_internal.cuh"
 
@@ -43,8 +45,20 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void *g_addr[64];   // device address of g_noalloc_scratch, per device ordinal
+std::vector<ExpertDesc> g_mirror[64];   // per device: the descriptors the scratch holds
 
-thread_local ExpertDesc g_host_table[kNoallocMaxExperts];
+// Descriptors per copy launch: 128 x 120 bytes of kernel parameters.
+constexpr int kFillChunk = 128;
+struct FillArgs {
+    ExpertDesc *dst;
+    int n;
+    ExpertDesc d[kFillChunk];
+};
+__global__ void table_fill_kernel(const FillArgs a) {
+    for (int i = threadIdx.x; i < a.n; i += blockDim.x) a.dst[i] = a.d[i];
+}
+
+bool same_desc(const ExpertDesc &p, const ExpertDesc &q) { return memcmp(&p, &q, sizeof p) == 0; }
 
 __attribute__((format(printf, 2, 3))) int bad(int code, const char *fmt, ...) {
     char msg[512];
@@ -57,9 +71,25 @@ __attribute__((format(printf, 2, 3))) int bad(int code, const char *fmt, ...) {
 
 }  // namespace
 
+namespace coli {
+cudaError_t launch_table_fill(ExpertDesc *dst, const ExpertDesc *src, int n, cudaStream_t st) {
+    for (int i0 = 0; i0 < n; i0 += kFillChunk) {
+        FillArgs a;
+        a.dst = dst + i0;
+        a.n = std::min(kFillChunk, n - i0);
+        memcpy(a.d, src + i0, sizeof(ExpertDesc) * (size_t)a.n);
+        table_fill_kernel<<<1, 128, 0, st>>>(a);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+}  // namespace coli
+
 extern "C" int coli_moe_block_noalloc(const float *x, int S, const coli_expert *experts, int n_experts,
                                       const int32_t *ids, const float *w, int K, float *y, int32_t *dev_error,
                                       void *stream) {
+    clear_last_error();
     cudaStream_t st = (cudaStream_t)stream;
     if (!x || !y || !ids || !w || !experts || !dev_error) return bad(COLI_EINVAL, "a pointer argument is NULL");
     if (S < 1 || K < 1 || K > 64) return bad(COLI_EINVAL, "need S >= 1 and 1 <= K <= 64 (got S=%d K=%d)", S, K);
@@ -91,6 +121,7 @@ extern "C" int coli_moe_block_noalloc(const float *x, int S, const coli_expert *
     if ((long long)n_slots * F > kNoallocMaxHidden)
         return bad(COLI_EINVAL, "S*K*F=%lld exceeds the no-allocation scratch (%lld floats)", (long long)n_slots * F,
                    kNoallocMaxHidden);
+    if (int rc = injected_gate()) return rc;
 
     // scratch address, once per device
     void *base = nullptr;
@@ -127,11 +158,14 @@ extern "C" int coli_moe_block_noalloc(const float *x, int S, const coli_expert *
         return bad(COLI_ECUDA, "decode kernel occupancy query failed");
     const int grid = per_sm * n_sm;
 
-    // descriptors -> scratch table; clear the barrier words and the error output
+    // descriptors -> scratch table (only when they changed since the previous
+    // call on this device); clear the barrier words and the error output
+    std::vector<ExpertDesc> h((size_t)n_experts);
     for (int e = 0; e < n_experts; e++) {
         const coli_tensor *m[3] = {experts[e].gate, experts[e].up, experts[e].down};
         for (int k = 0; k < 3; k++) {
-            MatDesc &d = g_host_table[e].m[k];
+            MatDesc &d = h[e].m[k];
+            memset(&d, 0, sizeof d);
             d.q = m[k]->q;
             d.s = m[k]->s;
             d.rs = m[k]->rs;
@@ -141,8 +175,22 @@ extern "C" int coli_moe_block_noalloc(const float *x, int S, const coli_expert *
         }
     }
     unsigned char *b = (unsigned char *)base;
-    cudaError_t e = cudaMemcpyAsync(b + kOffTable, g_host_table, sizeof(ExpertDesc) * (size_t)n_experts,
-                                    cudaMemcpyHostToDevice, st);
+    cudaError_t e = cudaSuccess;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        std::vector<ExpertDesc> &mir = g_mirror[dev];
+        bool same = mir.size() >= h.size();
+        for (size_t i = 0; i < h.size() && same; i++) same = same_desc(mir[i], h[i]);
+        if (!same) {
+            e = launch_table_fill((ExpertDesc *)(b + kOffTable), h.data(), n_experts, st);
+            if (e == cudaSuccess) {
+                if (mir.size() < h.size()) mir.resize(h.size());
+                std::copy(h.begin(), h.end(), mir.begin());
+            } else {
+                mir.clear();
+            }
+        }
+    }
     if (e == cudaSuccess) e = cudaMemsetAsync(b + kOffBar, 0, 2 * sizeof(unsigned), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st);
     if (e != cudaSuccess) return bad(COLI_ECUDA, "scratch set-up: %s", cudaGetErrorString(e));
@@ -169,5 +217,6 @@ extern "C" int coli_moe_block_noalloc(const float *x, int S, const coli_expert *
     a.timeout_ns = 2000000000LL;
     e = launch_moe_decode(a, fmt, grid, smem, st);
     if (e != cudaSuccess) return bad(COLI_ECUDA, "decode expert-block launch: %s", cudaGetErrorString(e));
+    count_call(1, 0);
     return COLI_OK;
 }

@@ -260,32 +260,58 @@ int coli_moe_router(const float *x, int S, const coli_tensor *router, const floa
  *   w        device f32 [S][K] routing weights, used as given.
  *   y        device f32 [S][H], overwritten; must not overlap x.
  *   S >= 1, 1 <= K <= 64.
- * S*K <= 64 runs a single-launch decode kernel (a cooperative grid with one
- * bounded grid-wide wait between the gate/up and down phases): for S = 1 and
- * fmt=4 (gs a power-of-two multiple of 32, a multiple of 4 groups per row,
- * H and F multiples of 128, x 16-byte aligned, K*F*4 <= 64 KB) the kernel that
- * streams the weights through shared memory with bulk copies; otherwise the
- * slab kernel (S = 1) or the general decode kernel.  Larger S*K runs the
- * prefill pipeline (routing, gather, grouped gate/up, grouped down, combine)
- * on the tensor cores for int4 tables with gs % 64 == 0, on the CUDA cores
- * otherwise.  An id out of range is recorded for coli_sync_check(stream) and
- * y is then unspecified.
+ * S*K <= 64 runs a single-launch decode kernel (one cooperative grid, one CTA
+ * per SM, weights streamed through shared memory with bulk copies): for S = 1
+ * and int4 tables (fmt=2, or fmt=4 with gs 64 or 128; H, F <= 6144; at most
+ * one routed expert per SM) the kernel whose dot products run on the tensor
+ * cores; for other S = 1 int4 / int8 tables the one that decodes with dp4a;
+ * otherwise the slab kernel (S = 1) or the general decode kernel.  Larger S*K
+ * runs the prefill pipeline (routing, gather, grouped gate/up, grouped down,
+ * combine) on the tensor cores for int4 tables with gs % 64 == 0, on the CUDA
+ * cores otherwise.  Every call checks the whole table (shapes, formats,
+ * device) on the host: for a table used over and over, create it once with
+ * coli_expert_table_create and call coli_moe_block_t.  An id out of range is
+ * recorded for coli_sync_check(stream) and y is then unspecified.
  * Errors: COLI_EINVAL, COLI_EFMT, COLI_EDEVICE, COLI_ENOMEM, COLI_ECUDA.
  */
 int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_experts,
                    const int32_t *ids, const float *w, int K, float *y, void *stream);
 
 /*
+ * An expert table checked and copied to the device once, for coli_moe_block_t
+ * (the host work of a call is then independent of the number of experts).
+ * The colibri pages have no counterpart of this entry point.
+ *   experts, n_experts  as coli_moe_block; copied, so the array may be freed.
+ *   out      receives the table; the tensors it names must stay alive until
+ *            coli_expert_table_free.  The table belongs to the device current
+ *            at creation.
+ * Errors: COLI_EINVAL, COLI_EFMT, COLI_EDEVICE, COLI_ENOMEM, COLI_ECUDA.
+ */
+typedef struct coli_expert_table coli_expert_table;
+int coli_expert_table_create(const coli_expert *experts, int n_experts, coli_expert_table **out);
+void coli_expert_table_free(coli_expert_table *table);
+
+/*
+ * coli_moe_block on a table from coli_expert_table_create: the same result,
+ * the same kernels.  The table's decode plan for the last K used is kept with
+ * it.  The table may be used from several host threads.
+ * Errors: COLI_EINVAL (NULL pointer, S or K out of range), COLI_EDEVICE (the
+ * current device is not the table's), COLI_ENOMEM, COLI_ECUDA.
+ */
+int coli_moe_block_t(const float *x, int S, const coli_expert_table *table, const int32_t *ids,
+                     const float *w, int K, float *y, void *stream);
+
+/*
  * The decode expert block of coli_moe_block for callers that cannot allocate
  * device memory.  The colibri pages have no counterpart of this entry point.
  *
- * Some callers must not call cudaMalloc/cudaFree: code that records CUDA
- * graphs, latency-critical decode loops (allocation synchronises the device),
- * processes whose GPU memory is owned by another allocator.  coli_moe_block
- * allocates scratch and an expert-table copy on first use; this entry point
- * allocates nothing.  Its scratch (expert descriptors, the h buffer, the grid
- * barrier words) is one file-scope device array of about 2.2 MB that every GPU
- * loading the library holds until the process exits.
+ * Some callers must not call cudaMalloc/cudaFree: latency-critical decode
+ * loops (allocation synchronises the device), processes whose GPU memory is
+ * owned by another allocator.  coli_moe_block allocates scratch and an
+ * expert-table copy on first use; this entry point allocates nothing.  Its
+ * scratch (expert descriptors, the h buffer, the grid barrier words) is one
+ * file-scope device array of about 2.2 MB that every GPU loading the library
+ * holds until the process exits.
  *   Arguments as coli_moe_block, plus:
  *   dev_error  device int32, an output: cleared by the call, then set by the
  *              kernel to 1 if its bounded grid-wide wait ran out or 2 if a
@@ -295,9 +321,14 @@ int coli_moe_block(const float *x, int S, const coli_expert *experts, int n_expe
  *   single-launch decode kernel's shared memory; fmt=4 needs gs % 32 == 0
  *   (COLI_EFMT).
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress); make that call before any stream capture.  Every
- * call shares the array: calls that may overlap on the GPU (unordered streams,
- * several host threads) race and must be serialised by the caller.
+ * (cudaGetSymbolAddress).  The expert descriptors go to the array through the
+ * parameters of a small copy kernel, and only when they differ from the ones
+ * the previous call on the device left there; no host memory is read by the
+ * device.  Every call shares the array: calls that may overlap on the GPU
+ * (unordered streams, several host threads) race and must be serialised by
+ * the caller.  Counts as a compute call for coli_set_fail_after and
+ * coli_get_stats.
+ * Errors: COLI_EINVAL, COLI_EFMT, COLI_EDEVICE, COLI_ECUDA, COLI_EINJECTED.
  */
 int coli_moe_block_noalloc(const float *x, int S, const coli_expert *experts, int n_experts,
                            const int32_t *ids, const float *w, int K, float *y, int32_t *dev_error,

@@ -77,6 +77,11 @@ def test_compute_calls_refuse_null(lib):
     assert lib.coli_matmul(None, None, None, 1, None) == -1
     assert lib.coli_moe_route(None, 1, 8, 256, None, None, None) == -1
     assert lib.coli_moe_block(None, 1, None, 1, None, None, 8, None, None) == -1
+    out = ctypes.c_void_p(1)
+    assert lib.coli_expert_table_create(None, 1, ctypes.byref(out)) == -1
+    assert out.value is None          # cleared before the arguments are refused
+    assert lib.coli_moe_block_t(None, 1, None, None, None, 8, None, None) == -1
+    lib.coli_expert_table_free(None)  # a NULL table is a no-op
     i64 = ctypes.c_int64
     assert lib.coli_matmul_rows(None, i64(0), i64(0), i64(1), 1, None, None, 1, None) == -1
     assert lib.coli_matmul_rows_t(None, i64(0), i64(0), i64(1), 1, None, None, 1, None) == -1

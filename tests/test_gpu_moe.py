@@ -142,7 +142,7 @@ def test_decode_ragged_routing_and_empty_slots():
     assert np.all(got[2] == 0.0)
 
 
-@pytest.mark.parametrize("fmt,gs", [(4, 128), (4, 64), (2, 0), (4, 16), (1, 0), (7, 0)])
+@pytest.mark.parametrize("fmt,gs", [(4, 128), (4, 64), (2, 0), (4, 16), (1, 0), (7, 0), (0, 0), (3, 0)])
 @pytest.mark.parametrize("S,K", [(9, 8), (40, 4), (100, 8)])
 def test_prefill_block(fmt, gs, S, K):
     torch = cuda_or_skip()
@@ -223,3 +223,70 @@ def test_prefill_workload_sampled_rows():
     rows = np.sort(g.choice(c["S"], 6, replace=False))
     ref = orc.moe_block(c["H"], c["F"], _oracle_mats(host), x[rows], ids[rows], w[rows])
     assert norm_err(got[rows], ref) <= TOL
+
+
+def test_prefill_workload_hot_expert_tiles():
+    """Prefill expert block at full size (as above): for the three experts
+    with the most tokens, the first and the last token of every 64-token tile
+    of the expert's rows (tokens in routing order, the order the grouped GEMMs
+    take them in) checked against the oracle."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    c = wl.MOE_PREFILL
+    g = wl.rng(c["seed"] + 1)
+    host = _experts(g, c["H"], c["F"], c["E"], c["fmt"], c["gs"], distinct=32)
+    table = _device_table(coli, host)
+    x = wl.activations(g, c["S"], c["H"], bf16_exact=True)
+    ids, w = wl.routing_zipf(g, c["S"], c["E"], c["K"], c["zipf"])
+    got = _run_block(coli, torch, table, x, ids, w, c["H"])
+    counts = np.bincount(ids[ids >= 0].ravel(), minlength=c["E"])
+    rows = set()
+    for e in np.argsort(-counts, kind="stable")[:3]:
+        toks = np.nonzero((ids == e).any(axis=1))[0]   # ascending token order
+        for t0 in range(0, len(toks), 64):
+            tile = toks[t0: t0 + 64]
+            rows.update((int(tile[0]), int(tile[-1])))
+    rows = np.array(sorted(rows))
+    assert len(rows) >= 6
+    ref = orc.moe_block(c["H"], c["F"], _oracle_mats(host), x[rows], ids[rows], w[rows])
+    assert norm_err(got[rows], ref) <= TOL
+
+
+@pytest.mark.parametrize("fmt,gs,S", [(4, 64, 1), (2, 0, 1), (1, 0, 1), (4, 32, 1), (4, 64, 16)])
+def test_block_table_handle_matches_array_path(fmt, gs, S):
+    """coli_moe_block_t on a table made once runs the same kernels as
+    coli_moe_block on the host array: the results agree bit for bit."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E, K = 1024, 512, 16, 8
+    g = wl.rng(5100 + fmt + gs + S)
+    host = _experts(g, H, F, E, fmt, gs, distinct=8)
+    table = _device_table(coli, host)
+    x = torch.from_numpy(wl.activations(g, S, H)).cuda()
+    ids, w = wl.routing_topk_softmax(g, S, E, K)
+    di, dw = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    y1 = torch.full((S, H), float("nan"), device="cuda")
+    y2 = torch.full((S, H), float("nan"), device="cuda")
+    coli.moe_block(x, table, di, dw, y1)
+    coli.moe_block_array(x, table, di, dw, y2)
+    coli.sync_check()
+    assert torch.equal(y1, y2)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x.cpu().numpy(), ids, w)
+    assert norm_err(y1.cpu().numpy(), ref) <= TOL
+
+
+def test_block_table_handle_keeps_one_plan_per_K():
+    """One table, calls with K = 4, 8, 4: the table's kept decode plan is the
+    one of the call's K each time."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E = 2048, 1024, 24
+    g = wl.rng(5200)
+    host = _experts(g, H, F, E, 4, 64, distinct=6)
+    table = _device_table(coli, host)
+    mats = _oracle_mats(host)
+    for K in (4, 8, 4):
+        x = wl.activations(g, 1, H)
+        ids, w = wl.routing_topk_softmax(g, 1, E, K)
+        got = _run_block(coli, torch, table, x, ids, w, H)
+        assert norm_err(got, orc.moe_block(H, F, mats, x, ids, w)) <= TOL
