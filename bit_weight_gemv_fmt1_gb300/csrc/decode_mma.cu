@@ -59,6 +59,8 @@
 // returns.  The last CTA to leave moves the tag on for the next call.
 #include <algorithm>
 #include <cstring>
+#include <map>
+#include <mutex>
 
 #include "coli_internal.cuh"
 #include "decode_route.cuh"
@@ -1043,8 +1045,18 @@ cudaError_t md_occupancy(const MdArgs &a, size_t smem, int *per_sm) {
 
 cudaError_t launch_decode_mma(const MdArgs &a, int grid, size_t smem, cudaStream_t st) {
     return md_dispatch(a, [&](auto kern) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+        // the shared-memory limit is set once per kernel instance and size
+        static std::mutex mu;
+        static std::map<const void *, size_t> done;
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            size_t &have = done[(const void *)kern];
+            if (have < smem) {
+                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+                have = smem;
+            }
+        }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(kMdThreads);
