@@ -252,6 +252,45 @@ class DecodeBlock:
 
 
 # ---------------------------------------------------------------- other workloads of the metric
+# The oracle timed beside each GPU number (bounded samples; off with --no-cpu-baseline).
+CPU_TIMING = {"on": True, "budget": 0.4}
+
+
+def oracle_time(fn, units_per_call: float, unit: str, sample: str):
+    """The oracle, as it stands, on a bounded sample: fn() is one oracle call
+    covering units_per_call units of the metric.  Timed single-threaded and on
+    all the host's cores (each: one call, then more until the budget is spent)."""
+    if not CPU_TIMING["on"]:
+        return None
+    from oracle import oracle as orc
+    n_all = orc.threads()
+    rate = {}
+    for label, n in (("single_thread", 1), ("all_cores", n_all)):
+        prev = orc.set_threads(n)
+        try:
+            calls, t0 = 0, time.perf_counter()
+            while True:
+                fn()
+                calls += 1
+                dt = time.perf_counter() - t0
+                if dt >= CPU_TIMING["budget"]:
+                    break
+        finally:
+            orc.set_threads(prev)
+        rate[label] = units_per_call * calls / dt
+    return {"value": rate["all_cores"], "unit": unit, "cores": n_all, "kind": "oracle",
+            "single_thread": rate["single_thread"], "sample": sample}
+
+
+def _orc():
+    from oracle import oracle as orc
+    return orc
+
+
+def _omat(m):
+    return _orc().Mat(m.fmt, m.gs, m.O, m.I, m.data, m.scales)
+
+
 def _time_loop(torch, fn, n, warm=5):
     for i in range(warm):
         fn(i)
@@ -318,7 +357,11 @@ def bench_gemv(coli, torch, peaks, l2_bytes, only=None):
             y = torch.empty(S, O, device="cuda")
             t = _time_graph(torch, lambda i: coli.matmul(Ws[i % ncopy], x, y), max(200, 2 * ncopy))
             nbytes = m.nbytes + 4 * S * (I + O)
-            res[f"S{S}"] = {"us": t * 1e6, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"]}
+            xh = x.cpu().numpy()
+            cpu = oracle_time(lambda: _orc().matmul(m.fmt, m.gs, O, I, m.data, m.scales, xh), nbytes / 1e9, "GB/s",
+                              f"whole {O}x{I} product at S={S}")
+            res[f"S{S}"] = {"us": t * 1e6, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+                            "cpu_baseline": cpu}
         coli.sync_check()
         out[name] = {"bytes": m.nbytes, "copies": ncopy, **res}
         del Ws
@@ -332,12 +375,14 @@ def bench_prefill(coli, torch, peaks, steps=5, n_experts=None):
     c = wl.MOE_PREFILL
     g = wl.rng(c["seed"])
     H, F, E, K, S = c["H"], c["F"], n_experts or c["E"], c["K"], c["S"]
-    dev = []
+    dev, hosts = [], []
     for _ in range(E):
         trip = wl.expert(g, H, F, c["fmt"], c["gs"])
         dev.append(tuple(coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in trip))
+        hosts.append(trip if CPU_TIMING["on"] else None)
     table = coli.ExpertTable(dev)
-    x = torch.from_numpy(wl.activations(g, S, H, bf16_exact=True)).cuda()
+    x_h = wl.activations(g, S, H, bf16_exact=True)
+    x = torch.from_numpy(x_h).cuda()
     ids_h, w_h = wl.routing_zipf(g, S, E, K, c["zipf"])
     ids = torch.from_numpy(ids_h).cuda()
     w = torch.from_numpy(w_h).cuda()
@@ -350,20 +395,32 @@ def bench_prefill(coli, torch, peaks, steps=5, n_experts=None):
     roof = sum(max(eb / (peaks["hbm_gbs"] * 1e9), n * flops_per_row / (peaks["bf16_tflops"] * 1e12))
                for n in counts if n > 0)
     touched = int((counts > 0).sum())
+    cpu = None
+    if CPU_TIMING["on"]:
+        rows = 2   # the oracle on the first rows of the batch, with their own routing
+        used = sorted(set(int(e) for e in ids_h[:rows].reshape(-1)))
+        mats = [tuple(_omat(m) for m in hosts[e]) for e in used]
+        ids_l = np.searchsorted(np.array(used), ids_h[:rows]).astype(np.int32)
+        cpu = oracle_time(lambda: _orc().moe_block(H, F, mats, x_h[:rows], ids_l, w_h[:rows]), rows, "tokens/s",
+                          f"the expert block on the batch's first {rows} rows (top-{K} each)")
+    del hosts
     return {"tokens/s": S / t, "ms": t * 1e3, "experts_touched": touched, "max_rows_per_expert": int(counts.max()),
             "GB/s": touched * eb / t / 1e9, "GFLOP": float(counts.sum() * flops_per_row / 1e9),
-            "roofline_ms": roof * 1e3, "frac_of_per_expert_roofline": roof / t}
+            "roofline_ms": roof * 1e3, "frac_of_per_expert_roofline": roof / t, "cpu_baseline": cpu}
 
 
-def bench_streaming(coli, torch, peaks, tokens=10):
+def bench_streaming(coli, torch, peaks, tokens=10, pool_gb=None, only_fmt=None):
     """Weight streaming: S=1 GEMVs of 2048x6144 over a 40 GB resident pool,
-    8 random matrices per layer (one launch: shared input), 75 layers per token."""
+    8 random matrices per layer (one launch: shared input), 75 layers per token.
+    pool_gb / only_fmt shrink the run (profiling captures)."""
     c = wl.STREAMING
     res = {}
     for fmt, gs in c["variants"]:
+        if only_fmt is not None and fmt != only_fmt:
+            continue
         g = wl.rng(c["seed"] + fmt)
         per = wl.tensor_bytes(fmt, c["O"], c["I"], gs)
-        n_pool = int(c["pool_gb"] * 1e9 // per)
+        n_pool = int((pool_gb or c["pool_gb"]) * 1e9 // per)
         srcs = [wl.random_matrix(g, fmt, c["O"], c["I"], gs) for _ in range(16)]
         pool = [coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in
                 (srcs[i % 16] for i in range(n_pool))]
@@ -374,10 +431,14 @@ def bench_streaming(coli, torch, peaks, tokens=10):
         t = _time_graph(torch, lambda i: coli.matmul_multi([pool[j] for j in sel[i]], x, ys), n_layers, warm=c["layers"])
         coli.sync_check()
         nbytes = c["per_layer"] * per
+        xh = x.cpu().numpy()
+        cpu = oracle_time(lambda: [_orc().matmul(m.fmt, m.gs, m.O, m.I, m.data, m.scales, xh)
+                                   for m in srcs[:c["per_layer"]]], nbytes / 1e9, "GB/s",
+                          f"one layer: {c['per_layer']} whole {c['O']}x{c['I']} products at S=1")
         res[f"fmt{fmt}" + (f"_g{gs}" if fmt == 4 else "")] = {
             "pool_matrices": n_pool, "pool_GB": n_pool * per / 1e9, "layer_us": t * 1e6,
             "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
-            "tokens/s": 1.0 / (c["layers"] * t)}
+            "tokens/s": 1.0 / (c["layers"] * t), "cpu_baseline": cpu}
         del pool
         torch.cuda.empty_cache()
     return res
@@ -430,7 +491,11 @@ def bench_router(coli, torch, peaks, steps=200):
                                coli.moe_block(xs[i], table, ids, w, y, stream=st)))
     coli.sync_check()
     rb = E * H * 4
-    return {"router_us": t_router * 1e6, "router_GB/s": rb / t_router / 1e9,
+    xh = xs[0].cpu().numpy()
+    bh = bias.cpu().numpy()
+    cpu = oracle_time(lambda: _orc().moe_topk(_orc().matmul(0, 0, E, H, Wr, None, xh), K, bias=bh, norm_topk=True),
+                      rb / 1e9, "GB/s", "one token: f32 router logits and the biased top-8")
+    return {"router_us": t_router * 1e6, "router_GB/s": rb / t_router / 1e9, "cpu_baseline": cpu,
             "router_plus_expert_block_us": t_layer * 1e6,
             "note": "S=1, f32 router 256x6144, top-8 of sigmoid+bias with norm_topk; expert block over a "
                     "64-expert resident pool (L2 sees part of it: the block time here is not the headline)"}
@@ -532,32 +597,44 @@ def bench_absorb(coli, torch, peaks, l2_bytes):
     return res
 
 
-def bench_decode_formats(coli, torch, peaks, steps=200):
-    """The decode expert block (H=6144, F=2048, S=1, top-8, a fresh routing per
-    call) for expert tables of other formats than the headline's int4 g64:
-    FP8 E4M3 with 128x128 block scales and int8; a 64-expert resident pool
-    (every pool > 2 GB, so L2 holds a small part of it)."""
+def bench_decode_formats(coli, torch, peaks, steps=200, only=None):
+    """The decode expert block (H=6144, F=2048, S=1, top-8 of 256 resident
+    experts, a fresh softmax top-8 routing per call) for every expert format:
+    f32, int8, int4 per-row, int2, int4 g64 (the headline's), int4 g128 and FP8
+    E4M3 with 128x128 block scales.  The 256 experts are distinct device copies
+    of 8 generated ones, so every pool is far larger than L2 (the smallest,
+    int2, is 2.5 GB)."""
     d = wl.MOE_DECODE
-    H, F, K = d["H"], d["F"], d["K"]
+    H, F, K, E = d["H"], d["F"], d["K"], d["E"]
     out = {}
-    for name, fmt, gs in (("fp8_fmt7_b128", 7, 0), ("int8_fmt1", 1, 0)):
-        g = wl.rng(d["seed"] + 300 + fmt)
+    cases = (("f32_fmt0", 0, 0), ("int8_fmt1", 1, 0), ("int4_fmt2", 2, 0), ("int2_fmt3", 3, 0),
+             ("int4_fmt4_g64", 4, 64), ("int4_fmt4_g128", 4, 128), ("fp8_fmt7_b128", 7, 0))
+    for name, fmt, gs in cases:
+        if only and name != only:
+            continue
+        g = wl.rng(d["seed"] + 300 + fmt + gs)
         hosts = [wl.expert(g, H, F, fmt, gs) for _ in range(8)]
-        n_pool = 64
         dev = [tuple(coli.tensor_upload(m.fmt, m.gs, m.O, m.I, m.data, m.scales) for m in hosts[e % 8])
-               for e in range(n_pool)]
+               for e in range(E)]
         table = coli.ExpertTable(dev)
-        ids_h, w_h = wl.routing_topk_softmax(g, steps, n_pool, K)
+        ids_h, w_h = wl.routing_topk_softmax(g, steps, E, K)
         ids = torch.from_numpy(ids_h).cuda()
         w = torch.from_numpy(w_h).cuda()
-        xs = torch.randn(steps, 1, H, device="cuda")
+        xs_h = wl.activations(g, steps, H)
+        xs = torch.from_numpy(xs_h).cuda().view(steps, 1, H)
         y = torch.empty(1, H, device="cuda")
         t = _time_graph(torch, lambda i: coli.moe_block(xs[i], table, ids[i: i + 1], w[i: i + 1], y), steps)
         coli.sync_check()
-        nbytes = K * wl.expert_bytes(H, F, fmt, gs)
+        eb = wl.expert_bytes(H, F, fmt, gs)
+        nbytes = K * eb + 2 * 4 * H + 8 * K
+        cpu = None
+        if CPU_TIMING["on"]:
+            mats = [tuple(_omat(m) for m in hosts[e % 8]) for e in ids_h[0]]
+            cpu = oracle_time(lambda: _orc().moe_block(H, F, mats, xs_h[:1], np.arange(K, dtype=np.int32)[None],
+                                                       w_h[:1]), nbytes / 1e9, "GB/s", "one token's block (8 experts)")
         out[name] = {"us": t * 1e6, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
-                     "pool_GB": n_pool * wl.expert_bytes(H, F, fmt, gs) / 1e9}
-        del dev, table
+                     "pool_GB": E * eb / 1e9, "cpu_baseline": cpu}
+        del dev, table, hosts
         torch.cuda.empty_cache()
     return out
 
@@ -640,12 +717,21 @@ def main():
     ap.add_argument("--experts-prefill", type=int, default=None, help="resident experts of the prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-entry-budget", type=float, default=0.4,
+                    help="seconds of oracle timing per by_workload entry and thread count (after one call)")
     ap.add_argument("--experts", type=int, default=None, help="resident experts of the decode workload (default 256)")
     ap.add_argument("--quick", action="store_true", help="headline workload only (no by_workload sweep)")
+    ap.add_argument("--decode-format", default=None,
+                    help="--workload decode_formats: run only this case (e.g. int8_fmt1, fp8_fmt7_b128)")
+    ap.add_argument("--stream-pool-gb", type=float, default=None,
+                    help="--workload streaming: resident pool size (default 40 GB)")
+    ap.add_argument("--stream-fmt", type=int, default=None, help="--workload streaming: only this format")
     ap.add_argument("--gemv-case", default=None,
                     help="--workload gemv_sweep: run only this case (e.g. sweep_fmt4_g64, fp8_fmt7_b128)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    CPU_TIMING["on"] = not args.no_cpu_baseline
+    CPU_TIMING["budget"] = args.cpu_entry_budget
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -668,7 +754,7 @@ def main():
             elif args.workload == "router":
                 res = bench_router(coli, torch, peaks)
             elif args.workload == "decode_formats":
-                res = bench_decode_formats(coli, torch, peaks)
+                res = bench_decode_formats(coli, torch, peaks, only=args.decode_format)
             elif args.workload == "absorb":
                 res = bench_absorb(coli, torch, peaks,
                                    torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
@@ -676,7 +762,7 @@ def main():
                 res = bench_host(coli, torch, peaks,
                                  torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
             else:
-                res = bench_streaming(coli, torch, peaks)
+                res = bench_streaming(coli, torch, peaks, pool_gb=args.stream_pool_gb, only_fmt=args.stream_fmt)
             print(json.dumps({"workload": args.workload, "result": res}), flush=True)
         return 0
 
@@ -746,14 +832,21 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         v, n, dt = wk.oracle_sample(args.cpu_budget)
         from oracle import oracle as orc
+        prev = orc.set_threads(1)
+        try:
+            v1, n1, dt1 = wk.oracle_sample(min(3.0, args.cpu_budget))
+        finally:
+            orc.set_threads(prev)
         cpu = {"value": v, "unit": "GB/s", "cores": orc.threads(), "kind": "oracle",
-               "sample": f"{n} whole decode steps (8 routed experts each) in {dt:.1f} s"}
+               "sample": f"{n} whole decode steps (8 routed experts each) in {dt:.1f} s",
+               "single_thread": v1, "single_thread_sample": f"{n1} whole decode steps in {dt1:.1f} s"}
 
     by_wl = None
     if rank == 0 and not args.quick:
         l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
         by_wl = {"gemv": bench_gemv(coli, torch, peaks, l2), "moe_prefill": bench_prefill(coli, torch, peaks),
-                 "weight_streaming": bench_streaming(coli, torch, peaks), "router": bench_router(coli, torch, peaks)}
+                 "weight_streaming": bench_streaming(coli, torch, peaks), "router": bench_router(coli, torch, peaks),
+                 "moe_decode_per_format": bench_decode_formats(coli, torch, peaks)}
 
     if rank == 0:
         line = {
@@ -770,7 +863,7 @@ def main():
             "hbm_frac_of_measured": value / peaks["hbm_gbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "peak_source": peaks["source"], "kernel": "moe_decode_mma_kernel<true,0>",
+                         "peak_source": peaks["source"], "kernel": "moe_decode_mma_kernel<1, 0>",
                          "avg_launch_us": avg_launch_s * 1e6, "timing": timing_mode},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": wk.h2d, "d2h_bytes_per_step": wk.d2h},

@@ -101,6 +101,21 @@ int oracle_threads(void)
 #endif
 }
 
+/* Threads of the parallel loops from now on (timing only: every result is the
+ * same at any thread count, each output element being one thread's ordered
+ * sum).  Returns the previous count. */
+int oracle_set_threads(int n)
+{
+    const int prev = oracle_threads();
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return prev;
+}
+
 /* Bytes of one packed row on the host, per the readings above ([Q] for int2). */
 int64_t oracle_row_bytes(int fmt, int64_t I)
 {

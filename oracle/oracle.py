@@ -83,6 +83,8 @@ def lib(mutation: int = 0) -> ctypes.CDLL:
             L.oracle_moe_block.argtypes = [_i64, _i64, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, _ptr,
                                            _ptr, _ptr, _ptr]
             L.oracle_threads.restype = ctypes.c_int
+            L.oracle_set_threads.restype = ctypes.c_int
+            L.oracle_set_threads.argtypes = [ctypes.c_int]
             L.oracle_mutation.restype = ctypes.c_int
             _LIBS[mutation] = L
         return _LIBS[mutation]
@@ -104,6 +106,11 @@ def _scales(scales):
 
 def threads(mutation: int = 0) -> int:
     return int(lib(mutation).oracle_threads())
+
+
+def set_threads(n: int, mutation: int = 0) -> int:
+    """Thread count of the oracle's parallel loops (for timing); returns the previous one."""
+    return int(lib(mutation).oracle_set_threads(int(n)))
 
 
 def row_bytes(fmt: int, I: int, mutation: int = 0) -> int:
