@@ -681,6 +681,25 @@ struct MdArgs {
     int *err;                  // device error word
     long long timeout_ns;      // bound of every wait
 };
+// Streamed S = 1 int4 matvec on the tensor cores (gemv_mma.cu).
+struct GmArgs {
+    const uint8_t *q[GemvJob::MAXM];
+    const float *s[GemvJob::MAXM];
+    float *y[GemvJob::MAXM];
+    int O[GemvJob::MAXM];
+    int stage_start[GemvJob::MAXM + 1];   // prefix of the matrices' stage counts
+    int n, fmt, I, rs, ng, gsh;            // rs: device row stride (bytes); gsh: log2(gs / 64)
+    int nseg, spw, nt;                     // 64-input segments per row and per warp; 16-row tiles per stage
+    int bs, so, ss, slot_bytes;            // stage layout: code-block stride, scale offset and block stride
+    int off_red, off_bar;                  // dynamic shared-memory layout (bytes)
+    const float *x;
+    int *err;
+    long long timeout_ns;
+};
+bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int n_sm, size_t smem_max, GmArgs *a,
+             size_t *smem, int *grid);
+cudaError_t launch_gemv_mma(const GmArgs &a, int grid, size_t smem, cudaStream_t st);
+
 bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int ng_d, int gs_gu, int gs_d, int n_sm,
              size_t smem_max, MdArgs *a, size_t *smem);
 cudaError_t md_occupancy(const MdArgs &a, size_t smem, int *per_sm);

@@ -745,6 +745,13 @@ struct XRegF8 {
     }
 };
 
+// Decoders whose lane unit is several 16-byte chunks (f32: four): chunk j of
+// lane l of a slab sits at (32 j + l) * 16 bytes, so each 16-byte load of a
+// warp reads 512 contiguous bytes (no bank conflicts), and the lane's inputs
+// follow the same interleave.
+template <class XR> struct Interleaved { static constexpr bool value = false; };
+template <> struct Interleaved<XRegF32> { static constexpr bool value = true; };
+
 // Decoders whose scale is per 128 x 128 block (read from global memory by the
 // consumer) instead of per row or per row group (copied with the rows).
 template <class XR> struct BlockScaled { static constexpr bool value = false; };
@@ -776,7 +783,9 @@ __device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v
 // reads the group scale of each 32-input chunk, fmt 1-3 the row scale (both
 // copied with the rows), fmt=7 the scale of the chunk's 128 x 128 block (from
 // global memory, where the whole scale grid stays cached).
-template <int NWC, class XR>
+// NR (1, 2 or 4): rows of a stage each consumer warp multiplies, the stage's
+// rows per slab group rounded up (RG <= NR * G).
+template <int NWC, class XR, int NR>
 __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const GemvJob job, int rpc, int RG,
                                                                          int gshift, long long timeout_ns) {
     constexpr int NCT = NWC * 32, NS = kStreamStages, SB = kStreamStageBytes;
@@ -857,10 +866,19 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
     }
     pdl_wait();
     deadline = global_ns() + (uint64_t)timeout_ns;
+    constexpr bool IL = Interleaved<XR>::value;
+    constexpr int NCH = XR::LB / 16;   // 16-byte chunks of a lane unit (interleaved decoders)
     float4 xraw[XR::NIN / 4];
 #pragma unroll
     for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (sl * 32 + lane < lpr) {
+    if constexpr (IL) {
+        // chunk j of this lane: inputs sl * 32 * NIN + (32 j + lane) * 4 .. + 3 (I is a multiple of 128)
+#pragma unroll
+        for (int j = 0; j < NCH; j++) {
+            const int i0 = sl * 32 * XR::NIN + (32 * j + lane) * 4;
+            if (i0 < job.I) xraw[j] = __ldg(reinterpret_cast<const float4 *>(job.x + i0));
+        }
+    } else if (sl * 32 + lane < lpr) {
         const float4 *p = reinterpret_cast<const float4 *>(job.x + (size_t)(sl * 32 + lane) * XR::NIN);
 #pragma unroll
         for (int j = 0; j < XR::NIN / 4; j++) xraw[j] = __ldg(p + j);
@@ -875,23 +893,45 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
     while (next(sm_, so, sn)) {
         if (warp_wait(&full[s], ph, deadline, &abort_flag, lane)) {
             const uint8_t *src = ring + s * SB;
-            Q qq[4];
-            float sc[4], dd[4];
+            Q qq[NR];
+            float sc[NR], dd[NR];
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
+            for (int k = 0; k < NR; k++) {
                 const int rr = sub + k * G;
                 const bool ok = okc && rr < sn;
-                qq[k] = ok ? *reinterpret_cast<const Q *>(src + rr * rs + c * XR::LB) : Q{};
-                if constexpr (BlockScaled<XR>::value)
+                if constexpr (IL) {
+                    const uint8_t *rb = src + rr * rs + sl * 32 * XR::LB + lane * 16;
+#pragma unroll
+                    for (int j = 0; j < NCH; j++)
+                        reinterpret_cast<uint4 *>(&qq[k])[j] =
+                            (rr < sn && sl * 32 * XR::NIN + (32 * j + lane) * 4 < job.I)
+                                ? *reinterpret_cast<const uint4 *>(rb + j * 512)
+                                : make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    qq[k] = ok ? *reinterpret_cast<const Q *>(src + rr * rs + c * XR::LB) : Q{};
+                }
+                if constexpr (IL)
+                    sc[k] = rr < sn ? 1.f : 0.f;   // (f32: no scales; chunk validity is in the loads)
+                else if constexpr (BlockScaled<XR>::value)
                     sc[k] = ok ? __ldg(job.s[sm_] + (size_t)((so + rr) / kFp8Block) * job.ng[sm_] + (c >> gshift)) : 0.f;
                 else
                     sc[k] = !ok ? 0.f : ng == 0 ? 1.f : *reinterpret_cast<const float *>(src + RG * rs + (rr * ng + (c >> gshift)) * 4);
             }
-            xr.template dotn<4>(qq, dd);
-            const float t = warp_sum4(dd[0] * sc[0], dd[1] * sc[1], dd[2] * sc[2], dd[3] * sc[3], lane);
-            if ((lane & 7) == 0) {
-                const int rr = sub + (lane >> 3) * G;
-                if (rr < sn) red[(job.row_start[sm_] + so + rr - r0) * ns + sl] = t;
+            xr.template dotn<NR>(qq, dd);
+            if constexpr (NR == 1) {
+                float t = dd[0] * sc[0];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0 && sub < sn) red[(job.row_start[sm_] + so + sub - r0) * ns + sl] = t;
+            } else {
+                float v[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) v[k] = k < NR ? dd[k] * sc[k] : 0.f;
+                const float t = warp_sum4(v[0], v[1], v[2], v[3], lane);
+                if ((lane & 7) == 0 && (lane >> 3) < NR) {
+                    const int rr = sub + (lane >> 3) * G;
+                    if (rr < sn) red[(job.row_start[sm_] + so + rr - r0) * ns + sl] = t;
+                }
             }
         } else if (!abort_flag && lane == 0) {
             abort_flag = 1;
@@ -1191,13 +1231,19 @@ cudaError_t launch_stream_gemv(const GemvJob &job, int rpc, int RG, int gshift, 
         return launch_pdl(kern, dim3(grid), dim3((kStreamConsumerWarps + 1) * 32), smem, st, job, rpc, RG, gshift,
                           2000000000LL);
     };
+    // rows of a stage per consumer warp: RG rows over G = warps / slabs-per-row groups
+    const int lpr = (job.I + stream_lane_inputs(job.fmt) - 1) / stream_lane_inputs(job.fmt);
+    const int G = kStreamConsumerWarps / ((lpr + 31) / 32);
+    const int nr = (RG + G - 1) / G;
+    constexpr int W = kStreamConsumerWarps;
     switch (job.fmt) {
-    case 0: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegF32>);
-    case 1: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS1>);
+    case 0: return nr <= 1 ? go(stream_gemv_kernel<W, XRegF32, 1>) : nr <= 2 ? go(stream_gemv_kernel<W, XRegF32, 2>)
+                                                                          : go(stream_gemv_kernel<W, XRegF32, 4>);
+    case 1: return go(stream_gemv_kernel<W, XRegS1, 4>);
     case 2:
-    case 4: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS4>);
-    case 3: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegS3>);
-    case 7: return go(stream_gemv_kernel<kStreamConsumerWarps, XRegF8>);
+    case 4: return go(stream_gemv_kernel<W, XRegS4, 4>);
+    case 3: return go(stream_gemv_kernel<W, XRegS3, 4>);
+    case 7: return go(stream_gemv_kernel<W, XRegF8, 4>);
     default: return cudaErrorInvalidValue;
     }
 }
