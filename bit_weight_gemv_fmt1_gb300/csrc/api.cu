@@ -454,6 +454,7 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
                 }
                 ga.x = x;
                 ga.err = ds->err;
+                if (int rc = decode_counters(ds, st, gm_counter_words(), &ga.ctr)) return rc;
                 e = launch_gemv_mma(ga, ggrid, gsm, st);
                 if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
                 count(1, wbytes);

@@ -693,9 +693,11 @@ struct GmArgs {
     int bs, so, ss, slot_bytes;            // stage layout: code-block stride, scale offset and block stride
     int off_red, off_bar;                  // dynamic shared-memory layout (bytes)
     const float *x;
+    unsigned *ctr;                         // [0] next claimed stage, [1] CTAs out: zero between calls
     int *err;
     long long timeout_ns;
 };
+size_t gm_counter_words();
 bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int n_sm, size_t smem_max, GmArgs *a,
              size_t *smem, int *grid);
 cudaError_t launch_gemv_mma(const GmArgs &a, int grid, size_t smem, cudaStream_t st);

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     __shared__ DecodeRouting rt;
     __shared__ volatile int abort_flag;
     __shared__ float4 s_cf[kMdWarps][kMdSegMax + 1];   // phase-A chain starts of each warp's segments, their sum
-    __shared__ __align__(16) uint8_t s_stg[kMdWarps][528];   // B-fragment staging of each consumer warp, + a zero row
+    __shared__ __align__(16) uint8_t s_stg[kMdWarps][kMdStgBytes];   // B-fragment staging of each consumer warp, + a zero row
     __shared__ float s_part[kMdWarps * 32];                  // the final sum: one (expert, row) per thread
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int SB = a.slot_bytes;
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     uint32_t bfA[kMdSegMax][8];
     float unA = 0.f;
     if (warp < kMdWarps) {
-        uint32_t *zr = reinterpret_cast<uint32_t *>(&s_stg[warp][512]);
+        uint32_t *zr = reinterpret_cast<uint32_t *>(&s_stg[warp][kMdStgZero]);
         if (lane < 4) zr[lane] = 0u;
         __syncwarp();
         const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(zr);
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
         const uint32_t ring_s = smem_addr(base);
         const int g = lane >> 2, t = lane & 3;
         const int blk = g & 3, rib = g >> 2;   // block and row in block of tile row g (row g + 8: rib + 2)
-        const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(&s_stg[warp][512]);
+        const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(&s_stg[warp][kMdStgZero]);
         int i = 0;                              // stage counter
         bool live = true;
         {
@@ -705,8 +705,8 @@ bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int n
     const size_t red_bytes = (size_t)kMdSlots * kMdRedSlot * 4;
     const size_t off_bar = off_red + red_bytes;
     const size_t total = off_bar + kMdSlots * 16 + 3 * kMdSlots * 8 + 128;   // + alignment slack
-    // static shared memory of the kernel: about 15 KB
-    if (total + 16 * 1024 > smem_max || SB > (1u << 30)) return false;
+    // static shared memory of the kernel: about 17 KB
+    if (total + 20 * 1024 > smem_max || SB > (1u << 30)) return false;
     memset(a, 0, sizeof *a);
     // CTAs of the expert finished last (md_share), for each possible number of
     // routed experts: the balance of expert 0's owners, which start at q + 2

@@ -4,8 +4,11 @@
 // coli_matmul_multi at S = 1; the pages' mm_gemv / matmul_i4_grouped).
 //
 // The rows of all matrices of a call form one list of stages; a stage is NT
-// tiles of 16 consecutive rows of one matrix, and CTA c owns a contiguous
-// range of stages.  Warps 0..15 consume, warp 16 produces (its lane 0 copies
+// tiles of 16 consecutive rows of one matrix.  CTA c takes stages c, c + G
+// and c + 2 G (the ones it can prefetch before the previous kernel ends), then
+// claims the rest one at a time from a counter in device memory, so that the
+// CTAs finish together however the bandwidth falls among them; the last CTA
+// out clears the counter for the next call.  Warps 0..15 consume, warp 16 produces (its lane 0 copies
 // each stage's rows and row scales into one of three shared-memory slots with
 // bulk copies), warp 17 finishes a stage: it sums the consumer warps' shares
 // of each row in warp order and writes y.  The dot products are the
@@ -13,9 +16,12 @@
 // segments [w S, (w + 1) S) of every row and builds their B fragments from x
 // once per call.
 //
-// Back-to-back calls: the producer issues its first stages (weights only,
-// which no kernel writes) before waiting for the previous kernel in the
-// stream (griddepcontrol.wait); x is read and y written only after that wait.
+// Back-to-back calls: every CTA lets the next kernel in the stream launch as
+// soon as it starts (griddepcontrol.launch_dependents; one CTA fills an SM, so
+// the next kernel's CTAs take SMs only as this kernel frees them), and the
+// producer issues its first stages (weights only, which no kernel writes)
+// before waiting for the previous kernel (griddepcontrol.wait); x is read and
+// y written only after that wait.
 // Every wait is bounded; on expiry the kernel records DEV_ERR_TIMEOUT.
 #include <algorithm>
 #include <cstring>
@@ -37,7 +43,7 @@ constexpr int kGmStageMax = 48;              // rows of a stage (NT <= 3 tiles)
 constexpr int kGmRedSlot = kGmStageMax * kGmRedB;
 constexpr uint32_t kGmNapE = 64, kGmNapP = 64;
 
-// d.x: matrix, d.y: first row, d.z: rows
+// Stage k: d.x = matrix, d.y = first row, d.z = rows (d.z = 0: no stage, the end).
 __device__ __forceinline__ int4 gm_stage(const GmArgs &a, int k) {
     int m = 0;
     while (k >= a.stage_start[m + 1]) m++;
@@ -52,19 +58,18 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
     extern __shared__ uint8_t sraw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)sraw + 127) & ~(uintptr_t)127);
     float *red = reinterpret_cast<float *>(base + a.off_red);   // [slot][row][kGmRedB]
-    uint64_t *full = reinterpret_cast<uint64_t *>(base + a.off_bar);
+    int4 *desc = reinterpret_cast<int4 *>(base + a.off_bar);   // [slot]: the stage it holds
+    uint64_t *full = reinterpret_cast<uint64_t *>(desc + kGmSlots);
     uint64_t *empty = full + kGmSlots;
     uint64_t *redfull = empty + kGmSlots;
     __shared__ volatile int abort_flag;
     __shared__ float4 s_cf[kMdWarps][kMdSegMax + 1];          // chain starts of each warp's segments, their sum
-    __shared__ __align__(16) uint8_t s_stg[kMdWarps][528];   // B-fragment staging of each consumer warp, + a zero row
+    __shared__ __align__(16) uint8_t s_stg[kMdWarps][kMdStgBytes];   // B-fragment staging of each consumer warp, + a zero row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int SB = a.slot_bytes;
     uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
     const int S = a.stage_start[a.n];
     const int G = gridDim.x;
-    const int k0 = (int)((long long)S * blockIdx.x / G), k1 = (int)((long long)S * (blockIdx.x + 1) / G);
-    const int nk = k1 - k0;
 
     if (tid == 0) {
         abort_flag = 0;
@@ -76,6 +81,10 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // one CTA fills an SM, so the next kernel's CTAs cannot sit beside this
+    // one: let it launch now, and each of its CTAs starts (and prefetches its
+    // weights) on the first SM this kernel frees
+    pdl_trigger();
     auto fail = [&]() {
         if (!abort_flag) {
             abort_flag = 1;
@@ -84,23 +93,39 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
     };
 
     if (warp == kMdWarps) {
-        // ---------------- producer: stage i of the CTA into slot i % kGmSlots
+        // ---------------- producer: stage i of the CTA into slot i % kGmSlots; an
+        // end marker (a descriptor with no rows, no bytes) after the last one
         if (lane == 0) {
             const int rs = a.rs;
             int i = 0;
-            for (; i < nk; i++) {
+            bool ok = true;
+            while (true) {
                 const int s = i % kGmSlots;
-                if (i == kGmSlots) {
-                    // the ring is full: from here on the consumers (past the
-                    // previous kernel) pace the copies
-                    pdl_wait();
-                    deadline = global_ns() + (uint64_t)a.timeout_ns;
+                int k;
+                if (i < kGmSlots) {
+                    k = (int)blockIdx.x + G * i;
+                } else {
+                    if (i == kGmSlots) {
+                        // the prefetched round is issued: the rest needs the
+                        // previous kernel to be complete (the shared counter)
+                        pdl_wait();
+                        deadline = global_ns() + (uint64_t)a.timeout_ns;
+                    }
+                    k = 3 * G + (int)atomicAdd(a.ctr, 1u);
                 }
                 if (i >= kGmSlots && !md_wait1(&empty[s], ((i / kGmSlots) & 1) ^ 1, deadline, &abort_flag, kGmNapP)) {
                     fail();
+                    ok = false;
                     break;
                 }
-                const int4 d = gm_stage(a, k0 + i);
+                if (k >= S) {
+                    desc[s] = make_int4(0, 0, 0, 0);
+                    mbar_arrive(&full[s]);   // end marker
+                    i++;
+                    break;
+                }
+                const int4 d = gm_stage(a, k);
+                desc[s] = d;
                 uint8_t *dst = base + (size_t)s * SB;
                 uint32_t tx = 0;
                 int cnt[4];
@@ -118,13 +143,21 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
                     if (GROUPED)
                         bulk_load(dst + a.so + b * a.ss, a.s[d.x] + r * a.ng, (uint32_t)(cnt[b] * a.ng * 4), &full[s]);
                 }
+                i++;
             }
-            if (i < kGmSlots) pdl_wait();
-            pdl_trigger();
+            if (i <= kGmSlots) pdl_wait();
             // every copy issued has landed before the CTA may exit
             const uint64_t dl2 = global_ns() + 200000000ull;
             volatile int no_abort = 0;
             for (int q = max(0, i - kGmSlots); q < i; q++) mbar_wait(&full[q % kGmSlots], (q / kGmSlots) & 1, dl2, &no_abort);
+            (void)ok;
+            // the last CTA out clears the stage counter and itself for the next call
+            __threadfence();
+            if (atomicAdd(a.ctr + 1, 1u) == (unsigned)G - 1) {
+                a.ctr[0] = 0u;
+                a.ctr[1] = 0u;
+                __threadfence();
+            }
         }
         return;
     }
@@ -134,14 +167,19 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
         pdl_wait();
         deadline = global_ns() + (uint64_t)a.timeout_ns;
         bool ok = true;
-        for (int i = 0; i < nk; i++) {
+        for (int i = 0;; i++) {
             const int s = i % kGmSlots;
             const uint32_t par = (uint32_t)((i / kGmSlots) & 1);
+            if (!md_wait(&full[s], par, deadline, &abort_flag, kGmNapE)) {
+                ok = false;
+                break;
+            }
+            const int4 d = desc[s];
+            if (d.z == 0) break;
             if (!md_wait(&redfull[s], par, deadline, &abort_flag, kGmNapE)) {
                 ok = false;
                 break;
             }
-            const int4 d = gm_stage(a, k0 + i);
             const float *rd = red + s * kGmRedSlot;
             float v[2] = {0.f, 0.f};
 #pragma unroll
@@ -172,7 +210,6 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
             }
         }
         if (!ok && lane == 0) fail();
-        pdl_trigger();
         return;
     }
 
@@ -187,7 +224,7 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
         float4 ld[NRD];
 #pragma unroll
         for (int r = 0; r < NRD; r++) ld[r] = md_load4(a.x, a.I, q0, nq, r, lane, false);
-        uint32_t *zr = reinterpret_cast<uint32_t *>(&s_stg[warp][512]);
+        uint32_t *zr = reinterpret_cast<uint32_t *>(&s_stg[warp][kMdStgZero]);
         if (lane < 4) zr[lane] = 0u;
         __syncwarp();
         const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(zr);
@@ -218,12 +255,13 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
     const uint32_t sofs = (uint32_t)(a.so + blk * a.ss + rib * a.ng * 4 + (q0 >> GSH) * 4);
     const uint32_t cfs = smem_addr(&s_cf[warp][0]);
     const bool fullw = nq == SEG;
-    for (int i = 0; i < nk; i++) {
+    for (int i = 0;; i++) {
         const int s = i % kGmSlots;
         if (!md_wait(&full[s], (uint32_t)((i / kGmSlots) & 1), deadline, &abort_flag, 0)) {
             if (lane == 0) fail();
             break;
         }
+        if (desc[s].z == 0) break;   // end marker
         const uint32_t sb = ring_s + (uint32_t)(s * SB);
         // tile row m = g, g + 8 of tile T is stage row 4 NT (m % 4) + 4 T + m / 4
         float *rw = red + s * kGmRedSlot + (blk * 4 * NT + rib) * kGmRedB + warp;
@@ -244,7 +282,6 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
         __syncwarp();
         if (lane == 0) mbar_arrive(&redfull[s]);
     }
-    pdl_trigger();
 }
 
 size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
@@ -308,8 +345,8 @@ bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int n_
     const size_t SB = round_up(so + 4 * ss, 128);
     const size_t off_red = kGmSlots * SB;
     const size_t off_bar = off_red + (size_t)kGmSlots * kGmRedSlot * 4;
-    const size_t total = off_bar + 3 * kGmSlots * 8 + 128;   // + alignment slack
-    if (total + 12 * 1024 > smem_max) return false;           // static shared memory: about 10 KB
+    const size_t total = off_bar + kGmSlots * 16 + 3 * kGmSlots * 8 + 128;   // + alignment slack
+    if (total + 16 * 1024 > smem_max) return false;           // static shared memory: about 11 KB
     a->fmt = fmt;
     a->I = I;
     a->rs = rs;
@@ -329,6 +366,8 @@ bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int n_
     *grid = std::min(n_sm, a->stage_start[n]);
     return true;
 }
+
+size_t gm_counter_words() { return 2; }
 
 cudaError_t launch_gemv_mma(const GmArgs &a, int grid, size_t smem, cudaStream_t st) {
     const bool g = a.fmt == 4;

@@ -28,6 +28,13 @@ namespace coli {
 
 constexpr int kMdWarps = 16;     // consumer warps of the tensor-core matvec kernels
 constexpr int kMdSegMax = 6;     // 64-input segments per warp and row (rows of up to 6144 inputs)
+// B-fragment staging area of a warp (md_frags): four blocks of eight 16-byte
+// rows, 144 bytes apart, so that the 2-byte stores of one instruction, which
+// hit row r of all four blocks, fall in four different bank quarters; then
+// one all-zero row
+constexpr int kMdStgBlock = 144;
+constexpr int kMdStgZero = 4 * kMdStgBlock;
+constexpr int kMdStgBytes = kMdStgZero + 16;
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 v;
@@ -145,7 +152,7 @@ __device__ __forceinline__ MdScale md_scale(const float4 (&ld)[NR]) {
 // inputs 4 L + 0..3 of the round).  nq = the warp's segments left from this
 // round on.
 //   Each lane converts its values to the hi / lo f16 halves and stores them
-//   into the warp's staging area `stg` (512 bytes) as the rows of the
+//   into the warp's staging area `stg` (kMdStgZero bytes) as the rows of the
 //   transposed B operands: for every B operand (segment, k-step, P or Q) and
 //   every half of its 16 k-slots, row 0 holds the hi column and row 1 the lo
 //   column, 8 slots of 2 bytes each.  ldmatrix then hands every lane its
@@ -164,17 +171,23 @@ __device__ __forceinline__ void md_frags(float4 ld, MdScale sc, int nq, int lane
     // store: lane L = 16 seg + 4 t + 2 i + h holds j = 4 h + 0..3
     {
         const int seg = lane >> 4, t = (lane >> 2) & 3, i = (lane >> 1) & 1, h = lane & 1;
-        const uint32_t wb = stg + (uint32_t)(((seg * 2 + i) * 2) * 64 + (2 * t + h) * 2);
+        const uint32_t wb = stg + (uint32_t)((seg * 2 + i) * kMdStgBlock + (2 * t + h) * 2);
         const float v[4] = {ld.x, ld.y, ld.z, ld.w};
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             // q = j % 4: operand P (q < 2) or Q, slot half q % 2 (the 16 n slots for odd q)
             const float sv = v[q] * sc.s2k * ((q & 1) ? 0.0625f : 1.f);
-            const __half hi = __float2half_rn(sv);
-            const __half lo = __float2half_rn((sv - __half2float(hi)) * 2048.f);
+            // hi: sv rounded to 11 significant bits, to nearest even, in integer
+            // arithmetic (the f16 value of sv wherever that is a normal f16);
+            // lo: the remainder times 2^11.  One conversion packs both halves.
+            const uint32_t b = __float_as_uint(sv);
+            const float h32 = __uint_as_float((b + 0xFFFu + ((b >> 13) & 1u)) & 0xFFFFE000u);
+            const float l32 = (sv - h32) * 2048.f;
+            uint32_t pk;
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(h32), "f"(l32));   // hi in the upper half
             const uint32_t ad = wb + (uint32_t)((((q >> 1) * 2 + (q & 1)) * 2) * 16);
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(ad), "h"(__half_as_ushort(hi)));
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(ad + 16), "h"(__half_as_ushort(lo)));
+            asm volatile("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %0;\n st.shared.u16 [%1], h;\n st.shared.u16 [%2], l;\n}"
+                         ::"r"(pk), "r"(ad), "r"(ad + 16));
         }
     }
     __syncwarp();
@@ -187,7 +200,8 @@ __device__ __forceinline__ void md_frags(float4 ld, MdScale sc, int nq, int lane
         const bool on = sg < nq;
 #pragma unroll
         for (int i = 0; i < 2; i++) {
-            const uint32_t ra = mr < 2 ? stg + (uint32_t)(((((sg * 2 + i) * 2 + (mq >> 1)) * 2 + (mq & 1)) * 2 + mr) * 16)
+            const uint32_t ra = mr < 2 ? stg + (uint32_t)((sg * 2 + i) * kMdStgBlock +
+                                                          ((((mq >> 1) * 2 + (mq & 1)) * 2 + mr) * 16))
                                        : zrow;
             uint32_t r0, r1, r2, r3;
             asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"

@@ -812,6 +812,9 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // one CTA fills an SM (its ring takes most of the shared memory): the next
+    // kernel may launch now; its CTAs start as this kernel frees SMs
+    pdl_trigger();
     // scales copied with each row: none for f32 and for block-scaled FP8
     const int ng = job.fmt == 4 ? job.ng[0] : (job.fmt == 0 || BlockScaled<XR>::value) ? 0 : 1;
     const long long rs = job.rs[0];
@@ -857,7 +860,6 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
                     ph ^= 1;
                 }
             }
-            pdl_trigger();
             const uint64_t dl2 = global_ns() + 200000000ull;
             volatile int no_abort = 0;
             for (int k = max(0, it - NS); k < it; k++) mbar_wait(&full[k % NS], (k / NS) & 1, dl2, &no_abort);
@@ -944,7 +946,6 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) stream_gemv_kernel(const Ge
             ph ^= 1;
         }
     }
-    pdl_trigger();
     named_sync(1, NCT);
     for (int rr = tid; rr < r1 - r0; rr += NCT) {
         float acc = 0.f;
