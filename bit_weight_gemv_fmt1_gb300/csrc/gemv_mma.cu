@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
     uint64_t *redfull = empty + kGmSlots;
     __shared__ volatile int abort_flag;
     __shared__ float4 s_cf[kMdWarps][kMdSegMax + 1];          // chain starts of each warp's segments, their sum
-    __shared__ __align__(16) uint8_t s_stg[kMdWarps][kMdStgBytes];   // B-fragment staging of each consumer warp, + a zero row
+    // B-fragment staging of each consumer warp: one area per round, then a zero row
+    __shared__ __align__(16) uint8_t s_stg[kMdWarps][(SEG / 2) * kMdStgZero + 16];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int SB = a.slot_bytes;
     uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
@@ -224,17 +225,18 @@ __global__ void __launch_bounds__(kGmThreads, 1) gemv_mma_kernel(const GmArgs a)
         float4 ld[NRD];
 #pragma unroll
         for (int r = 0; r < NRD; r++) ld[r] = md_load4(a.x, a.I, q0, nq, r, lane, false);
-        uint32_t *zr = reinterpret_cast<uint32_t *>(&s_stg[warp][kMdStgZero]);
+        uint32_t *zr = reinterpret_cast<uint32_t *>(&s_stg[warp][NRD * kMdStgZero]);
         if (lane < 4) zr[lane] = 0u;
         __syncwarp();
         const uint32_t stg = smem_addr(&s_stg[warp][0]), zrow = smem_addr(zr);
         const MdScale sc = md_scale<NRD>(ld);
         un = sc.unscale * 0x1p24f;
         float4 cft = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 cs[SEG];
+        md_frags_n<NRD>(ld, sc, nq, lane, stg, zrow, bf, cs);
 #pragma unroll
         for (int r = 0; r < NRD; r++) {
-            float4 c0, c1;
-            md_frags(ld[r], sc, nq - 2 * r, lane, stg, zrow, bf[2 * r], bf[2 * r + 1], c0, c1);
+            const float4 c0 = cs[2 * r], c1 = cs[2 * r + 1];
             if (lane == 0) {
                 s_cf[warp][2 * r] = c0;
                 s_cf[warp][2 * r + 1] = c1;
@@ -346,7 +348,9 @@ bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int n_
     const size_t off_red = kGmSlots * SB;
     const size_t off_bar = off_red + (size_t)kGmSlots * kGmRedSlot * 4;
     const size_t total = off_bar + kGmSlots * 16 + 3 * kGmSlots * 8 + 128;   // + alignment slack
-    if (total + 16 * 1024 > smem_max) return false;           // static shared memory: about 11 KB
+    // static shared memory: about 30 KB with six segments per warp (three
+    // staging areas per warp), 11 KB with two
+    if (total + (spw > 2 ? 31 : 12) * 1024 > smem_max) return false;
     a->fmt = fmt;
     a->I = I;
     a->rs = rs;

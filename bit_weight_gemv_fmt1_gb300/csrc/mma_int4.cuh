@@ -166,32 +166,34 @@ __device__ __forceinline__ MdScale md_scale(const float4 (&ld)[NR]) {
 //   quad (hi, lo, hi, lo) of the tile rows: four mma of the fragments with the
 //   constant A = -8 * 2^-24 (-128 * 2^-24 on the 16 n slots), exact f16
 //   subnormals.
-__device__ __forceinline__ void md_frags(float4 ld, MdScale sc, int nq, int lane, uint32_t stg, uint32_t zrow,
-                                         uint32_t (&b0)[8], uint32_t (&b1)[8], float4 &c0, float4 &c1) {
+// The parts of md_frags (below): the lane's stores of one round into a
+// staging area, the ldmatrix loads of a round's fragments, and the chain
+// starts of a round.
+__device__ __forceinline__ void md_frag_store(float4 ld, MdScale sc, int lane, uint32_t stg) {
     // store: lane L = 16 seg + 4 t + 2 i + h holds j = 4 h + 0..3
-    {
-        const int seg = lane >> 4, t = (lane >> 2) & 3, i = (lane >> 1) & 1, h = lane & 1;
-        const uint32_t wb = stg + (uint32_t)((seg * 2 + i) * kMdStgBlock + (2 * t + h) * 2);
-        const float v[4] = {ld.x, ld.y, ld.z, ld.w};
+    const int seg = lane >> 4, t = (lane >> 2) & 3, i = (lane >> 1) & 1, h = lane & 1;
+    const uint32_t wb = stg + (uint32_t)((seg * 2 + i) * kMdStgBlock + (2 * t + h) * 2);
+    const float v[4] = {ld.x, ld.y, ld.z, ld.w};
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            // q = j % 4: operand P (q < 2) or Q, slot half q % 2 (the 16 n slots for odd q)
-            const float sv = v[q] * sc.s2k * ((q & 1) ? 0.0625f : 1.f);
-            // hi: sv rounded to 11 significant bits, to nearest even, in integer
-            // arithmetic (the f16 value of sv wherever that is a normal f16);
-            // lo: the remainder times 2^11.  One conversion packs both halves.
-            const uint32_t b = __float_as_uint(sv);
-            const float h32 = __uint_as_float((b + 0xFFFu + ((b >> 13) & 1u)) & 0xFFFFE000u);
-            const float l32 = (sv - h32) * 2048.f;
-            uint32_t pk;
-            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(h32), "f"(l32));   // hi in the upper half
-            const uint32_t ad = wb + (uint32_t)((((q >> 1) * 2 + (q & 1)) * 2) * 16);
-            asm volatile("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %0;\n st.shared.u16 [%1], h;\n st.shared.u16 [%2], l;\n}"
-                         ::"r"(pk), "r"(ad), "r"(ad + 16));
-        }
+    for (int q = 0; q < 4; q++) {
+        // q = j % 4: operand P (q < 2) or Q, slot half q % 2 (the 16 n slots for odd q)
+        const float sv = v[q] * sc.s2k * ((q & 1) ? 0.0625f : 1.f);
+        // hi: sv rounded to 11 significant bits, to nearest even, in integer
+        // arithmetic (the f16 value of sv wherever that is a normal f16);
+        // lo: the remainder times 2^11.  One conversion packs both halves.
+        const uint32_t b = __float_as_uint(sv);
+        const float h32 = __uint_as_float((b + 0xFFFu + ((b >> 13) & 1u)) & 0xFFFFE000u);
+        const float l32 = (sv - h32) * 2048.f;
+        uint32_t pk;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(h32), "f"(l32));   // hi in the upper half
+        const uint32_t ad = wb + (uint32_t)((((q >> 1) * 2 + (q & 1)) * 2) * 16);
+        asm volatile("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %0;\n st.shared.u16 [%1], h;\n st.shared.u16 [%2], l;\n}"
+                     ::"r"(pk), "r"(ad), "r"(ad + 16));
     }
-    __syncwarp();
-    // load: matrix q of ldmatrix.x4 = (operand q / 2, slot half q % 2); lane L
+}
+__device__ __forceinline__ void md_frag_load(int nq, int lane, uint32_t stg, uint32_t zrow, uint32_t (&b0)[8],
+                                             uint32_t (&b1)[8]) {
+    // matrix q of ldmatrix.x4 = (operand q / 2, slot half q % 2); lane L
     // gives row L % 8 of matrix L / 8: column 0 (hi) or 1 (lo), else zeros
     const int mq = lane >> 3, mr = lane & 7;
 #pragma unroll
@@ -213,7 +215,9 @@ __device__ __forceinline__ void md_frags(float4 ld, MdScale sc, int nq, int lane
             bf[4 * i + 3] = on ? r3 : 0u;
         }
     }
-    __syncwarp();   // the staging area may be rewritten after this
+}
+__device__ __forceinline__ void md_frag_starts(const uint32_t (&b0)[8], const uint32_t (&b1)[8], float4 &c0,
+                                               float4 &c1) {
     const uint32_t e8 = 0x80088008u, e128 = 0x80808080u;   // -8 and -128 times 2^-24, two f16 each
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -223,6 +227,31 @@ __device__ __forceinline__ void md_frags(float4 ld, MdScale sc, int nq, int lane
     }
     c0 = make_float4(d0[0], d0[1], d0[2], d0[3]);
     c1 = make_float4(d1[0], d1[1], d1[2], d1[3]);
+}
+
+__device__ __forceinline__ void md_frags(float4 ld, MdScale sc, int nq, int lane, uint32_t stg, uint32_t zrow,
+                                         uint32_t (&b0)[8], uint32_t (&b1)[8], float4 &c0, float4 &c1) {
+    md_frag_store(ld, sc, lane, stg);
+    __syncwarp();
+    md_frag_load(nq, lane, stg, zrow, b0, b1);
+    __syncwarp();   // the staging area may be rewritten after this
+    md_frag_starts(b0, b1, c0, c1);
+}
+
+// md_frags for NR rounds at once, each with its own staging area (stg +
+// r * kMdStgZero): all the stores, then all the loads, then all the chain
+// starts, so that the rounds' latencies overlap.  nq: the warp's segments.
+template <int NR>
+__device__ __forceinline__ void md_frags_n(const float4 (&ld)[NR], MdScale sc, int nq, int lane, uint32_t stg,
+                                           uint32_t zrow, uint32_t (&bf)[2 * NR][8], float4 (&c)[2 * NR]) {
+#pragma unroll
+    for (int r = 0; r < NR; r++) md_frag_store(ld[r], sc, lane, stg + (uint32_t)(r * kMdStgZero));
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < NR; r++) md_frag_load(nq - 2 * r, lane, stg + (uint32_t)(r * kMdStgZero), zrow, bf[2 * r], bf[2 * r + 1]);
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < NR; r++) md_frag_starts(bf[2 * r], bf[2 * r + 1], c[2 * r], c[2 * r + 1]);
 }
 
 // A warp's share of one phase-A stage: its segments of the 16 tile rows.
