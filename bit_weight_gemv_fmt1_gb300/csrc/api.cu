@@ -1127,7 +1127,16 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         const size_t sz_tile = al((size_t)max_tiles * 4);
         const size_t sz_px = al((size_t)3 * rows_alloc * H_pad * 2), sz_gu = al((size_t)n_slots * 2 * F * 4);
         const size_t sz_ph = al((size_t)3 * rows_alloc * F_pad * 2), sz_out = al((size_t)n_slots * H * 4);
-        const size_t total = sz_off + 2 * sz_ord + 3 * sz_tile + 256 + sz_px + sz_gu + sz_ph + sz_out;
+        // experts with at most kSmallRows rows: groups of up to 4 rows on the mma.sync path (moe_small.cu)
+        constexpr int kSmallRows = 12;
+        SmArgs sgu, sdn;
+        size_t smem_gu = 0, smem_dn = 0;
+        const bool small = sm_plan(false, fmt, g0->gs, (int)H, (int)F, (int)g0->rs, g0->ng, (size_t)ds->smem_optin,
+                                   &sgu, &smem_gu) &&
+                           sm_plan(true, fmt, mi.d0->gs, (int)F, (int)H, (int)mi.d0->rs, mi.d0->ng,
+                                   (size_t)ds->smem_optin, &sdn, &smem_dn);
+        const size_t sz_sg = al((size_t)n_slots * 4);
+        const size_t total = sz_off + 2 * sz_ord + 3 * sz_tile + 256 + sz_px + sz_gu + sz_ph + sz_out + 3 * sz_sg;
         Workspace *ws = nullptr;
         if (int rc = workspace(ds, st, total, &ws)) return rc;
         char *p = (char *)ws->buf;
@@ -1143,8 +1152,12 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         void *px = p; p += sz_px;
         float *gu = (float *)p; p += sz_gu;
         void *ph = p; p += sz_ph;
-        float *slot_out = (float *)p;
-        CU(cudaMemsetAsync(flags, 0, 2 * sizeof(int), st), "cudaMemsetAsync(flags)");
+        float *slot_out = (float *)p; p += sz_out;
+        int32_t *sg_e = (int32_t *)p; p += sz_sg;
+        int32_t *sg_p0 = (int32_t *)p; p += sz_sg;
+        int32_t *sg_n = (int32_t *)p;
+        int32_t *n_sg = flags + 4;   // the small-group count, beside the plane flags (one zeroed block)
+        CU(cudaMemsetAsync(flags, 0, 8 * sizeof(int), st), "cudaMemsetAsync(flags)");
 
         RouteArgs r;
         memset(&r, 0, sizeof r);
@@ -1152,9 +1165,26 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         r.offsets = offsets; r.order = order; r.inv = inv;
         r.tile_e = te; r.tile_p0 = tp0; r.tile_p1 = tp1; r.n_tiles = ntiles;
         r.tile_rows = TR;
+        r.small_rows = small ? kSmallRows : 0;
+        r.sg_e = sg_e; r.sg_p0 = sg_p0; r.sg_n = sg_n; r.n_sg = n_sg;
         r.err = ds->err;
         cudaError_t e = launch_route(r, st);
         if (e != cudaSuccess) return cuda_fail(e, "routing launch");
+        int n_launch = 6;
+        if (small) {
+            for (SmArgs *sa : {&sgu, &sdn}) {
+                sa->table = table;
+                sa->sg_e = sg_e; sa->sg_p0 = sg_p0; sa->sg_n = sg_n; sa->n_sg = n_sg;
+                sa->err = ds->err;
+            }
+            sgu.x = x; sgu.ldx = H; sgu.order = order; sgu.K = K;
+            sgu.out = gu; sgu.ldo = 2 * F;
+            sdn.gu = gu;
+            sdn.out = slot_out; sdn.ldo = H;
+            e = launch_moe_small(sgu, ds->n_sm, smem_gu, st);
+            if (e != cudaSuccess) return cuda_fail(e, "small-expert gate/up launch");
+            n_launch++;
+        }
         e = launch_gather_planes(x, H, order, K, offsets + n_experts, n_slots, (int)H, H_pad, px,
                                  (long long)rows_alloc * H_pad, &flags[0], st);
         if (e != cudaSuccess) return cuda_fail(e, "activation planes launch");
@@ -1199,9 +1229,14 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         d.ldo = H;
         e = launch_gemm_tc(d, maph, max_tiles, ds->n_sm, st);
         if (e != cudaSuccess) return cuda_fail(e, "down tensor-core launch");
+        if (small) {
+            e = launch_moe_small(sdn, ds->n_sm, smem_dn, st);
+            if (e != cudaSuccess) return cuda_fail(e, "small-expert down launch");
+            n_launch++;
+        }
         e = launch_combine(slot_out, inv, w, S, K, (int)H, y, st);
         if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-        count(6, 0);
+        count(n_launch, 0);
         return COLI_OK;
     }
 

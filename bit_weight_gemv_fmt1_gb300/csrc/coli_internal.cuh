@@ -575,6 +575,10 @@ struct RouteArgs {
     int32_t *inv;             // [S*K] slot -> position or -1 (may be NULL)
     int32_t *tile_e, *tile_p0, *tile_p1, *n_tiles;   // may be NULL
     int tile_rows;
+    // experts with at most small_rows rows (0: none) go to the small-row list
+    // instead, in groups of up to 4 consecutive rows (moe_small.cu)
+    int small_rows;
+    int32_t *sg_e, *sg_p0, *sg_n, *n_sg;
     int *err;
 };
 
@@ -701,6 +705,26 @@ size_t gm_counter_words();
 bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int n_sm, size_t smem_max, GmArgs *a,
              size_t *smem, int *grid);
 cudaError_t launch_gemv_mma(const GmArgs &a, int grid, size_t smem, cudaStream_t st);
+
+// Prefill products of the experts with few rows (moe_small.cu).
+struct SmArgs {
+    const ExpertDesc *table;
+    const int32_t *sg_e, *sg_p0, *sg_n, *n_sg;   // groups of up to 4 rows (routing kernel)
+    const float *x;                              // gate|up: activations, row stride ldx, token of row p = order[p] / K
+    long long ldx;
+    const int32_t *order;
+    int K;
+    const float *gu;                             // down: the gate|up results [rows][2 I]
+    float *out;                                  // gate|up: gu [rows][2 O]; down: slot outputs [rows][O]
+    long long ldo;
+    int down, fmt, I, O, rs, ng, gsh;
+    int nseg, spw, nt, n_mat, nb;                // segments per row / warp, tiles per stage, matrices, row blocks
+    int bs, so, ss, slot_bytes, off_red, off_stg, off_bar;
+    int *err;
+    long long timeout_ns;
+};
+bool sm_plan(bool down, int fmt, int gs, int I, int O, int rs, int ng, size_t smem_max, SmArgs *a, size_t *smem);
+cudaError_t launch_moe_small(const SmArgs &a, int grid, size_t smem, cudaStream_t st);
 
 bool md_plan(int fmt, int H, int F, int K, int rs_gu, int rs_d, int ng_gu, int ng_d, int gs_gu, int gs_d, int n_sm,
              size_t smem_max, MdArgs *a, size_t *smem);

@@ -260,7 +260,8 @@ __device__ __forceinline__ void md_frags_n(const float4 (&ld)[NR], MdScale sc, i
 //   (hi, lo, hi, lo) per segment and one more for the sum over segments;
 //   sq: scale of row g for segment 0, sr2: bytes to row g + 8's scale.
 // FULL: the warp owns all kMdSegMax segments (no per-segment tests).
-template <bool GROUPED, int GSH, bool FULL, int SEG = kMdSegMax>
+// CFST: bytes between the chain starts of consecutive segments.
+template <bool GROUPED, int GSH, bool FULL, int SEG = kMdSegMax, int CFST = 16>
 __device__ __forceinline__ void md_tileA(float (&y)[4], uint32_t cq, uint32_t rs2, uint32_t cfs, uint32_t sq,
                                          uint32_t sr2, int nq, const uint32_t (&bf)[SEG][8]) {
     if (GROUPED) {
@@ -270,7 +271,7 @@ __device__ __forceinline__ void md_tileA(float (&y)[4], uint32_t cq, uint32_t rs
             if (FULL || q < nq) {
                 const uint2 cg = lds64(cq + 32 * q), ch = lds64(cq + rs2 + 32 * q);
                 float dd[4];
-                md_segment_c(dd, cg, ch, bf[q], lds128f(cfs + 16 * q));
+                md_segment_c(dd, cg, ch, bf[q], lds128f(cfs + CFST * q));
                 const float sg = md_ldsf(sq + 4 * (q >> GSH)), sh = md_ldsf(sq + sr2 + 4 * (q >> GSH));
                 y[0] = fmaf(sg, dd[0], y[0]);
                 y[1] = fmaf(sg, dd[1], y[1]);
@@ -282,7 +283,7 @@ __device__ __forceinline__ void md_tileA(float (&y)[4], uint32_t cq, uint32_t rs
         // two chains (even and odd segments) over the row
         float z[4];
         const uint2 cg0 = lds64(cq), ch0 = lds64(cq + rs2);
-        md_segment_c(y, cg0, ch0, bf[0], lds128f(cfs + 16 * kMdSegMax));
+        md_segment_c(y, cg0, ch0, bf[0], lds128f(cfs + CFST * kMdSegMax));
         if (SEG > 1 && (FULL || nq > 1)) {
             const uint2 cg1 = lds64(cq + 32), ch1 = lds64(cq + rs2 + 32);
             md_segment_c(z, cg1, ch1, bf[SEG > 1 ? 1 : 0], make_float4(0.f, 0.f, 0.f, 0.f));

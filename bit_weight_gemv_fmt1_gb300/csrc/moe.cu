@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
         if (tid == 0) {
             atomicCAS(a.err, 0, DEV_ERR_BAD_ID);
             if (a.n_tiles) *a.n_tiles = 0;
+            if (a.n_sg) *a.n_sg = 0;
         }
         for (int e = tid; e <= a.E; e += blockDim.x) a.offsets[e] = 0;
         for (int t = tid; t < n && a.inv; t += blockDim.x) a.inv[t] = -1;
@@ -326,12 +327,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
             __syncwarp();
         }
     }
-    // tile list: ceil(count / tile_rows) tiles per expert, in expert order
+    // tile list: ceil(count / tile_rows) tiles per expert, in expert order;
+    // experts of at most small_rows rows: groups of up to 4 rows instead
     if (a.n_tiles) {
         __syncthreads();
         if (tid == 0) {
-            int nt = 0;
+            int nt = 0, ng = 0;
             for (int e = 0; e < a.E; e++) {
+                const int c = base[e + 1] - base[e];
+                if (c > 0 && c <= a.small_rows) {
+                    for (int p = base[e]; p < base[e + 1]; p += 4) {
+                        a.sg_e[ng] = e;
+                        a.sg_p0[ng] = p;
+                        a.sg_n[ng] = min(4, base[e + 1] - p);
+                        ng++;
+                    }
+                    continue;
+                }
                 for (int p = base[e]; p < base[e + 1]; p += a.tile_rows) {
                     a.tile_e[nt] = e;
                     a.tile_p0[nt] = p;
@@ -340,6 +352,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
                 }
             }
             *a.n_tiles = nt;
+            if (a.n_sg) *a.n_sg = ng;
         }
     }
 }

@@ -290,3 +290,37 @@ def test_block_table_handle_keeps_one_plan_per_K():
         ids, w = wl.routing_topk_softmax(g, 1, E, K)
         got = _run_block(coli, torch, table, x, ids, w, H)
         assert norm_err(got, orc.moe_block(H, F, mats, x, ids, w)) <= TOL
+
+
+@pytest.mark.parametrize("fmt,gs,H,F", [(4, 64, 512, 256), (4, 128, 1024, 512), (2, 0, 384, 192), (4, 64, 2048, 2048),
+                                        (4, 128, 4096, 1024)])
+@pytest.mark.parametrize("S,K,E", [(40, 4, 24), (20, 2, 24), (60, 2, 2), (33, 8, 64)])
+def test_prefill_small_expert_groups(fmt, gs, H, F, S, K, E):
+    """Prefill shapes the small-row path takes: experts with at most 12 rows go
+    in groups of up to 4 rows to the mma.sync products, the rest to the tensor-
+    core GEMMs (mixed; every expert small; no expert small), against the oracle."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(5300 + fmt + gs + H + S + K + E)
+    host = _experts(g, H, F, E, fmt, gs, distinct=min(E, 8))
+    x = wl.activations(g, S, H, bf16_exact=True)
+    ids, w = wl.routing_zipf(g, S, E, K)
+    ids[1, 0] = -1
+    got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert norm_err(got, ref) <= TOL
+
+
+def test_prefill_small_expert_groups_general_x():
+    """The small-row path with activations that are not bf16-representable
+    (the hi / lo halves carry every bit the tolerance needs)."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E, S, K = 1024, 512, 32, 48, 4
+    g = wl.rng(5400)
+    host = _experts(g, H, F, E, 4, 64, distinct=8)
+    x = wl.activations(g, S, H) * np.float32(3.7)
+    ids, w = wl.routing_zipf(g, S, E, K)
+    got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert norm_err(got, ref) <= TOL
