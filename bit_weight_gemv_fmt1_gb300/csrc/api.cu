@@ -1136,7 +1136,8 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
                            sm_plan(true, fmt, mi.d0->gs, (int)F, (int)H, (int)mi.d0->rs, mi.d0->ng,
                                    (size_t)ds->smem_optin, &sdn, &smem_dn);
         const size_t sz_sg = al((size_t)n_slots * 4);
-        const size_t total = sz_off + 2 * sz_ord + 3 * sz_tile + 256 + sz_px + sz_gu + sz_ph + sz_out + 3 * sz_sg;
+        const size_t total =
+            sz_off + 2 * sz_ord + 3 * sz_tile + 256 + sz_px + sz_gu + sz_ph + sz_out + 3 * sz_sg + al(n_slots);
         Workspace *ws = nullptr;
         if (int rc = workspace(ds, st, total, &ws)) return rc;
         char *p = (char *)ws->buf;
@@ -1155,7 +1156,8 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         float *slot_out = (float *)p; p += sz_out;
         int32_t *sg_e = (int32_t *)p; p += sz_sg;
         int32_t *sg_p0 = (int32_t *)p; p += sz_sg;
-        int32_t *sg_n = (int32_t *)p;
+        int32_t *sg_n = (int32_t *)p; p += sz_sg;
+        uint8_t *row_small = (uint8_t *)p;
         int32_t *n_sg = flags + 4;   // the small-group count, beside the plane flags (one zeroed block)
         CU(cudaMemsetAsync(flags, 0, 8 * sizeof(int), st), "cudaMemsetAsync(flags)");
 
@@ -1167,6 +1169,7 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         r.tile_rows = TR;
         r.small_rows = small ? kSmallRows : 0;
         r.sg_e = sg_e; r.sg_p0 = sg_p0; r.sg_n = sg_n; r.n_sg = n_sg;
+        r.row_small = small ? row_small : nullptr;
         r.err = ds->err;
         cudaError_t e = launch_route(r, st);
         if (e != cudaSuccess) return cuda_fail(e, "routing launch");
@@ -1212,7 +1215,7 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         e = launch_gemm_tc(a, mapx, max_tiles, ds->n_sm, st);
         if (e != cudaSuccess) return cuda_fail(e, "gate/up tensor-core launch");
         e = launch_silu_planes(gu, (int)F, offsets + n_experts, n_slots, F_pad, ph, (long long)rows_alloc * F_pad,
-                               &flags[1], st);
+                               &flags[1], st, small ? row_small : nullptr);
         if (e != cudaSuccess) return cuda_fail(e, "silu planes launch");
         e = encode_plane_maps(ph, F_pad, rows_alloc, &maph);
         if (e != cudaSuccess) return cuda_fail(e, "hidden tensor map");

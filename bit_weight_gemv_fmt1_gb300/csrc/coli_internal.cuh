@@ -579,6 +579,7 @@ struct RouteArgs {
     // instead, in groups of up to 4 consecutive rows (moe_small.cu)
     int small_rows;
     int32_t *sg_e, *sg_p0, *sg_n, *n_sg;
+    uint8_t *row_small;       // [S*K]: 1 for the rows of such experts (may be NULL)
     int *err;
 };
 
@@ -613,7 +614,8 @@ cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *o
                                  int n_rows, int I, int I_pad, void *planes, long long plane_elems, int *flag,
                                  cudaStream_t st);
 cudaError_t launch_silu_planes(const float *gu, int F, const int32_t *n_valid, int n_rows, int F_pad, void *planes,
-                               long long plane_elems, int *flag, cudaStream_t st);
+                               long long plane_elems, int *flag, cudaStream_t st,
+                               const uint8_t *skip = nullptr);
 cudaError_t launch_gemm_tc(const TcArgs &a, const PlaneMapSet &maps, int max_tiles, int n_sm, cudaStream_t st);
 
 cudaError_t launch_moe_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t smem, cudaStream_t st);

@@ -584,9 +584,11 @@ __global__ void gather_planes_kernel(const float *__restrict__ X, long long ldx,
 // h = silu(g) * u from the fused gate|up output [rows][2F], written as bf16
 // planes for the down projection (same permutation as gather_planes_kernel).
 __global__ void silu_planes_kernel(const float *__restrict__ gu, int F, const int32_t *n_valid, int n_rows, int F_pad,
-                                   __nv_bfloat16 *planes, long long plane_elems, int *flag) {
+                                   __nv_bfloat16 *planes, long long plane_elems, int *flag, const uint8_t *skip) {
     const int p = blockIdx.x;
     if (p >= n_rows) return;
+    // rows another path multiplies (skip[p]) are neither read nor written
+    if (skip && p < *n_valid && skip[p]) return;
     const bool live = p < *n_valid;
     bool nz = false;
     for (int k8 = threadIdx.x; k8 < F_pad / 8; k8 += blockDim.x) {
@@ -678,10 +680,10 @@ cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *o
 }
 
 cudaError_t launch_silu_planes(const float *gu, int F, const int32_t *n_valid, int n_rows, int F_pad, void *planes,
-                               long long plane_elems, int *flag, cudaStream_t st) {
+                               long long plane_elems, int *flag, cudaStream_t st, const uint8_t *skip) {
     if (n_rows <= 0) return cudaSuccess;
     silu_planes_kernel<<<n_rows, 128, 0, st>>>(gu, F, n_valid, n_rows, F_pad, (__nv_bfloat16 *)planes, plane_elems,
-                                               flag);
+                                               flag, skip);
     return cudaGetLastError();
 }
 

@@ -354,6 +354,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
             *a.n_tiles = nt;
             if (a.n_sg) *a.n_sg = ng;
         }
+        if (a.row_small)
+            for (int e = tid; e < a.E; e += blockDim.x) {
+                const int c = base[e + 1] - base[e];
+                const uint8_t f = (c > 0 && c <= a.small_rows) ? 1 : 0;
+                for (int p = base[e]; p < base[e + 1]; p++) a.row_small[p] = f;
+            }
     }
 }
 

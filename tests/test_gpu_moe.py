@@ -294,7 +294,7 @@ def test_block_table_handle_keeps_one_plan_per_K():
 
 @pytest.mark.parametrize("fmt,gs,H,F", [(4, 64, 512, 256), (4, 128, 1024, 512), (2, 0, 384, 192), (4, 64, 2048, 2048),
                                         (4, 128, 4096, 1024)])
-@pytest.mark.parametrize("S,K,E", [(40, 4, 24), (20, 2, 24), (60, 2, 2), (33, 8, 64)])
+@pytest.mark.parametrize("S,K,E", [(40, 4, 24), (20, 2, 24), (60, 2, 2), (33, 8, 64), (100, 8, 64)])
 def test_prefill_small_expert_groups(fmt, gs, H, F, S, K, E):
     """Prefill shapes the small-row path takes: experts with at most 12 rows go
     in groups of up to 4 rows to the mma.sync products, the rest to the tensor-
