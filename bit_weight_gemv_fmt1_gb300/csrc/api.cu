@@ -1189,7 +1189,7 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
             n_launch++;
         }
         e = launch_gather_planes(x, H, order, K, offsets + n_experts, n_slots, (int)H, H_pad, px,
-                                 (long long)rows_alloc * H_pad, &flags[0], st);
+                                 (long long)rows_alloc * H_pad, &flags[0], st, small ? row_small : nullptr);
         if (e != cudaSuccess) return cuda_fail(e, "activation planes launch");
         PlaneMapSet mapx, maph;
         e = encode_plane_maps(px, H_pad, rows_alloc, &mapx);

@@ -612,7 +612,7 @@ struct PlaneMapSet {
 cudaError_t encode_plane_maps(const void *planes, long long I_pad, long long rows_alloc, PlaneMapSet *out);
 cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *order, int kdiv, const int32_t *n_valid,
                                  int n_rows, int I, int I_pad, void *planes, long long plane_elems, int *flag,
-                                 cudaStream_t st);
+                                 cudaStream_t st, const uint8_t *skip = nullptr);
 cudaError_t launch_silu_planes(const float *gu, int F, const int32_t *n_valid, int n_rows, int F_pad, void *planes,
                                long long plane_elems, int *flag, cudaStream_t st,
                                const uint8_t *skip = nullptr);

@@ -553,10 +553,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 // order the dequant writes the codes in), zero past I.
 __global__ void gather_planes_kernel(const float *__restrict__ X, long long ldx, const int32_t *order, int kdiv,
                                      const int32_t *n_valid, int n_rows, int I, int I_pad, __nv_bfloat16 *planes,
-                                     long long plane_elems, int *flag) {
+                                     long long plane_elems, int *flag, const uint8_t *skip) {
     const int p = blockIdx.x;
     if (p >= n_rows) return;
     const int nv = n_valid ? *n_valid : n_rows;
+    if (skip && p < nv && skip[p]) return;   // a row another path multiplies
     long long src = -1;
     if (p < nv) src = order ? (long long)(order[p] / kdiv) : (long long)p;
     bool nz = false;
@@ -672,10 +673,10 @@ cudaError_t encode_plane_maps(const void *planes, long long I_pad, long long row
 
 cudaError_t launch_gather_planes(const float *X, long long ldx, const int32_t *order, int kdiv, const int32_t *n_valid,
                                  int n_rows, int I, int I_pad, void *planes, long long plane_elems, int *flag,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, const uint8_t *skip) {
     if (n_rows <= 0) return cudaSuccess;
     gather_planes_kernel<<<n_rows, 128, 0, st>>>(X, ldx, order, kdiv, n_valid, n_rows, I, I_pad,
-                                                 (__nv_bfloat16 *)planes, plane_elems, flag);
+                                                 (__nv_bfloat16 *)planes, plane_elems, flag, skip);
     return cudaGetLastError();
 }
 
