@@ -435,9 +435,9 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
         job.err = ds->err;
         int nl = 0;
         cudaError_t e;
-        // S = 1, int4 (fmt 2; fmt 4 with gs 64 or 128), one row length and gs for all matrices, at
-        // least 4 MB: the tensor-core streamed matvec (gemv_mma.cu)
-        bool mma = S == 1 && !host_any && (W0->fmt == 2 || W0->fmt == 4) && wbytes >= (4u << 20);
+        // S = 1..4, int4 (fmt 2; fmt 4 with gs 64 or 128), one row length and gs for all matrices,
+        // at least 4 MB: the tensor-core streamed matvec (gemv_mma.cu)
+        bool mma = S <= 4 && !host_any && (W0->fmt == 2 || W0->fmt == 4) && wbytes >= (4u << 20);
         for (int m = 0; m < n && mma; m++)
             mma = W[m]->fmt == W0->fmt && W[m]->I == W0->I && W[m]->rs == W0->rs && W[m]->ng == W0->ng &&
                   (W0->fmt != 4 || W[m]->gs == W0->gs);
@@ -445,7 +445,7 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
             GmArgs ga;
             size_t gsm = 0;
             int ggrid = 0;
-            if (gm_plan(W0->fmt, W0->fmt == 4 ? W0->gs : 0, (int)W0->I, (int)W0->rs, W0->ng, n, job.O, ds->n_sm,
+            if (gm_plan(W0->fmt, W0->fmt == 4 ? W0->gs : 0, (int)W0->I, (int)W0->rs, W0->ng, n, job.O, S, ds->n_sm,
                         (size_t)ds->smem_optin, &ga, &gsm, &ggrid)) {
                 for (int m = 0; m < n; m++) {
                     ga.q[m] = W[m]->q;

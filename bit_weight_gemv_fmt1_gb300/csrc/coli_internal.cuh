@@ -694,7 +694,7 @@ struct GmArgs {
     float *y[GemvJob::MAXM];
     int O[GemvJob::MAXM];
     int stage_start[GemvJob::MAXM + 1];   // prefix of the matrices' stage counts
-    int n, fmt, I, rs, ng, gsh;            // rs: device row stride (bytes); gsh: log2(gs / 64)
+    int n, fmt, S, I, rs, ng, gsh;         // S rows of x (1..4); rs: device row stride (bytes); gsh: log2(gs / 64)
     int nseg, spw, nt;                     // 64-input segments per row and per warp; 16-row tiles per stage
     int bs, so, ss, slot_bytes;            // stage layout: code-block stride, scale offset and block stride
     int off_red, off_bar;                  // dynamic shared-memory layout (bytes)
@@ -704,8 +704,8 @@ struct GmArgs {
     long long timeout_ns;
 };
 size_t gm_counter_words();
-bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int n_sm, size_t smem_max, GmArgs *a,
-             size_t *smem, int *grid);
+bool gm_plan(int fmt, int gs, int I, int rs, int ng, int n, const int *O, int S, int n_sm, size_t smem_max,
+             GmArgs *a, size_t *smem, int *grid);
 cudaError_t launch_gemv_mma(const GmArgs &a, int grid, size_t smem, cudaStream_t st);
 
 // Prefill products of the experts with few rows (moe_small.cu).

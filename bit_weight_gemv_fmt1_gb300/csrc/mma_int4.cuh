@@ -337,4 +337,54 @@ __device__ __forceinline__ bool md_wait1(uint64_t *bar, uint32_t parity, uint64_
     return true;
 }
 
+constexpr int kMd4StgBlock = 528;
+constexpr int kMd4Stg = 4 * kMd4StgBlock;
+
+// Four activation rows per B operand (the prefill's small-row groups, S <= 4
+// matvecs): row t's hi half in B column 2 t, its lo half in column 2 t + 1, so
+// quad lane t of the mma result holds row t's sums.  md4_frag_store: one
+// round's stores for row t, as md_frag_store, into matrix rows 2 t and 2 t + 1
+// of a staging area of kMd4Stg bytes (blocks of one (segment, k-step) 528
+// bytes apart: the stores of one instruction fall in four bank quarters).
+__device__ __forceinline__ void md4_frag_store(float4 ld, MdScale sc, int lane, int t, uint32_t stg) {
+    const int seg = lane >> 4, tt = (lane >> 2) & 3, i = (lane >> 1) & 1, h = lane & 1;
+    const uint32_t wb = stg + (uint32_t)((seg * 2 + i) * kMd4StgBlock + (2 * t) * 16 + (2 * tt + h) * 2);
+    const float v[4] = {ld.x, ld.y, ld.z, ld.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const float sv = v[q] * sc.s2k * ((q & 1) ? 0.0625f : 1.f);
+        const uint32_t b = __float_as_uint(sv);
+        const float h32 = __uint_as_float((b + 0xFFFu + ((b >> 13) & 1u)) & 0xFFFFE000u);
+        const float l32 = (sv - h32) * 2048.f;
+        uint32_t pk;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(h32), "f"(l32));   // hi in the upper half
+        // matrix (operand q / 2, slot half q % 2): 8 rows of 16 bytes
+        const uint32_t ad = wb + (uint32_t)((((q >> 1) * 2 + (q & 1)) * 8) * 16);
+        asm volatile("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %0;\n st.shared.u16 [%1], h;\n st.shared.u16 [%2], l;\n}"
+                     ::"r"(pk), "r"(ad), "r"(ad + 16));
+    }
+}
+// md4_frag_load: the round's B registers, ldmatrix.x4 of the four matrices,
+// every row real.
+__device__ __forceinline__ void md4_frag_load(int nq, int lane, uint32_t stg, uint32_t (&b0)[8], uint32_t (&b1)[8]) {
+    const int mq = lane >> 3, mr = lane & 7;
+#pragma unroll
+    for (int sg = 0; sg < 2; sg++) {
+        uint32_t(&bf)[8] = sg ? b1 : b0;
+        const bool on = sg < nq;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const uint32_t ra = stg + (uint32_t)((sg * 2 + i) * kMd4StgBlock + (mq * 8 + mr) * 16);
+            uint32_t r0, r1, r2, r3;
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                         : "r"(ra));
+            bf[4 * i + 0] = on ? r0 : 0u;
+            bf[4 * i + 1] = on ? r1 : 0u;
+            bf[4 * i + 2] = on ? r2 : 0u;
+            bf[4 * i + 3] = on ? r3 : 0u;
+        }
+    }
+}
+
 }  // namespace coli

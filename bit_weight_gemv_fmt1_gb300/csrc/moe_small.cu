@@ -38,8 +38,7 @@ namespace {
 constexpr int kSmThreads = (kMdWarps + 2) * 32;
 constexpr int kSmSlots = 3;
 constexpr int kSmRedT = 17;                   // floats per (stage row, group row): 16 warps, padded
-constexpr int kSmStgBlock = 528;              // staging block of one (segment, k-step): 4 matrices x 8 rows, skewed
-constexpr int kSmStg = 4 * kSmStgBlock;       // staging area of one round
+constexpr int kSmStg = kMd4Stg;               // staging area of one round
 constexpr uint32_t kSmNapE = 64, kSmNapP = 64;
 
 // Item k: d.x = group, d.y = matrix (0 or 1 of the call), d.z = first row, d.w = rows.
@@ -77,48 +76,6 @@ __device__ __forceinline__ float4 sm_load4(const SmArgs &a, int p, int q0, int n
         }
     }
     return make_float4(v[0], v[1], v[2], v[3]);
-}
-
-// Stores of one round for group row t: as md_frag_store, into matrix rows
-// 2 t (hi) and 2 t + 1 (lo) of a staging area of kSmStg bytes.
-__device__ __forceinline__ void sm_frag_store(float4 ld, MdScale sc, int lane, int t, uint32_t stg) {
-    const int seg = lane >> 4, tt = (lane >> 2) & 3, i = (lane >> 1) & 1, h = lane & 1;
-    const uint32_t wb = stg + (uint32_t)((seg * 2 + i) * kSmStgBlock + (2 * t) * 16 + (2 * tt + h) * 2);
-    const float v[4] = {ld.x, ld.y, ld.z, ld.w};
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const float sv = v[q] * sc.s2k * ((q & 1) ? 0.0625f : 1.f);
-        const uint32_t b = __float_as_uint(sv);
-        const float h32 = __uint_as_float((b + 0xFFFu + ((b >> 13) & 1u)) & 0xFFFFE000u);
-        const float l32 = (sv - h32) * 2048.f;
-        uint32_t pk;
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(h32), "f"(l32));   // hi in the upper half
-        // matrix (operand q / 2, slot half q % 2): 8 rows of 16 bytes
-        const uint32_t ad = wb + (uint32_t)((((q >> 1) * 2 + (q & 1)) * 8) * 16);
-        asm volatile("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %0;\n st.shared.u16 [%1], h;\n st.shared.u16 [%2], l;\n}"
-                     ::"r"(pk), "r"(ad), "r"(ad + 16));
-    }
-}
-// The round's B registers: ldmatrix.x4 of the four matrices, every row real.
-__device__ __forceinline__ void sm_frag_load(int nq, int lane, uint32_t stg, uint32_t (&b0)[8], uint32_t (&b1)[8]) {
-    const int mq = lane >> 3, mr = lane & 7;
-#pragma unroll
-    for (int sg = 0; sg < 2; sg++) {
-        uint32_t(&bf)[8] = sg ? b1 : b0;
-        const bool on = sg < nq;
-#pragma unroll
-        for (int i = 0; i < 2; i++) {
-            const uint32_t ra = stg + (uint32_t)((sg * 2 + i) * kSmStgBlock + (mq * 8 + mr) * 16);
-            uint32_t r0, r1, r2, r3;
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                         : "r"(ra));
-            bf[4 * i + 0] = on ? r0 : 0u;
-            bf[4 * i + 1] = on ? r1 : 0u;
-            bf[4 * i + 2] = on ? r2 : 0u;
-            bf[4 * i + 3] = on ? r3 : 0u;
-        }
-    }
 }
 
 // SEG: segments per warp (compile-time bound), NT: 16-row tiles per stage,
@@ -303,9 +260,9 @@ __global__ void __launch_bounds__(kSmThreads, 1) moe_small_kernel(const SmArgs a
 #pragma unroll
             for (int r = 0; r < NRD; r++) {
 #pragma unroll
-                for (int t = 0; t < 4; t++) sm_frag_store(ld[t][r], sc[t], lane, t, stg);
+                for (int t = 0; t < 4; t++) md4_frag_store(ld[t][r], sc[t], lane, t, stg);
                 __syncwarp();
-                sm_frag_load(nq - 2 * r, lane, stg, bf[2 * r], bf[2 * r + 1]);
+                md4_frag_load(nq - 2 * r, lane, stg, bf[2 * r], bf[2 * r + 1]);
                 __syncwarp();   // the staging area may be rewritten after this
                 float4 c0, c1;
                 md_frag_starts(bf[2 * r], bf[2 * r + 1], c0, c1);

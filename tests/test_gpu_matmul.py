@@ -363,36 +363,39 @@ def test_ping_pong_chain_in_graph():
 
 @pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (2, 0)])
 @pytest.mark.parametrize("O,I", [(4100, 2048), (8200, 1024), (2100, 4096), (1370, 6144)])
-def test_tensor_core_matvec_exact_integers(fmt, gs, O, I):
-    """S = 1 int4 with >= 4 MB of weights takes the tensor-core streamed matvec:
-    stages of one 16-row tile (rows of more than 2048 inputs) or three tiles,
-    warps with fewer segments than the widest, a partial last stage.  Power-
-    of-two scales and integer x make every step exact: bit-equal to the oracle."""
+@pytest.mark.parametrize("S", [1, 2, 3, 4])
+def test_tensor_core_matvec_exact_integers(fmt, gs, O, I, S):
+    """S <= 4 int4 with >= 4 MB of weights takes the tensor-core streamed matvec:
+    stages of one 16-row tile (rows of more than 2048 inputs) or of two / three
+    tiles, warps with fewer segments than the widest, a partial last stage, one
+    pair of B columns per row of x.  Power-of-two scales and integer x make
+    every step exact: bit-equal to the oracle."""
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
-    g = wl.rng(900 + fmt + gs + O)
+    g = wl.rng(900 + fmt + gs + O + 7 * S)
     m = wl.random_matrix(g, fmt, O, I, gs)
     m.scales = (2.0 ** g.integers(-2, 3, m.scales.size)).astype(np.float32)
-    x = g.integers(-8, 9, (1, I)).astype(np.float32)
+    x = g.integers(-8, 9, (S, I)).astype(np.float32)
     got = _run(coli, torch, m, x)
     ref = orc.matmul(fmt, gs, O, I, m.data, m.scales, x)
     assert np.array_equal(got, ref)
 
 
 @pytest.mark.parametrize("fmt,gs", [(4, 64), (2, 0)])
-def test_tensor_core_matvec_multi_ragged(fmt, gs):
+@pytest.mark.parametrize("S", [1, 3])
+def test_tensor_core_matvec_multi_ragged(fmt, gs, S):
     """One call over matrices of different heights (stages never straddle two
     matrices; partial stages at every matrix end), random weights and x."""
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
-    g = wl.rng(950 + fmt)
+    g = wl.rng(950 + fmt + S)
     I = 6144
     Os = [2048, 1000, 16, 3, 2047, 640]
     mats = [wl.random_matrix(g, fmt, o, I, gs) for o in Os]
-    x = wl.activations(g, 1, I)
+    x = wl.activations(g, S, I)
     Ws = [upload(coli, mm) for mm in mats]
     xd = torch.from_numpy(x).cuda()
-    ys = [torch.full((1, o), float("nan"), device="cuda") for o in Os]
+    ys = [torch.full((S, o), float("nan"), device="cuda") for o in Os]
     coli.matmul_multi(Ws, xd, ys)
     coli.sync_check()
     for mm, y in zip(mats, ys):
