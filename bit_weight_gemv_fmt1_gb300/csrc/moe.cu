@@ -249,12 +249,42 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) moe_decode_kernel(const Moe
 
 // ------------------------------------------------------------ routing
 constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarpHistE = 256;   // up to this many experts: placement by all warps (per-warp histograms)
+
+// Block-wide exclusive scan of one value per thread (blockDim.x = kRouteThreads);
+// *total: the sum over the block.  Contains __syncthreads.
+__device__ __forceinline__ int route_block_excl(int v, int *s_part, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_part[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < (int)(blockDim.x / 32) ? s_part[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        s_part[lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    const int ex = incl - v + (warp > 0 ? s_part[warp - 1] : 0);
+    *total = s_part[blockDim.x / 32 - 1];
+    __syncthreads();   // s_part may be reused
+    return ex;
+}
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a) {
     extern __shared__ int rsm[];
     int *cnt = rsm;                // [E]
     int *base = rsm + a.E;         // [E+1]
     int *fill = base + a.E + 1;    // [E]
+    int *hist = fill + a.E;        // [32][E] when E <= kRouteWarpHistE
     __shared__ int s_bad;
     __shared__ int s_part[kRouteThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -309,50 +339,88 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     if (tid == blockDim.x - 1) base[a.E] = run;
     __syncthreads();
     for (int e = tid; e <= a.E; e += blockDim.x) a.offsets[e] = base[e];
-    // stable placement by warp 0, 32 slots at a time in slot order
-    if (warp == 0) {
-        for (int t0 = 0; t0 < n; t0 += 32) {
+    // stable placement (rows of an expert in slot order).  Up to
+    // kRouteWarpHistE experts: warp w takes the w-th of 32 equal slot ranges,
+    // counts its slots per expert, and places them after the earlier warps'
+    // ones; else warp 0 alone, 32 slots at a time.
+    const bool par = a.E <= kRouteWarpHistE;
+    const int span = par ? ((n + 31) / 32 + 31) / 32 * 32 : n;
+    const int t_lo = par ? min(n, warp * span) : 0, t_hi = par ? min(n, t_lo + span) : n;
+    int *wfill = par ? hist + warp * a.E : fill;
+    if (par) {
+        for (int i = tid; i < 32 * a.E; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        for (int t0 = t_lo; t0 < t_hi; t0 += 32) {
             const int t = t0 + lane;
-            const int e = t < n ? a.ids[t] : -2;
+            const int e = t < t_hi ? a.ids[t] : -2;
+            const unsigned grp = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && __popc(grp & ((1u << lane) - 1u)) == 0) wfill[e] += __popc(grp);
+            __syncwarp();
+        }
+        __syncthreads();
+        for (int e = tid; e < a.E; e += blockDim.x) {
+            int run = base[e];
+            for (int w = 0; w < 32; w++) {
+                const int c = hist[w * a.E + e];
+                hist[w * a.E + e] = run;
+                run += c;
+            }
+        }
+        __syncthreads();
+    }
+    if (par || warp == 0) {
+        for (int t0 = t_lo; t0 < t_hi; t0 += 32) {
+            const int t = t0 + lane;
+            const int e = t < t_hi ? a.ids[t] : -2;
             const unsigned grp = __match_any_sync(0xffffffffu, e);
             const int rank = __popc(grp & ((1u << lane) - 1u));
             int pos = -1;
-            if (e >= 0) pos = base[e] + fill[e] + rank;
+            if (e >= 0) pos = (par ? wfill[e] : base[e] + wfill[e]) + rank;
             __syncwarp();
             if (e >= 0) {
                 a.order[pos] = t;
-                if (rank == 0) fill[e] += __popc(grp);
+                if (rank == 0) wfill[e] += __popc(grp);
             }
-            if (t < n && a.inv) a.inv[t] = pos;
+            if (t < t_hi && a.inv) a.inv[t] = pos;
             __syncwarp();
         }
     }
     // tile list: ceil(count / tile_rows) tiles per expert, in expert order;
-    // experts of at most small_rows rows: groups of up to 4 rows instead
+    // experts of at most small_rows rows: groups of up to 4 rows instead.  Each
+    // thread writes the entries of its own range of experts.
     if (a.n_tiles) {
         __syncthreads();
-        if (tid == 0) {
-            int nt = 0, ng = 0;
-            for (int e = 0; e < a.E; e++) {
-                const int c = base[e + 1] - base[e];
-                if (c > 0 && c <= a.small_rows) {
-                    for (int p = base[e]; p < base[e + 1]; p += 4) {
-                        a.sg_e[ng] = e;
-                        a.sg_p0[ng] = p;
-                        a.sg_n[ng] = min(4, base[e + 1] - p);
-                        ng++;
-                    }
-                    continue;
+        int lt = 0, lg = 0;
+        for (int e = e0; e < e1; e++) {
+            const int c = base[e + 1] - base[e];
+            const bool sm = c > 0 && c <= a.small_rows;
+            lt += sm ? 0 : (c + a.tile_rows - 1) / a.tile_rows;
+            lg += sm ? (c + 3) / 4 : 0;
+        }
+        int tot_t = 0, tot_g = 0;
+        int nt = route_block_excl(lt, s_part, &tot_t);
+        int ng = route_block_excl(lg, s_part, &tot_g);
+        for (int e = e0; e < e1; e++) {
+            const int c = base[e + 1] - base[e];
+            if (c > 0 && c <= a.small_rows) {
+                for (int p = base[e]; p < base[e + 1]; p += 4) {
+                    a.sg_e[ng] = e;
+                    a.sg_p0[ng] = p;
+                    a.sg_n[ng] = min(4, base[e + 1] - p);
+                    ng++;
                 }
-                for (int p = base[e]; p < base[e + 1]; p += a.tile_rows) {
-                    a.tile_e[nt] = e;
-                    a.tile_p0[nt] = p;
-                    a.tile_p1[nt] = min(base[e + 1], p + a.tile_rows);
-                    nt++;
-                }
+                continue;
             }
-            *a.n_tiles = nt;
-            if (a.n_sg) *a.n_sg = ng;
+            for (int p = base[e]; p < base[e + 1]; p += a.tile_rows) {
+                a.tile_e[nt] = e;
+                a.tile_p0[nt] = p;
+                a.tile_p1[nt] = min(base[e + 1], p + a.tile_rows);
+                nt++;
+            }
+        }
+        if (tid == 0) {
+            *a.n_tiles = tot_t;
+            if (a.n_sg) *a.n_sg = tot_g;
         }
         if (a.row_small)
             for (int e = tid; e < a.E; e += blockDim.x) {
@@ -436,7 +504,7 @@ cudaError_t launch_moe_decode(const MoeDecodeArgs &a, int fmt, int grid, size_t 
 }
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
-    const size_t smem = (size_t)(3 * a.E + 1) * sizeof(int);
+    const size_t smem = (size_t)(3 * a.E + 1 + (a.E <= kRouteWarpHistE ? 32 * a.E : 0)) * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     route_kernel<<<1, kRouteThreads, smem, st>>>(a);
