@@ -324,3 +324,59 @@ def test_prefill_small_expert_groups_general_x():
     got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
     ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
     assert norm_err(got, ref) <= TOL
+
+
+def test_matvec_and_decode_blocks_interleaved_on_one_stream():
+    """The streamed matvec (its claimed-stage counter), the tensor-core decode
+    block (its epoch and exit counter) and the int8 streamed decode block share
+    one stream's counter words: each leaves them as it found them, so any
+    interleaving of calls on one stream, captured in a CUDA graph or not, gives
+    the oracle's results."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(6100)
+    m = wl.random_matrix(g, 4, 1400, 6144, 64)   # 4.3 MB: the tensor-core streamed matvec
+    W = upload(coli, m)
+    H, F = 1024, 512
+    host4 = _experts(g, H, F, 8, 4, 64)
+    host1 = _experts(g, H, F, 8, 1, 0)
+    t4, t1 = _device_table(coli, host4), _device_table(coli, host1)
+    xm = torch.from_numpy(wl.activations(g, 1, 6144)).cuda()
+    xb = torch.from_numpy(wl.activations(g, 1, H)).cuda()
+    ids, w = wl.routing_topk_softmax(g, 1, 8, 4)
+    di, dw = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    ref_m = orc.matmul(4, 64, 1400, 6144, m.data, m.scales, xm.cpu().numpy())
+    ref4 = orc.moe_block(H, F, _oracle_mats(host4), xb.cpu().numpy(), ids, w)
+    ref1 = orc.moe_block(H, F, _oracle_mats(host1), xb.cpu().numpy(), ids, w)
+    ym = torch.empty(1, 1400, device="cuda")
+    y4 = torch.empty(1, H, device="cuda")
+    y1 = torch.empty(1, H, device="cuda")
+    st = torch.cuda.Stream()
+
+    def seq():
+        for _ in range(3):
+            coli.matmul(W, xm, ym, stream=st)
+            coli.moe_block(xb, t4, di, dw, y4, stream=st)
+            coli.matmul(W, xm, ym, stream=st)
+            coli.moe_block(xb, t1, di, dw, y1, stream=st)
+
+    def check():
+        assert norm_err(ym.cpu().numpy(), ref_m) <= TOL
+        assert norm_err(y4.cpu().numpy(), ref4) <= TOL
+        assert norm_err(y1.cpu().numpy(), ref1) <= TOL
+
+    with torch.cuda.stream(st):
+        seq()
+    torch.cuda.synchronize()
+    coli.sync_check(st)
+    check()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        seq()
+    for y in (ym, y4, y1):
+        y.fill_(float("nan"))
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    coli.sync_check(st)
+    check()
