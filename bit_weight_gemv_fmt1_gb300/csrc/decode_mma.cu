@@ -42,10 +42,12 @@
 //            the slot's partial-sum table and moves on; warp 17 sums the table
 //            in warp order and writes h[a][j] = silu(gate) * up to global
 //            memory, each value as one 64-bit word under the call's tag.
-//   phase B: each CTA owns one routed expert and a range of whole 48-row
-//            stages of its down rows (md_share: expert 0, whose h is finished
-//            last, gets more CTAs; the others are interleaved so that every
-//            CTA's gate/up units plus down stages come out even).  Each warp polls until the h
+//   phase B: each CTA serves one routed expert (md_share sizes the groups:
+//            expert 0, whose h is finished last, gets more CTAs; the others
+//            are interleaved so that every CTA's gate/up units plus down
+//            stages come out even) and claims that expert's whole 48-row
+//            stages of down rows one at a time, as its slots free up, from a
+//            per-expert counter, so a group's CTAs finish together.  Each warp polls until the h
 //            values of its segments carry the call's tag (no fence or grid
 //            barrier: a 64-bit store is seen whole), builds their B fragments
 //            once and streams the CTA's rows in stages of 48; warp 17 sums the
@@ -84,8 +86,10 @@ constexpr int kMdStageRows = 4 * kMdBlockRows; // down rows of a phase-B stage (
 constexpr int kMdRedB = 20;
 constexpr int kMdRedSlot = kMdStageRows * kMdRedB;
 // state words of the kernel (zero before the first call): [1] CTAs out,
-// [3] epoch, then the tagged h [K][F] and part [K][H] (8 bytes each)
-constexpr int kMdCtrH = 4;
+// [3] epoch, [4, 4 + 64) down stages claimed per routed expert, then the
+// tagged h [K][F] and part [K][H] (8 bytes each)
+constexpr int kMdClaim = 4;
+constexpr int kMdCtrH = kMdClaim + 64;
 
 enum : int { MD_A = 0, MD_B = 1, MD_END = 2 };
 static_assert(kMaxDecodeSlots + 1 <= (int)(sizeof(MdArgs::m0) / sizeof(int)), "MdArgs::m0 covers every routed-expert count");
@@ -196,6 +200,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     const int SB = a.slot_bytes;
     const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
     unsigned *exitc = a.ctr + 1;
+    unsigned *claimB = a.ctr + kMdClaim;   // [routed expert]: down stages claimed so far
     // h values carry the call's tag in their high word: a 64-bit store is seen
     // whole or not at all, so a reader knows a value is this call's without a fence
     unsigned long long *htag = reinterpret_cast<unsigned long long *>(a.ctr + kMdCtrH);
@@ -277,24 +282,22 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             if ((int)blockIdx.x * rpc + r < a.H) a.y[blockIdx.x * rpc + r] = 0.f;
         return;
     }
-    // phase B: this CTA's routed expert eB (the CTAs of an expert split its
-    // down rows evenly) and its rows [rb0, rb1)
+    // phase B: this CTA's routed expert eB (md_share sizes the group of CTAs of
+    // each expert); the group's CTAs claim its 48-row down stages one at a time
     const int G = gridDim.x;
     const int spe = (a.F + 7) / 8;   // phase-A stages per routed expert
     const int nsE = (a.H + kMdStageRows - 1) / kMdStageRows;   // 48-row stages of a down matrix
     int eB = 0, sB0 = 0, sB1 = 0;
     md_share(blockIdx.x, nact, G, nact * spe, nsE, a.m0[nact], &eB, &sB0, &sB1);
-    const int rb0 = min(a.H, kMdStageRows * sB0), rb1 = min(a.H, kMdStageRows * sB1);
 
     if (warp == kMdWarps) {
         // ---------------- producer: lane 0 issues every stage of the CTA.  Phase-A
         // units are dealt round robin, the last routed expert's first, so that
         // the final round (a partial one) belongs to expert 0
         const unsigned totalA = (unsigned)(nact * spe);
-        const int nB = (rb1 - rb0 + kMdStageRows - 1) / kMdStageRows;
         const int rsA = a.rs_gu, rsB = a.rs_d;
         unsigned idx = blockIdx.x;
-        int jB = 0, i = 0;
+        int i = 0, sBc = 0;
         bool more = true;
         // stage i into slot i % kMdSlots; false after the end marker or an abort
         auto issue = [&]() -> bool {
@@ -330,8 +333,10 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                                   (uint32_t)(cnt[b] * a.ng_gu * 4), &full[s]);
                 }
                 idx += G;
-            } else if (jB < nB) {
-                const int r0 = rb0 + jB * kMdStageRows, nr = min(kMdStageRows, rb1 - r0);
+            } else if ((sBc = (int)atomicAdd(claimB + eB, 1u)) < nsE) {
+                // the next unclaimed 48-row stage of expert eB's down rows: the
+                // CTAs of an expert take its stages as their slots free up
+                const int r0 = sBc * kMdStageRows, nr = min(kMdStageRows, a.H - r0);
                 desc[s] = make_int4(MD_B, eB, r0, nr);
                 uint32_t tx = 0;
                 int cnt[4];
@@ -350,7 +355,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                         bulk_load(dst + a.soB + b * a.ssB, rt.s[eB][2] + rr * a.ng_d, (uint32_t)(cnt[b] * a.ng_d * 4),
                                   &full[s]);
                 }
-                jB++;
             } else {
                 desc[s] = make_int4(MD_END, 0, 0, 0);
                 mbar_arrive(&full[s]);   // end marker: no bytes
@@ -506,8 +510,8 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             }
         }
         // phase B: the warp's h values of expert eB (this call's tag on every one),
-        // its B fragments built once, then the CTA's rows of down[eB]
-        if (live && rb1 > rb0) {
+        // its B fragments built once, then the stages of down[eB] this CTA claimed
+        if (live) {
             const int q0B = warp * a.spwB, nqB = min(a.spwB, a.nsegB - q0B);
             const int rs = a.rs_d;
             const uint32_t cofs = (uint32_t)(blk * (a.bsB + 32) + rib * rs + 32 * q0B + 8 * t);
@@ -595,14 +599,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                 i++;
             }
         }
-        if (live && rb1 <= rb0) {
-            // no phase-B rows: pass the end marker
-            const int s = i % kMdSlots;
-            if (md_wait(&full[s], (uint32_t)((i / kMdSlots) & 1), deadline, &abort_flag, kMdNapC)) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-        }
         named_sync(2, (kMdWarps + 1) * 32);
         // y: CTA G - 1 - c sums the 64-row blocks c, c + G, ... (the CTAs at the end
         // of the grid have one gate/up unit fewer): each thread polls one
@@ -650,6 +646,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
             __threadfence();
             if (atomicAdd(exitc, 1u) == gridDim.x - 1) {
                 *(a.ctr + 3) += 1u;
+                for (int k = 0; k < a.K; k++) claimB[k] = 0u;
                 *exitc = 0u;
                 __threadfence();
             }
