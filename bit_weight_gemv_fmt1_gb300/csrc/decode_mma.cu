@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
         const unsigned totalA = (unsigned)(nact * spe);
         const int rsA = a.rs_gu, rsB = a.rs_d;
         unsigned idx = blockIdx.x;
-        int i = 0, sBc = 0;
+        int i = 0, sBc = -1;   // sBc: the down stage claimed next (-1: none yet)
         bool more = true;
         // stage i into slot i % kMdSlots; false after the end marker or an abort
         auto issue = [&]() -> bool {
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                                   (uint32_t)(cnt[b] * a.ng_gu * 4), &full[s]);
                 }
                 idx += G;
-            } else if ((sBc = (int)atomicAdd(claimB + eB, 1u)) < nsE) {
+            } else if ((sBc >= 0 ? sBc : (sBc = (int)atomicAdd(claimB + eB, 1u))) < nsE) {
                 // the next unclaimed 48-row stage of expert eB's down rows: the
                 // CTAs of an expert take its stages as their slots free up
                 const int r0 = sBc * kMdStageRows, nr = min(kMdStageRows, a.H - r0);
@@ -355,6 +355,8 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
                         bulk_load(dst + a.soB + b * a.ssB, rt.s[eB][2] + rr * a.ng_d, (uint32_t)(cnt[b] * a.ng_d * 4),
                                   &full[s]);
                 }
+                // claim the next one now: its round trip overlaps the wait for a free slot
+                sBc = (int)atomicAdd(claimB + eB, 1u);
             } else {
                 desc[s] = make_int4(MD_END, 0, 0, 0);
                 mbar_arrive(&full[s]);   // end marker: no bytes
