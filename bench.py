@@ -176,10 +176,10 @@ class DecodeBlock:
     def e2e_setup(self):
         """Each step's inputs (x, ids, w) packed in one pinned host record, so a
         step is one host-to-device copy, the block call and one device-to-host
-        copy of y.  The steps are independent tokens, so they run as a
-        three-stage pipeline over two device buffers: the copy of step i + 1's
-        inputs (stream h2d) and the copy of step i - 1's y (stream d2h) overlap
-        step i's block call (stream cmp); events order each buffer's reuse."""
+        copy of y.  The steps are independent tokens, so they run pipelined over
+        two device buffers: on a copy stream (the current stream of the whole
+        loop) step i + 1's inputs go in before step i's y comes out, and the
+        block calls run on a compute stream; events order each buffer's reuse."""
         t = self.torch
         H, K = self.H, self.K
         rec = np.zeros((64, H + 2 * K), np.float32)
@@ -194,30 +194,37 @@ class DecodeBlock:
         self.dw = [d[H + K:].view(1, K) for d in self.din]
         self.dy = [t.empty(1, H, device="cuda") for _ in range(2)]
         self.hy = [t.empty(1, H).pin_memory() for _ in range(2)]
-        self.s_h2d, self.s_cmp, self.s_d2h = t.cuda.Stream(), t.cuda.Stream(), t.cuda.Stream()
+        self.s_cp, self.s_cmp = t.cuda.Stream(), t.cuda.Stream()
         self.ev_in = [t.cuda.Event() for _ in range(2)]
         self.ev_cmp = [t.cuda.Event() for _ in range(2)]
         self.ev_out = [t.cuda.Event() for _ in range(2)]
         for b in range(2):   # every buffer starts out free
             self.ev_cmp[b].record(self.s_cmp)
-            self.ev_out[b].record(self.s_d2h)
+            self.ev_out[b].record(self.s_cp)
         self.h2d = 4 * H + 8 * K
         self.d2h = 4 * H
 
+    def e2e_begin(self, i0):
+        """Step i0's inputs in (the copy stream must be current)."""
+        b = i0 % 2
+        self.s_cp.wait_event(self.ev_cmp[b])
+        self.din[b].copy_(self.hin[i0 % 64], non_blocking=True)
+        self.ev_in[b].record(self.s_cp)
+
     def e2e_step(self, i):
-        b = i % 2
-        self.s_h2d.wait_event(self.ev_cmp[b])      # the block call of step i - 2 has read din[b]
-        with self.torch.cuda.stream(self.s_h2d):
-            self.din[b].copy_(self.hin[i % 64], non_blocking=True)
-        self.ev_in[b].record(self.s_h2d)
+        """Step i (its inputs already on their way): step i + 1's inputs in,
+        the block call, step i's y out.  The copy stream must be current."""
+        b, nb = i % 2, (i + 1) % 2
+        self.s_cp.wait_event(self.ev_cmp[nb])       # the call of step i - 1 has read din[nb]
+        self.din[nb].copy_(self.hin[(i + 1) % 64], non_blocking=True)
+        self.ev_in[nb].record(self.s_cp)
         self.s_cmp.wait_event(self.ev_in[b])
         self.s_cmp.wait_event(self.ev_out[b])      # y[b] of step i - 2 has reached the host
         self.coli.moe_block(self.dx[b], self.table, self.dids[b], self.dw[b], self.dy[b], stream=self.s_cmp)
         self.ev_cmp[b].record(self.s_cmp)
-        self.s_d2h.wait_event(self.ev_cmp[b])
-        with self.torch.cuda.stream(self.s_d2h):
-            self.hy[b].copy_(self.dy[b], non_blocking=True)
-        self.ev_out[b].record(self.s_d2h)
+        self.s_cp.wait_event(self.ev_cmp[b])
+        self.hy[b].copy_(self.dy[b], non_blocking=True)
+        self.ev_out[b].record(self.s_cp)
 
     def e2e_join(self, stream):
         """Make `stream` wait for every copy and call issued so far."""
@@ -794,27 +801,22 @@ def main():
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     wk.e2e_setup()
-    for i in range(args.warmup):
-        wk.e2e_step(i)
-    torch.cuda.synchronize()
     e2e_steps = args.steps
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    if hasattr(wk, "e2e_join"):   # pipelined: time from the first copy to the last one
-        for st_ in (wk.s_h2d, wk.s_cmp, wk.s_d2h):
-            st_.wait_event(t0)
-        t0.record(wk.s_h2d)
+    with torch.cuda.stream(wk.s_cp):   # pipelined: time from the first copy to the last one
+        wk.e2e_begin(0)
+        for i in range(args.warmup):
+            wk.e2e_step(i)
+        wk.e2e_join(wk.s_cp)
+        torch.cuda.synchronize()
+        t0.record(wk.s_cp)
         wk.s_cmp.wait_event(t0)
-        wk.s_d2h.wait_event(t0)
-        for i in range(e2e_steps):
+        wk.e2e_begin(args.warmup)
+        for i in range(args.warmup, args.warmup + e2e_steps):
             wk.e2e_step(i)
-        wk.e2e_join(wk.s_d2h)
-        t1.record(wk.s_d2h)
-    else:
-        t0.record()
-        for i in range(e2e_steps):
-            wk.e2e_step(i)
-        t1.record()
+        wk.e2e_join(wk.s_cp)
+        t1.record(wk.s_cp)
     torch.cuda.synchronize()
     e2e_s = t0.elapsed_time(t1) / 1e3
     e2e_units, e2e_max = aggregate(wk.bytes_per_step * e2e_steps, e2e_s, world)
