@@ -60,6 +60,7 @@
 // bounded (mbarrier.cuh); on expiry the kernel records DEV_ERR_TIMEOUT and
 // returns.  The last CTA to leave moves the tag on for the next call.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -197,6 +198,12 @@ __global__ void __launch_bounds__(kMdThreads, 1) moe_decode_mma_kernel(const MdA
     __shared__ __align__(16) uint8_t s_stg[kMdWarps][kMdStgBytes];   // B-fragment staging of each consumer warp, + a zero row
     __shared__ float s_part[kMdWarps * 32];                  // the final sum: one (expert, row) per thread
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // programmatic dependent launch: one CTA fills an SM, so the next kernel
+    // may begin launching now and its CTAs take the SMs this grid frees; every
+    // input of this one (x, the routing, the state words) may come from the
+    // previous kernel, so nothing is read before it has completed
+    pdl_trigger();
+    pdl_wait();
     const int SB = a.slot_bytes;
     const uint64_t deadline = global_ns() + (uint64_t)a.timeout_ns;
     unsigned *exitc = a.ctr + 1;
@@ -796,10 +803,23 @@ cudaError_t launch_decode_mma(const MdArgs &a, int grid, size_t smem, cudaStream
         cfg.blockDim = dim3(kMdThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        // co-resident CTAs (they wait on one another's h and part values), and
+        // programmatic serialization with the previous kernel where the driver
+        // takes the two together; otherwise the cooperative launch alone
+        static std::atomic<bool> no_pdl{false};
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeCooperative;
         attr[0].val.cooperative = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
+        if (!no_pdl.load(std::memory_order_relaxed)) {
+            cfg.numAttrs = 2;
+            const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+            if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
+            (void)cudaGetLastError();   // the refused configuration; nothing was launched
+            no_pdl.store(true, std::memory_order_relaxed);
+        }
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, a);
     });
