@@ -39,6 +39,11 @@
  *        an fp8 "passthrough" format holding one raw byte per element (the
  *        byte convention of fmt=1) and ceil(O/128) * ceil(I/128) per-block
  *        f32 scales; a [130,130] tensor has 4 blocks.
+ *   [V]  PR #298 page, Vulkan fmt=4 commit message and the #377 retarget
+ *        list: fmt=5 is int3 (#168); like fmt=4 it skips the per-row scale
+ *        (its scales vary along the row) and has a group size
+ *        (detect_group_size serves it); the fmt=4 shaders gate gs to
+ *        multiples of 8 so that a packed word never straddles a group.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   - element 2j of an int4 row is the LOW nibble of byte j;
@@ -65,6 +70,13 @@
  *     (o / 128, i / 128); the scales are stored block-row major,
  *     s[(o / 128) * ceil(I / 128) + i / 128]; blocks at the right and bottom
  *     edges are partial.  The gs argument is ignored for fmt=7;
+ *   - fmt=5 ([V]; the pages give no bit layout): element 8j+t of a row is
+ *     bits [3t, 3t+2] of the 24-bit little-endian word made of bytes 3j,
+ *     3j+1, 3j+2 of the row (low bits first, as int4 and int2 fill a byte),
+ *     a row is 3*ceil(I/8) bytes, the value is code - 4 (offset binary, as
+ *     int4's -8 and int2's -2), times the f32 scale of group i/gs stored as
+ *     for fmt=4 (O*ceil(I/gs) scales); gs is a multiple of 8, so the 8 codes
+ *     of a 3-byte unit share one group;
  *   - absorption ([A]): head h of n_heads owns rows o0 + h*stride + j,
  *     j < n_rows; the row-range matvec gives each head its own input vector,
  *     y[s][h][j] = sum_i w[o0+h*stride+j][i] x[s][h][i]; the transposed form
@@ -125,19 +137,20 @@ int64_t oracle_row_bytes(int fmt, int64_t I)
     case 2: return (I + 1) / 2;
     case 3: return (I + 3) / 4;
     case 4: return (I + 1) / 2;
+    case 5: return 3 * ((I + 7) / 8);
     case 7: return I;
     default: return -1;
     }
 }
 
 /* Number of f32 scales: none for fmt=0, one per row for fmt 1-3, O*ceil(I/gs)
- * for fmt=4 ([C]), one per 128 x 128 block for fmt=7 ([P]). */
+ * for fmt=4 ([C]) and fmt=5 ([V]), one per 128 x 128 block for fmt=7 ([P]). */
 int64_t oracle_scale_count(int fmt, int gs, int64_t O, int64_t I)
 {
     switch (fmt) {
     case 0: return 0;
     case 1: case 2: case 3: return O;
-    case 4: return gs > 0 ? O * ((I + gs - 1) / gs) : -1;
+    case 4: case 5: return gs > 0 ? O * ((I + gs - 1) / gs) : -1;
     case 7: return ((O + 127) / 128) * ((I + 127) / 128);
     default: return -1;
     }
@@ -172,6 +185,21 @@ static int oracle_code(int fmt, int64_t I, const uint8_t *q, int64_t o, int64_t 
         int cr = (b >> (2 * (int)(i % 4))) & 3;
         return cr - 2;                                     /* offset binary crumb */
     }
+    case 5: {
+        /* the 3-byte unit of elements 8j .. 8j+7, as one little-endian word */
+        const uint8_t *u = row + 3 * (i / 8);
+        const uint32_t word = (uint32_t)u[0] | ((uint32_t)u[1] << 8) | ((uint32_t)u[2] << 16);
+#if ORACLE_MUTATION == 13
+        const int c = (int)((word >> (21 - 3 * (int)(i % 8))) & 7);   /* planted: high bits first */
+#else
+        const int c = (int)((word >> (3 * (int)(i % 8))) & 7);
+#endif
+#if ORACLE_MUTATION == 14
+        return c - 3;                                      /* planted: wrong offset */
+#else
+        return c - 4;                                      /* offset binary 3-bit code */
+#endif
+    }
     default:
         return 0;
     }
@@ -203,7 +231,7 @@ static double oracle_scale(int fmt, int gs, int64_t I, const float *s, int64_t o
     switch (fmt) {
     case 1: case 2: case 3:
         return (double)s[o];
-    case 4: {
+    case 4: case 5: {
         const int64_t ng = (I + gs - 1) / gs;
 #if ORACLE_MUTATION == 3
         (void)ng; (void)i;
@@ -241,9 +269,11 @@ static double oracle_weight(int fmt, int gs, int64_t I, const void *data, const 
 
 static int oracle_check(int fmt, int gs, int64_t O, int64_t I)
 {
-    if (fmt < 0 || (fmt > 4 && fmt != 7) || O < 1 || I < 1)
+    if (fmt < 0 || fmt == 6 || fmt > 7 || O < 1 || I < 1)
         return ORACLE_EINVAL;
     if (fmt == 4 && (gs < 2 || (gs & 1)))
+        return ORACLE_EINVAL;
+    if (fmt == 5 && (gs < 8 || gs % 8 != 0))
         return ORACLE_EINVAL;
     return ORACLE_OK;
 }
@@ -291,7 +321,7 @@ int oracle_matmul(int fmt, int gs, int64_t O, int64_t I, const void *data, const
 
 /* The same product in the evaluation order the pages give for the kernels
  * ([M] Shader paragraph, [C]): fmt 1-3 multiply the row scale once after the
- * integer-code dot product; fmt=4 forms each group's code dot product and
+ * integer-code dot product; fmt=4 (and fmt=5, [V]) forms each group's code dot product and
  * folds the group scale in before summing over groups; fmt=7 does the same per
  * 128-input block with the scale of the row's block.  Mathematically equal
  * to oracle_matmul; used to pin that equality. */
@@ -309,7 +339,7 @@ int oracle_matmul_inline(int fmt, int gs, int64_t O, int64_t I, const void *data
             if (fmt == 0) {
                 for (int64_t i = 0; i < I; i++)
                     acc += (double)((const float *)data)[o * I + i] * (double)xs[i];
-            } else if (fmt == 4) {
+            } else if (fmt == 4 || fmt == 5) {
                 const int64_t ng = (I + gs - 1) / gs;
                 for (int64_t g = 0; g < ng; g++) {
                     const int64_t i0 = g * gs;

@@ -30,7 +30,7 @@ def _deq_from_raw(fmt, gs, codes, scales):
     """Dequantized matrix from raw codes (numpy, f64)."""
     v = codes.astype(np.float64) - wl.OFFSET[fmt]
     O, I = codes.shape
-    if fmt == 4:
+    if fmt in (4, 5):
         ng = wl.n_groups(I, gs)
         s = np.asarray(scales, np.float64).reshape(O, ng)
         return v * np.repeat(s, gs, axis=1)[:, :I]
@@ -94,7 +94,8 @@ def pin_exact_integer_cases(mutation=0):
     in f32 and f64, so the oracle's f32 output must equal the integer result."""
     g = wl.rng(11)
     for fmt, gs, O, I in ((1, 0, 7, 33), (2, 0, 5, 31), (3, 0, 6, 45), (4, 16, 5, 70),
-                          (4, 64, 4, 200), (4, 6, 3, 29), (4, 128, 3, 77)):
+                          (4, 64, 4, 200), (4, 6, 3, 29), (4, 128, 3, 77), (5, 8, 5, 37), (5, 64, 4, 200),
+                          (5, 24, 3, 50)):
         codes = _raw(g, fmt, O, I)
         sc = (2.0 ** g.integers(-3, 4, wl.scale_count(fmt, O, I, gs))).astype(np.float32)
         x = g.integers(-8, 9, (3, I)).astype(np.float32)
@@ -111,7 +112,7 @@ def pin_random_vs_library(mutation=0):
     g = wl.rng(12)
     for fmt, gs, O, I, S in ((1, 0, 9, 130, 2), (2, 0, 8, 129, 3), (3, 0, 7, 131, 2),
                              (4, 32, 6, 300, 2), (4, 64, 5, 1000, 1), (4, 128, 4, 100, 2),
-                             (4, 16, 3, 47, 1)):
+                             (4, 16, 3, 47, 1), (5, 64, 5, 301, 2), (5, 16, 4, 75, 1)):
         codes = _raw(g, fmt, O, I)
         sc = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(fmt, O, I, gs))
         x = g.standard_normal((S, I)).astype(np.float32)
@@ -158,7 +159,7 @@ def pin_inline_order(mutation=0):
     1e-14 of the sum of |terms|."""
     g = wl.rng(15)
     for fmt, gs, O, I in ((4, 64, 6, 500), (4, 16, 4, 97), (2, 0, 5, 99), (1, 0, 5, 77), (3, 0, 4, 70),
-                          (7, 0, 260, 300)):
+                          (7, 0, 260, 300), (5, 32, 5, 203)):
         if fmt == 7:
             m = wl.random_matrix(g, 7, O, I)
             data, sc = m.data, m.scales
@@ -208,6 +209,58 @@ def pin_partial_last_group(mutation=0):
         want = 0.5 * (x[:, i0:].astype(np.int64) @ (codes[:, i0:] - 8).T)
         got = orc.matmul(4, gs, 3, I, wl.pack(4, codes), sc.reshape(-1), x, mutation=mutation)
         if not np.array_equal(got.astype(np.float64), want.astype(np.float64)):
+            return False
+    return True
+
+
+def pin_int3_golden_layout(mutation=0):
+    """tests/golden/int3_layout.txt: fmt=5 bytes worked out by hand from the
+    layout reading decode to the listed values."""
+    for line in open(os.path.join(GOLDEN, "int3_layout.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        lhs, rhs = line.split("->")
+        want = [float(t) for t in rhs.split()]
+        data = np.frombuffer(bytes.fromhex(lhs.strip()), dtype=np.uint8).reshape(1, -1)
+        I = len(want)
+        if orc.row_bytes(5, I, mutation) != data.shape[1]:
+            return False
+        got = orc.dequant(5, 8, 1, I, data, np.ones(wl.n_groups(I, 8), np.float32), mutation=mutation)[0]
+        if list(got) != want:
+            return False
+    return True
+
+
+def pin_int3_single_codes(mutation=0):
+    """fmt=5, brute force over one code at a time: a 3-byte unit holding the
+    value v at position t and 0 elsewhere decodes to v - 4 at t and -4
+    elsewhere, for all 8 x 8 (t, v); the three bytes are the integer v * 8^t
+    written little-endian."""
+    for t in range(8):
+        for v in range(8):
+            data = np.frombuffer((v * 8 ** t).to_bytes(3, "little"), dtype=np.uint8).reshape(1, 3)
+            got = orc.dequant(5, 8, 1, 8, data, np.ones(1, np.float32), mutation=mutation)[0]
+            want = [-4.0] * 8
+            want[t] = float(v - 4)
+            if list(got) != want:
+                return False
+    return True
+
+
+def pin_int3_within_int4(mutation=0):
+    """Every int3 value c - 4 (c = 0..7) is the int4 value of the nibble c + 4,
+    and both formats take their group scales the same way, so a fmt=5 matrix
+    and the fmt=4 matrix of the same values and scales give the same double
+    results (fmt=4 is pinned on its own)."""
+    g = wl.rng(23)
+    for O, I, gs in ((5, 40, 8), (4, 203, 64), (3, 13, 8), (6, 130, 24), (2, 70, 128)):
+        codes = g.integers(0, 8, (O, I))
+        sc = wl.log_uniform(g, 1e-3, 1e-2, wl.scale_count(5, O, I, gs))
+        x = g.standard_normal((2, I)).astype(np.float32)
+        a, = orc.matmul(5, gs, O, I, wl.pack(5, codes), sc, x, mutation=mutation, want=("y64",))
+        b, = orc.matmul(4, gs, O, I, wl.pack(4, codes + 4), sc, x, mutation=mutation, want=("y64",))
+        if not np.array_equal(a, b):
             return False
     return True
 
@@ -528,7 +581,8 @@ PINS = [pin_golden_layout, pin_expert_bytes, pin_all_bytes_brute, pin_exact_inte
         pin_scale_linearity, pin_partial_last_group, pin_silu_closed_form, pin_route_vs_sorted,
         pin_moe_composition, pin_moe_invariants, pin_topk_worked_example, pin_topk_vs_sort,
         pin_fp8_block_count, pin_fp8_all_bytes, pin_fp8_block_structure, pin_fp8_unit_scale_vs_library,
-        pin_absorb_vs_library, pin_absorb_addrow_single, pin_absorb_adjoint]
+        pin_absorb_vs_library, pin_absorb_addrow_single, pin_absorb_adjoint, pin_int3_golden_layout,
+        pin_int3_single_codes, pin_int3_within_int4]
 
 MUTATIONS = {
     1: "int4 nibble order swapped",
@@ -543,4 +597,6 @@ MUTATIONS = {
     10: "fmt=7 block index transposed",
     11: "fmt=7 subnormals read as normals",
     12: "absorption heads packed at n_rows instead of the row stride",
+    13: "int3 codes read from the high bits of a unit first",
+    14: "int3 read with offset 3 instead of 4",
 }

@@ -14,9 +14,12 @@ Host byte layout (the library's upload input):
   fmt=3  int2 offset binary (value = crumb - 2), rows of ceil(I/4) bytes,
          element 4j+t in bits [2t, 2t+1] of byte j
   fmt=4  as fmt=2, plus f32 scales [O][ceil(I/gs)]
+  fmt=5  int3 offset binary (value = code - 4), rows of 3*ceil(I/8) bytes:
+         element 8j+t is bits [3t, 3t+2] of the little-endian 24-bit word in
+         bytes 3j..3j+2; f32 scales [O][ceil(I/gs)], gs a multiple of 8
   fmt=7  one FP8 E4M3 byte per element, row-major [O][I], plus f32 scales
          [ceil(O/128)][ceil(I/128)], one per 128 x 128 block
-Scales are f32: [O] for fmt 1-3, [O][ceil(I/gs)] for fmt=4, per block for
+Scales are f32: [O] for fmt 1-3, [O][ceil(I/gs)] for fmt 4 and 5, per block for
 fmt=7, none for fmt=0.
 """
 from __future__ import annotations
@@ -26,8 +29,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
-CODE_RANGE = {1: (-128, 127), 2: (0, 15), 3: (0, 3), 4: (0, 15)}
-OFFSET = {1: 0, 2: 8, 3: 2, 4: 8}
+CODE_RANGE = {1: (-128, 127), 2: (0, 15), 3: (0, 3), 4: (0, 15), 5: (0, 7)}
+OFFSET = {1: 0, 2: 8, 3: 2, 4: 8, 5: 4}
 FP8_BLOCK = 128                       # fmt=7 scale block edge (rows and inputs)
 FP8_NAN = (0x7F, 0xFF)                # the two E4M3 NaN bytes
 
@@ -37,7 +40,7 @@ def rng(seed: int) -> np.random.Generator:
 
 
 def row_bytes(fmt: int, I: int) -> int:
-    return {0: 4 * I, 1: I, 2: (I + 1) // 2, 3: (I + 3) // 4, 4: (I + 1) // 2, 7: I}[fmt]
+    return {0: 4 * I, 1: I, 2: (I + 1) // 2, 3: (I + 3) // 4, 4: (I + 1) // 2, 5: 3 * ((I + 7) // 8), 7: I}[fmt]
 
 
 def n_groups(I: int, gs: int) -> int:
@@ -47,7 +50,7 @@ def n_groups(I: int, gs: int) -> int:
 def scale_count(fmt: int, O: int, I: int, gs: int) -> int:
     if fmt == 0:
         return 0
-    if fmt == 4:
+    if fmt in (4, 5):
         return O * n_groups(I, gs)
     if fmt == 7:
         return n_groups(O, FP8_BLOCK) * n_groups(I, FP8_BLOCK)
@@ -61,7 +64,8 @@ def tensor_bytes(fmt: int, O: int, I: int, gs: int = 0) -> int:
 
 def pack(fmt: int, codes: np.ndarray) -> np.ndarray:
     """Write codes [O, I] in the host byte layout.  codes are raw codes: int8
-    values for fmt=1, nibbles 0..15 for fmt=2/4, crumbs 0..3 for fmt=3."""
+    values for fmt=1, nibbles 0..15 for fmt=2/4, crumbs 0..3 for fmt=3,
+    3-bit codes 0..7 for fmt=5."""
     codes = np.asarray(codes)
     O, I = codes.shape
     if fmt == 1:
@@ -74,6 +78,17 @@ def pack(fmt: int, codes: np.ndarray) -> np.ndarray:
         c = np.zeros((O, 4 * row_bytes(fmt, I)), dtype=np.uint8)
         c[:, :I] = codes
         return (c[:, 0::4] | (c[:, 1::4] << 2) | (c[:, 2::4] << 4) | (c[:, 3::4] << 6)).astype(np.uint8)
+    if fmt == 5:
+        n_units = row_bytes(fmt, I) // 3
+        c = np.zeros((O, 8 * n_units), dtype=np.uint32)
+        c[:, :I] = codes
+        word = np.zeros((O, n_units), dtype=np.uint32)
+        for t in range(8):
+            word |= c[:, t::8] << np.uint32(3 * t)
+        out = np.empty((O, n_units, 3), dtype=np.uint8)
+        for k in range(3):
+            out[:, :, k] = (word >> np.uint32(8 * k)) & np.uint32(0xFF)
+        return out.reshape(O, 3 * n_units)
     raise ValueError(fmt)
 
 
@@ -120,15 +135,15 @@ def random_matrix(g: np.random.Generator, fmt: int, O: int, I: int, gs: int = 0,
 
 def quantize(fmt: int, W: np.ndarray, gs: int = 0) -> Matrix:
     """Symmetric absmax quantiser for the format sweep's N(0, 0.02) weights:
-    scale = absmax / qmax per row (per group for fmt=4), qmax = 127 / 7 / 1,
+    scale = absmax / qmax per row (per group for fmt 4 and 5), qmax = 127 / 7 / 1 / 3,
     code = clip(round(w / scale)) + offset.  Input generation only."""
     W = np.asarray(W, dtype=np.float32)
     O, I = W.shape
     if fmt == 0:
         return Matrix(0, 0, O, I, W.copy(), None)
-    qmax = {1: 127, 2: 7, 3: 1, 4: 7}[fmt]
-    lo = {1: -127, 2: -8, 3: -2, 4: -8}[fmt]
-    if fmt == 4:
+    qmax = {1: 127, 2: 7, 3: 1, 4: 7, 5: 3}[fmt]
+    lo = {1: -127, 2: -8, 3: -2, 4: -8, 5: -4}[fmt]
+    if fmt in (4, 5):
         ng = n_groups(I, gs)
         pad = np.zeros((O, ng * gs), dtype=np.float32)
         pad[:, :I] = W
