@@ -346,6 +346,9 @@ def bench_gemv(coli, torch, peaks, l2_bytes, only=None):
     # FP8 E4M3 with 128 x 128 block scales (uniform over the finite bytes), same shape
     cases.append(("fp8_fmt7_b128", 7, 0, wl.GEMV_SWEEP["O"], wl.GEMV_SWEEP["I"], wl.GEMV_SWEEP["S"],
                   wl.GEMV_SWEEP["seed"]))
+    # int3 (fmt=5) with groups of 64, quantised from the same N(0, 0.02) weights
+    cases.append(("sweep_int3_fmt5_g64", 5, 64, wl.GEMV_SWEEP["O"], wl.GEMV_SWEEP["I"], wl.GEMV_SWEEP["S"],
+                  wl.GEMV_SWEEP["seed"]))
     if only:
         cases = [c for c in cases if c[0] == only]
         if not cases:
@@ -607,15 +610,15 @@ def bench_absorb(coli, torch, peaks, l2_bytes):
 def bench_decode_formats(coli, torch, peaks, steps=200, only=None):
     """The decode expert block (H=6144, F=2048, S=1, top-8 of 256 resident
     experts, a fresh softmax top-8 routing per call) for every expert format:
-    f32, int8, int4 per-row, int2, int4 g64 (the headline's), int4 g128 and FP8
-    E4M3 with 128x128 block scales.  The 256 experts are distinct device copies
+    f32, int8, int4 per-row, int2, int4 g64 (the headline's), int4 g128, int3
+    g64 and FP8 E4M3 with 128x128 block scales.  The 256 experts are distinct device copies
     of 8 generated ones, so every pool is far larger than L2 (the smallest,
     int2, is 2.5 GB)."""
     d = wl.MOE_DECODE
     H, F, K, E = d["H"], d["F"], d["K"], d["E"]
     out = {}
     cases = (("f32_fmt0", 0, 0), ("int8_fmt1", 1, 0), ("int4_fmt2", 2, 0), ("int2_fmt3", 3, 0),
-             ("int4_fmt4_g64", 4, 64), ("int4_fmt4_g128", 4, 128), ("fp8_fmt7_b128", 7, 0))
+             ("int4_fmt4_g64", 4, 64), ("int4_fmt4_g128", 4, 128), ("int3_fmt5_g64", 5, 64), ("fp8_fmt7_b128", 7, 0))
     for name, fmt, gs in cases:
         if only and name != only:
             continue

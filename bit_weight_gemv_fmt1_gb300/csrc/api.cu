@@ -201,6 +201,7 @@ int64_t host_row_bytes(int fmt, int64_t I) {
     case 1: return I;
     case 2: case 4: return (I + 1) / 2;
     case 3: return (I + 3) / 4;
+    case 5: return 3 * ((I + 7) / 8);
     case 7: return I;
     default: return -1;
     }
@@ -211,7 +212,7 @@ MatDesc desc_of(const coli_tensor *t) {
     m.q = t->q;
     m.s = t->s;
     m.rs = t->rs;
-    m.gs = t->fmt == 4 ? t->gs : t->fmt == 7 ? kFp8Block : 0;
+    m.gs = (t->fmt == 4 || t->fmt == 5) ? t->gs : t->fmt == 7 ? kFp8Block : 0;
     m.ng = t->ng;
     m.tmap = t->tmap;
     return m;
@@ -254,10 +255,12 @@ static int check_upload(int fmt, int gs, int64_t O, int64_t I, const void *data,
                         coli_tensor **out) {
     if (!out) return fail(COLI_EINVAL, "out is NULL");
     *out = nullptr;
-    if (fmt < 0 || (fmt > 4 && fmt != 7))
-        return fail(COLI_EFMT, "unknown weight format %d (supported: 0..4, 7)", fmt);
+    if (fmt < 0 || fmt == 6 || fmt > 7)
+        return fail(COLI_EFMT, "unknown weight format %d (supported: 0..5, 7)", fmt);
     if (fmt == 4 && (gs < 2 || (gs & 1)))
         return fail(COLI_EFMT, "fmt=4 needs an even group size >= 2, got gs=%d", gs);
+    if (fmt == 5 && (gs < 8 || gs % 8 != 0))
+        return fail(COLI_EFMT, "fmt=5 needs a group size that is a multiple of 8, got gs=%d", gs);
     if (O < 1 || I < 1) return fail(COLI_EINVAL, "O and I must be >= 1 (got O=%lld I=%lld)", (long long)O, (long long)I);
     if (O > (1LL << 31) - 1 || I > (1LL << 30))
         return fail(COLI_EINVAL, "matrix too large (O=%lld I=%lld)", (long long)O, (long long)I);
@@ -270,15 +273,17 @@ static int check_upload(int fmt, int gs, int64_t O, int64_t I, const void *data,
 static coli_tensor *new_tensor(int fmt, int gs, int64_t O, int64_t I, int64_t *n_scales) {
     coli_tensor *t = new coli_tensor();
     t->fmt = fmt;
-    t->gs = fmt == 4 ? gs : 0;
+    t->gs = (fmt == 4 || fmt == 5) ? gs : 0;
     t->O = O;
     t->I = I;
-    t->ng = fmt == 4 ? (int)((I + gs - 1) / gs) : fmt == 7 ? (int)((I + kFp8Block - 1) / kFp8Block) : 1;
+    t->ng = (fmt == 4 || fmt == 5) ? (int)((I + gs - 1) / gs)
+            : fmt == 7             ? (int)((I + kFp8Block - 1) / kFp8Block)
+                                   : 1;
     const int64_t hrb = host_row_bytes(fmt, I);
     t->rs = (hrb + 15) / 16 * 16;
     t->cpr = (int)((I + epc_of(fmt) - 1) / epc_of(fmt));
-    *n_scales = fmt == 0   ? 0
-                : fmt == 4 ? O * t->ng
+    *n_scales = fmt == 0                 ? 0
+                : (fmt == 4 || fmt == 5) ? O * t->ng
                 : fmt == 7 ? (O + kFp8Block - 1) / kFp8Block * t->ng
                            : O;
     t->alg_bytes = O * hrb + 4 * *n_scales;
@@ -412,6 +417,31 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
     const size_t smem = gemv_smem_bytes(W0->fmt, W0->cpr, S, (int)W0->I, generic);
     bool slab = S == 1 && !generic;
     for (int m = 0; m < n && slab; m++) slab = slab_supported(W[m]->fmt, W[m]->gs) && W[m]->gs == W0->gs;
+    // int3 (fmt=5), S <= 8: the CUDA-core matvec of int3.cu (larger S: the tiled GEMM below)
+    if (W0->fmt == 5 && S <= 8) {
+        GemvJob job;
+        memset(&job, 0, sizeof job);
+        job.n = n;
+        job.fmt = 5;
+        job.I = (int)W0->I;
+        job.S = S;
+        job.x = x;
+        for (int m = 0; m < n; m++) {
+            job.q[m] = W[m]->q;
+            job.s[m] = W[m]->s;
+            job.y[m] = y[m];
+            job.O[m] = (int)W[m]->O;
+            job.gs[m] = W[m]->gs;
+            job.ng[m] = W[m]->ng;
+            job.rs[m] = W[m]->rs;
+            job.row_start[m + 1] = job.row_start[m] + job.O[m];
+        }
+        job.err = ds->err;
+        cudaError_t e = launch_gemv_i3(job, ds->n_sm, st);
+        if (e != cudaSuccess) return cuda_fail(e, "int3 matvec launch");
+        count(1, wbytes);
+        return COLI_OK;
+    }
     if (S <= 8 && smem <= ds->smem_optin) {
         GemvJob job;
         memset(&job, 0, sizeof job);
@@ -632,6 +662,9 @@ static int run_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_
     if (o0 + (int64_t)(n_heads - 1) * stride + n_rows > W->O)
         return fail(COLI_EINVAL, "head rows run past the matrix: o0 + (n_heads-1)*stride + n_rows = %lld > O = %lld",
                     (long long)(o0 + (int64_t)(n_heads - 1) * stride + n_rows), (long long)W->O);
+    if (W->fmt == 5)
+        return fail(COLI_EFMT, "%s: fmt=5 (int3) is not supported by the row-range products",
+                    transposed ? "coli_matmul_rows_t" : "coli_matmul_rows");
     if (int rc = injected()) return rc;
     DeviceState *ds = nullptr;
     if (int rc = device_state(&ds)) return rc;
@@ -1068,8 +1101,8 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         }
     }
 
-    // ---------------- decode: one cooperative launch
-    if (n_slots <= kMaxDecodeSlots && gs_ok) {
+    // ---------------- decode: one cooperative launch (16-byte chunk formats; int3 takes the pipeline below)
+    if (n_slots <= kMaxDecodeSlots && gs_ok && fmt != 5) {
         const int xlen_gu = staged_len(fmt, cpr_gu), xlen_d = staged_len(fmt, cpr_d);
         const size_t budget = 110 * 1024 / 4;   // floats per CTA: two CTAs per SM
         const int rpc_alloc = (int)((H + ds->n_sm - 1) / ds->n_sm);

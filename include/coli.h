@@ -4,7 +4,7 @@
  *
  * The operation (colibri project pages):
  *   - y[s][o] = sum_i w[o][i] * x[s][i] over a quantized weight matrix W [O][I]
- *     in one of six formats (PR #298 page, commit message "metal: grouped-int4
+ *     in one of seven formats (PR #298 page, commit message "metal: grouped-int4
  *     (fmt=4) GEMV support": mm_gemv handled "fmt 0-3", fmt=4 added with one f32
  *     scale per gs inputs folded into the accumulation per group; commit message
  *     "CUDA backend had no fmt=4 case": per-row scale for fmt 1/2/3, per-group
@@ -27,6 +27,13 @@
  *   fmt=4  int4 as fmt=2; scales f32 [O][ceil(I/gs)], group g covering inputs
  *          [g*gs, min((g+1)*gs, I)) (PR #298 page, test_i4_grouped commit: the
  *          partial last group and gs > I).
+ *   fmt=5  int3 offset binary, value = code - 4; rows of 3*ceil(I/8) bytes;
+ *          element 8j+t is bits [3t, 3t+2] of the little-endian 24-bit word in
+ *          bytes 3j..3j+2; scales f32 [O][ceil(I/gs)] as for fmt=4, gs a
+ *          multiple of 8 (PR #298 page: "int3 fmt=5" in the #377 retarget
+ *          list; the Vulkan fmt=4 commit message skips the per-row scale "like
+ *          fmt=5"; the bit layout is this library's reading, the pages print
+ *          none).
  *   fmt=7  FP8 E4M3 (OCP: sign, 4 exponent bits with bias 7, 3 mantissa bits,
  *          exponent 0 subnormal, no infinities, S.1111.111 NaN), one byte per
  *          element, [O][I]; scales f32 [ceil(O/128)][ceil(I/128)], one per
@@ -36,7 +43,7 @@
  *          E4M3 encoding is this library's reading of its "fp8 passthrough").
  * The int4 offset encoding and the extremes 0x00 -> -8, 0xFF -> +7 are printed
  * on the PR #298 page (test_i4_grouped commit message); the element order in a
- * byte, the int2 and int8 encodings are this library's documented readings.
+ * byte, the int2, int3 and int8 encodings are this library's documented readings.
  *
  * Conventions for every entry point:
  *   - Return 0 (COLI_OK) or a negative COLI_E* code; coli_last_error() then
@@ -93,8 +100,9 @@ typedef struct {
  * Upload one weight matrix W [O][I] (PR #298 page, "CUDA backend had no fmt=4
  * case" commit message: coli_cuda_tensor_upload_grouped takes gs and stores
  * O*ceil(I/gs) scales; this entry point is that upload for every format).
- *   fmt     0..4 or 7 as in the layout above.
+ *   fmt     0..5 or 7 as in the layout above.
  *   gs      fmt=4: group size, even and >= 2 (gs >= I means one group per row).
+ *           fmt=5: group size, a multiple of 8.
  *           Other formats: ignored (fmt=7 blocks are always 128 x 128).
  *   O, I    rows (outputs) and columns (inputs), each >= 1, I <= 2^30.
  *   data    HOST pointer to the packed codes in the host layout above.
@@ -150,7 +158,8 @@ int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_
  *           runs the bandwidth-bound CUDA-core matvec kernels, S = 1 the
  *           slab kernel for fmt 0/1/2/4; larger S runs the tensor-core GEMM
  *           for fmt=2 and for fmt=4 with gs % 64 == 0, the tiled CUDA-core
- *           GEMM otherwise (fmt 0, 1, 3, 7).
+ *           GEMM otherwise (fmt 0, 1, 3, 5, 7).  fmt=5 at S <= 8 runs its own
+ *           CUDA-core matvec.
  * Errors: COLI_EINVAL (NULL/misaligned pointer, S < 1), COLI_EDEVICE, COLI_ECUDA.
  */
 int coli_matmul(const coli_tensor *W, const float *x, float *y, int S, void *stream);
@@ -179,12 +188,13 @@ int coli_matmul_multi(int n, const coli_tensor *const *W, const float *x, float 
  *                       x: device f32 [S][n_heads][I]; y: [S][n_heads][n_rows]
  *   coli_matmul_rows_t  y[s][h][i] = sum_j x[s][h][j] * W[o0 + h*stride + j][i]
  *                       x: device f32 [S][n_heads][n_rows]; y: [S][n_heads][I]
- *   W       any format (device or host resident); y overwritten, must not overlap x.
+ *   W       any format but fmt=5 (device or host resident; int3 is refused with
+ *           COLI_EFMT); y overwritten, must not overlap x.
  *   o0, stride, n_rows, n_heads  o0 >= 0, stride >= 0 (heads may share rows),
  *           1 <= n_rows <= 2^30, n_heads >= 1, o0 + (n_heads-1)*stride + n_rows <= O.
  *   S       rows of activations, >= 1 (each weight row is read once per 4 of them).
  * Errors: COLI_EINVAL (pointers, ranges, a head's activations too long for the
- * shared-memory stage), COLI_EDEVICE, COLI_ECUDA.
+ * shared-memory stage), COLI_EFMT (fmt=5), COLI_EDEVICE, COLI_ECUDA.
  */
 int coli_matmul_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_rows, int n_heads,
                      const float *x, float *y, int S, void *stream);
@@ -268,7 +278,8 @@ int coli_moe_router(const float *x, int S, const coli_tensor *router, const floa
  * otherwise the slab kernel (S = 1) or the general decode kernel.  Larger S*K
  * runs the prefill pipeline (routing, gather, grouped gate/up, grouped down,
  * combine) on the tensor cores for int4 tables with gs % 64 == 0, on the CUDA
- * cores otherwise.  Every call checks the whole table (shapes, formats,
+ * cores otherwise; int3 (fmt=5) tables take the CUDA-core pipeline at every
+ * S*K.  Every call checks the whole table (shapes, formats,
  * device) on the host: for a table used over and over, create it once with
  * coli_expert_table_create and call coli_moe_block_t.  An id out of range is
  * recorded for coli_sync_check(stream) and y is then unspecified.
@@ -319,7 +330,7 @@ int coli_moe_block_t(const float *x, int S, const coli_expert_table *table, cons
  *   Limits (refused with COLI_EINVAL, nothing launched): S*K <= 64,
  *   n_experts <= 1024, S*K*F <= 524288, and the activations must fit the
  *   single-launch decode kernel's shared memory; fmt=4 needs gs % 32 == 0
- *   (COLI_EFMT).
+ *   and fmt=5 tables are refused (COLI_EFMT).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress).  The expert descriptors go to the array through the
  * parameters of a small copy kernel, and only when they differ from the ones

@@ -44,7 +44,8 @@ def test_version(lib):
     assert b"sm_103a" in lib.coli_version()
 
 
-@pytest.mark.parametrize("fmt,gs,code", [(5, 0, -2), (6, 0, -2), (8, 0, -2), (-1, 0, -2), (4, 0, -2), (4, 63, -2), (4, 1, -2)])
+@pytest.mark.parametrize("fmt,gs,code", [(5, 0, -2), (5, 4, -2), (5, 12, -2), (6, 0, -2), (8, 0, -2), (-1, 0, -2),
+                                         (4, 0, -2), (4, 63, -2), (4, 1, -2)])
 def test_upload_refuses_bad_format(lib, fmt, gs, code):
     lib.coli_last_error.restype = ctypes.c_char_p
     out = ctypes.c_void_p(123)

@@ -105,3 +105,9 @@ def test_refusals():
             coli.matmul_rows(W, *args, x, y)
         with pytest.raises(coli.ColiError):
             coli.matmul_rows_t(W, *args, x, y)
+    # int3 is refused by the row-range products, with the format error
+    W5 = upload(coli, wl.random_matrix(g, 5, 100, 64, 8))
+    for fn in (coli.matmul_rows, coli.matmul_rows_t):
+        with pytest.raises(coli.ColiError) as ei:
+            fn(W5, 0, 50, 50, 2, x, y)
+        assert ei.value.code == coli.COLI_EFMT

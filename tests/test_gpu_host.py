@@ -16,7 +16,7 @@ def _host(coli, m):
     return coli.tensor_upload_host(m.fmt, m.gs, m.O, m.I, m.data, m.scales)
 
 
-@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 6), (7, 0)])
+@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 6), (5, 16), (7, 0)])
 @pytest.mark.parametrize("S", [1, 3, 12])
 def test_host_matmul(fmt, gs, S):
     torch = cuda_or_skip()
@@ -48,7 +48,7 @@ def test_host_and_device_in_one_multi_call():
         assert norm_err(y.cpu().numpy(), orc.matmul(4, 64, m.O, 6144, m.data, m.scales, x)) <= TOL
 
 
-@pytest.mark.parametrize("fmt,gs", [(4, 64), (2, 0), (7, 0)])
+@pytest.mark.parametrize("fmt,gs", [(4, 64), (2, 0), (7, 0), (5, 64)])
 @pytest.mark.parametrize("S,K", [(1, 8), (3, 4), (20, 8)])
 def test_moe_block_mixed_residency(fmt, gs, S, K):
     """An expert table with some experts in host memory and the rest in HBM:

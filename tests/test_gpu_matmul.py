@@ -15,7 +15,7 @@ from oracle import oracle as orc
 
 pytestmark = pytest.mark.gpu
 
-FMT_CASES = [(0, 0), (1, 0), (2, 0), (3, 0), (4, 32), (4, 64), (4, 128), (7, 0)]
+FMT_CASES = [(0, 0), (1, 0), (2, 0), (3, 0), (4, 32), (4, 64), (4, 128), (5, 8), (5, 64), (7, 0)]
 
 
 def _run(coli, torch, m, x):
@@ -40,7 +40,7 @@ def test_matvec_formats(fmt, gs, S):
     assert norm_err(got, ref) <= TOL
 
 
-@pytest.mark.parametrize("fmt,gs", FMT_CASES + [(4, 2), (4, 6), (4, 16), (4, 48), (4, 4096)])
+@pytest.mark.parametrize("fmt,gs", FMT_CASES + [(4, 2), (4, 6), (4, 16), (4, 48), (4, 4096), (5, 24), (5, 4096)])
 @pytest.mark.parametrize("O,I", [(1, 1), (3, 7), (5, 31), (17, 33), (9, 65), (64, 1023), (7, 1025), (130, 4097)])
 def test_ragged_shapes(fmt, gs, O, I):
     torch = cuda_or_skip()
@@ -54,7 +54,8 @@ def test_ragged_shapes(fmt, gs, O, I):
 
 
 @pytest.mark.parametrize("fmt,gs,O,I", [(1, 0, 70, 3000), (2, 0, 70, 3001), (3, 0, 65, 2999), (4, 64, 66, 3000),
-                                        (4, 128, 40, 700), (4, 16, 33, 500), (4, 6, 9, 100)])
+                                        (4, 128, 40, 700), (4, 16, 33, 500), (4, 6, 9, 100), (5, 8, 70, 3001),
+                                        (5, 64, 66, 3000), (5, 24, 9, 100)])
 @pytest.mark.parametrize("S", [1, 4, 20])
 def test_exact_integer_cases(fmt, gs, O, I, S):
     """Power-of-two scales and integer x in [-8, 8]: every product and partial
@@ -84,7 +85,7 @@ def test_fmt4_wide_group_equals_fmt2():
 
 
 @pytest.mark.parametrize("S", [9, 16, 33, 70])
-@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 10), (7, 0)])
+@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 10), (5, 16), (7, 0)])
 def test_large_s_gemm_path(fmt, gs, S):
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
@@ -185,7 +186,7 @@ def test_single_gemv_workload():
     assert norm_err(got, ref) <= TOL
 
 
-@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 128)])
+@pytest.mark.parametrize("fmt,gs", [(0, 0), (1, 0), (2, 0), (3, 0), (4, 64), (4, 128), (5, 64)])
 @pytest.mark.parametrize("S", [1, 2, 4])
 def test_format_sweep_workload(fmt, gs, S):
     """Format sweep at full size: I=6144, O=2048, N(0,0.02) weights quantised
@@ -401,3 +402,39 @@ def test_tensor_core_matvec_multi_ragged(fmt, gs, S):
     for mm, y in zip(mats, ys):
         ref = orc.matmul(fmt, gs, mm.O, I, mm.data, mm.scales, x)
         assert norm_err(y.cpu().numpy(), ref) <= TOL
+
+
+@pytest.mark.parametrize("S", [1, 3, 8, 12])
+def test_int3_multi_different_groups(S):
+    """coli_matmul_multi over int3 matrices of different O and gs sharing one x
+    (the matvec for S <= 8, the tiled GEMM above), each against the oracle."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(800 + S)
+    I = 1000
+    mats = [wl.random_matrix(g, 5, O, I, gs) for O, gs in ((300, 8), (17, 64), (129, 24), (64, 1024))]
+    Ws = [upload(coli, m) for m in mats]
+    x = wl.activations(g, S, I)
+    ys = [torch.full((S, m.O), float("nan"), device="cuda") for m in mats]
+    coli.matmul_multi(Ws, torch.from_numpy(x).cuda(), ys)
+    coli.sync_check()
+    for m, y in zip(mats, ys):
+        assert norm_err(y.cpu().numpy(), orc.matmul(5, m.gs, m.O, I, m.data, m.scales, x)) <= TOL
+
+
+def test_int3_unaligned_activations():
+    """int3 matvec with x at a 4-byte (not 16-byte) offset: the scalar-load
+    path of the kernel, against the oracle."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(810)
+    m = wl.random_matrix(g, 5, 200, 640, 32)
+    x = wl.activations(g, 2, 640)
+    W = upload(coli, m)
+    buf = torch.zeros(2 * 640 + 1, device="cuda")
+    buf[1:].copy_(torch.from_numpy(x.reshape(-1)))
+    xd = buf[1:].view(2, 640)
+    y = torch.full((2, 200), float("nan"), device="cuda")
+    coli.matmul(W, xd, y)
+    coli.sync_check()
+    assert norm_err(y.cpu().numpy(), orc.matmul(5, 32, 200, 640, m.data, m.scales, x)) <= TOL

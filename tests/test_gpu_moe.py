@@ -42,7 +42,8 @@ def _run_block(coli, torch, table, x, ids, w, H):
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (2, 0), (1, 0), (3, 0), (0, 0), (4, 32), (7, 0)])
+@pytest.mark.parametrize("fmt,gs", [(4, 64), (4, 128), (2, 0), (1, 0), (3, 0), (0, 0), (4, 32), (5, 64), (5, 24),
+                                    (7, 0)])
 @pytest.mark.parametrize("S,K", [(1, 8), (2, 4), (4, 8), (8, 8)])
 def test_decode_block(fmt, gs, S, K):
     torch = cuda_or_skip()
@@ -142,7 +143,7 @@ def test_decode_ragged_routing_and_empty_slots():
     assert np.all(got[2] == 0.0)
 
 
-@pytest.mark.parametrize("fmt,gs", [(4, 128), (4, 64), (2, 0), (4, 16), (1, 0), (7, 0), (0, 0), (3, 0)])
+@pytest.mark.parametrize("fmt,gs", [(4, 128), (4, 64), (2, 0), (4, 16), (1, 0), (7, 0), (0, 0), (3, 0), (5, 64)])
 @pytest.mark.parametrize("S,K", [(9, 8), (40, 4), (100, 8)])
 def test_prefill_block(fmt, gs, S, K):
     torch = cuda_or_skip()
