@@ -207,12 +207,29 @@ int64_t host_row_bytes(int fmt, int64_t I) {
     }
 }
 
+// Row of an int3 (fmt=5) upload, 3*ceil(I/8) bytes (element 8j+t is bits [3t, 3t+2] of the
+// little-endian 24-bit word in bytes 3j..3j+2), written as the int4 row of the device layout,
+// ceil(I/2) bytes: element i's code c becomes the nibble c + 4, element 2j the low nibble of
+// byte j.  The nibbles past I are zero.
+void int3_row_to_int4(const uint8_t *src, int64_t I, uint8_t *dst) {
+    const int64_t nb = (I + 1) / 2;
+    memset(dst, 0, (size_t)nb);
+    for (int64_t u = 0; 8 * u < I; u++) {
+        const uint32_t w = (uint32_t)src[3 * u] | ((uint32_t)src[3 * u + 1] << 8) | ((uint32_t)src[3 * u + 2] << 16);
+        for (int t = 0; t < 8 && 8 * u + t < I; t++) {
+            const int64_t i = 8 * u + t;
+            const uint8_t nib = (uint8_t)(((w >> (3 * t)) & 7u) + 4u);
+            dst[i / 2] |= (i & 1) ? (uint8_t)(nib << 4) : nib;
+        }
+    }
+}
+
 MatDesc desc_of(const coli_tensor *t) {
     MatDesc m;
     m.q = t->q;
     m.s = t->s;
     m.rs = t->rs;
-    m.gs = (t->fmt == 4 || t->fmt == 5) ? t->gs : t->fmt == 7 ? kFp8Block : 0;
+    m.gs = t->fmt == 4 ? t->gs : t->fmt == 7 ? kFp8Block : 0;
     m.ng = t->ng;
     m.tmap = t->tmap;
     return m;
@@ -270,23 +287,26 @@ static int check_upload(int fmt, int gs, int64_t O, int64_t I, const void *data,
 }
 
 // A new tensor with the shape, layout and byte counts of (fmt, gs, O, I); no storage yet.
+// int3 (fmt=5) is stored as int4 nibbles with fmt=4's group scales: code c becomes the nibble
+// c + 4, whose int4 value (nibble - 8) is the int3 value c - 4, so every int4 kernel serves it
+// (the device copy, and what the kernels read, is 4/3 of the int3 bytes).
 static coli_tensor *new_tensor(int fmt, int gs, int64_t O, int64_t I, int64_t *n_scales) {
     coli_tensor *t = new coli_tensor();
-    t->fmt = fmt;
-    t->gs = (fmt == 4 || fmt == 5) ? gs : 0;
+    const int dfmt = fmt == 5 ? 4 : fmt;
+    t->ufmt = fmt;
+    t->fmt = dfmt;
+    t->gs = dfmt == 4 ? gs : 0;
     t->O = O;
     t->I = I;
-    t->ng = (fmt == 4 || fmt == 5) ? (int)((I + gs - 1) / gs)
-            : fmt == 7             ? (int)((I + kFp8Block - 1) / kFp8Block)
-                                   : 1;
-    const int64_t hrb = host_row_bytes(fmt, I);
+    t->ng = dfmt == 4 ? (int)((I + gs - 1) / gs) : dfmt == 7 ? (int)((I + kFp8Block - 1) / kFp8Block) : 1;
+    const int64_t hrb = host_row_bytes(dfmt, I);
     t->rs = (hrb + 15) / 16 * 16;
-    t->cpr = (int)((I + epc_of(fmt) - 1) / epc_of(fmt));
-    *n_scales = fmt == 0                 ? 0
-                : (fmt == 4 || fmt == 5) ? O * t->ng
-                : fmt == 7 ? (O + kFp8Block - 1) / kFp8Block * t->ng
-                           : O;
-    t->alg_bytes = O * hrb + 4 * *n_scales;
+    t->cpr = (int)((I + epc_of(dfmt) - 1) / epc_of(dfmt));
+    *n_scales = dfmt == 0   ? 0
+                : dfmt == 4 ? O * t->ng
+                : dfmt == 7 ? (O + kFp8Block - 1) / kFp8Block * t->ng
+                            : O;
+    t->alg_bytes = O * host_row_bytes(fmt, I) + 4 * *n_scales;
     t->dev_bytes = O * t->rs + 4 * *n_scales;
     t->uid = g_uid++;
     return t;
@@ -304,7 +324,15 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
 
     int64_t n_scales = 0;
     coli_tensor *t = new_tensor(fmt, gs, O, I, &n_scales);
-    const int64_t hrb = host_row_bytes(fmt, I);
+    const int64_t hrb = host_row_bytes(t->fmt, I);   // bytes of a row in the device layout, unpadded
+    std::vector<uint8_t> conv;                        // int3 rows as int4 (kept until the copy completed)
+    if (fmt == 5) {
+        conv.resize((size_t)(O * hrb));
+        const int64_t srb = host_row_bytes(5, I);
+        for (int64_t o = 0; o < O; o++)
+            int3_row_to_int4((const uint8_t *)data + o * srb, I, conv.data() + o * hrb);
+        data = conv.data();
+    }
     t->device = device;
     cudaError_t e = cudaMalloc(&t->q, (size_t)(O * t->rs));
     if (e == cudaSuccess && n_scales) e = cudaMalloc(&t->s, (size_t)n_scales * 4);
@@ -318,7 +346,7 @@ int coli_tensor_upload(int fmt, int gs, int64_t O, int64_t I, const void *data, 
         e = launch_fmt1_encode(t->q, O * t->rs, st);
         g_launches++;
     }
-    if (e == cudaSuccess && (fmt == 2 || fmt == 4)) {
+    if (e == cudaSuccess && (t->fmt == 2 || t->fmt == 4)) {
         // without a map (a shape the TMA descriptor rejects) the tensor-core path is not used for this tensor
         alignas(64) unsigned char map[128];
         if (encode_codes_map(t->q, t->rs, O, map) == cudaSuccess) {
@@ -345,7 +373,8 @@ int coli_tensor_upload_host(int fmt, int gs, int64_t O, int64_t I, const void *d
     CU(cudaGetDevice(&device), "cudaGetDevice");
     int64_t n_scales = 0;
     coli_tensor *t = new_tensor(fmt, gs, O, I, &n_scales);
-    const int64_t hrb = host_row_bytes(fmt, I);
+    const int64_t hrb = host_row_bytes(t->fmt, I);   // bytes of a row in the device layout, unpadded
+    const int64_t srb = host_row_bytes(fmt, I);      // bytes of a row as uploaded
     t->host = 1;
     t->dev_bytes = 0;
     t->device = device;
@@ -359,7 +388,10 @@ int coli_tensor_upload_host(int fmt, int gs, int64_t O, int64_t I, const void *d
         const uint8_t *src = (const uint8_t *)data;
         for (int64_t o = 0; o < O; o++) {
             uint8_t *row = q + o * t->rs;
-            memcpy(row, src + o * hrb, (size_t)hrb);
+            if (fmt == 5)
+                int3_row_to_int4(src + o * srb, I, row);
+            else
+                memcpy(row, src + o * srb, (size_t)hrb);
             memset(row + hrb, 0, (size_t)(t->rs - hrb));
             if (fmt == 1)
                 for (int64_t i = 0; i < hrb; i++) row[i] ^= 0x80;
@@ -393,7 +425,7 @@ void coli_tensor_free(coli_tensor *t) {
 int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_t *I, int64_t *device_bytes,
                      int64_t *alg_bytes) {
     if (!t) return fail(COLI_EINVAL, "tensor is NULL");
-    if (fmt) *fmt = t->fmt;
+    if (fmt) *fmt = t->ufmt;
     if (gs) *gs = t->gs;
     if (O) *O = t->O;
     if (I) *I = t->I;
@@ -417,31 +449,6 @@ static int run_matmul(int n, const coli_tensor *const *W, const float *x, float 
     const size_t smem = gemv_smem_bytes(W0->fmt, W0->cpr, S, (int)W0->I, generic);
     bool slab = S == 1 && !generic;
     for (int m = 0; m < n && slab; m++) slab = slab_supported(W[m]->fmt, W[m]->gs) && W[m]->gs == W0->gs;
-    // int3 (fmt=5), S <= 8: the CUDA-core matvec of int3.cu (larger S: the tiled GEMM below)
-    if (W0->fmt == 5 && S <= 8) {
-        GemvJob job;
-        memset(&job, 0, sizeof job);
-        job.n = n;
-        job.fmt = 5;
-        job.I = (int)W0->I;
-        job.S = S;
-        job.x = x;
-        for (int m = 0; m < n; m++) {
-            job.q[m] = W[m]->q;
-            job.s[m] = W[m]->s;
-            job.y[m] = y[m];
-            job.O[m] = (int)W[m]->O;
-            job.gs[m] = W[m]->gs;
-            job.ng[m] = W[m]->ng;
-            job.rs[m] = W[m]->rs;
-            job.row_start[m + 1] = job.row_start[m] + job.O[m];
-        }
-        job.err = ds->err;
-        cudaError_t e = launch_gemv_i3(job, ds->n_sm, st);
-        if (e != cudaSuccess) return cuda_fail(e, "int3 matvec launch");
-        count(1, wbytes);
-        return COLI_OK;
-    }
     if (S <= 8 && smem <= ds->smem_optin) {
         GemvJob job;
         memset(&job, 0, sizeof job);
@@ -662,9 +669,6 @@ static int run_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_
     if (o0 + (int64_t)(n_heads - 1) * stride + n_rows > W->O)
         return fail(COLI_EINVAL, "head rows run past the matrix: o0 + (n_heads-1)*stride + n_rows = %lld > O = %lld",
                     (long long)(o0 + (int64_t)(n_heads - 1) * stride + n_rows), (long long)W->O);
-    if (W->fmt == 5)
-        return fail(COLI_EFMT, "%s: fmt=5 (int3) is not supported by the row-range products",
-                    transposed ? "coli_matmul_rows_t" : "coli_matmul_rows");
     if (int rc = injected()) return rc;
     DeviceState *ds = nullptr;
     if (int rc = device_state(&ds)) return rc;
@@ -1101,8 +1105,8 @@ static int moe_run(const MoeInfo &mi, const ExpertDesc *table, DeviceState *ds, 
         }
     }
 
-    // ---------------- decode: one cooperative launch (16-byte chunk formats; int3 takes the pipeline below)
-    if (n_slots <= kMaxDecodeSlots && gs_ok && fmt != 5) {
+    // ---------------- decode: one cooperative launch
+    if (n_slots <= kMaxDecodeSlots && gs_ok) {
         const int xlen_gu = staged_len(fmt, cpr_gu), xlen_d = staged_len(fmt, cpr_d);
         const size_t budget = 110 * 1024 / 4;   // floats per CTA: two CTAs per SM
         const int rpc_alloc = (int)((H + ds->n_sm - 1) / ds->n_sm);

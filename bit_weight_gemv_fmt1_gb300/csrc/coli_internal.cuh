@@ -28,7 +28,8 @@
 #include "coli.h"
 
 struct coli_tensor {
-    int fmt, gs, ng, device;
+    int fmt, gs, ng, device;   // fmt: the device layout's format (int3 is stored as int4, below)
+    int ufmt;                  // the format the caller uploaded
     int64_t O, I;
     int64_t rs;          // device row stride in bytes (multiple of 16)
     int cpr;             // 16-byte chunks per row that hold data
@@ -473,8 +474,6 @@ struct GemvJob {
 };
 
 cudaError_t launch_gemv(const GemvJob &job, cudaStream_t st, int *n_launch);
-// The S <= 8 matvec of int3 (fmt=5) weights (int3.cu); job.gs holds each matrix's group size.
-cudaError_t launch_gemv_i3(const GemvJob &job, int n_sm, cudaStream_t st);
 
 // Launch `kern` with programmatic stream serialization allowed (see pdl_wait).
 template <class... P, class... A>
@@ -513,7 +512,7 @@ struct ExpertDesc {
 // row's own scale(s), or for fmt=7 the scales of the row's block-row.
 __device__ __forceinline__ const float *row_scales(int fmt, const MatDesc &m, int row) {
     if (fmt == 0) return nullptr;
-    if (fmt == 4 || fmt == 5) return m.s + (size_t)row * m.ng;
+    if (fmt == 4) return m.s + (size_t)row * m.ng;
     if (fmt == 7) return m.s + (size_t)(row / kFp8Block) * m.ng;
     return m.s + row;
 }
@@ -530,12 +529,6 @@ __device__ __forceinline__ float decode_elem(int fmt, const uint8_t *row, const 
     case 1: return (float)((int)row[i] - 128) * rscale[0];
     case 2: { const uint8_t b = row[i >> 1]; return (float)(((i & 1) ? (b >> 4) : (b & 0xF)) - 8) * rscale[0]; }
     case 3: { const uint8_t b = row[i >> 2]; return (float)(((b >> (2 * (i & 3))) & 3) - 2) * rscale[0]; }
-    case 5: {
-        // int3: element 8j+t is bits [3t, 3t+2] of the little-endian 24-bit word in bytes 3j..3j+2
-        const uint8_t *u = row + 3 * (i >> 3);
-        const uint32_t w = (uint32_t)u[0] | ((uint32_t)u[1] << 8) | ((uint32_t)u[2] << 16);
-        return (float)((int)((w >> (3 * (i & 7))) & 7u) - 4) * rscale[i / gs];
-    }
     case 7: return e4m3_to_f32(row[i]) * rscale[i / kFp8Block];
     default: { const uint8_t b = row[i >> 1]; return (float)(((i & 1) ? (b >> 4) : (b & 0xF)) - 8) * rscale[i / gs]; }
     }
@@ -790,6 +783,7 @@ cudaError_t launch_table_fill(ExpertDesc *dst, const ExpertDesc *src, int n, cud
 
 constexpr int kDecodeThreads = 256;
 constexpr int kMaxDecodeSlots = 64;
+
 constexpr int kGemmBP = 32;    // token rows per GEMM tile
 
 }  // namespace coli

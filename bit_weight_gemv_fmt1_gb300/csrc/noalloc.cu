@@ -105,7 +105,6 @@ extern "C" int coli_moe_block_noalloc(const float *x, int S, const coli_expert *
     if (!g0) return bad(COLI_EINVAL, "expert 0 gate is NULL");
     const long long F = g0->O, H = g0->I;
     const int fmt = g0->fmt;
-    if (fmt == 5) return bad(COLI_EFMT, "fmt=5 (int3) tables are not supported by the no-allocation block");
     for (int e = 0; e < n_experts; e++) {
         const coli_tensor *m[3] = {experts[e].gate, experts[e].up, experts[e].down};
         for (int k = 0; k < 3; k++) {

@@ -1280,7 +1280,7 @@ cudaError_t launch_stream_gemv_s(const GemvJob &job, int rpc, int RG, int gshift
 
 // gs (fmt=4) usable by the slab kernels: a power-of-two number of 32-input chunks.
 bool slab_supported(int fmt, int gs) {
-    if (fmt == 3 || fmt == 5 || fmt == 7) return false;
+    if (fmt == 3 || fmt == 7) return false;
     if (fmt == 4) return gs % 32 == 0 && log2_exact(gs / 32) >= 0;
     return true;
 }

@@ -33,7 +33,9 @@
  *          multiple of 8 (PR #298 page: "int3 fmt=5" in the #377 retarget
  *          list; the Vulkan fmt=4 commit message skips the per-row scale "like
  *          fmt=5"; the bit layout is this library's reading, the pages print
- *          none).
+ *          none).  The device copy holds each code c as the int4 nibble c + 4
+ *          (the same value c - 4) with the same scales, so every int4 kernel
+ *          serves int3; it is 4/3 of the int3 bytes.
  *   fmt=7  FP8 E4M3 (OCP: sign, 4 exponent bits with bias 7, 3 mantissa bits,
  *          exponent 0 subnormal, no infinities, S.1111.111 NaN), one byte per
  *          element, [O][I]; scales f32 [ceil(O/128)][ceil(I/128)], one per
@@ -142,7 +144,8 @@ int coli_tensor_upload_host(int fmt, int gs, int64_t O, int64_t I, const void *d
 void coli_tensor_free(coli_tensor *t);
 
 /* Shape and storage of a tensor.  Any output pointer may be NULL.
- * device_bytes = device memory held; alg_bytes = host-layout codes + scales. */
+ * fmt is the format as uploaded; device_bytes = device memory held; alg_bytes =
+ * host-layout codes + scales. */
 int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_t *I,
                      int64_t *device_bytes, int64_t *alg_bytes);
 
@@ -158,8 +161,7 @@ int coli_tensor_info(const coli_tensor *t, int *fmt, int *gs, int64_t *O, int64_
  *           runs the bandwidth-bound CUDA-core matvec kernels, S = 1 the
  *           slab kernel for fmt 0/1/2/4; larger S runs the tensor-core GEMM
  *           for fmt=2 and for fmt=4 with gs % 64 == 0, the tiled CUDA-core
- *           GEMM otherwise (fmt 0, 1, 3, 5, 7).  fmt=5 at S <= 8 runs its own
- *           CUDA-core matvec.
+ *           GEMM otherwise (fmt 0, 1, 3, 7); fmt=5 runs the int4 kernels.
  * Errors: COLI_EINVAL (NULL/misaligned pointer, S < 1), COLI_EDEVICE, COLI_ECUDA.
  */
 int coli_matmul(const coli_tensor *W, const float *x, float *y, int S, void *stream);
@@ -188,13 +190,12 @@ int coli_matmul_multi(int n, const coli_tensor *const *W, const float *x, float 
  *                       x: device f32 [S][n_heads][I]; y: [S][n_heads][n_rows]
  *   coli_matmul_rows_t  y[s][h][i] = sum_j x[s][h][j] * W[o0 + h*stride + j][i]
  *                       x: device f32 [S][n_heads][n_rows]; y: [S][n_heads][I]
- *   W       any format but fmt=5 (device or host resident; int3 is refused with
- *           COLI_EFMT); y overwritten, must not overlap x.
+ *   W       any format (device or host resident); y overwritten, must not overlap x.
  *   o0, stride, n_rows, n_heads  o0 >= 0, stride >= 0 (heads may share rows),
  *           1 <= n_rows <= 2^30, n_heads >= 1, o0 + (n_heads-1)*stride + n_rows <= O.
  *   S       rows of activations, >= 1 (each weight row is read once per 4 of them).
  * Errors: COLI_EINVAL (pointers, ranges, a head's activations too long for the
- * shared-memory stage), COLI_EFMT (fmt=5), COLI_EDEVICE, COLI_ECUDA.
+ * shared-memory stage), COLI_EDEVICE, COLI_ECUDA.
  */
 int coli_matmul_rows(const coli_tensor *W, int64_t o0, int64_t stride, int64_t n_rows, int n_heads,
                      const float *x, float *y, int S, void *stream);
@@ -278,8 +279,7 @@ int coli_moe_router(const float *x, int S, const coli_tensor *router, const floa
  * otherwise the slab kernel (S = 1) or the general decode kernel.  Larger S*K
  * runs the prefill pipeline (routing, gather, grouped gate/up, grouped down,
  * combine) on the tensor cores for int4 tables with gs % 64 == 0, on the CUDA
- * cores otherwise; int3 (fmt=5) tables take the CUDA-core pipeline at every
- * S*K.  Every call checks the whole table (shapes, formats,
+ * cores otherwise; int3 (fmt=5) tables take the int4 paths.  Every call checks the whole table (shapes, formats,
  * device) on the host: for a table used over and over, create it once with
  * coli_expert_table_create and call coli_moe_block_t.  An id out of range is
  * recorded for coli_sync_check(stream) and y is then unspecified.
@@ -329,8 +329,8 @@ int coli_moe_block_t(const float *x, int S, const coli_expert_table *table, cons
  *              routing id was outside [-1, n_experts) (y is then unspecified).
  *   Limits (refused with COLI_EINVAL, nothing launched): S*K <= 64,
  *   n_experts <= 1024, S*K*F <= 524288, and the activations must fit the
- *   single-launch decode kernel's shared memory; fmt=4 needs gs % 32 == 0
- *   and fmt=5 tables are refused (COLI_EFMT).
+ *   single-launch decode kernel's shared memory; fmt=4 and fmt=5 need
+ *   gs % 32 == 0 (COLI_EFMT).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress).  The expert descriptors go to the array through the
  * parameters of a small copy kernel, and only when they differ from the ones

@@ -15,11 +15,12 @@ def _small_table(coli, g, H=128, F=64, E=4, fmt=4, gs=64):
 
 
 @pytest.mark.parametrize("S", [1, 20])
-def test_bad_routing_id_is_reported(S):
+@pytest.mark.parametrize("fmt,gs", [(4, 64), (5, 64)])
+def test_bad_routing_id_is_reported(S, fmt, gs):
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
     g = wl.rng(1)
-    table = _small_table(coli, g)
+    table = _small_table(coli, g, fmt=fmt, gs=gs)
     ids = np.zeros((S, 2), np.int32)
     ids[-1, 1] = 9    # out of range for 4 experts
     x = torch.zeros(S, 128, device="cuda")

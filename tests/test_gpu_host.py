@@ -26,6 +26,7 @@ def test_host_matmul(fmt, gs, S):
     x = wl.activations(g, S, 1500)
     W = _host(coli, m)
     assert W.info()["device_bytes"] == 0
+    assert W.info()["fmt"] == fmt and W.info()["alg_bytes"] == m.nbytes
     y = torch.full((S, 300), float("nan"), device="cuda")
     coli.matmul(W, torch.from_numpy(x).cuda(), y)
     coli.sync_check()

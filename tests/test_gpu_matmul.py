@@ -411,7 +411,7 @@ def test_int3_multi_different_groups(S):
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
     g = wl.rng(800 + S)
-    I = 1000
+    I = 9000
     mats = [wl.random_matrix(g, 5, O, I, gs) for O, gs in ((300, 8), (17, 64), (129, 24), (64, 1024))]
     Ws = [upload(coli, m) for m in mats]
     x = wl.activations(g, S, I)
@@ -423,8 +423,7 @@ def test_int3_multi_different_groups(S):
 
 
 def test_int3_unaligned_activations():
-    """int3 matvec with x at a 4-byte (not 16-byte) offset: the scalar-load
-    path of the kernel, against the oracle."""
+    """int3 matvec with x at a 4-byte (not 16-byte) offset, against the oracle."""
     torch = cuda_or_skip()
     import bit_weight_gemv_fmt1_gb300 as coli
     g = wl.rng(810)
@@ -438,3 +437,21 @@ def test_int3_unaligned_activations():
     coli.matmul(W, xd, y)
     coli.sync_check()
     assert norm_err(y.cpu().numpy(), orc.matmul(5, 32, 200, 640, m.data, m.scales, x)) <= TOL
+
+
+def test_int3_storage_and_info():
+    """An int3 upload reports fmt=5 and its int3 bytes; the device copy holds
+    the codes as int4 nibble rows (ceil(I/2) bytes padded to 16) plus the
+    scales, and computes the oracle's int3 product on the int4 kernels."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(820)
+    O, I, gs = 300, 1000, 40
+    m = wl.random_matrix(g, 5, O, I, gs)
+    W = upload(coli, m)
+    info = W.info()
+    assert info["fmt"] == 5 and info["gs"] == gs
+    assert info["alg_bytes"] == m.nbytes
+    assert info["device_bytes"] == O * (((I + 1) // 2 + 15) // 16 * 16) + 4 * m.scales.size
+    x = wl.activations(g, 2, I)
+    assert norm_err(_run(coli, torch, m, x), orc.matmul(5, gs, O, I, m.data, m.scales, x)) <= TOL

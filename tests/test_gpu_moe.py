@@ -101,6 +101,44 @@ def test_decode_streamed_duplicates_and_empty_slots():
             assert norm_err(got, ref) <= TOL
 
 
+@pytest.mark.parametrize("K", [4, 9, 16])
+def test_int3_decode_duplicates_and_empty_slots(K):
+    """int3 decode block: duplicate ids, empty slots, a token with no expert,
+    K from 4 to 16."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E = 1000, 2100, 10
+    g = wl.rng(4250 + K)
+    host = _experts(g, H, F, E, 5, 40)
+    table = _device_table(coli, host)
+    mats = _oracle_mats(host)
+    x = wl.activations(g, 3, H)
+    ids = g.integers(0, E, (3, K)).astype(np.int32)
+    ids[0, 1] = ids[0, 0]
+    ids[0, K - 1] = -1
+    ids[1, :] = -1
+    w = g.uniform(0.05, 1.0, ids.shape).astype(np.float32)
+    got = _run_block(coli, torch, table, x, ids, w, H)
+    ref = orc.moe_block(H, F, mats, x, ids, w)
+    assert np.all(got[1] == 0.0)
+    assert norm_err(got, ref) <= TOL
+
+
+def test_int3_decode_full_size():
+    """int3 g64 decode block at the decode workload's shape (H 6144, F 2048,
+    top-8 of 32 experts) against the oracle."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E, K = 6144, 2048, 32, 8
+    g = wl.rng(4260)
+    host = _experts(g, H, F, E, 5, 64, distinct=8)
+    x = wl.activations(g, 1, H)
+    ids, w = wl.routing_topk_softmax(g, 1, E, K)
+    got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert norm_err(got, ref) <= TOL
+
+
 @pytest.mark.parametrize("scale", [1e12, 2.0 ** 30, 1e-12])
 def test_decode_streamed_activation_magnitudes(scale):
     """Activations far from unit size: the streamed kernel rescales each lane's
