@@ -3,6 +3,7 @@
 // Every entry point refuses what it cannot compute (with a code and a
 // message) before launching anything; there is no other implementation to
 // fall back to.
+#include <array>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -210,16 +211,26 @@ int64_t host_row_bytes(int fmt, int64_t I) {
 // Row of an int3 (fmt=5) upload, 3*ceil(I/8) bytes (element 8j+t is bits [3t, 3t+2] of the
 // little-endian 24-bit word in bytes 3j..3j+2), written as the int4 row of the device layout,
 // ceil(I/2) bytes: element i's code c becomes the nibble c + 4, element 2j the low nibble of
-// byte j.  The nibbles past I are zero.
+// byte j.  Each output byte holds two consecutive codes, i.e. one 6-bit field of the word,
+// looked up in a table; the nibbles past I are zero.
 void int3_row_to_int4(const uint8_t *src, int64_t I, uint8_t *dst) {
-    const int64_t nb = (I + 1) / 2;
-    memset(dst, 0, (size_t)nb);
-    for (int64_t u = 0; 8 * u < I; u++) {
+    static const auto lut = [] {
+        std::array<uint8_t, 64> t{};
+        for (int v = 0; v < 64; v++) t[v] = (uint8_t)(((v & 7) + 4) | (((v >> 3) + 4) << 4));
+        return t;
+    }();
+    const int64_t full = I / 8;   // units whose 8 codes all lie inside the row
+    for (int64_t u = 0; u < full; u++) {
         const uint32_t w = (uint32_t)src[3 * u] | ((uint32_t)src[3 * u + 1] << 8) | ((uint32_t)src[3 * u + 2] << 16);
-        for (int t = 0; t < 8 && 8 * u + t < I; t++) {
-            const int64_t i = 8 * u + t;
-            const uint8_t nib = (uint8_t)(((w >> (3 * t)) & 7u) + 4u);
-            dst[i / 2] |= (i & 1) ? (uint8_t)(nib << 4) : nib;
+        for (int k = 0; k < 4; k++) dst[4 * u + k] = lut[(w >> (6 * k)) & 63u];
+    }
+    if (I % 8) {   // the last, partial unit
+        const int64_t u = full;
+        const uint32_t w = (uint32_t)src[3 * u] | ((uint32_t)src[3 * u + 1] << 8) | ((uint32_t)src[3 * u + 2] << 16);
+        for (int64_t i = 8 * u; i < 8 * u + 8; i += 2) {
+            const uint8_t lo = i < I ? (uint8_t)(((w >> (3 * (i - 8 * u))) & 7u) + 4u) : 0;
+            const uint8_t hi = i + 1 < I ? (uint8_t)(((w >> (3 * (i + 1 - 8 * u))) & 7u) + 4u) : 0;
+            if (i < I) dst[i / 2] = (uint8_t)(lo | (hi << 4));
         }
     }
 }
