@@ -815,10 +815,13 @@ cudaError_t launch_decode_mma(const MdArgs &a, int grid, size_t smem, cudaStream
         cfg.attrs = attr;
         if (!no_pdl.load(std::memory_order_relaxed)) {
             cfg.numAttrs = 2;
+            if (cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess) return cudaSuccess;
+            (void)cudaGetLastError();   // a refused launch configuration: nothing was launched
+            cfg.numAttrs = 1;
             const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
-            if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
-            (void)cudaGetLastError();   // the refused configuration; nothing was launched
-            no_pdl.store(true, std::memory_order_relaxed);
+            // the pair was the problem only if the cooperative launch alone goes through
+            if (e == cudaSuccess) no_pdl.store(true, std::memory_order_relaxed);
+            return e;
         }
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, a);
