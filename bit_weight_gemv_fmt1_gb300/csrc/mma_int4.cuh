@@ -76,19 +76,14 @@ __device__ __forceinline__ float4 lds128f(uint32_t addr) {
 // segment), bf the segment's eight B registers.  d = c + the segment's four
 // products (md_segment_c) or d += them (md_segment).
 __device__ __forceinline__ void md_segment_c(float (&d)[4], uint2 cg, uint2 ch, const uint32_t (&bf)[8], float4 c) {
-    // two chains of two (operands P and Q), so that two mma are in flight
+    // one chain of four: the other warps' chains fill the tensor pipe meanwhile
     const uint32_t L = 0x000F000Fu, Hm = 0x00F000F0u;
-    float e[4];
     mma16816c(d, cg.x & L, ch.x & L, cg.x & Hm, ch.x & Hm, bf[0], bf[1], c);
     const uint32_t ug = cg.x >> 8, uh = ch.x >> 8;
-    mma16816c(e, ug & L, uh & L, ug & Hm, uh & Hm, bf[2], bf[3], make_float4(0.f, 0.f, 0.f, 0.f));
+    mma16816(d, ug & L, uh & L, ug & Hm, uh & Hm, bf[2], bf[3]);
     mma16816(d, cg.y & L, ch.y & L, cg.y & Hm, ch.y & Hm, bf[4], bf[5]);
     const uint32_t vg = cg.y >> 8, vh = ch.y >> 8;
-    mma16816(e, vg & L, vh & L, vg & Hm, vh & Hm, bf[6], bf[7]);
-    d[0] += e[0];
-    d[1] += e[1];
-    d[2] += e[2];
-    d[3] += e[3];
+    mma16816(d, vg & L, vh & L, vg & Hm, vh & Hm, bf[6], bf[7]);
 }
 __device__ __forceinline__ void md_segment(float (&d)[4], uint2 cg, uint2 ch, const uint32_t (&bf)[8]) {
     const uint32_t L = 0x000F000Fu, Hm = 0x00F000F0u;
