@@ -455,3 +455,21 @@ def test_int3_storage_and_info():
     assert info["device_bytes"] == O * (((I + 1) // 2 + 15) // 16 * 16) + 4 * m.scales.size
     x = wl.activations(g, 2, I)
     assert norm_err(_run(coli, torch, m, x), orc.matmul(5, gs, O, I, m.data, m.scales, x)) <= TOL
+
+
+def test_int3_and_int4_in_one_multi_call():
+    """int3 matrices are stored as grouped int4, so one coli_matmul_multi call
+    may take both; each result against the oracle in its own format."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    g = wl.rng(830)
+    I = 2048
+    mats = [wl.random_matrix(g, 5, 300, I, 64), wl.random_matrix(g, 4, 200, I, 128), wl.random_matrix(g, 5, 77, I, 32)]
+    Ws = [upload(coli, m) for m in mats]
+    for S in (1, 3, 12):
+        x = wl.activations(g, S, I)
+        ys = [torch.full((S, m.O), float("nan"), device="cuda") for m in mats]
+        coli.matmul_multi(Ws, torch.from_numpy(x).cuda(), ys)
+        coli.sync_check()
+        for m, y in zip(mats, ys):
+            assert norm_err(y.cpu().numpy(), orc.matmul(m.fmt, m.gs, m.O, I, m.data, m.scales, x)) <= TOL

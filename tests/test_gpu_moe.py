@@ -419,3 +419,19 @@ def test_matvec_and_decode_blocks_interleaved_on_one_stream():
     torch.cuda.synchronize()
     coli.sync_check(st)
     check()
+
+
+@pytest.mark.parametrize("S,K", [(1, 8), (20, 4)])
+def test_int3_and_int4_experts_in_one_table(S, K):
+    """An expert table whose experts are int3 or grouped int4 (one device
+    format): decode and prefill against the oracle."""
+    torch = cuda_or_skip()
+    import bit_weight_gemv_fmt1_gb300 as coli
+    H, F, E = 1024, 512, 8
+    g = wl.rng(4270 + S)
+    host = [wl.expert(g, H, F, 5 if e % 2 else 4, 64) for e in range(E)]
+    x = wl.activations(g, S, H)
+    ids, w = wl.routing_topk_softmax(g, S, E, K)
+    got = _run_block(coli, torch, _device_table(coli, host), x, ids, w, H)
+    ref = orc.moe_block(H, F, _oracle_mats(host), x, ids, w)
+    assert norm_err(got, ref) <= TOL
